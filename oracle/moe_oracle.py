@@ -1,0 +1,286 @@
+"""CPU oracle for the DeepSeekMoE layer forward -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s
+``cpu_baseline`` / ``--impl reference`` legs may import this module.  It
+shares no code, header, table or constant with the CUDA path and imports
+nothing from the product package; the two meet only through the seeded input
+generator, which holds none of the method's arithmetic.
+
+What it computes, and where the pages say so (page titles as cited):
+
+* "02 · DeepSeek-V3" (PaperTrace) §1.3, eq. 12/13/15: the MoE output is the
+  residual plus the shared expert plus the gate-weighted sum of the routed
+  experts; affinities are sigmoids of the router scores; gates are the
+  chosen affinities normalised over the chosen top-8 (so they sum to 1).
+* same page §1.3, node-limited routing: experts fall into groups; a group's
+  score is the sum of its K_r/M = 2 highest affinities; the best 4 groups are
+  kept and top-8 is taken only among their experts.
+* same page §1.4, eq. 16: a per-expert bias b_i is added to the affinity for
+  the top-K selection only; the gate still uses the raw affinity; at step end
+  overloaded experts get b_i -= gamma and underloaded ones b_i += gamma,
+  gamma = 0.001.
+* same page §1.1: every expert is a SwiGLU FFN with three matrices
+  (7168 x 2048 each for V3).
+
+The page's formulas were lost in extraction; each step below restates the
+prose.  Readings where the pages are silent (tie-breaks, the "at the mean"
+case, the fp32 sigmoid op sequence needed for bit-exact selection) are marked
+READING and listed in the design notes.
+
+Precision: the expert FFN, the router logits and the layer output are fp64
+arithmetic on the exact values of the bf16 / fp32 inputs.  Routing decisions
+(sigmoid, bias add, group sums, top-K, gate division) are taken in fp32, in
+the exact IEEE operation order written here, because floating point decides
+an index there and both sides must take that decision in the same precision.
+
+Parity status: every function here is pinned by a ``-m "not gpu"`` test
+(closed forms, brute force on tiny inputs, invariants the pages state, and
+textbook reductions) -- see tests/test_oracle_pins.py.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+F32 = np.float32
+
+# --------------------------------------------------------------------------
+# Spec S1 -- the fp32 sigmoid used for selection (READING R7).
+#
+# sigma(z) = 1 / (1 + e^{-z}).  The pages fix no rounding; bit-exact routing
+# needs one fixed sequence of correctly-rounded IEEE fp32 operations:
+#   w = min(max(-z, -32), 80)           (fmax/fmin: NaN z -> -32)
+#   n = rint(w * LOG2E)                 (round half to even)
+#   r = (w - n*LN2_HI) - n*LN2_LO       (Cody & Waite 1980 two-part ln 2)
+#   p = Horner of the degree-7 Taylor polynomial of e^r, each step one
+#       rounded multiply then one rounded add (no fused multiply-add)
+#   e = p * 2^n                         (exact: the clamp keeps it normal)
+#   s = 1 / (1 + e)                     (rounded add, rounded divide)
+# For w < -32, e^w < 2^-46 so 1 + e rounds to 1 and the clamp changes
+# nothing; w > 80 (z < -80) is clamped (s stays a normal number).
+# The constants are derived here from the mathematics (double precision
+# ln 2 and factorials), not taken from any library.
+# --------------------------------------------------------------------------
+_LN2 = math.log(2.0)
+LN2_HI = F32(round(_LN2 * 2 ** 16) / 2 ** 16)  # 16 significant bits
+LN2_LO = F32(_LN2 - float(LN2_HI))
+LOG2E = F32(1.0 / _LN2)
+TAYLOR = [F32(1.0 / math.factorial(k)) for k in range(8)]  # 1/k!, k = 0..7
+
+
+def sig32(z: np.ndarray) -> np.ndarray:
+    """fp32 sigmoid by spec S1 (elementwise, any shape)."""
+    z = np.asarray(z, dtype=F32)
+    w = np.fmin(np.fmax(-z, F32(-32.0)), F32(80.0))
+    n = np.rint(w * LOG2E)                      # fp32 multiply, then rint
+    r = (w - n * LN2_HI) - n * LN2_LO           # n*LN2_HI is exact
+    p = np.full_like(r, TAYLOR[7])
+    for k in range(6, -1, -1):
+        p = p * r + TAYLOR[k]                   # two rounded fp32 ops
+    two_n = ((n.astype(np.int32) + 127) << 23).view(F32)
+    e = p * two_n
+    return F32(1.0) / (F32(1.0) + e)
+
+
+# --------------------------------------------------------------------------
+# Router logits (eq. 15 context: the affinity is the sigmoid of a token's
+# score against each expert's router vector).
+# --------------------------------------------------------------------------
+def router_logits(x_f32: np.ndarray, w_router: np.ndarray) -> np.ndarray:
+    """z[t, e] = fl32( sum_h x[t,h] * W_r[e,h] ), summed in fp64, rounded once.
+
+    ``x_f32`` holds the exact values of the bf16 activations."""
+    z = np.asarray(x_f32, np.float64) @ np.asarray(w_router, np.float64).T
+    return z.astype(F32)
+
+
+# --------------------------------------------------------------------------
+# Routing: sigmoid + bias, group limit, top-K, gates (§1.3, §1.4).
+# --------------------------------------------------------------------------
+def route(logits: np.ndarray, bias: np.ndarray, n_group: int,
+          topk_group: int, topk: int, group_on_unbiased: bool = False):
+    """Selection and gates for every token.
+
+    Returns dict with
+      idx[T,K] int32  -- chosen experts, slot k = k-th by (u desc, e asc)
+      gate[T,K] fp32  -- s_{e_k} / sum_j s_{e_j} (raw affinity, never u)
+      s[T,E], u[T,E] fp32, group_score[T,G] fp32, kept[T,G] bool
+
+    Steps (all fp32, in this order):
+      s = sig32(z); u = s + b                     (eq. 15, eq. 16)
+      S_g = u_(1) + u_(2) over the group's two largest u (duplicates count
+            twice)                                (§1.3, K_r/M = 2)
+      kept = first topk_group groups by (S_g desc, g asc)   READING R3
+      idx  = first topk experts of kept groups by (u desc, e asc)
+      den  = s_{e_0} + ... + s_{e_{K-1}}, left to right in slot order
+      gate = s_{e_k} / den                        (eq. 13)
+    ``group_on_unbiased`` scores groups on s instead of u (ablation only;
+    the default follows the reading that group limiting is part of the
+    biased selection condition, READING R2).
+    """
+    z = np.asarray(logits, F32)
+    T, E = z.shape
+    assert E % n_group == 0 and E // n_group >= 2
+    assert 1 <= topk_group <= n_group and topk <= topk_group * (E // n_group)
+    s = sig32(z)
+    u = s + np.asarray(bias, F32)[None, :]
+
+    gs = E // n_group
+    grp_vals = (s if group_on_unbiased else u).reshape(T, n_group, gs)
+    two = -np.sort(-grp_vals, axis=2)[:, :, :2]      # two largest, multiset
+    group_score = two[:, :, 0] + two[:, :, 1]        # fp32 add
+
+    gorder = np.argsort(-group_score, axis=1, kind="stable")[:, :topk_group]
+    kept = np.zeros((T, n_group), bool)
+    np.put_along_axis(kept, gorder, True, axis=1)
+
+    expert_kept = np.repeat(kept, gs, axis=1)
+    cand = np.where(expert_kept, u, F32(-np.inf))
+    idx = np.argsort(-cand, axis=1, kind="stable")[:, :topk].astype(np.int32)
+
+    sk = np.take_along_axis(s, idx, axis=1)
+    den = np.zeros(T, F32)
+    for k in range(topk):                            # slot order, fp32
+        den = den + sk[:, k]
+    gate = sk / den[:, None]
+    return dict(idx=idx, gate=gate.astype(F32), s=s, u=u,
+                group_score=group_score, kept=kept)
+
+
+def routing_margins(r: dict, topk_group: int, topk: int):
+    """Per-token decision margins on the oracle's own fp32 u / S:
+    top-K margin  u_(K) - u_(K+1) among the kept experts, and
+    group margin  S_(M) - S_(M+1) (inf when every group is kept).
+    Tokens with small margins may legitimately route differently when the
+    logits differ by fp32 rounding (tolerance scope, READING R11)."""
+    u = r["u"].astype(np.float64)
+    T, E = u.shape
+    G = r["group_score"].shape[1]
+    kept_e = np.repeat(r["kept"], E // G, axis=1)
+    cand = np.sort(np.where(kept_e, u, -np.inf), axis=1)[:, ::-1]
+    km = cand[:, topk - 1] - cand[:, topk] if topk < cand.shape[1] else \
+        np.full(T, np.inf)
+    km = np.where(np.isfinite(km), km, np.inf)
+    S = np.sort(r["group_score"].astype(np.float64), axis=1)[:, ::-1]
+    gm = S[:, topk_group - 1] - S[:, topk_group] if topk_group < G else \
+        np.full(T, np.inf)
+    return km, gm
+
+
+# --------------------------------------------------------------------------
+# Load histogram and the stable permutation (dispatch order).
+# --------------------------------------------------------------------------
+def expert_counts(idx: np.ndarray, E: int) -> np.ndarray:
+    """c_e = #{(t, k) : idx[t, k] == e}  (the batch load, §1.4)."""
+    return np.bincount(np.asarray(idx).ravel(), minlength=E).astype(np.int32)
+
+
+def permutation(idx: np.ndarray, E: int):
+    """Stable counting sort of the (token, slot) pairs by expert.
+
+    offsets[0] = 0, offsets[e+1] = offsets[e] + c_e
+    dest[t, k] = offsets[e] + #{t' < t : e chosen by t'}   (READING R10)
+    src_row[dest[t, k]] = t*K + k
+    A token chooses an expert at most once, so ordering flat positions
+    p = t*K + k is ordering by token inside each expert."""
+    idx = np.asarray(idx)
+    T, K = idx.shape
+    c = expert_counts(idx, E)
+    offsets = np.zeros(E + 1, np.int32)
+    offsets[1:] = np.cumsum(c)
+    order = np.argsort(idx.ravel(), kind="stable")
+    dest = np.empty(T * K, np.int32)
+    dest[order] = np.arange(T * K, dtype=np.int32)
+    return dict(offsets=offsets, dest=dest.reshape(T, K),
+                src_row=order.astype(np.int32), counts=c)
+
+
+# --------------------------------------------------------------------------
+# Expert FFN and the layer output (§1.1, eq. 12).
+# --------------------------------------------------------------------------
+def silu(v: np.ndarray) -> np.ndarray:
+    """silu(v) = v / (1 + e^{-v}) in fp64."""
+    return v / (1.0 + np.exp(-v))
+
+
+def swiglu_ffn(a: np.ndarray, w1: np.ndarray, w3: np.ndarray,
+               w2: np.ndarray) -> np.ndarray:
+    """y = W2 (silu(W1 a) * (W3 a)) for each row a, all fp64, no rounding of
+    the intermediate.  w1, w3: [I, H]; w2: [H, I] (values, any float dtype)."""
+    a = np.asarray(a, np.float64)
+    p = a @ np.asarray(w1, np.float64).T
+    q = a @ np.asarray(w3, np.float64).T
+    return (silu(p) * q) @ np.asarray(w2, np.float64).T
+
+
+def moe_output(x: np.ndarray, ys: np.ndarray, y_slots: np.ndarray,
+               gate: np.ndarray) -> np.ndarray:
+    """out_t = x_t + ys_t + sum_{k=0..K-1} g_{t,k} * y_{e_k}(t)   (eq. 12),
+    fp64, summed in slot order.  y_slots[t, k, :] is FFN_{e_k}(x_t)."""
+    out = np.asarray(x, np.float64) + np.asarray(ys, np.float64)
+    for k in range(y_slots.shape[1]):
+        out = out + np.asarray(gate[:, k], np.float64)[:, None] * y_slots[:, k]
+    return out
+
+
+def layer_forward(x_f32, w_router, bias, w1, w3, w2, ws1, ws3, ws2, *,
+                  n_group, topk_group, topk):
+    """Full layer for every token (small sizes).  Weight arguments hold the
+    values (fp32 or fp64 arrays): w1, w3 [E,I,H], w2 [E,H,I]; ws* shared.
+
+    Returns dict: out[T,H] fp64, logits, the routing dict, ys, y_slots."""
+    x64 = np.asarray(x_f32, np.float64)
+    z = router_logits(x_f32, w_router)
+    r = route(z, bias, n_group, topk_group, topk)
+    T, K = r["idx"].shape
+    E = w1.shape[0]
+    ys = swiglu_ffn(x64, ws1, ws3, ws2)
+    y_slots = np.zeros((T, K, x64.shape[1]))
+    for e in range(E):
+        t, k = np.nonzero(r["idx"] == e)
+        if t.size:
+            y_slots[t, k] = swiglu_ffn(x64[t], w1[e], w3[e], w2[e])
+    out = moe_output(x64, ys, y_slots, r["gate"])
+    return dict(out=out, logits=z, route=r, ys=ys, y_slots=y_slots)
+
+
+def layer_rows(x_rows_f32, idx_rows, gate_rows, expert_w, shared_w):
+    """Layer output for a sample of tokens whose routing is already known
+    (used to check sampled outputs at full V3 size).
+
+    expert_w(e) -> (w1[I,H], w3[I,H], w2[H,I]) values; shared_w likewise."""
+    x64 = np.asarray(x_rows_f32, np.float64)
+    ys = swiglu_ffn(x64, *shared_w)
+    n, K = idx_rows.shape
+    y_slots = np.zeros((n, K, x64.shape[1]))
+    for e in np.unique(idx_rows):
+        t, k = np.nonzero(idx_rows == e)
+        y_slots[t, k] = swiglu_ffn(x64[t], *expert_w(int(e)))
+    return moe_output(x64, ys, y_slots, gate_rows)
+
+
+# --------------------------------------------------------------------------
+# Auxiliary-loss-free bias update (§1.4).
+# --------------------------------------------------------------------------
+def bias_update(counts: np.ndarray, bias: np.ndarray, T: int, K: int,
+                gamma: float, tie_overloaded: bool = False):
+    """One end-of-step update on the whole batch's load.
+
+    Expert e is overloaded when c_e > T*K/E and underloaded when c_e < T*K/E
+    (compared exactly as c_e*E vs T*K in integers); b_e -= gamma resp.
+    b_e += gamma in fp32 with gamma = fl32(gamma).  An expert exactly at the
+    mean is left unchanged (READING R4; ``tie_overloaded`` instead treats
+    it as overloaded).  Returns (new_bias, (max, mean, min) load)."""
+    c = np.asarray(counts, np.int64)
+    b = np.asarray(bias, F32)
+    E = c.shape[0]
+    g = F32(gamma)
+    lhs = c * E
+    rhs = np.int64(T) * np.int64(K)
+    over = lhs >= rhs if tie_overloaded else lhs > rhs
+    under = lhs < rhs
+    nb = np.where(over, b - g, np.where(under, b + g, b)).astype(F32)
+    stats = (float(c.max()) if E else 0.0, float(T * K) / E if E else 0.0,
+             float(c.min()) if E else 0.0)
+    return nb, stats
