@@ -1,0 +1,71 @@
+// Host-side launch interface between the C-ABI layer (moe_api.cu) and the
+// kernel files.  Every launcher validates nothing (the API layer did) and
+// returns the cudaGetLastError() of its launches.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+// tokens per routing block: the per-block expert histogram and the stable
+// dispatch order are both computed over these token ranges
+constexpr int kRouteTokensPerBlock = 64;
+
+inline int route_blocks(int T) {
+  return (T + kRouteTokensPerBlock - 1) / kRouteTokensPerBlock;
+}
+
+struct DevStatus;
+
+// ---- routing.cu
+cudaError_t launch_router_logits(const uint16_t* x, const float* w_router,
+                                 float* logits, int T, int H, int E,
+                                 cudaStream_t s);
+cudaError_t launch_route(const float* logits, const float* bias, int T, int E,
+                         int n_group, int topk_group, int topk,
+                         int32_t* topk_idx, float* topk_gate,
+                         int32_t* block_counts, cudaStream_t s);
+cudaError_t launch_block_counts(const int32_t* topk_idx, int T, int E,
+                                int topk, int32_t* block_counts,
+                                DevStatus* st, cudaStream_t s);
+// reduces block_counts -> counts, scans -> offsets and block_base; if
+// bias != nullptr also applies the bias step (update_bias) and stats.
+cudaError_t launch_scan(const int32_t* block_counts, int T, int E, int topk,
+                        int32_t* counts, int32_t* offsets, int32_t* block_base,
+                        float* bias, float gamma, float* load_stats,
+                        cudaStream_t s);
+cudaError_t launch_dest(const int32_t* topk_idx, const int32_t* block_base,
+                        int T, int E, int topk, int32_t* dest,
+                        int32_t* src_row, DevStatus* st, cudaStream_t s);
+cudaError_t launch_gather(const uint16_t* x, const int32_t* dest, int T, int H,
+                          int topk, uint16_t* xp, cudaStream_t s);
+cudaError_t launch_combine(const uint16_t* x, const uint16_t* ys,
+                           const uint16_t* yp, const int32_t* dest,
+                           const float* gate, int T, int H, int topk,
+                           uint16_t* out, cudaStream_t s);
+cudaError_t launch_bias_update(const int32_t* counts, float* bias,
+                               float* load_stats, int T, int E, int topk,
+                               float gamma, cudaStream_t s);
+
+// ---- grouped_gemm.cu
+struct FfnArgs {
+  int T, H, E, topk, I, I_shared;
+  const uint16_t *xp, *x;          // A of the up GEMM
+  const int32_t* offsets;          // [E+1]
+  const uint16_t *w1, *w3, *w2;    // routed weights
+  const uint16_t *ws1, *ws3, *ws2; // shared expert
+  uint16_t *h, *hs;                // intermediate [T*K, I], [T, I_shared]
+  uint16_t *yp, *ys;               // outputs
+  DevStatus* status;
+  uint64_t wait_limit_ns;
+};
+// 0 on success, else a moe_status_t (encoding or launch failure)
+int launch_expert_ffn(const FfnArgs& a, cudaStream_t s);
+
+int sm_count();
+
+}  // namespace moe

@@ -1,0 +1,443 @@
+// C ABI of libmoe: host-side validation, workspace layout and the launch
+// sequences of the DeepSeekMoE layer forward (include/moe.h documents
+// every entry point).  Nothing here allocates device memory or
+// synchronises, except moe_get_device_error().
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include "../../include/moe.h"
+#include "device_common.cuh"
+#include "internal.h"
+
+namespace {
+
+using moe::DevStatus;
+
+constexpr size_t kAlign = 256;
+constexpr size_t kStatusBytes = 256;
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;
+uint64_t g_wait_limit_ns = kDefaultWaitNs;
+
+inline size_t up(size_t b) { return (b + kAlign - 1) / kAlign * kAlign; }
+inline bool aligned16(const void* p) {
+  return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
+}
+inline cudaStream_t cs(moe_stream_t s) { return static_cast<cudaStream_t>(s); }
+
+bool is_pow2(int v) { return v > 0 && (v & (v - 1)) == 0; }
+
+// Shape checks shared by every entry point.
+moe_status_t check_dims(const moe_dims_t* d, bool need_ffn) {
+  if (d == nullptr) return MOE_ERR_INVALID_ARG;
+  if (d->T < 0 || d->H <= 0 || d->E <= 0 || d->n_group <= 0 ||
+      d->topk_group <= 0 || d->topk <= 0)
+    return MOE_ERR_INVALID_ARG;
+  if (d->E % d->n_group != 0) return MOE_ERR_INVALID_ARG;
+  const int gs = d->E / d->n_group;
+  if (gs < 2) return MOE_ERR_INVALID_ARG;  // the group score needs a top-2
+  if (d->topk_group > d->n_group) return MOE_ERR_INVALID_ARG;
+  if (d->topk > d->topk_group * gs) return MOE_ERR_INVALID_ARG;
+  if (!std::isfinite(d->gamma)) return MOE_ERR_INVALID_ARG;
+  if ((long long)d->T * (d->topk + 1) >= (1ll << 31)) return MOE_ERR_UNSUPPORTED;
+  // routing kernel shape rules
+  if (d->E > 1024 || (d->E > 32 && d->E % 32 != 0)) return MOE_ERR_UNSUPPORTED;
+  if (d->n_group > 32 || d->topk > 32) return MOE_ERR_UNSUPPORTED;
+  const int epl = d->E <= 32 ? 1 : d->E / 32;  // experts per lane
+  if (!is_pow2(epl) || gs % epl != 0 || !is_pow2(gs / epl))
+    return MOE_ERR_UNSUPPORTED;
+  if (d->H % 64 != 0) return MOE_ERR_UNSUPPORTED;
+  if (d->H / 8 > 128 * 16) return MOE_ERR_UNSUPPORTED;  // gather row limit
+  if (need_ffn) {
+    if (d->I <= 0 || d->I_shared <= 0) return MOE_ERR_INVALID_ARG;
+    if (d->I % 64 != 0 || d->I_shared % 64 != 0) return MOE_ERR_UNSUPPORTED;
+    if ((long long)d->E * d->I >= (1ll << 31) ||
+        (long long)d->E * d->H >= (1ll << 31))
+      return MOE_ERR_UNSUPPORTED;
+  }
+  return MOE_OK;
+}
+
+// ----------------------------------------------------------- workspace
+struct Layout {
+  size_t status = 0;  // always at 0
+  size_t block_counts = 0, block_base = 0;
+  size_t logits = 0, idx = 0, gate = 0, counts = 0, offsets = 0, dest = 0,
+         src_row = 0;
+  size_t xp = 0, h = 0, hs = 0, yp = 0, ys = 0;
+  size_t total = 0;
+};
+
+Layout layout(const moe_dims_t* d, moe_ws_kind_t which) {
+  Layout L;
+  size_t o = kStatusBytes;
+  const size_t T = d->T, E = d->E, K = d->topk, H = d->H;
+  const size_t nblk = moe::route_blocks(d->T);
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o += up(bytes);
+    return at;
+  };
+  if (which == MOE_WS_ROUTE || which == MOE_WS_PERMUTE ||
+      which == MOE_WS_FORWARD) {
+    L.block_counts = take(nblk * E * 4);
+    L.block_base = take(nblk * E * 4);
+  }
+  if (which == MOE_WS_FORWARD) {
+    L.logits = take(T * E * 4);
+    L.idx = take(T * K * 4);
+    L.gate = take(T * K * 4);
+    L.counts = take(E * 4);
+    L.offsets = take((E + 1) * 4);
+    L.dest = take(T * K * 4);
+    L.src_row = take(T * K * 4);
+    L.xp = take(T * K * H * 2);
+    L.yp = take(T * K * H * 2);
+    L.ys = take(T * H * 2);
+  }
+  if (which == MOE_WS_EXPERT_FFN || which == MOE_WS_FORWARD) {
+    L.h = take(T * K * (size_t)d->I * 2);
+    L.hs = take(T * (size_t)d->I_shared * 2);
+  }
+  L.total = o;
+  return L;
+}
+
+template <typename P>
+P* at(void* ws, size_t off) {
+  return reinterpret_cast<P*>(static_cast<char*>(ws) + off);
+}
+
+moe_status_t check_ws(const moe_dims_t* d, moe_ws_kind_t which, void* ws,
+                      size_t ws_bytes) {
+  if (ws == nullptr) return MOE_ERR_WORKSPACE;
+  if (!aligned16(ws)) return MOE_ERR_ALIGNMENT;
+  if (ws_bytes < layout(d, which).total) return MOE_ERR_WORKSPACE;
+  return MOE_OK;
+}
+
+inline moe_status_t cuda_ok(cudaError_t e) {
+  return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+#define MOE_TRY(expr)                      \
+  do {                                     \
+    const moe_status_t st_ = (expr);       \
+    if (st_ != MOE_OK) return st_;         \
+  } while (0)
+
+#define MOE_NEED(p) \
+  do {              \
+    if ((p) == nullptr) return MOE_ERR_INVALID_ARG; \
+  } while (0)
+
+// a [T, ...] tensor may be NULL when there are no tokens
+#define MOE_NEED_T(p) \
+  do {                \
+    if (d->T > 0 && (p) == nullptr) return MOE_ERR_INVALID_ARG; \
+  } while (0)
+
+#define MOE_ALIGN(p) \
+  do {               \
+    if ((p) != nullptr && !aligned16(p)) return MOE_ERR_ALIGNMENT; \
+  } while (0)
+
+moe_status_t check_weights(const moe_weights_t* w) {
+  MOE_NEED(w);
+  MOE_NEED(w->w_router);
+  MOE_NEED(w->w1);
+  MOE_NEED(w->w3);
+  MOE_NEED(w->w2);
+  MOE_NEED(w->ws1);
+  MOE_NEED(w->ws3);
+  MOE_NEED(w->ws2);
+  MOE_ALIGN(w->w_router);
+  MOE_ALIGN(w->w1);
+  MOE_ALIGN(w->w3);
+  MOE_ALIGN(w->w2);
+  MOE_ALIGN(w->ws1);
+  MOE_ALIGN(w->ws3);
+  MOE_ALIGN(w->ws2);
+  return MOE_OK;
+}
+
+moe_status_t ffn_launch(const moe_dims_t* d, const moe_weights_t* w,
+                        const uint16_t* xp, const uint16_t* x,
+                        const int32_t* offsets, uint16_t* h, uint16_t* hs,
+                        uint16_t* yp, uint16_t* ys, DevStatus* st,
+                        cudaStream_t s) {
+  moe::FfnArgs a;
+  a.T = d->T;
+  a.H = d->H;
+  a.E = d->E;
+  a.topk = d->topk;
+  a.I = d->I;
+  a.I_shared = d->I_shared;
+  a.xp = xp;
+  a.x = x;
+  a.offsets = offsets;
+  a.w1 = w->w1;
+  a.w3 = w->w3;
+  a.w2 = w->w2;
+  a.ws1 = w->ws1;
+  a.ws3 = w->ws3;
+  a.ws2 = w->ws2;
+  a.h = h;
+  a.hs = hs;
+  a.yp = yp;
+  a.ys = ys;
+  a.status = st;
+  a.wait_limit_ns = g_wait_limit_ns;
+  return static_cast<moe_status_t>(moe::launch_expert_ffn(a, s));
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t moe_abi_version(void) { return MOE_ABI_VERSION; }
+
+const char* moe_status_string(moe_status_t s) {
+  switch (s) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED";
+    case MOE_ERR_ALIGNMENT: return "MOE_ERR_ALIGNMENT";
+    case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+    case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT";
+    case MOE_ERR_DEVICE_BOUNDS: return "MOE_ERR_DEVICE_BOUNDS";
+  }
+  return "MOE_ERR_UNKNOWN";
+}
+
+void moe_set_wait_timeout_ns(uint64_t ns) {
+  g_wait_limit_ns = ns == 0 ? kDefaultWaitNs : ns;
+}
+
+size_t moe_workspace_bytes(const moe_dims_t* d, moe_ws_kind_t which) {
+  const bool ffn = which == MOE_WS_EXPERT_FFN || which == MOE_WS_FORWARD;
+  if (check_dims(d, ffn) != MOE_OK) return 0;
+  if (which < MOE_WS_ROUTE || which > MOE_WS_FORWARD) return 0;
+  return layout(d, which).total;
+}
+
+moe_status_t moe_get_device_error(void* ws, moe_stream_t stream) {
+  if (ws == nullptr) return MOE_ERR_INVALID_ARG;
+  DevStatus h{0, 0};
+  if (cudaStreamSynchronize(cs(stream)) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemcpy(&h, ws, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (h.code != 0) {
+    const DevStatus zero{0, 0};
+    if (cudaMemcpy(ws, &zero, sizeof(zero), cudaMemcpyHostToDevice) !=
+        cudaSuccess)
+      return MOE_ERR_CUDA;
+  }
+  return static_cast<moe_status_t>(h.code);
+}
+
+moe_status_t moe_router_logits(const moe_dims_t* d, const uint16_t* x,
+                               const float* w_router, float* logits,
+                               moe_stream_t stream) {
+  MOE_TRY(check_dims(d, false));
+  MOE_NEED_T(x);
+  MOE_NEED(w_router);
+  MOE_NEED_T(logits);
+  MOE_ALIGN(x);
+  MOE_ALIGN(w_router);
+  MOE_ALIGN(logits);
+  if (d->T == 0) return MOE_OK;
+  return cuda_ok(moe::launch_router_logits(x, w_router, logits, d->T, d->H,
+                                           d->E, cs(stream)));
+}
+
+moe_status_t moe_route(const moe_dims_t* d, const float* logits,
+                       const float* bias, int32_t* topk_idx, float* topk_gate,
+                       int32_t* counts, void* ws, size_t ws_bytes,
+                       moe_stream_t stream) {
+  MOE_TRY(check_dims(d, false));
+  MOE_NEED_T(logits);
+  MOE_NEED(bias);
+  MOE_NEED_T(topk_idx);
+  MOE_NEED_T(topk_gate);
+  MOE_NEED(counts);
+  MOE_ALIGN(logits);
+  MOE_ALIGN(bias);
+  MOE_ALIGN(topk_idx);
+  MOE_ALIGN(topk_gate);
+  MOE_ALIGN(counts);
+  MOE_TRY(check_ws(d, MOE_WS_ROUTE, ws, ws_bytes));
+  const Layout L = layout(d, MOE_WS_ROUTE);
+  cudaStream_t s = cs(stream);
+  if (d->T == 0) {
+    return cuda_ok(cudaMemsetAsync(counts, 0, sizeof(int32_t) * d->E, s));
+  }
+  int32_t* bc = at<int32_t>(ws, L.block_counts);
+  MOE_TRY(cuda_ok(moe::launch_route(logits, bias, d->T, d->E, d->n_group,
+                                    d->topk_group, d->topk, topk_idx,
+                                    topk_gate, bc, s)));
+  return cuda_ok(moe::launch_scan(bc, d->T, d->E, d->topk, counts, nullptr,
+                                  nullptr, nullptr, 0.f, nullptr, s));
+}
+
+moe_status_t moe_permute(const moe_dims_t* d, const uint16_t* x,
+                         const int32_t* topk_idx, int32_t* offsets,
+                         int32_t* dest, int32_t* src_row, uint16_t* xp,
+                         void* ws, size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRY(check_dims(d, false));
+  MOE_NEED_T(topk_idx);
+  MOE_NEED(offsets);
+  MOE_NEED_T(dest);
+  MOE_NEED_T(src_row);
+  if (xp != nullptr) MOE_NEED_T(x);
+  MOE_ALIGN(x);
+  MOE_ALIGN(topk_idx);
+  MOE_ALIGN(offsets);
+  MOE_ALIGN(dest);
+  MOE_ALIGN(src_row);
+  MOE_ALIGN(xp);
+  MOE_TRY(check_ws(d, MOE_WS_PERMUTE, ws, ws_bytes));
+  const Layout L = layout(d, MOE_WS_PERMUTE);
+  cudaStream_t s = cs(stream);
+  if (d->T == 0)
+    return cuda_ok(cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (d->E + 1), s));
+  DevStatus* st = at<DevStatus>(ws, 0);
+  int32_t* bc = at<int32_t>(ws, L.block_counts);
+  int32_t* bb = at<int32_t>(ws, L.block_base);
+  MOE_TRY(cuda_ok(moe::launch_block_counts(topk_idx, d->T, d->E, d->topk, bc,
+                                           st, s)));
+  MOE_TRY(cuda_ok(moe::launch_scan(bc, d->T, d->E, d->topk, nullptr, offsets,
+                                   bb, nullptr, 0.f, nullptr, s)));
+  MOE_TRY(cuda_ok(moe::launch_dest(topk_idx, bb, d->T, d->E, d->topk, dest,
+                                   src_row, st, s)));
+  if (xp != nullptr)
+    MOE_TRY(cuda_ok(moe::launch_gather(x, dest, d->T, d->H, d->topk, xp, s)));
+  return MOE_OK;
+}
+
+moe_status_t moe_expert_ffn(const moe_dims_t* d, const moe_weights_t* w,
+                            const uint16_t* xp, const uint16_t* x,
+                            const int32_t* offsets, uint16_t* yp,
+                            uint16_t* ys, void* ws, size_t ws_bytes,
+                            moe_stream_t stream) {
+  MOE_TRY(check_dims(d, true));
+  MOE_TRY(check_weights(w));
+  MOE_NEED_T(xp);
+  MOE_NEED_T(x);
+  MOE_NEED(offsets);
+  MOE_NEED_T(yp);
+  MOE_NEED_T(ys);
+  MOE_ALIGN(xp);
+  MOE_ALIGN(x);
+  MOE_ALIGN(offsets);
+  MOE_ALIGN(yp);
+  MOE_ALIGN(ys);
+  MOE_TRY(check_ws(d, MOE_WS_EXPERT_FFN, ws, ws_bytes));
+  if (d->T == 0) return MOE_OK;
+  const Layout L = layout(d, MOE_WS_EXPERT_FFN);
+  return ffn_launch(d, w, xp, x, offsets, at<uint16_t>(ws, L.h),
+                    at<uint16_t>(ws, L.hs), yp, ys, at<DevStatus>(ws, 0),
+                    cs(stream));
+}
+
+moe_status_t moe_combine(const moe_dims_t* d, const uint16_t* x,
+                         const uint16_t* ys, const uint16_t* yp,
+                         const int32_t* dest, const float* topk_gate,
+                         uint16_t* out, moe_stream_t stream) {
+  MOE_TRY(check_dims(d, false));
+  MOE_NEED_T(x);
+  MOE_NEED_T(ys);
+  MOE_NEED_T(yp);
+  MOE_NEED_T(dest);
+  MOE_NEED_T(topk_gate);
+  MOE_NEED_T(out);
+  MOE_ALIGN(x);
+  MOE_ALIGN(ys);
+  MOE_ALIGN(yp);
+  MOE_ALIGN(dest);
+  MOE_ALIGN(topk_gate);
+  MOE_ALIGN(out);
+  if (d->T == 0) return MOE_OK;
+  return cuda_ok(moe::launch_combine(x, ys, yp, dest, topk_gate, d->T, d->H,
+                                     d->topk, out, cs(stream)));
+}
+
+moe_status_t moe_bias_update(const moe_dims_t* d, const int32_t* counts,
+                             float* bias, float* load_stats,
+                             moe_stream_t stream) {
+  MOE_TRY(check_dims(d, false));
+  MOE_NEED(counts);
+  MOE_NEED(bias);
+  MOE_ALIGN(counts);
+  MOE_ALIGN(bias);
+  MOE_ALIGN(load_stats);
+  return cuda_ok(moe::launch_bias_update(counts, bias, load_stats, d->T, d->E,
+                                         d->topk, d->gamma, cs(stream)));
+}
+
+moe_status_t moe_forward(const moe_dims_t* d, const moe_weights_t* w,
+                         const uint16_t* x, float* bias, int update_bias,
+                         uint16_t* out, float* logits_out,
+                         int32_t* topk_idx_out, float* topk_gate_out,
+                         int32_t* counts_out, float* load_stats_out, void* ws,
+                         size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRY(check_dims(d, true));
+  MOE_TRY(check_weights(w));
+  MOE_NEED_T(x);
+  MOE_NEED(bias);
+  MOE_NEED_T(out);
+  MOE_ALIGN(x);
+  MOE_ALIGN(bias);
+  MOE_ALIGN(out);
+  MOE_ALIGN(logits_out);
+  MOE_ALIGN(topk_idx_out);
+  MOE_ALIGN(topk_gate_out);
+  MOE_ALIGN(counts_out);
+  MOE_ALIGN(load_stats_out);
+  MOE_TRY(check_ws(d, MOE_WS_FORWARD, ws, ws_bytes));
+  cudaStream_t s = cs(stream);
+  const Layout L = layout(d, MOE_WS_FORWARD);
+  const int T = d->T, E = d->E, K = d->topk, H = d->H;
+  if (T == 0) {
+    if (counts_out)
+      MOE_TRY(cuda_ok(cudaMemsetAsync(counts_out, 0, sizeof(int32_t) * E, s)));
+    if (update_bias || load_stats_out) {
+      int32_t* cz = at<int32_t>(ws, L.counts);
+      MOE_TRY(cuda_ok(cudaMemsetAsync(cz, 0, sizeof(int32_t) * E, s)));
+      MOE_TRY(cuda_ok(moe::launch_bias_update(
+          cz, update_bias ? bias : nullptr, load_stats_out, T, E, K, d->gamma,
+          s)));
+    }
+    return MOE_OK;
+  }
+  DevStatus* st = at<DevStatus>(ws, 0);
+  float* logits = logits_out ? logits_out : at<float>(ws, L.logits);
+  int32_t* idx = topk_idx_out ? topk_idx_out : at<int32_t>(ws, L.idx);
+  float* gate = topk_gate_out ? topk_gate_out : at<float>(ws, L.gate);
+  int32_t* counts = counts_out ? counts_out : at<int32_t>(ws, L.counts);
+  int32_t* offsets = at<int32_t>(ws, L.offsets);
+  int32_t* dest = at<int32_t>(ws, L.dest);
+  int32_t* src_row = at<int32_t>(ws, L.src_row);
+  int32_t* bc = at<int32_t>(ws, L.block_counts);
+  int32_t* bb = at<int32_t>(ws, L.block_base);
+  uint16_t* xp = at<uint16_t>(ws, L.xp);
+  uint16_t* yp = at<uint16_t>(ws, L.yp);
+  uint16_t* ys = at<uint16_t>(ws, L.ys);
+
+  MOE_TRY(cuda_ok(moe::launch_router_logits(x, w->w_router, logits, T, H, E, s)));
+  MOE_TRY(cuda_ok(moe::launch_route(logits, bias, T, E, d->n_group,
+                                    d->topk_group, K, idx, gate, bc, s)));
+  // counts, offsets, block bases -- and the bias step on this batch's load,
+  // after routing consumed the old bias (same stream, so ordered)
+  MOE_TRY(cuda_ok(moe::launch_scan(bc, T, E, K, counts, offsets, bb,
+                                   update_bias ? bias : nullptr, d->gamma,
+                                   load_stats_out, s)));
+  MOE_TRY(cuda_ok(moe::launch_dest(idx, bb, T, E, K, dest, src_row, st, s)));
+  MOE_TRY(cuda_ok(moe::launch_gather(x, dest, T, H, K, xp, s)));
+  MOE_TRY(ffn_launch(d, w, xp, x, offsets, at<uint16_t>(ws, L.h),
+                     at<uint16_t>(ws, L.hs), yp, ys, st, s));
+  return cuda_ok(moe::launch_combine(x, ys, yp, dest, gate, T, H, K, out, s));
+}
+
+}  // extern "C"

@@ -1,0 +1,621 @@
+// Routing, dispatch order, gather, combine and the bias step of the
+// DeepSeekMoE layer ("02 · DeepSeek-V3" (PaperTrace) §1.3, §1.4; dispatch
+// and combine as in §2 / §5.1).  These are HBM- or latency-bound SIMT
+// kernels; the expert GEMMs live in grouped_gemm.cu.
+#include <cfloat>
+#include <climits>
+#include <cstdint>
+
+#include "device_common.cuh"
+#include "internal.h"
+
+namespace moe {
+
+// ===================================================================
+// Router logits: z[t, e] = sum_h x[t, h] * W_r[e, h], fp32 FMA chain in h
+// order per output.  64x64 output tile per 256-thread block, 4x4 outputs
+// per thread, K staged through shared memory 32 at a time.
+// ===================================================================
+namespace {
+constexpr int RL_BM = 64, RL_BN = 64, RL_BK = 32;
+
+__global__ void __launch_bounds__(256)
+    router_logits_kernel(const uint16_t* __restrict__ x,
+                         const float* __restrict__ w, float* __restrict__ z,
+                         int T, int H, int E) {
+  __shared__ float xs[RL_BK][RL_BM + 4];
+  __shared__ float ws[RL_BK][RL_BN + 4];
+  const int tid = threadIdx.x;
+  const int t0 = blockIdx.x * RL_BM, e0 = blockIdx.y * RL_BN;
+  const int ty = tid / 16, tx = tid % 16;
+  float acc[4][4] = {};
+  for (int k0 = 0; k0 < H; k0 += RL_BK) {
+    {  // x tile: 64 rows x 32 bf16 = 256 x 16 B
+      const int r = tid / 4, c = (tid % 4) * 8;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (t0 + r < T)
+        v = *reinterpret_cast<const uint4*>(x + (size_t)(t0 + r) * H + k0 + c);
+      const uint32_t q[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        xs[c + 2 * i][r] = bf16_lo(q[i]);
+        xs[c + 2 * i + 1][r] = bf16_hi(q[i]);
+      }
+    }
+#pragma unroll
+    for (int p = 0; p < 2; ++p) {  // w tile: 64 rows x 32 fp32 = 512 x 16 B
+      const int li = tid + p * 256;
+      const int r = li / 8, c = (li % 8) * 4;
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (e0 + r < E)
+        v = *reinterpret_cast<const float4*>(w + (size_t)(e0 + r) * H + k0 + c);
+      ws[c][r] = v.x;
+      ws[c + 1][r] = v.y;
+      ws[c + 2][r] = v.z;
+      ws[c + 3][r] = v.w;
+    }
+    __syncthreads();
+#pragma unroll 8
+    for (int k = 0; k < RL_BK; ++k) {
+      float a[4], b[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) a[i] = xs[k][ty * 4 + i];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) b[j] = ws[k][tx * 4 + j];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int t = t0 + ty * 4 + i;
+    if (t >= T) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int e = e0 + tx * 4 + j;
+      if (e < E) z[(size_t)t * E + e] = acc[i][j];
+    }
+  }
+}
+}  // namespace
+
+cudaError_t launch_router_logits(const uint16_t* x, const float* w_router,
+                                 float* logits, int T, int H, int E,
+                                 cudaStream_t s) {
+  dim3 grid((T + RL_BM - 1) / RL_BM, (E + RL_BN - 1) / RL_BN);
+  router_logits_kernel<<<grid, 256, 0, s>>>(x, w_router, logits, T, H, E);
+  return cudaGetLastError();
+}
+
+// ===================================================================
+// fp32 sigmoid, one fixed sequence of correctly rounded IEEE operations so
+// that selection is reproducible bit for bit on any conforming machine:
+//   w = min(max(-z, -32), 80); n = rint(w * log2 e)
+//   r = (w - n*LN2_HI) - n*LN2_LO     (Cody & Waite split of ln 2)
+//   p = Horner of sum_{k<=7} r^k / k!, one rounded multiply and one
+//       rounded add per step (explicit _rn intrinsics: never contracted)
+//   s = 1 / (1 + p * 2^n)
+// Constants, derived from the mathematics: LN2_HI = ln 2 rounded to 16
+// significant bits (so n*LN2_HI is exact for |n| < 2^8), LN2_LO = the fp32
+// rounding of ln 2 - LN2_HI, log2 e and 1/k! rounded to fp32.  For w < -32
+// the term 2^-46 vanishes against 1, so the lower clamp changes no result;
+// the upper one keeps p * 2^n a normal number.
+// ===================================================================
+__device__ __forceinline__ float sigmoid_f32(float z) {
+  constexpr float kLog2e = 0x1.715476p+0f;
+  constexpr float kLn2Hi = 0x1.62e4p-1f;
+  constexpr float kLn2Lo = 0x1.7f7d1cp-20f;
+  constexpr float kC7 = 0x1.a01a02p-13f;  // 1/5040
+  constexpr float kC6 = 0x1.6c16c2p-10f;  // 1/720
+  constexpr float kC5 = 0x1.111112p-7f;   // 1/120
+  constexpr float kC4 = 0x1.555556p-5f;   // 1/24
+  constexpr float kC3 = 0x1.555556p-3f;   // 1/6
+  const float w = fminf(fmaxf(-z, -32.0f), 80.0f);
+  const float n = rintf(__fmul_rn(w, kLog2e));
+  const float r = __fsub_rn(__fsub_rn(w, __fmul_rn(n, kLn2Hi)),
+                            __fmul_rn(n, kLn2Lo));
+  float p = kC7;
+  p = __fadd_rn(__fmul_rn(p, r), kC6);
+  p = __fadd_rn(__fmul_rn(p, r), kC5);
+  p = __fadd_rn(__fmul_rn(p, r), kC4);
+  p = __fadd_rn(__fmul_rn(p, r), kC3);
+  p = __fadd_rn(__fmul_rn(p, r), 0.5f);
+  p = __fadd_rn(__fmul_rn(p, r), 1.0f);
+  p = __fadd_rn(__fmul_rn(p, r), 1.0f);
+  const float two_n = __int_as_float((static_cast<int>(n) + 127) << 23);
+  const float e = __fmul_rn(p, two_n);
+  return __fdiv_rn(1.0f, __fadd_rn(1.0f, e));
+}
+
+// order-preserving map fp32 -> uint32 (larger float -> larger key)
+__device__ __forceinline__ uint32_t f32_order_key(float v) {
+  const uint32_t b = __float_as_uint(v);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+// ===================================================================
+// Routing: one warp per token.  Lane l holds experts [l*EPL, (l+1)*EPL);
+// expert groups are whole lane ranges of LPG lanes (LPG a power of 2), so
+// the group top-2 is a lane-local top-2 plus an xor butterfly.
+//   u = s + b                      selection score (eq. 16)
+//   S_g = top1 + top2 of u in g    group score (§1.3)
+//   kept = rank of (S_g desc, g asc) < topk_group
+//   slots: topk rounds of warp arg-max over kept u (ties: lower expert)
+//   gate_k = s_k / (s_0 + ... + s_{K-1}) summed in slot order (eq. 13)
+// The block's per-expert histogram is accumulated in shared memory with
+// integer atomics and written as one row of block_counts.
+// ===================================================================
+namespace {
+constexpr int kRouteWarps = 8;
+
+template <int EPL>
+__device__ __forceinline__ void load_row(const float* __restrict__ p,
+                                         float (&v)[EPL]) {
+  if constexpr (EPL % 4 == 0) {
+#pragma unroll
+    for (int j = 0; j < EPL; j += 4) {
+      const float4 q = __ldg(reinterpret_cast<const float4*>(p + j));
+      v[j] = q.x;
+      v[j + 1] = q.y;
+      v[j + 2] = q.z;
+      v[j + 3] = q.w;
+    }
+  } else if constexpr (EPL == 2) {
+    const float2 q = __ldg(reinterpret_cast<const float2*>(p));
+    v[0] = q.x;
+    v[1] = q.y;
+  } else {
+    v[0] = __ldg(p);
+  }
+}
+
+template <int EPL>
+__global__ void __launch_bounds__(kRouteWarps * 32)
+    route_kernel(const float* __restrict__ logits,
+                 const float* __restrict__ bias, int T, int E, int G, int M,
+                 int K, int LPG, int32_t* __restrict__ topk_idx,
+                 float* __restrict__ topk_gate,
+                 int32_t* __restrict__ block_counts) {
+  __shared__ int cnt[1024];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  for (int i = tid; i < E; i += blockDim.x) cnt[i] = 0;
+  __syncthreads();
+
+  const int lanes_used = E / EPL;
+  const bool active = lane < lanes_used;
+  const int my_g = lane / LPG;
+  float b[EPL];
+#pragma unroll
+  for (int j = 0; j < EPL; ++j) b[j] = active ? bias[lane * EPL + j] : 0.f;
+
+  const int tok0 = blockIdx.x * kRouteTokensPerBlock;
+  for (int tt = warp; tt < kRouteTokensPerBlock; tt += kRouteWarps) {
+    const int t = tok0 + tt;
+    if (t >= T) break;
+    float s[EPL], u[EPL];
+    if (active) {
+      load_row<EPL>(logits + (size_t)t * E + lane * EPL, s);
+#pragma unroll
+      for (int j = 0; j < EPL; ++j) {
+        s[j] = sigmoid_f32(s[j]);
+        u[j] = __fadd_rn(s[j], b[j]);
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < EPL; ++j) {
+        s[j] = 0.f;
+        u[j] = -INFINITY;
+      }
+    }
+    // ---- group score: two largest u of the group (a multiset)
+    float a1 = -INFINITY, a2 = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < EPL; ++j) {
+      if (u[j] > a1) {
+        a2 = a1;
+        a1 = u[j];
+      } else if (u[j] > a2) {
+        a2 = u[j];
+      }
+    }
+    for (int off = 1; off < LPG; off <<= 1) {
+      const float o1 = __shfl_xor_sync(0xffffffffu, a1, off);
+      const float o2 = __shfl_xor_sync(0xffffffffu, a2, off);
+      const float n2 = fmaxf(fminf(a1, o1), fmaxf(a2, o2));
+      a1 = fmaxf(a1, o1);
+      a2 = n2;
+    }
+    const float S = __fadd_rn(a1, a2);
+    // ---- kept groups: rank by (S desc, g asc)
+    int rank = 0;
+    for (int g = 0; g < G; ++g) {
+      const float Sg = __shfl_sync(0xffffffffu, S, g * LPG);
+      rank += (Sg > S) || (Sg == S && g < my_g);
+    }
+    const bool kept = active && my_g < G && rank < M;
+    float cu[EPL];
+#pragma unroll
+    for (int j = 0; j < EPL; ++j) cu[j] = kept ? u[j] : -INFINITY;
+    // ---- top-K by (u desc, e asc)
+    float den = 0.f, my_s = 0.f;
+    int my_e = 0;
+    for (int k = 0; k < K; ++k) {
+      float bv = -INFINITY;
+      int bj = 0;
+#pragma unroll
+      for (int j = 0; j < EPL; ++j) {
+        if (cu[j] > bv) {
+          bv = cu[j];
+          bj = j;
+        }
+      }
+      const uint32_t key = f32_order_key(bv);
+      const uint32_t kmax = __reduce_max_sync(0xffffffffu, key);
+      const int cand = (key == kmax && bv != -INFINITY) ? lane * EPL + bj
+                                                        : INT_MAX;
+      int e = __reduce_min_sync(0xffffffffu, cand);
+      if (e == INT_MAX) e = 0;  // only with non-finite scores: stay in bounds
+      const int owner = e / EPL, oj = e - owner * EPL;
+      float se = 0.f;
+      if (lane == owner) {
+#pragma unroll
+        for (int j = 0; j < EPL; ++j) {
+          if (j == oj) {
+            se = s[j];
+            cu[j] = -INFINITY;
+          }
+        }
+      }
+      se = __shfl_sync(0xffffffffu, se, owner);
+      den = __fadd_rn(den, se);
+      if (lane == k) {
+        my_e = e;
+        my_s = se;
+      }
+    }
+    if (lane < K) {
+      topk_idx[(size_t)t * K + lane] = my_e;
+      topk_gate[(size_t)t * K + lane] = __fdiv_rn(my_s, den);
+      atomicAdd(&cnt[my_e], 1);
+    }
+  }
+  __syncthreads();
+  for (int i = tid; i < E; i += blockDim.x)
+    block_counts[(size_t)blockIdx.x * E + i] = cnt[i];
+}
+
+// histogram of an existing topk_idx over the same token blocks
+__global__ void __launch_bounds__(256)
+    block_counts_kernel(const int32_t* __restrict__ topk_idx, int T, int E,
+                        int K, int32_t* __restrict__ block_counts,
+                        DevStatus* st) {
+  __shared__ int cnt[1024];
+  for (int i = threadIdx.x; i < E; i += blockDim.x) cnt[i] = 0;
+  __syncthreads();
+  const int t0 = blockIdx.x * kRouteTokensPerBlock;
+  const int t1 = min(T, t0 + kRouteTokensPerBlock);
+  for (int p = t0 * K + threadIdx.x; p < t1 * K; p += blockDim.x) {
+    const int e = topk_idx[p];
+    if (e >= 0 && e < E)
+      atomicAdd(&cnt[e], 1);
+    else
+      record_error(st, MOE_ERR_DEVICE_BOUNDS, 10);
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < E; i += blockDim.x)
+    block_counts[(size_t)blockIdx.x * E + i] = cnt[i];
+}
+
+// ===================================================================
+// One CTA: counts[e] = sum over blocks; offsets = exclusive scan of counts;
+// block_base[blk][e] = offsets[e] + counts of e in blocks before blk.
+// Optionally applies the bias step on the final counts (so a fused forward
+// needs no extra launch).
+// ===================================================================
+__global__ void __launch_bounds__(1024)
+    scan_kernel(const int32_t* __restrict__ block_counts, int nblk, int T,
+                int E, int K, int32_t* __restrict__ counts,
+                int32_t* __restrict__ offsets,
+                int32_t* __restrict__ block_base, float* __restrict__ bias,
+                float gamma, float* __restrict__ load_stats) {
+  __shared__ int warp_sums[32];
+  __shared__ int red_max[32], red_min[32];
+  const int e = threadIdx.x, lane = e & 31, warp = e >> 5;
+  int c = 0;
+  if (e < E)
+    for (int b = 0; b < nblk; ++b) c += block_counts[(size_t)b * E + e];
+  // block-wide exclusive scan of c
+  int incl = c;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += v;
+  }
+  if (lane == 31) warp_sums[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int nwarps = (blockDim.x + 31) / 32;
+    int ws = lane < nwarps ? warp_sums[lane] : 0;
+    int wi = ws;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, wi, off);
+      if (lane >= off) wi += v;
+    }
+    warp_sums[lane] = wi - ws;  // exclusive prefix of warp sums
+  }
+  __syncthreads();
+  const int excl = incl - c + warp_sums[warp];
+  if (e < E) {
+    if (counts) counts[e] = c;
+    if (offsets) {
+      offsets[e] = excl;
+      if (e == E - 1) offsets[E] = excl + c;
+    }
+    if (block_base) {
+      int run = excl;
+      for (int b = 0; b < nblk; ++b) {
+        block_base[(size_t)b * E + e] = run;
+        run += block_counts[(size_t)b * E + e];
+      }
+    }
+    if (bias) {
+      const long long lhs = (long long)c * E, rhs = (long long)T * K;
+      const float bv = bias[e];
+      bias[e] = lhs > rhs ? __fsub_rn(bv, gamma)
+                          : (lhs < rhs ? __fadd_rn(bv, gamma) : bv);
+    }
+  }
+  if (load_stats) {
+    int mx = (e < E) ? c : INT_MIN, mn = (e < E) ? c : INT_MAX;
+    mx = __reduce_max_sync(0xffffffffu, mx);
+    mn = __reduce_min_sync(0xffffffffu, mn);
+    if (lane == 0) {
+      red_max[warp] = mx;
+      red_min[warp] = mn;
+    }
+    __syncthreads();
+    if (e == 0) {
+      const int nw = (blockDim.x + 31) / 32;
+      for (int w = 1; w < nw; ++w) {
+        mx = max(mx, red_max[w]);
+        mn = min(mn, red_min[w]);
+      }
+      load_stats[0] = (float)mx;
+      load_stats[1] = (float)((double)T * K / E);
+      load_stats[2] = (float)mn;
+    }
+  }
+}
+
+// ===================================================================
+// Stable dispatch order.  Block = kRouteTokensPerBlock tokens, one warp per
+// 32-token chunk, lane = token.  mask[w][e] has bit l set when lane l's
+// token chose e; a token's rank among the block's tokens choosing e is
+// (earlier warps' popcounts) + popc(mask & lanes below).
+// ===================================================================
+constexpr int kDestWarps = kRouteTokensPerBlock / 32;
+
+__global__ void __launch_bounds__(kDestWarps * 32)
+    dest_kernel(const int32_t* __restrict__ topk_idx,
+                const int32_t* __restrict__ block_base, int T, int E, int K,
+                int32_t* __restrict__ dest, int32_t* __restrict__ src_row,
+                DevStatus* st) {
+  extern __shared__ uint32_t dsm[];
+  uint32_t* mask = dsm;                      // [kDestWarps][E]
+  uint32_t* pre = dsm + kDestWarps * E;      // [kDestWarps][E]
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  for (int i = tid; i < kDestWarps * E; i += blockDim.x) mask[i] = 0;
+  __syncthreads();
+  const int t = blockIdx.x * kRouteTokensPerBlock + warp * 32 + lane;
+  const bool valid = t < T;
+  if (valid)
+    for (int k = 0; k < K; ++k) {
+      const int e = topk_idx[(size_t)t * K + k];
+      if (e >= 0 && e < E) atomicOr(&mask[warp * E + e], 1u << lane);
+    }
+  __syncthreads();
+  for (int e = tid; e < E; e += blockDim.x) {
+    uint32_t run = 0;
+    for (int w = 0; w < kDestWarps; ++w) {
+      pre[w * E + e] = run;
+      run += __popc(mask[w * E + e]);
+    }
+  }
+  __syncthreads();
+  if (!valid) return;
+  const uint32_t below = (1u << lane) - 1u;
+  const int32_t* base = block_base + (size_t)blockIdx.x * E;
+  const int rows = T * K;
+  for (int k = 0; k < K; ++k) {
+    const int e = topk_idx[(size_t)t * K + k];
+    int r = -1;
+    if (e >= 0 && e < E)
+      r = base[e] + (int)pre[warp * E + e] +
+          __popc(mask[warp * E + e] & below);
+    if (r >= 0 && r < rows) {
+      src_row[r] = t * K + k;
+    } else {
+      r = -1;
+      record_error(st, MOE_ERR_DEVICE_BOUNDS, 11);
+    }
+    dest[(size_t)t * K + k] = r;
+  }
+}
+
+// ===================================================================
+// Gather (dispatch): xp[dest[t,k]] = x[t].  One block per token reads the
+// row once (16-byte vectors) and writes it K times.
+// ===================================================================
+constexpr int kRowThreads = 128;
+constexpr int kMaxVecPerThread = 16;  // H <= 128*16*8 = 16384
+
+__global__ void __launch_bounds__(kRowThreads)
+    gather_kernel(const uint16_t* __restrict__ x,
+                  const int32_t* __restrict__ dest, int H, int K, int rows,
+                  uint16_t* __restrict__ xp) {
+  const int t = blockIdx.x;
+  const int nvec = H / 8;
+  const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * H);
+  uint4 v[kMaxVecPerThread];
+#pragma unroll
+  for (int i = 0; i < kMaxVecPerThread; ++i) {
+    const int c = threadIdx.x + i * kRowThreads;
+    if (c < nvec) v[i] = __ldg(src + c);
+  }
+  for (int k = 0; k < K; ++k) {
+    const int r = __ldg(dest + (size_t)t * K + k);
+    if (r < 0 || r >= rows) continue;  // invalid slot: written nowhere
+    uint4* dst = reinterpret_cast<uint4*>(xp + (size_t)r * H);
+#pragma unroll
+    for (int i = 0; i < kMaxVecPerThread; ++i) {
+      const int c = threadIdx.x + i * kRowThreads;
+      if (c < nvec) dst[c] = v[i];
+    }
+  }
+}
+
+// ===================================================================
+// Combine (eq. 12): out_t = bf16(x_t + ys_t + sum_k g_k * yp[dest[t,k]]),
+// fp32 arithmetic, slots in order.  One block per token, 8 bf16 per thread
+// per step.
+// ===================================================================
+__global__ void __launch_bounds__(kRowThreads)
+    combine_kernel(const uint16_t* __restrict__ x,
+                   const uint16_t* __restrict__ ys,
+                   const uint16_t* __restrict__ yp,
+                   const int32_t* __restrict__ dest,
+                   const float* __restrict__ gate, int H, int K, int rows,
+                   uint16_t* __restrict__ out) {
+  __shared__ int sd[32];
+  __shared__ float sg[32];
+  const int t = blockIdx.x;
+  if (threadIdx.x < K) {
+    const int r = dest[(size_t)t * K + threadIdx.x];
+    const bool ok = r >= 0 && r < rows;  // an invalid slot adds nothing
+    sd[threadIdx.x] = ok ? r : 0;
+    sg[threadIdx.x] = ok ? gate[(size_t)t * K + threadIdx.x] : 0.f;
+  }
+  __syncthreads();
+  const int nvec = H / 8;
+  for (int c = threadIdx.x; c < nvec; c += kRowThreads) {
+    const uint4 xv = __ldg(reinterpret_cast<const uint4*>(x + (size_t)t * H) + c);
+    const uint4 sv =
+        __ldg(reinterpret_cast<const uint4*>(ys + (size_t)t * H) + c);
+    const uint32_t xa[4] = {xv.x, xv.y, xv.z, xv.w};
+    const uint32_t sa[4] = {sv.x, sv.y, sv.z, sv.w};
+    float acc[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      acc[2 * i] = bf16_lo(xa[i]) + bf16_lo(sa[i]);
+      acc[2 * i + 1] = bf16_hi(xa[i]) + bf16_hi(sa[i]);
+    }
+    for (int k = 0; k < K; ++k) {
+      const uint4 yv = __ldg(
+          reinterpret_cast<const uint4*>(yp + (size_t)sd[k] * H) + c);
+      const uint32_t ya[4] = {yv.x, yv.y, yv.z, yv.w};
+      const float g = sg[k];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        acc[2 * i] = fmaf(g, bf16_lo(ya[i]), acc[2 * i]);
+        acc[2 * i + 1] = fmaf(g, bf16_hi(ya[i]), acc[2 * i + 1]);
+      }
+    }
+    uint4 o;
+    o.x = pack_bf16x2(acc[0], acc[1]);
+    o.y = pack_bf16x2(acc[2], acc[3]);
+    o.z = pack_bf16x2(acc[4], acc[5]);
+    o.w = pack_bf16x2(acc[6], acc[7]);
+    reinterpret_cast<uint4*>(out + (size_t)t * H)[c] = o;
+  }
+}
+}  // namespace
+
+// ------------------------------------------------------------ launchers
+cudaError_t launch_route(const float* logits, const float* bias, int T, int E,
+                         int n_group, int topk_group, int topk,
+                         int32_t* topk_idx, float* topk_gate,
+                         int32_t* block_counts, cudaStream_t s) {
+  const int epl = E <= 32 ? 1 : E / 32;
+  const int lpg = (E / n_group) / epl;
+  const int nblk = route_blocks(T);
+  const dim3 block(kRouteWarps * 32);
+#define MOE_ROUTE_CASE(N)                                                   \
+  case N:                                                                   \
+    route_kernel<N><<<nblk, block, 0, s>>>(logits, bias, T, E, n_group,     \
+                                           topk_group, topk, lpg, topk_idx, \
+                                           topk_gate, block_counts);        \
+    break;
+  switch (epl) {
+    MOE_ROUTE_CASE(1)
+    MOE_ROUTE_CASE(2)
+    MOE_ROUTE_CASE(4)
+    MOE_ROUTE_CASE(8)
+    MOE_ROUTE_CASE(16)
+    MOE_ROUTE_CASE(32)
+    default:
+      return cudaErrorInvalidValue;
+  }
+#undef MOE_ROUTE_CASE
+  return cudaGetLastError();
+}
+
+cudaError_t launch_block_counts(const int32_t* topk_idx, int T, int E,
+                                int topk, int32_t* block_counts,
+                                DevStatus* st, cudaStream_t s) {
+  block_counts_kernel<<<route_blocks(T), 256, 0, s>>>(topk_idx, T, E, topk,
+                                                      block_counts, st);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scan(const int32_t* block_counts, int T, int E, int topk,
+                        int32_t* counts, int32_t* offsets, int32_t* block_base,
+                        float* bias, float gamma, float* load_stats,
+                        cudaStream_t s) {
+  const int threads = ((E + 31) / 32) * 32;
+  scan_kernel<<<1, threads, 0, s>>>(block_counts, route_blocks(T), T, E, topk,
+                                    counts, offsets, block_base, bias, gamma,
+                                    load_stats);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dest(const int32_t* topk_idx, const int32_t* block_base,
+                        int T, int E, int topk, int32_t* dest,
+                        int32_t* src_row, DevStatus* st, cudaStream_t s) {
+  const size_t smem = sizeof(uint32_t) * 2 * kDestWarps * E;
+  dest_kernel<<<route_blocks(T), kDestWarps * 32, smem, s>>>(
+      topk_idx, block_base, T, E, topk, dest, src_row, st);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather(const uint16_t* x, const int32_t* dest, int T, int H,
+                          int topk, uint16_t* xp, cudaStream_t s) {
+  if (H / 8 > kRowThreads * kMaxVecPerThread) return cudaErrorInvalidValue;
+  gather_kernel<<<T, kRowThreads, 0, s>>>(x, dest, H, topk, T * topk, xp);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const uint16_t* x, const uint16_t* ys,
+                           const uint16_t* yp, const int32_t* dest,
+                           const float* gate, int T, int H, int topk,
+                           uint16_t* out, cudaStream_t s) {
+  combine_kernel<<<T, kRowThreads, 0, s>>>(x, ys, yp, dest, gate, H, topk,
+                                           T * topk, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bias_update(const int32_t* counts, float* bias,
+                               float* load_stats, int T, int E, int topk,
+                               float gamma, cudaStream_t s) {
+  // the scan kernel with one "block" whose counts are the given counts:
+  // block_counts = counts, nblk = 1; it writes no offsets / base
+  const int threads = ((E + 31) / 32) * 32;
+  scan_kernel<<<1, threads, 0, s>>>(counts, 1, T, E, topk, nullptr, nullptr,
+                                    nullptr, bias, gamma, load_stats);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -2,10 +2,22 @@
 
 This module is the one piece that both the CUDA path's tests/bench and the CPU
 oracle consume.  It holds NO arithmetic of the method: it only draws random
-numbers, rounds them to bf16 storage, and lays them out.  Every tensor is keyed
-by (config seed, tensor id, expert, step) through numpy's ``SeedSequence`` so
-any single expert's weights can be regenerated on the host without touching
-the others (the oracle uses that to check sampled tokens at full V3 size).
+numbers, rounds them to bf16 storage, and lays them out.
+
+bf16 tensors (activations and expert weights) come from a counter-based
+generator: element i of a tensor with 32-bit key k (derived by numpy's
+``SeedSequence`` from config seed, tensor id, expert and step) gets the
+16-bit cell  mix32(i * 0x9E3779B1 + k) & 0xFFFF,  where mix32 is a
+multiply/xor-shift finaliser whose multipliers are below 2^31, so every
+intermediate fits in a signed 64-bit integer without overflow.  The cell
+picks one of 2^16 equiprobable cells of N(0, sigma); the value is that
+cell's midpoint quantile, rounded to bf16 (inverse-transform sampling from
+the normal quantised to 2^16 cells, support +-4.3 sigma, finer than bf16).
+The same integer formula runs in numpy on the host and in torch on the GPU
+and gives identical bits, so the 22.5 GB of V3 expert weights are generated
+directly in device memory while the oracle regenerates any single expert on
+the host.  fp32 tensors (router weight, bias, logits) are small and are
+drawn on the host from Philox streams keyed the same way.
 
 Shapes follow the DeepSeek-V3 MoE layer described on "02 · DeepSeek-V3"
 (PaperTrace) §1.1 and the walkthrough's config field list ("DeepSeek-V3
@@ -55,6 +67,7 @@ class MoEConfig:
     zipf_s: float = 0.0          # >0: skewed per-expert logit preference
     zipf_beta: float = 0.0
     steps: int = 1
+    weight_seed_id: int = -1     # config whose weights these are (-1: own)
 
     def dims(self, **over) -> dict:
         d = dict(T=self.T, H=self.H, E=self.E, n_group=self.n_group,
@@ -72,11 +85,14 @@ CONFIGS = {
                           topk_group=4, topk=8, I=2048, I_shared=2048),
     "prefill_v3": MoEConfig("prefill_v3", 2, T=4096, H=7168, E=256, n_group=8,
                             topk_group=4, topk=8, I=2048, I_shared=2048),
+    # decode and the skewed run use the prefill layer's weights and router
     "decode_v3": MoEConfig("decode_v3", 3, T=128, H=7168, E=256, n_group=8,
-                           topk_group=4, topk=8, I=2048, I_shared=2048),
+                           topk_group=4, topk=8, I=2048, I_shared=2048,
+                           weight_seed_id=2),
     "skewed_v3": MoEConfig("skewed_v3", 4, T=32768, H=7168, E=256, n_group=8,
                            topk_group=4, topk=8, I=2048, I_shared=2048,
-                           zipf_s=1.2, zipf_beta=1.0, steps=50),
+                           zipf_s=1.2, zipf_beta=1.0, steps=50,
+                           weight_seed_id=2),
 }
 
 
@@ -85,10 +101,24 @@ def custom_config(name: str, config_id: int, **kw) -> MoEConfig:
     return MoEConfig(name, config_id, **kw)
 
 
+_WEIGHT_TENSORS = ("w_router", "w1", "w3", "w2", "ws1", "ws3", "ws2", "bias")
+
+
+def _seed_seq(cfg: MoEConfig, tensor: str, expert: int = 0, step: int = 0):
+    cid = cfg.config_id
+    if tensor in _WEIGHT_TENSORS and cfg.weight_seed_id >= 0:
+        cid = cfg.weight_seed_id
+    return np.random.SeedSequence([BASE_SEED + cid, _TID[tensor], expert,
+                                   step])
+
+
 def _rng(cfg: MoEConfig, tensor: str, expert: int = 0, step: int = 0):
-    ss = np.random.SeedSequence([BASE_SEED + cfg.config_id, _TID[tensor],
-                                 expert, step])
-    return np.random.Generator(np.random.PCG64(ss))
+    return np.random.Generator(np.random.Philox(_seed_seq(cfg, tensor, expert,
+                                                          step)))
+
+
+def _key32(cfg: MoEConfig, tensor: str, expert: int = 0, step: int = 0) -> int:
+    return int(_seed_seq(cfg, tensor, expert, step).generate_state(1)[0])
 
 
 def f32_to_bf16_bits(a: np.ndarray) -> np.ndarray:
@@ -104,18 +134,73 @@ def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
             << np.uint32(16)).view(np.float32)
 
 
-def _normal_bf16(rng, shape, sigma):
-    a = rng.standard_normal(size=shape, dtype=np.float32)
-    if sigma != 1.0:
-        a *= np.float32(sigma)
-    return f32_to_bf16_bits(a)
+_QTABLE: dict = {}
+
+
+def quantile_table(sigma: float) -> np.ndarray:
+    """bf16 bits of sigma * Phi^-1((i + 1/2) / 2^16), i = 0 .. 2^16 - 1."""
+    t = _QTABLE.get(sigma)
+    if t is None:
+        from scipy.special import ndtri
+        q = ndtri((np.arange(65536, dtype=np.float64) + 0.5) / 65536.0)
+        t = f32_to_bf16_bits((q * sigma).astype(np.float32))
+        _QTABLE[sigma] = t
+    return t
+
+
+_GOLD, _MIX1, _MIX2, _M32 = 0x9E3779B1, 0x7FEB352D, 0x2C1B3C6D, 0xFFFFFFFF
+_CHUNK = 1 << 24
+
+
+def cells_numpy(n: int, key: int, start: int = 0) -> np.ndarray:
+    """16-bit cells of elements start .. start+n-1, in numpy (a second,
+    independent evaluation of the formula; the generator itself runs the
+    torch one on the host CPU or the GPU)."""
+    x = np.arange(start, start + n, dtype=np.int64)
+    x = (x * _GOLD + key) & _M32
+    x ^= x >> 16
+    x = (x * _MIX1) & _M32
+    x ^= x >> 15
+    x = (x * _MIX2) & _M32
+    x ^= x >> 16
+    return (x & 0xFFFF).astype(np.int64)
+
+
+def cells_torch(n: int, key: int, device, start: int = 0):
+    """The same cells computed with torch int64 ops on `device`."""
+    import torch
+    x = torch.arange(start, start + n, dtype=torch.int64, device=device)
+    x = (x * _GOLD + key) & _M32
+    x ^= x >> 16
+    x = (x * _MIX1) & _M32
+    x ^= x >> 15
+    x = (x * _MIX2) & _M32
+    x ^= x >> 16
+    return x & 0xFFFF
+
+
+def normal_bf16(key: int, shape, sigma: float, device=None):
+    """bf16 bits ~ N(0, sigma): numpy uint16 on the host (device=None), or a
+    torch int16 tensor generated on `device`; identical bits either way."""
+    import torch
+    n = int(np.prod(shape))
+    table = quantile_table(float(sigma))
+    dev = "cpu" if device is None else device
+    tab = torch.from_numpy(table.view(np.int16)).to(dev)
+    out = torch.empty(n, dtype=torch.int16, device=dev)
+    for s0 in range(0, n, _CHUNK):
+        m = min(_CHUNK, n - s0)
+        out[s0:s0 + m] = tab[cells_torch(m, key, dev, s0)]
+    out = out.reshape(shape)
+    return out.numpy().view(np.uint16) if device is None else out
 
 
 # ----------------------------------------------------------------- activations
-def x_tokens(cfg: MoEConfig, step: int = 0, T: int | None = None) -> np.ndarray:
-    """Activations x[T, H] ~ N(0, 1), bf16 bits."""
+def x_tokens(cfg: MoEConfig, step: int = 0, T: int | None = None,
+             device=None):
+    """Activations x[T, H] ~ N(0, 1), bf16 bits (host, or torch on device)."""
     T = cfg.T if T is None else T
-    return _normal_bf16(_rng(cfg, "x", 0, step), (T, cfg.H), 1.0)
+    return normal_bf16(_key32(cfg, "x", 0, step), (T, cfg.H), 1.0, device)
 
 
 def router_weight(cfg: MoEConfig) -> np.ndarray:
@@ -144,20 +229,32 @@ def zipf_preference(cfg: MoEConfig) -> np.ndarray:
 
 
 # --------------------------------------------------------------------- experts
-def expert_weights(cfg: MoEConfig, e: int):
+def expert_weights(cfg: MoEConfig, e: int, device=None):
     """Routed expert e: (w1[I,H], w3[I,H], w2[H,I]) bf16 bits ~ N(0, w_sigma)."""
     s = cfg.w_sigma
-    return (_normal_bf16(_rng(cfg, "w1", e), (cfg.I, cfg.H), s),
-            _normal_bf16(_rng(cfg, "w3", e), (cfg.I, cfg.H), s),
-            _normal_bf16(_rng(cfg, "w2", e), (cfg.H, cfg.I), s))
+    return (normal_bf16(_key32(cfg, "w1", e), (cfg.I, cfg.H), s, device),
+            normal_bf16(_key32(cfg, "w3", e), (cfg.I, cfg.H), s, device),
+            normal_bf16(_key32(cfg, "w2", e), (cfg.H, cfg.I), s, device))
 
 
-def shared_weights(cfg: MoEConfig):
+def shared_weights(cfg: MoEConfig, device=None):
     """Shared expert: (ws1[I_s,H], ws3[I_s,H], ws2[H,I_s]) bf16 bits."""
     s = cfg.w_sigma
-    return (_normal_bf16(_rng(cfg, "ws1"), (cfg.I_shared, cfg.H), s),
-            _normal_bf16(_rng(cfg, "ws3"), (cfg.I_shared, cfg.H), s),
-            _normal_bf16(_rng(cfg, "ws2"), (cfg.H, cfg.I_shared), s))
+    return (normal_bf16(_key32(cfg, "ws1"), (cfg.I_shared, cfg.H), s, device),
+            normal_bf16(_key32(cfg, "ws3"), (cfg.I_shared, cfg.H), s, device),
+            normal_bf16(_key32(cfg, "ws2"), (cfg.H, cfg.I_shared), s, device))
+
+
+def device_expert_weights(cfg: MoEConfig, device):
+    """All routed experts generated in device memory: torch int16 tensors
+    w1[E,I,H], w3[E,I,H], w2[E,H,I] (same bits as expert_weights)."""
+    import torch
+    w1 = torch.empty((cfg.E, cfg.I, cfg.H), dtype=torch.int16, device=device)
+    w3 = torch.empty_like(w1)
+    w2 = torch.empty((cfg.E, cfg.H, cfg.I), dtype=torch.int16, device=device)
+    for e in range(cfg.E):
+        w1[e], w3[e], w2[e] = expert_weights(cfg, e, device)
+    return w1, w3, w2
 
 
 def all_expert_weights(cfg: MoEConfig, threads: int | None = None):
@@ -172,16 +269,6 @@ def all_expert_weights(cfg: MoEConfig, threads: int | None = None):
     with ThreadPoolExecutor(threads or os.cpu_count() or 4) as ex:
         list(ex.map(fill, range(cfg.E)))
     return w1, w3, w2
-
-
-def stream_expert_weights(cfg: MoEConfig, sink, threads: int | None = None):
-    """Generate routed experts one at a time and hand each to ``sink(e, w1,
-    w3, w2)`` (used to fill device memory without holding all 22.5 GB of the
-    V3 layer on the host)."""
-    with ThreadPoolExecutor(threads or os.cpu_count() or 4) as ex:
-        for e, ws in enumerate(ex.map(lambda i: expert_weights(cfg, i),
-                                      range(cfg.E))):
-            sink(e, *ws)
 
 
 def layer_inputs(cfg: MoEConfig, step: int = 0) -> dict:

@@ -1,0 +1,203 @@
+"""ctypes binding of libmoe.so -- argument marshalling only.
+
+Each function has the name of the C entry point it calls (include/moe.h)
+and takes torch CUDA tensors; torch provides device memory and the current
+stream, nothing else.  Every step of the layer runs in the library's CUDA
+kernels.  There is no fallback: if the library is missing or a call fails,
+an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libmoe.so")
+
+MOE_WS_ROUTE, MOE_WS_PERMUTE, MOE_WS_EXPERT_FFN, MOE_WS_FORWARD = 0, 1, 2, 3
+
+STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
+          3: "MOE_ERR_ALIGNMENT", 4: "MOE_ERR_WORKSPACE", 5: "MOE_ERR_CUDA",
+          6: "MOE_ERR_TIMEOUT", 7: "MOE_ERR_DEVICE_BOUNDS"}
+STATUS_CODES = {v: k for k, v in STATUS.items()}
+
+
+class MoeError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        super().__init__(f"{fn} returned {STATUS.get(code, code)}")
+        self.code = code
+
+
+class MoeDims(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int32), ("H", ctypes.c_int32),
+                ("E", ctypes.c_int32), ("n_group", ctypes.c_int32),
+                ("topk_group", ctypes.c_int32), ("topk", ctypes.c_int32),
+                ("I", ctypes.c_int32), ("I_shared", ctypes.c_int32),
+                ("gamma", ctypes.c_float)]
+
+
+class MoeWeights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in
+                ("w_router", "w1", "w3", "w2", "ws1", "ws3", "ws2")]
+
+
+_P = ctypes.c_void_p
+_D = ctypes.POINTER(MoeDims)
+_W = ctypes.POINTER(MoeWeights)
+_S = ctypes.c_size_t
+_I = ctypes.c_int
+_SIGS = {
+    "moe_workspace_bytes": (ctypes.c_size_t, [_D, _I]),
+    "moe_router_logits": (_I, [_D, _P, _P, _P, _P]),
+    "moe_route": (_I, [_D, _P, _P, _P, _P, _P, _P, _S, _P]),
+    "moe_permute": (_I, [_D, _P, _P, _P, _P, _P, _P, _P, _S, _P]),
+    "moe_expert_ffn": (_I, [_D, _W, _P, _P, _P, _P, _P, _P, _S, _P]),
+    "moe_combine": (_I, [_D, _P, _P, _P, _P, _P, _P, _P]),
+    "moe_bias_update": (_I, [_D, _P, _P, _P, _P]),
+    "moe_forward": (_I, [_D, _W, _P, _P, _I, _P, _P, _P, _P, _P, _P, _P, _S,
+                         _P]),
+    "moe_status_string": (ctypes.c_char_p, [_I]),
+    "moe_get_device_error": (_I, [_P, _P]),
+    "moe_set_wait_timeout_ns": (None, [ctypes.c_uint64]),
+    "moe_abi_version": (ctypes.c_int32, []),
+}
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libmoe.so (once).  Raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing; build it with "
+                "`python -m deepseekmoe_routing_expert_moe_b300.build` "
+                "(there is no CPU fallback)")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib
+
+
+# ------------------------------------------------------------ marshalling
+def dims(T, H, E, n_group, topk_group, topk, I=64, I_shared=64,
+         gamma=0.001) -> MoeDims:
+    return MoeDims(T, H, E, n_group, topk_group, topk, I, I_shared, gamma)
+
+
+def dims_of(cfg, **over) -> MoeDims:
+    return dims(**cfg.dims(**over))
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def _check(fn: str, code: int):
+    if code != 0:
+        raise MoeError(fn, code)
+
+
+class Weights:
+    """Device weights of one layer (torch tensors; bf16 stored as int16)."""
+
+    def __init__(self, w_router, w1, w3, w2, ws1, ws3, ws2):
+        self.w_router, self.w1, self.w3, self.w2 = w_router, w1, w3, w2
+        self.ws1, self.ws3, self.ws2 = ws1, ws3, ws2
+        self.struct = MoeWeights(*(_ptr(t) for t in (w_router, w1, w3, w2,
+                                                      ws1, ws3, ws2)))
+
+
+def workspace_bytes(d: MoeDims, which: int) -> int:
+    return lib().moe_workspace_bytes(ctypes.byref(d), which)
+
+
+def workspace(d: MoeDims, which: int, device="cuda") -> torch.Tensor:
+    """A zeroed device workspace sized for entry point `which`."""
+    n = workspace_bytes(d, which)
+    if n == 0:
+        raise MoeError("moe_workspace_bytes", 1)
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+# ----------------------------------------------------------- entry points
+def moe_router_logits(d, x, w_router, logits, stream=None):
+    _check("moe_router_logits", lib().moe_router_logits(
+        ctypes.byref(d), _ptr(x), _ptr(w_router), _ptr(logits),
+        _stream(stream)))
+
+
+def moe_route(d, logits, bias, topk_idx, topk_gate, counts, ws, stream=None):
+    _check("moe_route", lib().moe_route(
+        ctypes.byref(d), _ptr(logits), _ptr(bias), _ptr(topk_idx),
+        _ptr(topk_gate), _ptr(counts), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def moe_permute(d, x, topk_idx, offsets, dest, src_row, xp, ws, stream=None):
+    _check("moe_permute", lib().moe_permute(
+        ctypes.byref(d), _ptr(x), _ptr(topk_idx), _ptr(offsets), _ptr(dest),
+        _ptr(src_row), _ptr(xp), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def moe_expert_ffn(d, w: Weights, xp, x, offsets, yp, ys, ws, stream=None):
+    _check("moe_expert_ffn", lib().moe_expert_ffn(
+        ctypes.byref(d), ctypes.byref(w.struct), _ptr(xp), _ptr(x),
+        _ptr(offsets), _ptr(yp), _ptr(ys), _ptr(ws), ws.numel(),
+        _stream(stream)))
+
+
+def moe_combine(d, x, ys, yp, dest, topk_gate, out, stream=None):
+    _check("moe_combine", lib().moe_combine(
+        ctypes.byref(d), _ptr(x), _ptr(ys), _ptr(yp), _ptr(dest),
+        _ptr(topk_gate), _ptr(out), _stream(stream)))
+
+
+def moe_bias_update(d, counts, bias, load_stats=None, stream=None):
+    _check("moe_bias_update", lib().moe_bias_update(
+        ctypes.byref(d), _ptr(counts), _ptr(bias), _ptr(load_stats),
+        _stream(stream)))
+
+
+def moe_forward(d, w: Weights, x, bias, out, ws, update_bias=False,
+                logits_out=None, topk_idx_out=None, topk_gate_out=None,
+                counts_out=None, load_stats_out=None, stream=None):
+    _check("moe_forward", lib().moe_forward(
+        ctypes.byref(d), ctypes.byref(w.struct), _ptr(x), _ptr(bias),
+        1 if update_bias else 0, _ptr(out), _ptr(logits_out),
+        _ptr(topk_idx_out), _ptr(topk_gate_out), _ptr(counts_out),
+        _ptr(load_stats_out), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def moe_get_device_error(ws, stream=None) -> int:
+    return lib().moe_get_device_error(_ptr(ws), _stream(stream))
+
+
+def moe_set_wait_timeout_ns(ns: int):
+    lib().moe_set_wait_timeout_ns(ns)
+
+
+def moe_status_string(code: int) -> str:
+    return lib().moe_status_string(code).decode()
+
+
+def moe_abi_version() -> int:
+    return lib().moe_abi_version()

@@ -1,0 +1,234 @@
+/*
+ * moe.h -- C ABI of the B300 (sm_103a) DeepSeekMoE layer forward.
+ *
+ * The layer (DeepSeek-V3 MoE block, as described on "02 · DeepSeek-V3"
+ * (PaperTrace) §1.1, §1.3 and §1.4):
+ *
+ *   s_{t,e}  = sigmoid(z_{t,e}),  z = x W_r^T              (eq. 15)
+ *   u_{t,e}  = s_{t,e} + b_e      -- used for selection only (eq. 16)
+ *   group score S_g = sum of the 2 largest u in group g; keep the best
+ *   topk_group groups; choose the topk experts with the largest u among them
+ *   g_{t,k}  = s_{t,e_k} / sum_j s_{t,e_j}                  (eq. 13)
+ *   out_t    = x_t + FFN_shared(x_t) + sum_k g_{t,k} FFN_{e_k}(x_t)  (eq. 12)
+ *   FFN(a)   = W2 (silu(W1 a) * (W3 a))                    (SwiGLU, §1.1)
+ *   end of step: c_e = load of expert e over the batch; b_e -= gamma if
+ *   c_e > T*K/E, b_e += gamma if c_e < T*K/E                (§1.4)
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - All tensor pointers are DEVICE pointers owned by the caller, dense,
+ *    row-major, 16-byte aligned (MOE_ERR_ALIGNMENT otherwise).  The library
+ *    never allocates or frees device memory; scratch comes from a caller
+ *    workspace sized by moe_workspace_bytes().
+ *  - bf16 tensors are passed as uint16_t bit patterns.
+ *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL = the
+ *    legacy default stream): no host synchronisation, no device-to-host copy.
+ *  - Arguments are validated on the host before anything is launched;
+ *    MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED / MOE_ERR_ALIGNMENT /
+ *    MOE_ERR_WORKSPACE are returned without touching the device.
+ *    Launch failures return MOE_ERR_CUDA (checked with cudaGetLastError,
+ *    without a sync).
+ *  - Kernels that wait on asynchronous copies bound every wait; a wait that
+ *    runs out records MOE_ERR_TIMEOUT in the workspace error word and the
+ *    kernel returns cleanly.  moe_get_device_error() reports it.
+ *  - Results are deterministic: no floating-point atomics, fixed orders.
+ *  - T = 0 is valid: token-sized tensors may then be NULL; counts and
+ *    offsets are zeroed, nothing else is written.
+ *
+ * Supported shapes (MOE_ERR_UNSUPPORTED outside them):
+ *    H, I, I_shared: multiples of 64, >= 64
+ *    E <= 32, or E in {64, 128, 256, 512, 1024}; E % n_group == 0;
+ *    group size E/n_group >= 2; with L = max(1, E/32) experts per lane,
+ *    (E/n_group) % L == 0 and (E/n_group)/L a power of two;
+ *    1 <= topk_group <= n_group <= 32; 1 <= topk <= min(32,
+ *    topk_group*E/n_group); T*(topk+1) < 2^31.
+ */
+#ifndef DEEPSEEKMOE_B300_MOE_H
+#define DEEPSEEKMOE_B300_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_ABI_VERSION 1
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,   /* NULL pointer, negative or inconsistent dims */
+  MOE_ERR_UNSUPPORTED = 2,   /* valid dims this build has no kernel for     */
+  MOE_ERR_ALIGNMENT = 3,     /* a pointer is not 16-byte aligned            */
+  MOE_ERR_WORKSPACE = 4,     /* workspace NULL or smaller than required     */
+  MOE_ERR_CUDA = 5,          /* a CUDA runtime/driver call failed           */
+  MOE_ERR_TIMEOUT = 6,       /* a bounded device-side wait ran out          */
+  MOE_ERR_DEVICE_BOUNDS = 7  /* a device-side index check failed            */
+} moe_status_t;
+
+/* A cudaStream_t, passed as an opaque handle so this header needs no CUDA
+ * include.  NULL selects the legacy default stream. */
+typedef void* moe_stream_t;
+
+/* Layer dimensions.  Names follow the pages: T tokens, H hidden size, E
+ * routed experts, n_group expert groups ("nodes" on the pages), topk_group
+ * groups kept per token (4 for V3), topk experts per token (8 for V3), I the
+ * routed expert intermediate size (2048 for V3), I_shared the shared expert
+ * intermediate size, gamma the bias step (0.001 for V3). */
+typedef struct {
+  int32_t T;
+  int32_t H;
+  int32_t E;
+  int32_t n_group;
+  int32_t topk_group;
+  int32_t topk;
+  int32_t I;
+  int32_t I_shared;
+  float gamma;
+} moe_dims_t;
+
+/* Expert and router weights (device pointers, caller-owned, read only).
+ *   w_router [E, H]    fp32   router vectors, one row per expert
+ *   w1       [E, I, H] bf16   gate projection of each routed expert
+ *   w3       [E, I, H] bf16   up projection
+ *   w2       [E, H, I] bf16   down projection
+ *   ws1 [I_shared, H], ws3 [I_shared, H], ws2 [H, I_shared]: shared expert
+ */
+typedef struct {
+  const float* w_router;
+  const uint16_t* w1;
+  const uint16_t* w3;
+  const uint16_t* w2;
+  const uint16_t* ws1;
+  const uint16_t* ws3;
+  const uint16_t* ws2;
+} moe_weights_t;
+
+/* Which entry point a workspace is sized for. */
+typedef enum {
+  MOE_WS_ROUTE = 0,
+  MOE_WS_PERMUTE = 1,
+  MOE_WS_EXPERT_FFN = 2,
+  MOE_WS_FORWARD = 3
+} moe_ws_kind_t;
+
+/* Bytes of device workspace `which` needs for dims `d` (0 if d is invalid).
+ * A MOE_WS_FORWARD-sized workspace is large enough for every entry point.
+ * The first 256 bytes hold the device error word; zero the whole workspace
+ * once after allocating it (moe_get_device_error() re-zeroes the word). */
+size_t moe_workspace_bytes(const moe_dims_t* d, moe_ws_kind_t which);
+
+/* Router logits z = x W_r^T (eq. 15 context), fp32 accumulation of the exact
+ * bf16->fp32 activations.  x [T, H] bf16, w_router [E, H] fp32 ->
+ * logits [T, E] fp32.  Needs no workspace. */
+moe_status_t moe_router_logits(const moe_dims_t* d, const uint16_t* x,
+                               const float* w_router, float* logits,
+                               moe_stream_t stream);
+
+/* Routing from precomputed logits ("02 · DeepSeek-V3" §1.3, §1.4):
+ * sigmoid, + bias for selection, group-limited top-K, gates renormalised
+ * over the chosen K, and the per-expert load histogram.
+ *   logits   [T, E] fp32      in
+ *   bias     [E]    fp32      in (not modified)
+ *   topk_idx [T, K] int32     out, slot k = k-th largest s+b among the kept
+ *                             groups' experts (ties: lower expert index)
+ *   topk_gate[T, K] fp32      out, s_{e_k} / sum_j s_{e_j}, summed in slot
+ *                             order (sum to 1)
+ *   counts   [E]    int32     out, tokens routed to each expert
+ * The fp32 sigmoid is one fixed sequence of correctly rounded operations
+ * (Cody-Waite reduction, degree-7 Taylor polynomial, rounded divide), so
+ * routing is reproducible bit for bit.  Workspace: MOE_WS_ROUTE. */
+moe_status_t moe_route(const moe_dims_t* d, const float* logits,
+                       const float* bias, int32_t* topk_idx, float* topk_gate,
+                       int32_t* counts, void* ws, size_t ws_bytes,
+                       moe_stream_t stream);
+
+/* Dispatch order and token gather (the single-GPU form of the pages'
+ * "dispatch" step, "02 · DeepSeek-V3" §2 and §5.1).  A stable counting sort
+ * of the (token, slot) pairs by expert:
+ *   offsets [E+1]  int32  out, offsets[e] = sum_{e'<e} c_e', offsets[E]=T*K
+ *   dest    [T, K] int32  out, row of (t, k) in the expert-sorted order:
+ *                         offsets[e] + #{t' < t that chose e}
+ *   src_row [T*K]  int32  out, inverse of dest: src_row[dest[t,k]] = t*K+k
+ *   xp      [T*K, H] bf16 out, xp[dest[t,k]] = x[t]; may be NULL (indices
+ *                         only), x may then be NULL too.
+ * topk_idx must hold valid, per-token distinct experts (as moe_route
+ * writes them).  Workspace: MOE_WS_PERMUTE. */
+moe_status_t moe_permute(const moe_dims_t* d, const uint16_t* x,
+                         const int32_t* topk_idx, int32_t* offsets,
+                         int32_t* dest, int32_t* src_row, uint16_t* xp,
+                         void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Expert FFNs ("02 · DeepSeek-V3" §1.1: SwiGLU, three matrices per expert)
+ * as grouped BF16 GEMMs on the tcgen05 tensor cores, fp32 accumulation in
+ * tensor memory, SwiGLU fused into the first GEMM's epilogue; the
+ * intermediate is stored as bf16.
+ *   xp      [T*K, H] bf16  routed rows, expert e owns rows
+ *                          [offsets[e], offsets[e+1])
+ *   x       [T, H]   bf16  token rows for the shared expert
+ *   offsets [E+1]    int32 as written by moe_permute (read on the device)
+ *   yp      [T*K, H] bf16  out, FFN_e(row) for every routed row (ungated)
+ *   ys      [T, H]   bf16  out, FFN_shared(x_t)
+ * Workspace: MOE_WS_EXPERT_FFN. */
+moe_status_t moe_expert_ffn(const moe_dims_t* d, const moe_weights_t* w,
+                            const uint16_t* xp, const uint16_t* x,
+                            const int32_t* offsets, uint16_t* yp,
+                            uint16_t* ys, void* ws, size_t ws_bytes,
+                            moe_stream_t stream);
+
+/* Combine (eq. 12): out_t = bf16( x_t + ys_t + sum_k g_{t,k} yp[dest[t,k]] ),
+ * fp32 arithmetic, slots summed in order.  out [T, H] bf16 may not alias
+ * the inputs.  Needs no workspace. */
+moe_status_t moe_combine(const moe_dims_t* d, const uint16_t* x,
+                         const uint16_t* ys, const uint16_t* yp,
+                         const int32_t* dest, const float* topk_gate,
+                         uint16_t* out, moe_stream_t stream);
+
+/* Auxiliary-loss-free bias step ("02 · DeepSeek-V3" §1.4), in place:
+ * b_e -= gamma if c_e*E > T*K (overloaded), b_e += gamma if c_e*E < T*K,
+ * unchanged at exactly the mean load.  counts [E] int32 in, bias [E] fp32
+ * in/out, load_stats [3] fp32 out (max, mean, min of c) or NULL.
+ * Call it after the step's routing: the next step routes with the new b. */
+moe_status_t moe_bias_update(const moe_dims_t* d, const int32_t* counts,
+                             float* bias, float* load_stats,
+                             moe_stream_t stream);
+
+/* The whole layer forward in one call: router logits, routing, dispatch,
+ * expert FFNs, combine, and -- if update_bias != 0 -- the bias step on this
+ * batch's load (applied after routing, so this call routes with the bias it
+ * was given).
+ *   x [T, H] bf16 in; bias [E] fp32 in (in/out when update_bias);
+ *   out [T, H] bf16 out.
+ *   Optional outputs (NULL = not written): logits_out [T, E] fp32,
+ *   topk_idx_out [T, K] int32, topk_gate_out [T, K] fp32, counts_out [E]
+ *   int32, load_stats_out [3] fp32.
+ * Workspace: MOE_WS_FORWARD. */
+moe_status_t moe_forward(const moe_dims_t* d, const moe_weights_t* w,
+                         const uint16_t* x, float* bias, int update_bias,
+                         uint16_t* out, float* logits_out,
+                         int32_t* topk_idx_out, float* topk_gate_out,
+                         int32_t* counts_out, float* load_stats_out, void* ws,
+                         size_t ws_bytes, moe_stream_t stream);
+
+/* Human-readable name of a status code (static string). */
+const char* moe_status_string(moe_status_t s);
+
+/* Synchronises `stream`, reads and clears the device error word at the
+ * start of `ws`, and returns it (MOE_OK if no kernel recorded an error).
+ * Meant for tests and debugging: it blocks the host. */
+moe_status_t moe_get_device_error(void* ws, moe_stream_t stream);
+
+/* Upper bound, in nanoseconds, on every device-side wait of the GEMM
+ * kernels (default 2e9 ns).  0 restores the default.  Takes effect for
+ * launches made after the call; not thread-safe against concurrent
+ * launches. */
+void moe_set_wait_timeout_ns(uint64_t ns);
+
+/* MOE_ABI_VERSION of the loaded library. */
+int32_t moe_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DEEPSEEKMOE_B300_MOE_H */

@@ -1,0 +1,133 @@
+"""The C ABI without a GPU: the library loads, exports every entry point
+include/moe.h declares, sizes workspaces, and rejects bad arguments on the
+host before anything is launched (only failing calls are made here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from deepseekmoe_routing_expert_moe_b300 import build, ops
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    build.build()
+    return ops.lib()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "moe.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_header_declares_the_six_layer_entry_points():
+    names = declared_functions()
+    for n in ("moe_route", "moe_permute", "moe_expert_ffn", "moe_combine",
+              "moe_bias_update", "moe_forward"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    names = declared_functions()
+    assert len(names) >= 12
+    for n in names:
+        assert hasattr(L, n), n
+    # and the binding wraps each under the same name
+    for n in names:
+        assert n in ops._SIGS, n
+
+
+def test_abi_version_and_status_strings(L):
+    assert ops.moe_abi_version() == 1
+    for code, name in ops.STATUS.items():
+        assert ops.moe_status_string(code) == name
+
+
+V3 = dict(T=4096, H=7168, E=256, n_group=8, topk_group=4, topk=8, I=2048,
+          I_shared=2048, gamma=0.001)
+
+
+def test_workspace_sizes_are_consistent(L):
+    d = ops.dims(**V3)
+    r = ops.workspace_bytes(d, ops.MOE_WS_ROUTE)
+    p = ops.workspace_bytes(d, ops.MOE_WS_PERMUTE)
+    f = ops.workspace_bytes(d, ops.MOE_WS_EXPERT_FFN)
+    fw = ops.workspace_bytes(d, ops.MOE_WS_FORWARD)
+    assert 0 < r <= fw and 0 < p <= fw and 0 < f <= fw
+    # the forward workspace holds xp, yp (T*K*H bf16 each) and h
+    assert fw >= 2 * 4096 * 8 * 7168 * 2 + 4096 * 8 * 2048 * 2
+    bad = ops.dims(**dict(V3, E=255))
+    assert ops.workspace_bytes(bad, ops.MOE_WS_FORWARD) == 0
+    assert ops.workspace_bytes(d, 9) == 0
+
+
+FAKE = 1 << 20  # a 16-byte aligned address; never dereferenced here
+
+
+def _route(L, d, ws_bytes=1 << 30, logits=FAKE, ws=FAKE):
+    return L.moe_route(ctypes.byref(d), logits, FAKE, FAKE, FAKE, FAKE, ws,
+                       ws_bytes, None)
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(E=255), 1),            # E % n_group != 0
+    (dict(n_group=4, topk_group=5), 1),
+    (dict(topk=33, topk_group=8), 2),
+    (dict(E=16, n_group=16, topk_group=2, topk=2), 1),  # group of 1
+    (dict(T=-1), 1),
+    (dict(topk=0), 1),
+    (dict(topk=129), 1),         # more than topk_group * group size
+    (dict(E=48, n_group=8, topk_group=4, topk=8), 2),   # E % 32
+    (dict(E=2048, n_group=32, topk_group=4, topk=8), 2),
+    (dict(H=7000), 2),
+    (dict(E=96, n_group=8, topk_group=4, topk=8), 2),   # 3 experts per lane
+    (dict(gamma=float("nan")), 1),
+])
+def test_route_rejects_bad_dims(L, over, code):
+    d = ops.dims(**dict(V3, **over))
+    assert _route(L, d) == code
+
+
+def test_null_misaligned_and_small_workspace(L):
+    d = ops.dims(**V3)
+    assert _route(L, d, logits=None) == 1
+    assert _route(L, d, logits=FAKE + 4) == 3
+    assert _route(L, d, ws=None) == 4
+    assert _route(L, d, ws_bytes=16) == 4
+    assert L.moe_route(None, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 30,
+                       None) == 1
+
+
+def test_ffn_and_forward_validation(L):
+    d = ops.dims(**V3)
+    w = ops.MoeWeights(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None)
+    assert L.moe_expert_ffn(ctypes.byref(d), ctypes.byref(w), FAKE, FAKE,
+                            FAKE, FAKE, FAKE, FAKE, 1 << 40, None) == 1
+    w = ops.MoeWeights(FAKE, FAKE, FAKE, FAKE + 2, FAKE, FAKE, FAKE)
+    assert L.moe_expert_ffn(ctypes.byref(d), ctypes.byref(w), FAKE, FAKE,
+                            FAKE, FAKE, FAKE, FAKE, 1 << 40, None) == 3
+    d2 = ops.dims(**dict(V3, I=100))
+    w = ops.MoeWeights(*(FAKE,) * 7)
+    assert L.moe_forward(ctypes.byref(d2), ctypes.byref(w), FAKE, FAKE, 0,
+                         FAKE, None, None, None, None, None, FAKE, 1 << 40,
+                         None) == 2
+    assert L.moe_forward(ctypes.byref(d), ctypes.byref(w), FAKE, FAKE, 0,
+                         FAKE, None, None, None, None, None, FAKE, 100,
+                         None) == 4
+    assert L.moe_combine(ctypes.byref(d), FAKE, FAKE, None, FAKE, FAKE, FAKE,
+                         None) == 1
+    assert L.moe_bias_update(ctypes.byref(d), FAKE, None, None, None) == 1
+    assert L.moe_permute(ctypes.byref(d), None, FAKE, FAKE, FAKE, FAKE, FAKE,
+                         FAKE, 1 << 30, None) == 1
+    assert L.moe_get_device_error(None, None) == 1
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(ops, "LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(ops, "_lib", None)
+    with pytest.raises(RuntimeError, match="no CPU fallback"):
+        ops.lib()

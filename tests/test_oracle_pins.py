@@ -419,3 +419,29 @@ def test_v3_shape_constants_match_the_pages():
     active = per_expert * (cfg.topk + g["n_shared_experts"])
     assert round(active / 1e6) == g["active_expert_params_per_layer_millions_approx"]
     assert cfg.gamma == g["bias_gamma"]
+
+
+# ------------------------------------------------------ input generator
+def test_generator_host_and_numpy_evaluations_agree():
+    """The counter-based cells are the same integers whether evaluated by
+    numpy or by torch (the device path uses the torch one)."""
+    from deepseekmoe_routing_expert_moe_b300.inputs import (cells_numpy,
+                                                            cells_torch)
+    for key, start in ((0, 0), (123456789, 5), (0xFFFFFFFF, (1 << 31) - 5000)):
+        a = cells_numpy(4096, key, start)
+        b = cells_torch(4096, key, "cpu", start).numpy()
+        assert np.array_equal(a, b)
+
+
+def test_generator_statistics():
+    from deepseekmoe_routing_expert_moe_b300.inputs import cells_numpy
+    c = cells_numpy(1 << 20, 987654321)
+    h = np.bincount(c, minlength=65536)
+    chi2 = (((h - h.mean()) ** 2) / h.mean()).sum() / 65535
+    assert 0.95 < chi2 < 1.05
+    cfg = inputs.CONFIGS["tiny"]
+    w = inputs.bf16_bits_to_f32(inputs.expert_weights(cfg, 0)[0]).ravel()
+    assert abs(w.mean()) < 1e-3 and abs(w.std() - 0.02) < 1e-3
+    x = inputs.bf16_bits_to_f32(inputs.x_tokens(cfg)).ravel()
+    assert abs(x.std() - 1.0) < 0.02
+    assert abs(np.corrcoef(x[:-1], x[1:])[0, 1]) < 0.02
