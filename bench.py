@@ -1,0 +1,436 @@
+#!/usr/bin/env python
+"""Throughput of the DeepSeek-V3-shaped MoE layer forward on B300.
+
+A step is one pass of the whole hot path over one batch: router logits,
+routing (sigmoid + bias, group-limited top-8, gates), load histogram and
+bias step, dispatch order, gather, grouped expert GEMMs (SwiGLU fused),
+combine with the shared expert and the residual.  Default workload: the
+prefill layer, T = 4096 tokens, hidden 7168, 256 routed experts (I = 2048) +
+1 shared, top-8 of 8 groups / 4 kept; bf16 weights and activations, fp32
+accumulation; seeded synthetic inputs.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl b300|reference]
+
+Prints ONE JSON line (rank 0).  --impl reference times the CPU oracle (the
+only reference that exists for this layer) on a bounded token sample.
+Multi-GPU: replicas only -- every rank runs its own layer on its own tokens,
+no collective on the data path; value = all ranks' tokens / max rank time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = ("tokens/s per V3-shaped MoE layer on 1 B300 (bf16); "
+          "% of TC peak / HBM roofline")
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0,
+                  "bf16_tflops_sustained": 1400.0}
+
+
+# ------------------------------------------------------------------ utils
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def blas_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i["num_threads"] for i in threadpool_info()
+             if i.get("user_api") == "blas"]
+        return max(n) if n else (os.cpu_count() or 1)
+    except Exception:  # noqa: BLE001
+        return os.cpu_count() or 1
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled during the timed region."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+             "sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.out = None
+
+    def __enter__(self):
+        try:
+            self.out = open(os.devnull, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx),
+                 f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        for l in self.lines:
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx.append(float(f[1]))
+            except ValueError:
+                continue
+            for name, v in zip(self.NAMES, f[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [],
+                    "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def gpu_index_for_smi(local_rank: int) -> int:
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        parts = [p.strip() for p in vis.split(",") if p.strip()]
+        if local_rank < len(parts) and parts[local_rank].isdigit():
+            return int(parts[local_rank])
+    return local_rank
+
+
+def source_hash(*rel) -> str:
+    h = hashlib.sha256()
+    for r in rel:
+        with open(os.path.join(ROOT, r), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str, workload: str):
+    """dram read+write bytes per launch of `kernel` from the committed ncu
+    summary, if it was taken on the current kernel source; else None."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        e = d[f"{kernel}@{workload}"]
+        if e["source_hash"] != source_hash(*e["sources"]):
+            return None
+        return float(e["dram_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+# ------------------------------------------------------------ CPU oracle
+def oracle_sample(cfg, n_tokens: int, step: int = 0):
+    """Inputs of a bounded sample for the oracle: the first n_tokens of the
+    step's batch plus the weights of every expert they route to (generated
+    outside the timed part)."""
+    from deepseekmoe_routing_expert_moe_b300 import inputs
+    from oracle import moe_oracle as O
+    f = inputs.bf16_bits_to_f32
+    x = f(inputs.x_tokens(cfg, step=step, T=n_tokens))
+    wr = inputs.router_weight(cfg)
+    b = inputs.bias(cfg)
+    z = O.router_logits(x, wr)
+    r = O.route(z, b, cfg.n_group, cfg.topk_group, cfg.topk)
+    ew = {int(e): tuple(f(a) for a in inputs.expert_weights(cfg, int(e)))
+          for e in np.unique(r["idx"])}
+    sw = tuple(f(a) for a in inputs.shared_weights(cfg))
+    return dict(x=x, wr=wr, b=b, ew=ew, sw=sw)
+
+
+def oracle_time(cfg, s) -> float:
+    """Seconds for the oracle's layer forward of the sample (logits,
+    routing, load + bias step, every chosen expert, shared expert, combine)."""
+    from oracle import moe_oracle as O
+    t0 = time.perf_counter()
+    z = O.router_logits(s["x"], s["wr"])
+    r = O.route(z, s["b"], cfg.n_group, cfg.topk_group, cfg.topk)
+    c = O.expert_counts(r["idx"], cfg.E)
+    O.bias_update(c, s["b"], len(s["x"]), cfg.topk, cfg.gamma)
+    O.layer_rows(s["x"], r["idx"], r["gate"], lambda e: s["ew"][e], s["sw"])
+    return time.perf_counter() - t0
+
+
+# --------------------------------------------------------------- the arm
+def workload_desc(cfg) -> str:
+    return (f"{cfg.name}: V3 MoE layer forward + bias step, T={cfg.T}, "
+            f"H={cfg.H}, E={cfg.E}+1 shared, I={cfg.I}, top-{cfg.topk} of "
+            f"{cfg.n_group} groups / {cfg.topk_group} kept")
+
+
+def config_json(cfg, n_gpus):
+    return {"workload": workload_desc(cfg), "T": cfg.T, "H": cfg.H,
+            "E": cfg.E, "I": cfg.I, "I_shared": cfg.I_shared,
+            "topk": cfg.topk, "n_group": cfg.n_group,
+            "topk_group": cfg.topk_group, "global_batch": cfg.T * n_gpus,
+            "parallelism": f"replicas x{n_gpus} (no data-path collective)",
+            "l2": "inputs larger than L2: 22.6 GB of expert weights streamed "
+                  "per step; 4 rotating activation batches"}
+
+
+def run_gpu(args, rank, world, local_rank):
+    import torch
+    from deepseekmoe_routing_expert_moe_b300 import inputs, ops
+    torch.cuda.set_device(local_rank)
+    cfg = inputs.CONFIGS[args.workload]
+    d = ops.dims_of(cfg)
+    T, H, E, K = cfg.T, cfg.H, cfg.E, cfg.topk
+
+    # ---- inputs resident in HBM
+    w1, w3, w2 = inputs.device_expert_weights(cfg, "cuda")
+    ws1, ws3, ws2 = inputs.shared_weights(cfg, "cuda")
+    wr = torch.from_numpy(inputs.router_weight(cfg)).cuda()
+    W = ops.Weights(wr, w1, w3, w2, ws1, ws3, ws2)
+    NB = 4
+    xs = [inputs.x_tokens(cfg, step=i + 1000 * rank, device="cuda")
+          for i in range(NB)]
+    bias = torch.from_numpy(inputs.bias(cfg)).cuda()
+    out = torch.empty((T, H), dtype=torch.int16, device="cuda")
+    counts = torch.zeros(E, dtype=torch.int32, device="cuda")
+    ws = ops.workspace(d, ops.MOE_WS_FORWARD)
+    stream = torch.cuda.current_stream()
+
+    def step(i, counts_out=None):
+        ops.moe_forward(d, W, xs[i % NB], bias, out, ws, update_bias=True,
+                        counts_out=counts_out)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    assert ops.moe_get_device_error(ws) == 0
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    # ---- timed region: exactly K steps
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(gpu_index_for_smi(local_rank)) as clk:
+        barrier()
+        ev0.record(stream)
+        for i in range(args.steps):
+            step(i)
+        ev1.record(stream)
+        barrier()
+    ms = ev0.elapsed_time(ev1)
+    clocks = clk.summary()
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_per_step = ms / args.steps
+    value = world * T * args.steps / (ms / 1e3)
+
+    # ---- kernel-level timing (separate pass, same steps, events between
+    #      the library's launches on its stream)
+    nk = ops.MOE_FORWARD_KERNELS
+    sets = [[torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)]
+            for _ in range(args.steps)]
+    for i in range(args.steps):
+        ops.moe_set_profile_events(sets[i])
+        step(i, counts_out=counts if i == args.steps - 1 else None)
+    ops.moe_set_profile_events(None)
+    torch.cuda.synchronize()
+    kt = np.array([[s[j].elapsed_time(s[j + 1]) for j in range(nk)]
+                   for s in sets])          # ms, [steps, kernels]
+    kmean = kt.mean(0)
+    kernels = {n: round(float(v), 4) for n, v in
+               zip(ops.FORWARD_KERNEL_NAMES, kmean)}
+    c = counts.cpu().numpy().astype(np.int64)
+    assert c.sum() == T * K
+
+    # ---- roofline of the dominant kernel (expert up-projection GEMM)
+    pk, pk_src = peaks()
+    touched = int((c > 0).sum())
+    I, Is = cfg.I, cfg.I_shared
+    up_bytes = (touched * 2 * I * H * 2 + 2 * Is * H * 2 +     # W1, W3 (+shared)
+                T * K * H * 2 + T * H * 2 +                    # A: xp, x
+                T * K * I * 2 + T * Is * 2)                    # h written
+    up_flops = 2.0 * (T * K + T) * H * 2 * I
+    dn_bytes = (touched * H * I * 2 + H * Is * 2 + T * K * I * 2 + T * Is * 2
+                + T * K * H * 2 + T * H * 2)
+    dn_flops = 2.0 * (T * K + T) * I * H
+    t_up = kmean[5] / 1e3
+    t_dn = kmean[6] / 1e3
+    hbm = float(pk["hbm_gbs"])
+    tc = float(pk.get("bf16_tflops_sustained", pk["bf16_tflops"]))
+    up_hbm_s = up_bytes / (hbm * 1e9)
+    up_tc_s = up_flops / (tc * 1e12)
+    if up_hbm_s >= up_tc_s:
+        roof = {"bound": "hbm", "achieved": round(up_bytes / t_up / 1e9, 1),
+                "peak": hbm, "unit": "GB/s"}
+    else:
+        roof = {"bound": "tensor",
+                "achieved": round(up_flops / t_up / 1e12, 1),
+                "peak": tc, "unit": "TFLOP/s"}
+    roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
+    roof["traffic"] = ncu_traffic("gemm_up_swiglu", cfg.name)
+    roof["kernel"] = "grouped_gemm_kernel<up,N=256> (expert up-projection + SwiGLU)"
+    roof["algorithmic_bytes"] = int(up_bytes)
+    roof["peak_source"] = f"{pk_src} (MEASURED_PEAKS.json)" \
+        if pk_src == "measured" else "fallback (profiling recipe)"
+    roof["tensor_frac"] = round(up_flops / t_up / 1e12 / tc, 4)
+    roof["down_gemm"] = {"ms": round(kmean[6], 4),
+                         "hbm_frac": round(dn_bytes / t_dn / 1e9 / hbm, 4),
+                         "tensor_frac": round(dn_flops / t_dn / 1e12 / tc, 4)}
+
+    # ---- end to end through the C ABI with host buffers
+    xh = [torch.empty((T, H), dtype=torch.int16).pin_memory() for _ in range(NB)]
+    for i in range(NB):
+        xh[i].copy_(xs[i].cpu())
+    oh = torch.empty((T, H), dtype=torch.int16).pin_memory()
+    xd = torch.empty((T, H), dtype=torch.int16, device="cuda")
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    barrier()
+    e0.record(stream)
+    for i in range(args.steps):
+        xd.copy_(xh[i % NB], non_blocking=True)
+        ops.moe_forward(d, W, xd, bias, out, ws, update_bias=True)
+        oh.copy_(out, non_blocking=True)
+    e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([e2e_ms], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    assert ops.moe_get_device_error(ws) == 0
+
+    res = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic, seeded (x ~N(0,1), expert weights ~N(0,0.02) "
+                "bf16, router ~N(0,0.006) fp32, bias ~U(-0.01,0.01))",
+        "config": config_json(cfg, world),
+        "roofline": roof,
+        "e2e": {"value": round(world * T * args.steps / (e2e_ms / 1e3), 1),
+                "unit": "tokens/s", "h2d_bytes_per_step": T * H * 2,
+                "d2h_bytes_per_step": T * H * 2},
+        "gpu_launches": nk * args.steps,
+        "clocks": clocks,
+        "kernels_ms": kernels,
+        "experts_touched": touched,
+        "impl": "b300",
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        s = oracle_sample(cfg, args.cpu_sample_tokens)
+        sec = oracle_time(cfg, s)
+        res["cpu_baseline"] = {
+            "value": round(args.cpu_sample_tokens / sec, 4),
+            "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
+            "sample": f"first {args.cpu_sample_tokens} tokens of the batch "
+                      f"through the numpy fp64 oracle ({sec:.1f} s: logits, "
+                      "routing, bias step, their experts + shared expert)"}
+    return res
+
+
+def run_reference(args):
+    """The oracle arm: the CPU oracle as it stands, per step one bounded
+    sample of the workload (the same tokens every step)."""
+    from deepseekmoe_routing_expert_moe_b300 import inputs
+    cfg = inputs.CONFIGS[args.workload]
+    n = args.ref_tokens
+    s = oracle_sample(cfg, n)
+    for _ in range(args.warmup):
+        oracle_time(cfg, s)
+    times = [oracle_time(cfg, s) for _ in range(args.steps)]
+    tot = sum(times)
+    v = n * args.steps / tot
+    cores = blas_threads()
+    sample = (f"{n} tokens of the {cfg.name} batch per step through the numpy "
+              "fp64 oracle (logits, routing, bias step, experts, combine)")
+    return {
+        "metric": METRIC, "value": round(v, 4), "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(tot / args.steps * 1e3, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic, seeded",
+        "config": config_json(cfg, 1),
+        "impl": "reference",
+        "cpu_baseline": {"value": round(v, 4), "unit": "tokens/s",
+                         "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(v, 4), "unit": "tokens/s",
+                "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=("b300", "reference"), default="b300")
+    ap.add_argument("--workload", default="prefill_v3",
+                    choices=("prefill_v3", "decode_v3", "skewed_v3",
+                             "prefill_v3_e32"))
+    ap.add_argument("--cpu-sample-tokens", type=int, default=4)
+    ap.add_argument("--ref-tokens", type=int, default=1)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    res = run_gpu(args, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

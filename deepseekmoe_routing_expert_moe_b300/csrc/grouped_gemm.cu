@@ -486,6 +486,8 @@ int launch_expert_ffn(const FfnArgs& a, cudaStream_t s) {
   int rc = (bf == 128) ? launch_one<kUp, 256, kStages>(up, s)
                        : launch_one<kUp, 128, kStages>(up, s);
   if (rc != MOE_OK) return rc;
+  if (a.between_event != nullptr)
+    cudaEventRecord(static_cast<cudaEvent_t>(a.between_event), s);
 
   // ---- down projection
   GemmParams dn;

@@ -62,6 +62,7 @@ struct FfnArgs {
   uint16_t *yp, *ys;               // outputs
   DevStatus* status;
   uint64_t wait_limit_ns;
+  void* between_event = nullptr;   // cudaEvent_t recorded between the GEMMs
 };
 // 0 on success, else a moe_status_t (encoding or launch failure)
 int launch_expert_ffn(const FfnArgs& a, cudaStream_t s);

@@ -18,6 +18,13 @@ constexpr size_t kAlign = 256;
 constexpr size_t kStatusBytes = 256;
 constexpr uint64_t kDefaultWaitNs = 2000000000ull;
 uint64_t g_wait_limit_ns = kDefaultWaitNs;
+void* const* g_prof_events = nullptr;  // moe_set_profile_events()
+
+// records profiling event i (if enabled) on stream s
+inline void prof_mark(int i, cudaStream_t s) {
+  if (g_prof_events != nullptr)
+    cudaEventRecord(static_cast<cudaEvent_t>(g_prof_events[i]), s);
+}
 
 inline size_t up(size_t b) { return (b + kAlign - 1) / kAlign * kAlign; }
 inline bool aligned16(const void* p) {
@@ -165,7 +172,7 @@ moe_status_t ffn_launch(const moe_dims_t* d, const moe_weights_t* w,
                         const uint16_t* xp, const uint16_t* x,
                         const int32_t* offsets, uint16_t* h, uint16_t* hs,
                         uint16_t* yp, uint16_t* ys, DevStatus* st,
-                        cudaStream_t s) {
+                        cudaStream_t s, void* between_event = nullptr) {
   moe::FfnArgs a;
   a.T = d->T;
   a.H = d->H;
@@ -188,6 +195,7 @@ moe_status_t ffn_launch(const moe_dims_t* d, const moe_weights_t* w,
   a.ys = ys;
   a.status = st;
   a.wait_limit_ns = g_wait_limit_ns;
+  a.between_event = between_event;
   return static_cast<moe_status_t>(moe::launch_expert_ffn(a, s));
 }
 
@@ -209,6 +217,12 @@ const char* moe_status_string(moe_status_t s) {
     case MOE_ERR_DEVICE_BOUNDS: return "MOE_ERR_DEVICE_BOUNDS";
   }
   return "MOE_ERR_UNKNOWN";
+}
+
+void moe_set_profile_events(void* const* events, int32_t n) {
+  g_prof_events = (events != nullptr && n >= MOE_FORWARD_KERNELS + 1)
+                      ? events
+                      : nullptr;
 }
 
 void moe_set_wait_timeout_ns(uint64_t ns) {
@@ -425,19 +439,29 @@ moe_status_t moe_forward(const moe_dims_t* d, const moe_weights_t* w,
   uint16_t* yp = at<uint16_t>(ws, L.yp);
   uint16_t* ys = at<uint16_t>(ws, L.ys);
 
+  prof_mark(0, s);
   MOE_TRY(cuda_ok(moe::launch_router_logits(x, w->w_router, logits, T, H, E, s)));
+  prof_mark(1, s);
   MOE_TRY(cuda_ok(moe::launch_route(logits, bias, T, E, d->n_group,
                                     d->topk_group, K, idx, gate, bc, s)));
+  prof_mark(2, s);
   // counts, offsets, block bases -- and the bias step on this batch's load,
   // after routing consumed the old bias (same stream, so ordered)
   MOE_TRY(cuda_ok(moe::launch_scan(bc, T, E, K, counts, offsets, bb,
                                    update_bias ? bias : nullptr, d->gamma,
                                    load_stats_out, s)));
+  prof_mark(3, s);
   MOE_TRY(cuda_ok(moe::launch_dest(idx, bb, T, E, K, dest, src_row, st, s)));
+  prof_mark(4, s);
   MOE_TRY(cuda_ok(moe::launch_gather(x, dest, T, H, K, xp, s)));
+  prof_mark(5, s);  // 6 is recorded between the two expert GEMMs
   MOE_TRY(ffn_launch(d, w, xp, x, offsets, at<uint16_t>(ws, L.h),
-                     at<uint16_t>(ws, L.hs), yp, ys, st, s));
-  return cuda_ok(moe::launch_combine(x, ys, yp, dest, gate, T, H, K, out, s));
+                     at<uint16_t>(ws, L.hs), yp, ys, st, s,
+                     g_prof_events ? g_prof_events[6] : nullptr));
+  prof_mark(7, s);
+  MOE_TRY(cuda_ok(moe::launch_combine(x, ys, yp, dest, gate, T, H, K, out, s)));
+  prof_mark(8, s);
+  return MOE_OK;
 }
 
 }  // extern "C"

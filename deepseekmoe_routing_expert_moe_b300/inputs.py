@@ -93,6 +93,12 @@ CONFIGS = {
                            topk_group=4, topk=8, I=2048, I_shared=2048,
                            zipf_s=1.2, zipf_beta=1.0, steps=50,
                            weight_seed_id=2),
+    # profiling stand-in for the prefill layer: the same 128 rows per expert
+    # and the same per-expert shapes, but 32 experts (2.9 GB of weights), so
+    # that a full counter capture holds only a few GB on the device
+    "prefill_v3_e32": MoEConfig("prefill_v3_e32", 5, T=512, H=7168, E=32,
+                                n_group=8, topk_group=4, topk=8, I=2048,
+                                I_shared=2048),
 }
 
 

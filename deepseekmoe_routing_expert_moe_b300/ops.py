@@ -62,7 +62,13 @@ _SIGS = {
     "moe_get_device_error": (_I, [_P, _P]),
     "moe_set_wait_timeout_ns": (None, [ctypes.c_uint64]),
     "moe_abi_version": (ctypes.c_int32, []),
+    "moe_set_profile_events": (None, [ctypes.POINTER(ctypes.c_void_p),
+                                       ctypes.c_int32]),
 }
+
+MOE_FORWARD_KERNELS = 8
+FORWARD_KERNEL_NAMES = ("router_logits", "route", "scan", "dest", "gather",
+                        "gemm_up_swiglu", "gemm_down", "combine")
 
 _lib = None
 
@@ -193,6 +199,25 @@ def moe_get_device_error(ws, stream=None) -> int:
 
 def moe_set_wait_timeout_ns(ns: int):
     lib().moe_set_wait_timeout_ns(ns)
+
+
+_prof_keep = None
+
+
+def moe_set_profile_events(events):
+    """events: a list of MOE_FORWARD_KERNELS + 1 torch.cuda.Event (enabled
+    for timing), or None to disable."""
+    global _prof_keep
+    if events is None:
+        _prof_keep = None
+        lib().moe_set_profile_events(None, 0)
+        return
+    for e in events:        # torch creates the CUDA event on first record
+        e.record()
+    torch.cuda.synchronize()
+    arr = (ctypes.c_void_p * len(events))(*(e.cuda_event for e in events))
+    _prof_keep = (events, arr)
+    lib().moe_set_profile_events(arr, len(events))
 
 
 def moe_status_string(code: int) -> str:

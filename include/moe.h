@@ -224,6 +224,19 @@ moe_status_t moe_get_device_error(void* ws, moe_stream_t stream);
  * launches. */
 void moe_set_wait_timeout_ns(uint64_t ns);
 
+/* Profiling hook for kernel-level timing.  When `events` is non-NULL and
+ * n >= MOE_FORWARD_KERNELS + 1, moe_forward records events[i] (cudaEvent_t
+ * handles created by the caller, passed as void*) on its stream just before
+ * its i-th kernel launch, and events[MOE_FORWARD_KERNELS] after the last,
+ * so consecutive events bracket one kernel each.  The launch order is:
+ *   0 router logits, 1 route, 2 count scan (+bias step), 3 dispatch order,
+ *   4 gather, 5 expert up-projection GEMM (+SwiGLU), 6 expert
+ *   down-projection GEMM, 7 combine.
+ * NULL / n = 0 disables.  The array must stay valid while enabled.  Global
+ * state: not for concurrent use from several threads. */
+#define MOE_FORWARD_KERNELS 8
+void moe_set_profile_events(void* const* events, int32_t n);
+
 /* MOE_ABI_VERSION of the loaded library. */
 int32_t moe_abi_version(void);
 

@@ -61,3 +61,27 @@ def rms_tolerance_check(got, ref, rows=None, frac=2e-2):
     err = np.max(np.abs(g - f)) if g.size else 0.0
     assert err <= frac * rms, (err, rms, err / rms)
     return err / rms
+
+
+U_BF16 = 2.0 ** -8   # unit roundoff of bf16 (8-bit significand)
+
+
+def ffn_bound_check(got, a, w1, w3, w2):
+    """Elementwise bound for one expert FFN whose intermediate h and output
+    y are stored in bf16 with fp32 accumulation:
+        |y_gpu - y| <= u*|y| + u*sum_i |m_i| |W2_ji|  (+ fp32 slack)
+    with u = 2^-8 and m = silu(W1 a) * (W3 a) in fp64 -- the first term is
+    the output rounding, the second the rounding of every h_i.  Returns the
+    largest error / bound ratio (must be <= 1)."""
+    from oracle import moe_oracle as O
+    a = np.asarray(a, np.float64)
+    p = a @ np.asarray(w1, np.float64).T
+    q = a @ np.asarray(w3, np.float64).T
+    m = O.silu(p) * q
+    w2 = np.asarray(w2, np.float64)
+    y = m @ w2.T
+    bound = 1.01 * U_BF16 * np.abs(y) + 1.1 * U_BF16 * (np.abs(m) @ np.abs(w2).T)
+    bound += 1e-5 * np.sqrt(np.mean(y * y)) + 1e-30
+    ratio = np.abs(np.asarray(got, np.float64) - y) / bound
+    assert ratio.max() <= 1.0, ratio.max()
+    return ratio.max()
