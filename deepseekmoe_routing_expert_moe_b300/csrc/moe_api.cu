@@ -5,6 +5,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 
 #include "../../include/moe.h"
 #include "device_common.cuh"
@@ -465,3 +466,75 @@ moe_status_t moe_forward(const moe_dims_t* d, const moe_weights_t* w,
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Routing without a caller workspace.
+//
+// Some callers cannot hand this library any device memory beyond their
+// inputs and outputs: a plugin inside a host framework that owns every
+// device allocation and offers its plugins no scratch, or a latency-critical
+// loop that must not call cudaMalloc after start-up (it synchronises the
+// device).  For them, moe_route_static_scratch keeps the one piece of
+// scratch routing needs -- the per-block expert histogram -- in the file-scope
+// array below, which the CUDA runtime places on every device that loads this
+// library and keeps there until the process exits.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr size_t kRouteScratchInts = 262144;  // 1 MiB of int32
+static __device__ __align__(256) int32_t g_route_scratch[kRouteScratchInts];
+
+constexpr int kMaxScratchDevices = 64;
+int32_t* g_route_scratch_ptr[kMaxScratchDevices] = {};
+std::mutex g_route_scratch_mu;
+
+// Device address of g_route_scratch on the current device, looked up once
+// per device (the host-side name is only a stand-in for it).
+moe_status_t route_scratch_current_device(int32_t** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxScratchDevices) return MOE_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_route_scratch_mu);
+  if (g_route_scratch_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_route_scratch) != cudaSuccess || p == nullptr)
+      return MOE_ERR_CUDA;
+    g_route_scratch_ptr[dev] = static_cast<int32_t*>(p);
+  }
+  *out = g_route_scratch_ptr[dev];
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" moe_status_t moe_route_static_scratch(
+    const moe_dims_t* d, const float* logits, const float* bias,
+    int32_t* topk_idx, float* topk_gate, int32_t* counts,
+    moe_stream_t stream) {
+  MOE_TRY(check_dims(d, false));
+  MOE_NEED_T(logits);
+  MOE_NEED(bias);
+  MOE_NEED_T(topk_idx);
+  MOE_NEED_T(topk_gate);
+  MOE_NEED(counts);
+  MOE_ALIGN(logits);
+  MOE_ALIGN(bias);
+  MOE_ALIGN(topk_idx);
+  MOE_ALIGN(topk_gate);
+  MOE_ALIGN(counts);
+  // the histogram needs one row of E counts per 64-token block
+  if ((size_t)moe::route_blocks(d->T) * (size_t)d->E > kRouteScratchInts)
+    return MOE_ERR_WORKSPACE;
+  cudaStream_t s = cs(stream);
+  if (d->T == 0)
+    return cuda_ok(cudaMemsetAsync(counts, 0, sizeof(int32_t) * d->E, s));
+  int32_t* scratch = nullptr;
+  MOE_TRY(route_scratch_current_device(&scratch));
+  // every block writes its whole histogram row before the scan reads it,
+  // so nothing left from an earlier call needs clearing
+  MOE_TRY(cuda_ok(moe::launch_route(logits, bias, d->T, d->E, d->n_group,
+                                    d->topk_group, d->topk, topk_idx,
+                                    topk_gate, scratch, s)));
+  return cuda_ok(moe::launch_scan(scratch, d->T, d->E, d->topk, counts,
+                                  nullptr, nullptr, nullptr, 0.f, nullptr, s));
+}

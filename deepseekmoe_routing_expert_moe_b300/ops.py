@@ -52,6 +52,7 @@ _SIGS = {
     "moe_workspace_bytes": (ctypes.c_size_t, [_D, _I]),
     "moe_router_logits": (_I, [_D, _P, _P, _P, _P]),
     "moe_route": (_I, [_D, _P, _P, _P, _P, _P, _P, _S, _P]),
+    "moe_route_static_scratch": (_I, [_D, _P, _P, _P, _P, _P, _P]),
     "moe_permute": (_I, [_D, _P, _P, _P, _P, _P, _P, _P, _S, _P]),
     "moe_expert_ffn": (_I, [_D, _W, _P, _P, _P, _P, _P, _P, _S, _P]),
     "moe_combine": (_I, [_D, _P, _P, _P, _P, _P, _P, _P]),
@@ -156,6 +157,15 @@ def moe_route(d, logits, bias, topk_idx, topk_gate, counts, ws, stream=None):
     _check("moe_route", lib().moe_route(
         ctypes.byref(d), _ptr(logits), _ptr(bias), _ptr(topk_idx),
         _ptr(topk_gate), _ptr(counts), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def moe_route_static_scratch(d, logits, bias, topk_idx, topk_gate, counts,
+                             stream=None):
+    """moe_route without a workspace (its scratch is a static device array;
+    concurrent calls on overlapping streams race on it)."""
+    _check("moe_route_static_scratch", lib().moe_route_static_scratch(
+        ctypes.byref(d), _ptr(logits), _ptr(bias), _ptr(topk_idx),
+        _ptr(topk_gate), _ptr(counts), _stream(stream)))
 
 
 def moe_permute(d, x, topk_idx, offsets, dest, src_row, xp, ws, stream=None):

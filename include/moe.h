@@ -143,6 +143,28 @@ moe_status_t moe_route(const moe_dims_t* d, const float* logits,
                        int32_t* counts, void* ws, size_t ws_bytes,
                        moe_stream_t stream);
 
+/* moe_route without a workspace argument, for callers that cannot give
+ * this library any device memory beyond inputs and outputs -- for example a
+ * plugin whose host framework owns all device allocations and offers no
+ * scratch, or a loop that must not call cudaMalloc after start-up because
+ * it synchronises the device.  (The pages have no counterpart: this is an
+ * interface variant, not part of the method.)  Results are identical to
+ * moe_route's.  Its scratch is one static device array of 1 MiB (262144
+ * int32) that every GPU loading this library holds until the process
+ * exits; it allocates nothing and calls no allocating routine.
+ *   Limit: ceil(T/64) * E <= 262144 (T <= 65536 at E = 256), else
+ *   MOE_ERR_WORKSPACE before anything is launched.
+ *   The first call on a device looks up the array's device address (one
+ *   cudaGetSymbolAddress per device); make that first call before any
+ *   stream capture.
+ *   All calls share the array: calls whose kernels overlap on the GPU (on
+ *   different streams, or from several threads) race on it and must be
+ *   serialised by the caller.  Nothing in it needs clearing between calls. */
+moe_status_t moe_route_static_scratch(const moe_dims_t* d, const float* logits,
+                                      const float* bias, int32_t* topk_idx,
+                                      float* topk_gate, int32_t* counts,
+                                      moe_stream_t stream);
+
 /* Dispatch order and token gather (the single-GPU form of the pages'
  * "dispatch" step, "02 · DeepSeek-V3" §2 and §5.1).  A stable counting sort
  * of the (token, slot) pairs by expert:
