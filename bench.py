@@ -310,20 +310,46 @@ def run_gpu(args, rank, world, local_rank):
                          "hbm_frac": round(dn_bytes / t_dn / 1e9 / hbm, 4),
                          "tensor_frac": round(dn_flops / t_dn / 1e12 / tc, 4)}
 
-    # ---- end to end through the C ABI with host buffers
+    # ---- end to end through the C ABI with host buffers: every step copies
+    #      its x from pinned host memory and its output back; the copies run
+    #      on their own streams (double-buffered device x/out) so that step
+    #      i+1's upload and step i's download overlap step i's compute
     xh = [torch.empty((T, H), dtype=torch.int16).pin_memory() for _ in range(NB)]
     for i in range(NB):
         xh[i].copy_(xs[i].cpu())
-    oh = torch.empty((T, H), dtype=torch.int16).pin_memory()
-    xd = torch.empty((T, H), dtype=torch.int16, device="cuda")
+    oh = [torch.empty((T, H), dtype=torch.int16).pin_memory() for _ in range(2)]
+    xd = [torch.empty((T, H), dtype=torch.int16, device="cuda") for _ in range(2)]
+    od = [torch.empty((T, H), dtype=torch.int16, device="cuda") for _ in range(2)]
+    up_s, dn_s = torch.cuda.Stream(), torch.cuda.Stream()
+    ev = lambda: torch.cuda.Event()  # noqa: E731
+    h2d_done = [ev() for _ in range(2)]
+    comp_done = [ev() for _ in range(2)]
+    d2h_done = [ev() for _ in range(2)]
+    for e in comp_done + d2h_done:
+        e.record(stream)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     barrier()
     e0.record(stream)
+    up_s.wait_event(e0)
+    dn_s.wait_event(e0)
     for i in range(args.steps):
-        xd.copy_(xh[i % NB], non_blocking=True)
-        ops.moe_forward(d, W, xd, bias, out, ws, update_bias=True)
-        oh.copy_(out, non_blocking=True)
+        b = i % 2
+        up_s.wait_event(comp_done[b])          # xd[b] no longer read
+        with torch.cuda.stream(up_s):
+            xd[b].copy_(xh[i % NB], non_blocking=True)
+        h2d_done[b].record(up_s)
+        stream.wait_event(h2d_done[b])
+        stream.wait_event(d2h_done[b])         # od[b] already downloaded
+        ops.moe_forward(d, W, xd[b], bias, od[b], ws, update_bias=True,
+                        stream=stream)
+        comp_done[b].record(stream)
+        dn_s.wait_event(comp_done[b])
+        with torch.cuda.stream(dn_s):
+            oh[b].copy_(od[b], non_blocking=True)
+        d2h_done[b].record(dn_s)
+    stream.wait_event(d2h_done[(args.steps - 1) % 2])
+    stream.wait_event(d2h_done[args.steps % 2])
     e1.record(stream)
     barrier()
     e2e_ms = e0.elapsed_time(e1)
@@ -345,8 +371,12 @@ def run_gpu(args, rank, world, local_rank):
         "roofline": roof,
         "e2e": {"value": round(world * T * args.steps / (e2e_ms / 1e3), 1),
                 "unit": "tokens/s", "h2d_bytes_per_step": T * H * 2,
-                "d2h_bytes_per_step": T * H * 2},
-        "gpu_launches": nk * args.steps,
+                "d2h_bytes_per_step": T * H * 2,
+                "overlap": "uploads/downloads on their own streams, "
+                           "double-buffered"},
+        # router logits are two launches (weight split + GEMM) on the
+        # tensor-core path, i.e. when E % 16 == 0
+        "gpu_launches": (nk + (1 if E % 16 == 0 else 0)) * args.steps,
         "clocks": clocks,
         "kernels_ms": kernels,
         "experts_touched": touched,

@@ -10,6 +10,12 @@
 //   up   (MODE kUp):   h = silu(A W1^T) * (A W3^T)   A = xp rows | x rows
 //   down (MODE kDown): y = h W2^T
 //
+// The same kernel also computes the router logits (MODE kRouter, one
+// segment of T token rows): the fp32 router weight is split exactly into
+// three bf16 parts, W = W_hi + W_mid + W_lo, and z = x W_hi^T + x W_mid^T +
+// x W_lo^T accumulates all three into one fp32 accumulator -- each bf16 x
+// bf16 product is exact, so this is an fp32-accumulated x W^T.
+//
 // Design (one persistent CTA per SM, 6 warps):
 //   warp 0 lane 0   TMA producer: A tile 128x64 and B tile BNx64 per stage,
 //                   128-byte swizzle, STAGES-deep mbarrier ring
@@ -46,7 +52,9 @@ constexpr int UMMA_K = 16;         // K of one kind::f16 MMA
 constexpr int kThreads = 192;      // 6 warps
 constexpr uint64_t kDrainNs = 2000000000ull;
 
-enum { kUp = 0, kDown = 1 };
+
+enum { kUp = 0, kDown = 1, kRouter = 2 };
+constexpr int kRouterParts = 3;  // W = hi + mid + lo, each bf16
 enum {
   kSiteProducer = 21,
   kSiteMmaAcc = 22,
@@ -76,8 +84,9 @@ struct GemmParams {  // CUtensorMap members carry their 64-byte alignment
 template <int MODE, int BN>
 struct Shape {
   static constexpr int OUT_COLS = (MODE == kUp) ? BN / 2 : BN;
+  static constexpr int B_PARTS = (MODE == kRouter) ? kRouterParts : 1;
   static constexpr uint32_t A_BYTES = BM * BK * 2;
-  static constexpr uint32_t B_BYTES = BN * BK * 2;
+  static constexpr uint32_t B_BYTES = B_PARTS * BN * BK * 2;
   static constexpr uint32_t TMEM_COLS = 2 * BN;  // two accumulators
   static constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
 };
@@ -243,6 +252,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_2d_hint(
                 smem_u32(sB + stage * S::B_BYTES + (BN / 2) * BK * 2), tb1,
                 kb * BK, brow, fb, pol_w);
+          } else if (MODE == kRouter) {
+            // the three bf16 parts of the router weight, one below the other
+#pragma unroll
+            for (int part = 0; part < kRouterParts; ++part)
+              tma_load_2d_hint(
+                  smem_u32(sB + stage * S::B_BYTES + part * BN * BK * 2), tb0,
+                  kb * BK, part * p.n_shared + brow, fb, pol_a);
           } else {
             tma_load_2d_hint(smem_u32(sB + stage * S::B_BYTES), tb0, kb * BK,
                              brow, fb, pol_w);
@@ -290,10 +306,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t a0 = smem_u32(sA + stage * S::A_BYTES);
           const uint32_t b0 = smem_u32(sB + stage * S::B_BYTES);
 #pragma unroll
-          for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-            tc_mma_f16(d, sw128_kmajor_desc(a0 + kk * UMMA_K * 2),
-                       sw128_kmajor_desc(b0 + kk * UMMA_K * 2), S::IDESC,
-                       (kb | kk) != 0);
+          for (int part = 0; part < S::B_PARTS; ++part) {
+#pragma unroll
+            for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+              tc_mma_f16(d, sw128_kmajor_desc(a0 + kk * UMMA_K * 2),
+                         sw128_kmajor_desc(b0 + part * BN * BK * 2 +
+                                           kk * UMMA_K * 2),
+                         S::IDESC, (kb | part | kk) != 0);
+            }
           }
           any = true;
           tc_commit(smem_u32(&empty[stage]));
@@ -358,6 +378,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint4* dst = reinterpret_cast<uint4*>(orow + c);
             dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
             dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+          }
+        }
+      } else if (MODE == kRouter) {
+        float* frow = reinterpret_cast<float*>(out) +
+                      (size_t)(valid ? row_in_seg : 0) * ld +
+                      (size_t)n * S::OUT_COLS;
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 16) {
+          uint32_t v[16];
+          tmem_ld16(tb + c, v);
+          tmem_ld_wait();
+          if (valid) {
+            uint4* dst = reinterpret_cast<uint4*>(frow + c);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              dst[i] = make_uint4(v[4 * i], v[4 * i + 1], v[4 * i + 2],
+                                  v[4 * i + 3]);
           }
         }
       } else {
@@ -448,6 +485,46 @@ int launch_one(const GemmParams& gp, cudaStream_t s) {
 constexpr int kStages = 4;
 
 }  // namespace
+
+int router_tile_n(int E) {
+  if (E % 64 == 0) return 64;
+  if (E % 32 == 0) return 32;
+  if (E % 16 == 0) return 16;
+  return 0;
+}
+
+int launch_router_logits_tc(const uint16_t* x, const uint16_t* w_split,
+                            float* logits, int T, int H, int E,
+                            DevStatus* status, uint64_t wait_limit_ns,
+                            cudaStream_t s) {
+  const int bn = router_tile_n(E);
+  if (bn == 0) return MOE_ERR_UNSUPPORTED;
+  GemmParams g;
+  std::memset(&g, 0, sizeof(g));
+  const bool ok = make_map(&g.a_shared, x, H, T, BM) &&
+                  make_map(&g.b0_shared, w_split, H,
+                           (uint64_t)kRouterParts * E, bn);
+  if (!ok) return MOE_ERR_CUDA;
+  g.a_routed = g.a_shared;
+  g.b0_routed = g.b1_routed = g.b1_shared = g.b0_shared;
+  g.offsets = nullptr;  // no routed segments: E = 0 below
+  g.out_routed = g.out_shared = reinterpret_cast<uint16_t*>(logits);
+  g.status = status;
+  g.wait_limit_ns = wait_limit_ns;
+  g.E = 0;
+  g.T = T;
+  g.TK = 0;
+  g.n_routed = g.n_shared = E;
+  g.k_routed = g.k_shared = H;
+  switch (bn) {
+    case 64:
+      return launch_one<kRouter, 64, kStages>(g, s);
+    case 32:
+      return launch_one<kRouter, 32, kStages>(g, s);
+    default:
+      return launch_one<kRouter, 16, kStages>(g, s);
+  }
+}
 
 int sm_count() {
   int dev = 0, n = 0;

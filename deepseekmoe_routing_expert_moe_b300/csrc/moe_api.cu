@@ -73,6 +73,7 @@ struct Layout {
   size_t logits = 0, idx = 0, gate = 0, counts = 0, offsets = 0, dest = 0,
          src_row = 0;
   size_t xp = 0, h = 0, hs = 0, yp = 0, ys = 0;
+  size_t w_split = 0;  // [3, E, H] bf16 parts of the router weight
   size_t total = 0;
 };
 
@@ -107,6 +108,8 @@ Layout layout(const moe_dims_t* d, moe_ws_kind_t which) {
     L.h = take(T * K * (size_t)d->I * 2);
     L.hs = take(T * (size_t)d->I_shared * 2);
   }
+  if (which == MOE_WS_ROUTER_LOGITS || which == MOE_WS_FORWARD)
+    L.w_split = take(3 * E * H * 2);
   L.total = o;
   return L;
 }
@@ -200,6 +203,21 @@ moe_status_t ffn_launch(const moe_dims_t* d, const moe_weights_t* w,
   return static_cast<moe_status_t>(moe::launch_expert_ffn(a, s));
 }
 
+// z = x W_r^T: tensor cores (exact bf16 split of W_r) when E % 16 == 0,
+// else the fp32 SIMT kernel
+moe_status_t router_logits_launch(const moe_dims_t* d, const uint16_t* x,
+                                  const float* w_router, float* logits,
+                                  uint16_t* w_split, DevStatus* st,
+                                  cudaStream_t s) {
+  if (moe::router_tile_n(d->E) == 0)
+    return cuda_ok(moe::launch_router_logits(x, w_router, logits, d->T, d->H,
+                                             d->E, s));
+  MOE_TRY(cuda_ok(moe::launch_split_router_weight(w_router, d->E, d->H,
+                                                  w_split, s)));
+  return static_cast<moe_status_t>(moe::launch_router_logits_tc(
+      x, w_split, logits, d->T, d->H, d->E, st, g_wait_limit_ns, s));
+}
+
 }  // namespace
 
 extern "C" {
@@ -233,7 +251,7 @@ void moe_set_wait_timeout_ns(uint64_t ns) {
 size_t moe_workspace_bytes(const moe_dims_t* d, moe_ws_kind_t which) {
   const bool ffn = which == MOE_WS_EXPERT_FFN || which == MOE_WS_FORWARD;
   if (check_dims(d, ffn) != MOE_OK) return 0;
-  if (which < MOE_WS_ROUTE || which > MOE_WS_FORWARD) return 0;
+  if (which < MOE_WS_ROUTE || which > MOE_WS_ROUTER_LOGITS) return 0;
   return layout(d, which).total;
 }
 
@@ -253,8 +271,8 @@ moe_status_t moe_get_device_error(void* ws, moe_stream_t stream) {
 }
 
 moe_status_t moe_router_logits(const moe_dims_t* d, const uint16_t* x,
-                               const float* w_router, float* logits,
-                               moe_stream_t stream) {
+                               const float* w_router, float* logits, void* ws,
+                               size_t ws_bytes, moe_stream_t stream) {
   MOE_TRY(check_dims(d, false));
   MOE_NEED_T(x);
   MOE_NEED(w_router);
@@ -262,9 +280,12 @@ moe_status_t moe_router_logits(const moe_dims_t* d, const uint16_t* x,
   MOE_ALIGN(x);
   MOE_ALIGN(w_router);
   MOE_ALIGN(logits);
+  MOE_TRY(check_ws(d, MOE_WS_ROUTER_LOGITS, ws, ws_bytes));
   if (d->T == 0) return MOE_OK;
-  return cuda_ok(moe::launch_router_logits(x, w_router, logits, d->T, d->H,
-                                           d->E, cs(stream)));
+  const Layout L = layout(d, MOE_WS_ROUTER_LOGITS);
+  return router_logits_launch(d, x, w_router, logits,
+                              at<uint16_t>(ws, L.w_split),
+                              at<DevStatus>(ws, 0), cs(stream));
 }
 
 moe_status_t moe_route(const moe_dims_t* d, const float* logits,
@@ -441,7 +462,8 @@ moe_status_t moe_forward(const moe_dims_t* d, const moe_weights_t* w,
   uint16_t* ys = at<uint16_t>(ws, L.ys);
 
   prof_mark(0, s);
-  MOE_TRY(cuda_ok(moe::launch_router_logits(x, w->w_router, logits, T, H, E, s)));
+  MOE_TRY(router_logits_launch(d, x, w->w_router, logits,
+                               at<uint16_t>(ws, L.w_split), st, s));
   prof_mark(1, s);
   MOE_TRY(cuda_ok(moe::launch_route(logits, bias, T, E, d->n_group,
                                     d->topk_group, K, idx, gate, bc, s)));

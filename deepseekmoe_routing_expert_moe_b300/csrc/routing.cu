@@ -3,6 +3,7 @@
 // and combine as in §2 / §5.1).  These are HBM- or latency-bound SIMT
 // kernels; the expert GEMMs live in grouped_gemm.cu.
 #include <cfloat>
+#include <algorithm>
 #include <climits>
 #include <cstdint>
 
@@ -81,6 +82,35 @@ __global__ void __launch_bounds__(256)
   }
 }
 }  // namespace
+
+// Exact split of the fp32 router weight into three bf16 parts:
+//   hi = bf16(w), mid = bf16(w - hi), lo = bf16(w - hi - mid),
+// each subtraction exact in fp32, so hi + mid + lo == w for every normal w
+// (8 + 8 + 8 significant bits cover fp32's 24).  Layout [3, E, H].
+__global__ void split_router_weight_kernel(const float* __restrict__ w,
+                                           size_t n,
+                                           uint16_t* __restrict__ out) {
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
+       i += (size_t)gridDim.x * blockDim.x) {
+    const float v = w[i];
+    const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+    const float r1 = v - __bfloat162float(hi);
+    const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+    const float r2 = r1 - __bfloat162float(mid);
+    const __nv_bfloat16 lo = __float2bfloat16_rn(r2);
+    out[i] = __bfloat16_as_ushort(hi);
+    out[n + i] = __bfloat16_as_ushort(mid);
+    out[2 * n + i] = __bfloat16_as_ushort(lo);
+  }
+}
+
+cudaError_t launch_split_router_weight(const float* w, int E, int H,
+                                       uint16_t* w_split, cudaStream_t s) {
+  const size_t n = (size_t)E * H;
+  const int blocks = (int)std::min<size_t>((n + 255) / 256, 4 * 148);
+  split_router_weight_kernel<<<blocks, 256, 0, s>>>(w, n, w_split);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_router_logits(const uint16_t* x, const float* w_router,
                                  float* logits, int T, int H, int E,

@@ -16,7 +16,8 @@ import torch
 PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libmoe.so")
 
-MOE_WS_ROUTE, MOE_WS_PERMUTE, MOE_WS_EXPERT_FFN, MOE_WS_FORWARD = 0, 1, 2, 3
+(MOE_WS_ROUTE, MOE_WS_PERMUTE, MOE_WS_EXPERT_FFN, MOE_WS_FORWARD,
+ MOE_WS_ROUTER_LOGITS) = 0, 1, 2, 3, 4
 
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
           3: "MOE_ERR_ALIGNMENT", 4: "MOE_ERR_WORKSPACE", 5: "MOE_ERR_CUDA",
@@ -50,7 +51,7 @@ _S = ctypes.c_size_t
 _I = ctypes.c_int
 _SIGS = {
     "moe_workspace_bytes": (ctypes.c_size_t, [_D, _I]),
-    "moe_router_logits": (_I, [_D, _P, _P, _P, _P]),
+    "moe_router_logits": (_I, [_D, _P, _P, _P, _P, _S, _P]),
     "moe_route": (_I, [_D, _P, _P, _P, _P, _P, _P, _S, _P]),
     "moe_route_static_scratch": (_I, [_D, _P, _P, _P, _P, _P, _P]),
     "moe_permute": (_I, [_D, _P, _P, _P, _P, _P, _P, _P, _S, _P]),
@@ -147,10 +148,10 @@ def workspace(d: MoeDims, which: int, device="cuda") -> torch.Tensor:
 
 
 # ----------------------------------------------------------- entry points
-def moe_router_logits(d, x, w_router, logits, stream=None):
+def moe_router_logits(d, x, w_router, logits, ws, stream=None):
     _check("moe_router_logits", lib().moe_router_logits(
-        ctypes.byref(d), _ptr(x), _ptr(w_router), _ptr(logits),
-        _stream(stream)))
+        ctypes.byref(d), _ptr(x), _ptr(w_router), _ptr(logits), _ptr(ws),
+        ws.numel(), _stream(stream)))
 
 
 def moe_route(d, logits, bias, topk_idx, topk_gate, counts, ws, stream=None):

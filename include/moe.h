@@ -109,7 +109,8 @@ typedef enum {
   MOE_WS_ROUTE = 0,
   MOE_WS_PERMUTE = 1,
   MOE_WS_EXPERT_FFN = 2,
-  MOE_WS_FORWARD = 3
+  MOE_WS_FORWARD = 3,
+  MOE_WS_ROUTER_LOGITS = 4
 } moe_ws_kind_t;
 
 /* Bytes of device workspace `which` needs for dims `d` (0 if d is invalid).
@@ -118,12 +119,16 @@ typedef enum {
  * once after allocating it (moe_get_device_error() re-zeroes the word). */
 size_t moe_workspace_bytes(const moe_dims_t* d, moe_ws_kind_t which);
 
-/* Router logits z = x W_r^T (eq. 15 context), fp32 accumulation of the exact
- * bf16->fp32 activations.  x [T, H] bf16, w_router [E, H] fp32 ->
- * logits [T, E] fp32.  Needs no workspace. */
+/* Router logits z = x W_r^T (the score whose sigmoid is the affinity,
+ * "02 · DeepSeek-V3" §1.3 eq. 15), fp32 accumulation of exact products.
+ * x [T, H] bf16, w_router [E, H] fp32 -> logits [T, E] fp32.  When E % 16
+ * == 0 it runs on the tensor cores: W_r is split exactly into three bf16
+ * parts (hi + mid + lo == W_r) in the workspace and the three products are
+ * accumulated into one fp32 accumulator; otherwise an fp32 SIMT kernel.
+ * Workspace: MOE_WS_ROUTER_LOGITS. */
 moe_status_t moe_router_logits(const moe_dims_t* d, const uint16_t* x,
-                               const float* w_router, float* logits,
-                               moe_stream_t stream);
+                               const float* w_router, float* logits, void* ws,
+                               size_t ws_bytes, moe_stream_t stream);
 
 /* Routing from precomputed logits ("02 · DeepSeek-V3" §1.3, §1.4):
  * sigmoid, + bias for selection, group-limited top-K, gates renormalised
@@ -251,7 +256,8 @@ void moe_set_wait_timeout_ns(uint64_t ns);
  * handles created by the caller, passed as void*) on its stream just before
  * its i-th kernel launch, and events[MOE_FORWARD_KERNELS] after the last,
  * so consecutive events bracket one kernel each.  The launch order is:
- *   0 router logits, 1 route, 2 count scan (+bias step), 3 dispatch order,
+ *   0 router logits (weight split + GEMM), 1 route, 2 count scan (+bias
+ *   step), 3 dispatch order,
  *   4 gather, 5 expert up-projection GEMM (+SwiGLU), 6 expert
  *   down-projection GEMM, 7 combine.
  * NULL / n = 0 disables.  The array must stay valid while enabled.  Global

@@ -48,6 +48,15 @@ def host_weights(cfg):
     return w, W
 
 
+def by_expert(idx, gate):
+    """Chosen experts and their gates ordered by expert id: with logits that
+    differ by fp32 rounding, two chosen experts of nearly equal score may
+    swap slots; the margin criterion protects the chosen set, not the
+    order inside it."""
+    o = np.argsort(idx, axis=1)
+    return np.take_along_axis(idx, o, 1), np.take_along_axis(gate, o, 1)
+
+
 def margins_ok(r, cfg):
     km, gm = O.routing_margins(r, cfg.topk_group, cfg.topk)
     return (km > MARGIN) & (gm > MARGIN)
@@ -65,9 +74,10 @@ def test_layer_tiny_config_all_tokens():
     np.testing.assert_allclose(g["logits"], ref["logits"], rtol=0, atol=2e-5)
     ok = margins_ok(ref["route"], cfg)
     assert ok.sum() >= 0.9 * cfg.T
-    assert np.array_equal(g["idx"][ok], ref["route"]["idx"][ok])
-    np.testing.assert_allclose(g["gate"][ok], ref["route"]["gate"][ok],
-                               rtol=1e-5)
+    gi, gg = by_expert(g["idx"][ok], g["gate"][ok])
+    ri, rg = by_expert(ref["route"]["idx"][ok], ref["route"]["gate"][ok])
+    assert np.array_equal(gi, ri)
+    np.testing.assert_allclose(gg, rg, rtol=1e-5)
     rms_tolerance_check(g["out"], ref["out"], rows=ok)
     # counts and the bias step are consistent with the GPU's own routing
     assert np.array_equal(g["counts"], O.expert_counts(g["idx"], cfg.E))
@@ -90,7 +100,9 @@ def test_layer_ragged_small_batches(T):
                           f(w["ws2"]), n_group=cfg.n_group,
                           topk_group=cfg.topk_group, topk=cfg.topk)
     ok = margins_ok(ref["route"], cfg)
-    assert np.array_equal(g["idx"][ok], ref["route"]["idx"][ok])
+    assert np.array_equal(by_expert(g["idx"][ok], g["gate"][ok])[0],
+                          by_expert(ref["route"]["idx"][ok],
+                                    ref["route"]["gate"][ok])[0])
     rms_tolerance_check(g["out"], ref["out"], rows=ok)
 
 
@@ -119,8 +131,10 @@ def _sampled_v3_check(cfg, v3_weights, n_sample, step=0):
     r = O.route(z, b, cfg.n_group, cfg.topk_group, cfg.topk)
     ok = margins_ok(r, cfg)
     assert ok.mean() > 0.9
-    agree = np.all(g["idx"] == r["idx"], axis=1)
-    assert np.all(agree[ok])
+    gi, gg = by_expert(g["idx"], g["gate"])
+    ri, rg = by_expert(r["idx"], r["gate"])
+    assert np.all(np.all(gi == ri, axis=1)[ok])
+    np.testing.assert_allclose(gg[ok], rg[ok], rtol=1e-4)
     assert np.array_equal(g["counts"], O.expert_counts(g["idx"], cfg.E))
     rows = np.nonzero(ok)[0]
     rows = rows[np.linspace(0, len(rows) - 1, n_sample).astype(int)]

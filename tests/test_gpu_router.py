@@ -1,0 +1,62 @@
+"""Router logits z = x W_r^T on the GPU against the oracle's fp64 sum.
+
+Every product x_h * w_h is exact (bf16 x the exact bf16 split of the fp32
+weight on the tensor-core path; fp32 FMA on the SIMT path), so the only
+error is fp32 accumulation: for any summation order
+    |z_gpu - z| <= H * 2^-24 * sum_h |x_h w_h| + 2^-24 |z|.
+The test asserts that bound elementwise, and a typical error far below it."""
+import numpy as np
+import pytest
+import torch
+
+from deepseekmoe_routing_expert_moe_b300 import inputs, ops
+from oracle import moe_oracle as O
+
+from gpu_helpers import dev, host
+
+pytestmark = pytest.mark.gpu
+
+
+def check_logits(cfg, T=None):
+    T = cfg.T if T is None else T
+    d = ops.dims_of(cfg, T=T)
+    x = inputs.x_tokens(cfg, T=T)
+    w = inputs.router_weight(cfg)
+    z = torch.full((T, cfg.E), np.nan, dtype=torch.float32, device="cuda")
+    ws = ops.workspace(d, ops.MOE_WS_ROUTER_LOGITS)
+    ops.moe_router_logits(d, dev(x), dev(w), z, ws)
+    assert ops.moe_get_device_error(ws) == 0
+    zg = host(z).astype(np.float64)
+    xf = inputs.bf16_bits_to_f32(x).astype(np.float64)
+    ref = xf @ w.astype(np.float64).T                 # exact-ish fp64
+    mag = np.abs(xf) @ np.abs(w.astype(np.float64)).T
+    bound = cfg.H * 2.0 ** -24 * mag + 2.0 ** -24 * np.abs(ref)
+    err = np.abs(zg - ref)
+    assert np.all(err <= bound), (err / bound).max()
+    assert np.sqrt(np.mean(err ** 2)) < 1e-2 * np.sqrt(np.mean(bound ** 2))
+    # and the oracle's own rounding of the same sum
+    np.testing.assert_allclose(zg, O.router_logits(xf, w), rtol=0,
+                               atol=float(bound.max()))
+
+
+def test_router_logits_v3_prefill_4096_tokens():
+    check_logits(inputs.CONFIGS["prefill_v3"])
+
+
+@pytest.mark.parametrize("T", [1, 100, 129])
+def test_router_logits_v3_ragged(T):
+    check_logits(inputs.CONFIGS["prefill_v3"], T=T)
+
+
+@pytest.mark.parametrize("E,G", [(16, 4), (32, 4), (64, 8), (128, 8),
+                                 (512, 16), (8, 4), (24, 3)])
+def test_router_logits_expert_counts(E, G):
+    # E % 16 == 0 -> tensor cores with 16/32/64-wide tiles; 8, 24 -> SIMT
+    cfg = inputs.custom_config("rl", 700 + E, T=300, H=512, E=E, n_group=G,
+                               topk_group=2, topk=2, I=64, I_shared=64,
+                               router_sigma=0.05)
+    check_logits(cfg)
+
+
+def test_router_logits_tiny_config():
+    check_logits(inputs.CONFIGS["tiny"])
