@@ -2,36 +2,42 @@
 //
 // Every routed expert of the DeepSeek-V3 MoE layer is a SwiGLU FFN with
 // three matrices ("02 · DeepSeek-V3" (PaperTrace) §1.1); the shared expert
-// has the same form and runs on every token (§1.1, §5.1 treats it as a
+// has the same form and runs on every token (§1.1; §5.1 treats it as a
 // ninth, always-chosen expert).  Rows of the dispatched activations are
-// grouped by expert (segments [offsets[e], offsets[e+1])), plus one extra
-// segment for the shared expert over all T tokens:
+// grouped by expert (segments [offsets[e], offsets[e+1])), plus one segment
+// for the shared expert over all T tokens:
 //
 //   up   (MODE kUp):   h = silu(A W1^T) * (A W3^T)   A = xp rows | x rows
 //   down (MODE kDown): y = h W2^T
 //
-// The same kernel also computes the router logits (MODE kRouter, one
-// segment of T token rows): the fp32 router weight is split exactly into
-// three bf16 parts, W = W_hi + W_mid + W_lo, and z = x W_hi^T + x W_mid^T +
-// x W_lo^T accumulates all three into one fp32 accumulator -- each bf16 x
-// bf16 product is exact, so this is an fp32-accumulated x W^T.
+// Weights are the MMA's M side and tokens its N side ("swap AB"): a unit
+// computes D[f, t] = W[f, :] . A[t, :] for 2 x 128 weight rows f and one
+// chunk of N <= 256 token rows t of one segment.  N is the chunk's row
+// count rounded up to 16 and is set per unit in the instruction descriptor,
+// so a segment of 140 rows costs 144 columns of MMA work, not two 128-row
+// tiles; segments longer than 256 rows are cut into equal chunks.  The two
+// weight tiles of a unit feed two accumulators:
+//   up:   W1 rows [f0, f0+128) and W3 rows [f0, f0+128) -- gate and up value
+//         of feature f land in the same TMEM lane, so SwiGLU needs no
+//         exchange between threads
+//   down: W2 rows [f0, f0+128) and [f0+128, f0+256)
 //
 // Design (one persistent CTA per SM, 6 warps):
-//   warp 0 lane 0   TMA producer: A tile 128x64 and B tile BNx64 per stage,
-//                   128-byte swizzle, STAGES-deep mbarrier ring
-//   warp 1 lane 0   tcgen05.mma issuer (M=128, N=BN, K=16 per instruction),
-//                   fp32 accumulators in tensor memory, double buffered;
-//                   warp 1 also owns the TMEM allocation
-//   warps 2..5      epilogue: tcgen05.ld of the accumulator rows, SwiGLU
-//                   (up) or plain conversion (down), bf16 stores of the
-//                   rows that belong to the segment
-// The work list -- (segment, n-block, m-tile) units, m fastest so that the
-// CTAs sharing a weight tile run side by side and hit L2 -- is derived on
-// the device from `offsets`; nothing is read back to the host.
-//
-// Up-projection B tile: rows [0, BN/2) come from W1 and rows [BN/2, BN)
-// from W3 for the same BN/2 features, so accumulator column c (gate) pairs
-// with column BN/2 + c (up) in the same thread: SwiGLU needs no exchange.
+//   warp 0 lane 0   TMA producer: per stage the two 128x64 weight tiles and
+//                   the Nx64 token tile (boxes of 128/64/32/16 rows summing
+//                   to N), 128-byte swizzle, STAGES-deep mbarrier ring
+//   warp 1 lane 0   tcgen05.mma issuer (M=128, N per unit, K=16), fp32
+//                   accumulators in tensor memory; warp 1 owns the TMEM
+//                   allocation (512 columns = two slots of 256)
+//   warps 2..5      epilogue: tcgen05.ld, SwiGLU (up) or conversion (down),
+//                   bf16 stores of the valid rows and features
+// TMEM: a unit with N <= 128 puts both accumulators in one 256-column slot,
+// so consecutive such units alternate slots and the epilogue of one overlaps
+// the MMAs of the next; a unit with N > 128 takes both slots.
+// The unit list -- the shared segment first (its units are the longest),
+// then the routed experts, each as (feature block, chunk) with the chunk
+// fastest so CTAs sharing a weight tile run side by side and hit L2 -- is
+// derived on the device from `offsets`; nothing is read back to the host.
 //
 // Every wait is bounded (MOE_ERR_TIMEOUT in the status word, then a clean
 // exit: in-flight copies and MMAs are drained, TMEM is freed).
@@ -46,15 +52,20 @@
 namespace moe {
 namespace {
 
-constexpr int BM = 128;            // tile rows (tokens) = MMA M
-constexpr int BK = 64;             // K per stage: 64 bf16 = one 128 B row
-constexpr int UMMA_K = 16;         // K of one kind::f16 MMA
-constexpr int kThreads = 192;      // 6 warps
+constexpr int BM = 128;         // weight rows per accumulator = MMA M
+constexpr int BK = 64;          // K per stage: 64 bf16 = one 128 B row
+constexpr int UMMA_K = 16;      // K of one kind::f16 MMA
+constexpr int NT = 256;         // largest token chunk = largest MMA N
+constexpr int kThreads = 192;   // 6 warps
+constexpr int kStages = 3;
+constexpr int kTokBoxes = 4;    // token boxes of 16, 32, 64, 128 rows
+constexpr uint32_t W_BYTES = BM * BK * 2;       // one weight tile
+constexpr uint32_t TOK_BYTES = NT * BK * 2;     // token tile (max)
+constexpr uint32_t STAGE_BYTES = 2 * W_BYTES + TOK_BYTES;
+constexpr uint32_t TMEM_COLS = 512;             // two slots of 256 columns
 constexpr uint64_t kDrainNs = 2000000000ull;
 
-
-enum { kUp = 0, kDown = 1, kRouter = 2 };
-constexpr int kRouterParts = 3;  // W = hi + mid + lo, each bf16
+enum { kUp = 0, kDown = 1 };
 enum {
   kSiteProducer = 21,
   kSiteMmaAcc = 22,
@@ -65,35 +76,44 @@ enum {
 };
 
 struct GemmParams {  // CUtensorMap members carry their 64-byte alignment
-  CUtensorMap a_routed;   // up: xp [TK, H]      down: h  [TK, I]
-  CUtensorMap a_shared;   // up: x  [T, H]       down: hs [T, I_s]
-  CUtensorMap b0_routed;  // up: w1 [E*I, H]     down: w2 [E*H, I]
-  CUtensorMap b1_routed;  // up: w3 [E*I, H]     down: unused
-  CUtensorMap b0_shared;  // up: ws1 [I_s, H]    down: ws2 [H, I_s]
-  CUtensorMap b1_shared;  // up: ws3 [I_s, H]    down: unused
+  CUtensorMap tok_routed[kTokBoxes];  // up: xp [TK, H]   down: h  [TK, I]
+  CUtensorMap tok_shared[kTokBoxes];  // up: x  [T, H]    down: hs [T, I_s]
+  CUtensorMap wa_routed;  // up: w1 [E*I, H]     down: w2 [E*H, I]
+  CUtensorMap wb_routed;  // up: w3 [E*I, H]     down: w2 (rows + 128)
+  CUtensorMap wa_shared;  // up: ws1 [I_s, H]    down: ws2 [H, I_s]
+  CUtensorMap wb_shared;  // up: ws3 [I_s, H]    down: ws2 (rows + 128)
   const int32_t* offsets; // [E+1]
   uint16_t* out_routed;   // up: h [TK, I]       down: yp [TK, H]
   uint16_t* out_shared;   // up: hs [T, I_s]     down: ys [T, H]
   DevStatus* status;
   unsigned long long wait_limit_ns;
   int E, T, TK;
-  int n_routed, n_shared;  // output columns of a routed / the shared segment
+  int n_routed, n_shared;  // output features of a routed / the shared segment
   int k_routed, k_shared;  // reduction length of a routed / the shared one
 };
 
-template <int MODE, int BN>
-struct Shape {
-  static constexpr int OUT_COLS = (MODE == kUp) ? BN / 2 : BN;
-  static constexpr int B_PARTS = (MODE == kRouter) ? kRouterParts : 1;
-  static constexpr uint32_t A_BYTES = BM * BK * 2;
-  static constexpr uint32_t B_BYTES = B_PARTS * BN * BK * 2;
-  static constexpr uint32_t TMEM_COLS = 2 * BN;  // two accumulators
-  static constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
+// output features one unit produces
+template <int MODE>
+struct Feat {
+  static constexpr int FB = (MODE == kUp) ? BM : 2 * BM;
 };
 
-__device__ __forceinline__ void decode_unit(int u, const int* useg,
-                                            const int* srows, int NS,
-                                            int& s, int& m, int& n) {
+// One unit of work, decoded identically by every role.
+struct Unit {
+  int seg;    // 0 = shared expert, 1 + e = routed expert e
+  int f;      // feature block
+  int row0;   // first row of the chunk in the token / output tensors
+  int rows;   // valid rows in the chunk (1..NT)
+  int n;      // MMA N: rows rounded up to 16
+};
+
+__device__ __forceinline__ int round16(int v) { return (v + 15) & ~15; }
+
+// Segment tables in shared memory: srow0/srows per segment, useg the
+// exclusive prefix of units per segment (useg[NS] = total).
+__device__ __forceinline__ Unit decode_unit(int u, const int* useg,
+                                            const int* srow0,
+                                            const int* srows, int NS) {
   int lo = 0, hi = NS - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -102,36 +122,42 @@ __device__ __forceinline__ void decode_unit(int u, const int* useg,
     else
       hi = mid - 1;
   }
-  s = lo;
-  const int mt = (srows[s] + BM - 1) / BM;
-  const int local = u - useg[s];
-  n = local / mt;
-  m = local - n * mt;
+  Unit x;
+  x.seg = lo;
+  const int R = srows[lo];
+  const int nch = (R + NT - 1) / NT;
+  const int cs = round16((R + nch - 1) / nch);
+  const int local = u - useg[lo];
+  x.f = local / nch;
+  const int c = local - x.f * nch;
+  x.row0 = srow0[lo] + c * cs;
+  x.rows = min(cs, R - c * cs);
+  x.n = round16(x.rows);
+  return x;
 }
 
 __device__ __forceinline__ float silu_f(float g) {
   return g * __frcp_rn(1.0f + __expf(-g));
 }
 
-template <int MODE, int BN, int STAGES>
+template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
-    grouped_gemm_kernel(const __grid_constant__ GemmParams p) {
-  using S = Shape<MODE, BN>;
+    expert_gemm_kernel(const __grid_constant__ GemmParams p) {
+  constexpr int FB = Feat<MODE>::FB;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sA = smem;
-  uint8_t* sB = smem + STAGES * S::A_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + STAGES * S::B_BYTES);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * STAGE_BYTES);
   uint64_t* full = bars;
-  uint64_t* empty = bars + STAGES;
-  uint64_t* tfull = bars + 2 * STAGES;
-  uint64_t* tempty = bars + 2 * STAGES + 2;
-  uint64_t* drain = bars + 2 * STAGES + 4;
-  volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(bars + 2 * STAGES + 5);
+  uint64_t* empty = bars + kStages;
+  uint64_t* tfull = bars + 2 * kStages;       // per TMEM slot
+  uint64_t* tempty = bars + 2 * kStages + 2;  // per TMEM slot
+  uint64_t* drain = bars + 2 * kStages + 4;
+  volatile uint32_t* misc =
+      reinterpret_cast<volatile uint32_t*>(bars + 2 * kStages + 5);
   // misc[0] TMEM base, misc[1] abort flag, misc[2] bad-offsets flag
   const int E = p.E;
-  const int NS = E + 1;  // routed segments + the shared one (index E)
+  const int NS = E + 1;  // the shared segment (0) + the routed ones
   int* useg = reinterpret_cast<int*>(const_cast<uint32_t*>(misc) + 4);
   int* srows = useg + NS + 1;
   int* srow0 = srows + NS;
@@ -140,7 +166,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < STAGES; ++i) {
+    for (int i = 0; i < kStages; ++i) {
       mbar_init(smem_u32(&full[i]), 1);
       mbar_init(smem_u32(&empty[i]), 1);
     }
@@ -154,28 +180,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
-    prefetch_tmap(&p.a_routed);
-    prefetch_tmap(&p.a_shared);
-    prefetch_tmap(&p.b0_routed);
-    prefetch_tmap(&p.b0_shared);
-    if (MODE == kUp) {
-      prefetch_tmap(&p.b1_routed);
-      prefetch_tmap(&p.b1_shared);
+#pragma unroll
+    for (int b = 0; b < kTokBoxes; ++b) {
+      prefetch_tmap(&p.tok_routed[b]);
+      prefetch_tmap(&p.tok_shared[b]);
     }
+    prefetch_tmap(&p.wa_routed);
+    prefetch_tmap(&p.wb_routed);
+    prefetch_tmap(&p.wa_shared);
+    prefetch_tmap(&p.wb_shared);
   }
   if (warp == 2) {
     // segment table: rows, first row, and the exclusive prefix of units
-    const int nb_r = p.n_routed / S::OUT_COLS;
-    const int nb_s = p.n_shared / S::OUT_COLS;
+    const int nfb_r = (p.n_routed + FB - 1) / FB;
+    const int nfb_s = (p.n_shared + FB - 1) / FB;
     const int per = (NS + 31) / 32;
     const int lo = min(NS, lane * per), hi = min(NS, lo + per);
     int mine = 0;
     bool bad = false;
     for (int s = lo; s < hi; ++s) {
       int r0 = 0, rows = p.T;
-      if (s < E) {
-        r0 = p.offsets[s];
-        const int r1 = p.offsets[s + 1];
+      if (s > 0) {
+        r0 = p.offsets[s - 1];
+        const int r1 = p.offsets[s];
         if (r0 < 0 || r1 < r0 || r1 > p.TK) {
           bad = true;
           r0 = 0;
@@ -186,7 +213,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       srows[s] = rows;
       srow0[s] = r0;
-      mine += ((rows + BM - 1) / BM) * (s < E ? nb_r : nb_s);
+      mine += ((rows + NT - 1) / NT) * (s > 0 ? nfb_r : nfb_s);
     }
     int incl = mine;
 #pragma unroll
@@ -197,13 +224,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     int run = incl - mine;
     for (int s = lo; s < hi; ++s) {
       useg[s] = run;
-      run += ((srows[s] + BM - 1) / BM) * (s < E ? nb_r : nb_s);
+      run += ((srows[s] + NT - 1) / NT) * (s > 0 ? nfb_r : nfb_s);
     }
     if (lane == 31) useg[NS] = incl;
     if (__any_sync(0xffffffffu, bad) && lane == 0) misc[2] = 1;
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(const_cast<uint32_t*>(&misc[0])), S::TMEM_COLS);
+    tmem_alloc(smem_u32(const_cast<uint32_t*>(&misc[0])), TMEM_COLS);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -223,17 +250,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ------------------------------------------------------ producer
       uint32_t stage = 0, phase = 0, issued = 0;
       const uint64_t pol_w = policy_evict_first();
-      const uint64_t pol_a = policy_evict_last();
+      const uint64_t pol_t = policy_evict_last();
       for (int u = blockIdx.x; u < total; u += gridDim.x) {
-        int s, m, n;
-        decode_unit(u, useg, srows, NS, s, m, n);
-        const bool sh = (s == E);
-        const CUtensorMap* ta = sh ? &p.a_shared : &p.a_routed;
-        const CUtensorMap* tb0 = sh ? &p.b0_shared : &p.b0_routed;
-        const CUtensorMap* tb1 = sh ? &p.b1_shared : &p.b1_routed;
-        const int arow = srow0[s] + m * BM;
-        const int brow = (sh ? 0 : s * p.n_routed) + n * S::OUT_COLS;
+        const Unit w = decode_unit(u, useg, srow0, srows, NS);
+        const bool sh = (w.seg == 0);
+        const CUtensorMap* tok = sh ? p.tok_shared : p.tok_routed;
+        const CUtensorMap* wa = sh ? &p.wa_shared : &p.wa_routed;
+        const CUtensorMap* wb = sh ? &p.wb_shared : &p.wb_routed;
+        const int wrow = (sh ? 0 : (w.seg - 1) * p.n_routed) + w.f * FB;
+        const int wrow_b = (MODE == kUp) ? wrow : wrow + BM;
         const int nkb = (sh ? p.k_shared : p.k_routed) / BK;
+        const uint32_t tx = 2 * W_BYTES + (uint32_t)w.n * BK * 2;
         bool ok = true;
         for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1,
@@ -243,38 +270,41 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           const uint32_t fb = smem_u32(&full[stage]);
-          mbar_arrive_expect_tx(fb, S::A_BYTES + S::B_BYTES);
-          tma_load_2d_hint(smem_u32(sA + stage * S::A_BYTES), ta, kb * BK,
-                           arow, fb, pol_a);
-          if (MODE == kUp) {
-            tma_load_2d_hint(smem_u32(sB + stage * S::B_BYTES), tb0, kb * BK,
-                             brow, fb, pol_w);
-            tma_load_2d_hint(
-                smem_u32(sB + stage * S::B_BYTES + (BN / 2) * BK * 2), tb1,
-                kb * BK, brow, fb, pol_w);
-          } else if (MODE == kRouter) {
-            // the three bf16 parts of the router weight, one below the other
-#pragma unroll
-            for (int part = 0; part < kRouterParts; ++part)
-              tma_load_2d_hint(
-                  smem_u32(sB + stage * S::B_BYTES + part * BN * BK * 2), tb0,
-                  kb * BK, part * p.n_shared + brow, fb, pol_a);
+          uint8_t* st = smem + stage * STAGE_BYTES;
+          mbar_arrive_expect_tx(fb, tx);
+          tma_load_2d_hint(smem_u32(st), wa, kb * BK, wrow, fb, pol_w);
+          tma_load_2d_hint(smem_u32(st + W_BYTES), wb, kb * BK, wrow_b, fb,
+                           pol_w);
+          // token rows [row0, row0 + n) as boxes of 128/64/32/16 rows
+          uint8_t* stok = st + 2 * W_BYTES;
+          if (w.n == NT) {
+            tma_load_2d_hint(smem_u32(stok), &tok[3], kb * BK, w.row0, fb,
+                             pol_t);
+            tma_load_2d_hint(smem_u32(stok + 128 * BK * 2), &tok[3], kb * BK,
+                             w.row0 + 128, fb, pol_t);
           } else {
-            tma_load_2d_hint(smem_u32(sB + stage * S::B_BYTES), tb0, kb * BK,
-                             brow, fb, pol_w);
+            int off = 0;
+#pragma unroll
+            for (int b = kTokBoxes - 1; b >= 0; --b) {
+              if ((w.n >> 4) & (1 << b)) {
+                tma_load_2d_hint(smem_u32(stok + off * BK * 2), &tok[b],
+                                 kb * BK, w.row0 + off, fb, pol_t);
+                off += 16 << b;
+              }
+            }
           }
           ++issued;
-          if (++stage == STAGES) {
+          if (++stage == kStages) {
             stage = 0;
             phase ^= 1;
           }
         }
         if (!ok) break;
       }
-      // drain: the last min(issued, STAGES) loads must land before exit
-      const uint32_t first = issued > STAGES ? issued - STAGES : 0;
+      // drain: the last min(issued, kStages) loads must land before exit
+      const uint32_t first = issued > kStages ? issued - kStages : 0;
       for (uint32_t i = first; i < issued; ++i)
-        mbar_wait_bounded(smem_u32(&full[i % STAGES]), (i / STAGES) & 1,
+        mbar_wait_bounded(smem_u32(&full[i % kStages]), (i / kStages) & 1,
                           nullptr, kDrainNs, p.status, kSiteDrain);
     }
     __syncwarp();
@@ -282,19 +312,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       // ----------------------------------------------------------- MMA
       uint32_t stage = 0, phase = 0;
+      uint32_t tph = 0;  // bit s: parity of the uses of TMEM slot s so far
+      int slot = 0;
       bool any = false;
-      int local = 0;
-      for (int u = blockIdx.x; u < total; u += gridDim.x, ++local) {
-        int s, m, n;
-        decode_unit(u, useg, srows, NS, s, m, n);
-        const int nkb = ((s == E) ? p.k_shared : p.k_routed) / BK;
-        const int buf = local & 1;
-        const uint32_t ap = (local >> 1) & 1;
-        if (!mbar_wait_bounded(smem_u32(&tempty[buf]), ap ^ 1, abort_flag,
-                               limit, p.status, kSiteMmaAcc))
+      for (int u = blockIdx.x; u < total; u += gridDim.x) {
+        const Unit w = decode_unit(u, useg, srow0, srows, NS);
+        const int nkb = ((w.seg == 0) ? p.k_shared : p.k_routed) / BK;
+        const bool wide = w.n > NT / 2;
+        const int s1 = wide ? (slot ^ 1) : slot;
+        if (!mbar_wait_bounded(smem_u32(&tempty[slot]),
+                               ((tph >> slot) & 1) ^ 1, abort_flag, limit,
+                               p.status, kSiteMmaAcc))
+          break;
+        if (wide && !mbar_wait_bounded(smem_u32(&tempty[s1]),
+                                       ((tph >> s1) & 1) ^ 1, abort_flag,
+                                       limit, p.status, kSiteMmaAcc))
           break;
         tc_fence_after();
-        const uint32_t d = tmem_base + buf * BN;
+        const uint32_t da = tmem_base + slot * (NT);
+        const uint32_t db = wide ? tmem_base + s1 * NT : da + NT / 2;
+        const uint32_t idesc = idesc_bf16_f32(BM, w.n);
         bool ok = true;
         for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait_bounded(smem_u32(&full[stage]), phase, abort_flag,
@@ -303,27 +340,33 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t a0 = smem_u32(sA + stage * S::A_BYTES);
-          const uint32_t b0 = smem_u32(sB + stage * S::B_BYTES);
+          const uint32_t s0 = smem_u32(smem + stage * STAGE_BYTES);
+          const uint32_t st = s0 + 2 * W_BYTES;
 #pragma unroll
-          for (int part = 0; part < S::B_PARTS; ++part) {
-#pragma unroll
-            for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-              tc_mma_f16(d, sw128_kmajor_desc(a0 + kk * UMMA_K * 2),
-                         sw128_kmajor_desc(b0 + part * BN * BK * 2 +
-                                           kk * UMMA_K * 2),
-                         S::IDESC, (kb | part | kk) != 0);
-            }
+          for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+            const uint64_t bdesc = sw128_kmajor_desc(st + kk * UMMA_K * 2);
+            const uint32_t acc = (kb | kk) != 0;
+            tc_mma_f16(da, sw128_kmajor_desc(s0 + kk * UMMA_K * 2), bdesc,
+                       idesc, acc);
+            tc_mma_f16(db, sw128_kmajor_desc(s0 + W_BYTES + kk * UMMA_K * 2),
+                       bdesc, idesc, acc);
           }
           any = true;
           tc_commit(smem_u32(&empty[stage]));
-          if (++stage == STAGES) {
+          if (++stage == kStages) {
             stage = 0;
             phase ^= 1;
           }
         }
         if (!ok) break;
-        tc_commit(smem_u32(&tfull[buf]));
+        tc_commit(smem_u32(&tfull[slot]));
+        tph ^= 1u << slot;
+        if (wide) {
+          tc_commit(smem_u32(&tfull[s1]));
+          tph ^= 1u << s1;
+        } else {
+          slot ^= 1;
+        }
       }
       if (any) {  // every issued MMA completes before TMEM is released
         tc_commit(smem_u32(drain));
@@ -336,217 +379,125 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------- epilogue
     const int q = warp & 3;  // TMEM lane quadrant this warp may access
     const int r = q * 32 + lane;
-    int local = 0;
-    for (int u = blockIdx.x; u < total; u += gridDim.x, ++local) {
-      int s, m, n;
-      decode_unit(u, useg, srows, NS, s, m, n);
-      const int buf = local & 1;
-      const uint32_t ap = (local >> 1) & 1;
+    uint32_t tph = 0;  // bit s: parity of the uses of TMEM slot s so far
+    int slot = 0;
+    for (int u = blockIdx.x; u < total; u += gridDim.x) {
+      const Unit w = decode_unit(u, useg, srow0, srows, NS);
+      const bool wide = w.n > NT / 2;
+      const int s1 = wide ? (slot ^ 1) : slot;
       int ok = 0;
-      if (lane == 0)
-        ok = mbar_wait_bounded(smem_u32(&tfull[buf]), ap, abort_flag, limit,
-                               p.status, kSiteEpilogue);
+      if (lane == 0) {
+        ok = mbar_wait_bounded(smem_u32(&tfull[slot]), (tph >> slot) & 1,
+                               abort_flag, limit, p.status, kSiteEpilogue);
+        if (ok && wide)
+          ok = mbar_wait_bounded(smem_u32(&tfull[s1]), (tph >> s1) & 1,
+                                 abort_flag, limit, p.status, kSiteEpilogue);
+      }
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       tc_fence_after();
-      const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                          static_cast<uint32_t>(buf * BN);
-      const bool sh = (s == E);
-      const int row_in_seg = m * BM + r;
-      const bool valid = row_in_seg < srows[s];
+      const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+      const uint32_t ta = tmem_base + lane_off + slot * NT;
+      const uint32_t tb =
+          wide ? tmem_base + lane_off + s1 * NT : ta + NT / 2;
+      const bool sh = (w.seg == 0);
       uint16_t* out = sh ? p.out_shared : p.out_routed;
       const int ld = sh ? p.n_shared : p.n_routed;
-      uint16_t* orow = out + (size_t)(srow0[s] + (valid ? row_in_seg : 0)) * ld +
-                       (size_t)n * S::OUT_COLS;
-      if (MODE == kUp) {
+      // feature columns of this thread's TMEM lane in both accumulators
+      const int fa = w.f * FB + r;
+      const int fbc = (MODE == kUp) ? fa : fa + BM;
+      const bool va = fa < ld, vb = fbc < ld;
+      uint16_t* obase = out + (size_t)w.row0 * ld;
 #pragma unroll 1
-        for (int c = 0; c < S::OUT_COLS; c += 16) {
-          uint32_t g[16], v[16];
-          tmem_ld16(tb + c, g);
-          tmem_ld16(tb + S::OUT_COLS + c, v);
-          tmem_ld_wait();
-          uint32_t pk[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const float h0 = silu_f(__uint_as_float(g[2 * i])) *
-                             __uint_as_float(v[2 * i]);
-            const float h1 = silu_f(__uint_as_float(g[2 * i + 1])) *
-                             __uint_as_float(v[2 * i + 1]);
-            pk[i] = pack_bf16x2(h0, h1);
-          }
-          if (valid) {
-            uint4* dst = reinterpret_cast<uint4*>(orow + c);
-            dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-            dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-          }
+      for (int j0 = 0; j0 < w.n; j0 += 16) {
+        uint32_t a[16], b[16];
+        tmem_ld16(ta + j0, a);
+        tmem_ld16(tb + j0, b);
+        tmem_ld_wait();
+        if (j0 + 16 >= w.n) {  // last columns read: hand TMEM back
+          tc_fence_before();
+          mbar_arrive(smem_u32(&tempty[slot]));
+          if (wide) mbar_arrive(smem_u32(&tempty[s1]));
         }
-      } else if (MODE == kRouter) {
-        float* frow = reinterpret_cast<float*>(out) +
-                      (size_t)(valid ? row_in_seg : 0) * ld +
-                      (size_t)n * S::OUT_COLS;
-#pragma unroll 1
-        for (int c = 0; c < BN; c += 16) {
-          uint32_t v[16];
-          tmem_ld16(tb + c, v);
-          tmem_ld_wait();
-          if (valid) {
-            uint4* dst = reinterpret_cast<uint4*>(frow + c);
+        const int nv = min(16, w.rows - j0);
+        if (MODE == kUp) {
+          if (va) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-              dst[i] = make_uint4(v[4 * i], v[4 * i + 1], v[4 * i + 2],
-                                  v[4 * i + 3]);
+            for (int i = 0; i < 16; ++i) {
+              if (i < nv) {
+                const float h = silu_f(__uint_as_float(a[i])) *
+                                __uint_as_float(b[i]);
+                obase[(size_t)(j0 + i) * ld + fa] =
+                    __bfloat16_as_ushort(__float2bfloat16_rn(h));
+              }
+            }
           }
-        }
-      } else {
-#pragma unroll 1
-        for (int c = 0; c < BN; c += 16) {
-          uint32_t v[16];
-          tmem_ld16(tb + c, v);
-          tmem_ld_wait();
-          uint32_t pk[8];
+        } else {
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            pk[i] = pack_bf16x2(__uint_as_float(v[2 * i]),
-                                __uint_as_float(v[2 * i + 1]));
-          if (valid) {
-            uint4* dst = reinterpret_cast<uint4*>(orow + c);
-            dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-            dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+          for (int i = 0; i < 16; ++i) {
+            if (i < nv) {
+              uint16_t* o = obase + (size_t)(j0 + i) * ld;
+              if (va)
+                o[fa] = __bfloat16_as_ushort(
+                    __float2bfloat16_rn(__uint_as_float(a[i])));
+              if (vb)
+                o[fbc] = __bfloat16_as_ushort(
+                    __float2bfloat16_rn(__uint_as_float(b[i])));
+            }
           }
         }
       }
-      tc_fence_before();
-      mbar_arrive(smem_u32(&tempty[buf]));
+      tph ^= 1u << slot;
+      if (wide)
+        tph ^= 1u << s1;
+      else
+        slot ^= 1;
     }
   }
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, S::TMEM_COLS);
+    tmem_dealloc(tmem_base, TMEM_COLS);
   }
 }
 
-// ---------------------------------------------------------------- host
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType,
-                                  cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*,
-                                  const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion,
-                                  CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = [] {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000,
-                                         cudaEnableDefault, &q) !=
-            cudaSuccess ||
-        q != cudaDriverEntryPointSuccess)
-      return static_cast<EncodeTiledFn>(nullptr);
-    return reinterpret_cast<EncodeTiledFn>(f);
-  }();
-  return fn;
-}
-
-// 2-D bf16 row-major [outer, inner] tensor, box [box_outer, 64], 128 B swizzle
-bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
-              uint32_t box_outer) {
-  EncodeTiledFn enc = encode_fn();
-  if (enc == nullptr) return false;
-  const cuuint64_t dims[2] = {inner, outer};
-  const cuuint64_t strides[1] = {inner * 2};
-  const cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), box_outer};
-  const cuuint32_t estr[2] = {1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base),
-             dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-template <int MODE, int BN, int STAGES>
 size_t smem_bytes(int E) {
-  using S = Shape<MODE, BN>;
-  return 1024 + STAGES * (S::A_BYTES + S::B_BYTES) +
-         (2 * STAGES + 5) * sizeof(uint64_t) + 4 * sizeof(uint32_t) +
-         sizeof(int) * (3 * (E + 1) + 1);
+  return 1024 + kStages * STAGE_BYTES + (2 * kStages + 5) * sizeof(uint64_t) +
+         4 * sizeof(uint32_t) + sizeof(int) * (3 * (E + 1) + 1);
 }
 
-template <int MODE, int BN, int STAGES>
+template <int MODE>
 int launch_one(const GemmParams& gp, cudaStream_t s) {
-  auto kern = grouped_gemm_kernel<MODE, BN, STAGES>;
-  const size_t smem = smem_bytes<MODE, BN, STAGES>(gp.E);
+  auto kern = expert_gemm_kernel<MODE>;
+  const size_t smem = smem_bytes(gp.E);
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem)) != cudaSuccess)
     return MOE_ERR_CUDA;
-  kern<<<sm_count(), kThreads, smem, s>>>(gp);
+  kern<<<gemm_ctas(), kThreads, smem, s>>>(gp);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
-constexpr int kStages = 4;
+// token-operand maps of one [rows, k] bf16 tensor, boxes of 16..128 rows
+bool token_maps(CUtensorMap (&m)[kTokBoxes], const void* base, uint64_t k,
+                uint64_t rows) {
+  for (int b = 0; b < kTokBoxes; ++b)
+    if (!make_tmap_bf16(&m[b], base, k, rows, 16u << b)) return false;
+  return true;
+}
 
 }  // namespace
-
-int router_tile_n(int E) {
-  if (E % 64 == 0) return 64;
-  if (E % 32 == 0) return 32;
-  if (E % 16 == 0) return 16;
-  return 0;
-}
-
-int launch_router_logits_tc(const uint16_t* x, const uint16_t* w_split,
-                            float* logits, int T, int H, int E,
-                            DevStatus* status, uint64_t wait_limit_ns,
-                            cudaStream_t s) {
-  const int bn = router_tile_n(E);
-  if (bn == 0) return MOE_ERR_UNSUPPORTED;
-  GemmParams g;
-  std::memset(&g, 0, sizeof(g));
-  const bool ok = make_map(&g.a_shared, x, H, T, BM) &&
-                  make_map(&g.b0_shared, w_split, H,
-                           (uint64_t)kRouterParts * E, bn);
-  if (!ok) return MOE_ERR_CUDA;
-  g.a_routed = g.a_shared;
-  g.b0_routed = g.b1_routed = g.b1_shared = g.b0_shared;
-  g.offsets = nullptr;  // no routed segments: E = 0 below
-  g.out_routed = g.out_shared = reinterpret_cast<uint16_t*>(logits);
-  g.status = status;
-  g.wait_limit_ns = wait_limit_ns;
-  g.E = 0;
-  g.T = T;
-  g.TK = 0;
-  g.n_routed = g.n_shared = E;
-  g.k_routed = g.k_shared = H;
-  switch (bn) {
-    case 64:
-      return launch_one<kRouter, 64, kStages>(g, s);
-    case 32:
-      return launch_one<kRouter, 32, kStages>(g, s);
-    default:
-      return launch_one<kRouter, 16, kStages>(g, s);
-  }
-}
-
-int sm_count() {
-  int dev = 0, n = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
-  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) !=
-      cudaSuccess)
-    return 148;
-  return n;
-}
 
 int launch_expert_ffn(const FfnArgs& a, cudaStream_t s) {
   const int TK = a.T * a.topk;
   // ---- up projection + SwiGLU
   GemmParams up;
   std::memset(&up, 0, sizeof(up));
-  const int bf = (a.I % 128 == 0 && a.I_shared % 128 == 0) ? 128 : 64;
-  bool ok = make_map(&up.a_routed, a.xp, a.H, TK, BM) &&
-            make_map(&up.a_shared, a.x, a.H, a.T, BM) &&
-            make_map(&up.b0_routed, a.w1, a.H, (uint64_t)a.E * a.I, bf) &&
-            make_map(&up.b1_routed, a.w3, a.H, (uint64_t)a.E * a.I, bf) &&
-            make_map(&up.b0_shared, a.ws1, a.H, a.I_shared, bf) &&
-            make_map(&up.b1_shared, a.ws3, a.H, a.I_shared, bf);
+  bool ok = token_maps(up.tok_routed, a.xp, a.H, TK) &&
+            token_maps(up.tok_shared, a.x, a.H, a.T) &&
+            make_tmap_bf16(&up.wa_routed, a.w1, a.H, (uint64_t)a.E * a.I, BM) &&
+            make_tmap_bf16(&up.wb_routed, a.w3, a.H, (uint64_t)a.E * a.I, BM) &&
+            make_tmap_bf16(&up.wa_shared, a.ws1, a.H, a.I_shared, BM) &&
+            make_tmap_bf16(&up.wb_shared, a.ws3, a.H, a.I_shared, BM);
   if (!ok) return MOE_ERR_CUDA;
   up.offsets = a.offsets;
   up.out_routed = a.h;
@@ -560,8 +511,7 @@ int launch_expert_ffn(const FfnArgs& a, cudaStream_t s) {
   up.n_shared = a.I_shared;
   up.k_routed = a.H;
   up.k_shared = a.H;
-  int rc = (bf == 128) ? launch_one<kUp, 256, kStages>(up, s)
-                       : launch_one<kUp, 128, kStages>(up, s);
+  int rc = launch_one<kUp>(up, s);
   if (rc != MOE_OK) return rc;
   if (a.between_event != nullptr)
     cudaEventRecord(static_cast<cudaEvent_t>(a.between_event), s);
@@ -569,14 +519,13 @@ int launch_expert_ffn(const FfnArgs& a, cudaStream_t s) {
   // ---- down projection
   GemmParams dn;
   std::memset(&dn, 0, sizeof(dn));
-  const int bn = (a.H % 256 == 0) ? 256 : (a.H % 128 == 0 ? 128 : 64);
-  ok = make_map(&dn.a_routed, a.h, a.I, TK, BM) &&
-       make_map(&dn.a_shared, a.hs, a.I_shared, a.T, BM) &&
-       make_map(&dn.b0_routed, a.w2, a.I, (uint64_t)a.E * a.H, bn) &&
-       make_map(&dn.b0_shared, a.ws2, a.I_shared, a.H, bn);
+  ok = token_maps(dn.tok_routed, a.h, a.I, TK) &&
+       token_maps(dn.tok_shared, a.hs, a.I_shared, a.T) &&
+       make_tmap_bf16(&dn.wa_routed, a.w2, a.I, (uint64_t)a.E * a.H, BM) &&
+       make_tmap_bf16(&dn.wa_shared, a.ws2, a.I_shared, a.H, BM);
   if (!ok) return MOE_ERR_CUDA;
-  dn.b1_routed = dn.b0_routed;
-  dn.b1_shared = dn.b0_shared;
+  dn.wb_routed = dn.wa_routed;
+  dn.wb_shared = dn.wa_shared;
   dn.offsets = a.offsets;
   dn.out_routed = a.yp;
   dn.out_shared = a.ys;
@@ -589,14 +538,7 @@ int launch_expert_ffn(const FfnArgs& a, cudaStream_t s) {
   dn.n_shared = a.H;
   dn.k_routed = a.I;
   dn.k_shared = a.I_shared;
-  switch (bn) {
-    case 256:
-      return launch_one<kDown, 256, kStages>(dn, s);
-    case 128:
-      return launch_one<kDown, 128, kStages>(dn, s);
-    default:
-      return launch_one<kDown, 64, kStages>(dn, s);
-  }
+  return launch_one<kDown>(dn, s);
 }
 
 }  // namespace moe

@@ -1,0 +1,71 @@
+// Host-side helpers of the tensor-core kernels: TMA tensor-map encoding
+// (through the driver entry point, so libmoe needs no -lcuda), the SM
+// count, and the persistent-grid size of the expert GEMMs.
+#include <cuda.h>
+
+#include <atomic>
+
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType,
+                                  cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                  CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000,
+                                         cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return static_cast<EncodeTiledFn>(nullptr);
+    return reinterpret_cast<EncodeTiledFn>(f);
+  }();
+  return fn;
+}
+
+std::atomic<int> g_gemm_ctas{0};  // 0: one CTA per SM
+
+}  // namespace
+
+bool make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t inner,
+                    uint64_t outer, uint32_t box_outer) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {inner * 2};
+  const cuuint32_t box[2] = {64u, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base),
+             dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) !=
+      cudaSuccess)
+    return 148;
+  return n;
+}
+
+int gemm_ctas() {
+  const int sms = sm_count();
+  const int n = g_gemm_ctas.load(std::memory_order_relaxed);
+  return (n > 0 && n < sms) ? n : sms;
+}
+
+void set_gemm_ctas(int n) {
+  g_gemm_ctas.store(n > 0 ? n : 0, std::memory_order_relaxed);
+}
+
+}  // namespace moe

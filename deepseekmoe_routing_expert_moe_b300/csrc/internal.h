@@ -3,6 +3,8 @@
 // returns the cudaGetLastError() of its launches.
 #pragma once
 
+#include <cuda.h>
+
 #include <cstddef>
 #include <cstdint>
 #include <cuda_runtime.h>
@@ -67,6 +69,7 @@ struct FfnArgs {
 // 0 on success, else a moe_status_t (encoding or launch failure)
 int launch_expert_ffn(const FfnArgs& a, cudaStream_t s);
 
+// ---- router_gemm.cu
 // router logits on the tensor cores from the exact 3-way bf16 split of the
 // fp32 router weight (w_split [3, E, H], see launch_split_router_weight);
 // returns MOE_ERR_UNSUPPORTED when E is not a multiple of 16
@@ -75,9 +78,17 @@ int launch_router_logits_tc(const uint16_t* x, const uint16_t* w_split,
                             DevStatus* status, uint64_t wait_limit_ns,
                             cudaStream_t s);
 int router_tile_n(int E);  // 0 if the tensor-core path does not apply
+// (routing.cu) the exact split itself
 cudaError_t launch_split_router_weight(const float* w, int E, int H,
                                        uint16_t* w_split, cudaStream_t s);
 
+// ---- host_util.cu
+// 2-D bf16 row-major [outer, inner] tensor map, box [box_outer rows, 64
+// elements], 128-byte swizzle; false if encoding fails
+bool make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t inner,
+                    uint64_t outer, uint32_t box_outer);
 int sm_count();
+int gemm_ctas();           // persistent CTAs of the expert GEMMs
+void set_gemm_ctas(int n); // 0: one per SM
 
 }  // namespace moe

@@ -244,6 +244,8 @@ void moe_set_profile_events(void* const* events, int32_t n) {
                       : nullptr;
 }
 
+void moe_set_gemm_ctas(int32_t n) { moe::set_gemm_ctas(n); }
+
 void moe_set_wait_timeout_ns(uint64_t ns) {
   g_wait_limit_ns = ns == 0 ? kDefaultWaitNs : ns;
 }

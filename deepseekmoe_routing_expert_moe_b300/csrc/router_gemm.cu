@@ -1,0 +1,303 @@
+// Router logits on the sm_103a tensor cores.
+//
+// The affinity of token t for expert e is the sigmoid of z[t,e] = x_t . w_e
+// ("02 · DeepSeek-V3" (PaperTrace) §1.3, eq. 15), with the router weight
+// kept in fp32.  The fp32 router weight is split exactly into three bf16
+// parts, W = W_hi + W_mid + W_lo, and z = x W_hi^T + x W_mid^T + x W_lo^T
+// accumulates all three into one fp32 accumulator -- each bf16 x bf16
+// product is exact in fp32, so this is an fp32-accumulated x W^T.
+//
+// Design (one persistent CTA per SM, 6 warps):
+//   warp 0 lane 0   TMA producer: x tile 128x64 and the three BNx64 parts of
+//                   W per stage, 128-byte swizzle, STAGES-deep mbarrier ring
+//   warp 1 lane 0   tcgen05.mma issuer (M=128 tokens, N=BN experts, K=16),
+//                   fp32 accumulators in tensor memory, double buffered;
+//                   warp 1 also owns the TMEM allocation
+//   warps 2..5      epilogue: tcgen05.ld of the accumulator rows, fp32
+//                   stores of the valid token rows
+// Units are (expert block n, token tile m), m fastest.  Every wait is
+// bounded (MOE_ERR_TIMEOUT in the status word, then a clean exit).
+#include <cuda.h>
+
+#include <cstdint>
+#include <cstring>
+
+#include "device_common.cuh"
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int BM = 128;        // token rows per tile = MMA M
+constexpr int BK = 64;         // K per stage: 64 bf16 = one 128 B row
+constexpr int UMMA_K = 16;     // K of one kind::f16 MMA
+constexpr int kThreads = 192;  // 6 warps
+constexpr int kParts = 3;      // W = hi + mid + lo
+constexpr int kStages = 4;
+constexpr uint64_t kDrainNs = 2000000000ull;
+
+enum {
+  kSiteProducer = 41,
+  kSiteMmaAcc = 42,
+  kSiteMmaFull = 43,
+  kSiteEpilogue = 44,
+  kSiteDrain = 45
+};
+
+struct RouterParams {
+  CUtensorMap x_map;  // x [T, H] bf16, box 128 x 64
+  CUtensorMap w_map;  // w_split [3*E, H] bf16, box BN x 64
+  float* logits;      // [T, E]
+  DevStatus* status;
+  unsigned long long wait_limit_ns;
+  int T, E, H;
+};
+
+template <int BN>
+struct RShape {
+  static constexpr uint32_t A_BYTES = BM * BK * 2;
+  static constexpr uint32_t B_BYTES = kParts * BN * BK * 2;
+  static constexpr uint32_t TMEM_COLS = (2 * BN < 32) ? 32 : 2 * BN;
+  static constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
+};
+
+template <int BN>
+__global__ void __launch_bounds__(kThreads, 1)
+    router_gemm_kernel(const __grid_constant__ RouterParams p) {
+  using S = RShape<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + kStages * S::A_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + kStages * S::B_BYTES);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + kStages;
+  uint64_t* tfull = bars + 2 * kStages;
+  uint64_t* tempty = bars + 2 * kStages + 2;
+  uint64_t* drain = bars + 2 * kStages + 4;
+  volatile uint32_t* misc =
+      reinterpret_cast<volatile uint32_t*>(bars + 2 * kStages + 5);
+  // misc[0] TMEM base, misc[1] abort flag
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(smem_u32(&full[i]), 1);
+      mbar_init(smem_u32(&empty[i]), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&tfull[i]), 1);
+      mbar_init(smem_u32(&tempty[i]), 128);
+    }
+    mbar_init(smem_u32(drain), 1);
+    misc[1] = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&p.x_map);
+    prefetch_tmap(&p.w_map);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(const_cast<uint32_t*>(&misc[0])), S::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = misc[0];
+  const int mt = (p.T + BM - 1) / BM;
+  const int total = mt * (p.E / BN);
+  const int nkb = p.H / BK;
+  const uint64_t limit = p.wait_limit_ns;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------ producer
+      uint32_t stage = 0, phase = 0, issued = 0;
+      const uint64_t pol = policy_evict_last();
+      for (int u = blockIdx.x; u < total; u += gridDim.x) {
+        const int n = u / mt, m = u - n * mt;
+        bool ok = true;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1,
+                                 abort_flag, limit, p.status,
+                                 kSiteProducer)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = smem_u32(&full[stage]);
+          mbar_arrive_expect_tx(fb, S::A_BYTES + S::B_BYTES);
+          tma_load_2d_hint(smem_u32(sA + stage * S::A_BYTES), &p.x_map,
+                           kb * BK, m * BM, fb, pol);
+#pragma unroll
+          for (int part = 0; part < kParts; ++part)
+            tma_load_2d_hint(
+                smem_u32(sB + stage * S::B_BYTES + part * BN * BK * 2),
+                &p.w_map, kb * BK, part * p.E + n * BN, fb, pol);
+          ++issued;
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+      }
+      const uint32_t first = issued > kStages ? issued - kStages : 0;
+      for (uint32_t i = first; i < issued; ++i)
+        mbar_wait_bounded(smem_u32(&full[i % kStages]), (i / kStages) & 1,
+                          nullptr, kDrainNs, p.status, kSiteDrain);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ----------------------------------------------------------- MMA
+      uint32_t stage = 0, phase = 0;
+      bool any = false;
+      int local = 0;
+      for (int u = blockIdx.x; u < total; u += gridDim.x, ++local) {
+        const int buf = local & 1;
+        const uint32_t ap = (local >> 1) & 1;
+        if (!mbar_wait_bounded(smem_u32(&tempty[buf]), ap ^ 1, abort_flag,
+                               limit, p.status, kSiteMmaAcc))
+          break;
+        tc_fence_after();
+        const uint32_t d = tmem_base + buf * BN;
+        bool ok = true;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait_bounded(smem_u32(&full[stage]), phase, abort_flag,
+                                 limit, p.status, kSiteMmaFull)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(sA + stage * S::A_BYTES);
+          const uint32_t b0 = smem_u32(sB + stage * S::B_BYTES);
+#pragma unroll
+          for (int part = 0; part < kParts; ++part) {
+#pragma unroll
+            for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+              tc_mma_f16(d, sw128_kmajor_desc(a0 + kk * UMMA_K * 2),
+                         sw128_kmajor_desc(b0 + part * BN * BK * 2 +
+                                           kk * UMMA_K * 2),
+                         S::IDESC, (kb | part | kk) != 0);
+            }
+          }
+          any = true;
+          tc_commit(smem_u32(&empty[stage]));
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        tc_commit(smem_u32(&tfull[buf]));
+      }
+      if (any) {  // every issued MMA completes before TMEM is released
+        tc_commit(smem_u32(drain));
+        mbar_wait_bounded(smem_u32(drain), 0, nullptr, kDrainNs, p.status,
+                          kSiteDrain);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------- epilogue
+    const int q = warp & 3;  // TMEM lane quadrant this warp may access
+    const int r = q * 32 + lane;
+    int local = 0;
+    for (int u = blockIdx.x; u < total; u += gridDim.x, ++local) {
+      const int n = u / mt, m = u - n * mt;
+      const int buf = local & 1;
+      const uint32_t ap = (local >> 1) & 1;
+      int ok = 0;
+      if (lane == 0)
+        ok = mbar_wait_bounded(smem_u32(&tfull[buf]), ap, abort_flag, limit,
+                               p.status, kSiteEpilogue);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                          static_cast<uint32_t>(buf * BN);
+      const int t = m * BM + r;
+      const bool valid = t < p.T;
+      float* frow = p.logits + (size_t)(valid ? t : 0) * p.E + (size_t)n * BN;
+#pragma unroll 1
+      for (int c = 0; c < BN; c += 16) {
+        uint32_t v[16];
+        tmem_ld16(tb + c, v);
+        tmem_ld_wait();
+        if (valid) {
+          uint4* dst = reinterpret_cast<uint4*>(frow + c);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            dst[i] = make_uint4(v[4 * i], v[4 * i + 1], v[4 * i + 2],
+                                v[4 * i + 3]);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(smem_u32(&tempty[buf]));
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, S::TMEM_COLS);
+  }
+}
+
+template <int BN>
+size_t router_smem_bytes() {
+  using S = RShape<BN>;
+  return 1024 + kStages * (S::A_BYTES + S::B_BYTES) +
+         (2 * kStages + 5) * sizeof(uint64_t) + 4 * sizeof(uint32_t);
+}
+
+template <int BN>
+int launch_router(const RouterParams& rp, cudaStream_t s) {
+  auto kern = router_gemm_kernel<BN>;
+  const size_t smem = router_smem_bytes<BN>();
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem)) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  kern<<<sm_count(), kThreads, smem, s>>>(rp);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+}  // namespace
+
+int router_tile_n(int E) {
+  if (E % 64 == 0) return 64;
+  if (E % 32 == 0) return 32;
+  if (E % 16 == 0) return 16;
+  return 0;
+}
+
+int launch_router_logits_tc(const uint16_t* x, const uint16_t* w_split,
+                            float* logits, int T, int H, int E,
+                            DevStatus* status, uint64_t wait_limit_ns,
+                            cudaStream_t s) {
+  const int bn = router_tile_n(E);
+  if (bn == 0) return MOE_ERR_UNSUPPORTED;
+  RouterParams rp;
+  std::memset(&rp, 0, sizeof(rp));
+  if (!make_tmap_bf16(&rp.x_map, x, H, T, BM) ||
+      !make_tmap_bf16(&rp.w_map, w_split, H, (uint64_t)kParts * E, bn))
+    return MOE_ERR_CUDA;
+  rp.logits = logits;
+  rp.status = status;
+  rp.wait_limit_ns = wait_limit_ns;
+  rp.T = T;
+  rp.E = E;
+  rp.H = H;
+  switch (bn) {
+    case 64:
+      return launch_router<64>(rp, s);
+    case 32:
+      return launch_router<32>(rp, s);
+    default:
+      return launch_router<16>(rp, s);
+  }
+}
+
+}  // namespace moe

@@ -63,6 +63,7 @@ _SIGS = {
     "moe_status_string": (ctypes.c_char_p, [_I]),
     "moe_get_device_error": (_I, [_P, _P]),
     "moe_set_wait_timeout_ns": (None, [ctypes.c_uint64]),
+    "moe_set_gemm_ctas": (None, [ctypes.c_int32]),
     "moe_abi_version": (ctypes.c_int32, []),
     "moe_set_profile_events": (None, [ctypes.POINTER(ctypes.c_void_p),
                                        ctypes.c_int32]),
@@ -210,6 +211,11 @@ def moe_get_device_error(ws, stream=None) -> int:
 
 def moe_set_wait_timeout_ns(ns: int):
     lib().moe_set_wait_timeout_ns(ns)
+
+
+def moe_set_gemm_ctas(n: int):
+    """Cap the expert GEMMs' persistent grid at n CTAs (0 = one per SM)."""
+    lib().moe_set_gemm_ctas(n)
 
 
 _prof_keep = None

@@ -251,6 +251,15 @@ moe_status_t moe_get_device_error(void* ws, moe_stream_t stream);
  * launches. */
 void moe_set_wait_timeout_ns(uint64_t ns);
 
+/* Number of persistent CTAs of the expert GEMM kernels: n > 0 caps the
+ * grid at n CTAs (at most one per SM), 0 restores one CTA per SM (the
+ * default).  Results do not depend on it -- every CTA walks the same unit
+ * list with a stride of the grid size -- so it serves tuning and tests that
+ * must drive many units, and both kinds of tensor-memory slot use, through
+ * one CTA.  Takes effect for launches made after the call; not thread-safe
+ * against concurrent launches. */
+void moe_set_gemm_ctas(int32_t n);
+
 /* Profiling hook for kernel-level timing.  When `events` is non-NULL and
  * n >= MOE_FORWARD_KERNELS + 1, moe_forward records events[i] (cudaEvent_t
  * handles created by the caller, passed as void*) on its stream just before

@@ -96,6 +96,34 @@ def test_ffn_one_expert_takes_everything():
     assert np.diff(p["offsets"])[17] == 600
 
 
+def mixed_load_idx(T, counts):
+    """topk=2 routing with the given per-expert loads: the expert-sorted
+    slot list is cut in two halves, token t takes slot t of each (distinct
+    experts while every load is below T)."""
+    flat = np.repeat(np.arange(len(counts), dtype=np.int32), counts)
+    assert flat.size == 2 * T and max(counts) < T
+    return np.stack([flat[:T], flat[T:]], axis=1)
+
+
+@pytest.mark.parametrize("ctas", [1, 3, 0])
+def test_ffn_mixed_chunk_widths_and_tmem_slots(ctas):
+    # loads hit every unit shape: N=16, 32, 128 (one TMEM slot), 144, 256
+    # (both slots; 256 = two 128-row token boxes), 257 rows -> chunks of
+    # 144 + 113, 762 rows -> 3 x 256; the shared segment (900 rows) is cut
+    # into 240 x 3 + 180.  With the grid capped, one CTA walks a mixed
+    # sequence of one-slot and two-slot units.
+    counts = [1, 17, 128, 129, 250, 256, 257, 762]
+    T = 900
+    cfg = inputs.custom_config("ffn_mix", 505, T=T, H=256, E=8, n_group=4,
+                               topk_group=2, topk=2, I=256, I_shared=192)
+    try:
+        ops.moe_set_gemm_ctas(ctas)
+        p, _, _ = run_ffn(cfg, mixed_load_idx(T, counts))
+    finally:
+        ops.moe_set_gemm_ctas(0)
+    assert list(np.diff(p["offsets"])) == counts
+
+
 def test_ffn_single_token():
     cfg = inputs.custom_config("ffn_e", 504, T=1, H=256, E=16, n_group=4,
                                topk_group=2, topk=4, I=64, I_shared=64)
