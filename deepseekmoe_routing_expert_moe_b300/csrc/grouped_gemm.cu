@@ -22,14 +22,18 @@
 //         exchange between threads
 //   down: W2 rows [f0, f0+128) and [f0+128, f0+256)
 //
-// Design (one persistent CTA per SM, 6 warps):
-//   warp 0 lane 0   TMA producer: per stage the two 128x64 weight tiles and
-//                   the Nx64 token tile (boxes of 128/64/32/16 rows summing
-//                   to N), 128-byte swizzle, STAGES-deep mbarrier ring
+// Design (one persistent CTA per SM, 7 warps):
+//   warp 0 lane 0   weight producer: the two 128x64 weight tiles of every
+//                   k-block into a deep ring (the HBM stream: its depth is
+//                   what keeps enough bytes in flight per SM)
+//   warp 2 lane 0   token producer: the Nx64 token tile (boxes of
+//                   128/64/32/16 rows summing to N) into a shallow ring (the
+//                   rows are L2-resident, re-read by every feature block)
+//                   both with 128-byte swizzle and mbarrier completion
 //   warp 1 lane 0   tcgen05.mma issuer (M=128, N per unit, K=16), fp32
 //                   accumulators in tensor memory; warp 1 owns the TMEM
 //                   allocation (512 columns = two slots of 256)
-//   warps 2..5      epilogue: tcgen05.ld, SwiGLU (up) or conversion (down),
+//   warps 3..6      epilogue: tcgen05.ld, SwiGLU (up) or conversion (down),
 //                   bf16 stores of the valid rows and features
 // TMEM: a unit with N <= 128 puts both accumulators in one 256-column slot,
 // so consecutive such units alternate slots and the epilogue of one overlaps
@@ -55,14 +59,36 @@ namespace {
 constexpr int BM = 128;         // weight rows per accumulator = MMA M
 constexpr int BK = 64;          // K per stage: 64 bf16 = one 128 B row
 constexpr int UMMA_K = 16;      // K of one kind::f16 MMA
-constexpr int NT = 256;         // largest token chunk = largest MMA N
-constexpr int kThreads = 192;   // 6 warps
-constexpr int kStages = 3;
+// Compile-time tuning (defaults are the measured best on B300):
+//   MOE_FFN_NT         largest token chunk = largest MMA N (<= 256, % 16)
+//   MOE_FFN_WSTAGES    depth of the weight ring (HBM stream)
+//   MOE_FFN_TSTAGES    depth of the token ring (L2-resident rows)
+#ifndef MOE_FFN_NT
+#define MOE_FFN_NT 192
+#endif
+#ifndef MOE_FFN_WSTAGES
+#define MOE_FFN_WSTAGES 4
+#endif
+#ifndef MOE_FFN_TSTAGES
+#define MOE_FFN_TSTAGES 3
+#endif
+constexpr int NT = MOE_FFN_NT;
+constexpr int kWStages = MOE_FFN_WSTAGES;
+constexpr int kTStages = MOE_FFN_TSTAGES;
+constexpr int kEpiWarps = 4;  // one per TMEM lane quadrant
+constexpr int kEpiWarp0 = 3;  // warps 0..2: weight producer, MMA, token producer
+constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps);
+constexpr int SLOT = 256;       // TMEM columns per accumulator slot
 constexpr int kTokBoxes = 4;    // token boxes of 16, 32, 64, 128 rows
-constexpr uint32_t W_BYTES = BM * BK * 2;       // one weight tile
-constexpr uint32_t TOK_BYTES = NT * BK * 2;     // token tile (max)
-constexpr uint32_t STAGE_BYTES = 2 * W_BYTES + TOK_BYTES;
-constexpr uint32_t TMEM_COLS = 512;             // two slots of 256 columns
+constexpr uint32_t W_BYTES = BM * BK * 2;         // one weight tile
+constexpr uint32_t WSTAGE_BYTES = 2 * W_BYTES;    // both weight tiles
+constexpr uint32_t TSTAGE_BYTES = NT * BK * 2;    // token tile (max)
+constexpr uint32_t RING_BYTES = kWStages * WSTAGE_BYTES + kTStages * TSTAGE_BYTES;
+constexpr int kBars = 2 * kWStages + 2 * kTStages + 5;
+constexpr uint32_t TMEM_COLS = 2 * SLOT;          // two slots
+constexpr size_t kSmemLimit = 232448;             // 227 KB per CTA
+static_assert(NT % 16 == 0 && NT >= 16 && NT <= SLOT, "token chunk");
+static_assert(TSTAGE_BYTES % 1024 == 0, "swizzle atoms stay aligned");
 constexpr uint64_t kDrainNs = 2000000000ull;
 
 enum { kUp = 0, kDown = 1 };
@@ -137,7 +163,47 @@ __device__ __forceinline__ Unit decode_unit(int u, const int* useg,
 }
 
 __device__ __forceinline__ float silu_f(float g) {
-  return g * __frcp_rn(1.0f + __expf(-g));
+  return __fdividef(g, 1.0f + __expf(-g));
+}
+
+// Columns [0, n) of this thread's TMEM lane (accumulator at `taddr`),
+// rounded to bf16 pairs: pk[j / 2] holds column j in its low (even j) or
+// high (odd j) half.  COLS bounds n at compile time so pk stays in
+// registers.
+template <int COLS>
+__device__ __forceinline__ void load_packed(uint32_t taddr, int n,
+                                            uint32_t (&pk)[COLS / 2]) {
+#pragma unroll
+  for (int c = 0; c < COLS / 16; ++c) {
+    if (16 * c < n) {
+      uint32_t v[16];
+      tmem_ld16(taddr + 16 * c, v);
+      tmem_ld_wait();
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        pk[8 * c + i] = pack_bf16x2(__uint_as_float(v[2 * i]),
+                                    __uint_as_float(v[2 * i + 1]));
+    }
+  }
+}
+
+// out[j * ld] = column j of pk for j < rows (one bf16 per token row).
+template <int COLS>
+__device__ __forceinline__ void store_packed(const uint32_t (&pk)[COLS / 2],
+                                             uint16_t* out, int ld,
+                                             int rows) {
+#pragma unroll
+  for (int c = 0; c < COLS / 16; ++c) {
+    if (16 * c < rows) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        if (16 * c + i < rows)
+          out[(size_t)(16 * c + i) * ld] = static_cast<uint16_t>(
+              (i & 1) ? (pk[8 * c + i / 2] >> 16)
+                      : (pk[8 * c + i / 2] & 0xFFFFu));
+      }
+    }
+  }
 }
 
 template <int MODE>
@@ -147,14 +213,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * STAGE_BYTES);
-  uint64_t* full = bars;
-  uint64_t* empty = bars + kStages;
-  uint64_t* tfull = bars + 2 * kStages;       // per TMEM slot
-  uint64_t* tempty = bars + 2 * kStages + 2;  // per TMEM slot
-  uint64_t* drain = bars + 2 * kStages + 4;
-  volatile uint32_t* misc =
-      reinterpret_cast<volatile uint32_t*>(bars + 2 * kStages + 5);
+  uint8_t* sW = smem;                                  // weight ring
+  uint8_t* sT = smem + kWStages * WSTAGE_BYTES;        // token ring
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + RING_BYTES);
+  uint64_t* wfull = bars;
+  uint64_t* wempty = wfull + kWStages;
+  uint64_t* kfull = wempty + kWStages;
+  uint64_t* kempty = kfull + kTStages;
+  uint64_t* tfull = kempty + kTStages;  // per TMEM slot
+  uint64_t* tempty = tfull + 2;         // per TMEM slot
+  uint64_t* drain = tempty + 2;
+  volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(bars + kBars);
   // misc[0] TMEM base, misc[1] abort flag, misc[2] bad-offsets flag
   const int E = p.E;
   const int NS = E + 1;  // the shared segment (0) + the routed ones
@@ -166,13 +235,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kStages; ++i) {
-      mbar_init(smem_u32(&full[i]), 1);
-      mbar_init(smem_u32(&empty[i]), 1);
+    for (int i = 0; i < kWStages; ++i) {
+      mbar_init(smem_u32(&wfull[i]), 1);
+      mbar_init(smem_u32(&wempty[i]), 1);
+    }
+    for (int i = 0; i < kTStages; ++i) {
+      mbar_init(smem_u32(&kfull[i]), 1);
+      mbar_init(smem_u32(&kempty[i]), 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&tfull[i]), 1);
-      mbar_init(smem_u32(&tempty[i]), 128);
+      mbar_init(smem_u32(&tempty[i]), 32 * kEpiWarps);
     }
     mbar_init(smem_u32(drain), 1);
     misc[1] = 0;
@@ -247,37 +320,78 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     if (lane == 0) {
-      // ------------------------------------------------------ producer
+      // ----------------------------------------------- weight producer
       uint32_t stage = 0, phase = 0, issued = 0;
       const uint64_t pol_w = policy_evict_first();
-      const uint64_t pol_t = policy_evict_last();
-      for (int u = blockIdx.x; u < total; u += gridDim.x) {
+      // weight tiles of unit u: maps, first rows, k-blocks
+      auto unit_w = [&](int u, const CUtensorMap*& wa, const CUtensorMap*& wb,
+                        int& wrow, int& wrow_b) {
         const Unit w = decode_unit(u, useg, srow0, srows, NS);
         const bool sh = (w.seg == 0);
-        const CUtensorMap* tok = sh ? p.tok_shared : p.tok_routed;
-        const CUtensorMap* wa = sh ? &p.wa_shared : &p.wa_routed;
-        const CUtensorMap* wb = sh ? &p.wb_shared : &p.wb_routed;
-        const int wrow = (sh ? 0 : (w.seg - 1) * p.n_routed) + w.f * FB;
-        const int wrow_b = (MODE == kUp) ? wrow : wrow + BM;
-        const int nkb = (sh ? p.k_shared : p.k_routed) / BK;
-        const uint32_t tx = 2 * W_BYTES + (uint32_t)w.n * BK * 2;
+        wa = sh ? &p.wa_shared : &p.wa_routed;
+        wb = sh ? &p.wb_shared : &p.wb_routed;
+        wrow = (sh ? 0 : (w.seg - 1) * p.n_routed) + w.f * FB;
+        wrow_b = (MODE == kUp) ? wrow : wrow + BM;
+        return (sh ? p.k_shared : p.k_routed) / BK;
+      };
+      for (int u = blockIdx.x; u < total; u += gridDim.x) {
+        const CUtensorMap *wa, *wb;
+        int wrow, wrow_b;
+        const int nkb = unit_w(u, wa, wb, wrow, wrow_b);
         bool ok = true;
         for (int kb = 0; kb < nkb; ++kb) {
-          if (!mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1,
+          if (!mbar_wait_bounded(smem_u32(&wempty[stage]), phase ^ 1,
                                  abort_flag, limit, p.status,
                                  kSiteProducer)) {
             ok = false;
             break;
           }
-          const uint32_t fb = smem_u32(&full[stage]);
-          uint8_t* st = smem + stage * STAGE_BYTES;
-          mbar_arrive_expect_tx(fb, tx);
+          const uint32_t fb = smem_u32(&wfull[stage]);
+          uint8_t* st = sW + stage * WSTAGE_BYTES;
+          mbar_arrive_expect_tx(fb, WSTAGE_BYTES);
           tma_load_2d_hint(smem_u32(st), wa, kb * BK, wrow, fb, pol_w);
           tma_load_2d_hint(smem_u32(st + W_BYTES), wb, kb * BK, wrow_b, fb,
                            pol_w);
+          ++issued;
+          if (++stage == kWStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+      }
+      // drain: the last min(issued, stages) loads must land before exit
+      const uint32_t first = issued > kWStages ? issued - kWStages : 0;
+      for (uint32_t i = first; i < issued; ++i)
+        mbar_wait_bounded(smem_u32(&wfull[i % kWStages]),
+                          (i / kWStages) & 1, nullptr, kDrainNs, p.status,
+                          kSiteDrain);
+    }
+    __syncwarp();
+  } else if (warp == 2) {
+    if (lane == 0) {
+      // ------------------------------------------------ token producer
+      uint32_t stage = 0, phase = 0, issued = 0;
+      const uint64_t pol_t = policy_evict_last();
+      for (int u = blockIdx.x; u < total; u += gridDim.x) {
+        const Unit w = decode_unit(u, useg, srow0, srows, NS);
+        const bool sh = (w.seg == 0);
+        const CUtensorMap* tok = sh ? p.tok_shared : p.tok_routed;
+        const int nkb = (sh ? p.k_shared : p.k_routed) / BK;
+        const uint32_t tx = (uint32_t)w.n * BK * 2;
+        bool ok = true;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait_bounded(smem_u32(&kempty[stage]), phase ^ 1,
+                                 abort_flag, limit, p.status,
+                                 kSiteProducer)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = smem_u32(&kfull[stage]);
+          uint8_t* stok = sT + stage * TSTAGE_BYTES;
+          mbar_arrive_expect_tx(fb, tx);
           // token rows [row0, row0 + n) as boxes of 128/64/32/16 rows
-          uint8_t* stok = st + 2 * W_BYTES;
-          if (w.n == NT) {
+          if (w.n == 256) {
             tma_load_2d_hint(smem_u32(stok), &tok[3], kb * BK, w.row0, fb,
                              pol_t);
             tma_load_2d_hint(smem_u32(stok + 128 * BK * 2), &tok[3], kb * BK,
@@ -294,31 +408,31 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           ++issued;
-          if (++stage == kStages) {
+          if (++stage == kTStages) {
             stage = 0;
             phase ^= 1;
           }
         }
         if (!ok) break;
       }
-      // drain: the last min(issued, kStages) loads must land before exit
-      const uint32_t first = issued > kStages ? issued - kStages : 0;
+      const uint32_t first = issued > kTStages ? issued - kTStages : 0;
       for (uint32_t i = first; i < issued; ++i)
-        mbar_wait_bounded(smem_u32(&full[i % kStages]), (i / kStages) & 1,
-                          nullptr, kDrainNs, p.status, kSiteDrain);
+        mbar_wait_bounded(smem_u32(&kfull[i % kTStages]),
+                          (i / kTStages) & 1, nullptr, kDrainNs, p.status,
+                          kSiteDrain);
     }
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0) {
       // ----------------------------------------------------------- MMA
-      uint32_t stage = 0, phase = 0;
+      uint32_t wstage = 0, wphase = 0, kstage = 0, kphase = 0;
       uint32_t tph = 0;  // bit s: parity of the uses of TMEM slot s so far
       int slot = 0;
       bool any = false;
       for (int u = blockIdx.x; u < total; u += gridDim.x) {
         const Unit w = decode_unit(u, useg, srow0, srows, NS);
         const int nkb = ((w.seg == 0) ? p.k_shared : p.k_routed) / BK;
-        const bool wide = w.n > NT / 2;
+        const bool wide = w.n > SLOT / 2;
         const int s1 = wide ? (slot ^ 1) : slot;
         if (!mbar_wait_bounded(smem_u32(&tempty[slot]),
                                ((tph >> slot) & 1) ^ 1, abort_flag, limit,
@@ -329,19 +443,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                                        limit, p.status, kSiteMmaAcc))
           break;
         tc_fence_after();
-        const uint32_t da = tmem_base + slot * (NT);
-        const uint32_t db = wide ? tmem_base + s1 * NT : da + NT / 2;
+        const uint32_t da = tmem_base + slot * SLOT;
+        const uint32_t db = wide ? tmem_base + s1 * SLOT : da + SLOT / 2;
         const uint32_t idesc = idesc_bf16_f32(BM, w.n);
         bool ok = true;
         for (int kb = 0; kb < nkb; ++kb) {
-          if (!mbar_wait_bounded(smem_u32(&full[stage]), phase, abort_flag,
-                                 limit, p.status, kSiteMmaFull)) {
+          if (!mbar_wait_bounded(smem_u32(&wfull[wstage]), wphase,
+                                 abort_flag, limit, p.status,
+                                 kSiteMmaFull) ||
+              !mbar_wait_bounded(smem_u32(&kfull[kstage]), kphase,
+                                 abort_flag, limit, p.status,
+                                 kSiteMmaFull)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t s0 = smem_u32(smem + stage * STAGE_BYTES);
-          const uint32_t st = s0 + 2 * W_BYTES;
+          const uint32_t s0 = smem_u32(sW + wstage * WSTAGE_BYTES);
+          const uint32_t st = smem_u32(sT + kstage * TSTAGE_BYTES);
 #pragma unroll
           for (int kk = 0; kk < BK / UMMA_K; ++kk) {
             const uint64_t bdesc = sw128_kmajor_desc(st + kk * UMMA_K * 2);
@@ -352,10 +470,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                        bdesc, idesc, acc);
           }
           any = true;
-          tc_commit(smem_u32(&empty[stage]));
-          if (++stage == kStages) {
-            stage = 0;
-            phase ^= 1;
+          tc_commit(smem_u32(&wempty[wstage]));
+          tc_commit(smem_u32(&kempty[kstage]));
+          if (++wstage == kWStages) {
+            wstage = 0;
+            wphase ^= 1;
+          }
+          if (++kstage == kTStages) {
+            kstage = 0;
+            kphase ^= 1;
           }
         }
         if (!ok) break;
@@ -377,13 +500,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------- epilogue
+    // Every accumulator column of a unit is read into registers (bf16
+    // pairs) before any global store, so TMEM goes back to the MMA warp as
+    // soon as it is read and the slow, scattered stores overlap the next
+    // unit's MMAs instead of delaying them.
     const int q = warp & 3;  // TMEM lane quadrant this warp may access
     const int r = q * 32 + lane;
     uint32_t tph = 0;  // bit s: parity of the uses of TMEM slot s so far
     int slot = 0;
     for (int u = blockIdx.x; u < total; u += gridDim.x) {
       const Unit w = decode_unit(u, useg, srow0, srows, NS);
-      const bool wide = w.n > NT / 2;
+      const bool wide = w.n > SLOT / 2;
       const int s1 = wide ? (slot ^ 1) : slot;
       int ok = 0;
       if (lane == 0) {
@@ -397,55 +524,51 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tc_fence_after();
       const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
-      const uint32_t ta = tmem_base + lane_off + slot * NT;
+      const uint32_t ta = tmem_base + lane_off + slot * SLOT;
       const uint32_t tb =
-          wide ? tmem_base + lane_off + s1 * NT : ta + NT / 2;
+          wide ? tmem_base + lane_off + s1 * SLOT : ta + SLOT / 2;
       const bool sh = (w.seg == 0);
       uint16_t* out = sh ? p.out_shared : p.out_routed;
       const int ld = sh ? p.n_shared : p.n_routed;
       // feature columns of this thread's TMEM lane in both accumulators
       const int fa = w.f * FB + r;
       const int fbc = (MODE == kUp) ? fa : fa + BM;
-      const bool va = fa < ld, vb = fbc < ld;
       uint16_t* obase = out + (size_t)w.row0 * ld;
-#pragma unroll 1
-      for (int j0 = 0; j0 < w.n; j0 += 16) {
-        uint32_t a[16], b[16];
-        tmem_ld16(ta + j0, a);
-        tmem_ld16(tb + j0, b);
-        tmem_ld_wait();
-        if (j0 + 16 >= w.n) {  // last columns read: hand TMEM back
-          tc_fence_before();
-          mbar_arrive(smem_u32(&tempty[slot]));
-          if (wide) mbar_arrive(smem_u32(&tempty[s1]));
-        }
-        const int nv = min(16, w.rows - j0);
-        if (MODE == kUp) {
-          if (va) {
+      auto release = [&](int sl) {
+        tc_fence_before();
+        mbar_arrive(smem_u32(&tempty[sl]));
+      };
+      if (MODE == kUp) {
+        uint32_t pk[NT / 2];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              if (i < nv) {
-                const float h = silu_f(__uint_as_float(a[i])) *
-                                __uint_as_float(b[i]);
-                obase[(size_t)(j0 + i) * ld + fa] =
-                    __bfloat16_as_ushort(__float2bfloat16_rn(h));
-              }
-            }
-          }
-        } else {
+        for (int c = 0; c < NT / 16; ++c) {
+          if (16 * c < w.n) {
+            uint32_t a[16], b[16];
+            tmem_ld16(ta + 16 * c, a);
+            tmem_ld16(tb + 16 * c, b);
+            tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            if (i < nv) {
-              uint16_t* o = obase + (size_t)(j0 + i) * ld;
-              if (va)
-                o[fa] = __bfloat16_as_ushort(
-                    __float2bfloat16_rn(__uint_as_float(a[i])));
-              if (vb)
-                o[fbc] = __bfloat16_as_ushort(
-                    __float2bfloat16_rn(__uint_as_float(b[i])));
-            }
+            for (int i = 0; i < 8; ++i)
+              pk[8 * c + i] = pack_bf16x2(
+                  silu_f(__uint_as_float(a[2 * i])) *
+                      __uint_as_float(b[2 * i]),
+                  silu_f(__uint_as_float(a[2 * i + 1])) *
+                      __uint_as_float(b[2 * i + 1]));
           }
         }
+        release(slot);
+        if (wide) release(s1);
+        if (fa < ld) store_packed<NT>(pk, obase + fa, ld, w.rows);
+      } else {
+        // a wide unit's accumulators sit in two slots: each is released as
+        // soon as it is read; a narrow unit's slot after both are read
+        uint32_t pk[NT / 2];
+        load_packed<NT>(ta, w.n, pk);
+        if (wide) release(slot);
+        if (fa < ld) store_packed<NT>(pk, obase + fa, ld, w.rows);
+        load_packed<NT>(tb, w.n, pk);
+        release(s1);
+        if (fbc < ld) store_packed<NT>(pk, obase + fbc, ld, w.rows);
       }
       tph ^= 1u << slot;
       if (wide)
@@ -462,14 +585,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 size_t smem_bytes(int E) {
-  return 1024 + kStages * STAGE_BYTES + (2 * kStages + 5) * sizeof(uint64_t) +
-         4 * sizeof(uint32_t) + sizeof(int) * (3 * (E + 1) + 1);
+  return 1024 + RING_BYTES + kBars * sizeof(uint64_t) + 4 * sizeof(uint32_t) +
+         sizeof(int) * (3 * (E + 1) + 1);
 }
 
 template <int MODE>
 int launch_one(const GemmParams& gp, cudaStream_t s) {
   auto kern = expert_gemm_kernel<MODE>;
   const size_t smem = smem_bytes(gp.E);
+  if (smem > kSmemLimit) return MOE_ERR_UNSUPPORTED;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem)) != cudaSuccess)
     return MOE_ERR_CUDA;
