@@ -59,22 +59,23 @@ namespace {
 constexpr int BM = 128;         // weight rows per accumulator = MMA M
 constexpr int BK = 64;          // K per stage: 64 bf16 = one 128 B row
 constexpr int UMMA_K = 16;      // K of one kind::f16 MMA
-// Compile-time tuning (defaults are the measured best on B300):
-//   MOE_FFN_NT         largest token chunk = largest MMA N (<= 256, % 16)
-//   MOE_FFN_WSTAGES    depth of the weight ring (HBM stream)
-//   MOE_FFN_TSTAGES    depth of the token ring (L2-resident rows)
-#ifndef MOE_FFN_NT
-#define MOE_FFN_NT 192
-#endif
-#ifndef MOE_FFN_WSTAGES
-#define MOE_FFN_WSTAGES 4
-#endif
-#ifndef MOE_FFN_TSTAGES
-#define MOE_FFN_TSTAGES 3
-#endif
-constexpr int NT = MOE_FFN_NT;
-constexpr int kWStages = MOE_FFN_WSTAGES;
-constexpr int kTStages = MOE_FFN_TSTAGES;
+// Two pipeline shapes, chosen per launch from the mean rows per routed
+// expert (T*K/E): below the bf16 ridge of ~256 rows (FLOP per weight byte
+// ~= rows) the GEMM streams weights from HBM and wants short token chunks
+// with a deeper token ring; above it, it is tensor-bound and wants the
+// widest MMA (N = 256).  Both were measured best of a sweep on B300.
+//   NT  largest token chunk = largest MMA N (<= 256, multiple of 16)
+//   WS  depth of the weight ring (the HBM stream)
+//   TS  depth of the token ring (L2-resident rows, re-read per block)
+template <int NT_, int WS_, int TS_>
+struct Pipe {
+  static constexpr int NT = NT_;
+  static constexpr int WS = WS_;
+  static constexpr int TS = TS_;
+};
+using PipeStream = Pipe<192, 4, 3>;   // mean rows per expert < 256
+using PipeCompute = Pipe<256, 4, 2>;  // mean rows per expert >= 256
+constexpr int kComputeRows = 256;
 constexpr int kEpiWarps = 4;  // one per TMEM lane quadrant
 constexpr int kEpiWarp0 = 3;  // warps 0..2: weight producer, MMA, token producer
 constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps);
@@ -82,13 +83,19 @@ constexpr int SLOT = 256;       // TMEM columns per accumulator slot
 constexpr int kTokBoxes = 4;    // token boxes of 16, 32, 64, 128 rows
 constexpr uint32_t W_BYTES = BM * BK * 2;         // one weight tile
 constexpr uint32_t WSTAGE_BYTES = 2 * W_BYTES;    // both weight tiles
-constexpr uint32_t TSTAGE_BYTES = NT * BK * 2;    // token tile (max)
-constexpr uint32_t RING_BYTES = kWStages * WSTAGE_BYTES + kTStages * TSTAGE_BYTES;
-constexpr int kBars = 2 * kWStages + 2 * kTStages + 5;
 constexpr uint32_t TMEM_COLS = 2 * SLOT;          // two slots
 constexpr size_t kSmemLimit = 232448;             // 227 KB per CTA
-static_assert(NT % 16 == 0 && NT >= 16 && NT <= SLOT, "token chunk");
-static_assert(TSTAGE_BYTES % 1024 == 0, "swizzle atoms stay aligned");
+
+// shared-memory layout of one pipeline shape
+template <class P>
+struct Ring {
+  static constexpr uint32_t TSTAGE_BYTES = P::NT * BK * 2;  // token tile
+  static constexpr uint32_t BYTES =
+      P::WS * WSTAGE_BYTES + P::TS * TSTAGE_BYTES;
+  static constexpr int BARS = 2 * P::WS + 2 * P::TS + 5;
+  static_assert(P::NT % 16 == 0 && P::NT >= 16 && P::NT <= SLOT, "chunk");
+  static_assert(TSTAGE_BYTES % 1024 == 0, "swizzle atoms stay aligned");
+};
 constexpr uint64_t kDrainNs = 2000000000ull;
 
 enum { kUp = 0, kDown = 1 };
@@ -129,7 +136,7 @@ struct Unit {
   int seg;    // 0 = shared expert, 1 + e = routed expert e
   int f;      // feature block
   int row0;   // first row of the chunk in the token / output tensors
-  int rows;   // valid rows in the chunk (1..NT)
+  int rows;   // valid rows in the chunk (1..NT of the pipeline shape)
   int n;      // MMA N: rows rounded up to 16
 };
 
@@ -137,6 +144,7 @@ __device__ __forceinline__ int round16(int v) { return (v + 15) & ~15; }
 
 // Segment tables in shared memory: srow0/srows per segment, useg the
 // exclusive prefix of units per segment (useg[NS] = total).
+template <int NT>
 __device__ __forceinline__ Unit decode_unit(int u, const int* useg,
                                             const int* srow0,
                                             const int* srows, int NS) {
@@ -206,16 +214,18 @@ __device__ __forceinline__ void store_packed(const uint32_t (&pk)[COLS / 2],
   }
 }
 
-template <int MODE>
+template <int MODE, class P>
 __global__ void __launch_bounds__(kThreads, 1)
     expert_gemm_kernel(const __grid_constant__ GemmParams p) {
   constexpr int FB = Feat<MODE>::FB;
+  constexpr int NT = P::NT, kWStages = P::WS, kTStages = P::TS;
+  constexpr uint32_t TSTAGE_BYTES = Ring<P>::TSTAGE_BYTES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sW = smem;                                  // weight ring
   uint8_t* sT = smem + kWStages * WSTAGE_BYTES;        // token ring
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + RING_BYTES);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Ring<P>::BYTES);
   uint64_t* wfull = bars;
   uint64_t* wempty = wfull + kWStages;
   uint64_t* kfull = wempty + kWStages;
@@ -223,7 +233,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* tfull = kempty + kTStages;  // per TMEM slot
   uint64_t* tempty = tfull + 2;         // per TMEM slot
   uint64_t* drain = tempty + 2;
-  volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(bars + kBars);
+  volatile uint32_t* misc =
+      reinterpret_cast<volatile uint32_t*>(bars + Ring<P>::BARS);
   // misc[0] TMEM base, misc[1] abort flag, misc[2] bad-offsets flag
   const int E = p.E;
   const int NS = E + 1;  // the shared segment (0) + the routed ones
@@ -326,7 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // weight tiles of unit u: maps, first rows, k-blocks
       auto unit_w = [&](int u, const CUtensorMap*& wa, const CUtensorMap*& wb,
                         int& wrow, int& wrow_b) {
-        const Unit w = decode_unit(u, useg, srow0, srows, NS);
+        const Unit w = decode_unit<NT>(u, useg, srow0, srows, NS);
         const bool sh = (w.seg == 0);
         wa = sh ? &p.wa_shared : &p.wa_routed;
         wb = sh ? &p.wb_shared : &p.wb_routed;
@@ -374,7 +385,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t stage = 0, phase = 0, issued = 0;
       const uint64_t pol_t = policy_evict_last();
       for (int u = blockIdx.x; u < total; u += gridDim.x) {
-        const Unit w = decode_unit(u, useg, srow0, srows, NS);
+        const Unit w = decode_unit<NT>(u, useg, srow0, srows, NS);
         const bool sh = (w.seg == 0);
         const CUtensorMap* tok = sh ? p.tok_shared : p.tok_routed;
         const int nkb = (sh ? p.k_shared : p.k_routed) / BK;
@@ -430,7 +441,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int slot = 0;
       bool any = false;
       for (int u = blockIdx.x; u < total; u += gridDim.x) {
-        const Unit w = decode_unit(u, useg, srow0, srows, NS);
+        const Unit w = decode_unit<NT>(u, useg, srow0, srows, NS);
         const int nkb = ((w.seg == 0) ? p.k_shared : p.k_routed) / BK;
         const bool wide = w.n > SLOT / 2;
         const int s1 = wide ? (slot ^ 1) : slot;
@@ -509,7 +520,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t tph = 0;  // bit s: parity of the uses of TMEM slot s so far
     int slot = 0;
     for (int u = blockIdx.x; u < total; u += gridDim.x) {
-      const Unit w = decode_unit(u, useg, srow0, srows, NS);
+      const Unit w = decode_unit<NT>(u, useg, srow0, srows, NS);
       const bool wide = w.n > SLOT / 2;
       const int s1 = wide ? (slot ^ 1) : slot;
       int ok = 0;
@@ -584,21 +595,30 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+template <class P>
 size_t smem_bytes(int E) {
-  return 1024 + RING_BYTES + kBars * sizeof(uint64_t) + 4 * sizeof(uint32_t) +
-         sizeof(int) * (3 * (E + 1) + 1);
+  return 1024 + Ring<P>::BYTES + Ring<P>::BARS * sizeof(uint64_t) +
+         4 * sizeof(uint32_t) + sizeof(int) * (3 * (E + 1) + 1);
 }
 
-template <int MODE>
-int launch_one(const GemmParams& gp, cudaStream_t s) {
-  auto kern = expert_gemm_kernel<MODE>;
-  const size_t smem = smem_bytes(gp.E);
+template <int MODE, class P>
+int launch_shape(const GemmParams& gp, cudaStream_t s) {
+  auto kern = expert_gemm_kernel<MODE, P>;
+  const size_t smem = smem_bytes<P>(gp.E);
   if (smem > kSmemLimit) return MOE_ERR_UNSUPPORTED;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem)) != cudaSuccess)
     return MOE_ERR_CUDA;
   kern<<<gemm_ctas(), kThreads, smem, s>>>(gp);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+// the pipeline shape for this launch's mean rows per routed expert
+template <int MODE>
+int launch_one(const GemmParams& gp, cudaStream_t s) {
+  const long long mean_rows = gp.E > 0 ? (long long)gp.TK / gp.E : 0;
+  return mean_rows >= kComputeRows ? launch_shape<MODE, PipeCompute>(gp, s)
+                                   : launch_shape<MODE, PipeStream>(gp, s);
 }
 
 // token-operand maps of one [rows, k] bf16 tensor, boxes of 16..128 rows

@@ -105,17 +105,27 @@ def mixed_load_idx(T, counts):
     return np.stack([flat[:T], flat[T:]], axis=1)
 
 
+# (T, per-expert loads) for 8 experts, topk 2.  The first set has a mean
+# of 225 rows per expert (the HBM-streaming pipeline shape, chunks <= 192
+# rows), the second 325 (the tensor-bound shape, chunks <= 256 rows).
+MIXED_LOADS = {
+    "stream": (900, [1, 17, 128, 129, 250, 256, 257, 762]),
+    "compute": (1300, [1, 17, 128, 129, 256, 257, 600, 1212]),
+}
+
+
+@pytest.mark.parametrize("shape", sorted(MIXED_LOADS))
 @pytest.mark.parametrize("ctas", [1, 3, 0])
-def test_ffn_mixed_chunk_widths_and_tmem_slots(ctas):
-    # loads hit every unit shape: N=16, 32, 128 (one TMEM slot), 144, 256
-    # (both slots; 256 = two 128-row token boxes), 257 rows -> chunks of
-    # 144 + 113, 762 rows -> 3 x 256; the shared segment (900 rows) is cut
-    # into 240 x 3 + 180.  With the grid capped, one CTA walks a mixed
-    # sequence of one-slot and two-slot units.
-    counts = [1, 17, 128, 129, 250, 256, 257, 762]
-    T = 900
-    cfg = inputs.custom_config("ffn_mix", 505, T=T, H=256, E=8, n_group=4,
-                               topk_group=2, topk=2, I=256, I_shared=192)
+def test_ffn_mixed_chunk_widths_and_tmem_slots(ctas, shape):
+    # loads hit every unit shape: N=16, 32, 128 (one TMEM slot), 144..256
+    # (both slots; 256 = two 128-row token boxes), segments cut into
+    # several chunks, and the shared segment (all T rows) cut into equal
+    # chunks.  With the grid capped, one CTA walks a mixed sequence of
+    # one-slot and two-slot units.
+    T, counts = MIXED_LOADS[shape]
+    cfg = inputs.custom_config("ffn_mix_" + shape, 505, T=T, H=256, E=8,
+                               n_group=4, topk_group=2, topk=2, I=256,
+                               I_shared=192)
     try:
         ops.moe_set_gemm_ctas(ctas)
         p, _, _ = run_ffn(cfg, mixed_load_idx(T, counts))
