@@ -162,12 +162,13 @@ def oracle_sample(cfg, n_tokens: int, step: int = 0):
     x = f(inputs.x_tokens(cfg, step=step, T=n_tokens))
     wr = inputs.router_weight(cfg)
     b = inputs.bias(cfg)
-    z = O.router_logits(x, wr)
+    pref = inputs.zipf_preference(cfg) if cfg.zipf_s > 0 else None
+    z = O.router_logits(x, wr, pref)
     r = O.route(z, b, cfg.n_group, cfg.topk_group, cfg.topk)
     ew = {int(e): tuple(f(a) for a in inputs.expert_weights(cfg, int(e)))
           for e in np.unique(r["idx"])}
     sw = tuple(f(a) for a in inputs.shared_weights(cfg))
-    return dict(x=x, wr=wr, b=b, ew=ew, sw=sw)
+    return dict(x=x, wr=wr, b=b, ew=ew, sw=sw, pref=pref)
 
 
 def oracle_time(cfg, s) -> float:
@@ -175,7 +176,7 @@ def oracle_time(cfg, s) -> float:
     routing, load + bias step, every chosen expert, shared expert, combine)."""
     from oracle import moe_oracle as O
     t0 = time.perf_counter()
-    z = O.router_logits(s["x"], s["wr"])
+    z = O.router_logits(s["x"], s["wr"], s["pref"])
     r = O.route(z, s["b"], cfg.n_group, cfg.topk_group, cfg.topk)
     c = O.expert_counts(r["idx"], cfg.E)
     O.bias_update(c, s["b"], len(s["x"]), cfg.topk, cfg.gamma)
@@ -185,9 +186,14 @@ def oracle_time(cfg, s) -> float:
 
 # --------------------------------------------------------------- the arm
 def workload_desc(cfg) -> str:
-    return (f"{cfg.name}: V3 MoE layer forward + bias step, T={cfg.T}, "
-            f"H={cfg.H}, E={cfg.E}+1 shared, I={cfg.I}, top-{cfg.topk} of "
-            f"{cfg.n_group} groups / {cfg.topk_group} kept")
+    d = (f"{cfg.name}: V3 MoE layer forward + bias step, T={cfg.T}, "
+         f"H={cfg.H}, E={cfg.E}+1 shared, I={cfg.I}, top-{cfg.topk} of "
+         f"{cfg.n_group} groups / {cfg.topk_group} kept")
+    if cfg.zipf_s > 0:
+        d += (f"; skewed load: logits + {cfg.zipf_beta} * r_e^-{cfg.zipf_s} "
+              "(Zipf preference over a seeded expert ranking), bias from 0, "
+              "fresh tokens each step")
+    return d
 
 
 def config_json(cfg, n_gpus):
@@ -212,19 +218,29 @@ def run_gpu(args, rank, world, local_rank):
     w1, w3, w2 = inputs.device_expert_weights(cfg, "cuda")
     ws1, ws3, ws2 = inputs.shared_weights(cfg, "cuda")
     wr = torch.from_numpy(inputs.router_weight(cfg)).cuda()
-    W = ops.Weights(wr, w1, w3, w2, ws1, ws3, ws2)
-    NB = 4
+    # the skewed-load workload's per-expert preference enters as the
+    # router's additive term (zero preference: no term)
+    pref = (torch.from_numpy(inputs.zipf_preference(cfg)).cuda()
+            if cfg.zipf_s > 0 else None)
+    W = ops.Weights(wr, w1, w3, w2, ws1, ws3, ws2, router_offset=pref)
+    # fresh seeded tokens every step for the skewed run (its config asks
+    # for them; up to its 50 steps), 4 rotating batches otherwise
+    NB = min(max(args.steps, 4), cfg.steps) if cfg.zipf_s > 0 else 4
     xs = [inputs.x_tokens(cfg, step=i + 1000 * rank, device="cuda")
           for i in range(NB)]
     bias = torch.from_numpy(inputs.bias(cfg)).cuda()
     out = torch.empty((T, H), dtype=torch.int16, device="cuda")
     counts = torch.zeros(E, dtype=torch.int32, device="cuda")
+    # per-step load statistics (max, mean, min of the expert counts),
+    # written by the count-scan kernel of each timed step
+    # (rows padded to 16 bytes: the library takes 16-byte-aligned pointers)
+    load = torch.zeros((args.steps, 4), dtype=torch.float32, device="cuda")
     ws = ops.workspace(d, ops.MOE_WS_FORWARD)
     stream = torch.cuda.current_stream()
 
-    def step(i, counts_out=None):
+    def step(i, counts_out=None, stats=None):
         ops.moe_forward(d, W, xs[i % NB], bias, out, ws, update_bias=True,
-                        counts_out=counts_out)
+                        counts_out=counts_out, load_stats_out=stats)
 
     for i in range(args.warmup):
         step(i)
@@ -244,7 +260,7 @@ def run_gpu(args, rank, world, local_rank):
         barrier()
         ev0.record(stream)
         for i in range(args.steps):
-            step(i)
+            step(i, stats=load[i])
         ev1.record(stream)
         barrier()
     ms = ev0.elapsed_time(ev1)
@@ -274,6 +290,15 @@ def run_gpu(args, rank, world, local_rank):
                zip(ops.FORWARD_KERNEL_NAMES, kmean)}
     c = counts.cpu().numpy().astype(np.int64)
     assert c.sum() == T * K
+    lo = load.cpu().numpy().astype(np.float64)
+    mom = lo[:, 0] / lo[:, 1]
+    load_json = {"max_over_mean_first": round(float(mom[0]), 3),
+                 "max_over_mean_last": round(float(mom[-1]), 3),
+                 "max_over_mean_avg": round(float(mom.mean()), 3),
+                 "min_over_mean_avg": round(float((lo[:, 2] / lo[:, 1]).mean()),
+                                            3)}
+    if cfg.zipf_s > 0:
+        load_json["max_over_mean_per_step"] = [round(float(v), 3) for v in mom]
 
     # ---- roofline of the dominant kernel (expert up-projection GEMM)
     pk, pk_src = peaks()
@@ -380,6 +405,7 @@ def run_gpu(args, rank, world, local_rank):
         "clocks": clocks,
         "kernels_ms": kernels,
         "experts_touched": touched,
+        "load": load_json,
         "impl": "b300",
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -24,9 +24,10 @@ inline int route_blocks(int T) {
 struct DevStatus;
 
 // ---- routing.cu
+// offset [E] may be NULL (no additive term)
 cudaError_t launch_router_logits(const uint16_t* x, const float* w_router,
-                                 float* logits, int T, int H, int E,
-                                 cudaStream_t s);
+                                 const float* offset, float* logits, int T,
+                                 int H, int E, cudaStream_t s);
 cudaError_t launch_route(const float* logits, const float* bias, int T, int E,
                          int n_group, int topk_group, int topk,
                          int32_t* topk_idx, float* topk_gate,
@@ -74,7 +75,8 @@ int launch_expert_ffn(const FfnArgs& a, cudaStream_t s);
 // fp32 router weight (w_split [3, E, H], see launch_split_router_weight);
 // returns MOE_ERR_UNSUPPORTED when E is not a multiple of 16
 int launch_router_logits_tc(const uint16_t* x, const uint16_t* w_split,
-                            float* logits, int T, int H, int E,
+                            const float* offset, float* logits, int T, int H,
+                            int E,
                             DevStatus* status, uint64_t wait_limit_ns,
                             cudaStream_t s);
 int router_tile_n(int E);  // 0 if the tensor-core path does not apply

@@ -163,6 +163,7 @@ moe_status_t check_weights(const moe_weights_t* w) {
   MOE_NEED(w->ws3);
   MOE_NEED(w->ws2);
   MOE_ALIGN(w->w_router);
+  MOE_ALIGN(w->router_offset);
   MOE_ALIGN(w->w1);
   MOE_ALIGN(w->w3);
   MOE_ALIGN(w->w2);
@@ -203,19 +204,20 @@ moe_status_t ffn_launch(const moe_dims_t* d, const moe_weights_t* w,
   return static_cast<moe_status_t>(moe::launch_expert_ffn(a, s));
 }
 
-// z = x W_r^T: tensor cores (exact bf16 split of W_r) when E % 16 == 0,
-// else the fp32 SIMT kernel
+// z = x W_r^T (+ offset): tensor cores (exact bf16 split of W_r) when
+// E % 16 == 0, else the fp32 SIMT kernel
 moe_status_t router_logits_launch(const moe_dims_t* d, const uint16_t* x,
-                                  const float* w_router, float* logits,
+                                  const float* w_router,
+                                  const float* offset, float* logits,
                                   uint16_t* w_split, DevStatus* st,
                                   cudaStream_t s) {
   if (moe::router_tile_n(d->E) == 0)
-    return cuda_ok(moe::launch_router_logits(x, w_router, logits, d->T, d->H,
-                                             d->E, s));
+    return cuda_ok(moe::launch_router_logits(x, w_router, offset, logits,
+                                             d->T, d->H, d->E, s));
   MOE_TRY(cuda_ok(moe::launch_split_router_weight(w_router, d->E, d->H,
                                                   w_split, s)));
   return static_cast<moe_status_t>(moe::launch_router_logits_tc(
-      x, w_split, logits, d->T, d->H, d->E, st, g_wait_limit_ns, s));
+      x, w_split, offset, logits, d->T, d->H, d->E, st, g_wait_limit_ns, s));
 }
 
 }  // namespace
@@ -273,19 +275,22 @@ moe_status_t moe_get_device_error(void* ws, moe_stream_t stream) {
 }
 
 moe_status_t moe_router_logits(const moe_dims_t* d, const uint16_t* x,
-                               const float* w_router, float* logits, void* ws,
-                               size_t ws_bytes, moe_stream_t stream) {
+                               const float* w_router,
+                               const float* router_offset, float* logits,
+                               void* ws, size_t ws_bytes,
+                               moe_stream_t stream) {
   MOE_TRY(check_dims(d, false));
   MOE_NEED_T(x);
   MOE_NEED(w_router);
   MOE_NEED_T(logits);
   MOE_ALIGN(x);
   MOE_ALIGN(w_router);
+  MOE_ALIGN(router_offset);
   MOE_ALIGN(logits);
   MOE_TRY(check_ws(d, MOE_WS_ROUTER_LOGITS, ws, ws_bytes));
   if (d->T == 0) return MOE_OK;
   const Layout L = layout(d, MOE_WS_ROUTER_LOGITS);
-  return router_logits_launch(d, x, w_router, logits,
+  return router_logits_launch(d, x, w_router, router_offset, logits,
                               at<uint16_t>(ws, L.w_split),
                               at<DevStatus>(ws, 0), cs(stream));
 }
@@ -464,7 +469,7 @@ moe_status_t moe_forward(const moe_dims_t* d, const moe_weights_t* w,
   uint16_t* ys = at<uint16_t>(ws, L.ys);
 
   prof_mark(0, s);
-  MOE_TRY(router_logits_launch(d, x, w->w_router, logits,
+  MOE_TRY(router_logits_launch(d, x, w->w_router, w->router_offset, logits,
                                at<uint16_t>(ws, L.w_split), st, s));
   prof_mark(1, s);
   MOE_TRY(cuda_ok(moe::launch_route(logits, bias, T, E, d->n_group,

@@ -5,7 +5,8 @@
 // kept in fp32.  The fp32 router weight is split exactly into three bf16
 // parts, W = W_hi + W_mid + W_lo, and z = x W_hi^T + x W_mid^T + x W_lo^T
 // accumulates all three into one fp32 accumulator -- each bf16 x bf16
-// product is exact in fp32, so this is an fp32-accumulated x W^T.
+// product is exact in fp32, so this is an fp32-accumulated x W^T.  An
+// optional per-expert additive term o[e] is added in the epilogue.
 //
 // Design (one persistent CTA per SM, 6 warps):
 //   warp 0 lane 0   TMA producer: x tile 128x64 and the three BNx64 parts of
@@ -47,6 +48,7 @@ enum {
 struct RouterParams {
   CUtensorMap x_map;  // x [T, H] bf16, box 128 x 64
   CUtensorMap w_map;  // w_split [3*E, H] bf16, box BN x 64
+  const float* offset;  // [E] or NULL
   float* logits;      // [T, E]
   DevStatus* status;
   unsigned long long wait_limit_ns;
@@ -227,6 +229,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t v[16];
         tmem_ld16(tb + c, v);
         tmem_ld_wait();
+        if (p.offset != nullptr) {
+          const float* o = p.offset + (size_t)n * BN + c;
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            v[i] = __float_as_uint(__uint_as_float(v[i]) + __ldg(o + i));
+        }
         if (valid) {
           uint4* dst = reinterpret_cast<uint4*>(frow + c);
 #pragma unroll
@@ -274,7 +282,8 @@ int router_tile_n(int E) {
 }
 
 int launch_router_logits_tc(const uint16_t* x, const uint16_t* w_split,
-                            float* logits, int T, int H, int E,
+                            const float* offset, float* logits, int T, int H,
+                            int E,
                             DevStatus* status, uint64_t wait_limit_ns,
                             cudaStream_t s) {
   const int bn = router_tile_n(E);
@@ -284,6 +293,7 @@ int launch_router_logits_tc(const uint16_t* x, const uint16_t* w_split,
   if (!make_tmap_bf16(&rp.x_map, x, H, T, BM) ||
       !make_tmap_bf16(&rp.w_map, w_split, H, (uint64_t)kParts * E, bn))
     return MOE_ERR_CUDA;
+  rp.offset = offset;
   rp.logits = logits;
   rp.status = status;
   rp.wait_limit_ns = wait_limit_ns;

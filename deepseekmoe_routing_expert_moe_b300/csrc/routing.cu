@@ -22,8 +22,9 @@ constexpr int RL_BM = 64, RL_BN = 64, RL_BK = 32;
 
 __global__ void __launch_bounds__(256)
     router_logits_kernel(const uint16_t* __restrict__ x,
-                         const float* __restrict__ w, float* __restrict__ z,
-                         int T, int H, int E) {
+                         const float* __restrict__ w,
+                         const float* __restrict__ offset,
+                         float* __restrict__ z, int T, int H, int E) {
   __shared__ float xs[RL_BK][RL_BM + 4];
   __shared__ float ws[RL_BK][RL_BN + 4];
   const int tid = threadIdx.x;
@@ -77,7 +78,9 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int e = e0 + tx * 4 + j;
-      if (e < E) z[(size_t)t * E + e] = acc[i][j];
+      if (e < E)
+        z[(size_t)t * E + e] =
+            offset != nullptr ? acc[i][j] + offset[e] : acc[i][j];
     }
   }
 }
@@ -113,10 +116,11 @@ cudaError_t launch_split_router_weight(const float* w, int E, int H,
 }
 
 cudaError_t launch_router_logits(const uint16_t* x, const float* w_router,
-                                 float* logits, int T, int H, int E,
-                                 cudaStream_t s) {
+                                 const float* offset, float* logits, int T,
+                                 int H, int E, cudaStream_t s) {
   dim3 grid((T + RL_BM - 1) / RL_BM, (E + RL_BN - 1) / RL_BN);
-  router_logits_kernel<<<grid, 256, 0, s>>>(x, w_router, logits, T, H, E);
+  router_logits_kernel<<<grid, 256, 0, s>>>(x, w_router, offset, logits, T,
+                                            H, E);
   return cudaGetLastError();
 }
 

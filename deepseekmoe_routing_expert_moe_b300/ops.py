@@ -41,7 +41,8 @@ class MoeDims(ctypes.Structure):
 
 class MoeWeights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in
-                ("w_router", "w1", "w3", "w2", "ws1", "ws3", "ws2")]
+                ("w_router", "w1", "w3", "w2", "ws1", "ws3", "ws2",
+                 "router_offset")]
 
 
 _P = ctypes.c_void_p
@@ -51,7 +52,7 @@ _S = ctypes.c_size_t
 _I = ctypes.c_int
 _SIGS = {
     "moe_workspace_bytes": (ctypes.c_size_t, [_D, _I]),
-    "moe_router_logits": (_I, [_D, _P, _P, _P, _P, _S, _P]),
+    "moe_router_logits": (_I, [_D, _P, _P, _P, _P, _P, _S, _P]),
     "moe_route": (_I, [_D, _P, _P, _P, _P, _P, _P, _S, _P]),
     "moe_route_static_scratch": (_I, [_D, _P, _P, _P, _P, _P, _P]),
     "moe_permute": (_I, [_D, _P, _P, _P, _P, _P, _P, _P, _S, _P]),
@@ -129,11 +130,14 @@ def _check(fn: str, code: int):
 class Weights:
     """Device weights of one layer (torch tensors; bf16 stored as int16)."""
 
-    def __init__(self, w_router, w1, w3, w2, ws1, ws3, ws2):
+    def __init__(self, w_router, w1, w3, w2, ws1, ws3, ws2,
+                 router_offset=None):
         self.w_router, self.w1, self.w3, self.w2 = w_router, w1, w3, w2
         self.ws1, self.ws3, self.ws2 = ws1, ws3, ws2
+        self.router_offset = router_offset
         self.struct = MoeWeights(*(_ptr(t) for t in (w_router, w1, w3, w2,
-                                                      ws1, ws3, ws2)))
+                                                      ws1, ws3, ws2,
+                                                      router_offset)))
 
 
 def workspace_bytes(d: MoeDims, which: int) -> int:
@@ -149,10 +153,11 @@ def workspace(d: MoeDims, which: int, device="cuda") -> torch.Tensor:
 
 
 # ----------------------------------------------------------- entry points
-def moe_router_logits(d, x, w_router, logits, ws, stream=None):
+def moe_router_logits(d, x, w_router, logits, ws, router_offset=None,
+                      stream=None):
     _check("moe_router_logits", lib().moe_router_logits(
-        ctypes.byref(d), _ptr(x), _ptr(w_router), _ptr(logits), _ptr(ws),
-        ws.numel(), _stream(stream)))
+        ctypes.byref(d), _ptr(x), _ptr(w_router), _ptr(router_offset),
+        _ptr(logits), _ptr(ws), ws.numel(), _stream(stream)))
 
 
 def moe_route(d, logits, bias, topk_idx, topk_gate, counts, ws, stream=None):

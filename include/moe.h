@@ -53,7 +53,7 @@
 extern "C" {
 #endif
 
-#define MOE_ABI_VERSION 1
+#define MOE_ABI_VERSION 2
 
 typedef enum {
   MOE_OK = 0,
@@ -89,6 +89,10 @@ typedef struct {
 
 /* Expert and router weights (device pointers, caller-owned, read only).
  *   w_router [E, H]    fp32   router vectors, one row per expert
+ *   router_offset [E]  fp32   optional (NULL = none) additive term of the
+ *                             router's linear map, z = x W_r^T + o.  V3's
+ *                             router has none; a benchmark can put a
+ *                             per-expert preference there to skew the load.
  *   w1       [E, I, H] bf16   gate projection of each routed expert
  *   w3       [E, I, H] bf16   up projection
  *   w2       [E, H, I] bf16   down projection
@@ -102,6 +106,7 @@ typedef struct {
   const uint16_t* ws1;
   const uint16_t* ws3;
   const uint16_t* ws2;
+  const float* router_offset;
 } moe_weights_t;
 
 /* Which entry point a workspace is sized for. */
@@ -119,16 +124,20 @@ typedef enum {
  * once after allocating it (moe_get_device_error() re-zeroes the word). */
 size_t moe_workspace_bytes(const moe_dims_t* d, moe_ws_kind_t which);
 
-/* Router logits z = x W_r^T (the score whose sigmoid is the affinity,
+/* Router logits z = x W_r^T + o (the score whose sigmoid is the affinity,
  * "02 · DeepSeek-V3" §1.3 eq. 15), fp32 accumulation of exact products.
- * x [T, H] bf16, w_router [E, H] fp32 -> logits [T, E] fp32.  When E % 16
+ * x [T, H] bf16, w_router [E, H] fp32, router_offset [E] fp32 or NULL
+ * (o = 0) -> logits [T, E] fp32; the offset is added once, in fp32, after
+ * the accumulation.  When E % 16
  * == 0 it runs on the tensor cores: W_r is split exactly into three bf16
  * parts (hi + mid + lo == W_r) in the workspace and the three products are
  * accumulated into one fp32 accumulator; otherwise an fp32 SIMT kernel.
  * Workspace: MOE_WS_ROUTER_LOGITS. */
 moe_status_t moe_router_logits(const moe_dims_t* d, const uint16_t* x,
-                               const float* w_router, float* logits, void* ws,
-                               size_t ws_bytes, moe_stream_t stream);
+                               const float* w_router,
+                               const float* router_offset, float* logits,
+                               void* ws, size_t ws_bytes,
+                               moe_stream_t stream);
 
 /* Routing from precomputed logits ("02 · DeepSeek-V3" §1.3, §1.4):
  * sigmoid, + bias for selection, group-limited top-K, gates renormalised

@@ -87,11 +87,18 @@ def sig32(z: np.ndarray) -> np.ndarray:
 # Router logits (eq. 15 context: the affinity is the sigmoid of a token's
 # score against each expert's router vector).
 # --------------------------------------------------------------------------
-def router_logits(x_f32: np.ndarray, w_router: np.ndarray) -> np.ndarray:
-    """z[t, e] = fl32( sum_h x[t,h] * W_r[e,h] ), summed in fp64, rounded once.
+def router_logits(x_f32: np.ndarray, w_router: np.ndarray,
+                  offset: np.ndarray | None = None) -> np.ndarray:
+    """z[t, e] = fl32( sum_h x[t,h] * W_r[e,h] + o[e] ), summed in fp64,
+    rounded once (the affinity's argument, §1.3 eq. 15).
 
-    ``x_f32`` holds the exact values of the bf16 activations."""
+    ``x_f32`` holds the exact values of the bf16 activations.  ``offset``
+    o[E] is an optional additive term of the router's linear map: V3's
+    router has none (o = 0); the skewed-load workload puts its per-expert
+    preference there."""
     z = np.asarray(x_f32, np.float64) @ np.asarray(w_router, np.float64).T
+    if offset is not None:
+        z = z + np.asarray(offset, np.float64)[None, :]
     return z.astype(F32)
 
 

@@ -42,7 +42,7 @@ def test_library_exports_every_declared_symbol(L):
 
 
 def test_abi_version_and_status_strings(L):
-    assert ops.moe_abi_version() == 1
+    assert ops.moe_abi_version() == 2
     for code, name in ops.STATUS.items():
         assert ops.moe_status_string(code) == name
 

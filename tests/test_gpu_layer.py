@@ -123,10 +123,15 @@ def _sampled_v3_check(cfg, v3_weights, n_sample, step=0):
     T = cfg.T
     x = inputs.x_tokens(cfg, step=step)
     b = inputs.bias(cfg)
-    g = forward_gpu(cfg, v3_weights, x, b)
+    pref = inputs.zipf_preference(cfg) if cfg.zipf_s > 0 else None
+    W = v3_weights
+    if pref is not None:   # the skewed workload's preference on the logits
+        W = ops.Weights(W.w_router, W.w1, W.w3, W.w2, W.ws1, W.ws3, W.ws2,
+                        router_offset=dev(pref))
+    g = forward_gpu(cfg, W, x, b)
     f = inputs.bf16_bits_to_f32
     xf = f(x)
-    z = O.router_logits(xf, inputs.router_weight(cfg))
+    z = O.router_logits(xf, inputs.router_weight(cfg), pref)
     np.testing.assert_allclose(g["logits"], z, rtol=0, atol=1e-4)
     r = O.route(z, b, cfg.n_group, cfg.topk_group, cfg.topk)
     ok = margins_ok(r, cfg)
@@ -148,6 +153,7 @@ def _sampled_v3_check(cfg, v3_weights, n_sample, step=0):
     ref = O.layer_rows(xf[rows], r["idx"][rows], r["gate"][rows], ew,
                        tuple(f(a) for a in inputs.shared_weights(cfg)))
     rms_tolerance_check(g["out"][rows], ref)
+    return g
 
 
 def test_layer_v3_decode_128_tokens(v3_weights):
@@ -156,3 +162,13 @@ def test_layer_v3_decode_128_tokens(v3_weights):
 
 def test_layer_v3_prefill_4096_tokens(v3_weights):
     _sampled_v3_check(inputs.CONFIGS["prefill_v3"], v3_weights, n_sample=4)
+
+
+def test_layer_v3_skewed_32768_tokens(v3_weights):
+    """The skewed-load layer (Zipf s=1.2 preference as the router's additive
+    term): hot experts take thousands of rows, so the expert GEMMs run their
+    tensor-bound pipeline shape (chunks of up to 256 rows)."""
+    cfg = inputs.CONFIGS["skewed_v3"]
+    g = _sampled_v3_check(cfg, v3_weights, n_sample=4)
+    c = g["counts"]
+    assert c.max() > 4 * c.mean() and c.sum() == cfg.T * cfg.topk

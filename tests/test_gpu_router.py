@@ -1,9 +1,11 @@
-"""Router logits z = x W_r^T on the GPU against the oracle's fp64 sum.
+"""Router logits z = x W_r^T (+ o) on the GPU against the oracle's fp64 sum.
 
 Every product x_h * w_h is exact (bf16 x the exact bf16 split of the fp32
 weight on the tensor-core path; fp32 FMA on the SIMT path), so the only
 error is fp32 accumulation: for any summation order
-    |z_gpu - z| <= H * 2^-24 * sum_h |x_h w_h| + 2^-24 |z|.
+    |z_gpu - z| <= H * 2^-24 * sum_h |x_h w_h| + 2^-24 |z|
+(with an additive per-expert offset o, one more fp32 rounding of the sum:
+another 2^-24 |z| + 2^-24 |o|).
 The test asserts that bound elementwise, and a typical error far below it."""
 import numpy as np
 import pytest
@@ -17,25 +19,30 @@ from gpu_helpers import dev, host
 pytestmark = pytest.mark.gpu
 
 
-def check_logits(cfg, T=None):
+def check_logits(cfg, T=None, offset=None):
     T = cfg.T if T is None else T
     d = ops.dims_of(cfg, T=T)
     x = inputs.x_tokens(cfg, T=T)
     w = inputs.router_weight(cfg)
     z = torch.full((T, cfg.E), np.nan, dtype=torch.float32, device="cuda")
     ws = ops.workspace(d, ops.MOE_WS_ROUTER_LOGITS)
-    ops.moe_router_logits(d, dev(x), dev(w), z, ws)
+    ops.moe_router_logits(d, dev(x), dev(w), z, ws,
+                          router_offset=None if offset is None else dev(offset))
     assert ops.moe_get_device_error(ws) == 0
     zg = host(z).astype(np.float64)
     xf = inputs.bf16_bits_to_f32(x).astype(np.float64)
     ref = xf @ w.astype(np.float64).T                 # exact-ish fp64
     mag = np.abs(xf) @ np.abs(w.astype(np.float64)).T
     bound = cfg.H * 2.0 ** -24 * mag + 2.0 ** -24 * np.abs(ref)
+    if offset is not None:
+        o = offset.astype(np.float64)[None, :]
+        bound = bound + 2.0 ** -24 * (np.abs(ref) + np.abs(o))
+        ref = ref + o
     err = np.abs(zg - ref)
     assert np.all(err <= bound), (err / bound).max()
     assert np.sqrt(np.mean(err ** 2)) < 1e-2 * np.sqrt(np.mean(bound ** 2))
     # and the oracle's own rounding of the same sum
-    np.testing.assert_allclose(zg, O.router_logits(xf, w), rtol=0,
+    np.testing.assert_allclose(zg, O.router_logits(xf, w, offset), rtol=0,
                                atol=float(bound.max()))
 
 
@@ -60,3 +67,14 @@ def test_router_logits_expert_counts(E, G):
 
 def test_router_logits_tiny_config():
     check_logits(inputs.CONFIGS["tiny"])
+
+
+@pytest.mark.parametrize("E,G", [(256, 8), (24, 3)])
+def test_router_logits_with_offset(E, G):
+    # the skewed workload's per-expert preference as the router's additive
+    # term, on the tensor-core (E=256) and SIMT (E=24) paths
+    cfg = inputs.custom_config("rlo", 720 + E, T=300, H=512, E=E, n_group=G,
+                               topk_group=2, topk=2, I=64, I_shared=64,
+                               router_sigma=0.05)
+    r = np.random.default_rng(E).permutation(E) + 1
+    check_logits(cfg, offset=(1.0 * r ** -1.2).astype(np.float32))

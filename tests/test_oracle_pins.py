@@ -312,6 +312,14 @@ def test_router_logits_exact_on_dyadic_inputs():
             ex = sum(Fraction(float(x[t, h])) * Fraction(float(w[e, h]))
                      for h in range(24))
             assert z[t, e] == F32(float(ex))
+    # an additive per-expert offset enters once, before the rounding
+    o = (rng.integers(-8, 9, size=7) / 4).astype(F32)
+    zo = O.router_logits(x, w, o)
+    for t in range(5):
+        for e in range(7):
+            ex = sum(Fraction(float(x[t, h])) * Fraction(float(w[e, h]))
+                     for h in range(24)) + Fraction(float(o[e]))
+            assert zo[t, e] == F32(float(ex))
 
 
 def test_swiglu_closed_form_scalar():
