@@ -420,6 +420,159 @@ def run_gpu(args, rank, world, local_rank):
     return res
 
 
+def run_route_gpu(args, rank, world, local_rank):
+    """The routing-only configuration (T=16384 at the V3 shape): per step,
+    from precomputed fp32 logits, moe_route (sigmoid + bias, group-limited
+    top-8, gates, histogram), moe_permute without rows (offsets, dest,
+    src_row) and moe_bias_update -- the public calls a user makes.  8
+    rotating logits batches (134 MB, larger than L2)."""
+    import torch
+    from deepseekmoe_routing_expert_moe_b300 import inputs, ops
+    torch.cuda.set_device(local_rank)
+    cfg = inputs.CONFIGS[args.workload]
+    d = ops.dims_of(cfg)
+    T, E, K = cfg.T, cfg.E, cfg.topk
+    NB = 8
+    wr = torch.from_numpy(inputs.router_weight(cfg)).cuda()
+    zs = []
+    for i in range(NB):   # logits on the device from the seeded tokens
+        x = inputs.x_tokens(cfg, step=i + 1000 * rank, device="cuda")
+        z = torch.empty((T, E), dtype=torch.float32, device="cuda")
+        wsl = ops.workspace(d, ops.MOE_WS_ROUTER_LOGITS)
+        ops.moe_router_logits(d, x, wr, z, wsl)
+        zs.append(z)
+    del wsl
+    bias = torch.from_numpy(inputs.bias(cfg)).cuda()
+    idx = torch.empty((T, K), dtype=torch.int32, device="cuda")
+    gate = torch.empty((T, K), dtype=torch.float32, device="cuda")
+    counts = torch.empty(E, dtype=torch.int32, device="cuda")
+    offsets = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    dest = torch.empty((T, K), dtype=torch.int32, device="cuda")
+    src_row = torch.empty(T * K, dtype=torch.int32, device="cuda")
+    ws = ops.workspace(d, ops.MOE_WS_PERMUTE)
+    stream = torch.cuda.current_stream()
+
+    def step(i, ev=None):
+        if ev: ev[0].record(stream)
+        ops.moe_route(d, zs[i % NB], bias, idx, gate, counts, ws)
+        if ev: ev[1].record(stream)
+        ops.moe_permute(d, None, idx, offsets, dest, src_row, None, ws)
+        if ev: ev[2].record(stream)
+        ops.moe_bias_update(d, counts, bias)
+        if ev: ev[3].record(stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    assert ops.moe_get_device_error(ws) == 0
+    # The step is six small kernels: launched one by one from Python the
+    # host would be timed, so NB consecutive steps (one per logits batch)
+    # are captured once in a CUDA graph and the graph is replayed.
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g, stream=side):
+            for i in range(NB):
+                step(i)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)]
+           for _ in range(NB)]
+    ge = torch.cuda.CUDAGraph()     # the same steps with events between calls
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(ge, stream=side):
+            for i in range(NB):
+                step(i, evs[i])
+    stream.wait_stream(side)
+    reps = max(1, args.steps // NB)
+    for _ in range(max(1, args.warmup // NB)):
+        g.replay()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(gpu_index_for_smi(local_rank)) as clk:
+        torch.cuda.synchronize()
+        ev0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    ms = ev0.elapsed_time(ev1)
+    clocks = clk.summary()
+    args.steps = reps * NB
+    ge.replay()
+    torch.cuda.synchronize()
+    kt = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(3)]
+                   for e in evs]).mean(0)
+    # algorithmic bytes of the routing call (logits + bias read; idx,
+    # gates, counts and the per-64-token histogram rows written)
+    nblk = (T + 63) // 64
+    route_bytes = T * E * 4 + E * 4 + T * K * 8 + E * 4 + 2 * nblk * E * 4
+    perm_bytes = T * K * 4 + 2 * T * K * 4 + (E + 1) * 4 + 3 * nblk * E * 4
+    pk, pk_src = peaks()
+    hbm = float(pk["hbm_gbs"])
+    roof = {"bound": "hbm",
+            "achieved": round(route_bytes / (kt[0] / 1e3) / 1e9, 1),
+            "peak": hbm, "unit": "GB/s"}
+    roof["frac"] = round(roof["achieved"] / hbm, 4)
+    roof["traffic"] = None
+    roof["kernel"] = ("moe_route call (route_tg_kernel + count scan): "
+                      "logits -> idx, gates, counts")
+    roof["algorithmic_bytes"] = int(route_bytes)
+    roof["peak_source"] = f"{pk_src} (MEASURED_PEAKS.json)"
+    roof["permute_call"] = {"ms": round(float(kt[1]), 4),
+                            "algorithmic_bytes": int(perm_bytes)}
+    # end to end with host buffers: each step uploads its logits from
+    # pinned memory and downloads idx, gates and dest (launched eagerly,
+    # host launch time included)
+    zh = [torch.empty((T, E), dtype=torch.float32).pin_memory()
+          for _ in range(2)]
+    for i in range(2):
+        zh[i].copy_(zs[i].cpu())
+    oh = [torch.empty((T, K), dtype=torch.int32).pin_memory() for _ in range(3)]
+    zd = torch.empty((T, E), dtype=torch.float32, device="cuda")
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        zd.copy_(zh[i % 2], non_blocking=True)
+        ops.moe_route(d, zd, bias, idx, gate, counts, ws)
+        ops.moe_permute(d, None, idx, offsets, dest, src_row, None, ws)
+        ops.moe_bias_update(d, counts, bias)
+        oh[0].copy_(idx, non_blocking=True)
+        oh[1].copy_(gate.view(torch.int32), non_blocking=True)
+        oh[2].copy_(dest, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    assert ops.moe_get_device_error(ws) == 0
+    return {
+        "metric": "tokens/s routed (routing + dispatch order + bias step) "
+                  "at the V3 shape on 1 B300; % of HBM roofline",
+        "value": round(T * args.steps / (ms / 1e3), 1), "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms / args.steps, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic, seeded (logits from x ~N(0,1), W_router "
+                "~N(0,0.006); bias ~U(-0.01,0.01))",
+        "config": {"workload": f"{cfg.name}: routing-only, T={T}, E={E}, "
+                               f"top-{K} of {cfg.n_group} groups / "
+                               f"{cfg.topk_group} kept, from fp32 logits",
+                   "T": T, "E": E, "topk": K, "n_group": cfg.n_group,
+                   "topk_group": cfg.topk_group,
+                   "l2": "8 rotating logits batches, 134 MB > L2"},
+        "roofline": roof,
+        "e2e": {"value": round(T * args.steps / (e2e_ms / 1e3), 1),
+                "unit": "tokens/s", "h2d_bytes_per_step": T * E * 4,
+                "d2h_bytes_per_step": 3 * T * K * 4},
+        "gpu_launches": 6 * args.steps,
+        "clocks": clocks,
+        "calls_ms": {"moe_route": round(float(kt[0]), 4),
+                     "moe_permute": round(float(kt[1]), 4),
+                     "moe_bias_update": round(float(kt[2]), 4)},
+        "impl": "b300",
+    }
+
+
 def run_reference(args):
     """The oracle arm: the CPU oracle as it stands, per step one bounded
     sample of the workload (the same tokens every step)."""
@@ -458,7 +611,7 @@ def main():
     ap.add_argument("--impl", choices=("b300", "reference"), default="b300")
     ap.add_argument("--workload", default="prefill_v3",
                     choices=("prefill_v3", "decode_v3", "skewed_v3",
-                             "prefill_v3_e32"))
+                             "route_v3", "prefill_v3_e32"))
     ap.add_argument("--cpu-sample-tokens", type=int, default=4)
     ap.add_argument("--ref-tokens", type=int, default=1)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -480,7 +633,10 @@ def main():
         import torch.distributed as dist
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl")
-    res = run_gpu(args, rank, world, local_rank)
+    if args.workload == "route_v3":
+        res = run_route_gpu(args, rank, world, local_rank)
+    else:
+        res = run_gpu(args, rank, world, local_rank)
     if rank == 0:
         print(json.dumps(res), flush=True)
     if world > 1:

@@ -35,15 +35,18 @@ cudaError_t launch_route(const float* logits, const float* bias, int T, int E,
 cudaError_t launch_block_counts(const int32_t* topk_idx, int T, int E,
                                 int topk, int32_t* block_counts,
                                 DevStatus* st, cudaStream_t s);
-// reduces block_counts -> counts, scans -> offsets and block_base; if
-// bias != nullptr also applies the bias step (update_bias) and stats.
+// column scan of the per-block histograms: counts[e] (may be NULL),
+// block_prefix[blk][e] = counts of e in blocks before blk (may be NULL),
+// and -- if bias != nullptr -- the bias step on the final counts
 cudaError_t launch_scan(const int32_t* block_counts, int T, int E, int topk,
-                        int32_t* counts, int32_t* offsets, int32_t* block_base,
-                        float* bias, float gamma, float* load_stats,
-                        cudaStream_t s);
-cudaError_t launch_dest(const int32_t* topk_idx, const int32_t* block_base,
-                        int T, int E, int topk, int32_t* dest,
-                        int32_t* src_row, DevStatus* st, cudaStream_t s);
+                        int32_t* counts, int32_t* block_prefix, float* bias,
+                        float gamma, cudaStream_t s);
+// stable dispatch order from topk_idx, counts and block_prefix; writes
+// offsets[E+1] and load_stats[3] when non-NULL
+cudaError_t launch_dest(const int32_t* topk_idx, const int32_t* counts,
+                        const int32_t* block_prefix, int T, int E, int topk,
+                        int32_t* offsets, int32_t* dest, int32_t* src_row,
+                        float* load_stats, DevStatus* st, cudaStream_t s);
 cudaError_t launch_gather(const uint16_t* x, const int32_t* dest, int T, int H,
                           int topk, uint16_t* xp, cudaStream_t s);
 cudaError_t launch_combine(const uint16_t* x, const uint16_t* ys,

@@ -92,6 +92,7 @@ Layout layout(const moe_dims_t* d, moe_ws_kind_t which) {
     L.block_counts = take(nblk * E * 4);
     L.block_base = take(nblk * E * 4);
   }
+  if (which == MOE_WS_PERMUTE) L.counts = take(E * 4);
   if (which == MOE_WS_FORWARD) {
     L.logits = take(T * E * 4);
     L.idx = take(T * K * 4);
@@ -321,7 +322,7 @@ moe_status_t moe_route(const moe_dims_t* d, const float* logits,
                                     d->topk_group, d->topk, topk_idx,
                                     topk_gate, bc, s)));
   return cuda_ok(moe::launch_scan(bc, d->T, d->E, d->topk, counts, nullptr,
-                                  nullptr, nullptr, 0.f, nullptr, s));
+                                  nullptr, 0.f, s));
 }
 
 moe_status_t moe_permute(const moe_dims_t* d, const uint16_t* x,
@@ -348,12 +349,13 @@ moe_status_t moe_permute(const moe_dims_t* d, const uint16_t* x,
   DevStatus* st = at<DevStatus>(ws, 0);
   int32_t* bc = at<int32_t>(ws, L.block_counts);
   int32_t* bb = at<int32_t>(ws, L.block_base);
+  int32_t* cnt = at<int32_t>(ws, L.counts);
   MOE_TRY(cuda_ok(moe::launch_block_counts(topk_idx, d->T, d->E, d->topk, bc,
                                            st, s)));
-  MOE_TRY(cuda_ok(moe::launch_scan(bc, d->T, d->E, d->topk, nullptr, offsets,
-                                   bb, nullptr, 0.f, nullptr, s)));
-  MOE_TRY(cuda_ok(moe::launch_dest(topk_idx, bb, d->T, d->E, d->topk, dest,
-                                   src_row, st, s)));
+  MOE_TRY(cuda_ok(moe::launch_scan(bc, d->T, d->E, d->topk, cnt, bb, nullptr,
+                                   0.f, s)));
+  MOE_TRY(cuda_ok(moe::launch_dest(topk_idx, cnt, bb, d->T, d->E, d->topk,
+                                   offsets, dest, src_row, nullptr, st, s)));
   if (xp != nullptr)
     MOE_TRY(cuda_ok(moe::launch_gather(x, dest, d->T, d->H, d->topk, xp, s)));
   return MOE_OK;
@@ -475,13 +477,14 @@ moe_status_t moe_forward(const moe_dims_t* d, const moe_weights_t* w,
   MOE_TRY(cuda_ok(moe::launch_route(logits, bias, T, E, d->n_group,
                                     d->topk_group, K, idx, gate, bc, s)));
   prof_mark(2, s);
-  // counts, offsets, block bases -- and the bias step on this batch's load,
+  // counts, per-block prefixes -- and the bias step on this batch's load,
   // after routing consumed the old bias (same stream, so ordered)
-  MOE_TRY(cuda_ok(moe::launch_scan(bc, T, E, K, counts, offsets, bb,
+  MOE_TRY(cuda_ok(moe::launch_scan(bc, T, E, K, counts, bb,
                                    update_bias ? bias : nullptr, d->gamma,
-                                   load_stats_out, s)));
+                                   s)));
   prof_mark(3, s);
-  MOE_TRY(cuda_ok(moe::launch_dest(idx, bb, T, E, K, dest, src_row, st, s)));
+  MOE_TRY(cuda_ok(moe::launch_dest(idx, counts, bb, T, E, K, offsets, dest,
+                                   src_row, load_stats_out, st, s)));
   prof_mark(4, s);
   MOE_TRY(cuda_ok(moe::launch_gather(x, dest, T, H, K, xp, s)));
   prof_mark(5, s);  // 6 is recorded between the two expert GEMMs
@@ -565,5 +568,5 @@ extern "C" moe_status_t moe_route_static_scratch(
                                     d->topk_group, d->topk, topk_idx,
                                     topk_gate, scratch, s)));
   return cuda_ok(moe::launch_scan(scratch, d->T, d->E, d->topk, counts,
-                                  nullptr, nullptr, nullptr, 0.f, nullptr, s));
+                                  nullptr, nullptr, 0.f, s));
 }
