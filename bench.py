@@ -333,7 +333,9 @@ def run_gpu(args, rank, world, local_rank):
     roof["tensor_frac"] = round(up_flops / t_up / 1e12 / tc, 4)
     roof["down_gemm"] = {"ms": round(kmean[6], 4),
                          "hbm_frac": round(dn_bytes / t_dn / 1e9 / hbm, 4),
-                         "tensor_frac": round(dn_flops / t_dn / 1e12 / tc, 4)}
+                         "tensor_frac": round(dn_flops / t_dn / 1e12 / tc, 4),
+                         "algorithmic_bytes": int(dn_bytes),
+                         "traffic": ncu_traffic("gemm_down", cfg.name)}
 
     # ---- end to end through the C ABI with host buffers: every step copies
     #      its x from pinned host memory and its output back; the copies run
