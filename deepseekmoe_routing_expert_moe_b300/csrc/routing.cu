@@ -578,8 +578,11 @@ __global__ void __launch_bounds__(kRowThreads)
 // ===================================================================
 // Combine (eq. 12): out_t = bf16(x_t + ys_t + sum_k g_k * yp[dest[t,k]]),
 // fp32 arithmetic, slots in order.  One block per token, 8 bf16 per thread
-// per step.
+// per step; for topk <= KU the K expert rows of a step are all requested
+// before any is accumulated (the kernel is an HBM stream of 10 rows per
+// token), the sum itself still in slot order.
 // ===================================================================
+template <int KU>
 __global__ void __launch_bounds__(kRowThreads)
     combine_kernel(const uint16_t* __restrict__ x,
                    const uint16_t* __restrict__ ys,
@@ -602,6 +605,14 @@ __global__ void __launch_bounds__(kRowThreads)
     const uint4 xv = __ldg(reinterpret_cast<const uint4*>(x + (size_t)t * H) + c);
     const uint4 sv =
         __ldg(reinterpret_cast<const uint4*>(ys + (size_t)t * H) + c);
+    uint4 yv[KU > 0 ? KU : 1];
+    if (KU > 0) {
+#pragma unroll
+      for (int k = 0; k < KU; ++k)
+        if (k < K)
+          yv[k] = __ldg(reinterpret_cast<const uint4*>(yp + (size_t)sd[k] * H) +
+                        c);
+    }
     const uint32_t xa[4] = {xv.x, xv.y, xv.z, xv.w};
     const uint32_t sa[4] = {sv.x, sv.y, sv.z, sv.w};
     float acc[8];
@@ -610,16 +621,23 @@ __global__ void __launch_bounds__(kRowThreads)
       acc[2 * i] = bf16_lo(xa[i]) + bf16_lo(sa[i]);
       acc[2 * i + 1] = bf16_hi(xa[i]) + bf16_hi(sa[i]);
     }
-    for (int k = 0; k < K; ++k) {
-      const uint4 yv = __ldg(
-          reinterpret_cast<const uint4*>(yp + (size_t)sd[k] * H) + c);
-      const uint32_t ya[4] = {yv.x, yv.y, yv.z, yv.w};
-      const float g = sg[k];
+    auto add_row = [&](const uint4& v, float g) {
+      const uint32_t ya[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         acc[2 * i] = fmaf(g, bf16_lo(ya[i]), acc[2 * i]);
         acc[2 * i + 1] = fmaf(g, bf16_hi(ya[i]), acc[2 * i + 1]);
       }
+    };
+    if (KU > 0) {
+#pragma unroll
+      for (int k = 0; k < KU; ++k)
+        if (k < K) add_row(yv[k], sg[k]);
+    } else {
+      for (int k = 0; k < K; ++k)
+        add_row(__ldg(reinterpret_cast<const uint4*>(yp + (size_t)sd[k] * H) +
+                      c),
+                sg[k]);
     }
     uint4 o;
     o.x = pack_bf16x2(acc[0], acc[1]);
@@ -707,8 +725,12 @@ cudaError_t launch_combine(const uint16_t* x, const uint16_t* ys,
                            const uint16_t* yp, const int32_t* dest,
                            const float* gate, int T, int H, int topk,
                            uint16_t* out, cudaStream_t s) {
-  combine_kernel<<<T, kRowThreads, 0, s>>>(x, ys, yp, dest, gate, H, topk,
-                                           T * topk, out);
+  if (topk <= 8)
+    combine_kernel<8><<<T, kRowThreads, 0, s>>>(x, ys, yp, dest, gate, H,
+                                                topk, T * topk, out);
+  else
+    combine_kernel<0><<<T, kRowThreads, 0, s>>>(x, ys, yp, dest, gate, H,
+                                                topk, T * topk, out);
   return cudaGetLastError();
 }
 
