@@ -77,12 +77,15 @@ int launch_expert_ffn(const FfnArgs& a, cudaStream_t s);
 // router logits on the tensor cores from the exact 3-way bf16 split of the
 // fp32 router weight (w_split [3, E, H], see launch_split_router_weight);
 // returns MOE_ERR_UNSUPPORTED when E is not a multiple of 16
+// (partial: [router_ksplit(T,H,E), T, E] fp32 scratch, used when the
+// reduction over H is split; may be NULL when router_ksplit() == 1)
 int launch_router_logits_tc(const uint16_t* x, const uint16_t* w_split,
-                            const float* offset, float* logits, int T, int H,
-                            int E,
+                            const float* offset, float* logits,
+                            float* partial, int T, int H, int E,
                             DevStatus* status, uint64_t wait_limit_ns,
                             cudaStream_t s);
 int router_tile_n(int E);  // 0 if the tensor-core path does not apply
+int router_ksplit(int T, int H, int E);  // k ranges of the router GEMM
 // (routing.cu) the exact split itself
 cudaError_t launch_split_router_weight(const float* w, int E, int H,
                                        uint16_t* w_split, cudaStream_t s);

@@ -74,6 +74,7 @@ struct Layout {
          src_row = 0;
   size_t xp = 0, h = 0, hs = 0, yp = 0, ys = 0;
   size_t w_split = 0;  // [3, E, H] bf16 parts of the router weight
+  size_t r_partial = 0;  // [ksplit, T, E] fp32 partial router sums
   size_t total = 0;
 };
 
@@ -109,8 +110,11 @@ Layout layout(const moe_dims_t* d, moe_ws_kind_t which) {
     L.h = take(T * K * (size_t)d->I * 2);
     L.hs = take(T * (size_t)d->I_shared * 2);
   }
-  if (which == MOE_WS_ROUTER_LOGITS || which == MOE_WS_FORWARD)
+  if (which == MOE_WS_ROUTER_LOGITS || which == MOE_WS_FORWARD) {
     L.w_split = take(3 * E * H * 2);
+    const size_t ks = moe::router_ksplit(d->T, d->H, d->E);
+    if (ks > 1) L.r_partial = take(ks * T * E * 4);
+  }
   L.total = o;
   return L;
 }
@@ -210,15 +214,16 @@ moe_status_t ffn_launch(const moe_dims_t* d, const moe_weights_t* w,
 moe_status_t router_logits_launch(const moe_dims_t* d, const uint16_t* x,
                                   const float* w_router,
                                   const float* offset, float* logits,
-                                  uint16_t* w_split, DevStatus* st,
-                                  cudaStream_t s) {
+                                  uint16_t* w_split, float* partial,
+                                  DevStatus* st, cudaStream_t s) {
   if (moe::router_tile_n(d->E) == 0)
     return cuda_ok(moe::launch_router_logits(x, w_router, offset, logits,
                                              d->T, d->H, d->E, s));
   MOE_TRY(cuda_ok(moe::launch_split_router_weight(w_router, d->E, d->H,
                                                   w_split, s)));
   return static_cast<moe_status_t>(moe::launch_router_logits_tc(
-      x, w_split, offset, logits, d->T, d->H, d->E, st, g_wait_limit_ns, s));
+      x, w_split, offset, logits, partial, d->T, d->H, d->E, st,
+      g_wait_limit_ns, s));
 }
 
 }  // namespace
@@ -291,9 +296,10 @@ moe_status_t moe_router_logits(const moe_dims_t* d, const uint16_t* x,
   MOE_TRY(check_ws(d, MOE_WS_ROUTER_LOGITS, ws, ws_bytes));
   if (d->T == 0) return MOE_OK;
   const Layout L = layout(d, MOE_WS_ROUTER_LOGITS);
-  return router_logits_launch(d, x, w_router, router_offset, logits,
-                              at<uint16_t>(ws, L.w_split),
-                              at<DevStatus>(ws, 0), cs(stream));
+  return router_logits_launch(
+      d, x, w_router, router_offset, logits, at<uint16_t>(ws, L.w_split),
+      L.r_partial ? at<float>(ws, L.r_partial) : nullptr,
+      at<DevStatus>(ws, 0), cs(stream));
 }
 
 moe_status_t moe_route(const moe_dims_t* d, const float* logits,
@@ -471,8 +477,10 @@ moe_status_t moe_forward(const moe_dims_t* d, const moe_weights_t* w,
   uint16_t* ys = at<uint16_t>(ws, L.ys);
 
   prof_mark(0, s);
-  MOE_TRY(router_logits_launch(d, x, w->w_router, w->router_offset, logits,
-                               at<uint16_t>(ws, L.w_split), st, s));
+  MOE_TRY(router_logits_launch(
+      d, x, w->w_router, w->router_offset, logits,
+      at<uint16_t>(ws, L.w_split),
+      L.r_partial ? at<float>(ws, L.r_partial) : nullptr, st, s));
   prof_mark(1, s);
   MOE_TRY(cuda_ok(moe::launch_route(logits, bias, T, E, d->n_group,
                                     d->topk_group, K, idx, gate, bc, s)));
