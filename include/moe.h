@@ -232,7 +232,9 @@ moe_status_t moe_bias_update(const moe_dims_t* d, const int32_t* counts,
 /* The whole layer forward in one call: router logits, routing, dispatch,
  * expert FFNs, combine, and -- if update_bias != 0 -- the bias step on this
  * batch's load (applied after routing, so this call routes with the bias it
- * was given).
+ * was given).  It allocates nothing and never synchronises, so a step can be
+ * captured into a CUDA graph and replayed (the tests capture it after one
+ * ordinary call on the device, and check the replay bit for bit).
  *   x [T, H] bf16 in; bias [E] fp32 in (in/out when update_bias);
  *   out [T, H] bf16 out.
  *   Optional outputs (NULL = not written): logits_out [T, E] fp32,

@@ -172,3 +172,40 @@ def test_layer_v3_skewed_32768_tokens(v3_weights):
     g = _sampled_v3_check(cfg, v3_weights, n_sample=4)
     c = g["counts"]
     assert c.max() > 4 * c.mean() and c.sum() == cfg.T * cfg.topk
+
+
+def test_forward_replays_from_a_cuda_graph():
+    """moe_forward neither synchronises nor allocates, so a whole layer
+    step can be captured once into a CUDA graph and replayed; the replay's
+    output and bias trajectory equal eager calls bit for bit."""
+    cfg = inputs.custom_config("graph", 950, T=300, H=256, E=16, n_group=4,
+                               topk_group=2, topk=4, I=128, I_shared=64,
+                               router_sigma=0.05)
+    w, W = host_weights(cfg)
+    d = ops.dims_of(cfg)
+    x = dev(w["x"])
+    outs = {}
+    for mode in ("eager", "graph"):
+        bias = dev(w["bias"])
+        out = torch.zeros((cfg.T, cfg.H), dtype=torch.int16, device="cuda")
+        ws = ops.workspace(d, ops.MOE_WS_FORWARD)
+        ops.moe_forward(d, W, x, bias, out, ws, update_bias=True)  # warm-up
+        torch.cuda.synchronize()
+        if mode == "eager":
+            for _ in range(3):
+                ops.moe_forward(d, W, x, bias, out, ws, update_bias=True)
+        else:
+            side = torch.cuda.Stream()
+            side.wait_stream(torch.cuda.current_stream())
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(side):
+                with torch.cuda.graph(g, stream=side):
+                    ops.moe_forward(d, W, x, bias, out, ws, update_bias=True)
+            torch.cuda.current_stream().wait_stream(side)
+            for _ in range(3):
+                g.replay()
+        torch.cuda.synchronize()
+        assert ops.moe_get_device_error(ws) == 0
+        outs[mode] = (host(out), host(bias))
+    assert np.array_equal(outs["eager"][0], outs["graph"][0])
+    assert np.array_equal(f32_bits(outs["eager"][1]), f32_bits(outs["graph"][1]))
