@@ -1,0 +1,87 @@
+"""Failure detection on the GPU without a fault.
+
+Every wait of the tensor-core kernels is bounded.  Here the bound is made
+shorter than any TMA copy takes (1 ns), so the first wait that is not
+already satisfied runs out: the kernel records MOE_ERR_TIMEOUT in the
+workspace status word, raises its abort flag, drains its in-flight copies
+and MMAs with their own bounded waits, frees tensor memory and returns.
+The host reads the status, restores the default bound, and the same
+context then computes correct results."""
+import numpy as np
+import pytest
+import torch
+
+from deepseekmoe_routing_expert_moe_b300 import inputs, ops
+from oracle import moe_oracle as O
+
+from gpu_helpers import bf16_dev_to_f32, dev
+
+pytestmark = pytest.mark.gpu
+
+TIMEOUT = ops.STATUS_CODES["MOE_ERR_TIMEOUT"]
+
+
+def _ffn_call(cfg):
+    d = ops.dims_of(cfg)
+    T, K, H, E = cfg.T, cfg.topk, cfg.H, cfg.E
+    x = inputs.x_tokens(cfg)
+    z = O.router_logits(inputs.bf16_bits_to_f32(x), inputs.router_weight(cfg))
+    idx = O.route(z, inputs.bias(cfg), cfg.n_group, cfg.topk_group,
+                  cfg.topk)["idx"]
+    p = O.permutation(idx, E)
+    w = inputs.layer_inputs(cfg)
+    W = ops.Weights(dev(w["w_router"]), dev(w["w1"]), dev(w["w3"]),
+                    dev(w["w2"]), dev(w["ws1"]), dev(w["ws3"]), dev(w["ws2"]))
+    args = (dev(x[p["src_row"] // K]), dev(x), dev(p["offsets"]))
+
+    def run():
+        yp = torch.zeros((T * K, H), dtype=torch.int16, device="cuda")
+        ys = torch.zeros((T, H), dtype=torch.int16, device="cuda")
+        ws = ops.workspace(d, ops.MOE_WS_EXPERT_FFN)
+        ops.moe_expert_ffn(d, W, *args, yp, ys, ws)
+        return ops.moe_get_device_error(ws), yp, ys
+    return run
+
+
+def test_expert_ffn_wait_runs_out_then_context_recovers():
+    cfg = inputs.custom_config("timeout", 960, T=300, H=512, E=8, n_group=4,
+                               topk_group=2, topk=2, I=256, I_shared=128,
+                               router_sigma=0.05)
+    run = _ffn_call(cfg)
+    code, _, _ = run()                    # reference, default bound
+    assert code == 0
+    _, yp_ref, ys_ref = run()
+    try:
+        ops.moe_set_wait_timeout_ns(1)
+        for _ in range(2):                # twice: each launch recovers
+            code, _, _ = run()
+            assert code == TIMEOUT
+    finally:
+        ops.moe_set_wait_timeout_ns(0)    # back to the default bound
+    code, yp, ys = run()
+    assert code == 0
+    assert torch.equal(yp, yp_ref) and torch.equal(ys, ys_ref)
+    assert np.isfinite(bf16_dev_to_f32(yp)).all()
+
+
+def test_router_gemm_wait_runs_out_then_context_recovers():
+    cfg = inputs.CONFIGS["prefill_v3"]
+    T = 512
+    d = ops.dims_of(cfg, T=T)
+    x = dev(inputs.x_tokens(cfg, T=T))
+    w = dev(inputs.router_weight(cfg))
+    ws = ops.workspace(d, ops.MOE_WS_ROUTER_LOGITS)
+    z_ref = torch.empty((T, cfg.E), dtype=torch.float32, device="cuda")
+    ops.moe_router_logits(d, x, w, z_ref, ws)
+    assert ops.moe_get_device_error(ws) == 0
+    try:
+        ops.moe_set_wait_timeout_ns(1)
+        z = torch.empty_like(z_ref)
+        ops.moe_router_logits(d, x, w, z, ws)
+        assert ops.moe_get_device_error(ws) == TIMEOUT
+    finally:
+        ops.moe_set_wait_timeout_ns(0)
+    z = torch.empty_like(z_ref)
+    ops.moe_router_logits(d, x, w, z, ws)
+    assert ops.moe_get_device_error(ws) == 0
+    assert torch.equal(z, z_ref)
