@@ -128,10 +128,12 @@ size_t moe_workspace_bytes(const moe_dims_t* d, moe_ws_kind_t which);
  * "02 · DeepSeek-V3" §1.3 eq. 15), fp32 accumulation of exact products.
  * x [T, H] bf16, w_router [E, H] fp32, router_offset [E] fp32 or NULL
  * (o = 0) -> logits [T, E] fp32; the offset is added once, in fp32, after
- * the accumulation.  When E % 16
- * == 0 it runs on the tensor cores: W_r is split exactly into three bf16
- * parts (hi + mid + lo == W_r) in the workspace and the three products are
- * accumulated into one fp32 accumulator; otherwise an fp32 SIMT kernel.
+ * the accumulation.  When E % 16 == 0 it runs on the tensor cores: W_r is
+ * split exactly into three bf16 parts (hi + mid + lo == W_r) in the
+ * workspace and the three products are accumulated into one fp32
+ * accumulator; with few 128-token tiles (a decode batch) the sum over H is
+ * split into ranges whose fp32 partial sums, kept in the workspace, are
+ * added in range order (deterministic).  Otherwise an fp32 SIMT kernel.
  * Workspace: MOE_WS_ROUTER_LOGITS. */
 moe_status_t moe_router_logits(const moe_dims_t* d, const uint16_t* x,
                                const float* w_router,
@@ -150,8 +152,9 @@ moe_status_t moe_router_logits(const moe_dims_t* d, const uint16_t* x,
  *                             order (sum to 1)
  *   counts   [E]    int32     out, tokens routed to each expert
  * The fp32 sigmoid is one fixed sequence of correctly rounded operations
- * (Cody-Waite reduction, degree-7 Taylor polynomial, rounded divide), so
- * routing is reproducible bit for bit.  Workspace: MOE_WS_ROUTE. */
+ * (Cody-Waite reduction, degree-7 Taylor polynomial, correctly rounded
+ * reciprocal of 1 + e), so routing is reproducible bit for bit.
+ * Workspace: MOE_WS_ROUTE. */
 moe_status_t moe_route(const moe_dims_t* d, const float* logits,
                        const float* bias, int32_t* topk_idx, float* topk_gate,
                        int32_t* counts, void* ws, size_t ws_bytes,
