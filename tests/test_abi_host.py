@@ -86,6 +86,7 @@ def _route(L, d, ws_bytes=1 << 30, logits=FAKE, ws=FAKE):
     (dict(H=7000), 2),
     (dict(E=96, n_group=8, topk_group=4, topk=8), 2),   # 3 experts per lane
     (dict(gamma=float("nan")), 1),
+    (dict(T=(1 << 31) // 9 + 1), 2),   # T*(topk+1) rows overflow int32
 ])
 def test_route_rejects_bad_dims(L, over, code):
     d = ops.dims(**dict(V3, **over))
@@ -124,6 +125,13 @@ def test_ffn_and_forward_validation(L):
     assert L.moe_permute(ctypes.byref(d), None, FAKE, FAKE, FAKE, FAKE, FAKE,
                          FAKE, 1 << 30, None) == 1
     assert L.moe_get_device_error(None, None) == 1
+    # the optional router offset must be 16-byte aligned too
+    w = ops.MoeWeights(*(FAKE,) * 7, FAKE + 4)
+    assert L.moe_forward(ctypes.byref(d), ctypes.byref(w), FAKE, FAKE, 0,
+                         FAKE, None, None, None, None, None, FAKE, 1 << 40,
+                         None) == 3
+    assert L.moe_router_logits(ctypes.byref(d), FAKE, FAKE, FAKE + 8, FAKE,
+                               FAKE, 1 << 40, None) == 3
 
 
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
