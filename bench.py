@@ -151,6 +151,23 @@ def ncu_traffic(kernel: str, workload: str):
         return None
 
 
+def router_extra_launches(T, H, E):
+    """Launches of the router logits beyond one: the weight split on the
+    tensor-core path, and the partial-sum kernel when the library splits
+    the reduction over H (when the 128-token tiles fill fewer than half of
+    the 148 SMs)."""
+    if E % 16:
+        return 0
+    bn = 64 if E % 64 == 0 else (32 if E % 32 == 0 else 16)
+    units = -(-T // 128) * (E // bn)
+    nkb = H // 64
+    if 2 * units > 148 or nkb // 4 < 2:
+        return 1
+    ks = min(-(-148 // units), nkb // 4)
+    kper = -(-nkb // ks)
+    return 2 if -(-nkb // kper) > 1 else 1
+
+
 # ------------------------------------------------------------ CPU oracle
 def oracle_sample(cfg, n_tokens: int, step: int = 0):
     """Inputs of a bounded sample for the oracle: the first n_tokens of the
@@ -402,8 +419,9 @@ def run_gpu(args, rank, world, local_rank):
                 "overlap": "uploads/downloads on their own streams, "
                            "double-buffered"},
         # router logits are two launches (weight split + GEMM) on the
-        # tensor-core path, i.e. when E % 16 == 0
-        "gpu_launches": (nk + (1 if E % 16 == 0 else 0)) * args.steps,
+        # tensor-core path (E % 16 == 0), three when its k ranges are split
+        # (few 128-token tiles: the partial sums are added by a kernel)
+        "gpu_launches": (nk + router_extra_launches(T, H, E)) * args.steps,
         "clocks": clocks,
         "kernels_ms": kernels,
         "experts_touched": touched,
