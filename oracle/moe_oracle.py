@@ -291,3 +291,50 @@ def bias_update(counts: np.ndarray, bias: np.ndarray, T: int, K: int,
     stats = (float(c.max()) if E else 0.0, float(T * K) / E if E else 0.0,
              float(c.min()) if E else 0.0)
     return nb, stats
+
+
+# --------------------------------------------------------------------------
+# Sequence-wise balance loss (§1.4, eq. 17-20): the small complementary
+# loss kept beside the bias, alpha = 1e-4 for V3.
+# --------------------------------------------------------------------------
+def seq_balance_loss(logits: np.ndarray, seq_len: int, topk: int,
+                     alpha: float = 1e-4):
+    """Forward value of the sequence-wise balance loss, one per sequence.
+
+    The batch's T tokens are cut into sequences of ``seq_len`` consecutive
+    tokens; the last one holds the remainder (READING R16).  For a sequence
+    of T_s tokens and E routed experts:
+      s      = sig32(z)                      the affinity, as in routing
+      s'_t,i = s_t,i / sum_j s_t,j           (eq. 19, normalised affinity)
+      P_i    = (1/T_s) sum_t s'_t,i          (eq. 20)
+      f_i    = E / (topk * T_s) * #{t : i among the topk largest s_t}
+                                             (eq. 18; raw s -- no bias, no
+                                             group limit; ties: lower index)
+      L      = alpha * sum_i f_i P_i         (eq. 17)
+    The top-K decision is taken on the fp32 s (bit-exact on both sides);
+    s', P, f and L are fp64 from those fp32 values.
+
+    Returns dict with counts[n_seq, E] int32 (the indicator sums), f and P
+    [n_seq, E] fp64 and loss[n_seq] fp64."""
+    z = np.asarray(logits, F32)
+    T, E = z.shape
+    assert seq_len >= 1 and 1 <= topk <= E
+    n_seq = -(-T // seq_len)
+    s = sig32(z)
+    top = np.argsort(-s, axis=1, kind="stable")[:, :topk]
+    chosen = np.zeros((T, E), bool)
+    np.put_along_axis(chosen, top, True, axis=1)
+    s64 = s.astype(np.float64)
+    sp = s64 / s64.sum(axis=1, keepdims=True)
+    counts = np.zeros((n_seq, E), np.int32)
+    P = np.zeros((n_seq, E))
+    f = np.zeros((n_seq, E))
+    loss = np.zeros(n_seq)
+    for q in range(n_seq):
+        a, b = q * seq_len, min(T, (q + 1) * seq_len)
+        Ts = b - a
+        counts[q] = chosen[a:b].sum(axis=0)
+        P[q] = sp[a:b].sum(axis=0) / Ts
+        f[q] = E * counts[q].astype(np.float64) / (topk * Ts)
+        loss[q] = alpha * float(np.dot(f[q], P[q]))
+    return dict(counts=counts, P=P, f=f, loss=loss)
