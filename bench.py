@@ -534,7 +534,7 @@ def run_route_gpu(args, rank, world, local_rank):
             "peak": hbm, "unit": "GB/s"}
     roof["frac"] = round(roof["achieved"] / hbm, 4)
     roof["traffic"] = None
-    roof["kernel"] = ("moe_route call (route_tg_kernel + count scan): "
+    roof["kernel"] = ("moe_route call (route_kernel + count scan): "
                       "logits -> idx, gates, counts")
     roof["algorithmic_bytes"] = int(route_bytes)
     roof["peak_source"] = f"{pk_src} (MEASURED_PEAKS.json)"
@@ -593,10 +593,182 @@ def run_route_gpu(args, rank, world, local_rank):
     }
 
 
+def run_balance_gpu(args, rank, world, local_rank):
+    """The sequence-wise balance loss (the complementary loss beside the
+    bias): per step, moe_seq_balance_loss on T=16384 fp32 logits at the V3
+    shape (256 experts, top-8) cut into four 4096-token sequences -> the
+    per-sequence counts, P and loss.  8 rotating logits batches (134 MB,
+    larger than L2), replayed from a CUDA graph like the routing workload."""
+    import torch
+    from deepseekmoe_routing_expert_moe_b300 import inputs, ops
+    from oracle import moe_oracle as O
+    torch.cuda.set_device(local_rank)
+    cfg = inputs.CONFIGS["route_v3"]
+    d = ops.dims_of(cfg)
+    T, E, K, S = cfg.T, cfg.E, cfg.topk, 4096
+    n_seq = -(-T // S)
+    alpha = 1e-4
+    NB = 8
+    wr = torch.from_numpy(inputs.router_weight(cfg)).cuda()
+    zs = []
+    wsl = ops.workspace(d, ops.MOE_WS_ROUTER_LOGITS)
+    for i in range(NB):
+        x = inputs.x_tokens(cfg, step=i + 1000 * rank, device="cuda")
+        z = torch.empty((T, E), dtype=torch.float32, device="cuda")
+        ops.moe_router_logits(d, x, wr, z, wsl)
+        zs.append(z)
+    del wsl
+    counts = torch.empty((n_seq, E), dtype=torch.int32, device="cuda")
+    P = torch.empty((n_seq, E), dtype=torch.float32, device="cuda")
+    loss = torch.empty(n_seq, dtype=torch.float32, device="cuda")
+    ws = ops.workspace(d, ops.MOE_WS_SEQ_BALANCE)
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        ops.moe_seq_balance_loss(d, zs[i % NB], S, alpha, counts, P, loss, ws)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    assert ops.moe_get_device_error(ws) == 0
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g, stream=side):
+            for i in range(NB):
+                step(i)
+    stream.wait_stream(side)
+    reps = max(1, args.steps // NB)
+    for _ in range(max(1, args.warmup // NB)):
+        g.replay()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(gpu_index_for_smi(local_rank)) as clk:
+        torch.cuda.synchronize()
+        ev0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    ms = ev0.elapsed_time(ev1)
+    args.steps = reps * NB
+    # algorithmic bytes: the logits read once, the per-sequence counts, P
+    # and loss written (the s' / flag rows the kernels pass between their
+    # passes are this implementation's own traffic, 10 bytes per logit)
+    alg = T * E * 4 + n_seq * E * 8 + n_seq * 4
+    pk, pk_src = peaks()
+    hbm = float(pk["hbm_gbs"])
+    roof = {"bound": "hbm",
+            "achieved": round(alg * args.steps / (ms / 1e3) / 1e9, 1),
+            "peak": hbm, "unit": "GB/s"}
+    roof["frac"] = round(roof["achieved"] / hbm, 4)
+    roof["traffic"] = None
+    roof["kernel"] = ("moe_seq_balance_loss call (balance_token_kernel + "
+                      "balance_seq_kernel + balance_loss_kernel)")
+    roof["algorithmic_bytes"] = int(alg)
+    roof["peak_source"] = f"{pk_src} (MEASURED_PEAKS.json)"
+    # end to end: logits uploaded from pinned memory, the per-sequence
+    # losses read back, every step
+    zh = [torch.empty((T, E), dtype=torch.float32).pin_memory()
+          for _ in range(2)]
+    for i in range(2):
+        zh[i].copy_(zs[i].cpu())
+    lh = torch.empty(n_seq, dtype=torch.float32).pin_memory()
+    zd = torch.empty((T, E), dtype=torch.float32, device="cuda")
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        zd.copy_(zh[i % 2], non_blocking=True)
+        ops.moe_seq_balance_loss(d, zd, S, alpha, counts, P, loss, ws)
+        lh.copy_(loss, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    assert ops.moe_get_device_error(ws) == 0
+    res = {
+        "metric": "tokens/s through the sequence-wise balance loss (eq. "
+                  "17-20) at the V3 shape on 1 B300; % of HBM roofline",
+        "value": round(T * args.steps / (ms / 1e3), 1), "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms / args.steps, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic, seeded (logits from x ~N(0,1), W_router "
+                "~N(0,0.006))",
+        "config": {"workload": f"balance_v3: sequence-wise balance loss, "
+                               f"T={T} as {n_seq} sequences of {S}, E={E}, "
+                               f"top-{K}, alpha={alpha}",
+                   "T": T, "E": E, "topk": K, "seq_len": S,
+                   "l2": "8 rotating logits batches, 134 MB > L2"},
+        "roofline": roof,
+        "e2e": {"value": round(T * args.steps / (e2e_ms / 1e3), 1),
+                "unit": "tokens/s", "h2d_bytes_per_step": T * E * 4,
+                "d2h_bytes_per_step": n_seq * 4},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clk.summary(),
+        "impl": "b300",
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        zc = zs[0][:S].cpu().numpy()
+        O.seq_balance_loss(zc, S, K, alpha)
+        t0 = time.perf_counter()
+        reps_cpu = 0
+        while time.perf_counter() - t0 < 10.0:
+            O.seq_balance_loss(zc, S, K, alpha)
+            reps_cpu += 1
+        dt = time.perf_counter() - t0
+        res["cpu_baseline"] = {
+            "value": round(S * reps_cpu / dt, 1), "unit": "tokens/s",
+            "cores": blas_threads(), "kind": "oracle",
+            "sample": f"one {S}-token sequence of the first logits batch "
+                      f"through the numpy oracle, repeated for ~10 s"}
+    return res
+
+
+def run_balance_reference(args):
+    """Oracle arm of balance_v3: one 4096-token sequence of V3-shaped
+    logits per step through the oracle's balance loss."""
+    from deepseekmoe_routing_expert_moe_b300 import inputs
+    from oracle import moe_oracle as O
+    cfg = inputs.CONFIGS["route_v3"]
+    S = 4096
+    z = inputs.random_logits(cfg, T=S)
+    for _ in range(args.warmup):
+        O.seq_balance_loss(z, S, cfg.topk)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        O.seq_balance_loss(z, S, cfg.topk)
+    tot = time.perf_counter() - t0
+    v = S * args.steps / tot
+    sample = f"one {S}-token sequence per step through the numpy oracle"
+    return {
+        "metric": "tokens/s through the sequence-wise balance loss (eq. "
+                  "17-20) at the V3 shape; oracle on the host cores",
+        "value": round(v, 1), "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(tot / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic, seeded",
+        "config": {"workload": f"balance_v3: sequence-wise balance loss, "
+                               f"one sequence of {S}, E={cfg.E}, "
+                               f"top-{cfg.topk}"},
+        "impl": "reference",
+        "cpu_baseline": {"value": round(v, 1), "unit": "tokens/s",
+                         "cores": blas_threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(v, 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
 def run_reference(args):
     """The oracle arm: the CPU oracle as it stands, per step one bounded
     sample of the workload (the same tokens every step)."""
     from deepseekmoe_routing_expert_moe_b300 import inputs
+    if args.workload == "balance_v3":
+        return run_balance_reference(args)
     cfg = inputs.CONFIGS[args.workload]
     n = args.ref_tokens
     s = oracle_sample(cfg, n)
@@ -631,7 +803,7 @@ def main():
     ap.add_argument("--impl", choices=("b300", "reference"), default="b300")
     ap.add_argument("--workload", default="prefill_v3",
                     choices=("prefill_v3", "decode_v3", "skewed_v3",
-                             "route_v3", "prefill_v3_e32"))
+                             "route_v3", "prefill_v3_e32", "balance_v3"))
     ap.add_argument("--cpu-sample-tokens", type=int, default=4)
     ap.add_argument("--ref-tokens", type=int, default=1)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -655,6 +827,8 @@ def main():
         dist.init_process_group("nccl")
     if args.workload == "route_v3":
         res = run_route_gpu(args, rank, world, local_rank)
+    elif args.workload == "balance_v3":
+        res = run_balance_gpu(args, rank, world, local_rank)
     else:
         res = run_gpu(args, rank, world, local_rank)
     if rank == 0:

@@ -56,6 +56,12 @@ cudaError_t launch_combine(const uint16_t* x, const uint16_t* ys,
 cudaError_t launch_bias_update(const int32_t* counts, float* bias,
                                float* load_stats, int T, int E, int topk,
                                float gamma, cudaStream_t s);
+// sequence-wise balance loss: sp [T, E] fp32 and flags [T, E] u8 are
+// scratch; P and counts [n_seq, E] and loss [n_seq] are written
+cudaError_t launch_seq_balance(const float* logits, int T, int E, int topk,
+                               int seq_len, float alpha, float* sp,
+                               uint8_t* flags, float* P, int32_t* counts,
+                               float* loss, cudaStream_t s);
 
 // ---- grouped_gemm.cu
 struct FfnArgs {

@@ -2,6 +2,7 @@
 // sequences of the DeepSeekMoE layer forward (include/moe.h documents
 // every entry point).  Nothing here allocates device memory or
 // synchronises, except moe_get_device_error().
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -75,6 +76,7 @@ struct Layout {
   size_t xp = 0, h = 0, hs = 0, yp = 0, ys = 0;
   size_t w_split = 0;  // [3, E, H] bf16 parts of the router weight
   size_t r_partial = 0;  // [ksplit, T, E] fp32 partial router sums
+  size_t bal_sp = 0, bal_flags = 0;  // [T, E] fp32 s', [T, E] u8 top-K flags
   size_t total = 0;
 };
 
@@ -115,7 +117,14 @@ Layout layout(const moe_dims_t* d, moe_ws_kind_t which) {
     const size_t ks = moe::router_ksplit(d->T, d->H, d->E);
     if (ks > 1) L.r_partial = take(ks * T * E * 4);
   }
+  if (which == MOE_WS_SEQ_BALANCE) {
+    L.bal_sp = take(T * E * 4);
+    L.bal_flags = take(T * E);
+  }
   L.total = o;
+  // one MOE_WS_FORWARD workspace serves every entry point
+  if (which == MOE_WS_FORWARD)
+    L.total = std::max(L.total, layout(d, MOE_WS_SEQ_BALANCE).total);
   return L;
 }
 
@@ -261,7 +270,7 @@ void moe_set_wait_timeout_ns(uint64_t ns) {
 size_t moe_workspace_bytes(const moe_dims_t* d, moe_ws_kind_t which) {
   const bool ffn = which == MOE_WS_EXPERT_FFN || which == MOE_WS_FORWARD;
   if (check_dims(d, ffn) != MOE_OK) return 0;
-  if (which < MOE_WS_ROUTE || which > MOE_WS_ROUTER_LOGITS) return 0;
+  if (which < MOE_WS_ROUTE || which > MOE_WS_SEQ_BALANCE) return 0;
   return layout(d, which).total;
 }
 
@@ -412,6 +421,29 @@ moe_status_t moe_combine(const moe_dims_t* d, const uint16_t* x,
   if (d->T == 0) return MOE_OK;
   return cuda_ok(moe::launch_combine(x, ys, yp, dest, topk_gate, d->T, d->H,
                                      d->topk, out, cs(stream)));
+}
+
+moe_status_t moe_seq_balance_loss(const moe_dims_t* d, const float* logits,
+                                  int32_t seq_len, float alpha,
+                                  int32_t* counts_seq, float* P_seq,
+                                  float* loss, void* ws, size_t ws_bytes,
+                                  moe_stream_t stream) {
+  MOE_TRY(check_dims(d, false));
+  if (seq_len < 1 || !std::isfinite(alpha)) return MOE_ERR_INVALID_ARG;
+  MOE_NEED_T(logits);
+  MOE_NEED_T(counts_seq);
+  MOE_NEED_T(P_seq);
+  MOE_NEED_T(loss);
+  MOE_ALIGN(logits);
+  MOE_ALIGN(counts_seq);
+  MOE_ALIGN(P_seq);
+  MOE_ALIGN(loss);
+  MOE_TRY(check_ws(d, MOE_WS_SEQ_BALANCE, ws, ws_bytes));
+  if (d->T == 0) return MOE_OK;
+  const Layout L = layout(d, MOE_WS_SEQ_BALANCE);
+  return cuda_ok(moe::launch_seq_balance(
+      logits, d->T, d->E, d->topk, seq_len, alpha, at<float>(ws, L.bal_sp),
+      at<uint8_t>(ws, L.bal_flags), P_seq, counts_seq, loss, cs(stream)));
 }
 
 moe_status_t moe_bias_update(const moe_dims_t* d, const int32_t* counts,

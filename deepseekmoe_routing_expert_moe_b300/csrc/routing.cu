@@ -321,6 +321,191 @@ __global__ void __launch_bounds__(WARPS * 32)
     block_counts[(size_t)blockIdx.x * E + i] = cnt[i];
 }
 
+// ===================================================================
+// Sequence-wise balance loss ("02 · DeepSeek-V3" §1.4, eq. 17-20), three
+// deterministic passes:
+//   1. one warp per token: s = sigmoid(z) (the routing sigmoid, so the
+//      top-K decision matches the oracle bit for bit), den = sum_j s_j
+//      (lane-local in expert order, then an xor butterfly, so every lane
+//      holds the same sum), s' = s / den, and the raw top-K of s over all
+//      experts (no bias, no group limit; ties: lower index).  Writes s'
+//      [T, E] fp32 and the top-K flags [T, E] u8 to the workspace.
+//   2. one CTA per (sequence, 32 experts): 32 row ranges of the sequence
+//      summed per expert in token order, then the 32 partial sums in range
+//      order: P_i = (sum_t s'_{t,i}) / T_s and c_i = sum_t flag_{t,i}.
+//   3. one CTA per sequence: f_i = E c_i / (K T_s), L = alpha sum_i f_i P_i
+//      (xor butterfly within a warp, warps added in order).
+// ===================================================================
+constexpr int kBalTokensPerBlock = 64;
+
+template <int EPL>
+__device__ __forceinline__ void store_row(float* __restrict__ p,
+                                          const float (&v)[EPL]) {
+  if constexpr (EPL % 4 == 0) {
+#pragma unroll
+    for (int j = 0; j < EPL; j += 4)
+      *reinterpret_cast<float4*>(p + j) =
+          make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+  } else if constexpr (EPL == 2) {
+    *reinterpret_cast<float2*>(p) = make_float2(v[0], v[1]);
+  } else {
+    p[0] = v[0];
+  }
+}
+
+// flag byte j = bit j of `pick`
+template <int EPL>
+__device__ __forceinline__ void store_flags(uint8_t* __restrict__ p,
+                                            uint32_t pick) {
+  if constexpr (EPL % 4 == 0) {
+#pragma unroll
+    for (int j = 0; j < EPL; j += 4)
+      *reinterpret_cast<uint32_t*>(p + j) =
+          ((pick >> j) & 1u) | (((pick >> (j + 1)) & 1u) << 8) |
+          (((pick >> (j + 2)) & 1u) << 16) | (((pick >> (j + 3)) & 1u) << 24);
+  } else {
+#pragma unroll
+    for (int j = 0; j < EPL; ++j) p[j] = (uint8_t)((pick >> j) & 1u);
+  }
+}
+
+template <int EPL, int WARPS>
+__global__ void __launch_bounds__(WARPS * 32)
+    balance_token_kernel(const float* __restrict__ logits, int T, int E,
+                         int K, float* __restrict__ sp,
+                         uint8_t* __restrict__ flags) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const bool active = lane < E / EPL;
+  const int tok0 = blockIdx.x * kBalTokensPerBlock;
+  for (int tt = warp; tt < kBalTokensPerBlock; tt += WARPS) {
+    const int t = tok0 + tt;
+    if (t >= T) break;
+    float s[EPL];
+    if (active) {
+      load_row<EPL>(logits + (size_t)t * E + lane * EPL, s);
+#pragma unroll
+      for (int j = 0; j < EPL; ++j) s[j] = sigmoid_f32(s[j]);
+    } else {
+#pragma unroll
+      for (int j = 0; j < EPL; ++j) s[j] = 0.f;
+    }
+    float den = 0.f;
+#pragma unroll
+    for (int j = 0; j < EPL; ++j) den = __fadd_rn(den, s[j]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+      den = __fadd_rn(den, __shfl_xor_sync(0xffffffffu, den, off));
+    // raw top-K of s by (s desc, e asc)
+    float cu[EPL];
+#pragma unroll
+    for (int j = 0; j < EPL; ++j) cu[j] = active ? s[j] : -INFINITY;
+    uint32_t pick = 0;
+    for (int k = 0; k < K; ++k) {
+      float bv = -INFINITY;
+      int bj = 0;
+#pragma unroll
+      for (int j = 0; j < EPL; ++j) {
+        if (cu[j] > bv) {
+          bv = cu[j];
+          bj = j;
+        }
+      }
+      const uint32_t key = f32_order_key(bv);
+      const uint32_t kmax = __reduce_max_sync(0xffffffffu, key);
+      const int cand = (key == kmax && bv != -INFINITY) ? lane * EPL + bj
+                                                        : INT_MAX;
+      const int e = __reduce_min_sync(0xffffffffu, cand);
+      if (e == INT_MAX) break;  // fewer than K finite scores: cannot happen
+      if (lane == e / EPL) {
+        const int oj = e - lane * EPL;
+#pragma unroll
+        for (int j = 0; j < EPL; ++j) {
+          if (j == oj) {
+            cu[j] = -INFINITY;
+            pick |= 1u << j;
+          }
+        }
+      }
+    }
+    if (active) {
+      float o[EPL];
+#pragma unroll
+      for (int j = 0; j < EPL; ++j) o[j] = __fdiv_rn(s[j], den);
+      store_row<EPL>(sp + (size_t)t * E + lane * EPL, o);
+      store_flags<EPL>(flags + (size_t)t * E + lane * EPL, pick);
+    }
+  }
+}
+
+// tokens [a, b) of sequence q
+__device__ __forceinline__ void seq_range(int q, int S, int T, int& a,
+                                          int& b) {
+  const long long a64 = (long long)q * S;
+  a = (int)a64;
+  b = (int)min((long long)T, a64 + S);
+}
+
+__global__ void __launch_bounds__(1024)
+    balance_seq_kernel(const float* __restrict__ sp,
+                       const uint8_t* __restrict__ flags, int T, int E, int S,
+                       float* __restrict__ P, int32_t* __restrict__ counts) {
+  __shared__ float ps[32][33];
+  __shared__ int pc[32][33];
+  const int c = threadIdx.x & 31, r = threadIdx.x >> 5;
+  const int q = blockIdx.x, e = blockIdx.y * 32 + c;
+  int a, b;
+  seq_range(q, S, T, a, b);
+  const int Ts = b - a, per = (Ts + 31) / 32;
+  const int t0 = a + min(Ts, r * per), t1 = a + min(Ts, (r + 1) * per);
+  float sum = 0.f;
+  int n = 0;
+  if (e < E) {
+#pragma unroll 4
+    for (int t = t0; t < t1; ++t) {
+      sum = __fadd_rn(sum, sp[(size_t)t * E + e]);
+      n += flags[(size_t)t * E + e];
+    }
+  }
+  ps[r][c] = sum;
+  pc[r][c] = n;
+  __syncthreads();
+  if (r != 0 || e >= E) return;
+  float tot = 0.f;
+  int nt = 0;
+  for (int i = 0; i < 32; ++i) {
+    tot = __fadd_rn(tot, ps[i][c]);
+    nt += pc[i][c];
+  }
+  P[(size_t)q * E + e] = __fdiv_rn(tot, (float)Ts);
+  counts[(size_t)q * E + e] = nt;
+}
+
+__global__ void __launch_bounds__(1024)
+    balance_loss_kernel(const float* __restrict__ P,
+                        const int32_t* __restrict__ counts, int T, int E,
+                        int K, int S, float alpha, float* __restrict__ loss) {
+  __shared__ float wsum[32];
+  const int e = threadIdx.x, lane = e & 31, warp = e >> 5, q = blockIdx.x;
+  int a, b;
+  seq_range(q, S, T, a, b);
+  float term = 0.f;
+  if (e < E) {
+    const float f = __fdiv_rn(
+        __fmul_rn((float)E, (float)counts[(size_t)q * E + e]),
+        (float)(K * (b - a)));
+    term = __fmul_rn(f, P[(size_t)q * E + e]);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1)
+    term = __fadd_rn(term, __shfl_xor_sync(0xffffffffu, term, off));
+  if (lane == 0) wsum[warp] = term;
+  __syncthreads();
+  if (e != 0) return;
+  float tot = 0.f;
+  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) tot = __fadd_rn(tot, wsum[w]);
+  loss[q] = __fmul_rn(alpha, tot);
+}
+
 // histogram of an existing topk_idx over the same token blocks
 __global__ void __launch_bounds__(256)
     block_counts_kernel(const int32_t* __restrict__ topk_idx, int T, int E,
@@ -683,6 +868,37 @@ cudaError_t launch_route(const float* logits, const float* bias, int T, int E,
       return cudaErrorInvalidValue;
   }
 #undef MOE_ROUTE_CASE
+  return cudaGetLastError();
+}
+
+cudaError_t launch_seq_balance(const float* logits, int T, int E, int topk,
+                               int seq_len, float alpha, float* sp,
+                               uint8_t* flags, float* P, int32_t* counts,
+                               float* loss, cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  const int epl = E <= 32 ? 1 : E / 32;
+  const int nblk = (T + kBalTokensPerBlock - 1) / kBalTokensPerBlock;
+#define MOE_BAL_CASE(N)                                                   \
+  case N:                                                                 \
+    balance_token_kernel<N, 16><<<nblk, 16 * 32, 0, s>>>(logits, T, E,    \
+                                                         topk, sp, flags); \
+    break;
+  switch (epl) {
+    MOE_BAL_CASE(1)
+    MOE_BAL_CASE(2)
+    MOE_BAL_CASE(4)
+    MOE_BAL_CASE(8)
+    MOE_BAL_CASE(16)
+    MOE_BAL_CASE(32)
+    default:
+      return cudaErrorInvalidValue;
+  }
+#undef MOE_BAL_CASE
+  const int n_seq = (int)(((long long)T + seq_len - 1) / seq_len);
+  balance_seq_kernel<<<dim3(n_seq, (E + 31) / 32), 1024, 0, s>>>(
+      sp, flags, T, E, seq_len, P, counts);
+  balance_loss_kernel<<<n_seq, ((E + 31) / 32) * 32, 0, s>>>(
+      P, counts, T, E, topk, seq_len, alpha, loss);
   return cudaGetLastError();
 }
 

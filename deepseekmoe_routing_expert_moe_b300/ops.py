@@ -17,7 +17,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libmoe.so")
 
 (MOE_WS_ROUTE, MOE_WS_PERMUTE, MOE_WS_EXPERT_FFN, MOE_WS_FORWARD,
- MOE_WS_ROUTER_LOGITS) = 0, 1, 2, 3, 4
+ MOE_WS_ROUTER_LOGITS, MOE_WS_SEQ_BALANCE) = 0, 1, 2, 3, 4, 5
 
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
           3: "MOE_ERR_ALIGNMENT", 4: "MOE_ERR_WORKSPACE", 5: "MOE_ERR_CUDA",
@@ -59,6 +59,8 @@ _SIGS = {
     "moe_expert_ffn": (_I, [_D, _W, _P, _P, _P, _P, _P, _P, _S, _P]),
     "moe_combine": (_I, [_D, _P, _P, _P, _P, _P, _P, _P]),
     "moe_bias_update": (_I, [_D, _P, _P, _P, _P]),
+    "moe_seq_balance_loss": (_I, [_D, _P, ctypes.c_int32, ctypes.c_float, _P,
+                                  _P, _P, _P, _S, _P]),
     "moe_forward": (_I, [_D, _W, _P, _P, _I, _P, _P, _P, _P, _P, _P, _P, _S,
                          _P]),
     "moe_status_string": (ctypes.c_char_p, [_I]),
@@ -197,6 +199,16 @@ def moe_combine(d, x, ys, yp, dest, topk_gate, out, stream=None):
 def moe_bias_update(d, counts, bias, load_stats=None, stream=None):
     _check("moe_bias_update", lib().moe_bias_update(
         ctypes.byref(d), _ptr(counts), _ptr(bias), _ptr(load_stats),
+        _stream(stream)))
+
+
+def moe_seq_balance_loss(d, logits, seq_len, alpha, counts_seq, P_seq, loss,
+                         ws, stream=None):
+    """Per-sequence balance loss: counts_seq [n_seq, E] int32, P_seq
+    [n_seq, E] fp32, loss [n_seq] fp32, n_seq = ceil(T / seq_len)."""
+    _check("moe_seq_balance_loss", lib().moe_seq_balance_loss(
+        ctypes.byref(d), _ptr(logits), int(seq_len), float(alpha),
+        _ptr(counts_seq), _ptr(P_seq), _ptr(loss), _ptr(ws), ws.numel(),
         _stream(stream)))
 
 

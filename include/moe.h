@@ -115,7 +115,8 @@ typedef enum {
   MOE_WS_PERMUTE = 1,
   MOE_WS_EXPERT_FFN = 2,
   MOE_WS_FORWARD = 3,
-  MOE_WS_ROUTER_LOGITS = 4
+  MOE_WS_ROUTER_LOGITS = 4,
+  MOE_WS_SEQ_BALANCE = 5
 } moe_ws_kind_t;
 
 /* Bytes of device workspace `which` needs for dims `d` (0 if d is invalid).
@@ -231,6 +232,30 @@ moe_status_t moe_combine(const moe_dims_t* d, const uint16_t* x,
 moe_status_t moe_bias_update(const moe_dims_t* d, const int32_t* counts,
                              float* bias, float* load_stats,
                              moe_stream_t stream);
+
+/* Sequence-wise balance loss, forward value ("02 · DeepSeek-V3" §1.4,
+ * eq. 17-20: the small complementary loss kept beside the bias, alpha =
+ * 1e-4 for V3).  The T tokens are cut into sequences of seq_len
+ * consecutive tokens (the last one holds the remainder), n_seq =
+ * ceil(T / seq_len).  For a sequence of T_s tokens:
+ *   s'_{t,i} = s_{t,i} / sum_j s_{t,j}    (s = the routing sigmoid of z)
+ *   P_i = (1/T_s) sum_t s'_{t,i}
+ *   c_i = #{t : i is among the topk largest s_{t,.}} -- the raw affinity
+ *         over all E experts: no bias, no group limit (ties: lower index)
+ *   f_i = E c_i / (topk T_s),   L = alpha sum_i f_i P_i
+ *   logits     [T, E]      fp32 in
+ *   counts_seq [n_seq, E]  int32 out, c_i per sequence (exact)
+ *   P_seq      [n_seq, E]  fp32  out
+ *   loss       [n_seq]     fp32  out
+ * fp32 arithmetic in a fixed order (per token: lane partial sums, then a
+ * butterfly; per sequence: 32 token ranges, then the ranges in order).
+ * seq_len < 1 or a non-finite alpha: MOE_ERR_INVALID_ARG.  n_group and
+ * topk_group are validated but not used.  Workspace: MOE_WS_SEQ_BALANCE. */
+moe_status_t moe_seq_balance_loss(const moe_dims_t* d, const float* logits,
+                                  int32_t seq_len, float alpha,
+                                  int32_t* counts_seq, float* P_seq,
+                                  float* loss, void* ws, size_t ws_bytes,
+                                  moe_stream_t stream);
 
 /* The whole layer forward in one call: router logits, routing, dispatch,
  * expert FFNs, combine, and -- if update_bias != 0 -- the bias step on this

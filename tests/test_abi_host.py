@@ -134,6 +134,39 @@ def test_ffn_and_forward_validation(L):
                                FAKE, 1 << 40, None) == 3
 
 
+def _balance(L, d, seq_len=4096, alpha=1e-4, logits=FAKE, out=FAKE,
+             ws=FAKE, ws_bytes=1 << 30):
+    return L.moe_seq_balance_loss(ctypes.byref(d), logits, seq_len, alpha,
+                                  out, FAKE, FAKE, ws, ws_bytes, None)
+
+
+def test_seq_balance_validation_and_workspace(L):
+    d = ops.dims(**V3)
+    need = ops.workspace_bytes(d, ops.MOE_WS_SEQ_BALANCE)
+    # s' (fp32) and the top-K flags (u8) for every token and expert
+    assert need >= 4096 * 256 * 5
+    assert need <= ops.workspace_bytes(d, ops.MOE_WS_FORWARD)
+    # a forward workspace covers it even where the layer's own buffers are
+    # small next to [T, E] (many experts, narrow hidden size)
+    wide = ops.dims(**dict(V3, H=64, E=1024, n_group=32, topk=1,
+                           topk_group=1, I=64, I_shared=64))
+    assert 0 < ops.workspace_bytes(wide, ops.MOE_WS_SEQ_BALANCE) <= \
+        ops.workspace_bytes(wide, ops.MOE_WS_FORWARD)
+    assert _balance(L, d, seq_len=0) == 1
+    assert _balance(L, d, seq_len=-5) == 1
+    assert _balance(L, d, alpha=float("nan")) == 1
+    assert _balance(L, d, alpha=float("inf")) == 1
+    assert _balance(L, d, logits=None) == 1
+    assert _balance(L, d, out=None) == 1
+    assert _balance(L, d, out=FAKE + 4) == 3
+    assert _balance(L, d, ws_bytes=need - 1) == 4
+    assert _balance(L, ops.dims(**dict(V3, E=255))) == 1
+    # no tokens: nothing to compute, nothing launched, NULL tensors allowed
+    d0 = ops.dims(**dict(V3, T=0))
+    assert L.moe_seq_balance_loss(ctypes.byref(d0), None, 7, 1e-4, None, None,
+                                  None, FAKE, 1 << 20, None) == 0
+
+
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(ops, "LIB_PATH", str(tmp_path / "missing.so"))
     monkeypatch.setattr(ops, "_lib", None)
