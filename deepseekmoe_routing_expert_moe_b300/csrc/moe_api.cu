@@ -77,6 +77,7 @@ struct Layout {
   size_t w_split = 0;  // [3, E, H] bf16 parts of the router weight
   size_t r_partial = 0;  // [ksplit, T, E] fp32 partial router sums
   size_t bal_sp = 0, bal_flags = 0;  // [T, E] fp32 s', [T, E] u8 top-K flags
+  size_t bal_pP = 0, bal_pc = 0;     // per-split partial sums (bounded)
   size_t total = 0;
 };
 
@@ -120,6 +121,8 @@ Layout layout(const moe_dims_t* d, moe_ws_kind_t which) {
   if (which == MOE_WS_SEQ_BALANCE) {
     L.bal_sp = take(T * E * 4);
     L.bal_flags = take(T * E);
+    L.bal_pP = take(moe::kBalPartialElems * 4);
+    L.bal_pc = take(moe::kBalPartialElems * 4);
   }
   L.total = o;
   // one MOE_WS_FORWARD workspace serves every entry point
@@ -441,9 +444,14 @@ moe_status_t moe_seq_balance_loss(const moe_dims_t* d, const float* logits,
   MOE_TRY(check_ws(d, MOE_WS_SEQ_BALANCE, ws, ws_bytes));
   if (d->T == 0) return MOE_OK;
   const Layout L = layout(d, MOE_WS_SEQ_BALANCE);
+  const long long n_seq = ((long long)d->T + seq_len - 1) / seq_len;
+  const int rs = moe::seq_balance_splits(d->T, d->E, seq_len);
+  if (rs > 1 && n_seq * rs * d->E > moe::kBalPartialElems)
+    return MOE_ERR_UNSUPPORTED;  // cannot happen: the split rule bounds it
   return cuda_ok(moe::launch_seq_balance(
       logits, d->T, d->E, d->topk, seq_len, alpha, at<float>(ws, L.bal_sp),
-      at<uint8_t>(ws, L.bal_flags), P_seq, counts_seq, loss, cs(stream)));
+      at<uint8_t>(ws, L.bal_flags), P_seq, counts_seq,
+      at<float>(ws, L.bal_pP), at<int32_t>(ws, L.bal_pc), loss, cs(stream)));
 }
 
 moe_status_t moe_bias_update(const moe_dims_t* d, const int32_t* counts,

@@ -327,14 +327,19 @@ __global__ void __launch_bounds__(WARPS * 32)
 //   1. one warp per token: s = sigmoid(z) (the routing sigmoid, so the
 //      top-K decision matches the oracle bit for bit), den = sum_j s_j
 //      (lane-local in expert order, then an xor butterfly, so every lane
-//      holds the same sum), s' = s / den, and the raw top-K of s over all
-//      experts (no bias, no group limit; ties: lower index).  Writes s'
-//      [T, E] fp32 and the top-K flags [T, E] u8 to the workspace.
-//   2. one CTA per (sequence, 32 experts): 32 row ranges of the sequence
-//      summed per expert in token order, then the 32 partial sums in range
-//      order: P_i = (sum_t s'_{t,i}) / T_s and c_i = sum_t flag_{t,i}.
-//   3. one CTA per sequence: f_i = E c_i / (K T_s), L = alpha sum_i f_i P_i
-//      (xor butterfly within a warp, warps added in order).
+//      holds the same sum), s' = s * (1/den) (one correctly rounded
+//      reciprocal per token), and the raw top-K of s over all experts (no
+//      bias, no group limit; ties: lower index).  Writes s' [T, E] fp32
+//      and the top-K flags [T, E] u8 to the workspace.
+//   2. one CTA per (sequence, 32 experts, row split): the split's rows are
+//      cut into 32 ranges summed per expert in token order, then the 32
+//      range sums added in order.  With one split per sequence it writes
+//      P_i = (sum_t s'_{t,i}) / T_s and c_i = sum_t flag_{t,i} directly;
+//      with rs > 1 splits (short batches: the grid would not fill the
+//      SMs) it writes per-split partial sums.
+//   3. one CTA per sequence: the rs partial sums added in split order (when
+//      rs > 1), f_i = E c_i / (K T_s), L = alpha sum_i f_i P_i (xor
+//      butterfly within a warp, warps added in order).
 // ===================================================================
 constexpr int kBalTokensPerBlock = 64;
 
@@ -428,9 +433,10 @@ __global__ void __launch_bounds__(WARPS * 32)
       }
     }
     if (active) {
+      const float rden = __frcp_rn(den);
       float o[EPL];
 #pragma unroll
-      for (int j = 0; j < EPL; ++j) o[j] = __fdiv_rn(s[j], den);
+      for (int j = 0; j < EPL; ++j) o[j] = __fmul_rn(s[j], rden);
       store_row<EPL>(sp + (size_t)t * E + lane * EPL, o);
       store_flags<EPL>(flags + (size_t)t * E + lane * EPL, pick);
     }
@@ -445,29 +451,36 @@ __device__ __forceinline__ void seq_range(int q, int S, int T, int& a,
   b = (int)min((long long)T, a64 + S);
 }
 
+// Sums of split j (of rs) of sequence q over 32 experts.  rs == 1: final
+// P and counts; rs > 1: partial sums part_P / part_c [n_seq, rs, E].
 __global__ void __launch_bounds__(1024)
     balance_seq_kernel(const float* __restrict__ sp,
                        const uint8_t* __restrict__ flags, int T, int E, int S,
-                       float* __restrict__ P, int32_t* __restrict__ counts) {
+                       int rs, float* __restrict__ P,
+                       int32_t* __restrict__ counts,
+                       float* __restrict__ part_P,
+                       int32_t* __restrict__ part_c) {
   __shared__ float ps[32][33];
   __shared__ int pc[32][33];
   const int c = threadIdx.x & 31, r = threadIdx.x >> 5;
-  const int q = blockIdx.x, e = blockIdx.y * 32 + c;
+  const int q = blockIdx.x, e = blockIdx.y * 32 + c, j = blockIdx.z;
   int a, b;
   seq_range(q, S, T, a, b);
-  const int Ts = b - a, per = (Ts + 31) / 32;
-  const int t0 = a + min(Ts, r * per), t1 = a + min(Ts, (r + 1) * per);
+  const int Ts = b - a, chunk = (Ts + rs - 1) / rs;
+  const int c0 = min(Ts, j * chunk), c1 = min(Ts, c0 + chunk);
+  const int n = c1 - c0, per = (n + 31) / 32;
+  const int t0 = a + c0 + min(n, r * per), t1 = a + c0 + min(n, (r + 1) * per);
   float sum = 0.f;
-  int n = 0;
+  int cnt = 0;
   if (e < E) {
 #pragma unroll 4
     for (int t = t0; t < t1; ++t) {
       sum = __fadd_rn(sum, sp[(size_t)t * E + e]);
-      n += flags[(size_t)t * E + e];
+      cnt += flags[(size_t)t * E + e];
     }
   }
   ps[r][c] = sum;
-  pc[r][c] = n;
+  pc[r][c] = cnt;
   __syncthreads();
   if (r != 0 || e >= E) return;
   float tot = 0.f;
@@ -476,24 +489,49 @@ __global__ void __launch_bounds__(1024)
     tot = __fadd_rn(tot, ps[i][c]);
     nt += pc[i][c];
   }
-  P[(size_t)q * E + e] = __fdiv_rn(tot, (float)Ts);
-  counts[(size_t)q * E + e] = nt;
+  if (rs == 1) {
+    P[(size_t)q * E + e] = __fdiv_rn(tot, (float)Ts);
+    counts[(size_t)q * E + e] = nt;
+  } else {
+    const size_t o = ((size_t)q * rs + j) * E + e;
+    part_P[o] = tot;
+    part_c[o] = nt;
+  }
 }
 
 __global__ void __launch_bounds__(1024)
-    balance_loss_kernel(const float* __restrict__ P,
-                        const int32_t* __restrict__ counts, int T, int E,
-                        int K, int S, float alpha, float* __restrict__ loss) {
+    balance_loss_kernel(float* __restrict__ P, int32_t* __restrict__ counts,
+                        const float* __restrict__ part_P,
+                        const int32_t* __restrict__ part_c, int rs, int T,
+                        int E, int K, int S, float alpha,
+                        float* __restrict__ loss) {
   __shared__ float wsum[32];
   const int e = threadIdx.x, lane = e & 31, warp = e >> 5, q = blockIdx.x;
   int a, b;
   seq_range(q, S, T, a, b);
   float term = 0.f;
   if (e < E) {
-    const float f = __fdiv_rn(
-        __fmul_rn((float)E, (float)counts[(size_t)q * E + e]),
-        (float)(K * (b - a)));
-    term = __fmul_rn(f, P[(size_t)q * E + e]);
+    const size_t o = (size_t)q * E + e;
+    float Pe;
+    int ce;
+    if (rs == 1) {
+      Pe = P[o];
+      ce = counts[o];
+    } else {
+      float tot = 0.f;
+      ce = 0;
+      for (int j = 0; j < rs; ++j) {
+        const size_t po = ((size_t)q * rs + j) * E + e;
+        tot = __fadd_rn(tot, part_P[po]);
+        ce += part_c[po];
+      }
+      Pe = __fdiv_rn(tot, (float)(b - a));
+      P[o] = Pe;
+      counts[o] = ce;
+    }
+    const float f = __fdiv_rn(__fmul_rn((float)E, (float)ce),
+                              (float)(K * (b - a)));
+    term = __fmul_rn(f, Pe);
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1)
@@ -871,10 +909,23 @@ cudaError_t launch_route(const float* logits, const float* bias, int T, int E,
   return cudaGetLastError();
 }
 
+int seq_balance_splits(int T, int E, int seq_len) {
+  if (T <= 0 || seq_len <= 0) return 1;
+  const long long n_seq = ((long long)T + seq_len - 1) / seq_len;
+  const long long base = n_seq * ((E + 31) / 32);
+  const long long want = 2LL * kBalSplitTarget;
+  if (base >= want) return 1;
+  const int smax = (int)std::min<long long>(seq_len, T);
+  // at least 256 rows (8 per warp) per split
+  const long long cap = std::max(1, (smax + 255) / 256);
+  return (int)std::min<long long>((want + base - 1) / base, cap);
+}
+
 cudaError_t launch_seq_balance(const float* logits, int T, int E, int topk,
                                int seq_len, float alpha, float* sp,
                                uint8_t* flags, float* P, int32_t* counts,
-                               float* loss, cudaStream_t s) {
+                               float* part_P, int32_t* part_c, float* loss,
+                               cudaStream_t s) {
   if (T == 0) return cudaSuccess;
   const int epl = E <= 32 ? 1 : E / 32;
   const int nblk = (T + kBalTokensPerBlock - 1) / kBalTokensPerBlock;
@@ -895,10 +946,11 @@ cudaError_t launch_seq_balance(const float* logits, int T, int E, int topk,
   }
 #undef MOE_BAL_CASE
   const int n_seq = (int)(((long long)T + seq_len - 1) / seq_len);
-  balance_seq_kernel<<<dim3(n_seq, (E + 31) / 32), 1024, 0, s>>>(
-      sp, flags, T, E, seq_len, P, counts);
+  const int rs = seq_balance_splits(T, E, seq_len);
+  balance_seq_kernel<<<dim3(n_seq, (E + 31) / 32, rs), 1024, 0, s>>>(
+      sp, flags, T, E, seq_len, rs, P, counts, part_P, part_c);
   balance_loss_kernel<<<n_seq, ((E + 31) / 32) * 32, 0, s>>>(
-      P, counts, T, E, topk, seq_len, alpha, loss);
+      P, counts, part_P, part_c, rs, T, E, topk, seq_len, alpha, loss);
   return cudaGetLastError();
 }
 

@@ -4,14 +4,17 @@ DeepSeek-V3" §1.4, eq. 17-20), given the same logits.
 The per-sequence top-K counts are integers decided on the bit-exact fp32
 sigmoid: compared exactly.  P and the loss are fp32 sums of positive terms
 whose rounding is bounded by the kernel's fixed order (u = 2^-24):
-  s'   = s / den, den summed in (EPL - 1) lane-local adds + 5 butterfly
-         adds, then one division              -> <= (EPL + 5) u relative
-  P    = ceil(T_s/32) adds inside a token range, 31 adds across the 32
-         ranges, one division                 -> <= (T_s/32 + 33) u more
+  s'   = s * (1/den), den summed in (EPL - 1) lane-local adds + 5
+         butterfly adds, one reciprocal, one multiply
+                                              -> <= (EPL + 7) u relative
+  P    = the sequence cut into rs row splits, each into 32 ranges:
+         ceil(T_s/(32 rs)) adds in a range, 31 across ranges, rs - 1
+         across splits, one division; the split rule (rs <= ceil(S/256))
+         keeps this          -> <= (ceil(S/32) + 33) u more
   loss = f (2 roundings) times P (1), 5 butterfly + up to 31 warp adds,
          times alpha (1)                      -> <= 40 u more
-so P is checked to (EPL + T_s/32 + 40) u and the loss to that + 40 u,
-relative to the oracle's fp64 values."""
+so P is checked to (EPL + ceil(S/32) + 40) u and the loss to that + 40 u,
+relative to the oracle's fp64 values (S = min(seq_len, T))."""
 import numpy as np
 import pytest
 import torch
