@@ -341,7 +341,11 @@ __global__ void __launch_bounds__(WARPS * 32)
 //      rs > 1), f_i = E c_i / (K T_s), L = alpha sum_i f_i P_i (xor
 //      butterfly within a warp, warps added in order).
 // ===================================================================
-constexpr int kBalTokensPerBlock = 64;
+// one token per warp, 8 warps per block: the grid is many small blocks, so
+// the SMs receive nearly equal shares of tokens (64-token blocks left some
+// SMs with two blocks and others with one at T = 16384)
+constexpr int kBalWarps = 8;
+constexpr int kBalTokensPerBlock = kBalWarps;
 
 template <int EPL>
 __device__ __forceinline__ void store_row(float* __restrict__ p,
@@ -520,6 +524,7 @@ __global__ void __launch_bounds__(1024)
     } else {
       float tot = 0.f;
       ce = 0;
+#pragma unroll 8
       for (int j = 0; j < rs; ++j) {
         const size_t po = ((size_t)q * rs + j) * E + e;
         tot = __fadd_rn(tot, part_P[po]);
@@ -931,8 +936,8 @@ cudaError_t launch_seq_balance(const float* logits, int T, int E, int topk,
   const int nblk = (T + kBalTokensPerBlock - 1) / kBalTokensPerBlock;
 #define MOE_BAL_CASE(N)                                                   \
   case N:                                                                 \
-    balance_token_kernel<N, 16><<<nblk, 16 * 32, 0, s>>>(logits, T, E,    \
-                                                         topk, sp, flags); \
+    balance_token_kernel<N, kBalWarps><<<nblk, kBalWarps * 32, 0, s>>>(   \
+        logits, T, E, topk, sp, flags);                                     \
     break;
   switch (epl) {
     MOE_BAL_CASE(1)
