@@ -60,8 +60,8 @@ cudaError_t launch_bias_update(const int32_t* counts, float* bias,
 // scratch, part_P / part_c [n_seq, rs, E] the per-split partial sums (used
 // when seq_balance_splits() > 1; n_seq * rs * E <= kBalPartialElems);
 // P and counts [n_seq, E] and loss [n_seq] are written
-constexpr int kBalSplitTarget = 148;  // aim for 2 x this many pass-2 CTAs
-constexpr long long kBalPartialElems = 4LL * kBalSplitTarget * 32;
+constexpr int kBalSplitTarget = 148;  // split up to 2 x this many CTAs
+constexpr long long kBalPartialElems = 2LL * kBalSplitTarget * 32;
 int seq_balance_splits(int T, int E, int seq_len);
 cudaError_t launch_seq_balance(const float* logits, int T, int E, int topk,
                                int seq_len, float alpha, float* sp,

@@ -921,9 +921,10 @@ int seq_balance_splits(int T, int E, int seq_len) {
   const long long want = 2LL * kBalSplitTarget;
   if (base >= want) return 1;
   const int smax = (int)std::min<long long>(seq_len, T);
-  // at least 256 rows (8 per warp) per split
+  // at least 256 rows (8 per warp) per split; at most `want` CTAs in all
+  // (two 1024-thread CTAs fit an SM: one wave)
   const long long cap = std::max(1, (smax + 255) / 256);
-  return (int)std::min<long long>((want + base - 1) / base, cap);
+  return (int)std::max<long long>(1, std::min<long long>(want / base, cap));
 }
 
 cudaError_t launch_seq_balance(const float* logits, int T, int E, int topk,
