@@ -338,3 +338,113 @@ def seq_balance_loss(logits: np.ndarray, seq_len: int, topk: int,
         f[q] = E * counts[q].astype(np.float64) / (topk * Ts)
         loss[q] = alpha * float(np.dot(f[q], P[q]))
     return dict(counts=counts, P=P, f=f, loss=loss)
+
+
+# --------------------------------------------------------------------------
+# FP8 (E4M3) fine-grained quantization ("02 · DeepSeek-V3" §2, mixed
+# precision): activations grouped in 1 x 128 tiles (one token, 128
+# channels), weights in 128 x 128 blocks, one scale per group from the
+# group's own max |value| taken online, every tensor in E4M3 (4 exponent
+# bits, 3 mantissa bits).
+# --------------------------------------------------------------------------
+E4M3_MAX = 448.0           # 1.75 * 2^8, the largest finite E4M3 value
+E4M3_MIN_NORMAL = 2.0 ** -6
+E4M3_SUB_STEP = 2.0 ** -9  # spacing of the subnormals
+
+
+def e4m3_decode(code: np.ndarray) -> np.ndarray:
+    """Value of each E4M3 code (uint8): sign bit, 4-bit exponent with bias
+    7, 3-bit mantissa; exponent 0 holds the subnormals m/8 * 2^-6; the
+    all-ones pattern (exponent 15, mantissa 7) is NaN; no infinities."""
+    c = np.asarray(code, np.uint8).astype(np.int64)
+    s = np.where(c >> 7, -1.0, 1.0)
+    e = (c >> 3) & 15
+    m = c & 7
+    mag = np.where(e == 0, m / 8.0 * E4M3_MIN_NORMAL,
+                   (1.0 + m / 8.0) * np.exp2(e - 7.0))
+    mag = np.where((e == 15) & (m == 7), np.nan, mag)
+    return s * mag
+
+
+def e4m3_encode(x: np.ndarray) -> np.ndarray:
+    """Round each fp32 value to the nearest E4M3 value, ties to the even
+    mantissa, magnitudes beyond 448 saturated to 448 (READING R19: the
+    "satfinite" conversion); the sign of a zero result is kept.  Finite
+    inputs only."""
+    x = np.asarray(x, F32).astype(np.float64)
+    assert np.all(np.isfinite(x))
+    neg = np.signbit(x)
+    a = np.abs(x)
+    _, k = np.frexp(np.maximum(a, E4M3_MIN_NORMAL))   # a = f 2^k, f in [.5,1)
+    step = np.where(a < E4M3_MIN_NORMAL, E4M3_SUB_STEP, np.exp2(k - 4.0))
+    q = np.minimum(np.rint(a / step) * step, E4M3_MAX)  # rint: half to even
+    # encode the (exactly representable) magnitude q
+    _, kq = np.frexp(np.maximum(q, E4M3_MIN_NORMAL))
+    sub = q < E4M3_MIN_NORMAL
+    ebits = np.where(sub, 0, kq - 1 + 7)
+    mbits = np.where(sub, np.rint(q / E4M3_SUB_STEP),
+                     np.rint(q / np.exp2(kq - 1.0) * 8.0) - 8.0)
+    code = (neg.astype(np.int64) << 7) | (ebits.astype(np.int64) << 3) | \
+        mbits.astype(np.int64)
+    return code.astype(np.uint8)
+
+
+def _group_scale(amax: np.ndarray) -> np.ndarray:
+    """scale = fl32(amax / 448); an all-zero group gets scale 1 (READING
+    R20), so its codes are all zero either way."""
+    amax = np.asarray(amax, F32)
+    return np.where(amax > 0, amax / F32(E4M3_MAX), F32(1.0)).astype(F32)
+
+
+def quantize_1x128(x: np.ndarray):
+    """Activation quantization: x [R, C] fp32 (C % 128 == 0) -> codes
+    [R, C] uint8 and scales [R, C/128] fp32.  Per row and 128-channel tile:
+    amax = max |x|, s = fl32(amax / 448), code = E4M3(fl32(x / s))."""
+    x = np.asarray(x, F32)
+    R, C = x.shape
+    assert C % 128 == 0
+    t = x.reshape(R, C // 128, 128)
+    s = _group_scale(np.abs(t).max(axis=2))
+    q = e4m3_encode((t / s[:, :, None]).astype(F32))
+    return q.reshape(R, C), s
+
+
+def quantize_128x128(w: np.ndarray):
+    """Weight quantization: w [R, C] fp32 (both multiples of 128) -> codes
+    [R, C] uint8 and scales [R/128, C/128] fp32, one scale per 128 x 128
+    block from the block's max |w|."""
+    w = np.asarray(w, F32)
+    R, C = w.shape
+    assert R % 128 == 0 and C % 128 == 0
+    b = w.reshape(R // 128, 128, C // 128, 128)
+    s = _group_scale(np.abs(b).max(axis=(1, 3)))
+    q = e4m3_encode((b / s[:, None, :, None]).astype(F32))
+    return q.reshape(R, C), s
+
+
+def dequantize(q: np.ndarray, s: np.ndarray, rows_per_scale: int):
+    """Exact value of quantized data in fp64: code value x its group's
+    scale (rows_per_scale = 1 for 1x128 tiles, 128 for 128x128 blocks)."""
+    v = e4m3_decode(q)
+    sc = np.repeat(np.repeat(np.asarray(s, np.float64), rows_per_scale,
+                             axis=0), 128, axis=1)
+    return v * sc
+
+
+def fp8_swiglu_ffn(a_q, a_s, w1, w3, w2):
+    """One expert on FP8 inputs (§2 mixed precision on §1.1's SwiGLU):
+    a_q / a_s the 1x128-quantized token rows; w1, w3, w2 each a
+    (codes, scales) pair of 128x128-quantized weights.
+      p, q = A W1^T, A W3^T on the dequantized values (fp64, exact
+             products: the pages' full-precision accumulation)
+      m    = silu(p) * q, rounded to fp32, then 1x128-quantized
+             (READING R21: the down projection's input is FP8 too)
+      y    = M W2^T on the dequantized values (fp64)
+    Returns y (fp64) and the intermediate (codes, scales)."""
+    A = dequantize(a_q, a_s, 1)
+    p = A @ dequantize(*w1, 128).T
+    q = A @ dequantize(*w3, 128).T
+    m = (silu(p) * q).astype(F32)
+    m_q, m_s = quantize_1x128(m)
+    y = dequantize(m_q, m_s, 1) @ dequantize(*w2, 128).T
+    return y, (m_q, m_s)
