@@ -69,6 +69,19 @@ cudaError_t launch_seq_balance(const float* logits, int T, int E, int topk,
                                float* part_P, int32_t* part_c, float* loss,
                                cudaStream_t s);
 
+// ---- fp8.cu
+// 1 x 128 tile quantization of x [R, C] bf16 (C % 128 == 0): codes to q
+// [R, C] and scales to s [R, C/128] when q != NULL; with dest [R, K] != NULL
+// also to the dispatch rows qp[dest[r*K+k]] / sp (bad rows: DEVICE_BOUNDS)
+cudaError_t launch_quant_rows(const uint16_t* x, long long R, int C,
+                              const int32_t* dest, int K, uint8_t* q,
+                              float* s, uint8_t* qp, float* sp,
+                              DevStatus* st, cudaStream_t stream);
+// 128 x 128 block quantization of w [R, C] bf16 (both multiples of 128):
+// codes q [R, C], scales s [R/128, C/128]
+cudaError_t launch_quant_blocks(const uint16_t* w, long long R, int C,
+                                uint8_t* q, float* s, cudaStream_t stream);
+
 // ---- grouped_gemm.cu
 struct FfnArgs {
   int T, H, E, topk, I, I_shared;

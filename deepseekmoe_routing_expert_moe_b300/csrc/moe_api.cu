@@ -454,6 +454,66 @@ moe_status_t moe_seq_balance_loss(const moe_dims_t* d, const float* logits,
       at<float>(ws, L.bal_pP), at<int32_t>(ws, L.bal_pc), loss, cs(stream)));
 }
 
+moe_status_t moe_quantize_fp8_blocks(const uint16_t* w, int64_t rows,
+                                     int64_t cols, uint8_t* q, float* scale,
+                                     moe_stream_t stream) {
+  if (rows < 0 || cols <= 0 || rows % 128 != 0 || cols % 128 != 0)
+    return MOE_ERR_INVALID_ARG;
+  if (rows / 128 > 65535 || cols > (1 << 30)) return MOE_ERR_UNSUPPORTED;
+  if (rows == 0) return MOE_OK;
+  MOE_NEED(w);
+  MOE_NEED(q);
+  MOE_NEED(scale);
+  MOE_ALIGN(w);
+  MOE_ALIGN(q);
+  MOE_ALIGN(scale);
+  return cuda_ok(
+      moe::launch_quant_blocks(w, rows, (int)cols, q, scale, cs(stream)));
+}
+
+moe_status_t moe_quantize_fp8_rows(const uint16_t* x, int64_t rows,
+                                   int64_t cols, uint8_t* q, float* scale,
+                                   moe_stream_t stream) {
+  if (rows < 0 || cols <= 0 || cols % 128 != 0) return MOE_ERR_INVALID_ARG;
+  if (cols > (1 << 30) || rows * (cols / 128) >= (1ll << 40))
+    return MOE_ERR_UNSUPPORTED;
+  if (rows == 0) return MOE_OK;
+  MOE_NEED(x);
+  MOE_NEED(q);
+  MOE_NEED(scale);
+  MOE_ALIGN(x);
+  MOE_ALIGN(q);
+  MOE_ALIGN(scale);
+  return cuda_ok(moe::launch_quant_rows(x, rows, (int)cols, nullptr, 0, q,
+                                        scale, nullptr, nullptr, nullptr,
+                                        cs(stream)));
+}
+
+moe_status_t moe_permute_fp8(const moe_dims_t* d, const uint16_t* x,
+                             const int32_t* dest, uint8_t* xq, float* xs,
+                             uint8_t* xpq, float* xps, void* ws,
+                             size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRY(check_dims(d, false));
+  if (d->H % 128 != 0) return MOE_ERR_UNSUPPORTED;
+  MOE_NEED_T(x);
+  MOE_NEED_T(dest);
+  MOE_NEED_T(xq);
+  MOE_NEED_T(xs);
+  MOE_NEED_T(xpq);
+  MOE_NEED_T(xps);
+  MOE_ALIGN(x);
+  MOE_ALIGN(dest);
+  MOE_ALIGN(xq);
+  MOE_ALIGN(xs);
+  MOE_ALIGN(xpq);
+  MOE_ALIGN(xps);
+  MOE_TRY(check_ws(d, MOE_WS_PERMUTE, ws, ws_bytes));
+  if (d->T == 0) return MOE_OK;
+  return cuda_ok(moe::launch_quant_rows(
+      x, d->T, d->H, dest, d->topk, xq, xs, xpq, xps,
+      at<DevStatus>(ws, 0), cs(stream)));
+}
+
 moe_status_t moe_bias_update(const moe_dims_t* d, const int32_t* counts,
                              float* bias, float* load_stats,
                              moe_stream_t stream) {

@@ -235,12 +235,15 @@ def zipf_preference(cfg: MoEConfig) -> np.ndarray:
 
 
 # --------------------------------------------------------------------- experts
+def expert_matrix(cfg: MoEConfig, name: str, e: int, device=None):
+    """One matrix ("w1", "w3" [I,H] or "w2" [H,I]) of routed expert e."""
+    shape = (cfg.H, cfg.I) if name == "w2" else (cfg.I, cfg.H)
+    return normal_bf16(_key32(cfg, name, e), shape, cfg.w_sigma, device)
+
+
 def expert_weights(cfg: MoEConfig, e: int, device=None):
     """Routed expert e: (w1[I,H], w3[I,H], w2[H,I]) bf16 bits ~ N(0, w_sigma)."""
-    s = cfg.w_sigma
-    return (normal_bf16(_key32(cfg, "w1", e), (cfg.I, cfg.H), s, device),
-            normal_bf16(_key32(cfg, "w3", e), (cfg.I, cfg.H), s, device),
-            normal_bf16(_key32(cfg, "w2", e), (cfg.H, cfg.I), s, device))
+    return tuple(expert_matrix(cfg, n, e, device) for n in ("w1", "w3", "w2"))
 
 
 def shared_weights(cfg: MoEConfig, device=None):

@@ -61,6 +61,11 @@ _SIGS = {
     "moe_bias_update": (_I, [_D, _P, _P, _P, _P]),
     "moe_seq_balance_loss": (_I, [_D, _P, ctypes.c_int32, ctypes.c_float, _P,
                                   _P, _P, _P, _S, _P]),
+    "moe_quantize_fp8_blocks": (_I, [_P, ctypes.c_int64, ctypes.c_int64, _P,
+                                     _P, _P]),
+    "moe_quantize_fp8_rows": (_I, [_P, ctypes.c_int64, ctypes.c_int64, _P,
+                                   _P, _P]),
+    "moe_permute_fp8": (_I, [_D, _P, _P, _P, _P, _P, _P, _P, _S, _P]),
     "moe_forward": (_I, [_D, _W, _P, _P, _I, _P, _P, _P, _P, _P, _P, _P, _S,
                          _P]),
     "moe_status_string": (ctypes.c_char_p, [_I]),
@@ -210,6 +215,26 @@ def moe_seq_balance_loss(d, logits, seq_len, alpha, counts_seq, P_seq, loss,
         ctypes.byref(d), _ptr(logits), int(seq_len), float(alpha),
         _ptr(counts_seq), _ptr(P_seq), _ptr(loss), _ptr(ws), ws.numel(),
         _stream(stream)))
+
+
+def moe_quantize_fp8_blocks(w, q, scale, stream=None):
+    """128 x 128 block E4M3 quantization of a 2-D bf16 (int16) tensor."""
+    rows, cols = w.shape
+    _check("moe_quantize_fp8_blocks", lib().moe_quantize_fp8_blocks(
+        _ptr(w), rows, cols, _ptr(q), _ptr(scale), _stream(stream)))
+
+
+def moe_quantize_fp8_rows(x, q, scale, stream=None):
+    """1 x 128 tile E4M3 quantization of a 2-D bf16 (int16) tensor."""
+    rows, cols = x.shape
+    _check("moe_quantize_fp8_rows", lib().moe_quantize_fp8_rows(
+        _ptr(x), rows, cols, _ptr(q), _ptr(scale), _stream(stream)))
+
+
+def moe_permute_fp8(d, x, dest, xq, xs, xpq, xps, ws, stream=None):
+    _check("moe_permute_fp8", lib().moe_permute_fp8(
+        ctypes.byref(d), _ptr(x), _ptr(dest), _ptr(xq), _ptr(xs), _ptr(xpq),
+        _ptr(xps), _ptr(ws), ws.numel(), _stream(stream)))
 
 
 def moe_forward(d, w: Weights, x, bias, out, ws, update_bias=False,

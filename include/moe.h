@@ -257,6 +257,50 @@ moe_status_t moe_seq_balance_loss(const moe_dims_t* d, const float* logits,
                                   float* loss, void* ws, size_t ws_bytes,
                                   moe_stream_t stream);
 
+/* FP8 (E4M3) fine-grained quantization ("02 · DeepSeek-V3" §2, mixed
+ * precision): every group of 128 x 128 weights or 1 x 128 activations
+ * (one row, 128 channels) gets its own fp32 scale from the group's max
+ * |value|, taken online:
+ *   s = amax / 448 (correctly rounded; s = 1 for an all-zero group)
+ *   code = the E4M3 value nearest to the fp32 quotient x / s, ties to
+ *          the even mantissa, saturated to +-448 (448 = largest E4M3)
+ * Codes are E4M3 bytes (sign, 4-bit exponent with bias 7, 3-bit
+ * mantissa); value = E4M3(code) * s.  Rows and columns are bf16 inputs,
+ * row-major; rows = 0 is valid and does nothing.
+ *
+ * moe_quantize_fp8_blocks: w [rows, cols] bf16 -> q [rows, cols] u8 and
+ *   scale [rows/128, cols/128] fp32 (block (i, j) at scale[i*cols/128+j]).
+ *   rows, cols multiples of 128 (MOE_ERR_INVALID_ARG otherwise); rows/128
+ *   <= 65535.  For the experts' weights pass [E*I, H] (w1, w3) and
+ *   [E*H, I] (w2): with I and H multiples of 128 no block straddles two
+ *   experts.  Needs no workspace. */
+moe_status_t moe_quantize_fp8_blocks(const uint16_t* w, int64_t rows,
+                                     int64_t cols, uint8_t* q, float* scale,
+                                     moe_stream_t stream);
+
+/* moe_quantize_fp8_rows: x [rows, cols] bf16 -> q [rows, cols] u8 and
+ * scale [rows, cols/128] fp32, one scale per 1 x 128 tile.  cols a multiple
+ * of 128.  Needs no workspace. */
+moe_status_t moe_quantize_fp8_rows(const uint16_t* x, int64_t rows,
+                                   int64_t cols, uint8_t* q, float* scale,
+                                   moe_stream_t stream);
+
+/* Quantise-on-permute: the tokens are quantized before dispatch, and the
+ * dispatch moves FP8 rows ("02 · DeepSeek-V3" §2: activations are cast to
+ * FP8 before they are sent).  x [T, H] bf16 (H % 128 == 0, else
+ * MOE_ERR_UNSUPPORTED) is quantized in 1 x 128 tiles once:
+ *   xq [T, H] u8, xs [T, H/128] fp32            the token rows (shared expert)
+ *   xpq[dest[t,k]] = xq[t], xps[dest[t,k]] = xs[t]  the expert-sorted rows
+ *                  ([T*K, H] u8 and [T*K, H/128] fp32)
+ * dest [T, K] as written by moe_permute (which may be called with xp =
+ * NULL for the indices alone).  A dest row outside [0, T*K) is skipped and
+ * records MOE_ERR_DEVICE_BOUNDS in the workspace error word.
+ * Workspace: MOE_WS_PERMUTE (only its error word is used). */
+moe_status_t moe_permute_fp8(const moe_dims_t* d, const uint16_t* x,
+                             const int32_t* dest, uint8_t* xq, float* xs,
+                             uint8_t* xpq, float* xps, void* ws,
+                             size_t ws_bytes, moe_stream_t stream);
+
 /* The whole layer forward in one call: router logits, routing, dispatch,
  * expert FFNs, combine, and -- if update_bias != 0 -- the bias step on this
  * batch's load (applied after routing, so this call routes with the bias it

@@ -167,6 +167,32 @@ def test_seq_balance_validation_and_workspace(L):
                                   None, FAKE, 1 << 20, None) == 0
 
 
+def test_fp8_quantization_validation(L):
+    qb, qr = L.moe_quantize_fp8_blocks, L.moe_quantize_fp8_rows
+    assert qb(FAKE, 100, 128, FAKE, FAKE, None) == 1       # rows % 128
+    assert qb(FAKE, 128, 100, FAKE, FAKE, None) == 1       # cols % 128
+    assert qb(FAKE, 128 * 65536, 128, FAKE, FAKE, None) == 2
+    assert qb(None, 128, 128, FAKE, FAKE, None) == 1
+    assert qb(FAKE, 128, 128, FAKE + 4, FAKE, None) == 3
+    assert qb(FAKE, 0, 128, None, None, None) == 0         # nothing to do
+    assert qr(FAKE, 5, 100, FAKE, FAKE, None) == 1
+    assert qr(FAKE, -1, 128, FAKE, FAKE, None) == 1
+    assert qr(FAKE, 5, 128, FAKE, FAKE + 8, None) == 3
+    assert qr(FAKE, 0, 128, None, None, None) == 0
+    d = ops.dims(**V3)
+    pf = L.moe_permute_fp8
+
+    def call(dd, x=FAKE, dest=FAKE, xps=FAKE, ws_bytes=1 << 30):
+        return pf(ctypes.byref(dd), x, dest, FAKE, FAKE, FAKE, xps, FAKE,
+                  ws_bytes, None)
+    assert call(d, dest=None) == 1
+    assert call(d, xps=FAKE + 8) == 3
+    assert call(d, ws_bytes=16) == 4
+    assert call(ops.dims(**dict(V3, H=192))) == 2           # H % 128
+    assert pf(ctypes.byref(ops.dims(**dict(V3, T=0))), None, None, None,
+              None, None, None, FAKE, 1 << 30, None) == 0
+
+
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(ops, "LIB_PATH", str(tmp_path / "missing.so"))
     monkeypatch.setattr(ops, "_lib", None)
