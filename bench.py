@@ -727,6 +727,201 @@ def run_balance_gpu(args, rank, world, local_rank):
     return res
 
 
+def run_decode_fp8_gpu(args, rank, world, local_rank):
+    """The V3 decode layer (T=128) with FP8 experts: per step, through the
+    public calls, router logits -> moe_route -> moe_permute (indices) ->
+    moe_permute_fp8 (quantise-on-permute) -> moe_expert_ffn_fp8 ->
+    moe_combine -> moe_bias_update.  The weights are quantized to E4M3
+    (128 x 128 block scales) once, before timing, as a deployment would
+    store them.  4 rotating token batches; 11.3 GB of FP8 weights > L2."""
+    import torch
+    from deepseekmoe_routing_expert_moe_b300 import inputs, ops
+    torch.cuda.set_device(local_rank)
+    cfg = inputs.CONFIGS["decode_v3"]
+    d = ops.dims_of(cfg)
+    T, H, E, K, I, Is = cfg.T, cfg.H, cfg.E, cfg.topk, cfg.I, cfg.I_shared
+    w1, w3, w2 = inputs.device_expert_weights(cfg, "cuda")
+    ws1, ws3, ws2 = inputs.shared_weights(cfg, "cuda")
+    Wq = ops.WeightsFp8.quantize(w1, w3, w2, ws1, ws3, ws2)
+    del w1, w3, w2
+    torch.cuda.empty_cache()
+    wr = torch.from_numpy(inputs.router_weight(cfg)).cuda()
+    NB = 4
+    xs = [inputs.x_tokens(cfg, step=i + 1000 * rank, device="cuda")
+          for i in range(NB)]
+    bias = torch.from_numpy(inputs.bias(cfg)).cuda()
+    z = torch.empty((T, E), dtype=torch.float32, device="cuda")
+    idx = torch.empty((T, K), dtype=torch.int32, device="cuda")
+    gate = torch.empty((T, K), dtype=torch.float32, device="cuda")
+    counts = torch.empty(E, dtype=torch.int32, device="cuda")
+    offsets = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    dest = torch.empty((T, K), dtype=torch.int32, device="cuda")
+    src_row = torch.empty(T * K, dtype=torch.int32, device="cuda")
+    xq = torch.empty((T, H), dtype=torch.uint8, device="cuda")
+    xsc = torch.empty((T, H // 128), dtype=torch.float32, device="cuda")
+    xpq = torch.empty((T * K, H), dtype=torch.uint8, device="cuda")
+    xps = torch.empty((T * K, H // 128), dtype=torch.float32, device="cuda")
+    yp = torch.empty((T * K, H), dtype=torch.int16, device="cuda")
+    ys = torch.empty((T, H), dtype=torch.int16, device="cuda")
+    out = torch.empty((T, H), dtype=torch.int16, device="cuda")
+    ws = ops.workspace(d, ops.MOE_WS_FORWARD)
+    stream = torch.cuda.current_stream()
+
+    def step(x, o, ev=None):
+        ops.moe_router_logits(d, x, wr, z, ws)
+        ops.moe_route(d, z, bias, idx, gate, counts, ws)
+        ops.moe_permute(d, None, idx, offsets, dest, src_row, None, ws)
+        ops.moe_permute_fp8(d, x, dest, xq, xsc, xpq, xps, ws)
+        if ev: ev[0].record(stream)
+        ops.moe_expert_ffn_fp8(d, Wq, xpq, xps, xq, xsc, offsets, yp, ys, ws)
+        if ev: ev[1].record(stream)
+        ops.moe_combine(d, x, ys, yp, dest, gate, o)
+        ops.moe_bias_update(d, counts, bias)
+
+    for i in range(args.warmup):
+        step(xs[i % NB], out)
+    torch.cuda.synchronize()
+    assert ops.moe_get_device_error(ws) == 0
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(gpu_index_for_smi(local_rank)) as clk:
+        torch.cuda.synchronize()
+        ev0.record(stream)
+        for i in range(args.steps):
+            step(xs[i % NB], out)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    ms = ev0.elapsed_time(ev1)
+    clocks = clk.summary()
+    # FFN call alone (events around it, separate pass)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)]
+           for _ in range(args.steps)]
+    for i in range(args.steps):
+        step(xs[i % NB], out, evs[i])
+    torch.cuda.synchronize()
+    t_ffn = float(np.mean([e[0].elapsed_time(e[1]) for e in evs])) / 1e3
+    c = counts.cpu().numpy().astype(np.int64)
+    touched = int((c > 0).sum())
+    nkh, nki, nks = H // 128, I // 128, Is // 128
+    ffn_bytes = (touched * 3 * I * H + 3 * Is * H +             # E4M3 weights
+                 (touched * 3 * (I // 128) * nkh) * 4 +         # their scales
+                 3 * (Is // 128) * nkh * 4 +
+                 (T * K + T) * H * (1 + 4 / 128) +              # token codes
+                 2 * (T * K * I + T * Is) * (1 + 4 / 128) +     # m out + in
+                 (T * K + T) * H * 2)                           # y (bf16)
+    pk, pk_src = peaks()
+    hbm = float(pk["hbm_gbs"])
+    roof = {"bound": "hbm", "achieved": round(ffn_bytes / t_ffn / 1e9, 1),
+            "peak": hbm, "unit": "GB/s"}
+    roof["frac"] = round(roof["achieved"] / hbm, 4)
+    roof["traffic"] = None
+    roof["kernel"] = ("moe_expert_ffn_fp8 call (fp8_gemm_kernel up + "
+                      "down, E4M3 weights streamed once)")
+    roof["algorithmic_bytes"] = int(ffn_bytes)
+    roof["ffn_ms"] = round(t_ffn * 1e3, 4)
+    roof["peak_source"] = f"{pk_src} (MEASURED_PEAKS.json)"
+    # end to end: x uploaded from pinned memory, out read back, every step
+    xh = [torch.empty((T, H), dtype=torch.int16).pin_memory()
+          for _ in range(2)]
+    for i in range(2):
+        xh[i].copy_(xs[i].cpu())
+    oh = torch.empty((T, H), dtype=torch.int16).pin_memory()
+    xd = torch.empty((T, H), dtype=torch.int16, device="cuda")
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        xd.copy_(xh[i % 2], non_blocking=True)
+        step(xd, out)
+        oh.copy_(out, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    assert ops.moe_get_device_error(ws) == 0
+    return {
+        "metric": "tokens/s per V3-shaped MoE decode layer on 1 B300 with "
+                  "FP8 (E4M3) experts; % of HBM roofline",
+        "value": round(T * args.steps / (ms / 1e3), 1), "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3 experts (1x128 / 128x128 fp32 scales), bf16 "
+                 "activations elsewhere, fp32 routing",
+        "data": "synthetic, seeded (the decode_v3 inputs; weights "
+                "quantized from the bf16 ones before timing)",
+        "config": {"workload": f"decode_v3_fp8: V3 decode layer T={T}, "
+                               f"H={H}, E={E}+1 shared, I={I}, top-{K}, "
+                               "FP8 experts",
+                   "T": T, "H": H, "E": E, "topk": K, "I": I,
+                   "l2": "11.3 GB of E4M3 weights streamed per step > L2"},
+        "roofline": roof,
+        "e2e": {"value": round(T * args.steps / (e2e_ms / 1e3), 1),
+                "unit": "tokens/s", "h2d_bytes_per_step": T * H * 2,
+                "d2h_bytes_per_step": T * H * 2},
+        "gpu_launches": (10 + router_extra_launches(T, H, E)) * args.steps,
+        "clocks": clocks,
+        "experts_touched": touched,
+        "impl": "b300",
+    }
+
+
+def run_decode_fp8_reference(args):
+    """Oracle arm of decode_v3_fp8: per step one token of the decode batch
+    through the oracle's routing and FP8 experts (its 8 routed experts and
+    the shared one); the oracle quantizes those experts' weights once
+    before timing, as the GPU arm does."""
+    from deepseekmoe_routing_expert_moe_b300 import inputs
+    from oracle import moe_oracle as O
+    cfg = inputs.CONFIGS["decode_v3"]
+    f32 = inputs.bf16_bits_to_f32
+    x = f32(inputs.x_tokens(cfg))[:1]
+    wr = inputs.router_weight(cfg)
+    b = inputs.bias(cfg)
+    idx = O.route(O.router_logits(x, wr), b, cfg.n_group, cfg.topk_group,
+                  cfg.topk)["idx"][0]
+    qw = {int(e): [O.quantize_128x128(f32(m))
+                   for m in inputs.expert_weights(cfg, int(e))] for e in idx}
+    qs = [O.quantize_128x128(f32(m)) for m in inputs.shared_weights(cfg)]
+
+    def one():
+        z = O.router_logits(x, wr)
+        r = O.route(z, b, cfg.n_group, cfg.topk_group, cfg.topk)
+        aq, as_ = O.quantize_1x128(x)
+        y = x.astype(np.float64) + O.fp8_swiglu_ffn(aq, as_, *qs)[0]
+        for k, e in enumerate(r["idx"][0]):
+            y = y + float(r["gate"][0, k]) * O.fp8_swiglu_ffn(
+                aq, as_, *qw[int(e)])[0]
+        return y
+
+    for _ in range(args.warmup):
+        one()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        one()
+    tot = time.perf_counter() - t0
+    v = args.steps / tot
+    sample = ("one decode token per step through the numpy oracle: logits, "
+              "routing, 1x128 quantization, its 8 FP8 experts + the shared "
+              "one (weights quantized before timing)")
+    return {
+        "metric": "tokens/s per V3-shaped MoE decode layer with FP8 experts; "
+                  "oracle on the host cores",
+        "value": round(v, 4), "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(tot / args.steps * 1e3, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64 on e4m3 values", "data": "synthetic, seeded",
+        "config": {"workload": "decode_v3_fp8: V3 decode layer, FP8 experts"},
+        "impl": "reference",
+        "cpu_baseline": {"value": round(v, 4), "unit": "tokens/s",
+                         "cores": blas_threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(v, 4), "unit": "tokens/s",
+                "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
 def run_balance_reference(args):
     """Oracle arm of balance_v3: one 4096-token sequence of V3-shaped
     logits per step through the oracle's balance loss."""
@@ -769,6 +964,8 @@ def run_reference(args):
     from deepseekmoe_routing_expert_moe_b300 import inputs
     if args.workload == "balance_v3":
         return run_balance_reference(args)
+    if args.workload == "decode_v3_fp8":
+        return run_decode_fp8_reference(args)
     cfg = inputs.CONFIGS[args.workload]
     n = args.ref_tokens
     s = oracle_sample(cfg, n)
@@ -803,7 +1000,8 @@ def main():
     ap.add_argument("--impl", choices=("b300", "reference"), default="b300")
     ap.add_argument("--workload", default="prefill_v3",
                     choices=("prefill_v3", "decode_v3", "skewed_v3",
-                             "route_v3", "prefill_v3_e32", "balance_v3"))
+                             "route_v3", "prefill_v3_e32", "balance_v3",
+                             "decode_v3_fp8"))
     ap.add_argument("--cpu-sample-tokens", type=int, default=4)
     ap.add_argument("--ref-tokens", type=int, default=1)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -829,6 +1027,8 @@ def main():
         res = run_route_gpu(args, rank, world, local_rank)
     elif args.workload == "balance_v3":
         res = run_balance_gpu(args, rank, world, local_rank)
+    elif args.workload == "decode_v3_fp8":
+        res = run_decode_fp8_gpu(args, rank, world, local_rank)
     else:
         res = run_gpu(args, rank, world, local_rank)
     if rank == 0:

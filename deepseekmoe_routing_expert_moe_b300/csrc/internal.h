@@ -98,6 +98,26 @@ struct FfnArgs {
 // 0 on success, else a moe_status_t (encoding or launch failure)
 int launch_expert_ffn(const FfnArgs& a, cudaStream_t s);
 
+// ---- fp8_gemm.cu
+struct FfnFp8Args {
+  int T, H, E, topk, I, I_shared;
+  const uint8_t *xpq, *xq;         // E4M3 token rows [T*K, H], [T, H]
+  const float *xps, *xs;           // their 1 x 128 scales
+  const int32_t* offsets;          // [E+1]
+  const uint8_t *w1, *w3, *w2;     // routed weights, E4M3
+  const float *w1s, *w3s, *w2s;    // their 128 x 128 block scales
+  const uint8_t *ws1, *ws3, *ws2;  // shared expert
+  const float *ws1s, *ws3s, *ws2s;
+  uint8_t *mq, *msq;               // intermediate codes [T*K, I], [T, I_s]
+  float *ms, *mss;                 // their scales
+  uint16_t *yp, *ys;               // outputs, bf16
+  DevStatus* status;
+  uint64_t wait_limit_ns;
+};
+// 1 when the FP8 kernels have a shape for these sizes
+int fp8_ffn_supported(int H, int I, int I_shared, int E);
+int launch_expert_ffn_fp8(const FfnFp8Args& a, cudaStream_t s);
+
 // ---- router_gemm.cu
 // router logits on the tensor cores from the exact 3-way bf16 split of the
 // fp32 router weight (w_split [3, E, H], see launch_split_router_weight);
@@ -120,6 +140,9 @@ cudaError_t launch_split_router_weight(const float* w, int E, int H,
 // elements], 128-byte swizzle; false if encoding fails
 bool make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t inner,
                     uint64_t outer, uint32_t box_outer);
+// the same for a byte tensor (E4M3 codes): box [box_outer rows, 128 B]
+bool make_tmap_u8(CUtensorMap* m, const void* base, uint64_t inner,
+                  uint64_t outer, uint32_t box_outer);
 int sm_count();
 int gemm_ctas();           // persistent CTAs of the expert GEMMs
 void set_gemm_ctas(int n); // 0: one per SM

@@ -78,6 +78,7 @@ struct Layout {
   size_t r_partial = 0;  // [ksplit, T, E] fp32 partial router sums
   size_t bal_sp = 0, bal_flags = 0;  // [T, E] fp32 s', [T, E] u8 top-K flags
   size_t bal_pP = 0, bal_pc = 0;     // per-split partial sums (bounded)
+  size_t f8_mq = 0, f8_ms = 0, f8_msq = 0, f8_mss = 0;  // FP8 intermediate
   size_t total = 0;
 };
 
@@ -124,10 +125,19 @@ Layout layout(const moe_dims_t* d, moe_ws_kind_t which) {
     L.bal_pP = take(moe::kBalPartialElems * 4);
     L.bal_pc = take(moe::kBalPartialElems * 4);
   }
+  if (which == MOE_WS_EXPERT_FFN_FP8) {
+    const size_t I = d->I, Is = d->I_shared;
+    L.f8_mq = take(T * K * I);
+    L.f8_ms = take(T * K * (I / 128) * 4);
+    L.f8_msq = take(T * Is);
+    L.f8_mss = take(T * (Is / 128) * 4);
+  }
   L.total = o;
   // one MOE_WS_FORWARD workspace serves every entry point
-  if (which == MOE_WS_FORWARD)
+  if (which == MOE_WS_FORWARD) {
     L.total = std::max(L.total, layout(d, MOE_WS_SEQ_BALANCE).total);
+    L.total = std::max(L.total, layout(d, MOE_WS_EXPERT_FFN_FP8).total);
+  }
   return L;
 }
 
@@ -271,9 +281,10 @@ void moe_set_wait_timeout_ns(uint64_t ns) {
 }
 
 size_t moe_workspace_bytes(const moe_dims_t* d, moe_ws_kind_t which) {
-  const bool ffn = which == MOE_WS_EXPERT_FFN || which == MOE_WS_FORWARD;
+  const bool ffn = which == MOE_WS_EXPERT_FFN || which == MOE_WS_FORWARD ||
+                   which == MOE_WS_EXPERT_FFN_FP8;
   if (check_dims(d, ffn) != MOE_OK) return 0;
-  if (which < MOE_WS_ROUTE || which > MOE_WS_SEQ_BALANCE) return 0;
+  if (which < MOE_WS_ROUTE || which > MOE_WS_EXPERT_FFN_FP8) return 0;
   return layout(d, which).total;
 }
 
@@ -512,6 +523,76 @@ moe_status_t moe_permute_fp8(const moe_dims_t* d, const uint16_t* x,
   return cuda_ok(moe::launch_quant_rows(
       x, d->T, d->H, dest, d->topk, xq, xs, xpq, xps,
       at<DevStatus>(ws, 0), cs(stream)));
+}
+
+moe_status_t moe_expert_ffn_fp8(const moe_dims_t* d, const moe_weights_fp8_t* w,
+                                const uint8_t* xpq, const float* xps,
+                                const uint8_t* xq, const float* xs,
+                                const int32_t* offsets, uint16_t* yp,
+                                uint16_t* ys, void* ws, size_t ws_bytes,
+                                moe_stream_t stream) {
+  MOE_TRY(check_dims(d, true));
+  if (!moe::fp8_ffn_supported(d->H, d->I, d->I_shared, d->E))
+    return MOE_ERR_UNSUPPORTED;
+  MOE_NEED(w);
+  const void* wp[12] = {w->w1,  w->w1_scale,  w->w3,  w->w3_scale,
+                        w->w2,  w->w2_scale,  w->ws1, w->ws1_scale,
+                        w->ws3, w->ws3_scale, w->ws2, w->ws2_scale};
+  for (const void* ptr : wp) {
+    MOE_NEED(ptr);
+    MOE_ALIGN(ptr);
+  }
+  MOE_NEED_T(xpq);
+  MOE_NEED_T(xps);
+  MOE_NEED_T(xq);
+  MOE_NEED_T(xs);
+  MOE_NEED(offsets);
+  MOE_NEED_T(yp);
+  MOE_NEED_T(ys);
+  MOE_ALIGN(xpq);
+  MOE_ALIGN(xps);
+  MOE_ALIGN(xq);
+  MOE_ALIGN(xs);
+  MOE_ALIGN(offsets);
+  MOE_ALIGN(yp);
+  MOE_ALIGN(ys);
+  MOE_TRY(check_ws(d, MOE_WS_EXPERT_FFN_FP8, ws, ws_bytes));
+  if (d->T == 0) return MOE_OK;
+  const Layout L = layout(d, MOE_WS_EXPERT_FFN_FP8);
+  moe::FfnFp8Args a;
+  a.T = d->T;
+  a.H = d->H;
+  a.E = d->E;
+  a.topk = d->topk;
+  a.I = d->I;
+  a.I_shared = d->I_shared;
+  a.xpq = xpq;
+  a.xq = xq;
+  a.xps = xps;
+  a.xs = xs;
+  a.offsets = offsets;
+  a.w1 = w->w1;
+  a.w3 = w->w3;
+  a.w2 = w->w2;
+  a.w1s = w->w1_scale;
+  a.w3s = w->w3_scale;
+  a.w2s = w->w2_scale;
+  a.ws1 = w->ws1;
+  a.ws3 = w->ws3;
+  a.ws2 = w->ws2;
+  a.ws1s = w->ws1_scale;
+  a.ws3s = w->ws3_scale;
+  a.ws2s = w->ws2_scale;
+  a.mq = at<uint8_t>(ws, L.f8_mq);
+  a.ms = at<float>(ws, L.f8_ms);
+  a.msq = at<uint8_t>(ws, L.f8_msq);
+  a.mss = at<float>(ws, L.f8_mss);
+  a.yp = yp;
+  a.ys = ys;
+  a.status = at<DevStatus>(ws, 0);
+  a.wait_limit_ns = g_wait_limit_ns;
+  const int rc = moe::launch_expert_ffn_fp8(a, cs(stream));
+  return static_cast<moe_status_t>(rc);
 }
 
 moe_status_t moe_bias_update(const moe_dims_t* d, const int32_t* counts,

@@ -17,7 +17,8 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libmoe.so")
 
 (MOE_WS_ROUTE, MOE_WS_PERMUTE, MOE_WS_EXPERT_FFN, MOE_WS_FORWARD,
- MOE_WS_ROUTER_LOGITS, MOE_WS_SEQ_BALANCE) = 0, 1, 2, 3, 4, 5
+ MOE_WS_ROUTER_LOGITS, MOE_WS_SEQ_BALANCE, MOE_WS_EXPERT_FFN_FP8) = \
+    0, 1, 2, 3, 4, 5, 6
 
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
           3: "MOE_ERR_ALIGNMENT", 4: "MOE_ERR_WORKSPACE", 5: "MOE_ERR_CUDA",
@@ -45,6 +46,12 @@ class MoeWeights(ctypes.Structure):
                  "router_offset")]
 
 
+class MoeWeightsFp8(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in
+                ("w1", "w1_scale", "w3", "w3_scale", "w2", "w2_scale",
+                 "ws1", "ws1_scale", "ws3", "ws3_scale", "ws2", "ws2_scale")]
+
+
 _P = ctypes.c_void_p
 _D = ctypes.POINTER(MoeDims)
 _W = ctypes.POINTER(MoeWeights)
@@ -66,6 +73,8 @@ _SIGS = {
     "moe_quantize_fp8_rows": (_I, [_P, ctypes.c_int64, ctypes.c_int64, _P,
                                    _P, _P]),
     "moe_permute_fp8": (_I, [_D, _P, _P, _P, _P, _P, _P, _P, _S, _P]),
+    "moe_expert_ffn_fp8": (_I, [_D, ctypes.POINTER(MoeWeightsFp8), _P, _P,
+                                _P, _P, _P, _P, _P, _P, _S, _P]),
     "moe_forward": (_I, [_D, _W, _P, _P, _I, _P, _P, _P, _P, _P, _P, _P, _S,
                          _P]),
     "moe_status_string": (ctypes.c_char_p, [_I]),
@@ -145,6 +154,36 @@ class Weights:
         self.struct = MoeWeights(*(_ptr(t) for t in (w_router, w1, w3, w2,
                                                       ws1, ws3, ws2,
                                                       router_offset)))
+
+
+class WeightsFp8:
+    """FP8 expert weights: (codes uint8, block scales fp32) pairs for w1,
+    w3, w2 (all experts) and ws1, ws3, ws2 (shared expert)."""
+
+    NAMES = ("w1", "w3", "w2", "ws1", "ws3", "ws2")
+
+    def __init__(self, **pairs):
+        self.pairs = pairs
+        flat = []
+        for n in self.NAMES:
+            q, s = pairs[n]
+            flat += [_ptr(q), _ptr(s)]
+        self.struct = MoeWeightsFp8(*flat)
+
+    @classmethod
+    def quantize(cls, w1, w3, w2, ws1, ws3, ws2, stream=None):
+        """128 x 128 block quantization of bf16 (int16) weights on the
+        device: w1, w3 [E, I, H], w2 [E, H, I], ws1, ws3 [I_s, H],
+        ws2 [H, I_s]."""
+        pairs = {}
+        for n, t in zip(cls.NAMES, (w1, w3, w2, ws1, ws3, ws2)):
+            t2 = t.reshape(-1, t.shape[-1])
+            q = torch.empty(t2.shape, dtype=torch.uint8, device=t.device)
+            s = torch.empty((t2.shape[0] // 128, t2.shape[1] // 128),
+                            dtype=torch.float32, device=t.device)
+            moe_quantize_fp8_blocks(t2, q, s, stream)
+            pairs[n] = (q, s)
+        return cls(**pairs)
 
 
 def workspace_bytes(d: MoeDims, which: int) -> int:
@@ -235,6 +274,14 @@ def moe_permute_fp8(d, x, dest, xq, xs, xpq, xps, ws, stream=None):
     _check("moe_permute_fp8", lib().moe_permute_fp8(
         ctypes.byref(d), _ptr(x), _ptr(dest), _ptr(xq), _ptr(xs), _ptr(xpq),
         _ptr(xps), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def moe_expert_ffn_fp8(d, w: WeightsFp8, xpq, xps, xq, xs, offsets, yp, ys,
+                       ws, stream=None):
+    _check("moe_expert_ffn_fp8", lib().moe_expert_ffn_fp8(
+        ctypes.byref(d), ctypes.byref(w.struct), _ptr(xpq), _ptr(xps),
+        _ptr(xq), _ptr(xs), _ptr(offsets), _ptr(yp), _ptr(ys), _ptr(ws),
+        ws.numel(), _stream(stream)))
 
 
 def moe_forward(d, w: Weights, x, bias, out, ws, update_bias=False,

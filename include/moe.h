@@ -116,7 +116,8 @@ typedef enum {
   MOE_WS_EXPERT_FFN = 2,
   MOE_WS_FORWARD = 3,
   MOE_WS_ROUTER_LOGITS = 4,
-  MOE_WS_SEQ_BALANCE = 5
+  MOE_WS_SEQ_BALANCE = 5,
+  MOE_WS_EXPERT_FFN_FP8 = 6
 } moe_ws_kind_t;
 
 /* Bytes of device workspace `which` needs for dims `d` (0 if d is invalid).
@@ -300,6 +301,50 @@ moe_status_t moe_permute_fp8(const moe_dims_t* d, const uint16_t* x,
                              const int32_t* dest, uint8_t* xq, float* xs,
                              uint8_t* xpq, float* xps, void* ws,
                              size_t ws_bytes, moe_stream_t stream);
+
+/* FP8 expert weights: E4M3 codes and 128 x 128 block scales as
+ * moe_quantize_fp8_blocks writes them (device pointers, caller-owned):
+ *   w1, w3 [E*I, H] codes, w1_scale, w3_scale [E*I/128, H/128]
+ *   w2     [E*H, I] codes, w2_scale          [E*H/128, I/128]
+ *   ws1, ws3 [I_s, H], ws1_scale, ws3_scale [I_s/128, H/128] (shared)
+ *   ws2    [H, I_s],   ws2_scale            [H/128, I_s/128] */
+typedef struct {
+  const uint8_t* w1;
+  const float* w1_scale;
+  const uint8_t* w3;
+  const float* w3_scale;
+  const uint8_t* w2;
+  const float* w2_scale;
+  const uint8_t* ws1;
+  const float* ws1_scale;
+  const uint8_t* ws3;
+  const float* ws3_scale;
+  const uint8_t* ws2;
+  const float* ws2_scale;
+} moe_weights_fp8_t;
+
+/* Expert FFNs in FP8 ("02 · DeepSeek-V3" §2 mixed precision on §1.1's
+ * SwiGLU experts): E4M3 x E4M3 products on the tcgen05 tensor cores, each
+ * 128-element slice of the reduction (one scale group of both operands)
+ * summed on its own in fp32 and promoted into fp32 registers times its
+ * activation and weight scales; the intermediate silu(p) * q is quantized
+ * to E4M3 in 1 x 128 tiles for the down projection.
+ *   xpq [T*K, H] u8, xps [T*K, H/128] fp32   routed rows (moe_permute_fp8)
+ *   xq  [T, H] u8,   xs  [T, H/128] fp32     token rows (shared expert)
+ *   offsets [E+1] int32                      as written by moe_permute
+ *   yp [T*K, H] bf16 out, FFN_e(row) for every routed row (ungated)
+ *   ys [T, H] bf16 out, FFN_shared(x_t)
+ * H, I, I_shared must be multiples of 128 and at most 8192
+ * (MOE_ERR_UNSUPPORTED otherwise).  Its tiles hold up to 32 token rows:
+ * it is built for batches where each expert sees few tokens (decode), whose
+ * time is the weight stream that FP8 halves.
+ * Workspace: MOE_WS_EXPERT_FFN_FP8. */
+moe_status_t moe_expert_ffn_fp8(const moe_dims_t* d, const moe_weights_fp8_t* w,
+                                const uint8_t* xpq, const float* xps,
+                                const uint8_t* xq, const float* xs,
+                                const int32_t* offsets, uint16_t* yp,
+                                uint16_t* ys, void* ws, size_t ws_bytes,
+                                moe_stream_t stream);
 
 /* The whole layer forward in one call: router logits, routing, dispatch,
  * expert FFNs, combine, and -- if update_bias != 0 -- the bias step on this

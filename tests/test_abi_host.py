@@ -193,6 +193,31 @@ def test_fp8_quantization_validation(L):
               None, None, None, FAKE, 1 << 30, None) == 0
 
 
+def test_fp8_ffn_validation(L):
+    d = ops.dims(**V3)
+    fn = L.moe_expert_ffn_fp8
+    need = ops.workspace_bytes(d, ops.MOE_WS_EXPERT_FFN_FP8)
+    # E4M3 intermediate codes + scales for the routed and the shared rows
+    assert need >= 4096 * 8 * 2048 + 4096 * 2048
+    assert need <= ops.workspace_bytes(d, ops.MOE_WS_FORWARD)
+
+    def call(dd, w, xs=FAKE, ws_bytes=1 << 40):
+        return fn(ctypes.byref(dd), ctypes.byref(w), FAKE, FAKE, FAKE, xs,
+                  FAKE, FAKE, FAKE, FAKE, ws_bytes, None)
+    good = ops.MoeWeightsFp8(*(FAKE,) * 12)
+    assert call(ops.dims(**dict(V3, H=192)), good) == 2      # H % 128
+    assert call(ops.dims(**dict(V3, I=64 * 3)), good) == 2   # I % 128
+    assert call(ops.dims(**dict(V3, H=8192 + 128)), good) == 2
+    assert call(d, ops.MoeWeightsFp8(*(FAKE,) * 11, None)) == 1
+    assert call(d, ops.MoeWeightsFp8(*(FAKE,) * 5, FAKE + 4,
+                                     *(FAKE,) * 6)) == 3
+    assert call(d, good, xs=FAKE + 8) == 3
+    assert call(d, good, ws_bytes=1024) == 4
+    d0 = ops.dims(**dict(V3, T=0))
+    assert fn(ctypes.byref(d0), ctypes.byref(good), None, None, None, None,
+              FAKE, None, None, FAKE, 1 << 20, None) == 0
+
+
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(ops, "LIB_PATH", str(tmp_path / "missing.so"))
     monkeypatch.setattr(ops, "_lib", None)
