@@ -4,10 +4,15 @@ every 128-element slice of the reduction into fp32).
 
 The oracle's codes and scales -- its own quantization of the same bf16
 tokens and weights -- are the GPU's inputs, so both sides multiply the same
-E4M3 values.  They differ by fp32 accumulation order, the fp32 SwiGLU, the
-rare intermediate code that lands on the other side of a rounding midpoint
-because of those, and the bf16 rounding of y (2^-9 relative).  Bar: max
-|y_gpu - y| <= 2e-2 RMS(y) per expert and RMS error <= 5e-3 RMS(y)."""
+E4M3 values.  They differ by fp32 accumulation order and the fp32 SwiGLU
+(~1e-6 relative), and so, rarely, in an intermediate code: the GPU's m and
+the oracle's (fp64) m can fall on the two sides of a rounding midpoint, and
+one E4M3 step is up to 1/8 of the value, carried into y through a column
+of W2.  Bar, per element of y (token t, feature j):
+  |y_gpu - y| <= 2^-8 |y| + 1e-3 RMS(y) + 2 max_i step_i(t) |W2_ji|
+(bf16 rounding of y, accumulation noise, and up to two one-step code
+differences per token, step_i(t) = the E4M3 spacing at the oracle's code
+of m_i(t) times its scale); and RMS error <= 5e-3 RMS(y)."""
 import numpy as np
 import pytest
 import torch
@@ -22,10 +27,31 @@ pytestmark = pytest.mark.gpu
 f32 = inputs.bf16_bits_to_f32
 
 
-def _check(got, ref, what):
+_TABLE = O.e4m3_decode(np.arange(0x7F, dtype=np.uint8))
+# spacing of the E4M3 grid around each magnitude code (the wider side)
+_STEP = np.maximum(np.diff(_TABLE, append=_TABLE[-1] + 32.0),
+                   np.diff(_TABLE, prepend=0.0))
+
+
+def _flip_bound(m, w2):
+    """2 max_i step_i(t) |W2_ji| for the oracle's intermediate m = (codes,
+    scales) of each token and the dequantized W2 [H, I]."""
+    mq, ms = m
+    step = _STEP[mq & 0x7F] * np.repeat(ms.astype(np.float64), 128, axis=1)
+    aw = np.abs(w2)
+    out = np.empty((mq.shape[0], aw.shape[0]))
+    for t in range(mq.shape[0]):
+        out[t] = 2.0 * (aw * step[t][None, :]).max(axis=1)
+    return out
+
+
+def _check(got, ref, what, m=None, w2=None):
     got = np.asarray(got, np.float64)
     rms = np.sqrt(np.mean(ref * ref))
     err = np.abs(got - ref)
+    bound = 2.0 ** -8 * np.abs(ref) + 1e-3 * rms
+    if m is not None:
+        bound = bound + _flip_bound(m, w2)
     # on failure, say how the two relate: a scale slip shows as a clean
     # fit with the wrong factor, a layout slip as low correlation
     g, r = got.ravel(), ref.ravel()
@@ -33,8 +59,9 @@ def _check(got, ref, what):
                 rms_err=float(np.sqrt(np.mean(err * err)) / rms),
                 corr=float(np.corrcoef(g, r)[0, 1]) if g.std() > 0 else 0.0,
                 fit=float(g @ r / (r @ r)), got_rms=float(np.sqrt(np.mean(
-                    g * g)) / rms), finite=bool(np.isfinite(g).all()))
-    assert err.max() <= 2e-2 * rms, diag
+                    g * g)) / rms), finite=bool(np.isfinite(g).all()),
+                over=int(np.sum(err > bound)))
+    assert np.all(err <= bound), diag
     assert np.sqrt(np.mean(err * err)) <= 5e-3 * rms, diag
 
 
@@ -95,12 +122,12 @@ def _assert_layer(cfg, idx, T=None, experts=None, shared_rows=None):
         if a == b:
             continue
         rows = p["src_row"][a:b] // cfg.topk
-        ref, _ = O.fp8_swiglu_ffn(xq[rows], xs[rows], *per[e])
-        _check(yp[a:b], ref, f"expert {e}")
+        ref, m = O.fp8_swiglu_ffn(xq[rows], xs[rows], *per[e])
+        _check(yp[a:b], ref, f"expert {e}", m, O.dequantize(*per[e][2], 128))
     rows = np.arange(xq.shape[0]) if shared_rows is None else shared_rows
-    ref, _ = O.fp8_swiglu_ffn(xq[rows], xs[rows], sh["ws1"], sh["ws3"],
+    ref, m = O.fp8_swiglu_ffn(xq[rows], xs[rows], sh["ws1"], sh["ws3"],
                               sh["ws2"])
-    _check(ys[rows], ref, "shared")
+    _check(ys[rows], ref, "shared", m, O.dequantize(*sh["ws2"], 128))
 
 
 def test_small_layer_every_row():
@@ -168,11 +195,11 @@ def test_decode_v3_full_size_sampled_experts():
     for e in busy + ([one] if one is not None else []):
         a, b = p["offsets"][e], p["offsets"][e + 1]
         rows = tok[a:b]
-        ref, _ = O.fp8_swiglu_ffn(xq[rows], xs[rows],
-                                  *_host_weights(cfg, e))
-        _check(yp[a:b], ref, f"expert {e}")
+        hw = _host_weights(cfg, e)
+        ref, m = O.fp8_swiglu_ffn(xq[rows], xs[rows], *hw)
+        _check(yp[a:b], ref, f"expert {e}", m, O.dequantize(*hw[2], 128))
     sh = _shared(cfg)
     rows = np.arange(0, T, 9)
-    ref, _ = O.fp8_swiglu_ffn(xq[rows], xs[rows], sh["ws1"], sh["ws3"],
+    ref, m = O.fp8_swiglu_ffn(xq[rows], xs[rows], sh["ws1"], sh["ws3"],
                               sh["ws2"])
-    _check(ys[rows], ref, "shared")
+    _check(ys[rows], ref, "shared", m, O.dequantize(*sh["ws2"], 128))
