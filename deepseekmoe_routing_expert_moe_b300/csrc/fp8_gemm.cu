@@ -22,7 +22,7 @@
 //                   tile (32 x 128 B), 128-byte swizzle, one mbarrier
 //   warp 1 lane 0   tcgen05.mma kind::f8f6f4 (E4M3 x E4M3 -> f32), M = 128,
 //                   N = rows rounded to 16, K = 32, four per k-block into a
-//                   fresh partial-sum buffer (one of 4 in tensor memory)
+//                   fresh partial-sum buffer (one of 8 in tensor memory)
 //   warps 2..5      promotion and epilogue: per k-block tcgen05.ld of the
 //                   partial sums, acc += partial * (s_w * s_t) in fp32,
 //                   then SwiGLU + E4M3 re-quantization (up) or bf16 (down),
@@ -44,13 +44,17 @@ constexpr int F_BM = 128;      // weight rows per accumulator = MMA M
 constexpr int F_BK = 128;      // k per stage: 128 E4M3 = one 128 B row
 constexpr int F_UMMA_K = 32;   // k of one kind::f8f6f4 MMA
 constexpr int F_NT = 32;       // token rows per unit (MMA N <= 32)
-constexpr int F_NBUF = 4;      // partial-sum buffers in tensor memory
+// partial-sum buffers in tensor memory: the MMAs run up to this many
+// k-blocks ahead of the promotion, which carries them (and the weight
+// stream behind them) across the epilogue's per-unit work -- scale loads,
+// SwiGLU, re-quantization, stores
+constexpr int F_NBUF = 8;
 constexpr int F_KBMAX = 64;    // k-blocks per unit (K <= 8192)
 constexpr int F_EPI0 = 2;      // first epilogue warp
 constexpr int F_THREADS = 32 * (F_EPI0 + 4);
 constexpr uint32_t F_W_BYTES = F_BM * F_BK;  // 16 KB
 constexpr uint32_t F_T_BYTES = F_NT * F_BK;  // 4 KB
-constexpr uint32_t F_TMEM_COLS = 256;
+constexpr uint32_t F_TMEM_COLS = 512;
 constexpr size_t F_SMEM_LIMIT = 232448;
 constexpr uint64_t F_DRAIN_NS = 2000000000ull;
 
