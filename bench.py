@@ -814,7 +814,7 @@ def run_decode_fp8_gpu(args, rank, world, local_rank):
     roof = {"bound": "hbm", "achieved": round(ffn_bytes / t_ffn / 1e9, 1),
             "peak": hbm, "unit": "GB/s"}
     roof["frac"] = round(roof["achieved"] / hbm, 4)
-    roof["traffic"] = None
+    roof["traffic"] = ncu_traffic("ffn_fp8", "decode_v3_fp8")
     roof["kernel"] = ("moe_expert_ffn_fp8 call (fp8_gemm_kernel up + "
                       "down, E4M3 weights streamed once)")
     roof["algorithmic_bytes"] = int(ffn_bytes)
