@@ -727,17 +727,19 @@ def run_balance_gpu(args, rank, world, local_rank):
     return res
 
 
-def run_decode_fp8_gpu(args, rank, world, local_rank):
-    """The V3 decode layer (T=128) with FP8 experts: per step, through the
-    public calls, router logits -> moe_route -> moe_permute (indices) ->
-    moe_permute_fp8 (quantise-on-permute) -> moe_expert_ffn_fp8 ->
-    moe_combine -> moe_bias_update.  The weights are quantized to E4M3
-    (128 x 128 block scales) once, before timing, as a deployment would
-    store them.  4 rotating token batches; 11.3 GB of FP8 weights > L2."""
+def run_fp8_gpu(args, rank, world, local_rank):
+    """A V3 layer with FP8 experts -- decode_v3_fp8 (T=128) or
+    prefill_v3_fp8 (T=4096): per step, through the public calls, router
+    logits -> moe_route -> moe_permute (indices) -> moe_permute_fp8
+    (quantise-on-permute) -> moe_expert_ffn_fp8 -> moe_combine ->
+    moe_bias_update.  The weights are quantized to E4M3 (128 x 128 block
+    scales) once, before timing, as a deployment would store them.  4
+    rotating token batches; 11.3 GB of FP8 weights > L2."""
     import torch
     from deepseekmoe_routing_expert_moe_b300 import inputs, ops
     torch.cuda.set_device(local_rank)
-    cfg = inputs.CONFIGS["decode_v3"]
+    base = args.workload[:-len("_fp8")]
+    cfg = inputs.CONFIGS[base]
     d = ops.dims_of(cfg)
     T, H, E, K, I, Is = cfg.T, cfg.H, cfg.E, cfg.topk, cfg.I, cfg.I_shared
     w1, w3, w2 = inputs.device_expert_weights(cfg, "cuda")
@@ -814,7 +816,7 @@ def run_decode_fp8_gpu(args, rank, world, local_rank):
     roof = {"bound": "hbm", "achieved": round(ffn_bytes / t_ffn / 1e9, 1),
             "peak": hbm, "unit": "GB/s"}
     roof["frac"] = round(roof["achieved"] / hbm, 4)
-    roof["traffic"] = ncu_traffic("ffn_fp8", "decode_v3_fp8")
+    roof["traffic"] = ncu_traffic("ffn_fp8", args.workload)
     roof["kernel"] = ("moe_expert_ffn_fp8 call (fp8_gemm_kernel up + "
                       "down, E4M3 weights streamed once)")
     roof["algorithmic_bytes"] = int(ffn_bytes)
@@ -840,17 +842,17 @@ def run_decode_fp8_gpu(args, rank, world, local_rank):
     e2e_ms = e0.elapsed_time(e1)
     assert ops.moe_get_device_error(ws) == 0
     return {
-        "metric": "tokens/s per V3-shaped MoE decode layer on 1 B300 with "
-                  "FP8 (E4M3) experts; % of HBM roofline",
+        "metric": f"tokens/s per V3-shaped MoE {base.split('_')[0]} layer "
+                  "on 1 B300 with FP8 (E4M3) experts; % of HBM roofline",
         "value": round(T * args.steps / (ms / 1e3), 1), "unit": "tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(ms / args.steps, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
         "dtype": "e4m3 experts (1x128 / 128x128 fp32 scales), bf16 "
                  "activations elsewhere, fp32 routing",
-        "data": "synthetic, seeded (the decode_v3 inputs; weights "
+        "data": f"synthetic, seeded (the {base} inputs; weights "
                 "quantized from the bf16 ones before timing)",
-        "config": {"workload": f"decode_v3_fp8: V3 decode layer T={T}, "
+        "config": {"workload": f"{args.workload}: V3 layer T={T}, "
                                f"H={H}, E={E}+1 shared, I={I}, top-{K}, "
                                "FP8 experts",
                    "T": T, "H": H, "E": E, "topk": K, "I": I,
@@ -867,13 +869,13 @@ def run_decode_fp8_gpu(args, rank, world, local_rank):
 
 
 def run_decode_fp8_reference(args):
-    """Oracle arm of decode_v3_fp8: per step one token of the decode batch
-    through the oracle's routing and FP8 experts (its 8 routed experts and
+    """Oracle arm of decode_v3_fp8 / prefill_v3_fp8: per step one token of
+    the batch through the oracle's routing and FP8 experts (its 8 routed experts and
     the shared one); the oracle quantizes those experts' weights once
     before timing, as the GPU arm does."""
     from deepseekmoe_routing_expert_moe_b300 import inputs
     from oracle import moe_oracle as O
-    cfg = inputs.CONFIGS["decode_v3"]
+    cfg = inputs.CONFIGS[args.workload[:-len("_fp8")]]
     f32 = inputs.bf16_bits_to_f32
     x = f32(inputs.x_tokens(cfg))[:1]
     wr = inputs.router_weight(cfg)
@@ -964,7 +966,7 @@ def run_reference(args):
     from deepseekmoe_routing_expert_moe_b300 import inputs
     if args.workload == "balance_v3":
         return run_balance_reference(args)
-    if args.workload == "decode_v3_fp8":
+    if args.workload in ("decode_v3_fp8", "prefill_v3_fp8"):
         return run_decode_fp8_reference(args)
     cfg = inputs.CONFIGS[args.workload]
     n = args.ref_tokens
@@ -1001,7 +1003,7 @@ def main():
     ap.add_argument("--workload", default="prefill_v3",
                     choices=("prefill_v3", "decode_v3", "skewed_v3",
                              "route_v3", "prefill_v3_e32", "balance_v3",
-                             "decode_v3_fp8"))
+                             "decode_v3_fp8", "prefill_v3_fp8"))
     ap.add_argument("--cpu-sample-tokens", type=int, default=4)
     ap.add_argument("--ref-tokens", type=int, default=1)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -1027,8 +1029,8 @@ def main():
         res = run_route_gpu(args, rank, world, local_rank)
     elif args.workload == "balance_v3":
         res = run_balance_gpu(args, rank, world, local_rank)
-    elif args.workload == "decode_v3_fp8":
-        res = run_decode_fp8_gpu(args, rank, world, local_rank)
+    elif args.workload in ("decode_v3_fp8", "prefill_v3_fp8"):
+        res = run_fp8_gpu(args, rank, world, local_rank)
     else:
         res = run_gpu(args, rank, world, local_rank)
     if rank == 0:

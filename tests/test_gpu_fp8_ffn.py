@@ -165,11 +165,14 @@ def test_empty_single_row_and_ragged_chunks():
     _assert_layer(cfg, idx, T=T)
 
 
-def test_decode_v3_full_size_sampled_experts():
-    """The V3 decode layer: T = 128, 256 experts of 7168 x 2048, top-8.
-    All weights are generated and quantized on the device; the oracle
-    quantizes the sampled experts' bf16 weights itself."""
-    cfg = inputs.CONFIGS["decode_v3"]
+@pytest.mark.parametrize("name", ["decode_v3", "prefill_v3"])
+def test_v3_full_size_sampled_experts(name):
+    """The V3 decode (T = 128) and prefill (T = 4096: ~128 rows per expert,
+    four 32-row chunks sharing each weight tile) layers: 256 experts of
+    7168 x 2048, top-8.  All weights are generated and quantized on the
+    device; the oracle quantizes the sampled experts' bf16 weights
+    itself."""
+    cfg = inputs.CONFIGS[name]
     T, K, E, H, I = cfg.T, cfg.topk, cfg.E, cfg.H, cfg.I
     d = ops.dims_of(cfg)
     w1, w3, w2 = inputs.device_expert_weights(cfg, "cuda")
@@ -199,7 +202,7 @@ def test_decode_v3_full_size_sampled_experts():
         ref, m = O.fp8_swiglu_ffn(xq[rows], xs[rows], *hw)
         _check(yp[a:b], ref, f"expert {e}", m, O.dequantize(*hw[2], 128))
     sh = _shared(cfg)
-    rows = np.arange(0, T, 9)
+    rows = np.arange(0, T, max(9, T // 40))
     ref, m = O.fp8_swiglu_ffn(xq[rows], xs[rows], sh["ws1"], sh["ws3"],
                               sh["ws2"])
     _check(ys[rows], ref, "shared", m, O.dequantize(*sh["ws2"], 128))
