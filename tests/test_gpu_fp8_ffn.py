@@ -165,6 +165,33 @@ def test_empty_single_row_and_ragged_chunks():
     _assert_layer(cfg, idx, T=T)
 
 
+@pytest.mark.parametrize("E,G,K,I,Is,T", [
+    (32, 4, 3, 384, 128, 77),      # 32 experts, shared I != routed I
+    (16, 4, 1, 128, 256, 33),      # top-1, one feature block per expert
+    (64, 8, 6, 256, 384, 250),
+])
+def test_expert_and_width_shapes(E, G, K, I, Is, T):
+    cfg = inputs.custom_config("fp8s", 980 + E + K, T=T, H=384, E=E,
+                               n_group=G, topk_group=G // 2, topk=K, I=I,
+                               I_shared=Is, router_sigma=0.05)
+    z = O.router_logits(f32(inputs.x_tokens(cfg)), inputs.router_weight(cfg))
+    idx = O.route(z, inputs.bias(cfg), cfg.n_group, cfg.topk_group,
+                  cfg.topk)["idx"]
+    _assert_layer(cfg, idx)
+
+
+def test_no_tokens_is_a_no_op():
+    cfg = _small_cfg()
+    d = ops.dims_of(cfg, T=0)
+    routed, _ = _stack(cfg, None)
+    W = ops.WeightsFp8(**{n: (dev(q), dev(s)) for n, (q, s) in
+                          {**routed, **_shared(cfg)}.items()})
+    ws = ops.workspace(d, ops.MOE_WS_EXPERT_FFN_FP8)
+    off = torch.zeros(cfg.E + 1, dtype=torch.int32, device="cuda")
+    ops.moe_expert_ffn_fp8(d, W, None, None, None, None, off, None, None, ws)
+    assert ops.moe_get_device_error(ws) == 0
+
+
 @pytest.mark.parametrize("name", ["decode_v3", "prefill_v3"])
 def test_v3_full_size_sampled_experts(name):
     """The V3 decode (T = 128) and prefill (T = 4096: ~128 rows per expert,
