@@ -75,6 +75,8 @@ _SIGS = {
     "moe_permute_fp8": (_I, [_D, _P, _P, _P, _P, _P, _P, _P, _S, _P]),
     "moe_expert_ffn_fp8": (_I, [_D, ctypes.POINTER(MoeWeightsFp8), _P, _P,
                                 _P, _P, _P, _P, _P, _P, _S, _P]),
+    "moe_plan_redundant_experts": (_I, [_P, ctypes.c_int32, ctypes.c_int32,
+                                        ctypes.c_int32, _P, _P]),
     "moe_forward": (_I, [_D, _W, _P, _P, _I, _P, _P, _P, _P, _P, _P, _P, _S,
                          _P]),
     "moe_status_string": (ctypes.c_char_p, [_I]),
@@ -282,6 +284,20 @@ def moe_expert_ffn_fp8(d, w: WeightsFp8, xpq, xps, xq, xs, offsets, yp, ys,
         ctypes.byref(d), ctypes.byref(w.struct), _ptr(xpq), _ptr(xps),
         _ptr(xq), _ptr(xs), _ptr(offsets), _ptr(yp), _ptr(ys), _ptr(ws),
         ws.numel(), _stream(stream)))
+
+
+def moe_plan_redundant_experts(load, n_devices, slots_per_device):
+    """Host planner: load [E] (numpy int64) -> (slot_expert [D, r] int32,
+    device_load [D] int64)."""
+    import numpy as np
+    load = np.ascontiguousarray(load, np.int64)
+    D, r = int(n_devices), int(slots_per_device)
+    slots = np.full((D, r), -7, np.int32)
+    dl = np.zeros(D, np.int64)
+    _check("moe_plan_redundant_experts", lib().moe_plan_redundant_experts(
+        load.ctypes.data, load.shape[0], D, r,
+        slots.ctypes.data if D * r else None, dl.ctypes.data))
+    return slots, dl
 
 
 def moe_forward(d, w: Weights, x, bias, out, ws, update_bias=False,

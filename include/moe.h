@@ -346,6 +346,31 @@ moe_status_t moe_expert_ffn_fp8(const moe_dims_t* d, const moe_weights_fp8_t* w,
                                 uint16_t* ys, void* ws, size_t ws_bytes,
                                 moe_stream_t stream);
 
+/* Redundant-expert placement ("02 · DeepSeek-V3" §5.1: high-load experts
+ * are replicated from online load statistics, e.g. 32 redundant experts
+ * with one extra expert per GPU, revised periodically).  HOST function:
+ * all pointers are host memory, nothing is launched; it plans between
+ * steps from a count vector the caller read back (e.g. moe_forward's
+ * counts_out summed over the statistics window).
+ *   load [E] int64            tokens routed to each expert (>= 0)
+ *   n_devices D, slots_per_device r; E % D == 0
+ *   slot_expert [D * r] int32 out: the expert copied into slot (d, s) at
+ *                             [d*r + s], -1 = left empty
+ *   device_load [D] int64     out: each device's load after planning
+ * Base placement: device d hosts experts [d*E/D, (d+1)*E/D).  An expert
+ * with a copy serves its c tokens round-robin: the original keeps
+ * ceil(c/2), the copy floor(c/2).  Experts are taken heaviest first (load
+ * desc, index asc) while slots are free and loads positive; each copy goes
+ * to the least-loaded device (ties: lower index) with a free slot other
+ * than the expert's own; an expert whose only free slots are on its own
+ * device is passed over.  MOE_ERR_INVALID_ARG on a NULL pointer (slot_expert
+ * may be NULL when D * r == 0), E % D != 0, or a negative load. */
+moe_status_t moe_plan_redundant_experts(const int64_t* load, int32_t E,
+                                        int32_t n_devices,
+                                        int32_t slots_per_device,
+                                        int32_t* slot_expert,
+                                        int64_t* device_load);
+
 /* The whole layer forward in one call: router logits, routing, dispatch,
  * expert FFNs, combine, and -- if update_bias != 0 -- the bias step on this
  * batch's load (applied after routing, so this call routes with the bias it

@@ -448,3 +448,57 @@ def fp8_swiglu_ffn(a_q, a_s, w1, w3, w2):
     m_q, m_s = quantize_1x128(m)
     y = dequantize(m_q, m_s, 1) @ dequantize(*w2, 128).T
     return y, (m_q, m_s)
+
+
+# --------------------------------------------------------------------------
+# Redundant-expert planning from the load histogram ("02 · DeepSeek-V3"
+# §5.1: high-load experts are replicated from online load statistics, e.g.
+# 32 redundant experts with one extra expert per GPU, and the set is
+# revised periodically).
+# --------------------------------------------------------------------------
+def plan_redundant_experts(load: np.ndarray, n_devices: int,
+                           slots_per_device: int):
+    """Place up to R = n_devices * slots_per_device redundant expert copies
+    (READING R24).
+
+    Base placement: device d hosts experts [d*E/D, (d+1)*E/D); its load is
+    the sum of their loads.  An expert with a copy serves its c tokens
+    round-robin: the original keeps ceil(c/2), the copy floor(c/2).
+    Walk the experts heaviest first (load desc, index asc) while slots are
+    free and loads are positive; an expert gets a copy on the device with
+    the smallest current load among those with a free slot other than its
+    own (ties: lower device); an expert whose only free slots are on its own
+    device is passed over.
+    Returns dict: slot_expert [D, slots] int32 (-1 = empty slot),
+    device_load [D] int64 after planning, base_load [D] int64 before,
+    replicated: the experts given a copy, in placement order."""
+    c = np.asarray(load, np.int64)
+    E = c.shape[0]
+    D, r = int(n_devices), int(slots_per_device)
+    assert D >= 1 and r >= 0 and E % D == 0
+    per = E // D
+    dev = np.array([c[d * per:(d + 1) * per].sum() for d in range(D)],
+                   np.int64)
+    base = dev.copy()
+    slots = [[] for _ in range(D)]
+    free = D * r
+    placed = []
+    for e in sorted(range(E), key=lambda q: (-c[q], q)):
+        if free == 0 or c[e] <= 0:
+            break
+        home = e // per
+        cand = [d for d in range(D) if len(slots[d]) < r and d != home]
+        if not cand:
+            continue
+        d = min(cand, key=lambda q: (dev[q], q))
+        share = c[e] // 2
+        dev[home] -= share
+        dev[d] += share
+        slots[d].append(e)
+        placed.append(e)
+        free -= 1
+    slot_expert = np.full((D, r), -1, np.int32)
+    for d in range(D):
+        slot_expert[d, :len(slots[d])] = slots[d]
+    return dict(slot_expert=slot_expert, device_load=dev, base_load=base,
+                replicated=np.array(placed, np.int32))
