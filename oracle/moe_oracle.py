@@ -502,3 +502,56 @@ def plan_redundant_experts(load: np.ndarray, n_devices: int,
         slot_expert[d, :len(slots[d])] = slots[d]
     return dict(slot_expert=slot_expert, device_load=dev, base_load=base,
                 replicated=np.array(placed, np.int32))
+
+
+# --------------------------------------------------------------------------
+# Backward of routing to the router logits (the training-side neighbour of
+# §1.4): the gates' and the balance loss's gradients.  The top-K choices
+# and the balance loss's indicator counts are piecewise constant in z, so
+# they carry no gradient (READING R25); the bias is not in backpropagation
+# (the pages say so).  s = sig32(z) as in the forward; the rest in fp64.
+# --------------------------------------------------------------------------
+def route_backward(logits: np.ndarray, idx: np.ndarray,
+                   dgate: np.ndarray) -> np.ndarray:
+    """dL/dz from the gates' upstream gradient dgate [T, K].
+    g_k = s_k / D with D = sum of the chosen s; for a chosen expert m:
+      dL/dz_m = s_m (1 - s_m) / D * (dgate_m - sum_k dgate_k g_k)
+    and 0 for the experts not chosen.  Returns [T, E] fp64."""
+    z = np.asarray(logits, F32)
+    T, E = z.shape
+    s = sig32(z).astype(np.float64)
+    idx = np.asarray(idx)
+    dg = np.asarray(dgate, np.float64)
+    sk = np.take_along_axis(s, idx, axis=1)
+    D = sk.sum(axis=1, keepdims=True)
+    g = sk / D
+    dot = (dg * g).sum(axis=1, keepdims=True)
+    out = np.zeros((T, E))
+    np.put_along_axis(out, idx, sk * (1 - sk) / D * (dg - dot), axis=1)
+    return out
+
+
+def seq_balance_loss_backward(logits: np.ndarray, seq_len: int, topk: int,
+                              alpha: float = 1e-4, dloss=None) -> np.ndarray:
+    """dL/dz of the sequence-wise balance loss (eq. 17-20), L per sequence
+    times its upstream gradient dloss[q] (default 1).  With S_t = sum_j
+    s_t,j, s' = s / S_t and f from the forward's counts:
+      dL/dz_t,i = dloss_q * alpha / T_s * s_i (1 - s_i) / S_t
+                  * (f_i - sum_j f_j s'_t,j)
+    Returns [T, E] fp64."""
+    z = np.asarray(logits, F32)
+    T, E = z.shape
+    fw = seq_balance_loss(z, seq_len, topk, alpha)
+    n_seq = fw["loss"].shape[0]
+    dl = np.ones(n_seq) if dloss is None else np.asarray(dloss, np.float64)
+    s = sig32(z).astype(np.float64)
+    S = s.sum(axis=1, keepdims=True)
+    out = np.zeros((T, E))
+    for q in range(n_seq):
+        a, b = q * seq_len, min(T, (q + 1) * seq_len)
+        f = fw["f"][q]
+        sp = s[a:b] / S[a:b]
+        dot = sp @ f
+        out[a:b] = dl[q] * alpha / (b - a) * s[a:b] * (1 - s[a:b]) / S[a:b] \
+            * (f[None, :] - dot[:, None])
+    return out
