@@ -60,6 +60,17 @@ cudaError_t launch_bias_update(const int32_t* counts, float* bias,
 // scratch, part_P / part_c [n_seq, rs, E] the per-split partial sums (used
 // when seq_balance_splits() > 1; n_seq * rs * E <= kBalPartialElems);
 // P and counts [n_seq, E] and loss [n_seq] are written
+// backward of routing to the logits (gates; balance loss), one warp per
+// token; accumulate != 0 adds to dz instead of overwriting it
+cudaError_t launch_route_backward(const float* logits, const int32_t* idx,
+                                  const float* dgate, int T, int E, int K,
+                                  int accumulate, float* dz, DevStatus* st,
+                                  cudaStream_t s);
+cudaError_t launch_seq_balance_backward(const float* logits, int T, int E,
+                                        int K, int seq_len, float alpha,
+                                        const int32_t* counts_seq,
+                                        const float* dloss, int accumulate,
+                                        float* dz, cudaStream_t s);
 constexpr int kBalSplitTarget = 148;  // split up to 2 x this many CTAs
 constexpr long long kBalPartialElems = 2LL * kBalSplitTarget * 32;
 int seq_balance_splits(int T, int E, int seq_len);

@@ -549,6 +549,131 @@ __global__ void __launch_bounds__(1024)
   loss[q] = __fmul_rn(alpha, tot);
 }
 
+// ===================================================================
+// Backward of routing to the router logits (training side of §1.4).  The
+// top-K choices and the balance loss's indicator counts are piecewise
+// constant in z and carry no gradient; the bias takes no part.  One warp
+// per token; s is the forward's sigmoid.
+//   gates:    g_k = s_k / D, D = sum of the chosen s;
+//             dz_m = s_m (1 - s_m) / D * (dgate_m - sum_k dgate_k g_k)
+//             for a chosen m, 0 for the rest
+//   balance:  dz_i = dloss_q alpha / T_s * s_i (1 - s_i) / S
+//                    * (f_i - sum_j f_j s_j / S),  S = sum_j s_j
+// With `accumulate` the row is added to dz, else it overwrites it.
+// ===================================================================
+template <int EPL, int WARPS>
+__global__ void __launch_bounds__(WARPS * 32)
+    route_backward_kernel(const float* __restrict__ logits,
+                          const int32_t* __restrict__ idx,
+                          const float* __restrict__ dgate, int T, int E,
+                          int K, int accumulate, float* __restrict__ dz,
+                          DevStatus* st) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * WARPS + warp;
+  if (t >= T) return;
+  const bool active = lane < E / EPL;
+  int e = -1;
+  float s = 0.f, dg = 0.f;
+  if (lane < K) {
+    e = idx[(size_t)t * K + lane];
+    if (e >= 0 && e < E) {
+      s = sigmoid_f32(logits[(size_t)t * E + e]);
+      dg = dgate[(size_t)t * K + lane];
+    } else {
+      record_error(st, MOE_ERR_DEVICE_BOUNDS, 50);
+      e = -1;
+    }
+  }
+  float D = s;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1)
+    D = __fadd_rn(D, __shfl_xor_sync(0xffffffffu, D, off));
+  const float rD = D > 0.f ? __frcp_rn(D) : 0.f;
+  float dot = __fmul_rn(dg, __fmul_rn(s, rD));
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1)
+    dot = __fadd_rn(dot, __shfl_xor_sync(0xffffffffu, dot, off));
+  const float c = __fmul_rn(__fmul_rn(__fmul_rn(s, __fsub_rn(1.f, s)), rD),
+                            __fsub_rn(dg, dot));
+  float o[EPL];
+  if (active && accumulate) {
+    load_row<EPL>(dz + (size_t)t * E + lane * EPL, o);
+  } else {
+#pragma unroll
+    for (int j = 0; j < EPL; ++j) o[j] = 0.f;
+  }
+  for (int k = 0; k < K; ++k) {
+    const int ek = __shfl_sync(0xffffffffu, e, k);
+    const float ck = __shfl_sync(0xffffffffu, c, k);
+    if (ek >= 0 && lane == ek / EPL) {
+      const int jj = ek - lane * EPL;
+#pragma unroll
+      for (int j = 0; j < EPL; ++j)
+        if (j == jj) o[j] = __fadd_rn(o[j], ck);
+    }
+  }
+  if (active) store_row<EPL>(dz + (size_t)t * E + lane * EPL, o);
+}
+
+template <int EPL, int WARPS>
+__global__ void __launch_bounds__(WARPS * 32)
+    balance_backward_kernel(const float* __restrict__ logits, int T, int E,
+                            int K, int S, float alpha,
+                            const int32_t* __restrict__ counts,
+                            const float* __restrict__ dloss, int accumulate,
+                            float* __restrict__ dz) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * WARPS + warp;
+  if (t >= T) return;
+  const bool active = lane < E / EPL;
+  const int q = t / S;
+  int a, b;
+  seq_range(q, S, T, a, b);
+  const int Ts = b - a;
+  float s[EPL], f[EPL];
+  if (active) {
+    load_row<EPL>(logits + (size_t)t * E + lane * EPL, s);
+#pragma unroll
+    for (int j = 0; j < EPL; ++j) {
+      s[j] = sigmoid_f32(s[j]);
+      f[j] = __fdiv_rn(
+          __fmul_rn((float)E,
+                    (float)counts[(size_t)q * E + lane * EPL + j]),
+          (float)(K * Ts));
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < EPL; ++j) s[j] = f[j] = 0.f;
+  }
+  float Ssum = 0.f, dot = 0.f;
+#pragma unroll
+  for (int j = 0; j < EPL; ++j) {
+    Ssum = __fadd_rn(Ssum, s[j]);
+    dot = __fadd_rn(dot, __fmul_rn(f[j], s[j]));
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    Ssum = __fadd_rn(Ssum, __shfl_xor_sync(0xffffffffu, Ssum, off));
+    dot = __fadd_rn(dot, __shfl_xor_sync(0xffffffffu, dot, off));
+  }
+  const float rS = __frcp_rn(Ssum);
+  dot = __fmul_rn(dot, rS);
+  const float pre = __fdiv_rn(
+      __fmul_rn(dloss != nullptr ? dloss[q] : 1.f, alpha), (float)Ts);
+  if (!active) return;
+  float o[EPL];
+  if (accumulate) load_row<EPL>(dz + (size_t)t * E + lane * EPL, o);
+#pragma unroll
+  for (int j = 0; j < EPL; ++j) {
+    const float gj = __fmul_rn(
+        __fmul_rn(__fmul_rn(pre, __fmul_rn(s[j], __fsub_rn(1.f, s[j]))),
+                  rS),
+        __fsub_rn(f[j], dot));
+    o[j] = accumulate ? __fadd_rn(o[j], gj) : gj;
+  }
+  store_row<EPL>(dz + (size_t)t * E + lane * EPL, o);
+}
+
 // histogram of an existing topk_idx over the same token blocks
 __global__ void __launch_bounds__(256)
     block_counts_kernel(const int32_t* __restrict__ topk_idx, int T, int E,
@@ -957,6 +1082,59 @@ cudaError_t launch_seq_balance(const float* logits, int T, int E, int topk,
       sp, flags, T, E, seq_len, rs, P, counts, part_P, part_c);
   balance_loss_kernel<<<n_seq, ((E + 31) / 32) * 32, 0, s>>>(
       P, counts, part_P, part_c, rs, T, E, topk, seq_len, alpha, loss);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_route_backward(const float* logits, const int32_t* idx,
+                                  const float* dgate, int T, int E, int K,
+                                  int accumulate, float* dz, DevStatus* st,
+                                  cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  const int epl = E <= 32 ? 1 : E / 32;
+  const int nblk = (T + kBalWarps - 1) / kBalWarps;
+#define MOE_RB_CASE(N)                                                      \
+  case N:                                                                   \
+    route_backward_kernel<N, kBalWarps><<<nblk, kBalWarps * 32, 0, s>>>(    \
+        logits, idx, dgate, T, E, K, accumulate, dz, st);                   \
+    break;
+  switch (epl) {
+    MOE_RB_CASE(1)
+    MOE_RB_CASE(2)
+    MOE_RB_CASE(4)
+    MOE_RB_CASE(8)
+    MOE_RB_CASE(16)
+    MOE_RB_CASE(32)
+    default:
+      return cudaErrorInvalidValue;
+  }
+#undef MOE_RB_CASE
+  return cudaGetLastError();
+}
+
+cudaError_t launch_seq_balance_backward(const float* logits, int T, int E,
+                                        int K, int seq_len, float alpha,
+                                        const int32_t* counts_seq,
+                                        const float* dloss, int accumulate,
+                                        float* dz, cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  const int epl = E <= 32 ? 1 : E / 32;
+  const int nblk = (T + kBalWarps - 1) / kBalWarps;
+#define MOE_BB_CASE(N)                                                      \
+  case N:                                                                   \
+    balance_backward_kernel<N, kBalWarps><<<nblk, kBalWarps * 32, 0, s>>>(  \
+        logits, T, E, K, seq_len, alpha, counts_seq, dloss, accumulate, dz); \
+    break;
+  switch (epl) {
+    MOE_BB_CASE(1)
+    MOE_BB_CASE(2)
+    MOE_BB_CASE(4)
+    MOE_BB_CASE(8)
+    MOE_BB_CASE(16)
+    MOE_BB_CASE(32)
+    default:
+      return cudaErrorInvalidValue;
+  }
+#undef MOE_BB_CASE
   return cudaGetLastError();
 }
 

@@ -77,6 +77,10 @@ _SIGS = {
                                 _P, _P, _P, _P, _P, _P, _S, _P]),
     "moe_plan_redundant_experts": (_I, [_P, ctypes.c_int32, ctypes.c_int32,
                                         ctypes.c_int32, _P, _P]),
+    "moe_route_backward": (_I, [_D, _P, _P, _P, _I, _P, _P, _S, _P]),
+    "moe_seq_balance_loss_backward": (_I, [_D, _P, ctypes.c_int32,
+                                           ctypes.c_float, _P, _P, _I, _P,
+                                           _P]),
     "moe_forward": (_I, [_D, _W, _P, _P, _I, _P, _P, _P, _P, _P, _P, _P, _S,
                          _P]),
     "moe_status_string": (ctypes.c_char_p, [_I]),
@@ -298,6 +302,24 @@ def moe_plan_redundant_experts(load, n_devices, slots_per_device):
         load.ctypes.data, load.shape[0], D, r,
         slots.ctypes.data if D * r else None, dl.ctypes.data))
     return slots, dl
+
+
+def moe_route_backward(d, logits, topk_idx, dgate, dlogits, ws,
+                       accumulate=False, stream=None):
+    _check("moe_route_backward", lib().moe_route_backward(
+        ctypes.byref(d), _ptr(logits), _ptr(topk_idx), _ptr(dgate),
+        1 if accumulate else 0, _ptr(dlogits), _ptr(ws), ws.numel(),
+        _stream(stream)))
+
+
+def moe_seq_balance_loss_backward(d, logits, seq_len, alpha, counts_seq,
+                                  dlogits, dloss=None, accumulate=False,
+                                  stream=None):
+    _check("moe_seq_balance_loss_backward",
+           lib().moe_seq_balance_loss_backward(
+               ctypes.byref(d), _ptr(logits), int(seq_len), float(alpha),
+               _ptr(counts_seq), _ptr(dloss), 1 if accumulate else 0,
+               _ptr(dlogits), _stream(stream)))
 
 
 def moe_forward(d, w: Weights, x, bias, out, ws, update_bias=False,

@@ -258,6 +258,40 @@ moe_status_t moe_seq_balance_loss(const moe_dims_t* d, const float* logits,
                                   float* loss, void* ws, size_t ws_bytes,
                                   moe_stream_t stream);
 
+/* Backward of routing to the router logits (the training side of
+ * "02 · DeepSeek-V3" §1.4).  The top-K choices and the balance loss's
+ * indicator counts are piecewise constant in z and carry no gradient; the
+ * bias is not part of backpropagation (the page says so).  s is the
+ * forward's sigmoid.  Both write dlogits [T, E] fp32, or add to it when
+ * accumulate != 0 (so the two can be summed in place).
+ *
+ * moe_route_backward: the gates g_k = s_k / D (D = sum of the chosen s):
+ *   dlogits[t, m] = s_m (1 - s_m) / D * (dgate[t, m] - sum_k dgate_k g_k)
+ * for each chosen expert m = topk_idx[t, k], 0 for the others.
+ *   logits [T, E], topk_idx [T, K] (as moe_route wrote it), dgate [T, K]
+ *   the upstream gradient of the gates.  An expert id outside [0, E) is
+ *   skipped and records MOE_ERR_DEVICE_BOUNDS in the workspace error word.
+ *   Workspace: MOE_WS_ROUTE (only its error word is used). */
+moe_status_t moe_route_backward(const moe_dims_t* d, const float* logits,
+                                const int32_t* topk_idx, const float* dgate,
+                                int accumulate, float* dlogits, void* ws,
+                                size_t ws_bytes, moe_stream_t stream);
+
+/* moe_seq_balance_loss_backward: the sequence-wise balance loss (eq. 17-20)
+ * with the forward's counts (moe_seq_balance_loss's counts_seq [n_seq, E])
+ * and an upstream gradient dloss [n_seq] per sequence (NULL = 1):
+ *   dlogits[t, i] = dloss_q alpha / T_s * s_i (1 - s_i) / S_t
+ *                   * (f_i - sum_j f_j s_j / S_t),
+ *   S_t = sum_j s_t,j, f_i = E c_i / (topk T_s).
+ * Needs no workspace. */
+moe_status_t moe_seq_balance_loss_backward(const moe_dims_t* d,
+                                           const float* logits,
+                                           int32_t seq_len, float alpha,
+                                           const int32_t* counts_seq,
+                                           const float* dloss, int accumulate,
+                                           float* dlogits,
+                                           moe_stream_t stream);
+
 /* FP8 (E4M3) fine-grained quantization ("02 · DeepSeek-V3" §2, mixed
  * precision): every group of 128 x 128 weights or 1 x 128 activations
  * (one row, 128 channels) gets its own fp32 scale from the group's max

@@ -218,6 +218,24 @@ def test_fp8_ffn_validation(L):
               FAKE, None, None, FAKE, 1 << 20, None) == 0
 
 
+def test_routing_backward_validation(L):
+    d = ops.dims(**V3)
+    rb, bb = L.moe_route_backward, L.moe_seq_balance_loss_backward
+    by = ctypes.byref
+    assert rb(by(d), FAKE, None, FAKE, 0, FAKE, FAKE, 1 << 30, None) == 1
+    assert rb(by(d), FAKE, FAKE, FAKE + 4, 0, FAKE, FAKE, 1 << 30, None) == 3
+    assert rb(by(d), FAKE, FAKE, FAKE, 0, FAKE, FAKE, 8, None) == 4
+    assert rb(by(ops.dims(**dict(V3, T=0))), None, None, None, 0, None,
+              FAKE, 1 << 20, None) == 0
+    assert bb(by(d), FAKE, 0, 1e-4, FAKE, None, 0, FAKE, None) == 1
+    assert bb(by(d), FAKE, 64, float("nan"), FAKE, None, 0, FAKE,
+              None) == 1
+    assert bb(by(d), FAKE, 64, 1e-4, None, None, 0, FAKE, None) == 1
+    assert bb(by(d), FAKE, 64, 1e-4, FAKE, FAKE + 4, 0, FAKE, None) == 3
+    assert bb(by(ops.dims(**dict(V3, T=0))), None, 64, 1e-4, None, None, 0,
+              None, None) == 0
+
+
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(ops, "LIB_PATH", str(tmp_path / "missing.so"))
     monkeypatch.setattr(ops, "_lib", None)
