@@ -924,6 +924,112 @@ def run_decode_fp8_reference(args):
     }
 
 
+def run_backward_gpu(args, rank, world, local_rank):
+    """The routing side of a training step's backward at the V3 shape: per
+    step, moe_route_backward (the gates' gradient to the logits) and
+    moe_seq_balance_loss_backward accumulated into the same dlogits, on
+    T=16384 fp32 logits (four 4096-token sequences).  8 rotating batches
+    (134 MB of logits > L2), replayed from a CUDA graph."""
+    import torch
+    from deepseekmoe_routing_expert_moe_b300 import inputs, ops
+    torch.cuda.set_device(local_rank)
+    cfg = inputs.CONFIGS["route_v3"]
+    d = ops.dims_of(cfg)
+    T, E, K, S = cfg.T, cfg.E, cfg.topk, 4096
+    n_seq = -(-T // S)
+    NB = 8
+    wr = torch.from_numpy(inputs.router_weight(cfg)).cuda()
+    bias = torch.from_numpy(inputs.bias(cfg)).cuda()
+    wsl = ops.workspace(d, ops.MOE_WS_FORWARD)
+    zs, idxs, cnts = [], [], []
+    for i in range(NB):   # logits, routing and balance counts per batch
+        x = inputs.x_tokens(cfg, step=i + 1000 * rank, device="cuda")
+        z = torch.empty((T, E), dtype=torch.float32, device="cuda")
+        ops.moe_router_logits(d, x, wr, z, wsl)
+        idx = torch.empty((T, K), dtype=torch.int32, device="cuda")
+        gate = torch.empty((T, K), dtype=torch.float32, device="cuda")
+        counts = torch.empty(E, dtype=torch.int32, device="cuda")
+        ops.moe_route(d, z, bias, idx, gate, counts, wsl)
+        cs = torch.empty((n_seq, E), dtype=torch.int32, device="cuda")
+        P = torch.empty((n_seq, E), dtype=torch.float32, device="cuda")
+        loss = torch.empty(n_seq, dtype=torch.float32, device="cuda")
+        ops.moe_seq_balance_loss(d, z, S, 1e-4, cs, P, loss, wsl)
+        zs.append(z)
+        idxs.append(idx)
+        cnts.append(cs)
+    g = torch.Generator(device="cuda").manual_seed(5 + rank)
+    dgate = torch.randn((T, K), device="cuda", generator=g)
+    dloss = torch.ones(n_seq, device="cuda")
+    dz = torch.empty((T, E), dtype=torch.float32, device="cuda")
+    ws = ops.workspace(d, ops.MOE_WS_ROUTE)
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        ops.moe_route_backward(d, zs[i % NB], idxs[i % NB], dgate, dz, ws)
+        ops.moe_seq_balance_loss_backward(d, zs[i % NB], S, 1e-4,
+                                          cnts[i % NB], dz, dloss=dloss,
+                                          accumulate=True)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    assert ops.moe_get_device_error(ws) == 0
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(gr, stream=side):
+            for i in range(NB):
+                step(i)
+    stream.wait_stream(side)
+    reps = max(1, args.steps // NB)
+    gr.replay()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(gpu_index_for_smi(local_rank)) as clk:
+        torch.cuda.synchronize()
+        ev0.record(stream)
+        for _ in range(reps):
+            gr.replay()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    ms = ev0.elapsed_time(ev1)
+    args.steps = reps * NB
+    # algorithmic bytes of a step: logits, top-K ids, gate gradients and
+    # counts read once; dlogits written once
+    alg = T * E * 4 + T * K * 8 + n_seq * E * 4 + n_seq * 4 + T * E * 4
+    pk, pk_src = peaks()
+    hbm = float(pk["hbm_gbs"])
+    roof = {"bound": "hbm",
+            "achieved": round(alg * args.steps / (ms / 1e3) / 1e9, 1),
+            "peak": hbm, "unit": "GB/s"}
+    roof["frac"] = round(roof["achieved"] / hbm, 4)
+    roof["traffic"] = None
+    roof["kernel"] = ("route_backward_kernel + balance_backward_kernel "
+                      "(the latter re-reads the logits and accumulates)")
+    roof["algorithmic_bytes"] = int(alg)
+    roof["peak_source"] = f"{pk_src} (MEASURED_PEAKS.json)"
+    return {
+        "metric": "tokens/s through the routing backward (gates + "
+                  "sequence-wise balance loss to the router logits) at the "
+                  "V3 shape on 1 B300; % of HBM roofline",
+        "value": round(T * args.steps / (ms / 1e3), 1), "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms / args.steps, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic, seeded (logits from the routing workload; "
+                "dgate ~N(0,1))",
+        "config": {"workload": f"route_backward_v3: T={T} as {n_seq} "
+                               f"sequences of {S}, E={E}, top-{K}",
+                   "T": T, "E": E, "topk": K, "seq_len": S,
+                   "l2": "8 rotating logits batches, 134 MB > L2"},
+        "roofline": roof,
+        "gpu_launches": 2 * args.steps,
+        "clocks": clk.summary(),
+        "impl": "b300",
+    }
+
+
 def run_balance_reference(args):
     """Oracle arm of balance_v3: one 4096-token sequence of V3-shaped
     logits per step through the oracle's balance loss."""
@@ -1003,7 +1109,8 @@ def main():
     ap.add_argument("--workload", default="prefill_v3",
                     choices=("prefill_v3", "decode_v3", "skewed_v3",
                              "route_v3", "prefill_v3_e32", "balance_v3",
-                             "decode_v3_fp8", "prefill_v3_fp8"))
+                             "decode_v3_fp8", "prefill_v3_fp8",
+                             "route_backward_v3"))
     ap.add_argument("--cpu-sample-tokens", type=int, default=4)
     ap.add_argument("--ref-tokens", type=int, default=1)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -1031,6 +1138,8 @@ def main():
         res = run_balance_gpu(args, rank, world, local_rank)
     elif args.workload in ("decode_v3_fp8", "prefill_v3_fp8"):
         res = run_fp8_gpu(args, rank, world, local_rank)
+    elif args.workload == "route_backward_v3":
+        res = run_backward_gpu(args, rank, world, local_rank)
     else:
         res = run_gpu(args, rank, world, local_rank)
     if rank == 0:
