@@ -1030,6 +1030,47 @@ def run_backward_gpu(args, rank, world, local_rank):
     }
 
 
+def run_backward_reference(args):
+    """Oracle arm of route_backward_v3: one 4096-token sequence of V3
+    logits per step through the oracle's gate and balance-loss gradients."""
+    from deepseekmoe_routing_expert_moe_b300 import inputs
+    from oracle import moe_oracle as O
+    cfg = inputs.CONFIGS["route_v3"]
+    S = 4096
+    z = inputs.random_logits(cfg, T=S)
+    idx = O.route(z, inputs.bias(cfg), cfg.n_group, cfg.topk_group,
+                  cfg.topk)["idx"]
+    dg = np.random.default_rng(5).standard_normal((S, cfg.topk))
+
+    def one():
+        O.route_backward(z, idx, dg)
+        O.seq_balance_loss_backward(z, S, cfg.topk)
+
+    for _ in range(args.warmup):
+        one()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        one()
+    tot = time.perf_counter() - t0
+    v = S * args.steps / tot
+    return {
+        "metric": "tokens/s through the routing backward at the V3 shape; "
+                  "oracle on the host cores",
+        "value": round(v, 1), "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(tot / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic, seeded",
+        "config": {"workload": f"route_backward_v3: one sequence of {S}"},
+        "impl": "reference",
+        "cpu_baseline": {"value": round(v, 1), "unit": "tokens/s",
+                         "cores": blas_threads(), "kind": "oracle",
+                         "sample": f"one {S}-token sequence per step"},
+        "e2e": {"value": round(v, 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
 def run_balance_reference(args):
     """Oracle arm of balance_v3: one 4096-token sequence of V3-shaped
     logits per step through the oracle's balance loss."""
@@ -1074,6 +1115,8 @@ def run_reference(args):
         return run_balance_reference(args)
     if args.workload in ("decode_v3_fp8", "prefill_v3_fp8"):
         return run_decode_fp8_reference(args)
+    if args.workload == "route_backward_v3":
+        return run_backward_reference(args)
     cfg = inputs.CONFIGS[args.workload]
     n = args.ref_tokens
     s = oracle_sample(cfg, n)
