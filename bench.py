@@ -734,7 +734,8 @@ def run_fp8_gpu(args, rank, world, local_rank):
     (quantise-on-permute) -> moe_expert_ffn_fp8 -> moe_combine ->
     moe_bias_update.  The weights are quantized to E4M3 (128 x 128 block
     scales) once, before timing, as a deployment would store them.  4
-    rotating token batches; 11.3 GB of FP8 weights > L2."""
+    rotating token batches; the E4M3 weights (11.3 GB at 256 experts, 1.4 GB
+    for the 32-expert profiling stand-in) exceed L2."""
     import torch
     from deepseekmoe_routing_expert_moe_b300 import inputs, ops
     torch.cuda.set_device(local_rank)
@@ -856,7 +857,8 @@ def run_fp8_gpu(args, rank, world, local_rank):
                                f"H={H}, E={E}+1 shared, I={I}, top-{K}, "
                                "FP8 experts",
                    "T": T, "H": H, "E": E, "topk": K, "I": I,
-                   "l2": "11.3 GB of E4M3 weights streamed per step > L2"},
+                   "l2": f"{(E * 3 * I * H + 3 * Is * H) / 1e9:.1f} GB of "
+                         "E4M3 weights streamed per step > L2"},
         "roofline": roof,
         "e2e": {"value": round(T * args.steps / (e2e_ms / 1e3), 1),
                 "unit": "tokens/s", "h2d_bytes_per_step": T * H * 2,
@@ -1113,7 +1115,8 @@ def run_reference(args):
     from deepseekmoe_routing_expert_moe_b300 import inputs
     if args.workload == "balance_v3":
         return run_balance_reference(args)
-    if args.workload in ("decode_v3_fp8", "prefill_v3_fp8"):
+    if args.workload in ("decode_v3_fp8", "prefill_v3_fp8",
+                         "decode_v3_e32_fp8"):
         return run_decode_fp8_reference(args)
     if args.workload == "route_backward_v3":
         return run_backward_reference(args)
@@ -1153,7 +1156,7 @@ def main():
                     choices=("prefill_v3", "decode_v3", "skewed_v3",
                              "route_v3", "prefill_v3_e32", "balance_v3",
                              "decode_v3_fp8", "prefill_v3_fp8",
-                             "route_backward_v3"))
+                             "decode_v3_e32_fp8", "route_backward_v3"))
     ap.add_argument("--cpu-sample-tokens", type=int, default=4)
     ap.add_argument("--ref-tokens", type=int, default=1)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -1179,7 +1182,8 @@ def main():
         res = run_route_gpu(args, rank, world, local_rank)
     elif args.workload == "balance_v3":
         res = run_balance_gpu(args, rank, world, local_rank)
-    elif args.workload in ("decode_v3_fp8", "prefill_v3_fp8"):
+    elif args.workload in ("decode_v3_fp8", "prefill_v3_fp8",
+                           "decode_v3_e32_fp8"):
         res = run_fp8_gpu(args, rank, world, local_rank)
     elif args.workload == "route_backward_v3":
         res = run_backward_gpu(args, rank, world, local_rank)

@@ -99,6 +99,12 @@ CONFIGS = {
     "prefill_v3_e32": MoEConfig("prefill_v3_e32", 5, T=512, H=7168, E=32,
                                 n_group=8, topk_group=4, topk=8, I=2048,
                                 I_shared=2048),
+    # profiling stand-in for the FP8 decode layer: the decode batch (128
+    # tokens, top-8) over 32 experts -- 32 rows each, one full token tile --
+    # so that the E4M3 weights (1.4 GB) fit a full counter capture
+    "decode_v3_e32": MoEConfig("decode_v3_e32", 6, T=128, H=7168, E=32,
+                               n_group=8, topk_group=4, topk=8, I=2048,
+                               I_shared=2048),
 }
 
 
