@@ -6,8 +6,10 @@ data-parallel step needs one exchange -- a sum of the E-entry count vector
 -- after which every replica applies the same +-gamma step.  This checks,
 with the oracle on two gloo ranks, that the all-reduced shard histograms
 equal the unsharded batch's and that both ranks end with the bias of the
-unsharded run, bit for bit; and that the bench's max-over-ranks timing
-reduction picks the slowest rank."""
+unsharded run, bit for bit; that every rank derives the same
+redundant-expert plan (§5.1) from the all-reduced load, equal to the plan of
+the unsharded batch; and that the bench's max-over-ranks timing reduction
+picks the slowest rank."""
 import os
 import socket
 
@@ -41,9 +43,10 @@ def _worker(rank, world, port, q):
     c = torch.from_numpy(O.expert_counts(r["idx"], cfg.E).astype(np.int64))
     dist.all_reduce(c, op=dist.ReduceOp.SUM)
     nb, _ = O.bias_update(c.numpy(), b, T, cfg.topk, cfg.gamma)
+    plan = O.plan_redundant_experts(c.numpy(), 32, 1)["slot_expert"]
     t = torch.tensor([1.0 + rank], dtype=torch.float64)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    q.put((rank, c.numpy(), nb, float(t)))
+    q.put((rank, c.numpy(), nb, plan, float(t)))
     dist.destroy_process_group()
 
 
@@ -69,7 +72,10 @@ def test_sharded_counts_and_bias_step_match_the_whole_batch():
     r = O.route(z, b, cfg.n_group, cfg.topk_group, cfg.topk)
     c_all = O.expert_counts(r["idx"], cfg.E)
     nb_all, _ = O.bias_update(c_all, b, 2048, cfg.topk, cfg.gamma)
-    for rank, c, nb, tmax in res:
+    plan_all = O.plan_redundant_experts(c_all.astype(np.int64), 32, 1)[
+        "slot_expert"]
+    for rank, c, nb, plan, tmax in res:
         assert np.array_equal(c, c_all)
         assert np.array_equal(nb.view(np.uint32), nb_all.view(np.uint32))
+        assert np.array_equal(plan, plan_all)
         assert tmax == 2.0
