@@ -863,7 +863,10 @@ def run_fp8_gpu(args, rank, world, local_rank):
         "e2e": {"value": round(T * args.steps / (e2e_ms / 1e3), 1),
                 "unit": "tokens/s", "h2d_bytes_per_step": T * H * 2,
                 "d2h_bytes_per_step": T * H * 2},
-        "gpu_launches": (10 + router_extra_launches(T, H, E)) * args.steps,
+        # router 1 (+ weight split, + split-K sum), route + count scan 2,
+        # dispatch order (block counts, scan, dest) 3, quantise-on-permute
+        # 1, FP8 up + down 2, combine 1, bias step 1
+        "gpu_launches": (11 + router_extra_launches(T, H, E)) * args.steps,
         "clocks": clocks,
         "experts_touched": touched,
         "impl": "b300",
