@@ -249,7 +249,9 @@ moe_status_t moe_bias_update(const moe_dims_t* d, const int32_t* counts,
  *   P_seq      [n_seq, E]  fp32  out
  *   loss       [n_seq]     fp32  out
  * fp32 arithmetic in a fixed order (per token: lane partial sums, then a
- * butterfly; per sequence: 32 token ranges, then the ranges in order).
+ * butterfly; per sequence: up to ceil(seq_len/256) row splits, each cut
+ * into 32 token ranges summed in token order, the ranges and then the
+ * splits added in order), so results are reproducible run to run.
  * seq_len < 1 or a non-finite alpha: MOE_ERR_INVALID_ARG.  n_group and
  * topk_group are validated but not used.  Workspace: MOE_WS_SEQ_BALANCE. */
 moe_status_t moe_seq_balance_loss(const moe_dims_t* d, const float* logits,
