@@ -21,6 +21,13 @@ What it computes, and where the pages say so (page titles as cited):
   gamma = 0.001.
 * same page §1.1: every expert is a SwiGLU FFN with three matrices
   (7168 x 2048 each for V3).
+* same page §1.4, eq. 17-20: the sequence-wise balance loss
+  alpha * sum_i f_i P_i (alpha = 1e-4), and its gradient to the logits
+  together with the gates' (the routing backward).
+* same page §2: FP8 (E4M3) with one scale per 1 x 128 activation tile and
+  128 x 128 weight block, and the expert FFN on those values.
+* same page §5.1: redundant copies of high-load experts from the load
+  statistics.
 
 The page's formulas were lost in extraction; each step below restates the
 prose.  Readings where the pages are silent (tie-breaks, the "at the mean"
@@ -34,8 +41,10 @@ the exact IEEE operation order written here, because floating point decides
 an index there and both sides must take that decision in the same precision.
 
 Parity status: every function here is pinned by a ``-m "not gpu"`` test
-(closed forms, brute force on tiny inputs, invariants the pages state, and
-textbook reductions) -- see tests/test_oracle_pins.py.
+(closed forms, brute force on tiny inputs, invariants the pages state,
+finite differences, and textbook reductions) -- see tests/test_oracle_pins.py,
+test_oracle_balance_pins.py, test_oracle_fp8_pins.py,
+test_oracle_backward_pins.py and test_planner.py.
 """
 from __future__ import annotations
 
