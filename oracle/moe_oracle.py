@@ -564,3 +564,40 @@ def seq_balance_loss_backward(logits: np.ndarray, seq_len: int, topk: int,
         out[a:b] = dl[q] * alpha / (b - a) * s[a:b] * (1 - s[a:b]) / S[a:b] \
             * (f[None, :] - dot[:, None])
     return out
+
+
+# --------------------------------------------------------------------------
+# Backward of the experts and of the combine (§1.1 SwiGLU, eq. 12), fp64.
+# --------------------------------------------------------------------------
+def swiglu_ffn_backward(a, w1, w3, w2, dy):
+    """Gradients of y = W2 (silu(W1 a) * (W3 a)) for rows a [n, H], given
+    dy [n, H]; with p = a W1^T, q = a W3^T, m = silu(p) q:
+      dm  = dy W2            dW2 = dy^T m
+      dq  = dm silu(p)       dp  = dm q silu'(p),
+                             silu'(p) = sigma(p) (1 + p (1 - sigma(p)))
+      dW1 = dp^T a           dW3 = dq^T a
+      da  = dp W1 + dq W3
+    Returns (da [n, H], dw1 [I, H], dw3 [I, H], dw2 [H, I])."""
+    a = np.asarray(a, np.float64)
+    w1, w3, w2 = (np.asarray(w, np.float64) for w in (w1, w3, w2))
+    dy = np.asarray(dy, np.float64)
+    p = a @ w1.T
+    q = a @ w3.T
+    sg = 1.0 / (1.0 + np.exp(-p))
+    m = p * sg * q
+    dm = dy @ w2
+    dw2 = dy.T @ m
+    dq = dm * p * sg
+    dp = dm * q * sg * (1.0 + p * (1.0 - sg))
+    return dp @ w1 + dq @ w3, dp.T @ a, dq.T @ a, dw2
+
+
+def combine_backward(dout, y_slots, gate):
+    """Gradients of out_t = x_t + ys_t + sum_k g_{t,k} y_{t,k} (eq. 12):
+    dx_t (residual) = dys_t = dout_t, dy_{t,k} = g_{t,k} dout_t and
+    dgate_{t,k} = <dout_t, y_{t,k}> (the input of route_backward).
+    Returns (dx_residual, dys, dy_slots [T, K, H], dgate [T, K])."""
+    d = np.asarray(dout, np.float64)
+    y = np.asarray(y_slots, np.float64)
+    g = np.asarray(gate, np.float64)
+    return d, d, g[:, :, None] * d[:, None, :], np.einsum("th,tkh->tk", d, y)
