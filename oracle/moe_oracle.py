@@ -43,8 +43,9 @@ an index there and both sides must take that decision in the same precision.
 Parity status: every function here is pinned by a ``-m "not gpu"`` test
 (closed forms, brute force on tiny inputs, invariants the pages state,
 finite differences, and textbook reductions) -- see tests/test_oracle_pins.py,
-test_oracle_balance_pins.py, test_oracle_fp8_pins.py,
-test_oracle_backward_pins.py and test_planner.py.
+test_oracle_margin_pins.py, test_oracle_balance_pins.py,
+test_oracle_fp8_pins.py, test_oracle_backward_pins.py,
+test_oracle_expert_backward_pins.py and test_planner.py.
 """
 from __future__ import annotations
 
