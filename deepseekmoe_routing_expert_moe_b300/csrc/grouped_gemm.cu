@@ -170,8 +170,13 @@ __device__ __forceinline__ Unit decode_unit(int u, const int* useg,
   return x;
 }
 
+// silu(g) = g / (1 + e^-g).  The exponent's argument is capped at 80 so
+// that 1 + e stays below 2^116, inside the documented range of the fast
+// division, for every g: below g = -80 the true value is under 1e-33 in
+// magnitude and the capped form returns g / (1 + e^80), also under 1e-33
+// (a NaN g stays NaN).
 __device__ __forceinline__ float silu_f(float g) {
-  return __fdividef(g, 1.0f + __expf(-g));
+  return __fdividef(g, 1.0f + __expf(fminf(-g, 80.0f)));
 }
 
 // Columns [0, n) of this thread's TMEM lane (accumulator at `taddr`),

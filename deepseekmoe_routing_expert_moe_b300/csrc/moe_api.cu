@@ -747,24 +747,71 @@ namespace {
 constexpr size_t kRouteScratchInts = 262144;  // 1 MiB of int32
 static __device__ __align__(256) int32_t g_route_scratch[kRouteScratchInts];
 
-constexpr int kMaxScratchDevices = 64;
-int32_t* g_route_scratch_ptr[kMaxScratchDevices] = {};
+// The address is cached per CUDA context, keyed by the context's unique id
+// (cuCtxGetId, through the runtime's driver entry point so libmoe needs no
+// -lcuda): after cudaDeviceReset the module may load at another address in
+// the new primary context, and a cache keyed by device ordinal would hand
+// the kernel a stale pointer.
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+struct ScratchEntry {
+  unsigned long long ctx_id;
+  int32_t* ptr;
+};
+constexpr int kMaxScratchContexts = 64;
+ScratchEntry g_route_scratch_ptr[kMaxScratchContexts] = {};
+int g_route_scratch_n = 0;
 std::mutex g_route_scratch_mu;
 
-// Device address of g_route_scratch on the current device, looked up once
-// per device (the host-side name is only a stand-in for it).
-moe_status_t route_scratch_current_device(int32_t** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
-  if (dev < 0 || dev >= kMaxScratchDevices) return MOE_ERR_UNSUPPORTED;
-  std::lock_guard<std::mutex> lock(g_route_scratch_mu);
-  if (g_route_scratch_ptr[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_route_scratch) != cudaSuccess || p == nullptr)
+template <typename F>
+F driver_fn(const char* name) {
+  void* f = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion(name, &f, 12000, cudaEnableDefault,
+                                       &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess)
+    return nullptr;
+  return reinterpret_cast<F>(f);
+}
+
+// Device address of g_route_scratch in the current context (the host-side
+// name is only a stand-in for it), looked up once per context.
+moe_status_t route_scratch_current_context(int32_t** out) {
+  static const CtxGetCurrentFn get_ctx =
+      driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent");
+  static const CtxGetIdFn get_id = driver_fn<CtxGetIdFn>("cuCtxGetId");
+  if (get_ctx == nullptr || get_id == nullptr) return MOE_ERR_CUDA;
+  CUcontext ctx = nullptr;
+  if (get_ctx(&ctx) != CUDA_SUCCESS) return MOE_ERR_CUDA;
+  if (ctx == nullptr) {
+    // no context bound to this thread yet: cudaSetDevice makes the current
+    // device's primary context current (it allocates nothing)
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaSetDevice(dev) != cudaSuccess ||
+        get_ctx(&ctx) != CUDA_SUCCESS || ctx == nullptr)
       return MOE_ERR_CUDA;
-    g_route_scratch_ptr[dev] = static_cast<int32_t*>(p);
   }
-  *out = g_route_scratch_ptr[dev];
+  unsigned long long id = 0;
+  if (get_id(ctx, &id) != CUDA_SUCCESS) return MOE_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_route_scratch_mu);
+  for (int i = 0; i < g_route_scratch_n; ++i) {
+    if (g_route_scratch_ptr[i].ctx_id == id) {
+      *out = g_route_scratch_ptr[i].ptr;
+      return MOE_OK;
+    }
+  }
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_route_scratch) != cudaSuccess || p == nullptr)
+    return MOE_ERR_CUDA;
+  // a full table (more than 64 contexts over the process's life) reuses
+  // the entry the id hashes to; ids are never reused, so no lookup can
+  // return another context's address
+  const int slot = g_route_scratch_n < kMaxScratchContexts
+                       ? g_route_scratch_n++
+                       : static_cast<int>(id % kMaxScratchContexts);
+  g_route_scratch_ptr[slot] = {id, static_cast<int32_t*>(p)};
+  *out = static_cast<int32_t*>(p);
   return MOE_OK;
 }
 
@@ -792,7 +839,7 @@ extern "C" moe_status_t moe_route_static_scratch(
   if (d->T == 0)
     return cuda_ok(cudaMemsetAsync(counts, 0, sizeof(int32_t) * d->E, s));
   int32_t* scratch = nullptr;
-  MOE_TRY(route_scratch_current_device(&scratch));
+  MOE_TRY(route_scratch_current_context(&scratch));
   // every block writes its whole histogram row before the scan reads it,
   // so nothing left from an earlier call needs clearing
   MOE_TRY(cuda_ok(moe::launch_route(logits, bias, d->T, d->E, d->n_group,

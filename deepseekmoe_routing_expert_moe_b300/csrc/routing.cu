@@ -933,7 +933,9 @@ __global__ void __launch_bounds__(kRowThreads)
 // fp32 arithmetic, slots in order.  One block per token, 8 bf16 per thread
 // per step; for topk <= KU the K expert rows of a step are all requested
 // before any is accumulated (the kernel is an HBM stream of 10 rows per
-// token), the sum itself still in slot order.
+// token), the sum itself still in slot order.  A slot whose dest lies
+// outside [0, rows) is skipped: its row is neither loaded nor added (the
+// test is uniform across the block, so it costs no divergence).
 // ===================================================================
 template <int KU>
 __global__ void __launch_bounds__(kRowThreads)
@@ -948,8 +950,8 @@ __global__ void __launch_bounds__(kRowThreads)
   const int t = blockIdx.x;
   if (threadIdx.x < K) {
     const int r = dest[(size_t)t * K + threadIdx.x];
-    const bool ok = r >= 0 && r < rows;  // an invalid slot adds nothing
-    sd[threadIdx.x] = ok ? r : 0;
+    const bool ok = r >= 0 && r < rows;
+    sd[threadIdx.x] = ok ? r : -1;
     sg[threadIdx.x] = ok ? gate[(size_t)t * K + threadIdx.x] : 0.f;
   }
   __syncthreads();
@@ -962,7 +964,7 @@ __global__ void __launch_bounds__(kRowThreads)
     if (KU > 0) {
 #pragma unroll
       for (int k = 0; k < KU; ++k)
-        if (k < K)
+        if (k < K && sd[k] >= 0)
           yv[k] = __ldg(reinterpret_cast<const uint4*>(yp + (size_t)sd[k] * H) +
                         c);
     }
@@ -985,12 +987,13 @@ __global__ void __launch_bounds__(kRowThreads)
     if (KU > 0) {
 #pragma unroll
       for (int k = 0; k < KU; ++k)
-        if (k < K) add_row(yv[k], sg[k]);
+        if (k < K && sd[k] >= 0) add_row(yv[k], sg[k]);
     } else {
       for (int k = 0; k < K; ++k)
-        add_row(__ldg(reinterpret_cast<const uint4*>(yp + (size_t)sd[k] * H) +
-                      c),
-                sg[k]);
+        if (sd[k] >= 0)
+          add_row(__ldg(reinterpret_cast<const uint4*>(yp + (size_t)sd[k] * H) +
+                        c),
+                  sg[k]);
     }
     uint4 o;
     o.x = pack_bf16x2(acc[0], acc[1]);

@@ -173,8 +173,9 @@ moe_status_t moe_route(const moe_dims_t* d, const float* logits,
  * exits; it allocates nothing and calls no allocating routine.
  *   Limit: ceil(T/64) * E <= 262144 (T <= 65536 at E = 256), else
  *   MOE_ERR_WORKSPACE before anything is launched.
- *   The first call on a device looks up the array's device address (one
- *   cudaGetSymbolAddress per device); make that first call before any
+ *   The first call in a CUDA context looks up the array's device address
+ *   (one cudaGetSymbolAddress per context, so a context re-created after
+ *   cudaDeviceReset gets its own lookup); make that first call before any
  *   stream capture.
  *   All calls share the array: calls whose kernels overlap on the GPU (on
  *   different streams, or from several threads) race on it and must be
@@ -210,7 +211,9 @@ moe_status_t moe_permute(const moe_dims_t* d, const uint16_t* x,
  *   offsets [E+1]    int32 as written by moe_permute (read on the device)
  *   yp      [T*K, H] bf16  out, FFN_e(row) for every routed row (ungated)
  *   ys      [T, H]   bf16  out, FFN_shared(x_t)
- * Workspace: MOE_WS_EXPERT_FFN. */
+ * Workspace: MOE_WS_EXPERT_FFN.  The intermediate h = silu(p) * q of the
+ * routed rows, [T*K, I] bf16, is left in a MOE_WS_EXPERT_FFN workspace at
+ * byte offset 256 until the next call (for inspection). */
 moe_status_t moe_expert_ffn(const moe_dims_t* d, const moe_weights_t* w,
                             const uint16_t* xp, const uint16_t* x,
                             const int32_t* offsets, uint16_t* yp,
@@ -219,7 +222,9 @@ moe_status_t moe_expert_ffn(const moe_dims_t* d, const moe_weights_t* w,
 
 /* Combine (eq. 12): out_t = bf16( x_t + ys_t + sum_k g_{t,k} yp[dest[t,k]] ),
  * fp32 arithmetic, slots summed in order.  out [T, H] bf16 may not alias
- * the inputs.  Needs no workspace. */
+ * the inputs.  A slot whose dest lies outside [0, T*K) (moe_permute writes
+ * -1 for an invalid expert id) contributes nothing: its yp row is not read.
+ * Needs no workspace. */
 moe_status_t moe_combine(const moe_dims_t* d, const uint16_t* x,
                          const uint16_t* ys, const uint16_t* yp,
                          const int32_t* dest, const float* topk_gate,

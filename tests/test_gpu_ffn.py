@@ -158,3 +158,20 @@ def test_ffn_bad_offsets_are_rejected_on_device():
     x_in = z((T, H), dtype=torch.int16, device="cuda")
     ops.moe_expert_ffn(d, W, xp_in, x_in, dev(off), yp, ys, ws)
     assert ops.moe_get_device_error(ws) == ops.STATUS_CODES["MOE_ERR_DEVICE_BOUNDS"]
+
+
+def test_ffn_large_magnitude_preactivations():
+    """Weights ~ N(0, 16): the gate pre-activations p = W1 a reach several
+    hundred in magnitude, so silu's far negative tail (p < -88, where
+    e^-p overflows fp32) and its linear regime are both exercised.  The
+    outputs stay finite and within the elementwise bound of the fp64
+    SwiGLU."""
+    cfg = inputs.custom_config("ffn_big", 506, T=200, H=256, E=8, n_group=4,
+                               topk_group=2, topk=2, I=128, I_shared=128,
+                               w_sigma=16.0, router_sigma=0.05)
+    f = inputs.bf16_bits_to_f32
+    x = f(inputs.x_tokens(cfg)).astype(np.float64)
+    ws1 = f(inputs.shared_weights(cfg)[0]).astype(np.float64)
+    pre = x @ ws1.T
+    assert pre.min() < -200 and pre.max() > 200
+    run_ffn(cfg)

@@ -109,3 +109,34 @@ def test_invalid_expert_ids_are_reported_not_followed():
     dh = host(dest)
     assert dh[7, 1] == -1 and dh[9, 0] == -1
     assert ops.moe_get_device_error(ws) == 0   # reading clears the word
+
+
+def test_permute_skewed_32768_tokens_bit_exact():
+    """The skewed-load batch (T = 32768, Zipf s = 1.2 preference on the
+    logits): hot experts hold thousands of rows each.  Offsets, dest and
+    src_row equal the oracle's stable counting sort bit for bit, and every
+    one of the 262144 gathered rows equals its token's row."""
+    cfg = inputs.CONFIGS["skewed_v3"]
+    T, K, E = cfg.T, cfg.topk, cfg.E
+    x = inputs.x_tokens(cfg)
+    z = O.router_logits(inputs.bf16_bits_to_f32(x), inputs.router_weight(cfg),
+                        inputs.zipf_preference(cfg))
+    r = O.route(z, inputs.bias(cfg), cfg.n_group, cfg.topk_group, K)
+    del z
+    ref = O.permutation(r["idx"], E)
+    counts = np.diff(ref["offsets"])
+    assert counts.max() > 8 * counts.mean()
+    d = ops.dims_of(cfg)
+    offsets = torch.full((E + 1,), -9, dtype=torch.int32, device="cuda")
+    dest = torch.full((T, K), -9, dtype=torch.int32, device="cuda")
+    src_row = torch.full((T * K,), -9, dtype=torch.int32, device="cuda")
+    xd = dev(x)
+    xp = torch.zeros((T * K, cfg.H), dtype=torch.int16, device="cuda")
+    ws = ops.workspace(d, ops.MOE_WS_PERMUTE)
+    ops.moe_permute(d, xd, dev(r["idx"]), offsets, dest, src_row, xp, ws)
+    assert ops.moe_get_device_error(ws) == 0
+    assert np.array_equal(host(offsets), ref["offsets"])
+    assert np.array_equal(host(dest), ref["dest"])
+    assert np.array_equal(host(src_row), ref["src_row"])
+    tok = torch.from_numpy((ref["src_row"] // K).astype(np.int64)).cuda()
+    assert torch.equal(xp, xd[tok])
