@@ -472,14 +472,16 @@ def run_route_gpu(args, rank, world, local_rank):
     ws = ops.workspace(d, ops.MOE_WS_PERMUTE)
     stream = torch.cuda.current_stream()
 
-    def step(i, ev=None):
-        if ev: ev[0].record(stream)
-        ops.moe_route(d, zs[i % NB], bias, idx, gate, counts, ws)
-        if ev: ev[1].record(stream)
-        ops.moe_permute(d, None, idx, offsets, dest, src_row, None, ws)
-        if ev: ev[2].record(stream)
-        ops.moe_bias_update(d, counts, bias)
-        if ev: ev[3].record(stream)
+    calls = (
+        lambda i: ops.moe_route(d, zs[i % NB], bias, idx, gate, counts, ws),
+        lambda i: ops.moe_permute(d, None, idx, offsets, dest, src_row, None,
+                                  ws),
+        lambda i: ops.moe_bias_update(d, counts, bias),
+    )
+
+    def step(i):
+        for c in calls:
+            c(i)
 
     for i in range(args.warmup):
         step(i)
@@ -490,18 +492,19 @@ def run_route_gpu(args, rank, world, local_rank):
     # are captured once in a CUDA graph and the graph is replayed.
     side = torch.cuda.Stream()
     side.wait_stream(stream)
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.stream(side):
-        with torch.cuda.graph(g, stream=side):
-            for i in range(NB):
-                step(i)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)]
-           for _ in range(NB)]
-    ge = torch.cuda.CUDAGraph()     # the same steps with events between calls
-    with torch.cuda.stream(side):
-        with torch.cuda.graph(ge, stream=side):
-            for i in range(NB):
-                step(i, evs[i])
+
+    def capture(fn):
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(gr, stream=side):
+                for i in range(NB):
+                    fn(i)
+        return gr
+
+    g = capture(step)
+    # each public call alone, NB times per graph (its own per-call time,
+    # with nothing recorded between the kernels)
+    g_calls = [capture(c) for c in calls]
     stream.wait_stream(side)
     reps = max(1, args.steps // NB)
     for _ in range(max(1, args.warmup // NB)):
@@ -518,10 +521,17 @@ def run_route_gpu(args, rank, world, local_rank):
     ms = ev0.elapsed_time(ev1)
     clocks = clk.summary()
     args.steps = reps * NB
-    ge.replay()
-    torch.cuda.synchronize()
-    kt = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(3)]
-                   for e in evs]).mean(0)
+    kt = []
+    for gc in g_calls:
+        gc.replay()
+        torch.cuda.synchronize()
+        ev0.record(stream)
+        for _ in range(reps):
+            gc.replay()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        kt.append(ev0.elapsed_time(ev1) / (reps * NB))
+    kt = np.array(kt)
     # algorithmic bytes of the routing call (logits + bias read; idx,
     # gates, counts and the per-64-token histogram rows written)
     nblk = (T + 63) // 64

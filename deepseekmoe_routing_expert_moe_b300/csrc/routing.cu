@@ -178,10 +178,17 @@ __device__ __forceinline__ uint32_t f32_order_key(float v) {
 //   u = s + b                      selection score (eq. 16)
 //   S_g = top1 + top2 of u in g    group score (§1.3)
 //   kept = rank of (S_g desc, g asc) < topk_group
-//   slots: topk rounds of warp arg-max over kept u (ties: lower expert)
+//   slots: the topk largest (u desc, e asc) among the kept groups' experts
 //   gate_k = s_k / (s_0 + ... + s_{K-1}) summed in slot order (eq. 13)
-// The block's per-expert histogram is accumulated in shared memory with
-// integer atomics and written as one row of block_counts.
+// Selection: every lane sorts its EPL candidates once (Batcher's odd-even
+// merge network on a 64-bit key: the order-preserving bits of u above ~e,
+// so the key order is (u desc, e asc) and all keys are distinct; experts of
+// dropped groups get u-bits 0, below every kept expert) into shared memory.
+// Each of the topk rounds then compares only the lanes' list heads -- one
+// warp max of the u-bits, one of the ~e bits among the lanes holding that
+// maximum -- and the winning lane advances its head.  The block's
+// per-expert histogram is accumulated in shared memory with integer atomics
+// and written as one row of block_counts.
 // ===================================================================
 namespace {
 
@@ -206,6 +213,53 @@ __device__ __forceinline__ void load_row(const float* __restrict__ p,
   }
 }
 
+// descending compare-exchange of two distinct 64-bit keys
+__device__ __forceinline__ void cx_desc(uint64_t& a, uint64_t& b) {
+  const uint64_t hi = a > b ? a : b;
+  const uint64_t lo = a > b ? b : a;
+  a = hi;
+  b = lo;
+}
+
+// Batcher's odd-even merge sort of N (a power of 2) keys, descending; all
+// indices are compile-time constants once the loops are unrolled, so the
+// keys stay in registers (19 compare-exchanges for N = 8)
+template <int N>
+__device__ __forceinline__ void sort_desc(uint64_t (&k)[N]) {
+#pragma unroll
+  for (int p = 1; p < N; p <<= 1) {
+#pragma unroll
+    for (int q = p; q >= 1; q >>= 1) {
+#pragma unroll
+      for (int j = q % p; j <= N - 1 - q; j += 2 * q) {
+#pragma unroll
+        for (int i = 0; i < q; ++i) {
+          if (i + j + q < N && (i + j) / (2 * p) == (i + j + q) / (2 * p))
+            cx_desc(k[i + j], k[i + j + q]);
+        }
+      }
+    }
+  }
+}
+
+// A plain load of shared memory the calling thread wrote earlier, kept as
+// a load: the sorted lists are written from registers that the sorting
+// network permuted, and the compiler is not to substitute a register for
+// this dynamically indexed read.
+__device__ __forceinline__ uint64_t ld_shared_u64(const uint64_t* p) {
+  uint64_t v;
+  asm volatile("ld.shared.u64 %0, [%1];" : "=l"(v) : "r"(smem_u32(p)) : "memory");
+  return v;
+}
+
+// shared memory of one warp: the sorted candidate lists, entry h of lane l
+// at [h][l] (a warp's stores of one h are consecutive), then s by expert
+template <int EPL>
+struct RouteWarpSmem {
+  static constexpr int KEY_BYTES = EPL * 32 * 8;
+  static constexpr int BYTES = KEY_BYTES + EPL * 32 * 4;
+};
+
 template <int EPL, int WARPS>
 __global__ void __launch_bounds__(WARPS * 32)
     route_kernel(const float* __restrict__ logits,
@@ -214,7 +268,13 @@ __global__ void __launch_bounds__(WARPS * 32)
                  float* __restrict__ topk_gate,
                  int32_t* __restrict__ block_counts) {
   __shared__ int cnt[1024];
+  extern __shared__ __align__(16) uint8_t route_smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  uint64_t* skey = reinterpret_cast<uint64_t*>(
+      route_smem + warp * RouteWarpSmem<EPL>::BYTES);
+  float* ss = reinterpret_cast<float*>(
+      route_smem + warp * RouteWarpSmem<EPL>::BYTES +
+      RouteWarpSmem<EPL>::KEY_BYTES);
   for (int i = tid; i < E; i += blockDim.x) cnt[i] = 0;
   __syncthreads();
 
@@ -270,40 +330,42 @@ __global__ void __launch_bounds__(WARPS * 32)
       rank += (Sg > S) || (Sg == S && g < my_g);
     }
     const bool kept = active && my_g < G && rank < M;
-    float cu[EPL];
+    // ---- this lane's candidates, sorted once by (u desc, e asc)
+    uint64_t key[EPL];
 #pragma unroll
-    for (int j = 0; j < EPL; ++j) cu[j] = kept ? u[j] : -INFINITY;
-    // ---- top-K by (u desc, e asc)
+    for (int j = 0; j < EPL; ++j) {
+      const uint32_t hi = kept ? f32_order_key(u[j]) : 0u;
+      key[j] = (static_cast<uint64_t>(hi) << 32) |
+               static_cast<uint32_t>(~(lane * EPL + j));
+    }
+    sort_desc<EPL>(key);
+#pragma unroll
+    for (int j = 0; j < EPL; ++j) skey[j * 32 + lane] = key[j];
+    if (active) {
+#pragma unroll
+      for (int j = 0; j < EPL; ++j) ss[lane * EPL + j] = s[j];
+    }
+    __syncwarp();
+    // ---- top-K: K rounds over the lane heads
+    uint64_t head = key[0];
+    int h = 0;
     float den = 0.f, my_s = 0.f;
     int my_e = 0;
     for (int k = 0; k < K; ++k) {
-      float bv = -INFINITY;
-      int bj = 0;
-#pragma unroll
-      for (int j = 0; j < EPL; ++j) {
-        if (cu[j] > bv) {
-          bv = cu[j];
-          bj = j;
-        }
-      }
-      const uint32_t key = f32_order_key(bv);
-      const uint32_t kmax = __reduce_max_sync(0xffffffffu, key);
-      const int cand = (key == kmax && bv != -INFINITY) ? lane * EPL + bj
-                                                        : INT_MAX;
-      int e = __reduce_min_sync(0xffffffffu, cand);
-      if (e == INT_MAX) e = 0;  // only with non-finite scores: stay in bounds
-      const int owner = e / EPL, oj = e - owner * EPL;
-      float se = 0.f;
-      if (lane == owner) {
-#pragma unroll
-        for (int j = 0; j < EPL; ++j) {
-          if (j == oj) {
-            se = s[j];
-            cu[j] = -INFINITY;
-          }
-        }
-      }
-      se = __shfl_sync(0xffffffffu, se, owner);
+      const uint32_t khi = static_cast<uint32_t>(head >> 32);
+      const uint32_t mhi = __reduce_max_sync(0xffffffffu, khi);
+      const uint32_t klo =
+          khi == mhi ? static_cast<uint32_t>(head) : 0u;
+      const uint32_t mlo = __reduce_max_sync(0xffffffffu, klo);
+      int e = static_cast<int>(~mlo);
+      // only a non-finite bias can exhaust the kept candidates: stay in
+      // bounds
+      if (mhi == 0u || e < 0 || e >= E) e = 0;
+      // the lane that won advances its head (every lane reloads its own,
+      // branch-free)
+      h += (khi == mhi && static_cast<uint32_t>(head) == mlo) ? 1 : 0;
+      head = h < EPL ? ld_shared_u64(&skey[h * 32 + lane]) : 0ull;
+      const float se = ss[e];
       den = __fadd_rn(den, se);
       if (lane == k) {
         my_e = e;
@@ -315,6 +377,7 @@ __global__ void __launch_bounds__(WARPS * 32)
       topk_gate[(size_t)t * K + lane] = __fdiv_rn(my_s, den);
       atomicAdd(&cnt[my_e], 1);
     }
+    __syncwarp();
   }
   __syncthreads();
   for (int i = tid; i < E; i += blockDim.x)
@@ -1014,31 +1077,45 @@ cudaError_t launch_route(const float* logits, const float* bias, int T, int E,
   const int epl = E <= 32 ? 1 : E / 32;
   const int lpg = (E / n_group) / epl;
   // more warps per block (fewer tokens per warp) while the grid fits on the
-  // SMs at once; measured on B300 at the V3 shape: T=4096 30 -> 18.5 us
-  // (8 -> 32 warps), T=16384 37 -> 33 us (8 -> 16 warps)
+  // SMs at once
   const bool wide = nblk <= sm_count() && epl <= 8;
+#define MOE_ROUTE_LAUNCH(N, W)                                               \
+  {                                                                          \
+    const int smem = (W) * RouteWarpSmem<N>::BYTES;                          \
+    /* the static histogram (4 KB) counts against the 48 KB default too */  \
+    if (cudaFuncSetAttribute(route_kernel<N, W>,                             \
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,    \
+                             smem) != cudaSuccess)                           \
+      return cudaErrorInvalidValue;                                          \
+    route_kernel<N, W><<<nblk, (W) * 32, smem, s>>>(                         \
+        logits, bias, T, E, n_group, topk_group, topk, lpg, topk_idx,        \
+        topk_gate, block_counts);                                            \
+  }
 #define MOE_ROUTE_CASE(N)                                                    \
   case N:                                                                    \
     if (wide)                                                                \
-      route_kernel<N, 32><<<nblk, 32 * 32, 0, s>>>(                          \
-          logits, bias, T, E, n_group, topk_group, topk, lpg, topk_idx,      \
-          topk_gate, block_counts);                                          \
+      MOE_ROUTE_LAUNCH(N, 32)                                                \
     else                                                                     \
-      route_kernel<N, 16><<<nblk, 16 * 32, 0, s>>>(                          \
-          logits, bias, T, E, n_group, topk_group, topk, lpg, topk_idx,      \
-          topk_gate, block_counts);                                          \
+      MOE_ROUTE_LAUNCH(N, 16)                                                \
+    break;
+  // 16 or 32 experts per lane (E = 512, 1024): 16 warps per block only
+#define MOE_ROUTE_CASE_NARROW(N)                                             \
+  case N:                                                                    \
+    MOE_ROUTE_LAUNCH(N, 16)                                                  \
     break;
   switch (epl) {
     MOE_ROUTE_CASE(1)
     MOE_ROUTE_CASE(2)
     MOE_ROUTE_CASE(4)
     MOE_ROUTE_CASE(8)
-    MOE_ROUTE_CASE(16)
-    MOE_ROUTE_CASE(32)
+    MOE_ROUTE_CASE_NARROW(16)
+    MOE_ROUTE_CASE_NARROW(32)
     default:
       return cudaErrorInvalidValue;
   }
+#undef MOE_ROUTE_CASE_NARROW
 #undef MOE_ROUTE_CASE
+#undef MOE_ROUTE_LAUNCH
   return cudaGetLastError();
 }
 
