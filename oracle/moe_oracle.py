@@ -602,3 +602,46 @@ def combine_backward(dout, y_slots, gate):
     y = np.asarray(y_slots, np.float64)
     g = np.asarray(gate, np.float64)
     return d, d, g[:, :, None] * d[:, None, :], np.einsum("th,tkh->tk", d, y)
+
+
+def layer_backward(x, dout, idx, gate, w1, w3, w2, ws1, ws3, ws2):
+    """Backward of the layer's expert part for a fixed routing (§1.1 SwiGLU
+    experts, eq. 12 combine), fp64, from the pinned pieces above.
+
+    out_t = x_t + FFN_s(x_t) + sum_k g_{t,k} FFN_{e_k}(x_t)   (eq. 12)
+    Given dout [T, H]:
+      dgate[t, k] = <dout_t, FFN_{e_k}(x_t)>                (combine_backward)
+      dx_t        = dout_t + dFFN_s(x_t)^T dout_t
+                    + sum_k dFFN_{e_k}(x_t)^T (g_{t,k} dout_t)
+                    (residual, shared and routed experts; the path through
+                    the router's logits is route_backward's, not this one)
+      dW*_e       = swiglu_ffn_backward over the rows routed to e, with the
+                    upstream gradient g_{t,k} dout_t; the shared expert's
+                    over all tokens with dout_t.
+    Weight arguments hold values: w1, w3 [E, I, H], w2 [E, H, I]; ws*
+    shared.  Returns dict(dx [T, H], dgate [T, K], dw1, dw3 [E, I, H],
+    dw2 [E, H, I], dws1, dws3 [I_s, H], dws2 [H, I_s])."""
+    x64 = np.asarray(x, np.float64)
+    d = np.asarray(dout, np.float64)
+    idx = np.asarray(idx)
+    g = np.asarray(gate, np.float64)
+    T, K = idx.shape
+    E = w1.shape[0]
+    dxs, dws1, dws3, dws2 = swiglu_ffn_backward(x64, ws1, ws3, ws2, d)
+    dx = d + dxs
+    dgate = np.zeros((T, K))
+    dw1 = np.zeros(np.shape(w1))
+    dw3 = np.zeros(np.shape(w3))
+    dw2 = np.zeros(np.shape(w2))
+    for e in range(E):
+        t, k = np.nonzero(idx == e)
+        if t.size == 0:
+            continue
+        a = x64[t]
+        y = swiglu_ffn(a, w1[e], w3[e], w2[e])
+        dgate[t, k] = np.einsum("nh,nh->n", d[t], y)
+        da, dw1[e], dw3[e], dw2[e] = swiglu_ffn_backward(
+            a, w1[e], w3[e], w2[e], g[t, k][:, None] * d[t])
+        dx[t] += da          # a token chooses an expert at most once
+    return dict(dx=dx, dgate=dgate, dw1=dw1, dw3=dw3, dw2=dw2, dws1=dws1,
+                dws3=dws3, dws2=dws2)

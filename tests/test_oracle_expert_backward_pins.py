@@ -1,7 +1,10 @@
 """Pins for the oracle's expert and combine backward (no GPU): central
 finite differences of the pinned forward functions (swiglu_ffn, moe_output)
 and the chain from the layer output to the router logits through the gates
-(combine_backward's dgate into route_backward)."""
+(combine_backward's dgate into route_backward); and the composed
+layer_backward (all token, gate and weight gradients of eq. 12 with fixed
+routing) against finite differences, an unchosen expert, and the zero
+routed-weights reduction to the dense SwiGLU backward."""
 import numpy as np
 
 from oracle import moe_oracle as O
@@ -96,3 +99,72 @@ def test_output_to_logits_chain_through_the_gates():
     grad = O.route_backward(z, idx, dg)
     num = _fd(out_of, z.astype(np.float64))
     np.testing.assert_allclose(grad, num, rtol=1e-5, atol=1e-8)
+
+
+def _tiny_layer(seed, T=5, H=6, E=4, I=3, Is=4, K=2):
+    g = np.random.default_rng(seed)
+    x = g.normal(0, 1, (T, H))
+    w1, w3 = g.normal(0, 0.5, (E, I, H)), g.normal(0, 0.5, (E, I, H))
+    w2 = g.normal(0, 0.5, (E, H, I))
+    ws1, ws3 = g.normal(0, 0.5, (Is, H)), g.normal(0, 0.5, (Is, H))
+    ws2 = g.normal(0, 0.5, (H, Is))
+    idx = np.stack([g.choice(E, K, replace=False) for _ in range(T)])
+    gate = g.uniform(0.1, 1.0, (T, K))
+    dout = g.normal(0, 1, (T, H))
+    return x, dout, idx, gate, [w1, w3, w2, ws1, ws3, ws2]
+
+
+def _out_fixed_routing(x, idx, gate, w):
+    """eq. 12 with the routing and the gates held fixed, straight from the
+    forward pieces (moe_output of the per-slot swiglu_ffn values)."""
+    w1, w3, w2, ws1, ws3, ws2 = w
+    T, K = idx.shape
+    ys = O.swiglu_ffn(x, ws1, ws3, ws2)
+    y = np.zeros((T, K, x.shape[1]))
+    for t in range(T):
+        for k in range(K):
+            e = idx[t, k]
+            y[t, k] = O.swiglu_ffn(x[t:t + 1], w1[e], w3[e], w2[e])[0]
+    return O.moe_output(x, ys, y, gate)
+
+
+def test_layer_backward_matches_finite_differences():
+    """Every gradient of layer_backward against central differences of
+    <dout, out> with the routing and gates fixed: the token gradient (the
+    residual, shared and routed terms together), the routed experts' and
+    the shared expert's three weight gradients, and the gates."""
+    x, dout, idx, gate, w = _tiny_layer(4)
+    r = O.layer_backward(x, dout, idx, gate, *w)
+    L = lambda X, G, W: float((_out_fixed_routing(X, idx, G, W) * dout).sum())  # noqa: E731
+    np.testing.assert_allclose(r["dx"], _fd(lambda v: L(v, gate, w), x),
+                               rtol=1e-6, atol=1e-8)
+    np.testing.assert_allclose(r["dgate"], _fd(lambda v: L(x, v, w), gate),
+                               rtol=1e-6, atol=1e-8)
+    names = ["dw1", "dw3", "dw2", "dws1", "dws3", "dws2"]
+    for i, n in enumerate(names):
+        def Lw(v, i=i):
+            ww = list(w)
+            ww[i] = v
+            return L(x, gate, ww)
+        np.testing.assert_allclose(r[n], _fd(Lw, w[i]), rtol=1e-6,
+                                   atol=1e-8, err_msg=n)
+
+
+def test_layer_backward_unchosen_expert_has_zero_gradient():
+    x, dout, idx, gate, w = _tiny_layer(5)
+    idx = np.array([[0, 1], [1, 2], [2, 0], [0, 2], [1, 0]])   # never 3
+    assert not np.any(idx == 3)
+    r = O.layer_backward(x, dout, idx, gate, *w)
+    assert np.all(r["dw1"][3] == 0) and np.all(r["dw2"][3] == 0)
+    assert np.all(r["dw3"][3] == 0)
+
+
+def test_layer_backward_zero_routed_weights_is_dense_swiglu_backward():
+    """Routed experts all zero: dx = dout + the dense shared-expert token
+    gradient, and the gates' gradient is 0 (every routed output is 0)."""
+    x, dout, idx, gate, w = _tiny_layer(6)
+    w = [0 * w[0], 0 * w[1], 0 * w[2]] + w[3:]
+    r = O.layer_backward(x, dout, idx, gate, *w)
+    da = O.swiglu_ffn_backward(x, w[3], w[4], w[5], dout)[0]
+    np.testing.assert_allclose(r["dx"], dout + da, rtol=1e-12, atol=1e-12)
+    assert np.all(r["dgate"] == 0)
