@@ -109,6 +109,34 @@ struct FfnArgs {
 // 0 on success, else a moe_status_t (encoding or launch failure)
 int launch_expert_ffn(const FfnArgs& a, cudaStream_t s);
 
+// ---- expert_backward.cu
+struct BwdArgs {
+  int T, H, E, topk, I, I_shared;
+  const uint16_t *x, *dout;                 // [T, H]
+  const int32_t *topk_idx, *dest, *offsets, *counts;  // unpadded dispatch
+  const float* gate;                         // [T, K]
+  const uint16_t *w1, *w3, *w2, *ws1, *ws3, *ws2;
+  int32_t *poff, *pdest;                     // [E+1], [T*K]
+  float* gp;                                 // [cap]
+  uint16_t *xpp, *dpp;                       // [cap, H]
+  float *p_r, *q_r;                          // [cap, I]
+  uint16_t *hg_r, *dp_r, *dq_r;              // [cap, I]
+  float* dgp;                                // [cap, ceil(I / 256)]
+  uint16_t* dxpp;                            // [cap, H]
+  float *p_s, *q_s;                          // [T, I_s]
+  uint16_t *hg_s, *dp_s, *dq_s;              // [T, I_s]
+  uint16_t* dxs;                             // [T, H]
+  uint16_t* dx;                              // [T, H] out
+  float* dgate;                              // [T, K] out
+  float *dw1, *dw3, *dw2, *dws1, *dws3, *dws2;  // out (fp32)
+  int accumulate;
+  DevStatus* status;
+  uint64_t wait_limit_ns;
+};
+// rows of the padded dispatch: T*K + 15*E (each segment rounded up to 16)
+size_t expert_backward_rows_cap(int T, int K, int E);
+int launch_expert_backward(const BwdArgs& a, cudaStream_t s);
+
 // ---- fp8_gemm.cu
 struct FfnFp8Args {
   int T, H, E, topk, I, I_shared;

@@ -79,6 +79,10 @@ struct Layout {
   size_t bal_sp = 0, bal_flags = 0;  // [T, E] fp32 s', [T, E] u8 top-K flags
   size_t bal_pP = 0, bal_pc = 0;     // per-split partial sums (bounded)
   size_t f8_mq = 0, f8_ms = 0, f8_msq = 0, f8_mss = 0;  // FP8 intermediate
+  // expert backward (padded dispatch of cap rows)
+  size_t b_poff = 0, b_pdest = 0, b_gp = 0, b_xpp = 0, b_dpp = 0, b_p = 0,
+         b_q = 0, b_hg = 0, b_dp = 0, b_dq = 0, b_dgp = 0, b_dxpp = 0,
+         b_ps = 0, b_qs = 0, b_hgs = 0, b_dps = 0, b_dqs = 0, b_dxs = 0;
   size_t total = 0;
 };
 
@@ -98,6 +102,35 @@ Layout layout(const moe_dims_t* d, moe_ws_kind_t which) {
     L.block_base = take(nblk * E * 4);
   }
   if (which == MOE_WS_PERMUTE) L.counts = take(E * 4);
+  if (which == MOE_WS_EXPERT_BWD) {
+    const size_t cap = moe::expert_backward_rows_cap(d->T, d->topk, d->E);
+    const size_t I = d->I, Is = d->I_shared;
+    const size_t nfb = (I + 255) / 256;
+    L.block_counts = take(nblk * E * 4);
+    L.block_base = take(nblk * E * 4);
+    L.counts = take(E * 4);
+    L.offsets = take((E + 1) * 4);
+    L.dest = take(T * K * 4);
+    L.src_row = take(T * K * 4);
+    L.b_poff = take((E + 1) * 4);
+    L.b_pdest = take(T * K * 4);
+    L.b_gp = take(cap * 4);
+    L.b_xpp = take(cap * H * 2);
+    L.b_dpp = take(cap * H * 2);
+    L.b_p = take(cap * I * 4);
+    L.b_q = take(cap * I * 4);
+    L.b_hg = take(cap * I * 2);
+    L.b_dp = take(cap * I * 2);
+    L.b_dq = take(cap * I * 2);
+    L.b_dgp = take(cap * nfb * 4);
+    L.b_dxpp = take(cap * H * 2);
+    L.b_ps = take(T * Is * 4);
+    L.b_qs = take(T * Is * 4);
+    L.b_hgs = take(T * Is * 2);
+    L.b_dps = take(T * Is * 2);
+    L.b_dqs = take(T * Is * 2);
+    L.b_dxs = take(T * H * 2);
+  }
   if (which == MOE_WS_FORWARD) {
     L.logits = take(T * E * 4);
     L.idx = take(T * K * 4);
@@ -282,9 +315,10 @@ void moe_set_wait_timeout_ns(uint64_t ns) {
 
 size_t moe_workspace_bytes(const moe_dims_t* d, moe_ws_kind_t which) {
   const bool ffn = which == MOE_WS_EXPERT_FFN || which == MOE_WS_FORWARD ||
-                   which == MOE_WS_EXPERT_FFN_FP8;
+                   which == MOE_WS_EXPERT_FFN_FP8 ||
+                   which == MOE_WS_EXPERT_BWD;
   if (check_dims(d, ffn) != MOE_OK) return 0;
-  if (which < MOE_WS_ROUTE || which > MOE_WS_EXPERT_FFN_FP8) return 0;
+  if (which < MOE_WS_ROUTE || which > MOE_WS_EXPERT_BWD) return 0;
   return layout(d, which).total;
 }
 
@@ -593,6 +627,123 @@ moe_status_t moe_expert_ffn_fp8(const moe_dims_t* d, const moe_weights_fp8_t* w,
   a.wait_limit_ns = g_wait_limit_ns;
   const int rc = moe::launch_expert_ffn_fp8(a, cs(stream));
   return static_cast<moe_status_t>(rc);
+}
+
+moe_status_t moe_expert_backward(const moe_dims_t* d, const moe_weights_t* w,
+                                 const uint16_t* x, const uint16_t* dout,
+                                 const int32_t* topk_idx,
+                                 const float* topk_gate, int accumulate,
+                                 uint16_t* dx, float* dgate, float* dw1,
+                                 float* dw3, float* dw2, float* dws1,
+                                 float* dws3, float* dws2, void* ws,
+                                 size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRY(check_dims(d, true));
+  MOE_NEED(w);
+  MOE_NEED(w->w1);
+  MOE_NEED(w->w3);
+  MOE_NEED(w->w2);
+  MOE_NEED(w->ws1);
+  MOE_NEED(w->ws3);
+  MOE_NEED(w->ws2);
+  MOE_ALIGN(w->w1);
+  MOE_ALIGN(w->w3);
+  MOE_ALIGN(w->w2);
+  MOE_ALIGN(w->ws1);
+  MOE_ALIGN(w->ws3);
+  MOE_ALIGN(w->ws2);
+  MOE_NEED_T(x);
+  MOE_NEED_T(dout);
+  MOE_NEED_T(topk_idx);
+  MOE_NEED_T(topk_gate);
+  MOE_NEED_T(dx);
+  MOE_NEED_T(dgate);
+  MOE_NEED(dw1);
+  MOE_NEED(dw3);
+  MOE_NEED(dw2);
+  MOE_NEED(dws1);
+  MOE_NEED(dws3);
+  MOE_NEED(dws2);
+  const void* al[] = {x, dout, topk_idx, topk_gate, dx, dgate,
+                      dw1, dw3, dw2, dws1, dws3, dws2};
+  for (const void* q : al) MOE_ALIGN(q);
+  MOE_TRY(check_ws(d, MOE_WS_EXPERT_BWD, ws, ws_bytes));
+  cudaStream_t s = cs(stream);
+  const size_t E = d->E, H = d->H, I = d->I, Is = d->I_shared;
+  if (d->T == 0) {
+    if (!accumulate) {
+      // no tokens: every weight gradient is zero
+      MOE_TRY(cuda_ok(cudaMemsetAsync(dw1, 0, E * I * H * 4, s)));
+      MOE_TRY(cuda_ok(cudaMemsetAsync(dw3, 0, E * I * H * 4, s)));
+      MOE_TRY(cuda_ok(cudaMemsetAsync(dw2, 0, E * H * I * 4, s)));
+      MOE_TRY(cuda_ok(cudaMemsetAsync(dws1, 0, Is * H * 4, s)));
+      MOE_TRY(cuda_ok(cudaMemsetAsync(dws3, 0, Is * H * 4, s)));
+      MOE_TRY(cuda_ok(cudaMemsetAsync(dws2, 0, H * Is * 4, s)));
+    }
+    return MOE_OK;
+  }
+  const Layout L = layout(d, MOE_WS_EXPERT_BWD);
+  DevStatus* st = at<DevStatus>(ws, 0);
+  int32_t* bc = at<int32_t>(ws, L.block_counts);
+  int32_t* bb = at<int32_t>(ws, L.block_base);
+  int32_t* cnt = at<int32_t>(ws, L.counts);
+  int32_t* off = at<int32_t>(ws, L.offsets);
+  int32_t* dst = at<int32_t>(ws, L.dest);
+  int32_t* src = at<int32_t>(ws, L.src_row);
+  const int T = d->T, K = d->topk;
+  MOE_TRY(cuda_ok(moe::launch_block_counts(topk_idx, T, d->E, K, bc, st, s)));
+  MOE_TRY(cuda_ok(moe::launch_scan(bc, T, d->E, K, cnt, bb, nullptr, 0.f, s)));
+  MOE_TRY(cuda_ok(moe::launch_dest(topk_idx, cnt, bb, T, d->E, K, off, dst,
+                                   src, nullptr, st, s)));
+  moe::BwdArgs a;
+  a.T = T;
+  a.H = d->H;
+  a.E = d->E;
+  a.topk = K;
+  a.I = d->I;
+  a.I_shared = d->I_shared;
+  a.x = x;
+  a.dout = dout;
+  a.topk_idx = topk_idx;
+  a.dest = dst;
+  a.offsets = off;
+  a.counts = cnt;
+  a.gate = topk_gate;
+  a.w1 = w->w1;
+  a.w3 = w->w3;
+  a.w2 = w->w2;
+  a.ws1 = w->ws1;
+  a.ws3 = w->ws3;
+  a.ws2 = w->ws2;
+  a.poff = at<int32_t>(ws, L.b_poff);
+  a.pdest = at<int32_t>(ws, L.b_pdest);
+  a.gp = at<float>(ws, L.b_gp);
+  a.xpp = at<uint16_t>(ws, L.b_xpp);
+  a.dpp = at<uint16_t>(ws, L.b_dpp);
+  a.p_r = at<float>(ws, L.b_p);
+  a.q_r = at<float>(ws, L.b_q);
+  a.hg_r = at<uint16_t>(ws, L.b_hg);
+  a.dp_r = at<uint16_t>(ws, L.b_dp);
+  a.dq_r = at<uint16_t>(ws, L.b_dq);
+  a.dgp = at<float>(ws, L.b_dgp);
+  a.dxpp = at<uint16_t>(ws, L.b_dxpp);
+  a.p_s = at<float>(ws, L.b_ps);
+  a.q_s = at<float>(ws, L.b_qs);
+  a.hg_s = at<uint16_t>(ws, L.b_hgs);
+  a.dp_s = at<uint16_t>(ws, L.b_dps);
+  a.dq_s = at<uint16_t>(ws, L.b_dqs);
+  a.dxs = at<uint16_t>(ws, L.b_dxs);
+  a.dx = dx;
+  a.dgate = dgate;
+  a.dw1 = dw1;
+  a.dw3 = dw3;
+  a.dw2 = dw2;
+  a.dws1 = dws1;
+  a.dws3 = dws3;
+  a.dws2 = dws2;
+  a.accumulate = accumulate ? 1 : 0;
+  a.status = st;
+  a.wait_limit_ns = g_wait_limit_ns;
+  return static_cast<moe_status_t>(moe::launch_expert_backward(a, s));
 }
 
 moe_status_t moe_route_backward(const moe_dims_t* d, const float* logits,

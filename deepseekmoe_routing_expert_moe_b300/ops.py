@@ -17,8 +17,8 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libmoe.so")
 
 (MOE_WS_ROUTE, MOE_WS_PERMUTE, MOE_WS_EXPERT_FFN, MOE_WS_FORWARD,
- MOE_WS_ROUTER_LOGITS, MOE_WS_SEQ_BALANCE, MOE_WS_EXPERT_FFN_FP8) = \
-    0, 1, 2, 3, 4, 5, 6
+ MOE_WS_ROUTER_LOGITS, MOE_WS_SEQ_BALANCE, MOE_WS_EXPERT_FFN_FP8,
+ MOE_WS_EXPERT_BWD) = 0, 1, 2, 3, 4, 5, 6, 7
 
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
           3: "MOE_ERR_ALIGNMENT", 4: "MOE_ERR_WORKSPACE", 5: "MOE_ERR_CUDA",
@@ -78,6 +78,8 @@ _SIGS = {
     "moe_plan_redundant_experts": (_I, [_P, ctypes.c_int32, ctypes.c_int32,
                                         ctypes.c_int32, _P, _P]),
     "moe_route_backward": (_I, [_D, _P, _P, _P, _I, _P, _P, _S, _P]),
+    "moe_expert_backward": (_I, [_D, _W, _P, _P, _P, _P, _I, _P, _P, _P, _P,
+                                 _P, _P, _P, _P, _P, _S, _P]),
     "moe_seq_balance_loss_backward": (_I, [_D, _P, ctypes.c_int32,
                                            ctypes.c_float, _P, _P, _I, _P,
                                            _P]),
@@ -310,6 +312,37 @@ def moe_route_backward(d, logits, topk_idx, dgate, dlogits, ws,
         ctypes.byref(d), _ptr(logits), _ptr(topk_idx), _ptr(dgate),
         1 if accumulate else 0, _ptr(dlogits), _ptr(ws), ws.numel(),
         _stream(stream)))
+
+
+class WeightGrads:
+    """fp32 weight gradients of one layer's experts: dw1, dw3 [E, I, H],
+    dw2 [E, H, I], dws1, dws3 [I_s, H], dws2 [H, I_s] (torch tensors)."""
+
+    NAMES = ("dw1", "dw3", "dw2", "dws1", "dws3", "dws2")
+
+    def __init__(self, dw1, dw3, dw2, dws1, dws3, dws2):
+        self.dw1, self.dw3, self.dw2 = dw1, dw3, dw2
+        self.dws1, self.dws3, self.dws2 = dws1, dws3, dws2
+
+    @classmethod
+    def empty(cls, d, device="cuda"):
+        E, H, I, Is = d.E, d.H, d.I, d.I_shared
+        f = lambda *s: torch.empty(s, dtype=torch.float32, device=device)  # noqa: E731
+        return cls(f(E, I, H), f(E, I, H), f(E, H, I), f(Is, H), f(Is, H),
+                   f(H, Is))
+
+    def tensors(self):
+        return [getattr(self, n) for n in self.NAMES]
+
+
+def moe_expert_backward(d, w: Weights, x, dout, topk_idx, topk_gate, dx,
+                        dgate, grads: WeightGrads, ws, accumulate=False,
+                        stream=None):
+    _check("moe_expert_backward", lib().moe_expert_backward(
+        ctypes.byref(d), ctypes.byref(w.struct), _ptr(x), _ptr(dout),
+        _ptr(topk_idx), _ptr(topk_gate), 1 if accumulate else 0, _ptr(dx),
+        _ptr(dgate), *(_ptr(t) for t in grads.tensors()), _ptr(ws),
+        ws.numel(), _stream(stream)))
 
 
 def moe_seq_balance_loss_backward(d, logits, seq_len, alpha, counts_seq,

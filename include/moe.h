@@ -117,7 +117,8 @@ typedef enum {
   MOE_WS_FORWARD = 3,
   MOE_WS_ROUTER_LOGITS = 4,
   MOE_WS_SEQ_BALANCE = 5,
-  MOE_WS_EXPERT_FFN_FP8 = 6
+  MOE_WS_EXPERT_FFN_FP8 = 6,
+  MOE_WS_EXPERT_BWD = 7
 } moe_ws_kind_t;
 
 /* Bytes of device workspace `which` needs for dims `d` (0 if d is invalid).
@@ -386,6 +387,42 @@ moe_status_t moe_expert_ffn_fp8(const moe_dims_t* d, const moe_weights_fp8_t* w,
                                 const int32_t* offsets, uint16_t* yp,
                                 uint16_t* ys, void* ws, size_t ws_bytes,
                                 moe_stream_t stream);
+
+/* Backward of the expert FFNs and the combine, for a fixed routing (the
+ * training side of "02 · DeepSeek-V3" §1.1 SwiGLU experts and §1.3 eq. 12;
+ * §1.4 trains the layer, §2 keeps the master weights and their gradients
+ * in higher precision than the GEMM inputs).  For the layer output
+ *   out_t = x_t + FFN_s(x_t) + sum_k g_{t,k} FFN_{e_k}(x_t)
+ * and its upstream gradient dout [T, H] (bf16):
+ *   dgate [T, K] fp32  dgate[t,k] = <dout_t, FFN_{e_k}(x_t)>, the input of
+ *                      moe_route_backward
+ *   dx    [T, H] bf16  dout_t + (shared expert's input gradient of dout_t)
+ *                      + sum_k (expert e_k's input gradient of g dout_t);
+ *                      the path through the router logits is not included
+ *                      (moe_route_backward gives dlogits; dlogits W_r is the
+ *                      caller's)
+ *   dw1, dw3 [E, I, H], dw2 [E, H, I], dws1, dws3 [I_s, H], dws2 [H, I_s]
+ *                      fp32: the weight gradients; written, or added to the
+ *                      arrays' contents when accumulate != 0 (gradient
+ *                      accumulation over micro-batches).  An expert that no
+ *                      token chose gets a zero gradient (or is left as it
+ *                      is when accumulating).
+ * x [T, H] bf16, topk_idx / topk_gate [T, K] as moe_route wrote them (valid,
+ * per-token distinct experts), weights as for moe_forward (w_router and
+ * router_offset are not used).  p = W1 a, q = W3 a and silu(p) q are
+ * recomputed on the tensor cores with fp32 accumulation; the intermediate
+ * gradients dp, dq and the rows g dout are bf16 GEMM operands, every GEMM
+ * accumulates in fp32.  H, I, I_shared multiples of 64; H <= 16384.
+ * Workspace: MOE_WS_EXPERT_BWD (it holds the recomputed p, q in fp32 and
+ * the rows dispatched to 16-row-aligned expert segments). */
+moe_status_t moe_expert_backward(const moe_dims_t* d, const moe_weights_t* w,
+                                 const uint16_t* x, const uint16_t* dout,
+                                 const int32_t* topk_idx,
+                                 const float* topk_gate, int accumulate,
+                                 uint16_t* dx, float* dgate, float* dw1,
+                                 float* dw3, float* dw2, float* dws1,
+                                 float* dws3, float* dws2, void* ws,
+                                 size_t ws_bytes, moe_stream_t stream);
 
 /* Redundant-expert placement ("02 · DeepSeek-V3" §5.1: high-load experts
  * are replicated from online load statistics, e.g. 32 redundant experts
