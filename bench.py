@@ -1045,6 +1045,260 @@ def run_backward_gpu(args, rank, world, local_rank):
     }
 
 
+def run_expert_backward_gpu(args, rank, world, local_rank):
+    """The experts' backward at the V3 prefill size (T = 4096, 256 experts of
+    7168 x 2048 + shared, top-8): per step one moe_expert_backward call --
+    recompute of p, q, dgrad of the down and up projections, fp32 weight
+    gradients of every expert, token and gate gradients -- for the routing
+    the forward chose.  Two rotating (x, dout) batches; 22.6 GB of weights
+    read and 45 GB of fp32 weight gradients written per step (> L2)."""
+    import torch
+    from deepseekmoe_routing_expert_moe_b300 import inputs, ops
+    torch.cuda.set_device(local_rank)
+    cfg = inputs.CONFIGS["prefill_v3"]
+    d = ops.dims_of(cfg)
+    T, H, E, K, I, Is = cfg.T, cfg.H, cfg.E, cfg.topk, cfg.I, cfg.I_shared
+    w1, w3, w2 = inputs.device_expert_weights(cfg, "cuda")
+    ws1, ws3, ws2 = inputs.shared_weights(cfg, "cuda")
+    wr = torch.from_numpy(inputs.router_weight(cfg)).cuda()
+    W = ops.Weights(wr, w1, w3, w2, ws1, ws3, ws2)
+    NB = 2
+    wsf = ops.workspace(d, ops.MOE_WS_FORWARD)
+    xs, dos, idxs, gates = [], [], [], []
+    bias = torch.from_numpy(inputs.bias(cfg)).cuda()
+    g = torch.Generator(device="cuda").manual_seed(11 + rank)
+    for i in range(NB):   # the forward's routing of each batch
+        x = inputs.x_tokens(cfg, step=i + 1000 * rank, device="cuda")
+        out = torch.empty((T, H), dtype=torch.int16, device="cuda")
+        idx = torch.empty((T, K), dtype=torch.int32, device="cuda")
+        gate = torch.empty((T, K), dtype=torch.float32, device="cuda")
+        ops.moe_forward(d, W, x, bias, out, wsf, topk_idx_out=idx,
+                        topk_gate_out=gate)
+        dout = (torch.randn((T, H), device="cuda", generator=g)
+                .to(torch.bfloat16).view(torch.int16))
+        xs.append(x)
+        dos.append(dout)
+        idxs.append(idx)
+        gates.append(gate)
+    del wsf
+    grads = ops.WeightGrads.empty(d)
+    dx = torch.empty((T, H), dtype=torch.int16, device="cuda")
+    dg = torch.empty((T, K), dtype=torch.float32, device="cuda")
+    ws = ops.workspace(d, ops.MOE_WS_EXPERT_BWD)
+    stream = torch.cuda.current_stream()
+
+    def step(i, xi=None, di=None, dxo=None, dgo=None):
+        b = i % NB
+        ops.moe_expert_backward(d, W, xs[b] if xi is None else xi,
+                                dos[b] if di is None else di, idxs[b],
+                                gates[b], dx if dxo is None else dxo,
+                                dg if dgo is None else dgo, grads, ws)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    assert ops.moe_get_device_error(ws) == 0
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(gpu_index_for_smi(local_rank)) as clk:
+        torch.cuda.synchronize()
+        ev0.record(stream)
+        for i in range(args.steps):
+            step(i)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    ms = ev0.elapsed_time(ev1)
+    clocks = clk.summary()
+    # per-stage times (separate pass, events between the stages)
+    ns = 6
+    sets = [[torch.cuda.Event(enable_timing=True)
+             for _ in range(ops.MOE_FORWARD_KERNELS + 1)]
+            for _ in range(args.steps)]
+    for i in range(args.steps):
+        ops.moe_set_profile_events(sets[i])
+        step(i)
+    ops.moe_set_profile_events(None)
+    torch.cuda.synchronize()
+    st = np.array([[s_[j].elapsed_time(s_[j + 1]) for j in range(ns)]
+                   for s_ in sets]).mean(0)
+    names = ("dispatch", "recompute", "dgrad_down", "dgrad_up", "wgrad",
+             "finalize")
+    c = np.bincount(idxs[(args.steps - 1) % NB].cpu().numpy().ravel(),
+                    minlength=E)
+    touched = int((c > 0).sum())
+    TK = T * K
+    # algorithmic bytes / flops per stage (real rows; the 16-row padding of
+    # the segments is this design's own)
+    wgt = touched * I * H * 2
+    stage_bytes = {
+        "recompute": 2 * wgt + 2 * Is * H * 2 + (TK + T) * H * 2 +
+                     (TK + T) * I * (4 + 4 + 2),
+        "dgrad_down": wgt + Is * H * 2 + (TK + T) * H * 2 +
+                      (TK + T) * I * (8 + 4),
+        "dgrad_up": 2 * wgt + 2 * Is * H * 2 + (TK + T) * I * 4 +
+                    (TK + T) * H * 2,
+        "wgrad": (touched + 0.0) * 3 * I * H * 4 + 3 * Is * H * 4 +
+                 (TK + T) * (2 * I * 2 + H * 2 + I * 2 + H * 2),
+    }
+    stage_flops = {"recompute": 2.0 * (TK + T) * H * 2 * I,
+                   "dgrad_down": 2.0 * (TK + T) * H * I,
+                   "dgrad_up": 2.0 * (TK + T) * H * 2 * I,
+                   "wgrad": 2.0 * (TK + T) * 3 * H * I}
+    pk, pk_src = peaks()
+    hbm = float(pk["hbm_gbs"])
+    tc = float(pk.get("bf16_tflops_sustained", pk["bf16_tflops"]))
+    stages = {}
+    for j, n in enumerate(names):
+        e = {"ms": round(float(st[j]), 4)}
+        if n in stage_bytes:
+            sec = st[j] / 1e3
+            e["hbm_frac"] = round(stage_bytes[n] / sec / 1e9 / hbm, 4)
+            e["tensor_frac"] = round(stage_flops[n] / sec / 1e12 / tc, 4)
+            e["algorithmic_bytes"] = int(stage_bytes[n])
+        stages[n] = e
+    dom = max(stage_bytes, key=lambda n: st[names.index(n)])
+    t_dom = st[names.index(dom)] / 1e3
+    if stage_bytes[dom] / (hbm * 1e9) >= stage_flops[dom] / (tc * 1e12):
+        roof = {"bound": "hbm",
+                "achieved": round(stage_bytes[dom] / t_dom / 1e9, 1),
+                "peak": hbm, "unit": "GB/s"}
+    else:
+        roof = {"bound": "tensor",
+                "achieved": round(stage_flops[dom] / t_dom / 1e12, 1),
+                "peak": tc, "unit": "TFLOP/s"}
+    roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
+    roof["traffic"] = ncu_traffic(dom, "expert_backward_v3")
+    roof["kernel"] = {"wgrad": "wgrad_gemm_kernel (fp32 dW1, dW3, dW2)",
+                      "recompute": "dgrad_gemm_kernel<recompute>",
+                      "dgrad_down": "dgrad_gemm_kernel<dgrad_down>",
+                      "dgrad_up": "dgrad_gemm_kernel<dgrad_up>"}[dom]
+    roof["algorithmic_bytes"] = int(stage_bytes[dom])
+    roof["peak_source"] = f"{pk_src} (MEASURED_PEAKS.json)"
+    # end to end: x and dout uploaded from pinned memory, dx and the gate
+    # gradients read back every step (the weight gradients stay on the
+    # device for the optimizer)
+    xh = [xs[i].cpu().pin_memory() for i in range(NB)]
+    dh = [dos[i].cpu().pin_memory() for i in range(NB)]
+    xd = torch.empty_like(xs[0])
+    dd_ = torch.empty_like(dos[0])
+    dxh = torch.empty((T, H), dtype=torch.int16).pin_memory()
+    dgh = torch.empty((T, K), dtype=torch.float32).pin_memory()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        xd.copy_(xh[i % NB], non_blocking=True)
+        dd_.copy_(dh[i % NB], non_blocking=True)
+        step(i, xd, dd_)
+        dxh.copy_(dx, non_blocking=True)
+        dgh.copy_(dg, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    assert ops.moe_get_device_error(ws) == 0
+    res = {
+        "metric": "tokens/s through the experts' backward (recompute, dgrad, "
+                  "fp32 weight gradients, token and gate gradients) of a "
+                  "V3-shaped MoE layer on 1 B300; % of HBM roofline",
+        "value": round(T * args.steps / (ms / 1e3), 1), "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic, seeded (x ~N(0,1), dout ~N(0,1) bf16, expert "
+                "weights ~N(0,0.02) bf16; routing from the layer forward)",
+        "config": {"workload": "expert_backward_v3: experts' backward of the "
+                               f"V3 prefill layer, T={T}, H={H}, E={E}+1 "
+                               f"shared, I={I}, top-{K}",
+                   "T": T, "H": H, "E": E, "I": I, "topk": K,
+                   "l2": "22.6 GB of weights read and 45 GB of fp32 weight "
+                         "gradients written per step"},
+        "roofline": roof,
+        "stages_ms": stages,
+        "e2e": {"value": round(T * args.steps / (e2e_ms / 1e3), 1),
+                "unit": "tokens/s", "h2d_bytes_per_step": 2 * T * H * 2,
+                "d2h_bytes_per_step": T * H * 2 + T * K * 4},
+        # block counts, count scan, dispatch order, padded dispatch (3),
+        # four GEMMs, token / gate gradients
+        "gpu_launches": 11 * args.steps,
+        "clocks": clocks,
+        "experts_touched": touched,
+        "impl": "b300",
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        s = expert_backward_sample(cfg, args.cpu_sample_tokens)
+        sec = expert_backward_oracle_time(s)
+        res["cpu_baseline"] = {
+            "value": round(args.cpu_sample_tokens / sec, 4),
+            "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
+            "sample": f"first {args.cpu_sample_tokens} tokens of the batch "
+                      f"through the oracle's expert backward ({sec:.1f} s: "
+                      "their experts and the shared expert)"}
+    return res
+
+
+def expert_backward_sample(cfg, n):
+    """A bounded sample for the oracle's expert backward: the first n
+    tokens, their routing, a dout, and the weights of their experts."""
+    from deepseekmoe_routing_expert_moe_b300 import inputs
+    from oracle import moe_oracle as O
+    f = inputs.bf16_bits_to_f32
+    x = f(inputs.x_tokens(cfg, T=n)).astype(np.float64)
+    z = O.router_logits(x, inputs.router_weight(cfg))
+    r = O.route(z, inputs.bias(cfg), cfg.n_group, cfg.topk_group, cfg.topk)
+    dout = np.random.default_rng(3).standard_normal(x.shape)
+    ew = {int(e): tuple(f(a) for a in inputs.expert_weights(cfg, int(e)))
+          for e in np.unique(r["idx"])}
+    sw = tuple(f(a) for a in inputs.shared_weights(cfg))
+    return dict(x=x, dout=dout, idx=r["idx"], gate=r["gate"], ew=ew, sw=sw)
+
+
+def expert_backward_oracle_time(s) -> float:
+    """Seconds for the oracle's backward of the sample: the shared expert
+    over every sample token and each chosen expert over its tokens
+    (swiglu_ffn_backward, the piece layer_backward is built from)."""
+    from oracle import moe_oracle as O
+    t0 = time.perf_counter()
+    x, d = s["x"], s["dout"]
+    dx = d + O.swiglu_ffn_backward(x, *s["sw"], d)[0]
+    for e, w in s["ew"].items():
+        t, k = np.nonzero(s["idx"] == e)
+        y = O.swiglu_ffn(x[t], *w)
+        np.einsum("nh,nh->n", d[t], y)
+        g = s["gate"][t, k].astype(np.float64)[:, None]
+        dx[t] += O.swiglu_ffn_backward(x[t], *w, g * d[t])[0]
+    return time.perf_counter() - t0
+
+
+def run_expert_backward_reference(args):
+    """Oracle arm of expert_backward_v3: a bounded token sample per step
+    through the oracle's expert backward."""
+    from deepseekmoe_routing_expert_moe_b300 import inputs
+    cfg = inputs.CONFIGS["prefill_v3"]
+    n = args.ref_tokens
+    s = expert_backward_sample(cfg, n)
+    for _ in range(args.warmup):
+        expert_backward_oracle_time(s)
+    tot = sum(expert_backward_oracle_time(s) for _ in range(args.steps))
+    v = n * args.steps / tot
+    return {
+        "metric": "tokens/s through the experts' backward of a V3-shaped MoE "
+                  "layer; oracle on the host cores",
+        "value": round(v, 4), "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(tot / args.steps * 1e3, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic, seeded",
+        "config": {"workload": f"expert_backward_v3: {n} tokens per step"},
+        "impl": "reference",
+        "cpu_baseline": {"value": round(v, 4), "unit": "tokens/s",
+                         "cores": blas_threads(), "kind": "oracle",
+                         "sample": f"{n} tokens of the prefill batch per step"},
+        "e2e": {"value": round(v, 4), "unit": "tokens/s",
+                "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
 def run_backward_reference(args):
     """Oracle arm of route_backward_v3: one 4096-token sequence of V3
     logits per step through the oracle's gate and balance-loss gradients."""
@@ -1133,6 +1387,8 @@ def run_reference(args):
         return run_decode_fp8_reference(args)
     if args.workload == "route_backward_v3":
         return run_backward_reference(args)
+    if args.workload == "expert_backward_v3":
+        return run_expert_backward_reference(args)
     cfg = inputs.CONFIGS[args.workload]
     n = args.ref_tokens
     s = oracle_sample(cfg, n)
@@ -1169,7 +1425,8 @@ def main():
                     choices=("prefill_v3", "decode_v3", "skewed_v3",
                              "route_v3", "prefill_v3_e32", "balance_v3",
                              "decode_v3_fp8", "prefill_v3_fp8",
-                             "decode_v3_e32_fp8", "route_backward_v3"))
+                             "decode_v3_e32_fp8", "route_backward_v3",
+                             "expert_backward_v3"))
     ap.add_argument("--cpu-sample-tokens", type=int, default=4)
     ap.add_argument("--ref-tokens", type=int, default=1)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -1200,6 +1457,8 @@ def main():
         res = run_fp8_gpu(args, rank, world, local_rank)
     elif args.workload == "route_backward_v3":
         res = run_backward_gpu(args, rank, world, local_rank)
+    elif args.workload == "expert_backward_v3":
+        res = run_expert_backward_gpu(args, rank, world, local_rank)
     else:
         res = run_gpu(args, rank, world, local_rank)
     if rank == 0:

@@ -351,6 +351,81 @@ __device__ __forceinline__ Unit decode_unit(int u, const int* useg,
   return x;
 }
 
+// One epilogue thread's view of a dgrad-of-down unit: its two feature
+// columns fa, fbb (one per accumulator) of the p, q inputs and the dp, dq
+// outputs, over the unit's rows.
+struct DdTile {
+  const float *p, *q;
+  uint16_t *dp, *dq;
+  const float* gp;  // NULL: the shared expert (g = 1)
+  int row0, rows, ld, fa, fbb;
+  bool va, vb;
+};
+
+// p, q of both columns and the gate, for the 16 token columns of chunk c:
+// v[0] p(fa), v[1] q(fa), v[2] p(fbb), v[3] q(fbb), v[4] g
+__device__ __forceinline__ void dd_fetch(const DdTile& t, int c,
+                                         float (&v)[5][16]) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const int j = 16 * c + i;
+    const bool in = j < t.rows;
+    const size_t row = (size_t)(t.row0 + (in ? j : 0));
+    v[0][i] = (in && t.va) ? t.p[row * t.ld + t.fa] : 0.0f;
+    v[1][i] = (in && t.va) ? t.q[row * t.ld + t.fa] : 0.0f;
+    v[2][i] = (in && t.vb) ? t.p[row * t.ld + t.fbb] : 0.0f;
+    v[3][i] = (in && t.vb) ? t.q[row * t.ld + t.fbb] : 0.0f;
+    v[4][i] = t.gp == nullptr ? 1.0f : (in ? t.gp[row] : 0.0f);
+  }
+}
+
+// chunk c of a dgrad-of-down unit: D from tensor memory, then per token
+// column j: dm = g D, dq = dm silu(p), dp = dm q silu'(p) (bf16), and this
+// warp's 32-lane sum of D h (h = silu(p) q) into dgs[j]
+__device__ __forceinline__ void dd_chunk(const DdTile& t, int c, uint32_t ta,
+                                         uint32_t tb, const float (&v)[5][16],
+                                         float* dgs, int lane) {
+  uint32_t a[16], b[16];
+  tmem_ld16(ta + 16 * c, a);
+  tmem_ld16(tb + 16 * c, b);
+  tmem_ld_wait();
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const int j = 16 * c + i;
+    float part = 0.0f;
+    if (j < t.rows) {
+      const size_t row = (size_t)(t.row0 + j);
+      const float g = v[4][i];
+      if (t.va) {
+        const float D = __uint_as_float(a[i]);
+        const float pv = v[0][i], qv = v[1][i];
+        const float sg = sigm_f(pv);
+        const float sl = pv * sg;
+        part = D * (sl * qv);
+        const float dm = g * D;
+        t.dq[row * t.ld + t.fa] = bf16_bits(dm * sl);
+        t.dp[row * t.ld + t.fa] =
+            bf16_bits(dm * qv * (sg * (1.0f + pv * (1.0f - sg))));
+      }
+      if (t.vb) {
+        const float D = __uint_as_float(b[i]);
+        const float pv = v[2][i], qv = v[3][i];
+        const float sg = sigm_f(pv);
+        const float sl = pv * sg;
+        part += D * (sl * qv);
+        const float dm = g * D;
+        t.dq[row * t.ld + t.fbb] = bf16_bits(dm * sl);
+        t.dp[row * t.ld + t.fbb] =
+            bf16_bits(dm * qv * (sg * (1.0f + pv * (1.0f - sg))));
+      }
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1)
+      part += __shfl_xor_sync(0xffffffffu, part, off);
+    if (lane == 0) dgs[j] = part;
+  }
+}
+
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     dgrad_gemm_kernel(const __grid_constant__ DgParams p) {
@@ -663,12 +738,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int u = blockIdx.x; u < total; u += gridDim.x, ++it) {
       const Unit w = decode_unit(u, useg, srow0, srows, NS);
       const bool wide = w.n > SLOT / 2;
-      const int s1 = wide ? (slot ^ 1) : slot;
+      const int s1_ = wide ? (slot ^ 1) : slot;
       if (et == 0) {
         int ok = mbar_wait_bounded(smem_u32(&tfull[slot]), (tph >> slot) & 1,
                                    abort_flag, limit, p.status, kSiteEpilogue);
         if (ok && wide)
-          ok = mbar_wait_bounded(smem_u32(&tfull[s1]), (tph >> s1) & 1,
+          ok = mbar_wait_bounded(smem_u32(&tfull[s1_]), (tph >> s1_) & 1,
                                  abort_flag, limit, p.status, kSiteEpilogue);
         misc[4 + (it & 1)] = ok;
       }
@@ -678,7 +753,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
       const uint32_t ta = tmem_base + lane_off + slot * SLOT;
       const uint32_t tb =
-          wide ? tmem_base + lane_off + s1 * SLOT : ta + SLOT / 2;
+          wide ? tmem_base + lane_off + s1_ * SLOT : ta + SLOT / 2;
       const bool sh = (w.seg == 0);
       const int nfeat = sh ? p.n_s : p.n_r;
       if (MODE == kRecomp) {
@@ -708,62 +783,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_before();
         mbar_arrive(smem_u32(&tempty[slot]));
-        if (wide) mbar_arrive(smem_u32(&tempty[s1]));
+        if (wide) mbar_arrive(smem_u32(&tempty[s1_]));
       } else if (MODE == kDgradDown) {
         const int fa = w.f * FB + r;
         const int fbb = fa + BM;
         const bool va = fa < nfeat, vb = fbb < nfeat;
-        const float* pi = sh ? p.p_s : p.p_r;
-        const float* qi = sh ? p.q_s : p.q_r;
-        uint16_t* dpo = sh ? p.dp_s : p.dp_r;
-        uint16_t* dqo = sh ? p.dq_s : p.dq_r;
-        for (int c = 0; 16 * c < w.n; ++c) {
-          uint32_t a[16], b[16];
-          tmem_ld16(ta + 16 * c, a);
-          tmem_ld16(tb + 16 * c, b);
-          tmem_ld_wait();
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int j = 16 * c + i;
-            float part = 0.0f;
-            if (j < w.rows) {
-              const size_t row = (size_t)(w.row0 + j);
-              const float g = sh ? 1.0f : p.gp[row];
-              if (va) {
-                const float D = __uint_as_float(a[i]);
-                const float pv = pi[row * nfeat + fa];
-                const float qv = qi[row * nfeat + fa];
-                const float sg = sigm_f(pv);
-                const float sl = pv * sg;
-                part = D * (sl * qv);
-                const float dm = g * D;
-                dqo[row * nfeat + fa] = bf16_bits(dm * sl);
-                dpo[row * nfeat + fa] =
-                    bf16_bits(dm * qv * (sg * (1.0f + pv * (1.0f - sg))));
-              }
-              if (vb) {
-                const float D = __uint_as_float(b[i]);
-                const float pv = pi[row * nfeat + fbb];
-                const float qv = qi[row * nfeat + fbb];
-                const float sg = sigm_f(pv);
-                const float sl = pv * sg;
-                part += D * (sl * qv);
-                const float dm = g * D;
-                dqo[row * nfeat + fbb] = bf16_bits(dm * sl);
-                dpo[row * nfeat + fbb] =
-                    bf16_bits(dm * qv * (sg * (1.0f + pv * (1.0f - sg))));
-              }
-            }
-            // this warp's 32 features (x2) of token column j, fixed order
-#pragma unroll
-            for (int off = 16; off >= 1; off >>= 1)
-              part += __shfl_xor_sync(0xffffffffu, part, off);
-            if (lane == 0) dg_s[q * NT + j] = part;
-          }
+        const DdTile t{sh ? p.p_s : p.p_r, sh ? p.q_s : p.q_r,
+                       sh ? p.dp_s : p.dp_r, sh ? p.dq_s : p.dq_r,
+                       sh ? nullptr : p.gp, w.row0, w.rows, nfeat, fa, fbb,
+                       va, vb};
+        // the p, q and gate values of chunk c + 1 are loaded while chunk c
+        // is computed (two register sets, alternating)
+        float s0[5][16], s1[5][16];
+        dd_fetch(t, 0, s0);
+        for (int c = 0; 16 * c < w.n; c += 2) {
+          if (16 * (c + 1) < w.n) dd_fetch(t, c + 1, s1);
+          dd_chunk(t, c, ta, tb, s0, dg_s + q * NT, lane);
+          if (16 * (c + 1) >= w.n) break;
+          if (16 * (c + 2) < w.n) dd_fetch(t, c + 2, s0);
+          dd_chunk(t, c + 1, ta, tb, s1, dg_s + q * NT, lane);
         }
         tc_fence_before();
         mbar_arrive(smem_u32(&tempty[slot]));
-        if (wide) mbar_arrive(smem_u32(&tempty[s1]));
+        if (wide) mbar_arrive(smem_u32(&tempty[s1_]));
         epi_bar();
         if (!sh) {
           for (int j = et; j < w.rows; j += 32 * kEpiWarps)
@@ -795,11 +837,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_before();
         mbar_arrive(smem_u32(&tempty[slot]));
-        if (wide) mbar_arrive(smem_u32(&tempty[s1]));
+        if (wide) mbar_arrive(smem_u32(&tempty[s1_]));
       }
       tph ^= 1u << slot;
       if (wide)
-        tph ^= 1u << s1;
+        tph ^= 1u << s1_;
       else
         slot ^= 1;
     }
@@ -835,15 +877,20 @@ int launch_dgrad(const DgParams& dp, cudaStream_t s) {
 // block); the reduction runs over the segment's token rows
 // --------------------------------------------------------------------------
 constexpr int WG_N = 256;
-constexpr int WG_STAGES = 4;
+constexpr int WG_STAGES = 3;
 constexpr uint32_t WG_A_BYTES = BM * BK * 2;         // 16 KB
 constexpr uint32_t WG_B_BYTES = WG_N * BK * 2;       // 32 KB
 constexpr uint32_t WG_STAGE_BYTES = WG_A_BYTES + WG_B_BYTES;
+// fp32 output staging: per epilogue warp two 32 x 32 tiles (4 KB each),
+// stored by TMA (or added to the output in L2 when accumulating)
+constexpr uint32_t WG_OUT_TILE = 32 * 32 * 4;
+constexpr uint32_t WG_OUT_BYTES = kEpiWarps * 2 * WG_OUT_TILE;
 constexpr int kMats = 3;   // dW1, dW3, dW2
 
 struct WgParams {
   CUtensorMap a_r[kMats], b_r[kMats];  // routed: (dp, xpp) (dq, xpp) (dpp, hg)
   CUtensorMap a_s[kMats], b_s[kMats];  // shared: (dps, x) (dqs, x) (dout, hs)
+  CUtensorMap o_r[kMats], o_s[kMats];  // outputs as [experts][M][N] fp32
   const int32_t* poff;
   float* out_r[kMats];   // dW1, dW3 [E, I, H], dW2 [E, H, I]
   float* out_s[kMats];   // dWs1, dWs3 [I_s, H], dWs2 [H, I_s]
@@ -897,7 +944,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sS = smem;  // stages: A tile then B tile
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sS + WG_STAGES * WG_STAGE_BYTES);
+  uint8_t* sO = sS + WG_STAGES * WG_STAGE_BYTES;  // output staging
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sO + WG_OUT_BYTES);
   uint64_t* full = bars;
   uint64_t* empty = full + WG_STAGES;
   uint64_t* tfull = empty + WG_STAGES;
@@ -1094,24 +1142,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp >= kEpiWarp0) {
     // ------------------------------------------------------- epilogue
+    // Each warp owns 32 rows (its TMEM lane quadrant): per 32 columns it
+    // writes its rows into a swizzled 4 KB staging tile and one lane
+    // issues the TMA store (or reduce-add) of the tile; two tiles
+    // alternate, so a tile is rewritten only after its store has read it.
     const int q = warp & 3;
     const int r = q * 32 + lane;
     uint32_t tph = 0;
     int slot = 0;
+    int ob = 0;
+    uint8_t* stage_base = sO + q * 2 * WG_OUT_TILE;
     for (int u = blockIdx.x; u < total; u += gridDim.x) {
       const WUnit w = wg_decode(p, u, upre, srow0, srows, NP);
       const bool sh = w.seg == 0;
-      float* outm = sh ? p.out_s[w.mat] : p.out_r[w.mat];
-      const size_t per = (size_t)w.M * w.N;
-      float* out = outm + (sh ? 0 : (size_t)(w.seg - 1) * per);
-      const int row = w.m0 + r;
-      const bool vr = row < w.M;
-      float* orow = out + (size_t)row * w.N + w.n0;
       if (w.rows == 0) {
         // an expert with no tokens has a zero gradient
-        if (!p.accumulate && vr)
+        const int row = w.m0 + r;
+        if (!p.accumulate && row < w.M) {
+          float* out = p.out_r[w.mat] + (size_t)(w.seg - 1) * w.M * w.N;
+          float* orow = out + (size_t)row * w.N + w.n0;
           for (int c = 0; c < w.nt; c += 4)
             *reinterpret_cast<float4*>(orow + c) = make_float4(0, 0, 0, 0);
+        }
         continue;
       }
       int ok = 0;
@@ -1123,33 +1175,47 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const uint32_t ta =
           tmem_base + (static_cast<uint32_t>(q * 32) << 16) + slot * SLOT;
-      for (int c = 0; 16 * c < w.nt; ++c) {
-        uint32_t v[16];
-        tmem_ld16(ta + 16 * c, v);
+      const CUtensorMap* om = sh ? &p.o_s[w.mat] : &p.o_r[w.mat];
+      const int mrow = w.m0 + q * 32;        // first row of this warp
+      const int mat_idx = sh ? 0 : w.seg - 1;
+      for (int c = 0; 32 * c < w.nt; ++c) {
+        uint32_t v[32];
+        tmem_ld16(ta + 32 * c, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
+        tmem_ld16(ta + 32 * c + 16,
+                  *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
         tmem_ld_wait();
-        if (vr) {
-          float4* o = reinterpret_cast<float4*>(orow + 16 * c);
+        uint8_t* tile = stage_base + ob * WG_OUT_TILE;
+        if (lane == 0) bulk_wait_read_le1();
+        __syncwarp();
+        // row `lane`: 16-byte chunk k at position k ^ (lane & 7) (the
+        // 128-byte swizzle of the tensor map)
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            float4 val = make_float4(
-                __uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
-                __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
-            if (p.accumulate) {
-              const float4 old = o[i];
-              val.x += old.x;
-              val.y += old.y;
-              val.z += old.z;
-              val.w += old.w;
-            }
-            o[i] = val;
-          }
+        for (int k = 0; k < 8; ++k) {
+          const uint32_t a = smem_u32(tile + lane * 128 + ((k ^ (lane & 7)) * 16));
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a),
+                       "r"(v[4 * k]), "r"(v[4 * k + 1]), "r"(v[4 * k + 2]),
+                       "r"(v[4 * k + 3])
+                       : "memory");
         }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0 && mrow < w.M) {
+          if (p.accumulate)
+            tma_reduce_add_3d(om, smem_u32(tile), w.n0 + 32 * c, mrow,
+                              mat_idx);
+          else
+            tma_store_3d(om, smem_u32(tile), w.n0 + 32 * c, mrow, mat_idx);
+          bulk_commit();
+        }
+        ob ^= 1;
       }
       tc_fence_before();
       mbar_arrive(smem_u32(&tempty[slot]));
       tph ^= 1u << slot;
       slot ^= 1;
     }
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
   }
   __syncthreads();
   if (warp == 1) {
@@ -1159,7 +1225,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 size_t wgrad_smem_bytes(int E) {
-  return 1024 + WG_STAGES * WG_STAGE_BYTES +
+  return 1024 + WG_STAGES * WG_STAGE_BYTES + WG_OUT_BYTES +
          (2 * WG_STAGES + 5) * sizeof(uint64_t) + 4 * sizeof(uint32_t) +
          sizeof(int) * (kMats * (E + 1) + 1 + 2 * (E + 1));
 }
@@ -1178,6 +1244,10 @@ size_t expert_backward_rows_cap(int T, int K, int E) {
 }
 
 int launch_expert_backward(const BwdArgs& a, cudaStream_t s) {
+  auto mark = [&](int i) {
+    if (a.events != nullptr)
+      cudaEventRecord(static_cast<cudaEvent_t>(a.events[i]), s);
+  };
   const int T = a.T, K = a.topk, E = a.E, H = a.H, I = a.I, Is = a.I_shared;
   const int TK = T * K;
   const int cap = static_cast<int>(expert_backward_rows_cap(T, K, E));
@@ -1185,6 +1255,7 @@ int launch_expert_backward(const BwdArgs& a, cudaStream_t s) {
   if (dgrad_smem_bytes(E) > kSmemLimit || wgrad_smem_bytes(E) > kSmemLimit)
     return MOE_ERR_UNSUPPORTED;
   // ---- padded dispatch
+  mark(0);
   bwd_pad_kernel<<<(TK + kPadThreads - 1) / kPadThreads, kPadThreads, 0, s>>>(
       a.topk_idx, a.dest, a.offsets, a.counts, a.gate, TK, E, cap, a.poff,
       a.pdest, a.gp, a.status);
@@ -1222,6 +1293,7 @@ int launch_expert_backward(const BwdArgs& a, cudaStream_t s) {
   rc.k_r = H;
   rc.k_s = H;
   rc.wrows_r = I;
+  mark(1);
   int rcode = launch_dgrad<kRecomp>(rc, s);
   if (rcode != MOE_OK) return rcode;
 
@@ -1257,6 +1329,7 @@ int launch_expert_backward(const BwdArgs& a, cudaStream_t s) {
   dd.k_s = H;
   dd.wrows_r = H;
   dd.nfb = (I + 2 * BM - 1) / (2 * BM);
+  mark(2);
   rcode = launch_dgrad<kDgradDown>(dd, s);
   if (rcode != MOE_OK) return rcode;
 
@@ -1286,6 +1359,7 @@ int launch_expert_backward(const BwdArgs& a, cudaStream_t s) {
   du.k_r = 2 * I;
   du.k_s = 2 * Is;
   du.wrows_r = I;
+  mark(3);
   rcode = launch_dgrad<kDgradUp>(du, s);
   if (rcode != MOE_OK) return rcode;
 
@@ -1304,6 +1378,12 @@ int launch_expert_backward(const BwdArgs& a, cudaStream_t s) {
        make_tmap_bf16(&wp.b_s[0], a.x, H, T, BK) &&
        make_tmap_bf16(&wp.b_s[1], a.x, H, T, BK) &&
        make_tmap_bf16(&wp.b_s[2], a.hg_s, Is, T, BK);
+  ok = make_tmap_f32_3d_store(&wp.o_r[0], a.dw1, H, I, E) &&
+       make_tmap_f32_3d_store(&wp.o_r[1], a.dw3, H, I, E) &&
+       make_tmap_f32_3d_store(&wp.o_r[2], a.dw2, I, H, E) &&
+       make_tmap_f32_3d_store(&wp.o_s[0], a.dws1, H, Is, 1) &&
+       make_tmap_f32_3d_store(&wp.o_s[1], a.dws3, H, Is, 1) &&
+       make_tmap_f32_3d_store(&wp.o_s[2], a.dws2, Is, H, 1);
   if (!ok) return MOE_ERR_CUDA;
   wp.poff = a.poff;
   wp.out_r[0] = a.dw1;
@@ -1327,13 +1407,16 @@ int launch_expert_backward(const BwdArgs& a, cudaStream_t s) {
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
       return MOE_ERR_CUDA;
+    mark(4);
     wgrad_gemm_kernel<<<gemm_ctas(), kThreads, smem, s>>>(wp);
     if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
   }
 
   // ---- token gradient and gate gradients
+  mark(5);
   bwd_finalize_kernel<<<T, kRowThreads, 0, s>>>(
       a.dout, a.dxs, a.dxpp, a.pdest, a.dgp, dd.nfb, H, K, a.dx, a.dgate);
+  mark(6);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

@@ -132,6 +132,10 @@ struct BwdArgs {
   int accumulate;
   DevStatus* status;
   uint64_t wait_limit_ns;
+  // cudaEvent_t handles recorded before each of the 6 stages and after the
+  // last (dispatch, recompute, dgrad down, dgrad up, wgrad, finalize), or
+  // NULL
+  void* const* events = nullptr;
 };
 // rows of the padded dispatch: T*K + 15*E (each segment rounded up to 16)
 size_t expert_backward_rows_cap(int T, int K, int E);
@@ -182,6 +186,10 @@ bool make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t inner,
 // the same for a byte tensor (E4M3 codes): box [box_outer rows, 128 B]
 bool make_tmap_u8(CUtensorMap* m, const void* base, uint64_t inner,
                   uint64_t outer, uint32_t box_outer);
+// 3-D fp32 tensor [mats][rows][n] (n contiguous) for TMA stores and
+// reductions of 32 x 32 tiles, 128-byte swizzle
+bool make_tmap_f32_3d_store(CUtensorMap* m, void* base, uint64_t n,
+                            uint64_t rows, uint64_t mats);
 int sm_count();
 int gemm_ctas();           // persistent CTAs of the expert GEMMs
 void set_gemm_ctas(int n); // 0: one per SM

@@ -743,6 +743,7 @@ moe_status_t moe_expert_backward(const moe_dims_t* d, const moe_weights_t* w,
   a.accumulate = accumulate ? 1 : 0;
   a.status = st;
   a.wait_limit_ns = g_wait_limit_ns;
+  a.events = g_prof_events;
   return static_cast<moe_status_t>(moe::launch_expert_backward(a, s));
 }
 

@@ -503,6 +503,12 @@ void moe_set_gemm_ctas(int32_t n);
  * NULL / n = 0 disables.  The array must stay valid while enabled.  Global
  * state: not for concurrent use from several threads. */
 #define MOE_FORWARD_KERNELS 8
+/* While enabled, moe_expert_backward records events[0..6] of the same array
+ * around its six stages: 0 padded dispatch (3 kernels), 1 recompute of p,
+ * q (GEMM), 2 dgrad of the down projection (GEMM), 3 dgrad of the up
+ * projections (GEMM), 4 weight gradients (GEMM), 5 token and gate
+ * gradients, and events[6] after the last. */
+#define MOE_BACKWARD_STAGES 6
 void moe_set_profile_events(void* const* events, int32_t n);
 
 /* MOE_ABI_VERSION of the loaded library. */
