@@ -1055,7 +1055,8 @@ def run_expert_backward_gpu(args, rank, world, local_rank):
     import torch
     from deepseekmoe_routing_expert_moe_b300 import inputs, ops
     torch.cuda.set_device(local_rank)
-    cfg = inputs.CONFIGS["prefill_v3"]
+    cfg = inputs.CONFIGS["prefill_v3_e16" if args.workload.endswith("_e16")
+                         else "prefill_v3"]
     d = ops.dims_of(cfg)
     T, H, E, K, I, Is = cfg.T, cfg.H, cfg.E, cfg.topk, cfg.I, cfg.I_shared
     w1, w3, w2 = inputs.device_expert_weights(cfg, "cuda")
@@ -1167,7 +1168,7 @@ def run_expert_backward_gpu(args, rank, world, local_rank):
                 "achieved": round(stage_flops[dom] / t_dom / 1e12, 1),
                 "peak": tc, "unit": "TFLOP/s"}
     roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
-    roof["traffic"] = ncu_traffic(dom, "expert_backward_v3")
+    roof["traffic"] = ncu_traffic(dom, args.workload)
     roof["kernel"] = {"wgrad": "wgrad_gemm_kernel (fp32 dW1, dW3, dW2)",
                       "recompute": "dgrad_gemm_kernel<recompute>",
                       "dgrad_down": "dgrad_gemm_kernel<dgrad_down>",
@@ -1207,7 +1208,7 @@ def run_expert_backward_gpu(args, rank, world, local_rank):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic, seeded (x ~N(0,1), dout ~N(0,1) bf16, expert "
                 "weights ~N(0,0.02) bf16; routing from the layer forward)",
-        "config": {"workload": "expert_backward_v3: experts' backward of the "
+        "config": {"workload": f"{args.workload}: experts' backward of the "
                                f"V3 prefill layer, T={T}, H={H}, E={E}+1 "
                                f"shared, I={I}, top-{K}",
                    "T": T, "H": H, "E": E, "I": I, "topk": K,
@@ -1387,7 +1388,7 @@ def run_reference(args):
         return run_decode_fp8_reference(args)
     if args.workload == "route_backward_v3":
         return run_backward_reference(args)
-    if args.workload == "expert_backward_v3":
+    if args.workload in ("expert_backward_v3", "expert_backward_v3_e16"):
         return run_expert_backward_reference(args)
     cfg = inputs.CONFIGS[args.workload]
     n = args.ref_tokens
@@ -1426,7 +1427,7 @@ def main():
                              "route_v3", "prefill_v3_e32", "balance_v3",
                              "decode_v3_fp8", "prefill_v3_fp8",
                              "decode_v3_e32_fp8", "route_backward_v3",
-                             "expert_backward_v3"))
+                             "expert_backward_v3", "expert_backward_v3_e16"))
     ap.add_argument("--cpu-sample-tokens", type=int, default=4)
     ap.add_argument("--ref-tokens", type=int, default=1)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -1457,7 +1458,7 @@ def main():
         res = run_fp8_gpu(args, rank, world, local_rank)
     elif args.workload == "route_backward_v3":
         res = run_backward_gpu(args, rank, world, local_rank)
-    elif args.workload == "expert_backward_v3":
+    elif args.workload in ("expert_backward_v3", "expert_backward_v3_e16"):
         res = run_expert_backward_gpu(args, rank, world, local_rank)
     else:
         res = run_gpu(args, rank, world, local_rank)

@@ -140,24 +140,28 @@ __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst,
       : "memory");
 }
 
-// 3-D tiled bulk tensor store shared -> global (bulk-group completion)
+// 3-D tiled bulk tensor store shared -> global (bulk-group completion),
+// with an L2 cache policy for the written lines
 __device__ __forceinline__ void tma_store_3d(const void* tmap, uint32_t src,
                                              int32_t c0, int32_t c1,
-                                             int32_t c2) {
+                                             int32_t c2, uint64_t policy) {
   asm volatile(
-      "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group "
-      "[%0, {%2, %3, %4}], [%1];" ::"l"(reinterpret_cast<uint64_t>(tmap)),
-      "r"(src), "r"(c0), "r"(c1), "r"(c2)
+      "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group"
+      ".L2::cache_hint [%0, {%2, %3, %4}], [%1], %5;" ::"l"(
+          reinterpret_cast<uint64_t>(tmap)),
+      "r"(src), "r"(c0), "r"(c1), "r"(c2), "l"(policy)
       : "memory");
 }
 // the same, added element-wise to the global tensor (fp32 add in L2)
 __device__ __forceinline__ void tma_reduce_add_3d(const void* tmap,
                                                   uint32_t src, int32_t c0,
-                                                  int32_t c1, int32_t c2) {
+                                                  int32_t c1, int32_t c2,
+                                                  uint64_t policy) {
   asm volatile(
-      "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group "
-      "[%0, {%2, %3, %4}], [%1];" ::"l"(reinterpret_cast<uint64_t>(tmap)),
-      "r"(src), "r"(c0), "r"(c1), "r"(c2)
+      "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group"
+      ".L2::cache_hint [%0, {%2, %3, %4}], [%1], %5;" ::"l"(
+          reinterpret_cast<uint64_t>(tmap)),
+      "r"(src), "r"(c0), "r"(c1), "r"(c2), "l"(policy)
       : "memory");
 }
 __device__ __forceinline__ void bulk_commit() {
@@ -166,6 +170,10 @@ __device__ __forceinline__ void bulk_commit() {
 // wait until at most one bulk group still reads its shared-memory source
 __device__ __forceinline__ void bulk_wait_read_le1() {
   asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+// wait until at most three bulk groups still read their sources
+__device__ __forceinline__ void bulk_wait_read_le3() {
+  asm volatile("cp.async.bulk.wait_group.read 3;" ::: "memory");
 }
 // wait until every bulk group of this thread has completed
 __device__ __forceinline__ void bulk_wait_all() {

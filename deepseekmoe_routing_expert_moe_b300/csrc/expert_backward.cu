@@ -881,10 +881,11 @@ constexpr int WG_STAGES = 3;
 constexpr uint32_t WG_A_BYTES = BM * BK * 2;         // 16 KB
 constexpr uint32_t WG_B_BYTES = WG_N * BK * 2;       // 32 KB
 constexpr uint32_t WG_STAGE_BYTES = WG_A_BYTES + WG_B_BYTES;
-// fp32 output staging: per epilogue warp two 32 x 32 tiles (4 KB each),
+// fp32 output staging: per epilogue warp four 32 x 32 tiles (4 KB each),
 // stored by TMA (or added to the output in L2 when accumulating)
+constexpr int WG_OUT_BUFS = 4;
 constexpr uint32_t WG_OUT_TILE = 32 * 32 * 4;
-constexpr uint32_t WG_OUT_BYTES = kEpiWarps * 2 * WG_OUT_TILE;
+constexpr uint32_t WG_OUT_BYTES = kEpiWarps * WG_OUT_BUFS * WG_OUT_TILE;
 constexpr int kMats = 3;   // dW1, dW3, dW2
 
 struct WgParams {
@@ -1144,14 +1145,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------- epilogue
     // Each warp owns 32 rows (its TMEM lane quadrant): per 32 columns it
     // writes its rows into a swizzled 4 KB staging tile and one lane
-    // issues the TMA store (or reduce-add) of the tile; two tiles
-    // alternate, so a tile is rewritten only after its store has read it.
+    // issues the TMA store (or reduce-add) of the tile; four tiles rotate,
+    // and a tile is rewritten only after its store has read it (at most
+    // three stores of the warp still reading).
     const int q = warp & 3;
     const int r = q * 32 + lane;
     uint32_t tph = 0;
     int slot = 0;
     int ob = 0;
-    uint8_t* stage_base = sO + q * 2 * WG_OUT_TILE;
+    uint8_t* stage_base = sO + q * WG_OUT_BUFS * WG_OUT_TILE;
+    // the gradients stream out once: their lines go first when L2 needs
+    // room, so the operand rows (kept with evict_last) stay resident
+    const uint64_t pol_out = policy_evict_first();
     for (int u = blockIdx.x; u < total; u += gridDim.x) {
       const WUnit w = wg_decode(p, u, upre, srow0, srows, NP);
       const bool sh = w.seg == 0;
@@ -1185,7 +1190,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
         tmem_ld_wait();
         uint8_t* tile = stage_base + ob * WG_OUT_TILE;
-        if (lane == 0) bulk_wait_read_le1();
+        if (lane == 0) bulk_wait_read_le3();
         __syncwarp();
         // row `lane`: 16-byte chunk k at position k ^ (lane & 7) (the
         // 128-byte swizzle of the tensor map)
@@ -1202,12 +1207,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0 && mrow < w.M) {
           if (p.accumulate)
             tma_reduce_add_3d(om, smem_u32(tile), w.n0 + 32 * c, mrow,
-                              mat_idx);
+                              mat_idx, pol_out);
           else
-            tma_store_3d(om, smem_u32(tile), w.n0 + 32 * c, mrow, mat_idx);
+            tma_store_3d(om, smem_u32(tile), w.n0 + 32 * c, mrow, mat_idx,
+                         pol_out);
           bulk_commit();
         }
-        ob ^= 1;
+        ob = (ob + 1) % WG_OUT_BUFS;
       }
       tc_fence_before();
       mbar_arrive(smem_u32(&tempty[slot]));

@@ -105,6 +105,13 @@ CONFIGS = {
     "decode_v3_e32": MoEConfig("decode_v3_e32", 6, T=128, H=7168, E=32,
                                n_group=8, topk_group=4, topk=8, I=2048,
                                I_shared=2048),
+    # profiling stand-in for the experts' backward at the prefill shape:
+    # 128 rows per expert as at T = 4096, 16 experts (1.4 GB of weights,
+    # 2.8 GB of fp32 weight gradients), so a full counter capture holds a
+    # few GB on the device
+    "prefill_v3_e16": MoEConfig("prefill_v3_e16", 7, T=256, H=7168, E=16,
+                                n_group=4, topk_group=2, topk=8, I=2048,
+                                I_shared=2048),
 }
 
 
