@@ -1,0 +1,126 @@
+// Expert parallelism: the row bookkeeping of the pages' dispatch / combine
+// ("02 · DeepSeek-V3" (PaperTrace) §1.3 node-limited routing, §2 and §5.1:
+// experts are partitioned over devices, each token's rows are sent to the
+// devices that hold its chosen experts and the outputs come back).
+//
+// With the experts of a device contiguous (device r holds experts
+// [r*El, (r+1)*El)), the expert-sorted dispatch rows of moe_permute are
+// already grouped by destination device, so the send side needs no kernel.
+// A device receives, from each source device s in order, that source's rows
+// for its El experts (expert-sorted within the source's block): the
+// "source-major" order.  The grouped GEMM wants the rows of each expert
+// together: the "expert-major" order, expert l's rows from source 0, then
+// source 1, ...  ep_plan_kernel computes, for every received row i, its
+// expert-major position perm[i] and the local segment offsets; the row
+// copies in both directions are ep_rows_kernel.
+#include <cstdint>
+
+#include "device_common.cuh"
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int kPlanThreads = 256;
+constexpr int kPlanRowsPerBlock = 4096;
+
+// counts [n_src][n_local]: rows source s sends for local expert l.
+// perm[i] for source-major row i = expert-major row; block 0 also writes
+// offsets_local [n_local + 1] (expert-major segment starts).
+__global__ void __launch_bounds__(kPlanThreads)
+    ep_plan_kernel(const int32_t* __restrict__ counts, int n_src, int n_local,
+                   long long rows, int32_t* __restrict__ perm,
+                   int32_t* __restrict__ offsets_local, DevStatus* st) {
+  extern __shared__ int sm[];
+  const int n = n_src * n_local;
+  int* src_off = sm;          // [n + 1] exclusive prefix, source-major
+  int* exp_off = sm + n + 1;  // [n] exclusive prefix, expert-major (l, s)
+  if (threadIdx.x == 0) {
+    int run = 0;
+    for (int i = 0; i < n; ++i) {
+      src_off[i] = run;
+      run += counts[i];
+    }
+    src_off[n] = run;
+    run = 0;
+    for (int l = 0; l < n_local; ++l)
+      for (int s = 0; s < n_src; ++s) {
+        exp_off[l * n_src + s] = run;
+        run += counts[s * n_local + l];
+      }
+    if (src_off[n] != rows) record_error(st, MOE_ERR_DEVICE_BOUNDS, 60);
+  }
+  __syncthreads();
+  if (blockIdx.x == 0) {
+    for (int l = threadIdx.x; l <= n_local; l += kPlanThreads)
+      offsets_local[l] = l < n_local ? exp_off[l * n_src] : src_off[n];
+  }
+  const long long lim = min((long long)src_off[n], rows);
+  const long long r0 = (long long)blockIdx.x * kPlanRowsPerBlock;
+  const long long r1 = min(lim, r0 + kPlanRowsPerBlock);
+  for (long long i = r0 + threadIdx.x; i < r1; i += kPlanThreads) {
+    // the (source, expert) cell holding source-major row i
+    int lo = 0, hi = n - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (src_off[mid] <= i)
+        lo = mid;
+      else
+        hi = mid - 1;
+    }
+    const int s = lo / n_local, l = lo - s * n_local;
+    perm[i] = exp_off[l * n_src + s] + (int)(i - src_off[lo]);
+  }
+  // rows beyond the counts (inconsistent sizes): mapped to themselves
+  for (long long i = max(r0, lim) + threadIdx.x;
+       i < min(rows, r0 + kPlanRowsPerBlock); i += kPlanThreads)
+    perm[i] = (int)i;
+}
+
+// inverse = 0: out[perm[i]] = in[i]; inverse = 1: out[i] = in[perm[i]];
+// rows of row_bytes (a multiple of 16), one block per row
+__global__ void __launch_bounds__(128)
+    ep_rows_kernel(const uint8_t* __restrict__ in, long long rows,
+                   long long row_bytes, const int32_t* __restrict__ perm,
+                   int inverse, uint8_t* __restrict__ out, DevStatus* st) {
+  const long long i = blockIdx.x;
+  const int p = perm[i];
+  if (p < 0 || p >= rows) {
+    record_error(st, MOE_ERR_DEVICE_BOUNDS, 61);
+    return;
+  }
+  const long long src = inverse ? p : i, dst = inverse ? i : p;
+  const uint4* a = reinterpret_cast<const uint4*>(in + src * row_bytes);
+  uint4* b = reinterpret_cast<uint4*>(out + dst * row_bytes);
+  for (long long c = threadIdx.x; c < row_bytes / 16; c += blockDim.x)
+    b[c] = __ldg(a + c);
+}
+
+}  // namespace
+
+int ep_plan_max_cells() { return 4096; }
+
+cudaError_t launch_ep_plan(const int32_t* counts, int n_src, int n_local,
+                           long long rows, int32_t* perm,
+                           int32_t* offsets_local, DevStatus* st,
+                           cudaStream_t s) {
+  const long long nb =
+      rows > 0 ? (rows + kPlanRowsPerBlock - 1) / kPlanRowsPerBlock : 1;
+  const size_t smem = sizeof(int) * (2 * n_src * n_local + 1);
+  ep_plan_kernel<<<(unsigned)nb, kPlanThreads, smem, s>>>(
+      counts, n_src, n_local, rows, perm, offsets_local, st);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_ep_rows(const void* in, long long rows,
+                           long long row_bytes, const int32_t* perm,
+                           int inverse, void* out, DevStatus* st,
+                           cudaStream_t s) {
+  if (rows == 0) return cudaSuccess;
+  ep_rows_kernel<<<(unsigned)rows, 128, 0, s>>>(
+      static_cast<const uint8_t*>(in), rows, row_bytes, perm, inverse,
+      static_cast<uint8_t*>(out), st);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

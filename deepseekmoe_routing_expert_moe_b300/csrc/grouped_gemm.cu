@@ -638,15 +638,24 @@ bool token_maps(CUtensorMap (&m)[kTokBoxes], const void* base, uint64_t k,
 
 int launch_expert_ffn(const FfnArgs& a, cudaStream_t s) {
   const int TK = a.T * a.topk;
+  // without x the shared expert is skipped: its segment gets no rows and
+  // its maps are encoded on the routed tensors (never read)
+  const bool shared = a.x != nullptr;
+  const int Ts = shared ? a.T : 0;
   // ---- up projection + SwiGLU
   GemmParams up;
   std::memset(&up, 0, sizeof(up));
   bool ok = token_maps(up.tok_routed, a.xp, a.H, TK) &&
-            token_maps(up.tok_shared, a.x, a.H, a.T) &&
+            (shared ? token_maps(up.tok_shared, a.x, a.H, a.T)
+                    : token_maps(up.tok_shared, a.xp, a.H, TK)) &&
             make_tmap_bf16(&up.wa_routed, a.w1, a.H, (uint64_t)a.E * a.I, BM) &&
             make_tmap_bf16(&up.wb_routed, a.w3, a.H, (uint64_t)a.E * a.I, BM) &&
-            make_tmap_bf16(&up.wa_shared, a.ws1, a.H, a.I_shared, BM) &&
-            make_tmap_bf16(&up.wb_shared, a.ws3, a.H, a.I_shared, BM);
+            (shared ? make_tmap_bf16(&up.wa_shared, a.ws1, a.H, a.I_shared, BM) &&
+                          make_tmap_bf16(&up.wb_shared, a.ws3, a.H, a.I_shared, BM)
+                    : make_tmap_bf16(&up.wa_shared, a.w1, a.H,
+                                     (uint64_t)a.E * a.I, BM) &&
+                          make_tmap_bf16(&up.wb_shared, a.w3, a.H,
+                                         (uint64_t)a.E * a.I, BM));
   if (!ok) return MOE_ERR_CUDA;
   up.offsets = a.offsets;
   up.out_routed = a.h;
@@ -654,7 +663,7 @@ int launch_expert_ffn(const FfnArgs& a, cudaStream_t s) {
   up.status = a.status;
   up.wait_limit_ns = a.wait_limit_ns;
   up.E = a.E;
-  up.T = a.T;
+  up.T = Ts;
   up.TK = TK;
   up.n_routed = a.I;
   up.n_shared = a.I_shared;
@@ -669,9 +678,12 @@ int launch_expert_ffn(const FfnArgs& a, cudaStream_t s) {
   GemmParams dn;
   std::memset(&dn, 0, sizeof(dn));
   ok = token_maps(dn.tok_routed, a.h, a.I, TK) &&
-       token_maps(dn.tok_shared, a.hs, a.I_shared, a.T) &&
+       (shared ? token_maps(dn.tok_shared, a.hs, a.I_shared, a.T)
+               : token_maps(dn.tok_shared, a.h, a.I, TK)) &&
        make_tmap_bf16(&dn.wa_routed, a.w2, a.I, (uint64_t)a.E * a.H, BM) &&
-       make_tmap_bf16(&dn.wa_shared, a.ws2, a.I_shared, a.H, BM);
+       (shared ? make_tmap_bf16(&dn.wa_shared, a.ws2, a.I_shared, a.H, BM)
+               : make_tmap_bf16(&dn.wa_shared, a.w2, a.I,
+                                (uint64_t)a.E * a.H, BM));
   if (!ok) return MOE_ERR_CUDA;
   dn.wb_routed = dn.wa_routed;
   dn.wb_shared = dn.wa_shared;
@@ -681,7 +693,7 @@ int launch_expert_ffn(const FfnArgs& a, cudaStream_t s) {
   dn.status = a.status;
   dn.wait_limit_ns = a.wait_limit_ns;
   dn.E = a.E;
-  dn.T = a.T;
+  dn.T = Ts;
   dn.TK = TK;
   dn.n_routed = a.H;
   dn.n_shared = a.H;

@@ -141,6 +141,17 @@ struct BwdArgs {
 size_t expert_backward_rows_cap(int T, int K, int E);
 int launch_expert_backward(const BwdArgs& a, cudaStream_t s);
 
+// ---- ep.cu
+int ep_plan_max_cells();  // n_src * n_local limit of launch_ep_plan
+cudaError_t launch_ep_plan(const int32_t* counts, int n_src, int n_local,
+                           long long rows, int32_t* perm,
+                           int32_t* offsets_local, DevStatus* st,
+                           cudaStream_t s);
+cudaError_t launch_ep_rows(const void* in, long long rows,
+                           long long row_bytes, const int32_t* perm,
+                           int inverse, void* out, DevStatus* st,
+                           cudaStream_t s);
+
 // ---- fp8_gemm.cu
 struct FfnFp8Args {
   int T, H, E, topk, I, I_shared;

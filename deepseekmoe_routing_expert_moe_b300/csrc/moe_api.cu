@@ -36,6 +36,21 @@ inline cudaStream_t cs(moe_stream_t s) { return static_cast<cudaStream_t>(s); }
 
 bool is_pow2(int v) { return v > 0 && (v & (v - 1)) == 0; }
 
+// Shape checks of the expert GEMMs alone (no routing: any E >= 1).
+moe_status_t check_ffn_only_dims(const moe_dims_t* d) {
+  if (d == nullptr) return MOE_ERR_INVALID_ARG;
+  if (d->T < 0 || d->H <= 0 || d->E <= 0 || d->topk <= 0 || d->I <= 0 ||
+      d->I_shared <= 0)
+    return MOE_ERR_INVALID_ARG;
+  if ((long long)d->T * (d->topk + 1) >= (1ll << 31)) return MOE_ERR_UNSUPPORTED;
+  if (d->H % 64 != 0 || d->I % 64 != 0 || d->I_shared % 64 != 0)
+    return MOE_ERR_UNSUPPORTED;
+  if (d->E > 1024 || (long long)d->E * d->I >= (1ll << 31) ||
+      (long long)d->E * d->H >= (1ll << 31))
+    return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
 // Shape checks shared by every entry point.
 moe_status_t check_dims(const moe_dims_t* d, bool need_ffn) {
   if (d == nullptr) return MOE_ERR_INVALID_ARG;
@@ -317,8 +332,14 @@ size_t moe_workspace_bytes(const moe_dims_t* d, moe_ws_kind_t which) {
   const bool ffn = which == MOE_WS_EXPERT_FFN || which == MOE_WS_FORWARD ||
                    which == MOE_WS_EXPERT_FFN_FP8 ||
                    which == MOE_WS_EXPERT_BWD;
-  if (check_dims(d, ffn) != MOE_OK) return 0;
   if (which < MOE_WS_ROUTE || which > MOE_WS_EXPERT_BWD) return 0;
+  // the expert GEMMs alone (moe_expert_ffn, moe_expert_ffn_routed) do not
+  // route: their workspace takes any expert count
+  if (which == MOE_WS_EXPERT_FFN) {
+    if (check_ffn_only_dims(d) != MOE_OK) return 0;
+  } else if (check_dims(d, ffn) != MOE_OK) {
+    return 0;
+  }
   return layout(d, which).total;
 }
 
@@ -447,6 +468,72 @@ moe_status_t moe_expert_ffn(const moe_dims_t* d, const moe_weights_t* w,
   return ffn_launch(d, w, xp, x, offsets, at<uint16_t>(ws, L.h),
                     at<uint16_t>(ws, L.hs), yp, ys, at<DevStatus>(ws, 0),
                     cs(stream));
+}
+
+moe_status_t moe_expert_ffn_routed(const moe_dims_t* d, const moe_weights_t* w,
+                                   const uint16_t* xp, const int32_t* offsets,
+                                   uint16_t* yp, void* ws, size_t ws_bytes,
+                                   moe_stream_t stream) {
+  MOE_TRY(check_ffn_only_dims(d));
+  MOE_NEED(w);
+  MOE_NEED(w->w1);
+  MOE_NEED(w->w3);
+  MOE_NEED(w->w2);
+  MOE_ALIGN(w->w1);
+  MOE_ALIGN(w->w3);
+  MOE_ALIGN(w->w2);
+  MOE_NEED_T(xp);
+  MOE_NEED(offsets);
+  MOE_NEED_T(yp);
+  MOE_ALIGN(xp);
+  MOE_ALIGN(offsets);
+  MOE_ALIGN(yp);
+  MOE_TRY(check_ws(d, MOE_WS_EXPERT_FFN, ws, ws_bytes));
+  if (d->T == 0) return MOE_OK;
+  const Layout L = layout(d, MOE_WS_EXPERT_FFN);
+  moe_weights_t rw = *w;
+  rw.ws1 = rw.ws3 = rw.ws2 = nullptr;
+  return ffn_launch(d, &rw, xp, nullptr, offsets, at<uint16_t>(ws, L.h),
+                    nullptr, yp, nullptr, at<DevStatus>(ws, 0), cs(stream));
+}
+
+moe_status_t moe_ep_plan(int32_t n_src, int32_t n_local, const int32_t* counts,
+                         int64_t rows, int32_t* perm, int32_t* offsets_local,
+                         void* ws, moe_stream_t stream) {
+  if (n_src < 1 || n_local < 1 || rows < 0 || rows >= (1ll << 31))
+    return MOE_ERR_INVALID_ARG;
+  if ((long long)n_src * n_local > moe::ep_plan_max_cells())
+    return MOE_ERR_UNSUPPORTED;
+  MOE_NEED(counts);
+  MOE_NEED(offsets_local);
+  if (rows > 0) MOE_NEED(perm);
+  MOE_ALIGN(counts);
+  MOE_ALIGN(perm);
+  MOE_ALIGN(offsets_local);
+  MOE_ALIGN(ws);
+  return cuda_ok(moe::launch_ep_plan(
+      counts, n_src, n_local, rows, perm, offsets_local,
+      ws ? at<DevStatus>(ws, 0) : nullptr, cs(stream)));
+}
+
+moe_status_t moe_ep_permute_rows(const void* in, int64_t rows,
+                                 int64_t row_bytes, const int32_t* perm,
+                                 int32_t inverse, void* out, void* ws,
+                                 moe_stream_t stream) {
+  if (rows < 0 || rows >= (1ll << 31) || row_bytes <= 0 || row_bytes % 16)
+    return MOE_ERR_INVALID_ARG;
+  if (rows == 0) return MOE_OK;
+  MOE_NEED(in);
+  MOE_NEED(out);
+  MOE_NEED(perm);
+  MOE_ALIGN(in);
+  MOE_ALIGN(out);
+  MOE_ALIGN(perm);
+  MOE_ALIGN(ws);
+  return cuda_ok(moe::launch_ep_rows(in, rows, row_bytes, perm,
+                                     inverse ? 1 : 0, out,
+                                     ws ? at<DevStatus>(ws, 0) : nullptr,
+                                     cs(stream)));
 }
 
 moe_status_t moe_combine(const moe_dims_t* d, const uint16_t* x,

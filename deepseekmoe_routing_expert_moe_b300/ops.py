@@ -65,6 +65,11 @@ _SIGS = {
     "moe_permute": (_I, [_D, _P, _P, _P, _P, _P, _P, _P, _S, _P]),
     "moe_expert_ffn": (_I, [_D, _W, _P, _P, _P, _P, _P, _P, _S, _P]),
     "moe_combine": (_I, [_D, _P, _P, _P, _P, _P, _P, _P]),
+    "moe_expert_ffn_routed": (_I, [_D, _W, _P, _P, _P, _P, _S, _P]),
+    "moe_ep_plan": (_I, [ctypes.c_int32, ctypes.c_int32, _P, ctypes.c_int64,
+                         _P, _P, _P, _P]),
+    "moe_ep_permute_rows": (_I, [_P, ctypes.c_int64, ctypes.c_int64, _P,
+                                 ctypes.c_int32, _P, _P, _P]),
     "moe_bias_update": (_I, [_D, _P, _P, _P, _P]),
     "moe_seq_balance_loss": (_I, [_D, _P, ctypes.c_int32, ctypes.c_float, _P,
                                   _P, _P, _P, _S, _P]),
@@ -240,6 +245,30 @@ def moe_expert_ffn(d, w: Weights, xp, x, offsets, yp, ys, ws, stream=None):
         ctypes.byref(d), ctypes.byref(w.struct), _ptr(xp), _ptr(x),
         _ptr(offsets), _ptr(yp), _ptr(ys), _ptr(ws), ws.numel(),
         _stream(stream)))
+
+
+def moe_expert_ffn_routed(d, w: Weights, xp, offsets, yp, ws, stream=None):
+    """Routed experts only over d.T * d.topk expert-sorted rows."""
+    _check("moe_expert_ffn_routed", lib().moe_expert_ffn_routed(
+        ctypes.byref(d), ctypes.byref(w.struct), _ptr(xp), _ptr(offsets),
+        _ptr(yp), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def moe_ep_plan(counts, rows, perm, offsets_local, ws=None, stream=None):
+    """counts: [n_src, n_local] int32 device tensor."""
+    n_src, n_local = counts.shape
+    _check("moe_ep_plan", lib().moe_ep_plan(
+        n_src, n_local, _ptr(counts), int(rows), _ptr(perm),
+        _ptr(offsets_local), _ptr(ws), _stream(stream)))
+
+
+def moe_ep_permute_rows(inp, perm, out, inverse=False, ws=None, stream=None):
+    """Rows of a 2-D device tensor moved by an expert-parallel map."""
+    rows = inp.shape[0]
+    row_bytes = inp.numel() * inp.element_size() // max(rows, 1)
+    _check("moe_ep_permute_rows", lib().moe_ep_permute_rows(
+        _ptr(inp), rows, row_bytes, _ptr(perm), 1 if inverse else 0,
+        _ptr(out), _ptr(ws), _stream(stream)))
 
 
 def moe_combine(d, x, ys, yp, dest, topk_gate, out, stream=None):

@@ -221,6 +221,49 @@ moe_status_t moe_expert_ffn(const moe_dims_t* d, const moe_weights_t* w,
                             uint16_t* ys, void* ws, size_t ws_bytes,
                             moe_stream_t stream);
 
+/* Routed experts only: the grouped SwiGLU FFNs of moe_expert_ffn over
+ * R = d->T * d->topk expert-sorted rows, without the shared expert -- the
+ * receive side of expert parallelism ("02 · DeepSeek-V3" §5.1: a device
+ * runs its own experts on the rows other devices sent it); pass d->T = R,
+ * d->topk = 1 for R received rows and d->E = the device's experts.
+ *   xp [R, H] bf16, offsets [E+1] int32 (device; offsets[E] <= R),
+ *   yp [R, H] bf16 out.  Only w->w1, w3, w2 are read (others may be NULL).
+ * Nothing is routed here, so the routing shape rules do not apply: any
+ * E >= 1 (<= 1024); n_group and topk_group are not read.  (The shared
+ * expert can run through this call too, as one expert over the tokens.)
+ * Workspace: MOE_WS_EXPERT_FFN (its shared-expert part is unused), which
+ * moe_workspace_bytes sizes for such dims as well. */
+moe_status_t moe_expert_ffn_routed(const moe_dims_t* d, const moe_weights_t* w,
+                                   const uint16_t* xp, const int32_t* offsets,
+                                   uint16_t* yp, void* ws, size_t ws_bytes,
+                                   moe_stream_t stream);
+
+/* Expert parallelism: the receive-side row order ("02 · DeepSeek-V3" §1.3
+ * node-limited routing, §2 and §5.1 dispatch / combine across devices).
+ * Device r holds experts [r*El, (r+1)*El); the rows it receives arrive
+ * from each source device s in order, each source's rows sorted by expert
+ * ("source-major").  moe_ep_plan maps them to "expert-major" order (expert
+ * l's rows from source 0, 1, ... together, the grouped GEMM's segments):
+ *   counts [n_src, n_local] int32 (device): rows source s sends for local
+ *          expert l (the sources' moe_route counts of these experts)
+ *   rows   = sum of counts (the host knows it: it sized the exchange)
+ *   perm   [rows] int32 out: expert-major row of source-major row i
+ *   offsets_local [n_local + 1] int32 out: expert-major segment starts
+ * n_src * n_local <= 4096 (MOE_ERR_UNSUPPORTED beyond).  A sum of counts
+ * other than rows records MOE_ERR_DEVICE_BOUNDS in the error word of ws
+ * (any workspace; may be NULL: nothing recorded).
+ * moe_ep_permute_rows moves rows of row_bytes (a multiple of 16) by such
+ * a map: inverse = 0: out[perm[i]] = in[i] (source-major -> expert-major);
+ * inverse = 1: out[i] = in[perm[i]] (back, for the return trip).  in and
+ * out may not alias. */
+moe_status_t moe_ep_plan(int32_t n_src, int32_t n_local, const int32_t* counts,
+                         int64_t rows, int32_t* perm, int32_t* offsets_local,
+                         void* ws, moe_stream_t stream);
+moe_status_t moe_ep_permute_rows(const void* in, int64_t rows,
+                                 int64_t row_bytes, const int32_t* perm,
+                                 int32_t inverse, void* out, void* ws,
+                                 moe_stream_t stream);
+
 /* Combine (eq. 12): out_t = bf16( x_t + ys_t + sum_k g_{t,k} yp[dest[t,k]] ),
  * fp32 arithmetic, slots summed in order.  out [T, H] bf16 may not alias
  * the inputs.  A slot whose dest lies outside [0, T*K) (moe_permute writes
