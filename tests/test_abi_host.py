@@ -241,3 +241,52 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(ops, "_lib", None)
     with pytest.raises(RuntimeError, match="no CPU fallback"):
         ops.lib()
+
+
+def test_expert_backward_validation(L):
+    d = ops.dims(**V3)
+    fn = L.moe_expert_backward
+    by = ctypes.byref
+    need = ops.workspace_bytes(d, ops.MOE_WS_EXPERT_BWD)
+    # padded dispatch rows (T*K + 15*E) of x, dout, the recomputed p, q
+    # (fp32) and the dgrad rows
+    cap = 4096 * 8 + 15 * 256
+    assert need >= cap * 7168 * 2 * 3 + cap * 2048 * 4 * 2
+    w = ops.MoeWeights(*(FAKE,) * 7, None)
+
+    def call(dd=d, ww=w, x=FAKE, dw1=FAKE, ws_bytes=1 << 40):
+        return fn(by(dd), by(ww), x, FAKE, FAKE, FAKE, 0, FAKE, FAKE, dw1,
+                  FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ws_bytes, None)
+    assert call(x=None) == 1
+    assert call(dw1=None) == 1
+    assert call(ww=ops.MoeWeights(FAKE, None, *(FAKE,) * 5, None)) == 1
+    assert call(x=FAKE + 2) == 3
+    assert call(ws_bytes=4096) == 4
+    assert call(dd=ops.dims(**dict(V3, I=100))) == 2
+
+
+def test_routed_ffn_and_expert_parallel_maps_validation(L):
+    by = ctypes.byref
+    # no routing here: one expert, one group is fine
+    d1 = ops.dims(T=100, H=256, E=1, n_group=1, topk_group=1, topk=1, I=128,
+                  I_shared=64)
+    assert ops.workspace_bytes(d1, ops.MOE_WS_EXPERT_FFN) > 0
+    assert ops.workspace_bytes(d1, ops.MOE_WS_ROUTE) == 0   # routing rules
+    w = ops.MoeWeights(None, FAKE, FAKE, FAKE, None, None, None, None)
+    fr = L.moe_expert_ffn_routed
+    assert fr(by(d1), by(w), FAKE, FAKE, FAKE, FAKE, 8, None) == 4
+    assert fr(by(d1), by(ops.MoeWeights(None, None, FAKE, FAKE, None, None,
+                                        None, None)),
+              FAKE, FAKE, FAKE, FAKE, 1 << 30, None) == 1
+    assert fr(by(ops.dims(T=100, H=250, E=1, n_group=1, topk_group=1,
+                          topk=1, I=128, I_shared=64)), by(w), FAKE, FAKE,
+              FAKE, FAKE, 1 << 30, None) == 2
+    plan, rows = L.moe_ep_plan, L.moe_ep_permute_rows
+    assert plan(0, 4, FAKE, 10, FAKE, FAKE, None, None) == 1
+    assert plan(65, 64, FAKE, 10, FAKE, FAKE, None, None) == 2  # > 4096 cells
+    assert plan(2, 4, FAKE, -1, FAKE, FAKE, None, None) == 1
+    assert plan(2, 4, FAKE + 4, 10, FAKE, FAKE, None, None) == 3
+    assert rows(FAKE, 10, 24, FAKE, 0, FAKE, None, None) == 1   # % 16
+    assert rows(FAKE, 10, 32, None, 0, FAKE, None, None) == 1
+    assert rows(FAKE + 8, 10, 32, FAKE, 0, FAKE, None, None) == 3
+    assert rows(None, 0, 32, None, 0, None, None, None) == 0
