@@ -1384,7 +1384,7 @@ def run_reference(args):
     if args.workload == "balance_v3":
         return run_balance_reference(args)
     if args.workload in ("decode_v3_fp8", "prefill_v3_fp8",
-                         "decode_v3_e32_fp8"):
+                         "decode_v3_e32_fp8", "prefill_v3_e32_fp8"):
         return run_decode_fp8_reference(args)
     if args.workload == "route_backward_v3":
         return run_backward_reference(args)
@@ -1426,7 +1426,8 @@ def main():
                     choices=("prefill_v3", "decode_v3", "skewed_v3",
                              "route_v3", "prefill_v3_e32", "balance_v3",
                              "decode_v3_fp8", "prefill_v3_fp8",
-                             "decode_v3_e32_fp8", "route_backward_v3",
+                             "decode_v3_e32_fp8", "prefill_v3_e32_fp8",
+                             "route_backward_v3",
                              "expert_backward_v3", "expert_backward_v3_e16"))
     ap.add_argument("--cpu-sample-tokens", type=int, default=4)
     ap.add_argument("--ref-tokens", type=int, default=1)
@@ -1454,7 +1455,7 @@ def main():
     elif args.workload == "balance_v3":
         res = run_balance_gpu(args, rank, world, local_rank)
     elif args.workload in ("decode_v3_fp8", "prefill_v3_fp8",
-                           "decode_v3_e32_fp8"):
+                           "decode_v3_e32_fp8", "prefill_v3_e32_fp8"):
         res = run_fp8_gpu(args, rank, world, local_rank)
     elif args.workload == "route_backward_v3":
         res = run_backward_gpu(args, rank, world, local_rank)
