@@ -881,11 +881,15 @@ constexpr int WG_STAGES = 3;
 constexpr uint32_t WG_A_BYTES = BM * BK * 2;         // 16 KB
 constexpr uint32_t WG_B_BYTES = WG_N * BK * 2;       // 32 KB
 constexpr uint32_t WG_STAGE_BYTES = WG_A_BYTES + WG_B_BYTES;
-// fp32 output staging: per epilogue warp four 32 x 32 tiles (4 KB each),
+// eight epilogue warps: two per tensor-memory lane quadrant, each storing
+// half of a unit's columns (the fp32 stores are the kernel's long pole)
+constexpr int kWgEpiWarps = 8;
+constexpr int kWgThreads = 32 * (kEpiWarp0 + kWgEpiWarps);
+// fp32 output staging: per epilogue warp two 32 x 32 tiles (4 KB each),
 // stored by TMA (or added to the output in L2 when accumulating)
-constexpr int WG_OUT_BUFS = 4;
+constexpr int WG_OUT_BUFS = 2;
 constexpr uint32_t WG_OUT_TILE = 32 * 32 * 4;
-constexpr uint32_t WG_OUT_BYTES = kEpiWarps * WG_OUT_BUFS * WG_OUT_TILE;
+constexpr uint32_t WG_OUT_BYTES = kWgEpiWarps * WG_OUT_BUFS * WG_OUT_TILE;
 constexpr int kMats = 3;   // dW1, dW3, dW2
 
 struct WgParams {
@@ -939,7 +943,7 @@ __device__ __forceinline__ WUnit wg_decode(const WgParams& p, int u,
   return x;
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kWgThreads, 1)
     wgrad_gemm_kernel(const __grid_constant__ WgParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -968,7 +972,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&tfull[i]), 1);
-      mbar_init(smem_u32(&tempty[i]), 32 * kEpiWarps);
+      mbar_init(smem_u32(&tempty[i]), 32 * kWgEpiWarps);
     }
     mbar_init(smem_u32(drain), 1);
     misc[1] = 0;
@@ -1143,30 +1147,35 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp >= kEpiWarp0) {
     // ------------------------------------------------------- epilogue
-    // Each warp owns 32 rows (its TMEM lane quadrant): per 32 columns it
-    // writes its rows into a swizzled 4 KB staging tile and one lane
-    // issues the TMA store (or reduce-add) of the tile; four tiles rotate,
-    // and a tile is rewritten only after its store has read it (at most
-    // three stores of the warp still reading).
+    // Each warp owns 32 rows (its TMEM lane quadrant) and half of a unit's
+    // columns: per 32 columns it writes its rows into a swizzled 4 KB
+    // staging tile and one lane issues the TMA store (or reduce-add) of the
+    // tile; two tiles alternate, so a tile is rewritten only after its
+    // store has read it.
     const int q = warp & 3;
+    const int hw = (warp - kEpiWarp0) >> 2;  // which half of the columns
     const int r = q * 32 + lane;
     uint32_t tph = 0;
     int slot = 0;
     int ob = 0;
-    uint8_t* stage_base = sO + q * WG_OUT_BUFS * WG_OUT_TILE;
+    uint8_t* stage_base =
+        sO + (warp - kEpiWarp0) * WG_OUT_BUFS * WG_OUT_TILE;
     // the gradients stream out once: their lines go first when L2 needs
     // room, so the operand rows (kept with evict_last) stay resident
     const uint64_t pol_out = policy_evict_first();
     for (int u = blockIdx.x; u < total; u += gridDim.x) {
       const WUnit w = wg_decode(p, u, upre, srow0, srows, NP);
       const bool sh = w.seg == 0;
+      const int nch = (w.nt + 31) / 32;
+      const int c_lo = hw ? (nch + 1) / 2 : 0;
+      const int c_hi = hw ? nch : (nch + 1) / 2;
       if (w.rows == 0) {
         // an expert with no tokens has a zero gradient
         const int row = w.m0 + r;
         if (!p.accumulate && row < w.M) {
           float* out = p.out_r[w.mat] + (size_t)(w.seg - 1) * w.M * w.N;
           float* orow = out + (size_t)row * w.N + w.n0;
-          for (int c = 0; c < w.nt; c += 4)
+          for (int c = 32 * c_lo; c < min(w.nt, 32 * c_hi); c += 4)
             *reinterpret_cast<float4*>(orow + c) = make_float4(0, 0, 0, 0);
         }
         continue;
@@ -1183,14 +1192,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const CUtensorMap* om = sh ? &p.o_s[w.mat] : &p.o_r[w.mat];
       const int mrow = w.m0 + q * 32;        // first row of this warp
       const int mat_idx = sh ? 0 : w.seg - 1;
-      for (int c = 0; 32 * c < w.nt; ++c) {
+      for (int c = c_lo; c < c_hi; ++c) {
         uint32_t v[32];
         tmem_ld16(ta + 32 * c, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
         tmem_ld16(ta + 32 * c + 16,
                   *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
         tmem_ld_wait();
         uint8_t* tile = stage_base + ob * WG_OUT_TILE;
-        if (lane == 0) bulk_wait_read_le3();
+        if (lane == 0) bulk_wait_read_le1();
         __syncwarp();
         // row `lane`: 16-byte chunk k at position k ^ (lane & 7) (the
         // 128-byte swizzle of the tensor map)
@@ -1414,7 +1423,7 @@ int launch_expert_backward(const BwdArgs& a, cudaStream_t s) {
                              static_cast<int>(smem)) != cudaSuccess)
       return MOE_ERR_CUDA;
     mark(4);
-    wgrad_gemm_kernel<<<gemm_ctas(), kThreads, smem, s>>>(wp);
+    wgrad_gemm_kernel<<<gemm_ctas(), kWgThreads, smem, s>>>(wp);
     if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
   }
 

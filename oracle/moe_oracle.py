@@ -217,8 +217,10 @@ def permutation(idx: np.ndarray, E: int):
 # Expert FFN and the layer output (§1.1, eq. 12).
 # --------------------------------------------------------------------------
 def silu(v: np.ndarray) -> np.ndarray:
-    """silu(v) = v / (1 + e^{-v}) in fp64."""
-    return v / (1.0 + np.exp(-v))
+    """silu(v) = v / (1 + e^{-v}) in fp64.  For v below about -709, e^{-v}
+    overflows to inf and the quotient is the correct limit -0."""
+    with np.errstate(over="ignore"):
+        return v / (1.0 + np.exp(-v))
 
 
 def swiglu_ffn(a: np.ndarray, w1: np.ndarray, w3: np.ndarray,
