@@ -132,3 +132,44 @@ def test_fp8_expert_ffn_wait_runs_out_then_context_recovers():
     code, yp, ys = run()
     assert code == 0
     assert torch.equal(yp, yp_ref) and torch.equal(ys, ys_ref)
+
+
+def test_expert_backward_waits_run_out_then_context_recovers():
+    """The backward's four tensor-core GEMMs (recompute, both dgrads, the
+    weight gradients) under the 1 ns bound: the call reports
+    MOE_ERR_TIMEOUT, twice in a row; with the default bound restored the
+    same context reproduces every output bit for bit."""
+    cfg = inputs.custom_config("timeout_bwd", 963, T=96, H=256, E=8,
+                               n_group=4, topk_group=2, topk=2, I=128,
+                               I_shared=128, router_sigma=0.05)
+    d = ops.dims_of(cfg)
+    w = inputs.layer_inputs(cfg)
+    z = O.router_logits(inputs.bf16_bits_to_f32(w["x"]), w["w_router"])
+    r = O.route(z, w["bias"], cfg.n_group, cfg.topk_group, cfg.topk)
+    W = ops.Weights(dev(w["w_router"]), dev(w["w1"]), dev(w["w3"]),
+                    dev(w["w2"]), dev(w["ws1"]), dev(w["ws3"]), dev(w["ws2"]))
+    dout = inputs.normal_bf16(12345, (cfg.T, cfg.H), 1.0)
+    args = (dev(w["x"]), dev(dout), dev(r["idx"]), dev(r["gate"]))
+
+    def run():
+        dx = torch.zeros((cfg.T, cfg.H), dtype=torch.int16, device="cuda")
+        dg = torch.zeros((cfg.T, cfg.topk), dtype=torch.float32,
+                         device="cuda")
+        g = ops.WeightGrads.empty(d)
+        ws = ops.workspace(d, ops.MOE_WS_EXPERT_BWD)
+        ops.moe_expert_backward(d, W, *args, dx, dg, g, ws)
+        code = ops.moe_get_device_error(ws)
+        return code, [t.cpu().numpy() for t in [dx, dg] + g.tensors()]
+    code, ref = run()
+    assert code == 0
+    try:
+        ops.moe_set_wait_timeout_ns(1)
+        for _ in range(2):
+            code, _ = run()
+            assert code == TIMEOUT
+    finally:
+        ops.moe_set_wait_timeout_ns(0)
+    code, again = run()
+    assert code == 0
+    for a, b in zip(ref, again):
+        assert np.array_equal(a.view(np.uint8), b.view(np.uint8))
