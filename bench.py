@@ -543,7 +543,7 @@ def run_route_gpu(args, rank, world, local_rank):
             "achieved": round(route_bytes / (kt[0] / 1e3) / 1e9, 1),
             "peak": hbm, "unit": "GB/s"}
     roof["frac"] = round(roof["achieved"] / hbm, 4)
-    roof["traffic"] = None
+    roof["traffic"] = ncu_traffic("route", cfg.name)
     roof["kernel"] = ("moe_route call (route_kernel + count scan): "
                       "logits -> idx, gates, counts")
     roof["algorithmic_bytes"] = int(route_bytes)
