@@ -25,7 +25,9 @@ What it computes, and where the pages say so (page titles as cited):
   alpha * sum_i f_i P_i (alpha = 1e-4), and its gradient to the logits
   together with the gates' (the routing backward).
 * same page §2: FP8 (E4M3) with one scale per 1 x 128 activation tile and
-  128 x 128 weight block, and the expert FFN on those values.
+  128 x 128 weight block, and the expert FFN on those values; the same
+  groups with power-of-two scales (the microscaling form the page points
+  to for Blackwell's tensor cores).
 * same page §5.1: redundant copies of high-load experts from the load
   statistics.
 
@@ -44,8 +46,9 @@ Parity status: every function here is pinned by a ``-m "not gpu"`` test
 (closed forms, brute force on tiny inputs, invariants the pages state,
 finite differences, and textbook reductions) -- see tests/test_oracle_pins.py,
 test_oracle_margin_pins.py, test_oracle_balance_pins.py,
-test_oracle_fp8_pins.py, test_oracle_backward_pins.py,
-test_oracle_expert_backward_pins.py and test_planner.py.
+test_oracle_fp8_pins.py, test_oracle_mx_pins.py,
+test_oracle_backward_pins.py, test_oracle_expert_backward_pins.py and
+test_planner.py.
 """
 from __future__ import annotations
 
@@ -443,23 +446,98 @@ def dequantize(q: np.ndarray, s: np.ndarray, rows_per_scale: int):
     return v * sc
 
 
-def fp8_swiglu_ffn(a_q, a_s, w1, w3, w2):
+def fp8_swiglu_ffn(a_q, a_s, w1, w3, w2, requant=None):
     """One expert on FP8 inputs (§2 mixed precision on §1.1's SwiGLU):
     a_q / a_s the 1x128-quantized token rows; w1, w3, w2 each a
     (codes, scales) pair of 128x128-quantized weights.
       p, q = A W1^T, A W3^T on the dequantized values (fp64, exact
              products: the pages' full-precision accumulation)
       m    = silu(p) * q, rounded to fp32, then 1x128-quantized
-             (READING R21: the down projection's input is FP8 too)
+             (READING R21: the down projection's input is FP8 too) by
+             `requant` (quantize_1x128 unless given: the power-of-two
+             variant passes quantize_1x128_pow2)
       y    = M W2^T on the dequantized values (fp64)
     Returns y (fp64) and the intermediate (codes, scales)."""
+    requant = quantize_1x128 if requant is None else requant
     A = dequantize(a_q, a_s, 1)
     p = A @ dequantize(*w1, 128).T
     q = A @ dequantize(*w3, 128).T
     m = (silu(p) * q).astype(F32)
-    m_q, m_s = quantize_1x128(m)
+    m_q, m_s = requant(m)
     y = dequantize(m_q, m_s, 1) @ dequantize(*w2, 128).T
     return y, (m_q, m_s)
+
+
+# --------------------------------------------------------------------------
+# The same groups with power-of-two scales.  The pages (same page, §2) liken
+# the fine-grained groups to the microscaling formats whose scaling
+# Blackwell's tensor cores apply natively; in those formats a group's scale
+# is a power of two, stored as an 8-bit biased exponent (UE8M0).  READING
+# R22: with power-of-two scales the group scale is the least power of two
+# that keeps the group's largest magnitude within 448, i.e. 2^e with e the
+# least integer such that 448 * 2^e >= amax (clamped below at -127, the
+# smallest UE8M0 exponent; an all-zero group gets e = 0), and every code is
+# the E4M3 rounding of the exact quotient x / 2^e.
+# --------------------------------------------------------------------------
+UE8M0_BIAS = 127
+
+
+def group_exponent_pow2(amax: np.ndarray) -> np.ndarray:
+    """e = min{integer e : 448 * 2^e >= amax}, at least -127; 0 when
+    amax == 0.  From the definition: a floating estimate of log2(amax/448),
+    then exact corrections (448 * 2^e is exact in fp64)."""
+    a = np.asarray(amax, F32).astype(np.float64)
+    pos = a > 0
+    est = np.where(pos, np.ceil(np.log2(np.where(pos, a, 1.0) / E4M3_MAX)),
+                   0.0).astype(np.int64)
+    for _ in range(2):
+        est = np.where(pos & (np.ldexp(E4M3_MAX, est) < a), est + 1, est)
+        est = np.where(pos & (np.ldexp(E4M3_MAX, est - 1) >= a), est - 1,
+                       est)
+    assert np.all(~pos | (np.ldexp(E4M3_MAX, est) >= a))
+    assert np.all(~pos | (np.ldexp(E4M3_MAX, est - 1) < a))
+    return np.where(pos, np.maximum(est, -UE8M0_BIAS), 0)
+
+
+def ue8m0_encode(e: np.ndarray) -> np.ndarray:
+    """The scale 2^e as its UE8M0 byte e + 127."""
+    return (np.asarray(e, np.int64) + UE8M0_BIAS).astype(np.uint8)
+
+
+def ue8m0_decode(b: np.ndarray) -> np.ndarray:
+    """The scale of a UE8M0 byte: 2^(b - 127) (fp32; byte 255 is not a
+    scale this quantizer writes)."""
+    return np.ldexp(1.0, np.asarray(b, np.int64) - UE8M0_BIAS).astype(F32)
+
+
+def _codes_pow2(t: np.ndarray, e: np.ndarray) -> np.ndarray:
+    # x / 2^e is exact in fp64; rounded to fp32 it changes only below
+    # 2^-126, where the E4M3 code is 0 either way
+    return e4m3_encode(np.ldexp(t.astype(np.float64), -e).astype(F32))
+
+
+def quantize_1x128_pow2(x: np.ndarray):
+    """quantize_1x128 with power-of-two scales: codes [R, C] uint8 and
+    scales [R, C/128] fp32 (each 2^e, e from group_exponent_pow2)."""
+    x = np.asarray(x, F32)
+    R, C = x.shape
+    assert C % 128 == 0
+    t = x.reshape(R, C // 128, 128)
+    e = group_exponent_pow2(np.abs(t).max(axis=2))
+    q = _codes_pow2(t, e[:, :, None])
+    return q.reshape(R, C), ue8m0_decode(ue8m0_encode(e))
+
+
+def quantize_128x128_pow2(w: np.ndarray):
+    """quantize_128x128 with power-of-two scales: codes [R, C] uint8 and
+    scales [R/128, C/128] fp32 (each 2^e)."""
+    w = np.asarray(w, F32)
+    R, C = w.shape
+    assert R % 128 == 0 and C % 128 == 0
+    b = w.reshape(R // 128, 128, C // 128, 128)
+    e = group_exponent_pow2(np.abs(b).max(axis=(1, 3)))
+    q = _codes_pow2(b, e[:, None, :, None])
+    return q.reshape(R, C), ue8m0_decode(ue8m0_encode(e))
 
 
 # --------------------------------------------------------------------------
