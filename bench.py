@@ -223,6 +223,60 @@ def config_json(cfg, n_gpus):
                   "per step; 4 rotating activation batches"}
 
 
+def e2e_loop(step, xs, T, H, steps, stream, barrier=lambda: None):
+    """End to end with host buffers: every step uploads its x [T, H] bf16
+    from pinned host memory and downloads its output [T, H] bf16 into
+    pinned host memory.  The copies run on their own streams with
+    double-buffered device x / out, so that step i+1's upload and step i's
+    download overlap step i's compute.  step(x_dev, out_dev) enqueues one
+    layer on `stream`.  Returns the elapsed ms of `steps` steps."""
+    import torch
+    NB = len(xs)
+    xh = [torch.empty((T, H), dtype=torch.int16).pin_memory()
+          for _ in range(NB)]
+    for i in range(NB):
+        xh[i].copy_(xs[i].cpu())
+    oh = [torch.empty((T, H), dtype=torch.int16).pin_memory()
+          for _ in range(2)]
+    xd = [torch.empty((T, H), dtype=torch.int16, device="cuda")
+          for _ in range(2)]
+    od = [torch.empty((T, H), dtype=torch.int16, device="cuda")
+          for _ in range(2)]
+    up_s, dn_s = torch.cuda.Stream(), torch.cuda.Stream()
+    ev = lambda: torch.cuda.Event()  # noqa: E731
+    h2d_done = [ev() for _ in range(2)]
+    comp_done = [ev() for _ in range(2)]
+    d2h_done = [ev() for _ in range(2)]
+    for e in comp_done + d2h_done:
+        e.record(stream)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    barrier()
+    e0.record(stream)
+    up_s.wait_event(e0)
+    dn_s.wait_event(e0)
+    for i in range(steps):
+        b = i % 2
+        up_s.wait_event(comp_done[b])          # xd[b] no longer read
+        with torch.cuda.stream(up_s):
+            xd[b].copy_(xh[i % NB], non_blocking=True)
+        h2d_done[b].record(up_s)
+        stream.wait_event(h2d_done[b])
+        stream.wait_event(d2h_done[b])         # od[b] already downloaded
+        step(xd[b], od[b])
+        comp_done[b].record(stream)
+        dn_s.wait_event(comp_done[b])
+        with torch.cuda.stream(dn_s):
+            oh[b].copy_(od[b], non_blocking=True)
+        d2h_done[b].record(dn_s)
+    stream.wait_event(d2h_done[(steps - 1) % 2])
+    stream.wait_event(d2h_done[steps % 2])
+    e1.record(stream)
+    barrier()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1)
+
+
 def run_gpu(args, rank, world, local_rank):
     import torch
     from deepseekmoe_routing_expert_moe_b300 import inputs, ops
@@ -358,45 +412,10 @@ def run_gpu(args, rank, world, local_rank):
     #      its x from pinned host memory and its output back; the copies run
     #      on their own streams (double-buffered device x/out) so that step
     #      i+1's upload and step i's download overlap step i's compute
-    xh = [torch.empty((T, H), dtype=torch.int16).pin_memory() for _ in range(NB)]
-    for i in range(NB):
-        xh[i].copy_(xs[i].cpu())
-    oh = [torch.empty((T, H), dtype=torch.int16).pin_memory() for _ in range(2)]
-    xd = [torch.empty((T, H), dtype=torch.int16, device="cuda") for _ in range(2)]
-    od = [torch.empty((T, H), dtype=torch.int16, device="cuda") for _ in range(2)]
-    up_s, dn_s = torch.cuda.Stream(), torch.cuda.Stream()
-    ev = lambda: torch.cuda.Event()  # noqa: E731
-    h2d_done = [ev() for _ in range(2)]
-    comp_done = [ev() for _ in range(2)]
-    d2h_done = [ev() for _ in range(2)]
-    for e in comp_done + d2h_done:
-        e.record(stream)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    barrier()
-    e0.record(stream)
-    up_s.wait_event(e0)
-    dn_s.wait_event(e0)
-    for i in range(args.steps):
-        b = i % 2
-        up_s.wait_event(comp_done[b])          # xd[b] no longer read
-        with torch.cuda.stream(up_s):
-            xd[b].copy_(xh[i % NB], non_blocking=True)
-        h2d_done[b].record(up_s)
-        stream.wait_event(h2d_done[b])
-        stream.wait_event(d2h_done[b])         # od[b] already downloaded
-        ops.moe_forward(d, W, xd[b], bias, od[b], ws, update_bias=True,
-                        stream=stream)
-        comp_done[b].record(stream)
-        dn_s.wait_event(comp_done[b])
-        with torch.cuda.stream(dn_s):
-            oh[b].copy_(od[b], non_blocking=True)
-        d2h_done[b].record(dn_s)
-    stream.wait_event(d2h_done[(args.steps - 1) % 2])
-    stream.wait_event(d2h_done[args.steps % 2])
-    e1.record(stream)
-    barrier()
-    e2e_ms = e0.elapsed_time(e1)
+    e2e_ms = e2e_loop(
+        lambda x, o: ops.moe_forward(d, W, x, bias, o, ws, update_bias=True,
+                                     stream=stream),
+        xs, T, H, args.steps, stream, barrier)
     if world > 1:
         import torch.distributed as dist
         t = torch.tensor([e2e_ms], dtype=torch.float64, device="cuda")
@@ -737,25 +756,41 @@ def run_balance_gpu(args, rank, world, local_rank):
     return res
 
 
+FP8_WORKLOADS = ("decode_v3_fp8", "prefill_v3_fp8", "decode_v3_e32_fp8",
+                 "prefill_v3_e32_fp8", "decode_v3_mx", "prefill_v3_mx",
+                 "prefill_v3_e32_mx")
+
+
+def fp8_kind(workload):
+    """("fp8" | "mx", base configuration) of an FP8 workload name: _fp8 is
+    the fp32-scale path (CUDA-core promotion), _mx the power-of-two-scale
+    path (scales applied by the tensor cores)."""
+    kind = "mx" if workload.endswith("_mx") else "fp8"
+    return kind, workload[:-len("_" + kind)]
+
+
 def run_fp8_gpu(args, rank, world, local_rank):
-    """A V3 layer with FP8 experts -- decode_v3_fp8 (T=128) or
-    prefill_v3_fp8 (T=4096): per step, through the public calls, router
-    logits -> moe_route -> moe_permute (indices) -> moe_permute_fp8
-    (quantise-on-permute) -> moe_expert_ffn_fp8 -> moe_combine ->
-    moe_bias_update.  The weights are quantized to E4M3 (128 x 128 block
-    scales) once, before timing, as a deployment would store them.  4
-    rotating token batches; the E4M3 weights (11.3 GB at 256 experts, 1.4 GB
-    for the 32-expert profiling stand-in) exceed L2."""
+    """A V3 layer with FP8 experts -- decode (T=128) or prefill (T=4096):
+    per step, through the public calls, router logits -> moe_route ->
+    moe_permute (indices) -> quantise-on-permute (moe_permute_fp8 |
+    moe_permute_mx) -> FP8 experts (moe_expert_ffn_fp8 | moe_expert_ffn_mx)
+    -> moe_combine -> moe_bias_update.  The weights are quantized to E4M3
+    (128 x 128 block scales: fp32, or power-of-two UE8M0 bytes) once,
+    before timing, as a deployment would store them.  4 rotating token
+    batches; the E4M3 weights (11.3 GB at 256 experts, 1.4 GB for the
+    32-expert profiling stand-in) exceed L2."""
     import torch
     from deepseekmoe_routing_expert_moe_b300 import inputs, ops
     torch.cuda.set_device(local_rank)
-    base = args.workload[:-len("_fp8")]
+    kind, base = fp8_kind(args.workload)
+    mx = kind == "mx"
     cfg = inputs.CONFIGS[base]
     d = ops.dims_of(cfg)
     T, H, E, K, I, Is = cfg.T, cfg.H, cfg.E, cfg.topk, cfg.I, cfg.I_shared
     w1, w3, w2 = inputs.device_expert_weights(cfg, "cuda")
     ws1, ws3, ws2 = inputs.shared_weights(cfg, "cuda")
-    Wq = ops.WeightsFp8.quantize(w1, w3, w2, ws1, ws3, ws2)
+    Wq = (ops.WeightsMx if mx else ops.WeightsFp8).quantize(
+        w1, w3, w2, ws1, ws3, ws2)
     del w1, w3, w2
     torch.cuda.empty_cache()
     wr = torch.from_numpy(inputs.router_weight(cfg)).cuda()
@@ -770,10 +805,13 @@ def run_fp8_gpu(args, rank, world, local_rank):
     offsets = torch.empty(E + 1, dtype=torch.int32, device="cuda")
     dest = torch.empty((T, K), dtype=torch.int32, device="cuda")
     src_row = torch.empty(T * K, dtype=torch.int32, device="cuda")
+    sdt = torch.uint8 if mx else torch.float32
     xq = torch.empty((T, H), dtype=torch.uint8, device="cuda")
-    xsc = torch.empty((T, H // 128), dtype=torch.float32, device="cuda")
+    xsc = torch.empty((T, H // 128), dtype=sdt, device="cuda")
     xpq = torch.empty((T * K, H), dtype=torch.uint8, device="cuda")
-    xps = torch.empty((T * K, H // 128), dtype=torch.float32, device="cuda")
+    xps = torch.empty((T * K, H // 128), dtype=sdt, device="cuda")
+    permute_q = ops.moe_permute_mx if mx else ops.moe_permute_fp8
+    ffn_q = ops.moe_expert_ffn_mx if mx else ops.moe_expert_ffn_fp8
     yp = torch.empty((T * K, H), dtype=torch.int16, device="cuda")
     ys = torch.empty((T, H), dtype=torch.int16, device="cuda")
     out = torch.empty((T, H), dtype=torch.int16, device="cuda")
@@ -784,9 +822,9 @@ def run_fp8_gpu(args, rank, world, local_rank):
         ops.moe_router_logits(d, x, wr, z, ws)
         ops.moe_route(d, z, bias, idx, gate, counts, ws)
         ops.moe_permute(d, None, idx, offsets, dest, src_row, None, ws)
-        ops.moe_permute_fp8(d, x, dest, xq, xsc, xpq, xps, ws)
+        permute_q(d, x, dest, xq, xsc, xpq, xps, ws)
         if ev: ev[0].record(stream)
-        ops.moe_expert_ffn_fp8(d, Wq, xpq, xps, xq, xsc, offsets, yp, ys, ws)
+        ffn_q(d, Wq, xpq, xps, xq, xsc, offsets, yp, ys, ws)
         if ev: ev[1].record(stream)
         ops.moe_combine(d, x, ys, yp, dest, gate, o)
         ops.moe_bias_update(d, counts, bias)
@@ -815,57 +853,50 @@ def run_fp8_gpu(args, rank, world, local_rank):
     t_ffn = float(np.mean([e[0].elapsed_time(e[1]) for e in evs])) / 1e3
     c = counts.cpu().numpy().astype(np.int64)
     touched = int((c > 0).sum())
-    nkh, nki, nks = H // 128, I // 128, Is // 128
+    nkh = H // 128
+    sb = 1 if mx else 4                                         # scale bytes
     ffn_bytes = (touched * 3 * I * H + 3 * Is * H +             # E4M3 weights
-                 (touched * 3 * (I // 128) * nkh) * 4 +         # their scales
-                 3 * (Is // 128) * nkh * 4 +
-                 (T * K + T) * H * (1 + 4 / 128) +              # token codes
-                 2 * (T * K * I + T * Is) * (1 + 4 / 128) +     # m out + in
+                 (touched * 3 * (I // 128) * nkh) * sb +        # their scales
+                 3 * (Is // 128) * nkh * sb +
+                 (T * K + T) * H * (1 + sb / 128) +             # token codes
+                 2 * (T * K * I + T * Is) * (1 + sb / 128) +    # m out + in
                  (T * K + T) * H * 2)                           # y (bf16)
     pk, pk_src = peaks()
     hbm = float(pk["hbm_gbs"])
     roof = {"bound": "hbm", "achieved": round(ffn_bytes / t_ffn / 1e9, 1),
             "peak": hbm, "unit": "GB/s"}
     roof["frac"] = round(roof["achieved"] / hbm, 4)
-    roof["traffic"] = ncu_traffic("ffn_fp8", args.workload)
-    roof["kernel"] = ("moe_expert_ffn_fp8 call (fp8_gemm_kernel up + "
-                      "down, E4M3 weights streamed once)")
+    roof["traffic"] = ncu_traffic("ffn_" + kind, args.workload)
+    roof["kernel"] = (("moe_expert_ffn_mx call (mx_gemm_kernel up + down, "
+                       "block-scaled tcgen05 MMAs" if mx else
+                       "moe_expert_ffn_fp8 call (fp8_gemm_kernel up + down")
+                      + ", E4M3 weights streamed once)")
     roof["algorithmic_bytes"] = int(ffn_bytes)
     roof["ffn_ms"] = round(t_ffn * 1e3, 4)
     roof["peak_source"] = f"{pk_src} (MEASURED_PEAKS.json)"
     # end to end: x uploaded from pinned memory, out read back, every step
-    xh = [torch.empty((T, H), dtype=torch.int16).pin_memory()
-          for _ in range(2)]
-    for i in range(2):
-        xh[i].copy_(xs[i].cpu())
-    oh = torch.empty((T, H), dtype=torch.int16).pin_memory()
-    xd = torch.empty((T, H), dtype=torch.int16, device="cuda")
+    # (copies overlapped with the neighbouring steps' compute)
     torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for i in range(args.steps):
-        xd.copy_(xh[i % 2], non_blocking=True)
-        step(xd, out)
-        oh.copy_(out, non_blocking=True)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
+    e2e_ms = e2e_loop(step, xs, T, H, args.steps, stream)
     assert ops.moe_get_device_error(ws) == 0
     return {
         "metric": f"tokens/s per V3-shaped MoE {base.split('_')[0]} layer "
-                  "on 1 B300 with FP8 (E4M3) experts; % of HBM roofline",
+                  "on 1 B300 with FP8 (E4M3) experts"
+                  + (" (power-of-two scales)" if mx else "")
+                  + "; % of HBM roofline",
         "value": round(T * args.steps / (ms / 1e3), 1), "unit": "tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(ms / args.steps, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
-        "dtype": "e4m3 experts (1x128 / 128x128 fp32 scales), bf16 "
-                 "activations elsewhere, fp32 routing",
+        "dtype": "e4m3 experts (1x128 / 128x128 "
+                 + ("UE8M0 power-of-two" if mx else "fp32")
+                 + " scales), bf16 activations elsewhere, fp32 routing",
         "data": f"synthetic, seeded (the {base} inputs; weights "
                 "quantized from the bf16 ones before timing)",
         "config": {"workload": f"{args.workload}: V3 layer T={T}, "
                                f"H={H}, E={E}+1 shared, I={I}, top-{K}, "
-                               "FP8 experts",
+                               "FP8 experts"
+                               + (", power-of-two scales" if mx else ""),
                    "T": T, "H": H, "E": E, "topk": K, "I": I,
                    "l2": f"{(E * 3 * I * H + 3 * Is * H) / 1e9:.1f} GB of "
                          "E4M3 weights streamed per step > L2"},
@@ -884,31 +915,38 @@ def run_fp8_gpu(args, rank, world, local_rank):
 
 
 def run_decode_fp8_reference(args):
-    """Oracle arm of decode_v3_fp8 / prefill_v3_fp8: per step one token of
-    the batch through the oracle's routing and FP8 experts (its 8 routed experts and
-    the shared one); the oracle quantizes those experts' weights once
-    before timing, as the GPU arm does."""
+    """Oracle arm of the FP8 workloads: per step one token of the batch
+    through the oracle's routing and FP8 experts (its 8 routed experts and
+    the shared one; fp32 or power-of-two scales as the workload's GPU arm);
+    the oracle quantizes those experts' weights once before timing, as the
+    GPU arm does."""
     from deepseekmoe_routing_expert_moe_b300 import inputs
     from oracle import moe_oracle as O
-    cfg = inputs.CONFIGS[args.workload[:-len("_fp8")]]
+    kind, base = fp8_kind(args.workload)
+    cfg = inputs.CONFIGS[base]
+    if kind == "mx":
+        q_w, q_a = O.quantize_128x128_pow2, O.quantize_1x128_pow2
+    else:
+        q_w, q_a = O.quantize_128x128, O.quantize_1x128
     f32 = inputs.bf16_bits_to_f32
     x = f32(inputs.x_tokens(cfg))[:1]
     wr = inputs.router_weight(cfg)
     b = inputs.bias(cfg)
     idx = O.route(O.router_logits(x, wr), b, cfg.n_group, cfg.topk_group,
                   cfg.topk)["idx"][0]
-    qw = {int(e): [O.quantize_128x128(f32(m))
-                   for m in inputs.expert_weights(cfg, int(e))] for e in idx}
-    qs = [O.quantize_128x128(f32(m)) for m in inputs.shared_weights(cfg)]
+    qw = {int(e): [q_w(f32(m)) for m in inputs.expert_weights(cfg, int(e))]
+          for e in idx}
+    qs = [q_w(f32(m)) for m in inputs.shared_weights(cfg)]
 
     def one():
         z = O.router_logits(x, wr)
         r = O.route(z, b, cfg.n_group, cfg.topk_group, cfg.topk)
-        aq, as_ = O.quantize_1x128(x)
-        y = x.astype(np.float64) + O.fp8_swiglu_ffn(aq, as_, *qs)[0]
+        aq, as_ = q_a(x)
+        y = x.astype(np.float64) + O.fp8_swiglu_ffn(aq, as_, *qs,
+                                                    requant=q_a)[0]
         for k, e in enumerate(r["idx"][0]):
             y = y + float(r["gate"][0, k]) * O.fp8_swiglu_ffn(
-                aq, as_, *qw[int(e)])[0]
+                aq, as_, *qw[int(e)], requant=q_a)[0]
         return y
 
     for _ in range(args.warmup):
@@ -918,18 +956,20 @@ def run_decode_fp8_reference(args):
         one()
     tot = time.perf_counter() - t0
     v = args.steps / tot
-    sample = ("one decode token per step through the numpy oracle: logits, "
+    sample = ("one token per step through the numpy oracle: logits, "
               "routing, 1x128 quantization, its 8 FP8 experts + the shared "
               "one (weights quantized before timing)")
     return {
-        "metric": "tokens/s per V3-shaped MoE decode layer with FP8 experts; "
-                  "oracle on the host cores",
+        "metric": f"tokens/s per V3-shaped MoE {base.split('_')[0]} layer "
+                  "with FP8 experts"
+                  + (" (power-of-two scales)" if kind == "mx" else "")
+                  + "; oracle on the host cores",
         "value": round(v, 4), "unit": "tokens/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(tot / args.steps * 1e3, 2),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64 on e4m3 values", "data": "synthetic, seeded",
-        "config": {"workload": "decode_v3_fp8: V3 decode layer, FP8 experts"},
+        "config": {"workload": f"{args.workload}: V3 layer, FP8 experts"},
         "impl": "reference",
         "cpu_baseline": {"value": round(v, 4), "unit": "tokens/s",
                          "cores": blas_threads(), "kind": "oracle",
@@ -1383,8 +1423,7 @@ def run_reference(args):
     from deepseekmoe_routing_expert_moe_b300 import inputs
     if args.workload == "balance_v3":
         return run_balance_reference(args)
-    if args.workload in ("decode_v3_fp8", "prefill_v3_fp8",
-                         "decode_v3_e32_fp8", "prefill_v3_e32_fp8"):
+    if args.workload in FP8_WORKLOADS:
         return run_decode_fp8_reference(args)
     if args.workload == "route_backward_v3":
         return run_backward_reference(args)
@@ -1425,8 +1464,7 @@ def main():
     ap.add_argument("--workload", default="prefill_v3",
                     choices=("prefill_v3", "decode_v3", "skewed_v3",
                              "route_v3", "prefill_v3_e32", "balance_v3",
-                             "decode_v3_fp8", "prefill_v3_fp8",
-                             "decode_v3_e32_fp8", "prefill_v3_e32_fp8",
+                             *FP8_WORKLOADS,
                              "route_backward_v3",
                              "expert_backward_v3", "expert_backward_v3_e16"))
     ap.add_argument("--cpu-sample-tokens", type=int, default=4)
@@ -1454,8 +1492,7 @@ def main():
         res = run_route_gpu(args, rank, world, local_rank)
     elif args.workload == "balance_v3":
         res = run_balance_gpu(args, rank, world, local_rank)
-    elif args.workload in ("decode_v3_fp8", "prefill_v3_fp8",
-                           "decode_v3_e32_fp8", "prefill_v3_e32_fp8"):
+    elif args.workload in FP8_WORKLOADS:
         res = run_fp8_gpu(args, rank, world, local_rank)
     elif args.workload == "route_backward_v3":
         res = run_backward_gpu(args, rank, world, local_rank)

@@ -204,6 +204,26 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
   return p;
 }
 
+// ------------------------------------------------- power-of-two scales
+// Exponent e of the least power of two with 448 * 2^e >= amax (amax >= 0,
+// finite), at least -127 (the smallest UE8M0 exponent); 0 for amax = 0.
+// For a normal amax = 1.m * 2^E: amax / 448 = (1.m / 1.75) * 2^(E - 8), and
+// 1.m / 1.75 lies in [4/7, 8/7), so e = E - 8 when 1.m <= 1.75 (mantissa
+// field <= 0x600000) and E - 7 otherwise.  A subnormal amax needs an e
+// below -134, clamped to -127.
+__device__ __forceinline__ int ue8m0_exponent(float amax) {
+  const uint32_t b = __float_as_uint(amax);
+  if (b == 0u) return 0;
+  const int E = (int)(b >> 23) - 127;
+  if ((b >> 23) == 0u) return -127;
+  const int e = (b & 0x7FFFFFu) <= 0x600000u ? E - 8 : E - 7;
+  return e < -127 ? -127 : e;
+}
+// 2^-e as an fp32 (exact: e in [-127, 127] keeps it a normal number)
+__device__ __forceinline__ float pow2_neg(int e) {
+  return __uint_as_float((uint32_t)(127 - e) << 23);
+}
+
 // -------------------------------------------------------------- tcgen05
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
   asm volatile(

@@ -6,6 +6,11 @@
 //   code = E4M3(x / s), the fp32 quotient rounded to nearest even and
 //          saturated to +-448 (cvt.rn.satfinite)
 // so every code is decided from the same fp32 values as the CPU oracle's.
+// The power-of-two variant (the microscaling form the same section points
+// to for Blackwell's tensor cores) takes s = 2^e, e the least exponent with
+// 448 * 2^e >= amax, stores e + 127 as one byte (UE8M0) and codes
+// E4M3(x * 2^-e) -- an exact product, so the code is the E4M3 rounding of
+// the exact quotient.
 #include <cuda_fp8.h>
 
 #include <cstdint>
@@ -18,20 +23,42 @@ namespace {
 
 constexpr float kE4m3Max = 448.0f;
 
-__device__ __forceinline__ float group_scale(float amax) {
-  return amax > 0.0f ? __fdiv_rn(amax, kE4m3Max) : 1.0f;
-}
+// A group's scale, from its max |value|: the fp32 scale amax / 448 ...
+struct ScaleF32 {
+  using T = float;
+  float s;
+  __device__ explicit ScaleF32(float amax) {
+    s = amax > 0.0f ? __fdiv_rn(amax, kE4m3Max) : 1.0f;
+  }
+  __device__ uint32_t code(float v) const {
+    return (uint32_t)__nv_cvt_float_to_fp8(__fdiv_rn(v, s), __NV_SATFINITE,
+                                           __NV_E4M3);
+  }
+  __device__ T stored() const { return s; }
+};
 
-__device__ __forceinline__ uint32_t e4m3(float v, float s) {
-  return (uint32_t)__nv_cvt_float_to_fp8(__fdiv_rn(v, s), __NV_SATFINITE,
-                                         __NV_E4M3);
-}
+// ... or the power-of-two scale 2^e, stored as the byte e + 127
+struct ScaleE8 {
+  using T = uint8_t;
+  int e;
+  float inv;  // 2^-e
+  __device__ explicit ScaleE8(float amax) {
+    e = ue8m0_exponent(amax);
+    inv = pow2_neg(e);
+  }
+  __device__ uint32_t code(float v) const {
+    return (uint32_t)__nv_cvt_float_to_fp8(v * inv, __NV_SATFINITE,
+                                           __NV_E4M3);
+  }
+  __device__ T stored() const { return (uint8_t)(e + 127); }
+};
 
 // four codes, first value in the lowest byte (memory order)
+template <class S>
 __device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c,
-                                           float d, float s) {
-  return e4m3(a, s) | (e4m3(b, s) << 8) | (e4m3(c, s) << 16) |
-         (e4m3(d, s) << 24);
+                                           float d, const S& s) {
+  return s.code(a) | (s.code(b) << 8) | (s.code(c) << 16) |
+         (s.code(d) << 24);
 }
 
 // ------------------------------------------------------------------
@@ -41,12 +68,13 @@ __device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c,
 // ------------------------------------------------------------------
 constexpr int kRowsWarps = 8;
 
+template <class S>
 __global__ void __launch_bounds__(kRowsWarps * 32)
     quant_rows_kernel(const uint16_t* __restrict__ x, long long R, int C,
                       const int32_t* __restrict__ dest, int K, long long RK,
-                      uint8_t* __restrict__ q, float* __restrict__ s,
-                      uint8_t* __restrict__ qp, float* __restrict__ sp,
-                      DevStatus* st) {
+                      uint8_t* __restrict__ q, typename S::T* __restrict__ s,
+                      uint8_t* __restrict__ qp,
+                      typename S::T* __restrict__ sp, DevStatus* st) {
   const int lane = threadIdx.x & 31;
   const int tiles = C / 128;
   const long long g =
@@ -63,11 +91,11 @@ __global__ void __launch_bounds__(kRowsWarps * 32)
   // |v| bit patterns order like the values (non-negative floats)
   const float amax =
       __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(m)));
-  const float sc = group_scale(amax);
+  const S sc(amax);
   const uint32_t code = e4m3x4(v0, v1, v2, v3, sc);
   if (q != nullptr) {
     *reinterpret_cast<uint32_t*>(q + off) = code;
-    if (lane == 0) s[(size_t)r * tiles + tile] = sc;
+    if (lane == 0) s[(size_t)r * tiles + tile] = sc.stored();
   }
   if (dest != nullptr) {
     for (int k = 0; k < K; ++k) {
@@ -78,7 +106,7 @@ __global__ void __launch_bounds__(kRowsWarps * 32)
       }
       *reinterpret_cast<uint32_t*>(qp + (size_t)dr * C + (size_t)tile * 128 +
                                    lane * 4) = code;
-      if (lane == 0) sp[(size_t)dr * tiles + tile] = sc;
+      if (lane == 0) sp[(size_t)dr * tiles + tile] = sc.stored();
     }
   }
 }
@@ -88,9 +116,11 @@ __global__ void __launch_bounds__(kRowsWarps * 32)
 // {i/16 + 16 j : j < 8}, columns (i % 16) * 8 .. +8 of the block (64
 // values), so a warp reads two full 256-byte row segments per step.
 // ------------------------------------------------------------------
+template <class S>
 __global__ void __launch_bounds__(256)
     quant_blocks_kernel(const uint16_t* __restrict__ w, int C,
-                        uint8_t* __restrict__ q, float* __restrict__ s) {
+                        uint8_t* __restrict__ q,
+                        typename S::T* __restrict__ s) {
   __shared__ float wmax[8];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int bc = blockIdx.x, br = blockIdx.y, nbc = gridDim.x;
@@ -116,7 +146,7 @@ __global__ void __launch_bounds__(256)
   float amax = wmax[0];
 #pragma unroll
   for (int i = 1; i < 8; ++i) amax = fmaxf(amax, wmax[i]);
-  const float sc = group_scale(amax);
+  const S sc(amax);
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
     uint2 o;
@@ -124,7 +154,31 @@ __global__ void __launch_bounds__(256)
     o.y = e4m3x4(v[j][4], v[j][5], v[j][6], v[j][7], sc);
     *reinterpret_cast<uint2*>(q + (r0 + 16 * j) * C + c0) = o;
   }
-  if (tid == 0) s[(size_t)br * nbc + bc] = sc;
+  if (tid == 0) s[(size_t)br * nbc + bc] = sc.stored();
+}
+
+template <class S>
+cudaError_t quant_rows(const uint16_t* x, long long R, int C,
+                       const int32_t* dest, int K, uint8_t* q,
+                       typename S::T* s, uint8_t* qp, typename S::T* sp,
+                       DevStatus* st, cudaStream_t stream) {
+  const long long warps = R * (C / 128);
+  if (warps == 0) return cudaSuccess;
+  const long long blocks = (warps + kRowsWarps - 1) / kRowsWarps;
+  if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+  quant_rows_kernel<S><<<(unsigned)blocks, kRowsWarps * 32, 0, stream>>>(
+      x, R, C, dest, K, R * K, q, s, qp, sp, st);
+  return cudaGetLastError();
+}
+
+template <class S>
+cudaError_t quant_blocks(const uint16_t* w, long long R, int C, uint8_t* q,
+                         typename S::T* s, cudaStream_t stream) {
+  if (R == 0) return cudaSuccess;
+  if (R / 128 > 65535) return cudaErrorInvalidValue;
+  quant_blocks_kernel<S><<<dim3(C / 128, (unsigned)(R / 128)), 256, 0,
+                           stream>>>(w, C, q, s);
+  return cudaGetLastError();
 }
 
 }  // namespace
@@ -133,22 +187,25 @@ cudaError_t launch_quant_rows(const uint16_t* x, long long R, int C,
                               const int32_t* dest, int K, uint8_t* q,
                               float* s, uint8_t* qp, float* sp,
                               DevStatus* st, cudaStream_t stream) {
-  const long long warps = R * (C / 128);
-  if (warps == 0) return cudaSuccess;
-  const long long blocks = (warps + kRowsWarps - 1) / kRowsWarps;
-  if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
-  quant_rows_kernel<<<(unsigned)blocks, kRowsWarps * 32, 0, stream>>>(
-      x, R, C, dest, K, R * K, q, s, qp, sp, st);
-  return cudaGetLastError();
+  return quant_rows<ScaleF32>(x, R, C, dest, K, q, s, qp, sp, st, stream);
 }
 
 cudaError_t launch_quant_blocks(const uint16_t* w, long long R, int C,
                                 uint8_t* q, float* s, cudaStream_t stream) {
-  if (R == 0) return cudaSuccess;
-  if (R / 128 > 65535) return cudaErrorInvalidValue;
-  quant_blocks_kernel<<<dim3(C / 128, (unsigned)(R / 128)), 256, 0,
-                        stream>>>(w, C, q, s);
-  return cudaGetLastError();
+  return quant_blocks<ScaleF32>(w, R, C, q, s, stream);
+}
+
+cudaError_t launch_quant_rows_e8(const uint16_t* x, long long R, int C,
+                                 const int32_t* dest, int K, uint8_t* q,
+                                 uint8_t* s, uint8_t* qp, uint8_t* sp,
+                                 DevStatus* st, cudaStream_t stream) {
+  return quant_rows<ScaleE8>(x, R, C, dest, K, q, s, qp, sp, st, stream);
+}
+
+cudaError_t launch_quant_blocks_e8(const uint16_t* w, long long R, int C,
+                                   uint8_t* q, uint8_t* s,
+                                   cudaStream_t stream) {
+  return quant_blocks<ScaleE8>(w, R, C, q, s, stream);
 }
 
 }  // namespace moe

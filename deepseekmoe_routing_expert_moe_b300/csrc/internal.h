@@ -92,6 +92,14 @@ cudaError_t launch_quant_rows(const uint16_t* x, long long R, int C,
 // codes q [R, C], scales s [R/128, C/128]
 cudaError_t launch_quant_blocks(const uint16_t* w, long long R, int C,
                                 uint8_t* q, float* s, cudaStream_t stream);
+// the same with power-of-two scales, stored as UE8M0 bytes (e + 127)
+cudaError_t launch_quant_rows_e8(const uint16_t* x, long long R, int C,
+                                 const int32_t* dest, int K, uint8_t* q,
+                                 uint8_t* s, uint8_t* qp, uint8_t* sp,
+                                 DevStatus* st, cudaStream_t stream);
+cudaError_t launch_quant_blocks_e8(const uint16_t* w, long long R, int C,
+                                   uint8_t* q, uint8_t* s,
+                                   cudaStream_t stream);
 
 // ---- grouped_gemm.cu
 struct FfnArgs {
@@ -171,6 +179,28 @@ struct FfnFp8Args {
 // 1 when the FP8 kernels have a shape for these sizes
 int fp8_ffn_supported(int H, int I, int I_shared, int E);
 int launch_expert_ffn_fp8(const FfnFp8Args& a, cudaStream_t s);
+
+// ---- mx_gemm.cu
+// The FP8 expert FFNs with power-of-two (UE8M0) group scales applied by
+// the tensor cores' block scaling; same tensors as FfnFp8Args, scales as
+// UE8M0 bytes (2^(b - 127)).
+struct FfnMxArgs {
+  int T, H, E, topk, I, I_shared;
+  const uint8_t *xpq, *xq;         // E4M3 token rows [T*K, H], [T, H]
+  const uint8_t *xps, *xs;         // their 1 x 128 scales (UE8M0)
+  const int32_t* offsets;          // [E+1]
+  const uint8_t *w1, *w3, *w2;     // routed weights, E4M3
+  const uint8_t *w1s, *w3s, *w2s;  // their 128 x 128 block scales (UE8M0)
+  const uint8_t *ws1, *ws3, *ws2;  // shared expert
+  const uint8_t *ws1s, *ws3s, *ws2s;
+  uint8_t *mq, *msq;               // intermediate codes [T*K, I], [T, I_s]
+  uint8_t *ms, *mss;               // their scales (UE8M0)
+  uint16_t *yp, *ys;               // outputs, bf16
+  DevStatus* status;
+  uint64_t wait_limit_ns;
+};
+int mx_ffn_supported(int H, int I, int I_shared, int E);
+int launch_expert_ffn_mx(const FfnMxArgs& a, cudaStream_t s);
 
 // ---- router_gemm.cu
 // router logits on the tensor cores from the exact 3-way bf16 split of the

@@ -94,6 +94,7 @@ struct Layout {
   size_t bal_sp = 0, bal_flags = 0;  // [T, E] fp32 s', [T, E] u8 top-K flags
   size_t bal_pP = 0, bal_pc = 0;     // per-split partial sums (bounded)
   size_t f8_mq = 0, f8_ms = 0, f8_msq = 0, f8_mss = 0;  // FP8 intermediate
+  size_t mx_mq = 0, mx_ms = 0, mx_msq = 0, mx_mss = 0;  // its UE8M0 form
   // expert backward (padded dispatch of cap rows)
   size_t b_poff = 0, b_pdest = 0, b_gp = 0, b_xpp = 0, b_dpp = 0, b_p = 0,
          b_q = 0, b_hg = 0, b_dp = 0, b_dq = 0, b_dgp = 0, b_dxpp = 0,
@@ -180,11 +181,19 @@ Layout layout(const moe_dims_t* d, moe_ws_kind_t which) {
     L.f8_msq = take(T * Is);
     L.f8_mss = take(T * (Is / 128) * 4);
   }
+  if (which == MOE_WS_EXPERT_FFN_MX) {
+    const size_t I = d->I, Is = d->I_shared;
+    L.mx_mq = take(T * K * I);
+    L.mx_ms = take(T * K * (I / 128));
+    L.mx_msq = take(T * Is);
+    L.mx_mss = take(T * (Is / 128));
+  }
   L.total = o;
   // one MOE_WS_FORWARD workspace serves every entry point
   if (which == MOE_WS_FORWARD) {
     L.total = std::max(L.total, layout(d, MOE_WS_SEQ_BALANCE).total);
     L.total = std::max(L.total, layout(d, MOE_WS_EXPERT_FFN_FP8).total);
+    L.total = std::max(L.total, layout(d, MOE_WS_EXPERT_FFN_MX).total);
   }
   return L;
 }
@@ -331,8 +340,9 @@ void moe_set_wait_timeout_ns(uint64_t ns) {
 size_t moe_workspace_bytes(const moe_dims_t* d, moe_ws_kind_t which) {
   const bool ffn = which == MOE_WS_EXPERT_FFN || which == MOE_WS_FORWARD ||
                    which == MOE_WS_EXPERT_FFN_FP8 ||
-                   which == MOE_WS_EXPERT_BWD;
-  if (which < MOE_WS_ROUTE || which > MOE_WS_EXPERT_BWD) return 0;
+                   which == MOE_WS_EXPERT_BWD ||
+                   which == MOE_WS_EXPERT_FFN_MX;
+  if (which < MOE_WS_ROUTE || which > MOE_WS_EXPERT_FFN_MX) return 0;
   // the expert GEMMs alone (moe_expert_ffn, moe_expert_ffn_routed) do not
   // route: their workspace takes any expert count
   if (which == MOE_WS_EXPERT_FFN) {
@@ -713,6 +723,136 @@ moe_status_t moe_expert_ffn_fp8(const moe_dims_t* d, const moe_weights_fp8_t* w,
   a.status = at<DevStatus>(ws, 0);
   a.wait_limit_ns = g_wait_limit_ns;
   const int rc = moe::launch_expert_ffn_fp8(a, cs(stream));
+  return static_cast<moe_status_t>(rc);
+}
+
+moe_status_t moe_quantize_mx_blocks(const uint16_t* w, int64_t rows,
+                                    int64_t cols, uint8_t* q, uint8_t* scale,
+                                    moe_stream_t stream) {
+  if (rows < 0 || cols <= 0 || rows % 128 != 0 || cols % 128 != 0)
+    return MOE_ERR_INVALID_ARG;
+  if (rows / 128 > 65535 || cols > (1 << 30)) return MOE_ERR_UNSUPPORTED;
+  if (rows == 0) return MOE_OK;
+  MOE_NEED(w);
+  MOE_NEED(q);
+  MOE_NEED(scale);
+  MOE_ALIGN(w);
+  MOE_ALIGN(q);
+  MOE_ALIGN(scale);
+  return cuda_ok(
+      moe::launch_quant_blocks_e8(w, rows, (int)cols, q, scale, cs(stream)));
+}
+
+moe_status_t moe_quantize_mx_rows(const uint16_t* x, int64_t rows,
+                                  int64_t cols, uint8_t* q, uint8_t* scale,
+                                  moe_stream_t stream) {
+  if (rows < 0 || cols <= 0 || cols % 128 != 0) return MOE_ERR_INVALID_ARG;
+  if (cols > (1 << 30) || rows * (cols / 128) >= (1ll << 40))
+    return MOE_ERR_UNSUPPORTED;
+  if (rows == 0) return MOE_OK;
+  MOE_NEED(x);
+  MOE_NEED(q);
+  MOE_NEED(scale);
+  MOE_ALIGN(x);
+  MOE_ALIGN(q);
+  MOE_ALIGN(scale);
+  return cuda_ok(moe::launch_quant_rows_e8(x, rows, (int)cols, nullptr, 0, q,
+                                           scale, nullptr, nullptr, nullptr,
+                                           cs(stream)));
+}
+
+moe_status_t moe_permute_mx(const moe_dims_t* d, const uint16_t* x,
+                            const int32_t* dest, uint8_t* xq, uint8_t* xs,
+                            uint8_t* xpq, uint8_t* xps, void* ws,
+                            size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRY(check_dims(d, false));
+  if (d->H % 128 != 0) return MOE_ERR_UNSUPPORTED;
+  MOE_NEED_T(x);
+  MOE_NEED_T(dest);
+  MOE_NEED_T(xq);
+  MOE_NEED_T(xs);
+  MOE_NEED_T(xpq);
+  MOE_NEED_T(xps);
+  MOE_ALIGN(x);
+  MOE_ALIGN(dest);
+  MOE_ALIGN(xq);
+  MOE_ALIGN(xs);
+  MOE_ALIGN(xpq);
+  MOE_ALIGN(xps);
+  MOE_TRY(check_ws(d, MOE_WS_PERMUTE, ws, ws_bytes));
+  if (d->T == 0) return MOE_OK;
+  return cuda_ok(moe::launch_quant_rows_e8(
+      x, d->T, d->H, dest, d->topk, xq, xs, xpq, xps,
+      at<DevStatus>(ws, 0), cs(stream)));
+}
+
+moe_status_t moe_expert_ffn_mx(const moe_dims_t* d, const moe_weights_mx_t* w,
+                               const uint8_t* xpq, const uint8_t* xps,
+                               const uint8_t* xq, const uint8_t* xs,
+                               const int32_t* offsets, uint16_t* yp,
+                               uint16_t* ys, void* ws, size_t ws_bytes,
+                               moe_stream_t stream) {
+  MOE_TRY(check_dims(d, true));
+  if (!moe::mx_ffn_supported(d->H, d->I, d->I_shared, d->E))
+    return MOE_ERR_UNSUPPORTED;
+  MOE_NEED(w);
+  const void* wp[12] = {w->w1,  w->w1_scale,  w->w3,  w->w3_scale,
+                        w->w2,  w->w2_scale,  w->ws1, w->ws1_scale,
+                        w->ws3, w->ws3_scale, w->ws2, w->ws2_scale};
+  for (const void* ptr : wp) {
+    MOE_NEED(ptr);
+    MOE_ALIGN(ptr);
+  }
+  MOE_NEED_T(xpq);
+  MOE_NEED_T(xps);
+  MOE_NEED_T(xq);
+  MOE_NEED_T(xs);
+  MOE_NEED(offsets);
+  MOE_NEED_T(yp);
+  MOE_NEED_T(ys);
+  MOE_ALIGN(xpq);
+  MOE_ALIGN(xps);
+  MOE_ALIGN(xq);
+  MOE_ALIGN(xs);
+  MOE_ALIGN(offsets);
+  MOE_ALIGN(yp);
+  MOE_ALIGN(ys);
+  MOE_TRY(check_ws(d, MOE_WS_EXPERT_FFN_MX, ws, ws_bytes));
+  if (d->T == 0) return MOE_OK;
+  const Layout L = layout(d, MOE_WS_EXPERT_FFN_MX);
+  moe::FfnMxArgs a;
+  a.T = d->T;
+  a.H = d->H;
+  a.E = d->E;
+  a.topk = d->topk;
+  a.I = d->I;
+  a.I_shared = d->I_shared;
+  a.xpq = xpq;
+  a.xq = xq;
+  a.xps = xps;
+  a.xs = xs;
+  a.offsets = offsets;
+  a.w1 = w->w1;
+  a.w3 = w->w3;
+  a.w2 = w->w2;
+  a.w1s = w->w1_scale;
+  a.w3s = w->w3_scale;
+  a.w2s = w->w2_scale;
+  a.ws1 = w->ws1;
+  a.ws3 = w->ws3;
+  a.ws2 = w->ws2;
+  a.ws1s = w->ws1_scale;
+  a.ws3s = w->ws3_scale;
+  a.ws2s = w->ws2_scale;
+  a.mq = at<uint8_t>(ws, L.mx_mq);
+  a.ms = at<uint8_t>(ws, L.mx_ms);
+  a.msq = at<uint8_t>(ws, L.mx_msq);
+  a.mss = at<uint8_t>(ws, L.mx_mss);
+  a.yp = yp;
+  a.ys = ys;
+  a.status = at<DevStatus>(ws, 0);
+  a.wait_limit_ns = g_wait_limit_ns;
+  const int rc = moe::launch_expert_ffn_mx(a, cs(stream));
   return static_cast<moe_status_t>(rc);
 }
 

@@ -18,7 +18,7 @@ LIB_PATH = os.path.join(PKG, "libmoe.so")
 
 (MOE_WS_ROUTE, MOE_WS_PERMUTE, MOE_WS_EXPERT_FFN, MOE_WS_FORWARD,
  MOE_WS_ROUTER_LOGITS, MOE_WS_SEQ_BALANCE, MOE_WS_EXPERT_FFN_FP8,
- MOE_WS_EXPERT_BWD) = 0, 1, 2, 3, 4, 5, 6, 7
+ MOE_WS_EXPERT_BWD, MOE_WS_EXPERT_FFN_MX) = 0, 1, 2, 3, 4, 5, 6, 7, 8
 
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
           3: "MOE_ERR_ALIGNMENT", 4: "MOE_ERR_WORKSPACE", 5: "MOE_ERR_CUDA",
@@ -52,6 +52,10 @@ class MoeWeightsFp8(ctypes.Structure):
                  "ws1", "ws1_scale", "ws3", "ws3_scale", "ws2", "ws2_scale")]
 
 
+class MoeWeightsMx(MoeWeightsFp8):
+    """moe_weights_mx_t: the same twelve pointers (UE8M0 byte scales)."""
+
+
 _P = ctypes.c_void_p
 _D = ctypes.POINTER(MoeDims)
 _W = ctypes.POINTER(MoeWeights)
@@ -80,6 +84,13 @@ _SIGS = {
     "moe_permute_fp8": (_I, [_D, _P, _P, _P, _P, _P, _P, _P, _S, _P]),
     "moe_expert_ffn_fp8": (_I, [_D, ctypes.POINTER(MoeWeightsFp8), _P, _P,
                                 _P, _P, _P, _P, _P, _P, _S, _P]),
+    "moe_quantize_mx_blocks": (_I, [_P, ctypes.c_int64, ctypes.c_int64, _P,
+                                    _P, _P]),
+    "moe_quantize_mx_rows": (_I, [_P, ctypes.c_int64, ctypes.c_int64, _P,
+                                  _P, _P]),
+    "moe_permute_mx": (_I, [_D, _P, _P, _P, _P, _P, _P, _P, _S, _P]),
+    "moe_expert_ffn_mx": (_I, [_D, ctypes.POINTER(MoeWeightsMx), _P, _P,
+                               _P, _P, _P, _P, _P, _P, _S, _P]),
     "moe_plan_redundant_experts": (_I, [_P, ctypes.c_int32, ctypes.c_int32,
                                         ctypes.c_int32, _P, _P]),
     "moe_route_backward": (_I, [_D, _P, _P, _P, _I, _P, _P, _S, _P]),
@@ -195,6 +206,33 @@ class WeightsFp8:
             s = torch.empty((t2.shape[0] // 128, t2.shape[1] // 128),
                             dtype=torch.float32, device=t.device)
             moe_quantize_fp8_blocks(t2, q, s, stream)
+            pairs[n] = (q, s)
+        return cls(**pairs)
+
+
+class WeightsMx(WeightsFp8):
+    """FP8 expert weights with power-of-two scales: (codes uint8, UE8M0
+    block scales uint8) pairs for w1, w3, w2 and ws1, ws3, ws2."""
+
+    def __init__(self, **pairs):
+        self.pairs = pairs
+        flat = []
+        for n in self.NAMES:
+            q, s = pairs[n]
+            flat += [_ptr(q), _ptr(s)]
+        self.struct = MoeWeightsMx(*flat)
+
+    @classmethod
+    def quantize(cls, w1, w3, w2, ws1, ws3, ws2, stream=None):
+        """128 x 128 block quantization with power-of-two scales of bf16
+        (int16) weights on the device (shapes as WeightsFp8.quantize)."""
+        pairs = {}
+        for n, t in zip(cls.NAMES, (w1, w3, w2, ws1, ws3, ws2)):
+            t2 = t.reshape(-1, t.shape[-1])
+            q = torch.empty(t2.shape, dtype=torch.uint8, device=t.device)
+            s = torch.empty((t2.shape[0] // 128, t2.shape[1] // 128),
+                            dtype=torch.uint8, device=t.device)
+            moe_quantize_mx_blocks(t2, q, s, stream)
             pairs[n] = (q, s)
         return cls(**pairs)
 
@@ -316,6 +354,36 @@ def moe_permute_fp8(d, x, dest, xq, xs, xpq, xps, ws, stream=None):
 def moe_expert_ffn_fp8(d, w: WeightsFp8, xpq, xps, xq, xs, offsets, yp, ys,
                        ws, stream=None):
     _check("moe_expert_ffn_fp8", lib().moe_expert_ffn_fp8(
+        ctypes.byref(d), ctypes.byref(w.struct), _ptr(xpq), _ptr(xps),
+        _ptr(xq), _ptr(xs), _ptr(offsets), _ptr(yp), _ptr(ys), _ptr(ws),
+        ws.numel(), _stream(stream)))
+
+
+def moe_quantize_mx_blocks(w, q, scale, stream=None):
+    """128 x 128 block E4M3 quantization with power-of-two (UE8M0) scales of
+    a 2-D bf16 (int16) tensor."""
+    rows, cols = w.shape
+    _check("moe_quantize_mx_blocks", lib().moe_quantize_mx_blocks(
+        _ptr(w), rows, cols, _ptr(q), _ptr(scale), _stream(stream)))
+
+
+def moe_quantize_mx_rows(x, q, scale, stream=None):
+    """1 x 128 tile E4M3 quantization with power-of-two (UE8M0) scales of a
+    2-D bf16 (int16) tensor."""
+    rows, cols = x.shape
+    _check("moe_quantize_mx_rows", lib().moe_quantize_mx_rows(
+        _ptr(x), rows, cols, _ptr(q), _ptr(scale), _stream(stream)))
+
+
+def moe_permute_mx(d, x, dest, xq, xs, xpq, xps, ws, stream=None):
+    _check("moe_permute_mx", lib().moe_permute_mx(
+        ctypes.byref(d), _ptr(x), _ptr(dest), _ptr(xq), _ptr(xs), _ptr(xpq),
+        _ptr(xps), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def moe_expert_ffn_mx(d, w: WeightsMx, xpq, xps, xq, xs, offsets, yp, ys,
+                      ws, stream=None):
+    _check("moe_expert_ffn_mx", lib().moe_expert_ffn_mx(
         ctypes.byref(d), ctypes.byref(w.struct), _ptr(xpq), _ptr(xps),
         _ptr(xq), _ptr(xs), _ptr(offsets), _ptr(yp), _ptr(ys), _ptr(ws),
         ws.numel(), _stream(stream)))

@@ -118,7 +118,8 @@ typedef enum {
   MOE_WS_ROUTER_LOGITS = 4,
   MOE_WS_SEQ_BALANCE = 5,
   MOE_WS_EXPERT_FFN_FP8 = 6,
-  MOE_WS_EXPERT_BWD = 7
+  MOE_WS_EXPERT_BWD = 7,
+  MOE_WS_EXPERT_FFN_MX = 8
 } moe_ws_kind_t;
 
 /* Bytes of device workspace `which` needs for dims `d` (0 if d is invalid).
@@ -430,6 +431,76 @@ moe_status_t moe_expert_ffn_fp8(const moe_dims_t* d, const moe_weights_fp8_t* w,
                                 const int32_t* offsets, uint16_t* yp,
                                 uint16_t* ys, void* ws, size_t ws_bytes,
                                 moe_stream_t stream);
+
+/* FP8 with power-of-two group scales ("02 · DeepSeek-V3" §2 likens its
+ * 1 x 128 / 128 x 128 groups to the microscaling formats whose scaling
+ * Blackwell's tensor cores apply natively; there a scale is a power of two
+ * held as an 8-bit exponent).  Same groups and codes as the FP8 calls
+ * above, but each group's scale is
+ *   s = 2^e, e the least integer with 448 * 2^e >= amax (amax = the
+ *       group's max |value|), at least -127; e = 0 for an all-zero group
+ * stored as the byte e + 127 (UE8M0), and
+ *   code = the E4M3 value nearest to x / s (exact quotient), ties to the
+ *          even mantissa, saturated to +-448.
+ * moe_quantize_mx_blocks: w [rows, cols] bf16 -> q [rows, cols] u8 and
+ *   scale [rows/128, cols/128] u8; sizes and errors as
+ *   moe_quantize_fp8_blocks.
+ * moe_quantize_mx_rows: x [rows, cols] bf16 -> q u8 and scale
+ *   [rows, cols/128] u8, one per 1 x 128 tile; as moe_quantize_fp8_rows.
+ * moe_permute_mx: quantise-on-permute as moe_permute_fp8 with these
+ *   scales: xq [T, H] u8, xs [T, H/128] u8, xpq[dest[t,k]] = xq[t],
+ *   xps[dest[t,k]] = xs[t]; workspace MOE_WS_PERMUTE (error word only). */
+moe_status_t moe_quantize_mx_blocks(const uint16_t* w, int64_t rows,
+                                    int64_t cols, uint8_t* q, uint8_t* scale,
+                                    moe_stream_t stream);
+moe_status_t moe_quantize_mx_rows(const uint16_t* x, int64_t rows,
+                                  int64_t cols, uint8_t* q, uint8_t* scale,
+                                  moe_stream_t stream);
+moe_status_t moe_permute_mx(const moe_dims_t* d, const uint16_t* x,
+                            const int32_t* dest, uint8_t* xq, uint8_t* xs,
+                            uint8_t* xpq, uint8_t* xps, void* ws,
+                            size_t ws_bytes, moe_stream_t stream);
+
+/* Expert weights with power-of-two scales: E4M3 codes and UE8M0 block
+ * scales as moe_quantize_mx_blocks writes them (device pointers,
+ * caller-owned), shapes as moe_weights_fp8_t. */
+typedef struct {
+  const uint8_t* w1;
+  const uint8_t* w1_scale;
+  const uint8_t* w3;
+  const uint8_t* w3_scale;
+  const uint8_t* w2;
+  const uint8_t* w2_scale;
+  const uint8_t* ws1;
+  const uint8_t* ws1_scale;
+  const uint8_t* ws3;
+  const uint8_t* ws3_scale;
+  const uint8_t* ws2;
+  const uint8_t* ws2_scale;
+} moe_weights_mx_t;
+
+/* Expert FFNs in FP8 with power-of-two group scales, scaled by the tensor
+ * cores ("02 · DeepSeek-V3" §2 mixed precision on §1.1's SwiGLU experts):
+ * tcgen05 block-scaled MMAs multiply every 32-element slice of a product by
+ * its token's and its weight block's scale and accumulate the whole
+ * reduction in fp32, so no partial sum is promoted on the CUDA cores; the
+ * intermediate silu(p) * q is quantized to E4M3 in 1 x 128 tiles with
+ * power-of-two scales for the down projection.
+ *   xpq [T*K, H] u8, xps [T*K, H/128] u8    routed rows (moe_permute_mx)
+ *   xq  [T, H] u8,   xs  [T, H/128] u8      token rows (shared expert)
+ *   offsets [E+1] int32                     as written by moe_permute
+ *   yp [T*K, H] bf16 out, FFN_e(row) for every routed row (ungated)
+ *   ys [T, H] bf16 out, FFN_shared(x_t)
+ * H, I, I_shared must be multiples of 128 (MOE_ERR_UNSUPPORTED otherwise).
+ * Token chunks of up to 192 rows (224 when the experts average 256 rows or
+ * more), so one weight tile serves a prefill expert's rows at once.
+ * Workspace: MOE_WS_EXPERT_FFN_MX. */
+moe_status_t moe_expert_ffn_mx(const moe_dims_t* d, const moe_weights_mx_t* w,
+                               const uint8_t* xpq, const uint8_t* xps,
+                               const uint8_t* xq, const uint8_t* xs,
+                               const int32_t* offsets, uint16_t* yp,
+                               uint16_t* ys, void* ws, size_t ws_bytes,
+                               moe_stream_t stream);
 
 /* Backward of the expert FFNs and the combine, for a fixed routing (the
  * training side of "02 · DeepSeek-V3" §1.1 SwiGLU experts and §1.3 eq. 12;

@@ -85,3 +85,44 @@ def ffn_bound_check(got, a, w1, w3, w2):
     ratio = np.abs(np.asarray(got, np.float64) - y) / bound
     assert ratio.max() <= 1.0, ratio.max()
     return ratio.max()
+
+
+_TABLE = O.e4m3_decode(np.arange(0x7F, dtype=np.uint8))
+# spacing of the E4M3 grid around each magnitude code (the wider side)
+_STEP = np.maximum(np.diff(_TABLE, append=_TABLE[-1] + 32.0),
+                   np.diff(_TABLE, prepend=0.0))
+
+
+def _flip_bound(m, w2):
+    """2 max_i step_i(t) |W2_ji| for the oracle's intermediate m = (codes,
+    scales) of each token and the dequantized W2 [H, I]."""
+    mq, ms = m
+    step = _STEP[mq & 0x7F] * np.repeat(ms.astype(np.float64), 128, axis=1)
+    aw = np.abs(w2)
+    out = np.empty((mq.shape[0], aw.shape[0]))
+    for t in range(mq.shape[0]):
+        out[t] = 2.0 * (aw * step[t][None, :]).max(axis=1)
+    return out
+
+
+def fp8_ffn_check(got, ref, what, m=None, w2=None):
+    """The FP8 expert bar (see test_gpu_fp8_ffn.py's module docstring):
+    |y_gpu - y| <= 2^-8 |y| + 1e-3 RMS(y) + the one-step code flips of the
+    intermediate, and RMS error <= 5e-3 RMS(y)."""
+    got = np.asarray(got, np.float64)
+    rms = np.sqrt(np.mean(ref * ref))
+    err = np.abs(got - ref)
+    bound = 2.0 ** -8 * np.abs(ref) + 1e-3 * rms
+    if m is not None:
+        bound = bound + _flip_bound(m, w2)
+    # on failure, say how the two relate: a scale slip shows as a clean
+    # fit with the wrong factor, a layout slip as low correlation
+    g, r = got.ravel(), ref.ravel()
+    diag = dict(what=what, max_err=float(err.max() / rms),
+                rms_err=float(np.sqrt(np.mean(err * err)) / rms),
+                corr=float(np.corrcoef(g, r)[0, 1]) if g.std() > 0 else 0.0,
+                fit=float(g @ r / (r @ r)), got_rms=float(np.sqrt(np.mean(
+                    g * g)) / rms), finite=bool(np.isfinite(g).all()),
+                over=int(np.sum(err > bound)))
+    assert np.all(err <= bound), diag
+    assert np.sqrt(np.mean(err * err)) <= 5e-3 * rms, diag

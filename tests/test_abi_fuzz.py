@@ -64,6 +64,9 @@ def _calls(L, d, fault, which, ws_bytes):
     def weights8(P):
         return ops.MoeWeightsFp8(*(P(i) for i in range(12)))
 
+    def weightsmx(P):
+        return ops.MoeWeightsMx(*(P(i) for i in range(12)))
+
     table = {
         "moe_route": (5, lambda P: L.moe_route(
             by(d), P(0), P(1), P(2), P(3), P(4), A, ws_bytes, None)),
@@ -84,6 +87,10 @@ def _calls(L, d, fault, which, ws_bytes):
             by(d), P(0), P(1), P(2), P(3), P(4), P(5), A, ws_bytes, None)),
         "moe_expert_ffn_fp8": (12, lambda P: L.moe_expert_ffn_fp8(
             by(d), by(weights8(P)), A, A, A, A, A, A, A, A, ws_bytes, None)),
+        "moe_permute_mx": (6, lambda P: L.moe_permute_mx(
+            by(d), P(0), P(1), P(2), P(3), P(4), P(5), A, ws_bytes, None)),
+        "moe_expert_ffn_mx": (12, lambda P: L.moe_expert_ffn_mx(
+            by(d), by(weightsmx(P)), A, A, A, A, A, A, A, A, ws_bytes, None)),
         "moe_route_backward": (4, lambda P: L.moe_route_backward(
             by(d), P(0), P(1), P(2), 0, P(3), A, ws_bytes, None)),
     }
@@ -97,7 +104,8 @@ def test_invalid_calls_are_rejected_before_any_launch(L, seed):
     d = ops.dims(**dict(V3, **over))
     which = int(g.integers(0, 12))
     ws_bytes = 64 if fault == "small_ws" else 1 << 40
-    ffn = {"moe_expert_ffn", "moe_forward", "moe_expert_ffn_fp8"}
+    ffn = {"moe_expert_ffn", "moe_forward", "moe_expert_ffn_fp8",
+           "moe_expert_ffn_mx"}
     for name, call in _calls(L, d, fault, which, ws_bytes).items():
         if fault == "small_ws" and name == "moe_combine":
             continue                      # takes no workspace

@@ -218,6 +218,56 @@ def test_fp8_ffn_validation(L):
               FAKE, None, None, FAKE, 1 << 20, None) == 0
 
 
+def test_mx_quantization_validation(L):
+    qb, qr = L.moe_quantize_mx_blocks, L.moe_quantize_mx_rows
+    assert qb(FAKE, 100, 128, FAKE, FAKE, None) == 1       # rows % 128
+    assert qb(FAKE, 128, 100, FAKE, FAKE, None) == 1       # cols % 128
+    assert qb(FAKE, 128 * 65536, 128, FAKE, FAKE, None) == 2
+    assert qb(FAKE, 128, 128, FAKE, None, None) == 1
+    assert qb(FAKE, 128, 128, FAKE, FAKE + 4, None) == 3
+    assert qb(FAKE, 0, 128, None, None, None) == 0         # nothing to do
+    assert qr(FAKE, 5, 100, FAKE, FAKE, None) == 1
+    assert qr(FAKE, -1, 128, FAKE, FAKE, None) == 1
+    assert qr(FAKE + 2, 5, 128, FAKE, FAKE, None) == 3
+    assert qr(FAKE, 0, 128, None, None, None) == 0
+    d = ops.dims(**V3)
+    pm = L.moe_permute_mx
+
+    def call(dd, x=FAKE, dest=FAKE, xps=FAKE, ws_bytes=1 << 30):
+        return pm(ctypes.byref(dd), x, dest, FAKE, FAKE, FAKE, xps, FAKE,
+                  ws_bytes, None)
+    assert call(d, x=None) == 1
+    assert call(d, xps=FAKE + 8) == 3
+    assert call(d, ws_bytes=16) == 4
+    assert call(ops.dims(**dict(V3, H=192))) == 2           # H % 128
+    assert pm(ctypes.byref(ops.dims(**dict(V3, T=0))), None, None, None,
+              None, None, None, FAKE, 1 << 30, None) == 0
+
+
+def test_mx_ffn_validation(L):
+    d = ops.dims(**V3)
+    fn = L.moe_expert_ffn_mx
+    need = ops.workspace_bytes(d, ops.MOE_WS_EXPERT_FFN_MX)
+    # E4M3 intermediate codes + UE8M0 scales, routed and shared rows
+    assert need >= 4096 * 8 * 2048 * (1 + 1 / 128) + 4096 * 2048
+    assert need <= ops.workspace_bytes(d, ops.MOE_WS_FORWARD)
+
+    def call(dd, w, xs=FAKE, ws_bytes=1 << 40):
+        return fn(ctypes.byref(dd), ctypes.byref(w), FAKE, FAKE, FAKE, xs,
+                  FAKE, FAKE, FAKE, FAKE, ws_bytes, None)
+    good = ops.MoeWeightsMx(*(FAKE,) * 12)
+    assert call(ops.dims(**dict(V3, H=192)), good) == 2      # H % 128
+    assert call(ops.dims(**dict(V3, I=64 * 3)), good) == 2   # I % 128
+    assert call(d, ops.MoeWeightsMx(*(FAKE,) * 11, None)) == 1
+    assert call(d, ops.MoeWeightsMx(*(FAKE,) * 5, FAKE + 4,
+                                    *(FAKE,) * 6)) == 3
+    assert call(d, good, xs=FAKE + 8) == 3
+    assert call(d, good, ws_bytes=1024) == 4
+    d0 = ops.dims(**dict(V3, T=0))
+    assert fn(ctypes.byref(d0), ctypes.byref(good), None, None, None, None,
+              FAKE, None, None, FAKE, 1 << 20, None) == 0
+
+
 def test_routing_backward_validation(L):
     d = ops.dims(**V3)
     rb, bb = L.moe_route_backward, L.moe_seq_balance_loss_backward

@@ -20,49 +20,11 @@ import torch
 from deepseekmoe_routing_expert_moe_b300 import inputs, ops
 from oracle import moe_oracle as O
 
-from gpu_helpers import bf16_dev_to_f32, dev
+from gpu_helpers import bf16_dev_to_f32, dev, fp8_ffn_check
 
 pytestmark = pytest.mark.gpu
 
 f32 = inputs.bf16_bits_to_f32
-
-
-_TABLE = O.e4m3_decode(np.arange(0x7F, dtype=np.uint8))
-# spacing of the E4M3 grid around each magnitude code (the wider side)
-_STEP = np.maximum(np.diff(_TABLE, append=_TABLE[-1] + 32.0),
-                   np.diff(_TABLE, prepend=0.0))
-
-
-def _flip_bound(m, w2):
-    """2 max_i step_i(t) |W2_ji| for the oracle's intermediate m = (codes,
-    scales) of each token and the dequantized W2 [H, I]."""
-    mq, ms = m
-    step = _STEP[mq & 0x7F] * np.repeat(ms.astype(np.float64), 128, axis=1)
-    aw = np.abs(w2)
-    out = np.empty((mq.shape[0], aw.shape[0]))
-    for t in range(mq.shape[0]):
-        out[t] = 2.0 * (aw * step[t][None, :]).max(axis=1)
-    return out
-
-
-def _check(got, ref, what, m=None, w2=None):
-    got = np.asarray(got, np.float64)
-    rms = np.sqrt(np.mean(ref * ref))
-    err = np.abs(got - ref)
-    bound = 2.0 ** -8 * np.abs(ref) + 1e-3 * rms
-    if m is not None:
-        bound = bound + _flip_bound(m, w2)
-    # on failure, say how the two relate: a scale slip shows as a clean
-    # fit with the wrong factor, a layout slip as low correlation
-    g, r = got.ravel(), ref.ravel()
-    diag = dict(what=what, max_err=float(err.max() / rms),
-                rms_err=float(np.sqrt(np.mean(err * err)) / rms),
-                corr=float(np.corrcoef(g, r)[0, 1]) if g.std() > 0 else 0.0,
-                fit=float(g @ r / (r @ r)), got_rms=float(np.sqrt(np.mean(
-                    g * g)) / rms), finite=bool(np.isfinite(g).all()),
-                over=int(np.sum(err > bound)))
-    assert np.all(err <= bound), diag
-    assert np.sqrt(np.mean(err * err)) <= 5e-3 * rms, diag
 
 
 def _host_weights(cfg, e):
@@ -123,11 +85,13 @@ def _assert_layer(cfg, idx, T=None, experts=None, shared_rows=None):
             continue
         rows = p["src_row"][a:b] // cfg.topk
         ref, m = O.fp8_swiglu_ffn(xq[rows], xs[rows], *per[e])
-        _check(yp[a:b], ref, f"expert {e}", m, O.dequantize(*per[e][2], 128))
+        fp8_ffn_check(yp[a:b], ref, f"expert {e}", m,
+                      O.dequantize(*per[e][2], 128))
     rows = np.arange(xq.shape[0]) if shared_rows is None else shared_rows
     ref, m = O.fp8_swiglu_ffn(xq[rows], xs[rows], sh["ws1"], sh["ws3"],
                               sh["ws2"])
-    _check(ys[rows], ref, "shared", m, O.dequantize(*sh["ws2"], 128))
+    fp8_ffn_check(ys[rows], ref, "shared", m,
+                  O.dequantize(*sh["ws2"], 128))
 
 
 def test_small_layer_every_row():
@@ -227,9 +191,11 @@ def test_v3_full_size_sampled_experts(name):
         rows = tok[a:b]
         hw = _host_weights(cfg, e)
         ref, m = O.fp8_swiglu_ffn(xq[rows], xs[rows], *hw)
-        _check(yp[a:b], ref, f"expert {e}", m, O.dequantize(*hw[2], 128))
+        fp8_ffn_check(yp[a:b], ref, f"expert {e}", m,
+                      O.dequantize(*hw[2], 128))
     sh = _shared(cfg)
     rows = np.arange(0, T, max(9, T // 40))
     ref, m = O.fp8_swiglu_ffn(xq[rows], xs[rows], sh["ws1"], sh["ws3"],
                               sh["ws2"])
-    _check(ys[rows], ref, "shared", m, O.dequantize(*sh["ws2"], 128))
+    fp8_ffn_check(ys[rows], ref, "shared", m,
+                  O.dequantize(*sh["ws2"], 128))
