@@ -20,7 +20,7 @@
 // Orientation and work list as the BF16 kernels (grouped_gemm.cu): weights
 // are the MMA's M side (128 rows = one scale block), tokens its N side; a
 // unit is (segment, feature block, chunk of rows); one persistent CTA per
-// SM, 7 warps:
+// SM, 11 warps:
 //   warp 0 lane 0   weight producer: per 128-wide k-block the two 128 x 128
 //                   E4M3 tiles, 128-byte swizzle, a deep ring (HBM stream)
 //   warp 2          token producer: per k-block the scale atoms (below) and
@@ -28,9 +28,14 @@
 //   warp 1 lane 0   MMA: tcgen05.cp of the k-block's scale atoms into
 //                   tensor memory, then 4 block-scaled MMAs (K = 32) per
 //                   accumulator, slice j reading byte j of each scale word
-//   warps 3..6      epilogue: tcgen05.ld, SwiGLU + the 1 x 128 power-of-two
-//                   re-quantization (the tile of token j is column j over
-//                   the four lane quadrants) or bf16 conversion
+//   warps 3..10     epilogue, two warps per tensor-memory lane quadrant,
+//                   each with half of the unit's 16-column chunks:
+//                   tcgen05.ld, then (up) SwiGLU into fp32 registers and
+//                   each column's max over the warp's 32 feature rows; the
+//                   tensor memory is released at once, and after one
+//                   barrier every column's 1 x 128 tile maximum (the four
+//                   quadrants' maxima) gives its power-of-two scale and the
+//                   codes; (down) bf16 conversion and stores
 // Scale atoms (the layout tcgen05.cp 32x128b.warpx4 copies into the four
 // lane quadrants): 512 bytes for 128 rows (or columns) r and 4 slices k at
 // byte (r % 32) * 16 + (r / 32) * 4 + k.  Per k-block: one atom per weight
@@ -67,7 +72,7 @@ constexpr int XSF_SET = 24;
 constexpr uint32_t XTMEM_COLS = 512;
 constexpr int XTOK_BOXES = 4;               // token boxes of 16..128 rows
 constexpr int XEPI0 = 3;                    // first epilogue warp
-constexpr int XEPI = 4;                     // one per lane quadrant
+constexpr int XEPI = 8;  // two per lane quadrant, half the columns each
 constexpr int XTHREADS = 32 * (XEPI0 + XEPI);
 constexpr size_t XSMEM_LIMIT = 232448;      // 227 KB per CTA
 constexpr uint64_t XDRAIN_NS = 2000000000ull;
@@ -370,8 +375,30 @@ __global__ void __launch_bounds__(XTHREADS, 1)
       // (its outputs are not stored): scale 1 there
       const bool b_live = (MODE == kMxUp) || (w.f * FB + XM < nout);
       const uint32_t tx = (uint32_t)w.n * XK;
+      // the scale bytes of k-block kb: weight tiles a, b and token rows
+      // lane + 32 c (c < 8: columns 0..255), 127 (scale 1) past the chunk;
+      // loaded two k-blocks ahead of their atoms
+      auto fetch = [&](int kb, uint32_t (&v)[10]) {
+        if (kb >= nkb) {
+#pragma unroll
+          for (int i = 0; i < 10; ++i) v[i] = 127u;
+          return;
+        }
+        v[0] = __ldg(sa + (size_t)blk_a * nkb + kb);
+        v[1] = b_live ? __ldg(sb + (size_t)blk_b * nkb + kb) : 127u;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const int n = 32 * c + lane;
+          v[2 + c] =
+              n < w.rows ? __ldg(ts + (size_t)(w.row0 + n) * nkb + kb) : 127u;
+        }
+      };
+      uint32_t v0[10], v1[10], v2[10];
+      fetch(0, v0);
+      fetch(1, v1);
       bool ok = true;
       for (int kb = 0; kb < nkb; ++kb) {
+        fetch(kb + 2, v2);
         int okw = 1;
         if (lane == 0)
           okw = mbar_wait_bounded(smem_u32(&kempty[stage]), phase ^ 1,
@@ -383,26 +410,22 @@ __global__ void __launch_bounds__(XTHREADS, 1)
           break;
         }
         uint8_t* sf = sF + stage * XSF_BYTES;
-        const uint32_t ea = __ldg(sa + (size_t)blk_a * nkb + kb);
-        const uint32_t eb = b_live ? __ldg(sb + (size_t)blk_b * nkb + kb)
-                                   : 127u;
-        const uint32_t wa4 = ea * 0x01010101u, wb4 = eb * 0x01010101u;
+        const uint32_t wa4 = v0[0] * 0x01010101u, wb4 = v0[1] * 0x01010101u;
         reinterpret_cast<uint4*>(sf)[lane] = make_uint4(wa4, wa4, wa4, wa4);
         reinterpret_cast<uint4*>(sf + 512)[lane] =
             make_uint4(wb4, wb4, wb4, wb4);
         // token columns 128 t .. 128 t + 127: lane holds rows lane + 32 c
-        for (int t = 0; 128 * t < w.n; ++t) {
-          uint32_t v[4];
+        reinterpret_cast<uint4*>(sf + 1024)[lane] =
+            make_uint4(v0[2] * 0x01010101u, v0[3] * 0x01010101u,
+                       v0[4] * 0x01010101u, v0[5] * 0x01010101u);
+        if (w.n > 128)
+          reinterpret_cast<uint4*>(sf + 1536)[lane] =
+              make_uint4(v0[6] * 0x01010101u, v0[7] * 0x01010101u,
+                         v0[8] * 0x01010101u, v0[9] * 0x01010101u);
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const int n = 128 * t + 32 * c + lane;
-            const uint32_t b =
-                n < w.rows ? __ldg(ts + (size_t)(w.row0 + n) * nkb + kb)
-                           : 127u;
-            v[c] = b * 0x01010101u;
-          }
-          reinterpret_cast<uint4*>(sf + 1024 + 512 * t)[lane] =
-              make_uint4(v[0], v[1], v[2], v[3]);
+        for (int i = 0; i < 10; ++i) {
+          v0[i] = v1[i];
+          v1[i] = v2[i];
         }
         fence_proxy_async_smem();
         __syncwarp();
@@ -523,7 +546,9 @@ __global__ void __launch_bounds__(XTHREADS, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------- epilogue
+    constexpr int MC = (NT / 16 + 1) / 2;  // chunks of one half, at most
     const int q = warp & 3;  // TMEM lane quadrant this warp may access
+    const int half = (warp - XEPI0) >> 2;
     const int r = q * 32 + lane;
     const int et = threadIdx.x - 32 * XEPI0;
     uint32_t tph = 0;
@@ -559,63 +584,106 @@ __global__ void __launch_bounds__(XTHREADS, 1)
           wide ? tmem_base + lane_off + s1 * XSLOT : ta + XNARROW;
       const bool sh = (w.seg == 0);
       const int nout = sh ? p.n_shared : p.n_routed;
+      // this warp's chunks [c_lo, c_hi) of the unit's n / 16
+      const int nch = w.n >> 4;
+      const int c_lo = half ? (nch + 1) >> 1 : 0;
+      const int c_hi = half ? nch : (nch + 1) >> 1;
       auto release = [&](int sl) {
         tc_fence_before();
         mbar_arrive(smem_u32(&tempty[sl]));
       };
       if (MODE == kMxUp) {
-        // m for 16 token columns at a time; each column's amax over the
-        // 128 features of this block (the lanes of the four quadrants)
+        float* red = s_red + (it & 1) * 4 * NT;
+        float m[MC][16];
+#pragma unroll
+        for (int i = 0; i < MC; ++i) {
+          const int c = c_lo + i;
+          if (c < c_hi) {
+            uint32_t a[16], b[16];
+            tmem_ld16(ta + 16 * c, a);
+            tmem_ld16(tb + 16 * c, b);
+            tmem_ld_wait();
+            uint32_t mine = 0;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              m[i][j] = silu_f(__uint_as_float(a[j])) * __uint_as_float(b[j]);
+              // |m| bit patterns order like the values
+              const uint32_t mx = __reduce_max_sync(
+                  0xffffffffu, __float_as_uint(fabsf(m[i][j])));
+              if (lane == j) mine = mx;
+            }
+            if (lane < 16)
+              red[q * NT + 16 * c + lane] = __uint_as_float(mine);
+          }
+        }
+        release(slot);
+        if (wide) release(s1);
+        epi_bar();
         uint8_t* qo = (sh ? p.q_shared : p.q_routed) +
                       (size_t)w.row0 * nout + w.f * XM + r;
         uint8_t* qs = (sh ? p.qs_shared : p.qs_routed) +
                       (size_t)w.row0 * (nout / XM) + w.f;
-        float* red = s_red + (it & 1) * 4 * NT;
-        for (int c = 0; 16 * c < w.n; ++c) {
-          uint32_t a[16], b[16];
-          tmem_ld16(ta + 16 * c, a);
-          tmem_ld16(tb + 16 * c, b);
-          tmem_ld_wait();
-          float m[16];
-          uint32_t mine = 0;
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            m[j] = silu_f(__uint_as_float(a[j])) * __uint_as_float(b[j]);
-            // |m| bit patterns order like the values
-            const uint32_t mx = __reduce_max_sync(
-                0xffffffffu, __float_as_uint(fabsf(m[j])));
-            if (lane == j) mine = mx;
+        for (int i = 0; i < MC; ++i) {
+          const int c = c_lo + i;
+          if (c < c_hi) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int col = 16 * c + j;
+              const float amax =
+                  fmaxf(fmaxf(red[col], red[NT + col]),
+                        fmaxf(red[2 * NT + col], red[3 * NT + col]));
+              const int e = ue8m0_exponent(amax);
+              if (col < w.rows) {
+                qo[(size_t)col * nout] =
+                    (uint8_t)e4m3_of(m[i][j] * pow2_neg(e));
+                if (r == j) qs[(size_t)col * (nout / XM)] = (uint8_t)(e + 127);
+              }
+            }
           }
-          if (lane < 16) red[q * NT + 16 * c + lane] = __uint_as_float(mine);
-          epi_bar();
+        }
+      } else {
+        // every column of this warp's chunks into bf16 pairs first, so the
+        // tensor memory goes back to the MMA before the scattered stores
+        uint32_t pa[MC][8], pb[MC][8];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int col = 16 * c + j;
-            const float amax =
-                fmaxf(fmaxf(red[col], red[NT + col]),
-                      fmaxf(red[2 * NT + col], red[3 * NT + col]));
-            const int e = ue8m0_exponent(amax);
-            if (col < w.rows) {
-              qo[(size_t)col * nout] = (uint8_t)e4m3_of(m[j] * pow2_neg(e));
-              if (r == j) qs[(size_t)col * (nout / XM)] = (uint8_t)(e + 127);
+        for (int i = 0; i < MC; ++i) {
+          const int c = c_lo + i;
+          if (c < c_hi) {
+            uint32_t a[16], b[16];
+            tmem_ld16(ta + 16 * c, a);
+            tmem_ld16(tb + 16 * c, b);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              pa[i][j] = pack_bf16x2(__uint_as_float(a[2 * j]),
+                                     __uint_as_float(a[2 * j + 1]));
+              pb[i][j] = pack_bf16x2(__uint_as_float(b[2 * j]),
+                                     __uint_as_float(b[2 * j + 1]));
             }
           }
         }
         release(slot);
         if (wide) release(s1);
-      } else {
-        // a wide unit's accumulators sit in two slots: each is released as
-        // soon as it is read; a narrow unit's slot after both are read
-        uint16_t* out = sh ? p.y_shared : p.y_routed;
-        uint16_t* obase = out + (size_t)w.row0 * nout;
-        const int fa = w.f * FB + r;
-        uint32_t pk[NT / 2];
-        load_packed<NT>(ta, w.n, pk);
-        if (wide) release(slot);
-        if (fa < nout) store_packed<NT>(pk, obase + fa, nout, w.rows);
-        load_packed<NT>(tb, w.n, pk);
-        release(s1);
-        if (fa + XM < nout) store_packed<NT>(pk, obase + fa + XM, nout, w.rows);
+        uint16_t* out = (sh ? p.y_shared : p.y_routed) +
+                        (size_t)w.row0 * nout + w.f * FB + r;
+        const bool live_b = w.f * FB + XM + r < nout;
+#pragma unroll
+        for (int i = 0; i < MC; ++i) {
+          const int c = c_lo + i;
+          if (c < c_hi) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int row = 16 * c + j;
+              if (row < w.rows) {
+                uint16_t* o = out + (size_t)row * nout;
+                const int sh16 = (j & 1) * 16;
+                o[0] = (uint16_t)(pa[i][j >> 1] >> sh16);
+                if (live_b) o[XM] = (uint16_t)(pb[i][j >> 1] >> sh16);
+              }
+            }
+          }
+        }
       }
       tph ^= 1u << slot;
       if (wide)
