@@ -140,6 +140,20 @@ __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst,
       : "memory");
 }
 
+// Four rows of a 2-D tensor gathered into shared memory: rows r0..r3 (any
+// order, each a box of one row) at columns c0.., landing as four
+// consecutive rows at `dst`; completion counted in bytes on `bar`.
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const void* tmap,
+                                            int32_t c0, int4 rows,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cta.global.tile::gather4.mbarrier::"
+      "complete_tx::bytes [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(rows.x),
+      "r"(rows.y), "r"(rows.z), "r"(rows.w), "r"(bar)
+      : "memory");
+}
+
 // 3-D tiled bulk tensor store shared -> global (bulk-group completion),
 // with an L2 cache policy for the written lines
 __device__ __forceinline__ void tma_store_3d(const void* tmap, uint32_t src,

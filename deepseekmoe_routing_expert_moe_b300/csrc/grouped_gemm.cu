@@ -29,7 +29,12 @@
 //   warp 2 lane 0   token producer: the Nx64 token tile (boxes of
 //                   128/64/32/16 rows summing to N) into a shallow ring (the
 //                   rows are L2-resident, re-read by every feature block)
-//                   both with 128-byte swizzle and mbarrier completion
+//                   both with 128-byte swizzle and mbarrier completion.  In
+//                   the gather mode of the up projection the routed rows
+//                   are not copied out beforehand: the warp reads the
+//                   chunk's token ids (dispatch order / top-K) once per
+//                   unit and every k-block gathers the rows from x itself,
+//                   four rows per TMA gather4
 //   warp 1 lane 0   tcgen05.mma issuer (M=128, N per unit, K=16), fp32
 //                   accumulators in tensor memory; warp 1 owns the TMEM
 //                   allocation (512 columns = two slots of 256)
@@ -116,6 +121,9 @@ struct GemmParams {  // CUtensorMap members carry their 64-byte alignment
   CUtensorMap wb_routed;  // up: w3 [E*I, H]     down: w2 (rows + 128)
   CUtensorMap wa_shared;  // up: ws1 [I_s, H]    down: ws2 [H, I_s]
   CUtensorMap wb_shared;  // up: ws3 [I_s, H]    down: ws2 (rows + 128)
+  CUtensorMap tok_gather; // gather mode: x [T, H], boxes of one row
+  const int32_t* src_row; // gather mode: [TK] t * topk + k of each row
+  int topk, gather;       // gather: routed rows gathered from x
   const int32_t* offsets; // [E+1]
   uint16_t* out_routed;   // up: h [TK, I]       down: yp [TK, H]
   uint16_t* out_shared;   // up: hs [T, I_s]     down: ys [T, H]
@@ -159,6 +167,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   int* useg = reinterpret_cast<int*>(const_cast<uint32_t*>(misc) + 4);
   int* srows = useg + NS + 1;
   int* srow0 = srows + NS;
+  // gather mode: the current chunk's token ids (16-byte aligned)
+  int* s_tok = reinterpret_cast<int*>(
+      (reinterpret_cast<uintptr_t>(srow0 + NS) + 15) & ~uintptr_t(15));
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
@@ -191,6 +202,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&p.wb_routed);
     prefetch_tmap(&p.wa_shared);
     prefetch_tmap(&p.wb_shared);
+    if (p.gather) prefetch_tmap(&p.tok_gather);
   }
   if (warp == 2) {
     // segment table: rows, first row, and the exclusive prefix of units
@@ -298,52 +310,68 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else if (warp == 2) {
-    if (lane == 0) {
-      // ------------------------------------------------ token producer
-      uint32_t stage = 0, phase = 0, issued = 0;
-      const uint64_t pol_t = policy_evict_last();
-      for (int u = blockIdx.x; u < total; u += gridDim.x) {
-        const Unit w = decode_unit<NT>(u, useg, srow0, srows, NS);
-        const bool sh = (w.seg == 0);
-        const CUtensorMap* tok = sh ? p.tok_shared : p.tok_routed;
-        const int nkb = (sh ? p.k_shared : p.k_routed) / BK;
-        const uint32_t tx = (uint32_t)w.n * BK * 2;
-        bool ok = true;
-        for (int kb = 0; kb < nkb; ++kb) {
-          if (!mbar_wait_bounded(smem_u32(&kempty[stage]), phase ^ 1,
-                                 abort_flag, limit, p.status,
-                                 kSiteProducer)) {
-            ok = false;
-            break;
-          }
-          const uint32_t fb = smem_u32(&kfull[stage]);
-          uint8_t* stok = sT + stage * TSTAGE_BYTES;
-          mbar_arrive_expect_tx(fb, tx);
-          // token rows [row0, row0 + n) as boxes of 128/64/32/16 rows
-          if (w.n == 256) {
-            tma_load_2d_hint(smem_u32(stok), &tok[3], kb * BK, w.row0, fb,
-                             pol_t);
-            tma_load_2d_hint(smem_u32(stok + 128 * BK * 2), &tok[3], kb * BK,
-                             w.row0 + 128, fb, pol_t);
-          } else {
-            int off = 0;
+    // -------------------------------------------------- token producer
+    uint32_t stage = 0, phase = 0, issued = 0;
+    const uint64_t pol_t = policy_evict_last();
+    for (int u = blockIdx.x; u < total; u += gridDim.x) {
+      const Unit w = decode_unit<NT>(u, useg, srow0, srows, NS);
+      const bool sh = (w.seg == 0);
+      const bool gat = !sh && p.gather;
+      const CUtensorMap* tok = sh ? p.tok_shared : p.tok_routed;
+      const int nkb = (sh ? p.k_shared : p.k_routed) / BK;
+      const uint32_t tx = (uint32_t)w.n * BK * 2;
+      if (gat) {
+        // the token of every row of the chunk; the padding rows up to the
+        // MMA's N repeat the last one (their columns are not stored)
+        for (int i = lane; i < w.n; i += 32)
+          s_tok[i] = p.src_row[w.row0 + min(i, w.rows - 1)] / p.topk;
+        __syncwarp();
+      }
+      int ok = 1;
+      for (int kb = 0; kb < nkb; ++kb) {
+        if (lane == 0) {
+          ok = mbar_wait_bounded(smem_u32(&kempty[stage]), phase ^ 1,
+                                 abort_flag, limit, p.status, kSiteProducer);
+          if (ok) {
+            const uint32_t fb = smem_u32(&kfull[stage]);
+            uint8_t* stok = sT + stage * TSTAGE_BYTES;
+            mbar_arrive_expect_tx(fb, tx);
+            if (gat) {
+              for (int g = 0; g < w.n; g += 4)
+                tma_gather4(smem_u32(stok + g * BK * 2), &p.tok_gather,
+                            kb * BK, *reinterpret_cast<const int4*>(s_tok + g),
+                            fb);
+            } else if (w.n == 256) {
+              // token rows [row0, row0 + n) as boxes of 128/64/32/16 rows
+              tma_load_2d_hint(smem_u32(stok), &tok[3], kb * BK, w.row0, fb,
+                               pol_t);
+              tma_load_2d_hint(smem_u32(stok + 128 * BK * 2), &tok[3],
+                               kb * BK, w.row0 + 128, fb, pol_t);
+            } else {
+              int off = 0;
 #pragma unroll
-            for (int b = kTokBoxes - 1; b >= 0; --b) {
-              if ((w.n >> 4) & (1 << b)) {
-                tma_load_2d_hint(smem_u32(stok + off * BK * 2), &tok[b],
-                                 kb * BK, w.row0 + off, fb, pol_t);
-                off += 16 << b;
+              for (int b = kTokBoxes - 1; b >= 0; --b) {
+                if ((w.n >> 4) & (1 << b)) {
+                  tma_load_2d_hint(smem_u32(stok + off * BK * 2), &tok[b],
+                                   kb * BK, w.row0 + off, fb, pol_t);
+                  off += 16 << b;
+                }
               }
             }
           }
-          ++issued;
-          if (++stage == kTStages) {
-            stage = 0;
-            phase ^= 1;
-          }
         }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
+        ++issued;
+        if (++stage == kTStages) {
+          stage = 0;
+          phase ^= 1;
+        }
       }
+      __syncwarp();  // s_tok is rewritten for the next unit
+      if (!ok) break;
+    }
+    if (lane == 0) {
       const uint32_t first = issued > kTStages ? issued - kTStages : 0;
       for (uint32_t i = first; i < issued; ++i)
         mbar_wait_bounded(smem_u32(&kfull[i % kTStages]),
@@ -516,7 +544,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <class P>
 size_t smem_bytes(int E) {
   return 1024 + Ring<P>::BYTES + Ring<P>::BARS * sizeof(uint64_t) +
-         4 * sizeof(uint32_t) + sizeof(int) * (3 * (E + 1) + 1);
+         4 * sizeof(uint32_t) + sizeof(int) * (3 * (E + 1) + 1) + 16 +
+         sizeof(int) * P::NT;
 }
 
 template <int MODE, class P>
@@ -555,10 +584,17 @@ int launch_expert_ffn(const FfnArgs& a, cudaStream_t s) {
   // its maps are encoded on the routed tensors (never read)
   const bool shared = a.x != nullptr;
   const int Ts = shared ? a.T : 0;
+  // without xp the routed rows are gathered from x by src_row
+  const bool gather = a.xp == nullptr;
+  if (gather && (a.x == nullptr || a.src_row == nullptr))
+    return MOE_ERR_INVALID_ARG;
   // ---- up projection + SwiGLU
   GemmParams up;
   std::memset(&up, 0, sizeof(up));
-  bool ok = token_maps(up.tok_routed, a.xp, a.H, TK) &&
+  bool ok = token_maps(up.tok_routed, gather ? a.x : a.xp, a.H,
+                       gather ? a.T : TK) &&
+            make_tmap_bf16(&up.tok_gather, shared ? a.x : a.xp, a.H,
+                           shared ? a.T : TK, 1) &&
             (shared ? token_maps(up.tok_shared, a.x, a.H, a.T)
                     : token_maps(up.tok_shared, a.xp, a.H, TK)) &&
             make_tmap_bf16(&up.wa_routed, a.w1, a.H, (uint64_t)a.E * a.I, BM) &&
@@ -570,6 +606,9 @@ int launch_expert_ffn(const FfnArgs& a, cudaStream_t s) {
                           make_tmap_bf16(&up.wb_shared, a.w3, a.H,
                                          (uint64_t)a.E * a.I, BM));
   if (!ok) return MOE_ERR_CUDA;
+  up.gather = gather ? 1 : 0;
+  up.src_row = a.src_row;
+  up.topk = a.topk;
   up.offsets = a.offsets;
   up.out_routed = a.h;
   up.out_shared = a.hs;

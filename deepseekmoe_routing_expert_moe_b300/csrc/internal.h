@@ -105,6 +105,9 @@ cudaError_t launch_quant_blocks_e8(const uint16_t* w, long long R, int C,
 struct FfnArgs {
   int T, H, E, topk, I, I_shared;
   const uint16_t *xp, *x;          // A of the up GEMM
+  // with xp == NULL: the routed rows are gathered from x inside the up
+  // GEMM, row r being token src_row[r] / topk (moe_permute's src_row)
+  const int32_t* src_row = nullptr;
   const int32_t* offsets;          // [E+1]
   const uint16_t *w1, *w3, *w2;    // routed weights
   const uint16_t *ws1, *ws3, *ws2; // shared expert

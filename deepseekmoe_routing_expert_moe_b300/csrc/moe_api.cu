@@ -102,6 +102,15 @@ struct Layout {
   size_t total = 0;
 };
 
+// moe_forward gathers the routed rows from x inside the up GEMM (TMA
+// gather4, four 128-byte rows per copy) when the experts see few rows each;
+// with more rows per expert the gathers' issue rate would bound the GEMM,
+// and the rows are copied out once (expert-sorted) instead.
+constexpr long long kGatherMeanRows = 64;
+bool gather_rows(const moe_dims_t* d) {
+  return (long long)d->T * d->topk < kGatherMeanRows * d->E;
+}
+
 Layout layout(const moe_dims_t* d, moe_ws_kind_t which) {
   Layout L;
   size_t o = kStatusBytes;
@@ -155,7 +164,7 @@ Layout layout(const moe_dims_t* d, moe_ws_kind_t which) {
     L.offsets = take((E + 1) * 4);
     L.dest = take(T * K * 4);
     L.src_row = take(T * K * 4);
-    L.xp = take(T * K * H * 2);
+    if (!gather_rows(d)) L.xp = take(T * K * H * 2);
     L.yp = take(T * K * H * 2);
     L.ys = take(T * H * 2);
   }
@@ -261,7 +270,8 @@ moe_status_t ffn_launch(const moe_dims_t* d, const moe_weights_t* w,
                         const uint16_t* xp, const uint16_t* x,
                         const int32_t* offsets, uint16_t* h, uint16_t* hs,
                         uint16_t* yp, uint16_t* ys, DevStatus* st,
-                        cudaStream_t s, void* between_event = nullptr) {
+                        cudaStream_t s, void* between_event = nullptr,
+                        const int32_t* src_row = nullptr) {
   moe::FfnArgs a;
   a.T = d->T;
   a.H = d->H;
@@ -271,6 +281,7 @@ moe_status_t ffn_launch(const moe_dims_t* d, const moe_weights_t* w,
   a.I_shared = d->I_shared;
   a.xp = xp;
   a.x = x;
+  a.src_row = src_row;
   a.offsets = offsets;
   a.w1 = w->w1;
   a.w3 = w->w3;
@@ -1074,7 +1085,6 @@ moe_status_t moe_forward(const moe_dims_t* d, const moe_weights_t* w,
   int32_t* src_row = at<int32_t>(ws, L.src_row);
   int32_t* bc = at<int32_t>(ws, L.block_counts);
   int32_t* bb = at<int32_t>(ws, L.block_base);
-  uint16_t* xp = at<uint16_t>(ws, L.xp);
   uint16_t* yp = at<uint16_t>(ws, L.yp);
   uint16_t* ys = at<uint16_t>(ws, L.ys);
 
@@ -1096,11 +1106,14 @@ moe_status_t moe_forward(const moe_dims_t* d, const moe_weights_t* w,
   MOE_TRY(cuda_ok(moe::launch_dest(idx, counts, bb, T, E, K, offsets, dest,
                                    src_row, load_stats_out, st, s)));
   prof_mark(4, s);
-  MOE_TRY(cuda_ok(moe::launch_gather(x, dest, T, H, K, xp, s)));
+  // few rows per expert: the up GEMM gathers them from x; else one copy
+  const bool gat = gather_rows(d);
+  uint16_t* xp = gat ? nullptr : at<uint16_t>(ws, L.xp);
+  if (!gat) MOE_TRY(cuda_ok(moe::launch_gather(x, dest, T, H, K, xp, s)));
   prof_mark(5, s);  // 6 is recorded between the two expert GEMMs
   MOE_TRY(ffn_launch(d, w, xp, x, offsets, at<uint16_t>(ws, L.h),
                      at<uint16_t>(ws, L.hs), yp, ys, st, s,
-                     g_prof_events ? g_prof_events[6] : nullptr));
+                     g_prof_events ? g_prof_events[6] : nullptr, src_row));
   prof_mark(7, s);
   MOE_TRY(cuda_ok(moe::launch_combine(x, ys, yp, dest, gate, T, H, K, out, s)));
   prof_mark(8, s);

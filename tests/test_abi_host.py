@@ -58,8 +58,12 @@ def test_workspace_sizes_are_consistent(L):
     f = ops.workspace_bytes(d, ops.MOE_WS_EXPERT_FFN)
     fw = ops.workspace_bytes(d, ops.MOE_WS_FORWARD)
     assert 0 < r <= fw and 0 < p <= fw and 0 < f <= fw
-    # the forward workspace holds xp, yp (T*K*H bf16 each) and h
+    # the forward workspace holds xp, yp (T*K*H bf16 each) and h at 128
+    # rows per expert (at decode the up GEMM gathers the rows from x)
     assert fw >= 2 * 4096 * 8 * 7168 * 2 + 4096 * 8 * 2048 * 2
+    dd = ops.dims(**dict(V3, T=128))
+    fd = ops.workspace_bytes(dd, ops.MOE_WS_FORWARD)
+    assert 128 * 8 * 7168 * 2 + 128 * 8 * 2048 * 2 <= fd
     bad = ops.dims(**dict(V3, E=255))
     assert ops.workspace_bytes(bad, ops.MOE_WS_FORWARD) == 0
     assert ops.workspace_bytes(d, 9) == 0
