@@ -758,7 +758,7 @@ def run_balance_gpu(args, rank, world, local_rank):
 
 FP8_WORKLOADS = ("decode_v3_fp8", "prefill_v3_fp8", "decode_v3_e32_fp8",
                  "prefill_v3_e32_fp8", "decode_v3_mx", "prefill_v3_mx",
-                 "prefill_v3_e32_mx")
+                 "decode_v3_e32_mx", "prefill_v3_e32_mx")
 
 
 def fp8_kind(workload):
