@@ -439,8 +439,11 @@ def run_gpu(args, rank, world, local_rank):
                            "double-buffered"},
         # router logits are two launches (weight split + GEMM) on the
         # tensor-core path (E % 16 == 0), three when its k ranges are split
-        # (few 128-token tiles: the partial sums are added by a kernel)
-        "gpu_launches": (nk + router_extra_launches(T, H, E)) * args.steps,
+        # (few 128-token tiles: the partial sums are added by a kernel);
+        # the dispatch copy is a launch only at >= 64 rows per expert (below
+        # that the up GEMM gathers the rows from x itself)
+        "gpu_launches": (nk - (0 if T * K >= 64 * E else 1)
+                         + router_extra_launches(T, H, E)) * args.steps,
         "clocks": clocks,
         "kernels_ms": kernels,
         "experts_touched": touched,

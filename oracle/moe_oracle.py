@@ -473,7 +473,7 @@ def fp8_swiglu_ffn(a_q, a_s, w1, w3, w2, requant=None):
 # the fine-grained groups to the microscaling formats whose scaling
 # Blackwell's tensor cores apply natively; in those formats a group's scale
 # is a power of two, stored as an 8-bit biased exponent (UE8M0).  READING
-# R22: with power-of-two scales the group scale is the least power of two
+# R28: with power-of-two scales the group scale is the least power of two
 # that keeps the group's largest magnitude within 448, i.e. 2^e with e the
 # least integer such that 448 * 2^e >= amax (clamped below at -127, the
 # smallest UE8M0 exponent; an all-zero group gets e = 0), and every code is

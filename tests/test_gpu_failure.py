@@ -134,6 +134,59 @@ def test_fp8_expert_ffn_wait_runs_out_then_context_recovers():
     assert torch.equal(yp, yp_ref) and torch.equal(ys, ys_ref)
 
 
+def test_mx_expert_ffn_wait_runs_out_then_context_recovers():
+    """The power-of-two-scale FP8 GEMMs' waits (weight producer, the scale
+    and token producer warp, MMA, the eight epilogue warps) are bounded the
+    same way: the epilogue warps vote per unit and stop together, the
+    in-flight copies and MMAs are drained, TMEM is freed, and the next
+    launch is exact again."""
+    cfg = inputs.custom_config("timeoutmx", 962, T=300, H=512, E=8,
+                               n_group=4, topk_group=2, topk=2, I=256,
+                               I_shared=256, router_sigma=0.05)
+    d = ops.dims_of(cfg)
+    T, K, H, E = cfg.T, cfg.topk, cfg.H, cfg.E
+    f32 = inputs.bf16_bits_to_f32
+    x = f32(inputs.x_tokens(cfg))
+    idx = O.route(O.router_logits(x, inputs.router_weight(cfg)),
+                  inputs.bias(cfg), cfg.n_group, cfg.topk_group, K)["idx"]
+    p = O.permutation(idx, E)
+
+    def e8(s):   # power-of-two scales -> UE8M0 bytes
+        return (np.frexp(s.astype(np.float64))[1] + 126).astype(np.uint8)
+    xq, xs = O.quantize_1x128_pow2(x)
+    tok = p["src_row"] // K
+    per = [[O.quantize_128x128_pow2(f32(m))
+            for m in inputs.expert_weights(cfg, e)] for e in range(E)]
+    pairs = {n: (dev(np.concatenate([per[e][i][0] for e in range(E)])),
+                 dev(np.concatenate([e8(per[e][i][1]) for e in range(E)])))
+             for i, n in enumerate(("w1", "w3", "w2"))}
+    for n, m in zip(("ws1", "ws3", "ws2"), inputs.shared_weights(cfg)):
+        q, s = O.quantize_128x128_pow2(f32(m))
+        pairs[n] = (dev(q), dev(e8(s)))
+    W = ops.WeightsMx(**pairs)
+    args = (dev(xq[tok]), dev(e8(xs)[tok]), dev(xq), dev(e8(xs)),
+            dev(p["offsets"]))
+
+    def run():
+        yp = torch.zeros((T * K, H), dtype=torch.int16, device="cuda")
+        ys = torch.zeros((T, H), dtype=torch.int16, device="cuda")
+        ws = ops.workspace(d, ops.MOE_WS_EXPERT_FFN_MX)
+        ops.moe_expert_ffn_mx(d, W, *args, yp, ys, ws)
+        return ops.moe_get_device_error(ws), yp, ys
+    code, yp_ref, ys_ref = run()
+    assert code == 0
+    try:
+        ops.moe_set_wait_timeout_ns(1)
+        for _ in range(2):
+            code, _, _ = run()
+            assert code == TIMEOUT
+    finally:
+        ops.moe_set_wait_timeout_ns(0)
+    code, yp, ys = run()
+    assert code == 0
+    assert torch.equal(yp, yp_ref) and torch.equal(ys, ys_ref)
+
+
 def test_expert_backward_waits_run_out_then_context_recovers():
     """The backward's four tensor-core GEMMs (recompute, both dgrads, the
     weight gradients) under the 1 ns bound: the call reports
