@@ -62,11 +62,15 @@ __device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c,
 }
 
 // ------------------------------------------------------------------
-// 1 x 128 tiles: one warp per (row, tile), 4 consecutive values per lane.
-// q[r] (if q != NULL) and, with dest != NULL, the dispatch copies
-// qp[dest[r*K + k]] for k < K receive the codes; s / sp the scales.
+// 1 x 128 tiles: one warp per (row, group of up to kTilesPerWarp tiles), 4
+// consecutive values per lane; the group's loads are all issued before the
+// first tile is reduced, and the token's dispatch rows are read once per
+// group (lane k < K holds dest[r*K + k]).  q[r] (if q != NULL) and, with
+// dest != NULL, the dispatch copies qp[dest[r*K + k]] for k < K (K <= 32)
+// receive the codes; s / sp the scales.
 // ------------------------------------------------------------------
 constexpr int kRowsWarps = 8;
+constexpr int kTilesPerWarp = 8;
 
 template <class S>
 __global__ void __launch_bounds__(kRowsWarps * 32)
@@ -77,36 +81,50 @@ __global__ void __launch_bounds__(kRowsWarps * 32)
                       typename S::T* __restrict__ sp, DevStatus* st) {
   const int lane = threadIdx.x & 31;
   const int tiles = C / 128;
+  const int groups = (tiles + kTilesPerWarp - 1) / kTilesPerWarp;
   const long long g =
       (long long)blockIdx.x * kRowsWarps + (threadIdx.x >> 5);
-  if (g >= R * tiles) return;
-  const long long r = g / tiles;
-  const int tile = (int)(g - r * tiles);
-  const size_t off = (size_t)r * C + (size_t)tile * 128 + lane * 4;
-  const uint2 raw = __ldg(reinterpret_cast<const uint2*>(x + off));
-  const float v0 = bf16_lo(raw.x), v1 = bf16_hi(raw.x);
-  const float v2 = bf16_lo(raw.y), v3 = bf16_hi(raw.y);
-  const float m = fmaxf(fmaxf(fabsf(v0), fabsf(v1)),
-                        fmaxf(fabsf(v2), fabsf(v3)));
-  // |v| bit patterns order like the values (non-negative floats)
-  const float amax =
-      __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(m)));
-  const S sc(amax);
-  const uint32_t code = e4m3x4(v0, v1, v2, v3, sc);
-  if (q != nullptr) {
-    *reinterpret_cast<uint32_t*>(q + off) = code;
-    if (lane == 0) s[(size_t)r * tiles + tile] = sc.stored();
+  if (g >= R * groups) return;
+  const long long r = g / groups;
+  const int t0 = (int)(g - r * groups) * kTilesPerWarp;
+  int dr_mine = 0;
+  bool ok_mine = false;
+  if (dest != nullptr && lane < K) {
+    dr_mine = __ldg(dest + (size_t)r * K + lane);
+    ok_mine = dr_mine >= 0 && dr_mine < RK;
+    if (!ok_mine && t0 == 0) record_error(st, MOE_ERR_DEVICE_BOUNDS, 40);
   }
-  if (dest != nullptr) {
-    for (int k = 0; k < K; ++k) {
-      const int dr = __ldg(dest + (size_t)r * K + k);
-      if (dr < 0 || dr >= RK) {
-        if (lane == 0) record_error(st, MOE_ERR_DEVICE_BOUNDS, 40);
-        continue;
+  uint2 raw[kTilesPerWarp];
+#pragma unroll
+  for (int i = 0; i < kTilesPerWarp; ++i)
+    if (t0 + i < tiles)
+      raw[i] = __ldg(reinterpret_cast<const uint2*>(
+          x + (size_t)r * C + (size_t)(t0 + i) * 128 + lane * 4));
+#pragma unroll
+  for (int i = 0; i < kTilesPerWarp; ++i) {
+    const int tile = t0 + i;
+    if (tile >= tiles) break;
+    const float v0 = bf16_lo(raw[i].x), v1 = bf16_hi(raw[i].x);
+    const float v2 = bf16_lo(raw[i].y), v3 = bf16_hi(raw[i].y);
+    const float m = fmaxf(fmaxf(fabsf(v0), fabsf(v1)),
+                          fmaxf(fabsf(v2), fabsf(v3)));
+    // |v| bit patterns order like the values (non-negative floats)
+    const float amax =
+        __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(m)));
+    const S sc(amax);
+    const uint32_t code = e4m3x4(v0, v1, v2, v3, sc);
+    const size_t off = (size_t)tile * 128 + lane * 4;
+    if (q != nullptr) {
+      *reinterpret_cast<uint32_t*>(q + (size_t)r * C + off) = code;
+      if (lane == 0) s[(size_t)r * tiles + tile] = sc.stored();
+    }
+    if (dest != nullptr) {
+      for (int k = 0; k < K; ++k) {
+        const int dr = __shfl_sync(0xffffffffu, dr_mine, k);
+        if (!__shfl_sync(0xffffffffu, ok_mine, k)) continue;
+        *reinterpret_cast<uint32_t*>(qp + (size_t)dr * C + off) = code;
+        if (lane == 0) sp[(size_t)dr * tiles + tile] = sc.stored();
       }
-      *reinterpret_cast<uint32_t*>(qp + (size_t)dr * C + (size_t)tile * 128 +
-                                   lane * 4) = code;
-      if (lane == 0) sp[(size_t)dr * tiles + tile] = sc.stored();
     }
   }
 }
@@ -162,7 +180,8 @@ cudaError_t quant_rows(const uint16_t* x, long long R, int C,
                        const int32_t* dest, int K, uint8_t* q,
                        typename S::T* s, uint8_t* qp, typename S::T* sp,
                        DevStatus* st, cudaStream_t stream) {
-  const long long warps = R * (C / 128);
+  const long long warps =
+      R * ((C / 128 + kTilesPerWarp - 1) / kTilesPerWarp);
   if (warps == 0) return cudaSuccess;
   const long long blocks = (warps + kRowsWarps - 1) / kRowsWarps;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;

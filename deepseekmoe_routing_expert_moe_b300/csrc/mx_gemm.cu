@@ -37,9 +37,13 @@
 //                   quadrants' maxima) gives its power-of-two scale and the
 //                   codes; (down) bf16 conversion and stores
 // Scale atoms (the layout tcgen05.cp 32x128b.warpx4 copies into the four
-// lane quadrants): 512 bytes for 128 rows (or columns) r and 4 slices k at
-// byte (r % 32) * 16 + (r / 32) * 4 + k.  Per k-block: one atom per weight
-// tile (its block scale in every byte), one per 128 token columns.
+// lane quadrants): 512 bytes for 128 rows (or columns) r, 4 bytes j per row
+// at byte (r % 32) * 16 + (r / 32) * 4 + j; an MMA slice reads byte j = its
+// scale ID.  A group scale is the same for the four 32-element slices of
+// its k-block, so byte j holds the scale of k-block 4g + j and the four
+// k-blocks of group g share one atom set (every slice of k-block kb reads
+// byte kb % 4): one atom per weight tile and one per 128 token columns,
+// built and copied once per four k-blocks.
 // Tensor memory: two accumulator slots of 232 columns (a unit with N <= 112
 // puts both accumulators in one slot, so consecutive units alternate slots
 // and the epilogue of one overlaps the MMAs of the next; a wider unit takes
@@ -65,6 +69,8 @@ constexpr int XUMMA_K = 32;   // k of one block-scaled MMA (one scale)
 constexpr uint32_t XW_BYTES = XM * XK;      // one weight tile, 16 KB
 constexpr uint32_t XWSTAGE = 2 * XW_BYTES;  // both weight tiles
 constexpr uint32_t XSF_BYTES = 2048;        // atoms: W tile a, b, tokens x2
+constexpr int XSF_RING = 4;    // atom groups in shared memory
+constexpr int XGROUP = 4;      // k-blocks per atom group (one byte each)
 constexpr int XSLOT = 232;                  // accumulator slot columns
 constexpr int XNARROW = 112;  // widest N with both accumulators in a slot
 constexpr int XSF_COL0 = 464;               // scale sets: 464, 488
@@ -102,7 +108,7 @@ template <class P>
 struct MxRing {
   static constexpr uint32_t TSTAGE = P::NT * XK;  // token tile bytes
   static constexpr uint32_t BYTES =
-      P::WS * XWSTAGE + P::TS * (TSTAGE + XSF_BYTES);
+      P::WS * XWSTAGE + P::TS * TSTAGE + XSF_RING * XSF_BYTES;
   static constexpr int BARS = 2 * P::WS + 2 * P::TS + 5;
   static constexpr uint32_t RED = 2 * 4 * P::NT * sizeof(float);
   static_assert(P::NT % 16 == 0 && P::NT <= 2 * XNARROW, "chunk");
@@ -205,7 +211,7 @@ __global__ void __launch_bounds__(XTHREADS, 1)
   uint8_t* sW = smem;                              // weight ring
   uint8_t* sT = smem + kWStages * XWSTAGE;         // token ring
   uint8_t* sF = sT + kTStages * TSTAGE;            // scale atoms per stage
-  float* s_red = reinterpret_cast<float*>(sF + kTStages * XSF_BYTES);
+  float* s_red = reinterpret_cast<float*>(sF + XSF_RING * XSF_BYTES);
   uint64_t* bars =
       reinterpret_cast<uint64_t*>(smem + MxRing<P>::BYTES + MxRing<P>::RED);
   uint64_t* wfull = bars;
@@ -357,7 +363,7 @@ __global__ void __launch_bounds__(XTHREADS, 1)
     __syncwarp();
   } else if (warp == 2) {
     // ------------------------------------ scale atoms + token producer
-    uint32_t stage = 0, phase = 0, issued = 0;
+    uint32_t stage = 0, phase = 0, issued = 0, sfg = 0;
     const uint64_t pol_t = policy_evict_last();
     for (int u = blockIdx.x; u < total; u += gridDim.x) {
       const Unit w = decode_unit<NT>(u, useg, srow0, srows, NS);
@@ -375,30 +381,41 @@ __global__ void __launch_bounds__(XTHREADS, 1)
       // (its outputs are not stored): scale 1 there
       const bool b_live = (MODE == kMxUp) || (w.f * FB + XM < nout);
       const uint32_t tx = (uint32_t)w.n * XK;
-      // the scale bytes of k-block kb: weight tiles a, b and token rows
-      // lane + 32 c (c < 8: columns 0..255), 127 (scale 1) past the chunk;
-      // loaded two k-blocks ahead of their atoms
-      auto fetch = [&](int kb, uint32_t (&v)[10]) {
-        if (kb >= nkb) {
+      // the scale words of k-block group g (byte j: k-block 4g + j): weight
+      // tiles a, b and token rows lane + 32 c (c < 8: columns 0..255); 127
+      // (scale 1) past the chunk or past the last k-block; fetched one
+      // group ahead of their atoms
+      const bool word_loads = (nkb % XGROUP) == 0;
+      auto word = [&](const uint8_t* base, size_t at, int kb0) -> uint32_t {
+        if (word_loads)
+          return __ldg(reinterpret_cast<const uint32_t*>(base + at + kb0));
+        uint32_t v = 0;
 #pragma unroll
-          for (int i = 0; i < 10; ++i) v[i] = 127u;
+        for (int j = 0; j < XGROUP; ++j)
+          v |= (kb0 + j < nkb ? (uint32_t)__ldg(base + at + kb0 + j) : 127u)
+               << (8 * j);
+        return v;
+      };
+      auto fetch = [&](int g, uint32_t (&v)[10]) {
+        const int kb0 = g * XGROUP;
+        if (kb0 >= nkb) {
+#pragma unroll
+          for (int i = 0; i < 10; ++i) v[i] = 0x7F7F7F7Fu;
           return;
         }
-        v[0] = __ldg(sa + (size_t)blk_a * nkb + kb);
-        v[1] = b_live ? __ldg(sb + (size_t)blk_b * nkb + kb) : 127u;
+        v[0] = word(sa, (size_t)blk_a * nkb, kb0);
+        v[1] = b_live ? word(sb, (size_t)blk_b * nkb, kb0) : 0x7F7F7F7Fu;
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
           const int n = 32 * c + lane;
-          v[2 + c] =
-              n < w.rows ? __ldg(ts + (size_t)(w.row0 + n) * nkb + kb) : 127u;
+          v[2 + c] = n < w.rows ? word(ts, (size_t)(w.row0 + n) * nkb, kb0)
+                                : 0x7F7F7F7Fu;
         }
       };
-      uint32_t v0[10], v1[10], v2[10];
+      uint32_t v0[10], v1[10];
       fetch(0, v0);
-      fetch(1, v1);
       bool ok = true;
       for (int kb = 0; kb < nkb; ++kb) {
-        fetch(kb + 2, v2);
         int okw = 1;
         if (lane == 0)
           okw = mbar_wait_bounded(smem_u32(&kempty[stage]), phase ^ 1,
@@ -409,23 +426,25 @@ __global__ void __launch_bounds__(XTHREADS, 1)
           ok = false;
           break;
         }
-        uint8_t* sf = sF + stage * XSF_BYTES;
-        const uint32_t wa4 = v0[0] * 0x01010101u, wb4 = v0[1] * 0x01010101u;
-        reinterpret_cast<uint4*>(sf)[lane] = make_uint4(wa4, wa4, wa4, wa4);
-        reinterpret_cast<uint4*>(sf + 512)[lane] =
-            make_uint4(wb4, wb4, wb4, wb4);
-        // token columns 128 t .. 128 t + 127: lane holds rows lane + 32 c
-        reinterpret_cast<uint4*>(sf + 1024)[lane] =
-            make_uint4(v0[2] * 0x01010101u, v0[3] * 0x01010101u,
-                       v0[4] * 0x01010101u, v0[5] * 0x01010101u);
-        if (w.n > 128)
-          reinterpret_cast<uint4*>(sf + 1536)[lane] =
-              make_uint4(v0[6] * 0x01010101u, v0[7] * 0x01010101u,
-                         v0[8] * 0x01010101u, v0[9] * 0x01010101u);
+        if (kb % XGROUP == 0) {
+          // a new group: its atoms into ring entry sfg % XSF_RING (the
+          // entry's previous group started >= XSF_RING k-blocks ago, so
+          // the kempty wait above has seen its copies complete)
+          fetch(kb / XGROUP + 1, v1);
+          uint8_t* sf = sF + (sfg % XSF_RING) * XSF_BYTES;
+          reinterpret_cast<uint4*>(sf)[lane] =
+              make_uint4(v0[0], v0[0], v0[0], v0[0]);
+          reinterpret_cast<uint4*>(sf + 512)[lane] =
+              make_uint4(v0[1], v0[1], v0[1], v0[1]);
+          // token columns 128 t .. 128 t + 127: lane holds rows lane + 32 c
+          reinterpret_cast<uint4*>(sf + 1024)[lane] =
+              make_uint4(v0[2], v0[3], v0[4], v0[5]);
+          if (w.n > 128)
+            reinterpret_cast<uint4*>(sf + 1536)[lane] =
+                make_uint4(v0[6], v0[7], v0[8], v0[9]);
 #pragma unroll
-        for (int i = 0; i < 10; ++i) {
-          v0[i] = v1[i];
-          v1[i] = v2[i];
+          for (int i = 0; i < 10; ++i) v0[i] = v1[i];
+          ++sfg;
         }
         fence_proxy_async_smem();
         __syncwarp();
@@ -465,7 +484,7 @@ __global__ void __launch_bounds__(XTHREADS, 1)
       // ----------------------------------------------------------- MMA
       uint32_t wstage = 0, wphase = 0, kstage = 0, kphase = 0;
       uint32_t tph = 0;  // bit s: parity of the uses of TMEM slot s so far
-      uint32_t kglob = 0;
+      uint32_t sfg = 0;  // atom groups copied so far
       int slot = 0;
       bool any = false;
       for (int u = blockIdx.x; u < total; u += gridDim.x) {
@@ -486,7 +505,8 @@ __global__ void __launch_bounds__(XTHREADS, 1)
         const uint32_t db = wide ? tmem_base + s1 * XSLOT : da + XNARROW;
         const uint32_t idesc = idesc_mx_e4m3(XM, w.n);
         bool ok = true;
-        for (int kb = 0; kb < nkb; ++kb, ++kglob) {
+        uint32_t sfc = 0;
+        for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait_bounded(smem_u32(&wfull[wstage]), wphase,
                                  abort_flag, limit, p.status,
                                  kMxSiteMmaFull) ||
@@ -497,18 +517,24 @@ __global__ void __launch_bounds__(XTHREADS, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t sfc = tmem_base + XSF_COL0 + XSF_SET * (kglob & 1);
-          const uint32_t sf = smem_u32(sF + kstage * XSF_BYTES);
-          tc_cp_atom(sfc, sf);               // weight tile a
-          tc_cp_atom(sfc + 8, sf + 512);     // weight tile b
-          tc_cp_atom(sfc + 16, sf + 1024);   // token columns 0..127
-          if (w.n > 128) tc_cp_atom(sfc + 20, sf + 1536);  // 128..
+          if (kb % XGROUP == 0) {
+            // the group's atoms (written before this k-block's kfull
+            // arrive) into one of two tensor-memory scale sets
+            sfc = tmem_base + XSF_COL0 + XSF_SET * (sfg & 1);
+            const uint32_t sf = smem_u32(sF + (sfg % XSF_RING) * XSF_BYTES);
+            tc_cp_atom(sfc, sf);               // weight tile a
+            tc_cp_atom(sfc + 8, sf + 512);     // weight tile b
+            tc_cp_atom(sfc + 16, sf + 1024);   // token columns 0..127
+            if (w.n > 128) tc_cp_atom(sfc + 20, sf + 1536);  // 128..
+            ++sfg;
+          }
           const uint32_t s0 = smem_u32(sW + wstage * XWSTAGE);
           const uint32_t st = smem_u32(sT + kstage * TSTAGE);
+          // every slice of this k-block reads byte kb % 4 of the atoms
+          const uint32_t id = idesc_slice(idesc, kb % XGROUP);
 #pragma unroll
           for (int kk = 0; kk < XK / XUMMA_K; ++kk) {
             const uint64_t bdesc = sw128_kmajor_desc(st + kk * XUMMA_K);
-            const uint32_t id = idesc_slice(idesc, kk);
             const uint32_t acc = (kb | kk) != 0;
             tc_mma_mx(da, sw128_kmajor_desc(s0 + kk * XUMMA_K), bdesc, id,
                       sfc, sfc + 16, acc);
