@@ -158,12 +158,15 @@ def router_extra_launches(T, H, E):
     the 148 SMs)."""
     if E % 16:
         return 0
-    bn = 64 if E % 64 == 0 else (32 if E % 32 == 0 else 16)
+    if T >= 1024 and E % 128 == 0:
+        bn = 256 if E % 256 == 0 else 128
+    else:
+        bn = 64 if E % 64 == 0 else (32 if E % 32 == 0 else 16)
     units = -(-T // 128) * (E // bn)
     nkb = H // 64
     if 2 * units > 148 or nkb // 4 < 2:
         return 1
-    ks = min(-(-148 // units), nkb // 4)
+    ks = min(148 // units, nkb // 4)
     kper = -(-nkb // ks)
     return 2 if -(-nkb // kper) > 1 else 1
 

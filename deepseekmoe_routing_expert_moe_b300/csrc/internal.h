@@ -216,7 +216,7 @@ int launch_router_logits_tc(const uint16_t* x, const uint16_t* w_split,
                             float* partial, int T, int H, int E,
                             DevStatus* status, uint64_t wait_limit_ns,
                             cudaStream_t s);
-int router_tile_n(int E);  // 0 if the tensor-core path does not apply
+int router_tile_n(int T, int E);  // 0: the tensor-core path does not apply
 int router_ksplit(int T, int H, int E);  // k ranges of the router GEMM
 // (routing.cu) the exact split itself
 cudaError_t launch_split_router_weight(const float* w, int E, int H,

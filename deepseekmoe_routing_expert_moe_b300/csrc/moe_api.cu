@@ -306,7 +306,7 @@ moe_status_t router_logits_launch(const moe_dims_t* d, const uint16_t* x,
                                   const float* offset, float* logits,
                                   uint16_t* w_split, float* partial,
                                   DevStatus* st, cudaStream_t s) {
-  if (moe::router_tile_n(d->E) == 0)
+  if (moe::router_tile_n(d->T, d->E) == 0)
     return cuda_ok(moe::launch_router_logits(x, w_router, offset, logits,
                                              d->T, d->H, d->E, s));
   MOE_TRY(cuda_ok(moe::launch_split_router_weight(w_router, d->E, d->H,

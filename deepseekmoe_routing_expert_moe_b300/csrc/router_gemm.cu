@@ -39,7 +39,7 @@ constexpr int BK = 64;         // K per stage: 64 bf16 = one 128 B row
 constexpr int UMMA_K = 16;     // K of one kind::f16 MMA
 constexpr int kThreads = 192;  // 6 warps
 constexpr int kParts = 3;      // W = hi + mid + lo
-constexpr int kStages = 4;
+
 constexpr uint64_t kDrainNs = 2000000000ull;
 
 enum {
@@ -66,6 +66,8 @@ template <int BN>
 struct RShape {
   static constexpr uint32_t A_BYTES = BM * BK * 2;
   static constexpr uint32_t B_BYTES = kParts * BN * BK * 2;
+  // ring depth: as deep as 227 KB of shared memory allows
+  static constexpr int STAGES = BN >= 256 ? 2 : (BN >= 128 ? 3 : 4);
   static constexpr uint32_t TMEM_COLS = (2 * BN < 32) ? 32 : 2 * BN;
   static constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
 };
@@ -78,21 +80,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
-  uint8_t* sB = smem + kStages * S::A_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + kStages * S::B_BYTES);
+  uint8_t* sB = smem + S::STAGES * S::A_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + S::STAGES * S::B_BYTES);
   uint64_t* full = bars;
-  uint64_t* empty = bars + kStages;
-  uint64_t* tfull = bars + 2 * kStages;
-  uint64_t* tempty = bars + 2 * kStages + 2;
-  uint64_t* drain = bars + 2 * kStages + 4;
+  uint64_t* empty = bars + S::STAGES;
+  uint64_t* tfull = bars + 2 * S::STAGES;
+  uint64_t* tempty = bars + 2 * S::STAGES + 2;
+  uint64_t* drain = bars + 2 * S::STAGES + 4;
   volatile uint32_t* misc =
-      reinterpret_cast<volatile uint32_t*>(bars + 2 * kStages + 5);
+      reinterpret_cast<volatile uint32_t*>(bars + 2 * S::STAGES + 5);
   // misc[0] TMEM base, misc[1] abort flag
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kStages; ++i) {
+    for (int i = 0; i < S::STAGES; ++i) {
       mbar_init(smem_u32(&full[i]), 1);
       mbar_init(smem_u32(&empty[i]), 1);
     }
@@ -150,16 +152,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 smem_u32(sB + stage * S::B_BYTES + part * BN * BK * 2),
                 &p.w_map, kb * BK, part * p.E + n * BN, fb, pol);
           ++issued;
-          if (++stage == kStages) {
+          if (++stage == S::STAGES) {
             stage = 0;
             phase ^= 1;
           }
         }
         if (!ok) break;
       }
-      const uint32_t first = issued > kStages ? issued - kStages : 0;
+      const uint32_t first = issued > S::STAGES ? issued - S::STAGES : 0;
       for (uint32_t i = first; i < issued; ++i)
-        mbar_wait_bounded(smem_u32(&full[i % kStages]), (i / kStages) & 1,
+        mbar_wait_bounded(smem_u32(&full[i % S::STAGES]), (i / S::STAGES) & 1,
                           nullptr, kDrainNs, p.status, kSiteDrain);
     }
     __syncwarp();
@@ -201,7 +203,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           any = true;
           tc_commit(smem_u32(&empty[stage]));
-          if (++stage == kStages) {
+          if (++stage == S::STAGES) {
             stage = 0;
             phase ^= 1;
           }
@@ -287,8 +289,8 @@ __global__ void router_reduce_kernel(const float* __restrict__ partial,
 template <int BN>
 size_t router_smem_bytes() {
   using S = RShape<BN>;
-  return 1024 + kStages * (S::A_BYTES + S::B_BYTES) +
-         (2 * kStages + 5) * sizeof(uint64_t) + 4 * sizeof(uint32_t);
+  return 1024 + S::STAGES * (S::A_BYTES + S::B_BYTES) +
+         (2 * S::STAGES + 5) * sizeof(uint64_t) + 4 * sizeof(uint32_t);
 }
 
 template <int BN>
@@ -305,14 +307,14 @@ int launch_router(const RouterParams& rp, cudaStream_t s) {
 }  // namespace
 
 int router_ksplit(int T, int H, int E) {
-  const int bn = router_tile_n(E);
+  const int bn = router_tile_n(T, E);
   if (bn == 0 || T <= 0) return 1;
   const int units = ((T + BM - 1) / BM) * (E / bn);
-  // split only when the plain grid leaves most SMs idle (measured on B300:
-  // T=128 95 -> 43 us; at T=4096, 128 units, a 3-way split was slower)
+  // split only when the plain grid leaves most SMs idle, into as many
+  // ranges as keep the units within one wave
   const int sms = 148;
   if (2 * units > sms) return 1;
-  const int ks = (sms + units - 1) / units;
+  const int ks = sms / units;
   const int nkb = H / BK;
   const int max_ks = nkb / 4;  // at least 4 k-blocks per unit
   int k = ks < 1 ? 1 : (ks > max_ks ? (max_ks < 1 ? 1 : max_ks) : ks);
@@ -321,7 +323,17 @@ int router_ksplit(int T, int H, int E) {
   return (nkb + kper - 1) / kper;
 }
 
-int router_tile_n(int E) {
+// Experts per tile.  Every tile costs the same three MMAs per 16-wide
+// k-step whatever its width (up to 256 columns the tensor core's issue, not
+// its arithmetic, sets an MMA's time), so wide tiles cut the router's MMA
+// count when the token tiles alone fill the SMs (measured on B300 at 4096
+// tokens: 111 -> 88 us live); a decode batch keeps 64-wide tiles, split
+// over k (54 vs 65 us).
+int router_tile_n(int T, int E) {
+  if (T >= 1024) {
+    if (E % 256 == 0) return 256;
+    if (E % 128 == 0) return 128;
+  }
   if (E % 64 == 0) return 64;
   if (E % 32 == 0) return 32;
   if (E % 16 == 0) return 16;
@@ -333,7 +345,7 @@ int launch_router_logits_tc(const uint16_t* x, const uint16_t* w_split,
                             float* partial, int T, int H, int E,
                             DevStatus* status, uint64_t wait_limit_ns,
                             cudaStream_t s) {
-  const int bn = router_tile_n(E);
+  const int bn = router_tile_n(T, E);
   if (bn == 0) return MOE_ERR_UNSUPPORTED;
   RouterParams rp;
   std::memset(&rp, 0, sizeof(rp));
@@ -352,6 +364,12 @@ int launch_router_logits_tc(const uint16_t* x, const uint16_t* w_split,
   rp.H = H;
   int rc;
   switch (bn) {
+    case 256:
+      rc = launch_router<256>(rp, s);
+      break;
+    case 128:
+      rc = launch_router<128>(rp, s);
+      break;
     case 64:
       rc = launch_router<64>(rp, s);
       break;

@@ -70,12 +70,19 @@ def test_committed_traffic_entries_name_existing_sources():
         assert e["dram_bytes_per_launch"] > 0
 
 
-@pytest.mark.parametrize("T,extra", [(4096, 1), (16384, 1), (128, 2),
+@pytest.mark.parametrize("T,extra", [(4096, 2), (16384, 1), (128, 2),
                                      (512, 2), (32768, 1)])
 def test_router_extra_launches(T, extra):
-    """The weight split always; the split-K sum only when the 128-token
-    tiles would fill fewer than half of the 148 SMs."""
+    """The weight split always; the split-K sum only when the router's
+    tiles (256 experts wide from 1024 tokens, else 64) would fill fewer than
+    half of the 148 SMs -- the same decision as the library's, which
+    reserves the partial sums in the router workspace exactly then."""
     assert bench.router_extra_launches(T, 7168, 256) == extra
+    from deepseekmoe_routing_expert_moe_b300 import ops
+    d = ops.dims(T, 7168, 256, 8, 4, 8, 2048, 2048, 0.001)
+    ws = ops.workspace_bytes(d, ops.MOE_WS_ROUTER_LOGITS)
+    split_parts = 256 + 3 * 256 * 7168 * 2   # status word + the bf16 parts
+    assert (ws > split_parts + 4096) == (extra == 2)
 
 
 def test_gpu_index_for_smi(monkeypatch):
