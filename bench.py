@@ -151,13 +151,14 @@ def ncu_traffic(kernel: str, workload: str):
         return None
 
 
-def router_extra_launches(T, H, E):
+def router_extra_launches(T, H, E, presplit=False):
     """Launches of the router logits beyond one: the weight split on the
-    tensor-core path, and the partial-sum kernel when the library splits
-    the reduction over H (when the 128-token tiles fill fewer than half of
-    the 148 SMs)."""
+    tensor-core path (none when the weights carry a prepared split), and
+    the partial-sum kernel when the library splits the reduction over H
+    (when the router's tiles fill fewer than half of the 148 SMs)."""
     if E % 16:
         return 0
+    split = 0 if presplit else 1
     if T >= 1024 and E % 128 == 0:
         bn = 256 if E % 256 == 0 else 128
     else:
@@ -165,10 +166,10 @@ def router_extra_launches(T, H, E):
     units = -(-T // 128) * (E // bn)
     nkb = H // 64
     if 2 * units > 148 or nkb // 4 < 2:
-        return 1
+        return split
     ks = min(148 // units, nkb // 4)
     kper = -(-nkb // ks)
-    return 2 if -(-nkb // kper) > 1 else 1
+    return split + (1 if -(-nkb // kper) > 1 else 0)
 
 
 # ------------------------------------------------------------ CPU oracle
@@ -296,7 +297,10 @@ def run_gpu(args, rank, world, local_rank):
     # router's additive term (zero preference: no term)
     pref = (torch.from_numpy(inputs.zipf_preference(cfg)).cuda()
             if cfg.zipf_s > 0 else None)
-    W = ops.Weights(wr, w1, w3, w2, ws1, ws3, ws2, router_offset=pref)
+    # the router weight's bf16 split made once, as deployed weights would
+    # carry it (moe_router_weight_split)
+    W = ops.Weights(wr, w1, w3, w2, ws1, ws3, ws2,
+                    router_offset=pref).with_router_split()
     # fresh seeded tokens every step for the skewed run (its config asks
     # for them; up to its 50 steps), 4 rotating batches otherwise
     NB = min(max(args.steps, 4), cfg.steps) if cfg.zipf_s > 0 else 4
@@ -440,13 +444,14 @@ def run_gpu(args, rank, world, local_rank):
                 "d2h_bytes_per_step": T * H * 2,
                 "overlap": "uploads/downloads on their own streams, "
                            "double-buffered"},
-        # router logits are two launches (weight split + GEMM) on the
-        # tensor-core path (E % 16 == 0), three when its k ranges are split
-        # (few 128-token tiles: the partial sums are added by a kernel);
-        # the dispatch copy is a launch only at >= 64 rows per expert (below
-        # that the up GEMM gathers the rows from x itself)
+        # the router logits are one launch (the weights carry their
+        # prepared bf16 split), two when its k ranges are split (the partial
+        # sums are added by a kernel); the dispatch copy is a launch only at
+        # >= 64 rows per expert (below that the up GEMM gathers the rows
+        # from x itself)
         "gpu_launches": (nk - (0 if T * K >= 64 * E else 1)
-                         + router_extra_launches(T, H, E)) * args.steps,
+                         + router_extra_launches(T, H, E, presplit=True))
+                        * args.steps,
         "clocks": clocks,
         "kernels_ms": kernels,
         "experts_touched": touched,

@@ -257,6 +257,7 @@ moe_status_t check_weights(const moe_weights_t* w) {
   MOE_NEED(w->ws2);
   MOE_ALIGN(w->w_router);
   MOE_ALIGN(w->router_offset);
+  MOE_ALIGN(w->router_split);
   MOE_ALIGN(w->w1);
   MOE_ALIGN(w->w3);
   MOE_ALIGN(w->w2);
@@ -301,19 +302,23 @@ moe_status_t ffn_launch(const moe_dims_t* d, const moe_weights_t* w,
 
 // z = x W_r^T (+ offset): tensor cores (exact bf16 split of W_r) when
 // E % 16 == 0, else the fp32 SIMT kernel
+// (presplit: the caller's moe_router_weight_split of w_router, or NULL:
+// split into w_split now)
 moe_status_t router_logits_launch(const moe_dims_t* d, const uint16_t* x,
                                   const float* w_router,
                                   const float* offset, float* logits,
                                   uint16_t* w_split, float* partial,
-                                  DevStatus* st, cudaStream_t s) {
+                                  DevStatus* st, cudaStream_t s,
+                                  const uint16_t* presplit = nullptr) {
   if (moe::router_tile_n(d->T, d->E) == 0)
     return cuda_ok(moe::launch_router_logits(x, w_router, offset, logits,
                                              d->T, d->H, d->E, s));
-  MOE_TRY(cuda_ok(moe::launch_split_router_weight(w_router, d->E, d->H,
-                                                  w_split, s)));
+  if (presplit == nullptr)
+    MOE_TRY(cuda_ok(moe::launch_split_router_weight(w_router, d->E, d->H,
+                                                    w_split, s)));
   return static_cast<moe_status_t>(moe::launch_router_logits_tc(
-      x, w_split, offset, logits, partial, d->T, d->H, d->E, st,
-      g_wait_limit_ns, s));
+      x, presplit ? presplit : w_split, offset, logits, partial, d->T, d->H,
+      d->E, st, g_wait_limit_ns, s));
 }
 
 }  // namespace
@@ -321,6 +326,19 @@ moe_status_t router_logits_launch(const moe_dims_t* d, const uint16_t* x,
 extern "C" {
 
 int32_t moe_abi_version(void) { return MOE_ABI_VERSION; }
+
+moe_status_t moe_router_weight_split(const float* w_router, int32_t E,
+                                     int32_t H, uint16_t* split,
+                                     moe_stream_t stream) {
+  if (E <= 0 || H <= 0) return MOE_ERR_INVALID_ARG;
+  if (E % 16 != 0) return MOE_ERR_UNSUPPORTED;
+  MOE_NEED(w_router);
+  MOE_NEED(split);
+  MOE_ALIGN(w_router);
+  MOE_ALIGN(split);
+  return cuda_ok(
+      moe::launch_split_router_weight(w_router, E, H, split, cs(stream)));
+}
 
 const char* moe_status_string(moe_status_t s) {
   switch (s) {
@@ -1092,7 +1110,8 @@ moe_status_t moe_forward(const moe_dims_t* d, const moe_weights_t* w,
   MOE_TRY(router_logits_launch(
       d, x, w->w_router, w->router_offset, logits,
       at<uint16_t>(ws, L.w_split),
-      L.r_partial ? at<float>(ws, L.r_partial) : nullptr, st, s));
+      L.r_partial ? at<float>(ws, L.r_partial) : nullptr, st, s,
+      w->router_split));
   prof_mark(1, s);
   MOE_TRY(cuda_ok(moe::launch_route(logits, bias, T, E, d->n_group,
                                     d->topk_group, K, idx, gate, bc, s)));

@@ -43,7 +43,7 @@ class MoeDims(ctypes.Structure):
 class MoeWeights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in
                 ("w_router", "w1", "w3", "w2", "ws1", "ws3", "ws2",
-                 "router_offset")]
+                 "router_offset", "router_split")]
 
 
 class MoeWeightsFp8(ctypes.Structure):
@@ -106,6 +106,8 @@ _SIGS = {
     "moe_set_wait_timeout_ns": (None, [ctypes.c_uint64]),
     "moe_set_gemm_ctas": (None, [ctypes.c_int32]),
     "moe_abi_version": (ctypes.c_int32, []),
+    "moe_router_weight_split": (_I, [_P, ctypes.c_int32, ctypes.c_int32,
+                                     _P, _P]),
     "moe_set_profile_events": (None, [ctypes.POINTER(ctypes.c_void_p),
                                        ctypes.c_int32]),
 }
@@ -171,13 +173,25 @@ class Weights:
     """Device weights of one layer (torch tensors; bf16 stored as int16)."""
 
     def __init__(self, w_router, w1, w3, w2, ws1, ws3, ws2,
-                 router_offset=None):
+                 router_offset=None, router_split=None):
         self.w_router, self.w1, self.w3, self.w2 = w_router, w1, w3, w2
         self.ws1, self.ws3, self.ws2 = ws1, ws3, ws2
         self.router_offset = router_offset
+        self.router_split = router_split
         self.struct = MoeWeights(*(_ptr(t) for t in (w_router, w1, w3, w2,
                                                       ws1, ws3, ws2,
-                                                      router_offset)))
+                                                      router_offset,
+                                                      router_split)))
+
+    def with_router_split(self, stream=None):
+        """The same weights with the router weight's bf16 split made once
+        (moe_router_weight_split), so moe_forward does not redo it."""
+        E, H = self.w_router.shape
+        split = torch.empty((3, E, H), dtype=torch.int16,
+                            device=self.w_router.device)
+        moe_router_weight_split(self.w_router, split, stream)
+        return Weights(self.w_router, self.w1, self.w3, self.w2, self.ws1,
+                       self.ws3, self.ws2, self.router_offset, split)
 
 
 class WeightsFp8:
@@ -496,6 +510,13 @@ def moe_set_profile_events(events):
 
 def moe_status_string(code: int) -> str:
     return lib().moe_status_string(code).decode()
+
+
+def moe_router_weight_split(w_router, split, stream=None):
+    """w_router [E, H] fp32 -> split [3, E, H] bf16 (as int16)."""
+    E, H = w_router.shape
+    _check("moe_router_weight_split", lib().moe_router_weight_split(
+        _ptr(w_router), E, H, _ptr(split), _stream(stream)))
 
 
 def moe_abi_version() -> int:

@@ -53,7 +53,7 @@
 extern "C" {
 #endif
 
-#define MOE_ABI_VERSION 2
+#define MOE_ABI_VERSION 3
 
 typedef enum {
   MOE_OK = 0,
@@ -97,6 +97,11 @@ typedef struct {
  *   w3       [E, I, H] bf16   up projection
  *   w2       [E, H, I] bf16   down projection
  *   ws1 [I_shared, H], ws3 [I_shared, H], ws2 [H, I_shared]: shared expert
+ *   router_split [3, E, H] bf16  optional (NULL = none): the exact bf16
+ *                             split of w_router that moe_router_weight_split
+ *                             wrote; with it moe_forward does not split the
+ *                             router weight again on every call.  It must
+ *                             be the split of this w_router (not checked).
  */
 typedef struct {
   const float* w_router;
@@ -107,6 +112,7 @@ typedef struct {
   const uint16_t* ws3;
   const uint16_t* ws2;
   const float* router_offset;
+  const uint16_t* router_split;
 } moe_weights_t;
 
 /* Which entry point a workspace is sized for. */
@@ -144,6 +150,16 @@ moe_status_t moe_router_logits(const moe_dims_t* d, const uint16_t* x,
                                const float* router_offset, float* logits,
                                void* ws, size_t ws_bytes,
                                moe_stream_t stream);
+
+/* The router weight's exact three-way bf16 split, done once for weights
+ * that do not change between calls: w_router [E, H] fp32 -> split
+ * [3, E, H] bf16 (hi, mid, lo; hi + mid + lo == w_router for every normal
+ * value, the parts moe_router_logits forms in its workspace).  E % 16 == 0
+ * (the tensor-core path; MOE_ERR_UNSUPPORTED otherwise), H > 0.  Pass the
+ * result as moe_weights_t.router_split.  Needs no workspace. */
+moe_status_t moe_router_weight_split(const float* w_router, int32_t E,
+                                     int32_t H, uint16_t* split,
+                                     moe_stream_t stream);
 
 /* Routing from precomputed logits ("02 · DeepSeek-V3" §1.3, §1.4):
  * sigmoid, + bias for selection, group-limited top-K, gates renormalised

@@ -42,7 +42,7 @@ def test_library_exports_every_declared_symbol(L):
 
 
 def test_abi_version_and_status_strings(L):
-    assert ops.moe_abi_version() == 2
+    assert ops.moe_abi_version() == 3
     for code, name in ops.STATUS.items():
         assert ops.moe_status_string(code) == name
 
@@ -136,6 +136,22 @@ def test_ffn_and_forward_validation(L):
                          None) == 3
     assert L.moe_router_logits(ctypes.byref(d), FAKE, FAKE, FAKE + 8, FAKE,
                                FAKE, 1 << 40, None) == 3
+    # ... and so must the optional prepared router split
+    w = ops.MoeWeights(*(FAKE,) * 7, None, FAKE + 2)
+    assert L.moe_forward(ctypes.byref(d), ctypes.byref(w), FAKE, FAKE, 0,
+                         FAKE, None, None, None, None, None, FAKE, 1 << 40,
+                         None) == 3
+
+
+def test_router_weight_split_validation(L):
+    rs = L.moe_router_weight_split
+    assert rs(FAKE, 0, 7168, FAKE, None) == 1
+    assert rs(FAKE, 256, 0, FAKE, None) == 1
+    assert rs(FAKE, 200, 7168, FAKE, None) == 2       # E % 16: no split
+    assert rs(None, 256, 7168, FAKE, None) == 1
+    assert rs(FAKE, 256, 7168, None, None) == 1
+    assert rs(FAKE + 4, 256, 7168, FAKE, None) == 3
+    assert rs(FAKE, 256, 7168, FAKE + 8, None) == 3
 
 
 def _balance(L, d, seq_len=4096, alpha=1e-4, logits=FAKE, out=FAKE,

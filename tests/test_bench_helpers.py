@@ -78,6 +78,8 @@ def test_router_extra_launches(T, extra):
     half of the 148 SMs -- the same decision as the library's, which
     reserves the partial sums in the router workspace exactly then."""
     assert bench.router_extra_launches(T, 7168, 256) == extra
+    assert bench.router_extra_launches(T, 7168, 256, presplit=True) == \
+        extra - 1
     from deepseekmoe_routing_expert_moe_b300 import ops
     d = ops.dims(T, 7168, 256, 8, 4, 8, 2048, 2048, 0.001)
     ws = ops.workspace_bytes(d, ops.MOE_WS_ROUTER_LOGITS)

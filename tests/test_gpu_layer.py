@@ -209,3 +209,43 @@ def test_forward_replays_from_a_cuda_graph():
         outs[mode] = (host(out), host(bias))
     assert np.array_equal(outs["eager"][0], outs["graph"][0])
     assert np.array_equal(f32_bits(outs["eager"][1]), f32_bits(outs["graph"][1]))
+
+
+@pytest.mark.parametrize("T,E,K", [(96, 16, 4), (37, 32, 6), (256, 8, 4)])
+def test_forward_equals_the_public_calls_bit_for_bit(T, E, K):
+    """moe_forward against the same layer composed from the public calls,
+    which copy the routed rows out (moe_permute with xp) before the grouped
+    GEMMs.  Below 64 rows per expert moe_forward instead gathers the rows
+    from x inside the up GEMM (TMA gather4, ragged chunks padded by
+    repeating the last row); above, it copies them too.  The GEMMs
+    accumulate every row in the same order either way, so the outputs must
+    agree bit for bit."""
+    cfg = inputs.custom_config("gather", 1000 + T, T=T, H=384, E=E,
+                               n_group=4, topk_group=2, topk=K, I=256,
+                               I_shared=128, router_sigma=0.05)
+    w, W = host_weights(cfg)
+    d = ops.dims_of(cfg)
+    H = cfg.H
+    x = dev(w["x"])
+    ws = ops.workspace(d, ops.MOE_WS_FORWARD)
+    out_f = torch.zeros((T, H), dtype=torch.int16, device="cuda")
+    ops.moe_forward(d, W, x, dev(w["bias"]), out_f, ws, update_bias=False)
+    assert ops.moe_get_device_error(ws) == 0
+    z = torch.zeros((T, E), dtype=torch.float32, device="cuda")
+    idx = torch.zeros((T, K), dtype=torch.int32, device="cuda")
+    gate = torch.zeros((T, K), dtype=torch.float32, device="cuda")
+    counts = torch.zeros(E, dtype=torch.int32, device="cuda")
+    off = torch.zeros(E + 1, dtype=torch.int32, device="cuda")
+    dest = torch.zeros((T, K), dtype=torch.int32, device="cuda")
+    src = torch.zeros(T * K, dtype=torch.int32, device="cuda")
+    xp = torch.zeros((T * K, H), dtype=torch.int16, device="cuda")
+    yp = torch.zeros((T * K, H), dtype=torch.int16, device="cuda")
+    ys = torch.zeros((T, H), dtype=torch.int16, device="cuda")
+    out_c = torch.zeros((T, H), dtype=torch.int16, device="cuda")
+    ops.moe_router_logits(d, x, W.w_router, z, ws)
+    ops.moe_route(d, z, dev(w["bias"]), idx, gate, counts, ws)
+    ops.moe_permute(d, x, idx, off, dest, src, xp, ws)
+    ops.moe_expert_ffn(d, W, xp, x, off, yp, ys, ws)
+    ops.moe_combine(d, x, ys, yp, dest, gate, out_c)
+    assert ops.moe_get_device_error(ws) == 0
+    assert torch.equal(out_f, out_c)

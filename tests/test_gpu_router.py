@@ -78,3 +78,47 @@ def test_router_logits_with_offset(E, G):
                                router_sigma=0.05)
     r = np.random.default_rng(E).permutation(E) + 1
     check_logits(cfg, offset=(1.0 * r ** -1.2).astype(np.float32))
+
+
+def _bf16_rn(v):
+    """fp32 -> nearest bf16 (ties to even), as fp32 (finite inputs)."""
+    b = np.asarray(v, np.float32).view(np.uint32).astype(np.uint64)
+    r = (b + 0x7FFF + ((b >> 16) & 1)) >> 16
+    return (r << 16).astype(np.uint32).view(np.float32)
+
+
+def test_router_weight_split_is_exact_and_reused_by_the_forward():
+    """moe_router_weight_split writes hi = bf16(w), mid = bf16(w - hi),
+    lo = bf16(w - hi - mid) (each residual exact in fp32), whose sum is w
+    exactly; and moe_forward given that split (no per-call split) produces
+    the same layer output, bit for bit, as moe_forward that splits."""
+    cfg = inputs.custom_config("split", 1010, T=300, H=512, E=32, n_group=4,
+                               topk_group=2, topk=4, I=128, I_shared=128,
+                               router_sigma=0.05)
+    w = inputs.router_weight(cfg)
+    split = torch.zeros((3, cfg.E, cfg.H), dtype=torch.int16, device="cuda")
+    ops.moe_router_weight_split(dev(w), split)
+    parts = inputs.bf16_bits_to_f32(host(split, np.uint16))
+    hi = _bf16_rn(w)
+    mid = _bf16_rn(w - hi)
+    lo = _bf16_rn((w - hi) - mid)
+    np.testing.assert_array_equal(parts[0], hi)
+    np.testing.assert_array_equal(parts[1], mid)
+    np.testing.assert_array_equal(parts[2], lo)
+    total = (parts[0].astype(np.float64) + parts[1] + parts[2])
+    np.testing.assert_array_equal(total, w.astype(np.float64))
+    lw = inputs.layer_inputs(cfg)
+    W = ops.Weights(dev(lw["w_router"]), dev(lw["w1"]), dev(lw["w3"]),
+                    dev(lw["w2"]), dev(lw["ws1"]), dev(lw["ws3"]),
+                    dev(lw["ws2"]))
+    Wp = W.with_router_split()
+    d = ops.dims_of(cfg)
+    outs = []
+    for ww in (W, Wp):
+        out = torch.zeros((cfg.T, cfg.H), dtype=torch.int16, device="cuda")
+        ws = ops.workspace(d, ops.MOE_WS_FORWARD)
+        ops.moe_forward(d, ww, dev(lw["x"]), dev(lw["bias"]), out, ws,
+                        update_bias=False)
+        assert ops.moe_get_device_error(ws) == 0
+        outs.append(out)
+    assert torch.equal(outs[0], outs[1])
