@@ -78,7 +78,10 @@ __global__ void __launch_bounds__(kPlanThreads)
 }
 
 // inverse = 0: out[perm[i]] = in[i]; inverse = 1: out[i] = in[perm[i]];
-// rows of row_bytes (a multiple of 16), one block per row
+// rows of row_bytes bytes in the widest unit that divides them (16-byte
+// vectors for bf16 rows and E4M3 codes; 4, 2 or 1 bytes for the rows of
+// their scale bytes, H/128 per token), one block per row
+template <typename V>
 __global__ void __launch_bounds__(128)
     ep_rows_kernel(const uint8_t* __restrict__ in, long long rows,
                    long long row_bytes, const int32_t* __restrict__ perm,
@@ -90,9 +93,10 @@ __global__ void __launch_bounds__(128)
     return;
   }
   const long long src = inverse ? p : i, dst = inverse ? i : p;
-  const uint4* a = reinterpret_cast<const uint4*>(in + src * row_bytes);
-  uint4* b = reinterpret_cast<uint4*>(out + dst * row_bytes);
-  for (long long c = threadIdx.x; c < row_bytes / 16; c += blockDim.x)
+  const V* a = reinterpret_cast<const V*>(in + src * row_bytes);
+  V* b = reinterpret_cast<V*>(out + dst * row_bytes);
+  for (long long c = threadIdx.x; c < row_bytes / (long long)sizeof(V);
+       c += blockDim.x)
     b[c] = __ldg(a + c);
 }
 
@@ -117,9 +121,20 @@ cudaError_t launch_ep_rows(const void* in, long long rows,
                            int inverse, void* out, DevStatus* st,
                            cudaStream_t s) {
   if (rows == 0) return cudaSuccess;
-  ep_rows_kernel<<<(unsigned)rows, 128, 0, s>>>(
-      static_cast<const uint8_t*>(in), rows, row_bytes, perm, inverse,
-      static_cast<uint8_t*>(out), st);
+  const uint8_t* a = static_cast<const uint8_t*>(in);
+  uint8_t* b = static_cast<uint8_t*>(out);
+  if (row_bytes % 16 == 0)
+    ep_rows_kernel<uint4><<<(unsigned)rows, 128, 0, s>>>(
+        a, rows, row_bytes, perm, inverse, b, st);
+  else if (row_bytes % 4 == 0)
+    ep_rows_kernel<uint32_t><<<(unsigned)rows, 128, 0, s>>>(
+        a, rows, row_bytes, perm, inverse, b, st);
+  else if (row_bytes % 2 == 0)
+    ep_rows_kernel<uint16_t><<<(unsigned)rows, 128, 0, s>>>(
+        a, rows, row_bytes, perm, inverse, b, st);
+  else
+    ep_rows_kernel<uint8_t><<<(unsigned)rows, 128, 0, s>>>(
+        a, rows, row_bytes, perm, inverse, b, st);
   return cudaGetLastError();
 }
 

@@ -372,9 +372,10 @@ size_t moe_workspace_bytes(const moe_dims_t* d, moe_ws_kind_t which) {
                    which == MOE_WS_EXPERT_BWD ||
                    which == MOE_WS_EXPERT_FFN_MX;
   if (which < MOE_WS_ROUTE || which > MOE_WS_EXPERT_FFN_MX) return 0;
-  // the expert GEMMs alone (moe_expert_ffn, moe_expert_ffn_routed) do not
-  // route: their workspace takes any expert count
-  if (which == MOE_WS_EXPERT_FFN) {
+  // the expert GEMMs alone (moe_expert_ffn, moe_expert_ffn_routed and
+  // their FP8 power-of-two forms) do not route: their workspace takes any
+  // expert count
+  if (which == MOE_WS_EXPERT_FFN || which == MOE_WS_EXPERT_FFN_MX) {
     if (check_ffn_only_dims(d) != MOE_OK) return 0;
   } else if (check_dims(d, ffn) != MOE_OK) {
     return 0;
@@ -559,7 +560,7 @@ moe_status_t moe_ep_permute_rows(const void* in, int64_t rows,
                                  int64_t row_bytes, const int32_t* perm,
                                  int32_t inverse, void* out, void* ws,
                                  moe_stream_t stream) {
-  if (rows < 0 || rows >= (1ll << 31) || row_bytes <= 0 || row_bytes % 16)
+  if (rows < 0 || rows >= (1ll << 31) || row_bytes <= 0)
     return MOE_ERR_INVALID_ARG;
   if (rows == 0) return MOE_OK;
   MOE_NEED(in);
@@ -883,6 +884,58 @@ moe_status_t moe_expert_ffn_mx(const moe_dims_t* d, const moe_weights_mx_t* w,
   a.wait_limit_ns = g_wait_limit_ns;
   const int rc = moe::launch_expert_ffn_mx(a, cs(stream));
   return static_cast<moe_status_t>(rc);
+}
+
+moe_status_t moe_expert_ffn_mx_routed(const moe_dims_t* d,
+                                      const moe_weights_mx_t* w,
+                                      const uint8_t* xpq, const uint8_t* xps,
+                                      const int32_t* offsets, uint16_t* yp,
+                                      void* ws, size_t ws_bytes,
+                                      moe_stream_t stream) {
+  MOE_TRY(check_ffn_only_dims(d));
+  if (!moe::mx_ffn_supported(d->H, d->I, d->I_shared, d->E))
+    return MOE_ERR_UNSUPPORTED;
+  MOE_NEED(w);
+  const void* wp[6] = {w->w1, w->w1_scale, w->w3, w->w3_scale, w->w2,
+                       w->w2_scale};
+  for (const void* ptr : wp) {
+    MOE_NEED(ptr);
+    MOE_ALIGN(ptr);
+  }
+  MOE_NEED_T(xpq);
+  MOE_NEED_T(xps);
+  MOE_NEED(offsets);
+  MOE_NEED_T(yp);
+  MOE_ALIGN(xpq);
+  MOE_ALIGN(xps);
+  MOE_ALIGN(offsets);
+  MOE_ALIGN(yp);
+  MOE_TRY(check_ws(d, MOE_WS_EXPERT_FFN_MX, ws, ws_bytes));
+  if (d->T == 0) return MOE_OK;
+  const Layout L = layout(d, MOE_WS_EXPERT_FFN_MX);
+  moe::FfnMxArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.T = d->T;
+  a.H = d->H;
+  a.E = d->E;
+  a.topk = d->topk;
+  a.I = d->I;
+  a.I_shared = d->I_shared;
+  a.xpq = xpq;
+  a.xps = xps;
+  a.offsets = offsets;
+  a.w1 = w->w1;
+  a.w3 = w->w3;
+  a.w2 = w->w2;
+  a.w1s = w->w1_scale;
+  a.w3s = w->w3_scale;
+  a.w2s = w->w2_scale;
+  a.mq = at<uint8_t>(ws, L.mx_mq);
+  a.ms = at<uint8_t>(ws, L.mx_ms);
+  a.yp = yp;
+  a.status = at<DevStatus>(ws, 0);
+  a.wait_limit_ns = g_wait_limit_ns;
+  return static_cast<moe_status_t>(moe::launch_expert_ffn_mx(a, cs(stream)));
 }
 
 moe_status_t moe_expert_backward(const moe_dims_t* d, const moe_weights_t* w,

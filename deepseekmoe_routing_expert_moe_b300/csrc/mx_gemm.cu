@@ -770,23 +770,32 @@ int mx_ffn_supported(int H, int I, int I_shared, int E) {
 
 int launch_expert_ffn_mx(const FfnMxArgs& a, cudaStream_t s) {
   const int TK = a.T * a.topk;
+  // without xq the shared expert is skipped: its segment gets no rows and
+  // its maps and scales are set on the routed tensors (never read)
+  const bool shared = a.xq != nullptr;
+  const int Ts = shared ? a.T : 0;
   // ---- up projection + SwiGLU + power-of-two re-quantization
   MxParams up;
   std::memset(&up, 0, sizeof(up));
   bool ok =
       mx_token_maps(up.tok_routed, a.xpq, a.H, TK) &&
-      mx_token_maps(up.tok_shared, a.xq, a.H, a.T) &&
+      (shared ? mx_token_maps(up.tok_shared, a.xq, a.H, a.T)
+              : mx_token_maps(up.tok_shared, a.xpq, a.H, TK)) &&
       make_tmap_u8(&up.wa_routed, a.w1, a.H, (uint64_t)a.E * a.I, XM) &&
       make_tmap_u8(&up.wb_routed, a.w3, a.H, (uint64_t)a.E * a.I, XM) &&
-      make_tmap_u8(&up.wa_shared, a.ws1, a.H, a.I_shared, XM) &&
-      make_tmap_u8(&up.wb_shared, a.ws3, a.H, a.I_shared, XM);
+      (shared ? make_tmap_u8(&up.wa_shared, a.ws1, a.H, a.I_shared, XM) &&
+                    make_tmap_u8(&up.wb_shared, a.ws3, a.H, a.I_shared, XM)
+              : make_tmap_u8(&up.wa_shared, a.w1, a.H,
+                             (uint64_t)a.E * a.I, XM) &&
+                    make_tmap_u8(&up.wb_shared, a.w3, a.H,
+                                 (uint64_t)a.E * a.I, XM));
   if (!ok) return MOE_ERR_CUDA;
   up.ts_routed = a.xps;
-  up.ts_shared = a.xs;
+  up.ts_shared = shared ? a.xs : a.xps;
   up.sa_routed = a.w1s;
   up.sb_routed = a.w3s;
-  up.sa_shared = a.ws1s;
-  up.sb_shared = a.ws3s;
+  up.sa_shared = shared ? a.ws1s : a.w1s;
+  up.sb_shared = shared ? a.ws3s : a.w3s;
   up.offsets = a.offsets;
   up.q_routed = a.mq;
   up.qs_routed = a.ms;
@@ -795,7 +804,7 @@ int launch_expert_ffn_mx(const FfnMxArgs& a, cudaStream_t s) {
   up.status = a.status;
   up.wait_limit_ns = a.wait_limit_ns;
   up.E = a.E;
-  up.T = a.T;
+  up.T = Ts;
   up.TK = TK;
   up.n_routed = a.I;
   up.n_shared = a.I_shared;
@@ -808,25 +817,28 @@ int launch_expert_ffn_mx(const FfnMxArgs& a, cudaStream_t s) {
   MxParams dn;
   std::memset(&dn, 0, sizeof(dn));
   ok = mx_token_maps(dn.tok_routed, a.mq, a.I, TK) &&
-       mx_token_maps(dn.tok_shared, a.msq, a.I_shared, a.T) &&
+       (shared ? mx_token_maps(dn.tok_shared, a.msq, a.I_shared, a.T)
+               : mx_token_maps(dn.tok_shared, a.mq, a.I, TK)) &&
        make_tmap_u8(&dn.wa_routed, a.w2, a.I, (uint64_t)a.E * a.H, XM) &&
-       make_tmap_u8(&dn.wa_shared, a.ws2, a.I_shared, a.H, XM);
+       (shared ? make_tmap_u8(&dn.wa_shared, a.ws2, a.I_shared, a.H, XM)
+               : make_tmap_u8(&dn.wa_shared, a.w2, a.I, (uint64_t)a.E * a.H,
+                              XM));
   if (!ok) return MOE_ERR_CUDA;
   dn.wb_routed = dn.wa_routed;
   dn.wb_shared = dn.wa_shared;
   dn.ts_routed = a.ms;
-  dn.ts_shared = a.mss;
+  dn.ts_shared = shared ? a.mss : a.ms;
   dn.sa_routed = a.w2s;
   dn.sb_routed = a.w2s;
-  dn.sa_shared = a.ws2s;
-  dn.sb_shared = a.ws2s;
+  dn.sa_shared = shared ? a.ws2s : a.w2s;
+  dn.sb_shared = shared ? a.ws2s : a.w2s;
   dn.offsets = a.offsets;
   dn.y_routed = a.yp;
   dn.y_shared = a.ys;
   dn.status = a.status;
   dn.wait_limit_ns = a.wait_limit_ns;
   dn.E = a.E;
-  dn.T = a.T;
+  dn.T = Ts;
   dn.TK = TK;
   dn.n_routed = a.H;
   dn.n_shared = a.H;

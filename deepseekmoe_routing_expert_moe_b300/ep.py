@@ -23,6 +23,16 @@ The arithmetic runs in a backend; ``CudaBackend`` calls this library's C
 ABI (there is no fallback: it raises when the library is missing).  The
 exchanges use ``torch.distributed``: NCCL exchanges device tensors; with a
 gloo group the rows are staged through host memory.
+
+Dispatch in FP8 (same page, §2: activations are cast to FP8 before they are
+sent, the outputs return in BF16): with ``CudaBackend(..., mx=...)`` a rank
+quantizes its tokens once (E4M3 codes with power-of-two 1 x 128 scales,
+``moe_permute_mx``), sends the expert-sorted codes and their scale bytes
+(1 + 1/128 bytes per value instead of 2), the receiver runs its experts on
+them (``moe_expert_ffn_mx_routed``) and returns bf16 rows; the shared
+expert runs on the same codes.  A backend's ``permute`` may return the rows
+as a tuple of tensors with the same leading dimension (codes, scales): each
+is exchanged and regrouped alike.
 """
 from __future__ import annotations
 
@@ -35,7 +45,7 @@ class CudaBackend:
     """The per-rank arithmetic on this GPU through the C ABI (ops.py)."""
 
     def __init__(self, cfg_dims, weights, local_weights, rank, world,
-                 device="cuda"):
+                 device="cuda", mx=None):
         from . import ops
         self.ops = ops
         self.d = cfg_dims              # global layer dims (ops.MoeDims)
@@ -43,10 +53,14 @@ class CudaBackend:
         self.Wl = local_weights        # ops.Weights: this rank's experts
         self.rank, self.world = rank, world
         self.device = device
+        # FP8 dispatch: mx = (ops.WeightsMx of this rank's experts,
+        # ops.WeightsMx holding the shared expert as one expert), or None
+        self.mx = mx
+        self._tok_q = None             # this step's token codes and scales
         self._ws = {}
 
     def _workspace(self, d, which):
-        key = (d.T, d.topk, d.E, which)
+        key = (d.T, d.topk, d.E, d.I, which)
         if key not in self._ws:
             self._ws[key] = self.ops.workspace(d, which, self.device)
         return self._ws[key]
@@ -71,10 +85,23 @@ class CudaBackend:
         offsets = torch.empty(E + 1, dtype=torch.int32, device=self.device)
         dest = torch.empty((T, K), dtype=torch.int32, device=self.device)
         src = torch.empty(T * K, dtype=torch.int32, device=self.device)
-        xp = torch.empty((T * K, H), dtype=torch.int16, device=self.device)
-        o.moe_permute(d, x, idx, offsets, dest, src, xp,
-                      self._workspace(d, o.MOE_WS_PERMUTE))
-        return offsets, dest, xp
+        ws = self._workspace(d, o.MOE_WS_PERMUTE)
+        if self.mx is None:
+            xp = torch.empty((T * K, H), dtype=torch.int16,
+                             device=self.device)
+            o.moe_permute(d, x, idx, offsets, dest, src, xp, ws)
+            return offsets, dest, xp
+        # FP8 dispatch: the indices, then the tokens quantized once and
+        # their codes and scales copied to the expert-sorted rows
+        o.moe_permute(d, None, idx, offsets, dest, src, None, ws)
+        u8 = dict(dtype=torch.uint8, device=self.device)
+        xq = torch.empty((T, H), **u8)
+        xs = torch.empty((T, H // 128), **u8)
+        xpq = torch.empty((T * K, H), **u8)
+        xps = torch.empty((T * K, H // 128), **u8)
+        o.moe_permute_mx(d, x, dest, xq, xs, xpq, xps, ws)
+        self._tok_q = (xq, xs)
+        return offsets, dest, (xpq, xps)
 
     def plan(self, recv_counts, rows):
         n_local = recv_counts.shape[1]
@@ -97,6 +124,17 @@ class CudaBackend:
 
     def experts(self, xr, offsets_local):
         o = self.ops
+        if self.mx is not None:
+            codes, scales = xr
+            R = codes.shape[0]
+            yr = torch.empty((R, self.d.H), dtype=torch.int16,
+                             device=self.device)
+            if R:
+                dl = self._local_dims(R, offsets_local.shape[0] - 1)
+                o.moe_expert_ffn_mx_routed(
+                    dl, self.mx[0], codes, scales, offsets_local, yr,
+                    self._workspace(dl, o.MOE_WS_EXPERT_FFN_MX))
+            return yr
         R = xr.shape[0]
         yr = torch.empty_like(xr)
         if R == 0:
@@ -107,18 +145,26 @@ class CudaBackend:
         return yr
 
     def shared(self, x):
-        """The shared expert as a one-expert routed FFN over the tokens."""
+        """The shared expert as a one-expert routed FFN over the tokens (on
+        the step's token codes when dispatching in FP8)."""
         o, d = self.ops, self.d
         T = x.shape[0]
         ys = torch.empty_like(x)
         if T == 0:
             return ys
         dl = self._local_dims(T, 1)
+        off = torch.tensor([0, T], dtype=torch.int32, device=self.device)
+        if self.mx is not None:
+            dl.I = d.I_shared
+            xq, xs = self._tok_q
+            o.moe_expert_ffn_mx_routed(
+                dl, self.mx[1], xq, xs, off, ys,
+                self._workspace(dl, o.MOE_WS_EXPERT_FFN_MX))
+            return ys
         Ws = o.Weights(self.W.w_router, self.W.ws1.unsqueeze(0),
                        self.W.ws3.unsqueeze(0), self.W.ws2.unsqueeze(0),
                        self.W.ws1, self.W.ws3, self.W.ws2)
         dl.I = d.I_shared
-        off = torch.tensor([0, T], dtype=torch.int32, device=self.device)
         o.moe_expert_ffn_routed(dl, Ws, x, off, ys,
                                 self._workspace(dl, o.MOE_WS_EXPERT_FFN))
         return ys
@@ -180,7 +226,8 @@ class ExpertParallel:
         be, P, El = self.be, self.P, self.El
         T, H = x.shape
         idx, gate, counts = be.route(x, bias)
-        offsets, dest, xp = be.permute(x, idx)
+        offsets, dest, rows = be.permute(x, idx)
+        parts = rows if isinstance(rows, tuple) else (rows,)
         off = np.asarray(offsets.cpu()).astype(np.int64)
         send = [int(off[(r + 1) * El] - off[r * El]) for r in range(P)]
         # counts of my experts from every source, [P, El]
@@ -190,13 +237,21 @@ class ExpertParallel:
         rc = np.asarray(recv_counts.cpu()).astype(np.int64).reshape(P, El)
         recv = [int(v) for v in rc.sum(1)]
         R = sum(recv)
-        xr_src = torch.empty((R, H), dtype=xp.dtype, device=xp.device)
-        _exchange(self.group, xr_src, xp, recv, send)
+        # the dispatch: every part of the rows (bf16 rows, or E4M3 codes and
+        # their scale bytes), then each regrouped alike
+        received = []
+        for part in parts:
+            dst = torch.empty((R, part.shape[1]), dtype=part.dtype,
+                              device=part.device)
+            _exchange(self.group, dst, part, recv, send)
+            received.append(dst)
         perm, off_local = be.plan(recv_counts.view(P, El), R)
-        xr = be.permute_rows(xr_src, perm, inverse=False)
-        yr = be.experts(xr, off_local)
+        xr = tuple(be.permute_rows(p, perm, inverse=False) for p in received)
+        yr = be.experts(xr if isinstance(rows, tuple) else xr[0], off_local)
         yr_src = be.permute_rows(yr, perm, inverse=True)
-        yp = torch.empty_like(xp)
+        # the return trip: the experts' outputs in BF16
+        yp = torch.empty((parts[0].shape[0], H), dtype=yr.dtype,
+                         device=yr.device)
         _exchange(self.group, yp, yr_src, send, recv)
         ys = be.shared(x)
         out = be.combine(x, ys, yp, dest, gate)

@@ -91,6 +91,8 @@ _SIGS = {
     "moe_permute_mx": (_I, [_D, _P, _P, _P, _P, _P, _P, _P, _S, _P]),
     "moe_expert_ffn_mx": (_I, [_D, ctypes.POINTER(MoeWeightsMx), _P, _P,
                                _P, _P, _P, _P, _P, _P, _S, _P]),
+    "moe_expert_ffn_mx_routed": (_I, [_D, ctypes.POINTER(MoeWeightsMx), _P,
+                                      _P, _P, _P, _P, _S, _P]),
     "moe_plan_redundant_experts": (_I, [_P, ctypes.c_int32, ctypes.c_int32,
                                         ctypes.c_int32, _P, _P]),
     "moe_route_backward": (_I, [_D, _P, _P, _P, _I, _P, _P, _S, _P]),
@@ -229,10 +231,12 @@ class WeightsMx(WeightsFp8):
     block scales uint8) pairs for w1, w3, w2 and ws1, ws3, ws2."""
 
     def __init__(self, **pairs):
+        """(codes, scales) pairs by name; a name left out (the shared expert
+        of moe_expert_ffn_mx_routed's weights) is passed as NULL."""
         self.pairs = pairs
         flat = []
         for n in self.NAMES:
-            q, s = pairs[n]
+            q, s = pairs.get(n, (None, None))
             flat += [_ptr(q), _ptr(s)]
         self.struct = MoeWeightsMx(*flat)
 
@@ -401,6 +405,13 @@ def moe_expert_ffn_mx(d, w: WeightsMx, xpq, xps, xq, xs, offsets, yp, ys,
         ctypes.byref(d), ctypes.byref(w.struct), _ptr(xpq), _ptr(xps),
         _ptr(xq), _ptr(xs), _ptr(offsets), _ptr(yp), _ptr(ys), _ptr(ws),
         ws.numel(), _stream(stream)))
+
+
+def moe_expert_ffn_mx_routed(d, w: WeightsMx, xpq, xps, offsets, yp, ws,
+                             stream=None):
+    _check("moe_expert_ffn_mx_routed", lib().moe_expert_ffn_mx_routed(
+        ctypes.byref(d), ctypes.byref(w.struct), _ptr(xpq), _ptr(xps),
+        _ptr(offsets), _ptr(yp), _ptr(ws), ws.numel(), _stream(stream)))
 
 
 def moe_plan_redundant_experts(load, n_devices, slots_per_device):

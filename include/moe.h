@@ -269,7 +269,7 @@ moe_status_t moe_expert_ffn_routed(const moe_dims_t* d, const moe_weights_t* w,
  * n_src * n_local <= 4096 (MOE_ERR_UNSUPPORTED beyond).  A sum of counts
  * other than rows records MOE_ERR_DEVICE_BOUNDS in the error word of ws
  * (any workspace; may be NULL: nothing recorded).
- * moe_ep_permute_rows moves rows of row_bytes (a multiple of 16) by such
+ * moe_ep_permute_rows moves rows of row_bytes (any width) by such
  * a map: inverse = 0: out[perm[i]] = in[i] (source-major -> expert-major);
  * inverse = 1: out[i] = in[perm[i]] (back, for the return trip).  in and
  * out may not alias. */
@@ -517,6 +517,24 @@ moe_status_t moe_expert_ffn_mx(const moe_dims_t* d, const moe_weights_mx_t* w,
                                const int32_t* offsets, uint16_t* yp,
                                uint16_t* ys, void* ws, size_t ws_bytes,
                                moe_stream_t stream);
+
+/* The routed experts alone in FP8 with power-of-two scales, over any
+ * number of expert-sorted rows: expert parallelism's receive side when the
+ * rows are dispatched as E4M3 codes ("02 · DeepSeek-V3" §2: activations
+ * are cast to FP8 before dispatch, the expert outputs return in BF16).
+ * d->T = the rows R, d->topk = 1, d->E = the local experts; d's routing
+ * fields are not used.  xpq [R, H] u8, xps [R, H/128] u8 (UE8M0), offsets
+ * [E+1], yp [R, H] bf16 out.  w->w1, w3, w2 and their scales as in
+ * moe_expert_ffn_mx (the shared pointers are not read; the shared expert
+ * can run through this call as one expert over the tokens).
+ * Workspace: MOE_WS_EXPERT_FFN_MX, which moe_workspace_bytes sizes for
+ * such dims as well. */
+moe_status_t moe_expert_ffn_mx_routed(const moe_dims_t* d,
+                                      const moe_weights_mx_t* w,
+                                      const uint8_t* xpq, const uint8_t* xps,
+                                      const int32_t* offsets, uint16_t* yp,
+                                      void* ws, size_t ws_bytes,
+                                      moe_stream_t stream);
 
 /* Backward of the expert FFNs and the combine, for a fixed routing (the
  * training side of "02 · DeepSeek-V3" §1.1 SwiGLU experts and §1.3 eq. 12;

@@ -356,7 +356,26 @@ def test_routed_ffn_and_expert_parallel_maps_validation(L):
     assert plan(65, 64, FAKE, 10, FAKE, FAKE, None, None) == 2  # > 4096 cells
     assert plan(2, 4, FAKE, -1, FAKE, FAKE, None, None) == 1
     assert plan(2, 4, FAKE + 4, 10, FAKE, FAKE, None, None) == 3
-    assert rows(FAKE, 10, 24, FAKE, 0, FAKE, None, None) == 1   # % 16
+    assert rows(FAKE, 10, 0, FAKE, 0, FAKE, None, None) == 1    # width
     assert rows(FAKE, 10, 32, None, 0, FAKE, None, None) == 1
     assert rows(FAKE + 8, 10, 32, FAKE, 0, FAKE, None, None) == 3
     assert rows(None, 0, 32, None, 0, None, None, None) == 0
+    # the FP8 (power-of-two) routed experts: the same dims rules, widths
+    # multiples of 128, NULL shared weights allowed
+    d2 = ops.dims(T=100, H=256, E=1, n_group=1, topk_group=1, topk=1, I=128,
+                  I_shared=128)
+    assert ops.workspace_bytes(d2, ops.MOE_WS_EXPERT_FFN_MX) > 0
+    wm = ops.MoeWeightsMx(*(FAKE,) * 6, *(None,) * 6)
+    fm = L.moe_expert_ffn_mx_routed
+    assert fm(by(d2), by(wm), FAKE, FAKE, FAKE, FAKE, FAKE, 8, None) == 4
+    assert fm(by(d2), by(ops.MoeWeightsMx(*(FAKE,) * 5, None, *(None,) * 6)),
+              FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 30, None) == 1
+    assert fm(by(d2), by(wm), FAKE, FAKE + 4, FAKE, FAKE, FAKE, 1 << 30,
+              None) == 3
+    assert fm(by(ops.dims(T=100, H=192, E=1, n_group=1, topk_group=1,
+                          topk=1, I=128, I_shared=128)), by(wm), FAKE, FAKE,
+              FAKE, FAKE, FAKE, 1 << 30, None) == 2
+    d0 = ops.dims(T=0, H=256, E=1, n_group=1, topk_group=1, topk=1, I=128,
+                  I_shared=128)
+    assert fm(by(d0), by(wm), None, None, FAKE, None, FAKE, 1 << 20,
+              None) == 0

@@ -22,6 +22,8 @@ import torch.multiprocessing as mp
 
 CFG = dict(T=64, H=128, E=16, n_group=4, topk_group=2, topk=4, I=64,
            I_shared=64)
+CFG8 = dict(T=64, H=256, E=16, n_group=4, topk_group=2, topk=4, I=128,
+            I_shared=128)
 
 
 def _free_port():
@@ -111,13 +113,59 @@ class NumpyBackend:
         bias.copy_(torch.from_numpy(nb))
 
 
-def _setup():
+class NumpyBackendFp8(NumpyBackend):
+    """FP8 dispatch (§2: activations cast to FP8 before they are sent, the
+    outputs returned in BF16 -- here fp64): the tokens' E4M3 codes and
+    power-of-two 1 x 128 scales travel as two row tensors, and the experts
+    and the shared expert run the oracle's FP8 FFN on them."""
+
+    def __init__(self, cfg, w, rank, world):
+        super().__init__(cfg, w, rank, world)
+        O, f32 = self.O, np.float32
+        self.wq = {e: [O.quantize_128x128_pow2(w[n][e].astype(f32))
+                       for n in ("w1", "w3", "w2")]
+                   for e in range(self.e0, self.e0 + self.El)}
+        self.sq = [O.quantize_128x128_pow2(w[n].astype(f32))
+                   for n in ("ws1", "ws3", "ws2")]
+
+    def permute(self, x, idx):
+        O = self.O
+        p = O.permutation(idx.numpy(), self.cfg.E)
+        xq, xs = O.quantize_1x128_pow2(x.numpy().astype(np.float32))
+        self._tok = (xq, xs)
+        tok = p["src_row"] // self.cfg.topk
+        rows = (torch.from_numpy(np.ascontiguousarray(xq[tok])),
+                torch.from_numpy(np.ascontiguousarray(xs[tok])))
+        return (torch.from_numpy(p["offsets"]), torch.from_numpy(p["dest"]),
+                rows)
+
+    def experts(self, xr, offsets_local):
+        O = self.O
+        codes, scales = (t.numpy() for t in xr)
+        off = offsets_local.numpy()
+        y = np.zeros((codes.shape[0], self.cfg.H))
+        for l in range(self.El):
+            a, b = off[l], off[l + 1]
+            if b > a:
+                y[a:b] = O.fp8_swiglu_ffn(codes[a:b], scales[a:b],
+                                          *self.wq[self.e0 + l],
+                                          requant=O.quantize_1x128_pow2)[0]
+        return torch.from_numpy(y)
+
+    def shared(self, x):
+        xq, xs = self._tok
+        return torch.from_numpy(self.O.fp8_swiglu_ffn(
+            xq, xs, *self.sq, requant=self.O.quantize_1x128_pow2)[0])
+
+
+def _setup(fp8=False):
     import sys
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
     if root not in sys.path:
         sys.path.insert(0, root)
     from deepseekmoe_routing_expert_moe_b300 import inputs
-    cfg = inputs.custom_config("ep_gloo", 900, **CFG)
+    cfg = (inputs.custom_config("ep_gloo8", 901, **CFG8) if fp8 else
+           inputs.custom_config("ep_gloo", 900, **CFG))
     w = inputs.layer_inputs(cfg)
     f = inputs.bf16_bits_to_f32
     vals = {k: (f(v).astype(np.float64) if v.dtype == np.uint16 else v)
@@ -125,12 +173,12 @@ def _setup():
     return cfg, w, vals
 
 
-def _worker(rank, world, port, q):
+def _worker(rank, world, port, q, fp8=False):
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
     dist.init_process_group("gloo", rank=rank, world_size=world)
-    cfg, w, vals = _setup()
+    cfg, w, vals = _setup(fp8)
     from deepseekmoe_routing_expert_moe_b300 import ep
-    be = NumpyBackend(cfg, vals, rank, world)
+    be = (NumpyBackendFp8 if fp8 else NumpyBackend)(cfg, vals, rank, world)
     layer = ep.ExpertParallel(be, cfg.E, cfg.topk, cfg.topk_group,
                               cfg.n_group)
     n = cfg.T // world
@@ -184,3 +232,59 @@ def test_expert_parallel_exchange_equals_the_unsharded_layer():
     nb, _ = O.bias_update(c_all, w["bias"], cfg.T, cfg.topk, cfg.gamma)
     for r in res:
         assert np.array_equal(r[2].view(np.uint32), nb.view(np.uint32))
+
+
+def _fp8_layer(cfg, vals, bias):
+    """The unsharded layer with FP8 experts (power-of-two scales) on every
+    token: x + FFN_s(xq) + sum_k g_k FFN_{e_k}(xq), the oracle's FP8 FFN."""
+    from oracle import moe_oracle as O
+    f32 = np.float32
+    x = vals["x"]
+    z = O.router_logits(x, vals["w_router"])
+    r = O.route(z, bias, cfg.n_group, cfg.topk_group, cfg.topk)
+    xq, xs = O.quantize_1x128_pow2(x.astype(f32))
+    pow2 = O.quantize_1x128_pow2
+    sq = [O.quantize_128x128_pow2(vals[n].astype(f32))
+          for n in ("ws1", "ws3", "ws2")]
+    out = x + O.fp8_swiglu_ffn(xq, xs, *sq, requant=pow2)[0]
+    for e in range(cfg.E):
+        t, k = np.nonzero(r["idx"] == e)
+        if len(t):
+            wq = [O.quantize_128x128_pow2(vals[n][e].astype(f32))
+                  for n in ("w1", "w3", "w2")]
+            y = O.fp8_swiglu_ffn(xq[t], xs[t], *wq, requant=pow2)[0]
+            out[t] += r["gate"][t, k][:, None] * y
+    return out, r
+
+
+def test_expert_parallel_fp8_dispatch_equals_the_unsharded_fp8_layer():
+    """Dispatch in FP8: the codes and scale rows cross the all-to-all, the
+    outputs come back; every rank's output must equal the unsharded layer
+    with the same FP8 experts on its tokens (fp64; only summation order may
+    differ), and the bias step on the all-reduced load must be the whole
+    batch's."""
+    world = 2
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    ps = [ctx.Process(target=_worker, args=(r, world, port, q, True))
+          for r in range(world)]
+    for p in ps:
+        p.start()
+    res = sorted([q.get(timeout=180) for _ in range(world)],
+                 key=lambda v: v[0])
+    for p in ps:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    cfg, w, vals = _setup(True)
+    from oracle import moe_oracle as O
+    ref, r = _fp8_layer(cfg, vals, w["bias"])
+    n = cfg.T // world
+    for rank, out, bias, rc, send, idx in res:
+        rows = slice(rank * n, (rank + 1) * n)
+        assert np.array_equal(idx, r["idx"][rows])
+        np.testing.assert_allclose(out, ref[rows], rtol=1e-12, atol=1e-12)
+    c_all = O.expert_counts(r["idx"], cfg.E)
+    nb, _ = O.bias_update(c_all, w["bias"], cfg.T, cfg.topk, cfg.gamma)
+    for rr in res:
+        assert np.array_equal(rr[2].view(np.uint32), nb.view(np.uint32))

@@ -306,3 +306,30 @@ def test_v3_full_size_sampled_experts(name):
     ref, m = O.fp8_swiglu_ffn(xq[rows], xs[rows], sh["ws1"], sh["ws3"],
                               sh["ws2"], requant=pow2)
     fp8_ffn_check(ys[rows], ref, "shared", m, O.dequantize(*sh["ws2"], 128))
+
+
+def test_routed_only_call_equals_the_full_call():
+    """moe_expert_ffn_mx_routed (expert parallelism's receive side: rows
+    only, no shared expert) on the full call's routed rows gives the same
+    outputs bit for bit: the same units, the same accumulation order."""
+    cfg = inputs.custom_config("mxro", 996, T=200, H=384, E=8, n_group=4,
+                               topk_group=2, topk=2, I=256, I_shared=128,
+                               router_sigma=0.05)
+    T, K, E, H = cfg.T, cfg.topk, cfg.E, cfg.H
+    per = [_host_weights(cfg, e) for e in range(E)]
+    sh = _shared(cfg)
+    yp, ys, p, xq, xs = _ffn(cfg, _routed(cfg), per, sh, T)
+    routed = {n: _dev_pair(np.concatenate([per[e][i][0] for e in range(E)]),
+                           np.concatenate([per[e][i][1] for e in range(E)]))
+              for i, n in enumerate(("w1", "w3", "w2"))}
+    W = ops.WeightsMx(**routed)
+    R = T * K
+    d = ops.dims(R, H, E, 1, 1, 1, cfg.I, cfg.I_shared, cfg.gamma)
+    tok = p["src_row"] // K
+    out = torch.zeros((R, H), dtype=torch.int16, device="cuda")
+    ws = ops.workspace(d, ops.MOE_WS_EXPERT_FFN_MX)
+    ops.moe_expert_ffn_mx_routed(d, W, dev(xq[tok]),
+                                 dev(_scale_bytes(xs)[tok]),
+                                 dev(p["offsets"]), out, ws)
+    assert ops.moe_get_device_error(ws) == 0
+    np.testing.assert_array_equal(bf16_dev_to_f32(out), yp)
