@@ -1,6 +1,6 @@
 """The whole layer forward (moe_forward) against the oracle.
 
-Tolerance (spec bar): max |out - oracle| <= 2e-2 x RMS(oracle out) on
+Tolerance (the layer bar): max |out - oracle| <= 2e-2 x RMS(oracle out) on
 tokens whose top-K margin and group margin (on the oracle's own u and S)
 both exceed 1e-4; routing must agree on those tokens.  The GPU computes
 its own fp32 logits, so low-margin tokens may route differently and are
