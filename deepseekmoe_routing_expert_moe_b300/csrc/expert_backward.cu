@@ -133,7 +133,7 @@ __global__ void __launch_bounds__(kPadThreads)
                    const float* __restrict__ gate, int TK, int E, int cap,
                    int32_t* __restrict__ poff_out,
                    int32_t* __restrict__ pdest, float* __restrict__ gp,
-                   DevStatus* st) {
+                   int* __restrict__ ticket, DevStatus* st) {
   __shared__ int poff[1025];
   __shared__ int wsum[kPadThreads / 32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -160,8 +160,10 @@ __global__ void __launch_bounds__(kPadThreads)
   }
   if (tid == 0) poff[E] = total;
   __syncthreads();
-  if (blockIdx.x == 0)
+  if (blockIdx.x == 0) {
     for (int e = tid; e <= E; e += kPadThreads) poff_out[e] = poff[e];
+    if (tid == 0) *ticket = 0;  // the weight-gradient kernel's task counter
+  }
   const int i = blockIdx.x * kPadThreads + tid;
   if (i >= TK) return;
   const int e = idx[i];
@@ -873,16 +875,32 @@ int launch_dgrad(const DgParams& dp, cudaStream_t s) {
 }
 
 // --------------------------------------------------------------------------
-// weight gradients: units (matrix, segment, 128-row block, 256-column
-// block); the reduction runs over the segment's token rows
+// weight gradients: tasks (matrix, segment, 256-column block, group of
+// 128-row blocks); the reduction runs over the segment's token rows.
+//
+// Per 128 x 256 fp32 output block the MMA reads a 128-column slice of the
+// A side (dp, dq or dpp rows) and a 256-column slice of the B side (xpp or
+// hg rows) over the segment's rows.  A segment of at most 192 rows keeps
+// its B slice in shared memory for a group of up to 16 row blocks, so each
+// further block streams only its A slice (a third of the operand bytes);
+// longer segments (the shared expert, skewed experts) stream both per
+// block.  The tail of a segment is loaded in 16-row boxes, so no rows past
+// it are fetched.  CTAs take tasks from a counter in global memory that the
+// dispatch kernel of the same call zeroes: a CTA on a slower path through
+// the memory system simply takes fewer tasks.
 // --------------------------------------------------------------------------
 constexpr int WG_N = 256;
-constexpr int WG_STAGES = 3;
-constexpr uint32_t WG_A_BYTES = BM * BK * 2;         // 16 KB
-constexpr uint32_t WG_B_BYTES = WG_N * BK * 2;       // 32 KB
-constexpr uint32_t WG_STAGE_BYTES = WG_A_BYTES + WG_B_BYTES;
+constexpr int WG_ASTAGES = 3;   // A ring: 128 columns x 64 rows (16 KB)
+constexpr int WG_BSLOTS = 3;    // B ring: 256 columns x 64 rows (32 KB)
+constexpr int WG_GROUP = 16;    // row blocks per task while B is resident
+constexpr int WG_QN = 8;        // depth of the task queue in shared memory
+constexpr int WG_RES_ROWS = WG_BSLOTS * BK;         // 192
+constexpr uint32_t WG_A_BYTES = BM * BK * 2;        // 16 KB
+constexpr uint32_t WG_B_BYTES = WG_N * BK * 2;      // 32 KB
+constexpr uint32_t WG_BOX_BYTES = 64 * BK * 2;      // one 64 x 64 box, 8 KB
+constexpr uint32_t WG_BOX16_BYTES = 64 * 16 * 2;    // one 64 x 16 box, 2 KB
 // eight epilogue warps: two per tensor-memory lane quadrant, each storing
-// half of a unit's columns (the fp32 stores are the kernel's long pole)
+// half of a block's columns (the fp32 stores are the kernel's long pole)
 constexpr int kWgEpiWarps = 8;
 constexpr int kWgThreads = 32 * (kEpiWarp0 + kWgEpiWarps);
 // fp32 output staging: per epilogue warp two 32 x 32 tiles (4 KB each),
@@ -891,12 +909,17 @@ constexpr int WG_OUT_BUFS = 2;
 constexpr uint32_t WG_OUT_TILE = 32 * 32 * 4;
 constexpr uint32_t WG_OUT_BYTES = kWgEpiWarps * WG_OUT_BUFS * WG_OUT_TILE;
 constexpr int kMats = 3;   // dW1, dW3, dW2
+constexpr int kWgBars = 2 * WG_ASTAGES + 2 * WG_BSLOTS + 4 + 2 * WG_QN + 1;
+enum { kSiteQueue = 48 };
 
 struct WgParams {
-  CUtensorMap a_r[kMats], b_r[kMats];  // routed: (dp, xpp) (dq, xpp) (dpp, hg)
-  CUtensorMap a_s[kMats], b_s[kMats];  // shared: (dps, x) (dqs, x) (dout, hs)
+  // routed: (dp, xpp) (dq, xpp) (dpp, hg); shared: (dps, x) (dqs, x)
+  // (dout, hs); 64-row boxes and 16-row boxes (segment tails)
+  CUtensorMap a_r[kMats], b_r[kMats], a_s[kMats], b_s[kMats];
+  CUtensorMap a_r16[kMats], b_r16[kMats], a_s16[kMats], b_s16[kMats];
   CUtensorMap o_r[kMats], o_s[kMats];  // outputs as [experts][M][N] fp32
   const int32_t* poff;
+  int* ticket;           // task counter, zero at launch
   float* out_r[kMats];   // dW1, dW3 [E, I, H], dW2 [E, H, I]
   float* out_s[kMats];   // dWs1, dWs3 [I_s, H], dWs2 [H, I_s]
   DevStatus* status;
@@ -905,8 +928,9 @@ struct WgParams {
   int accumulate;
 };
 
-struct WUnit {
-  int mat, seg, m0, n0, M, N, rows, row0, nt;
+struct WTask {
+  int mat, seg, M, N, rows, row0, n0, nt, mb0, mb1;
+  bool res;   // B slice resident for the group
 };
 
 // M and N of matrix `mat` for a segment (shared: s == 0)
@@ -917,30 +941,80 @@ __device__ __forceinline__ void wg_dims(const WgParams& p, int mat, int s,
   N = mat < 2 ? p.H : If;
 }
 
-__device__ __forceinline__ WUnit wg_decode(const WgParams& p, int u,
-                                           const int* upre, const int* srow0,
-                                           const int* srows, int NP) {
+// row blocks per task of a segment with `rows` rows (an empty segment's
+// blocks are zero-filled, a group at a time)
+__device__ __forceinline__ int wg_group(int rows) {
+  return rows <= WG_RES_ROWS ? WG_GROUP : 1;
+}
+
+__device__ __forceinline__ int wg_tasks(int M, int N, int rows) {
+  const int G = wg_group(rows);
+  return ((M + BM - 1) / BM + G - 1) / G * ((N + WG_N - 1) / WG_N);
+}
+
+// rows and first row of segment s (0: the shared expert over the T tokens;
+// s >= 1: routed expert s - 1 between its padded offsets)
+__device__ __forceinline__ int wg_rows(const WgParams& p, const int* spoff,
+                                       int s) {
+  return s == 0 ? p.T : spoff[s] - spoff[s - 1];
+}
+
+__device__ __forceinline__ WTask wg_decode(const WgParams& p, int t,
+                                           const int* upre, const int* spoff,
+                                           int NP) {
   int lo = 0, hi = NP - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (upre[mid] <= u)
+    if (upre[mid] <= t)
       lo = mid;
     else
       hi = mid - 1;
   }
   const int NS = p.E + 1;
-  WUnit x;
+  WTask x;
   x.mat = lo / NS;
   x.seg = lo - x.mat * NS;
   wg_dims(p, x.mat, x.seg, x.M, x.N);
+  x.rows = wg_rows(p, spoff, x.seg);
+  x.row0 = x.seg == 0 ? 0 : spoff[x.seg - 1];
+  const int G = wg_group(x.rows);
   const int nb = (x.N + WG_N - 1) / WG_N;
-  const int local = u - upre[lo];
-  x.m0 = (local / nb) * BM;
-  x.n0 = (local - (local / nb) * nb) * WG_N;
+  const int local = t - upre[lo];
+  const int g = local / nb;
+  x.n0 = (local - g * nb) * WG_N;
   x.nt = min(WG_N, x.N - x.n0);
-  x.rows = srows[x.seg];
-  x.row0 = srow0[x.seg];
+  x.mb0 = g * G;
+  x.mb1 = min((x.M + BM - 1) / BM, x.mb0 + G);
+  x.res = x.rows > 0 && x.rows <= WG_RES_ROWS;
   return x;
+}
+
+// Reduction rows [row, row + min(left, 64)) of `nbox` 64-column boxes
+// (columns x0, x0 + 64, ...) into a stage of 64-row boxes `box_bytes`
+// apart.  A tail (left < 64) is fetched in 16-row boxes, which land where
+// the 64-row box would put those rows (whole 1 KB swizzle atoms).  Returns
+// the bytes the copies deliver.
+__device__ __forceinline__ uint32_t wg_load_rows(
+    uint32_t dst, const CUtensorMap* m64, const CUtensorMap* m16, int x0,
+    int nbox, uint32_t box_bytes, int row, int left, uint32_t bar,
+    uint64_t pol) {
+  if (left >= BK) {
+    for (int b = 0; b < nbox; ++b)
+      tma_load_2d_hint(dst + b * box_bytes, m64, x0 + 64 * b, row, bar, pol);
+    return nbox * WG_BOX_BYTES;
+  }
+  const int n16 = (left + 15) / 16;
+  for (int j = 0; j < n16; ++j)
+    for (int b = 0; b < nbox; ++b)
+      tma_load_2d_hint(dst + b * box_bytes + j * WG_BOX16_BYTES, m16,
+                       x0 + 64 * b, row + 16 * j, bar, pol);
+  return n16 * nbox * WG_BOX16_BYTES;
+}
+
+// bytes wg_load_rows delivers (the transaction count of the stage)
+__device__ __forceinline__ uint32_t wg_rows_bytes(int nbox, int left) {
+  return left >= BK ? nbox * WG_BOX_BYTES
+                    : ((left + 15) / 16) * nbox * WG_BOX16_BYTES;
 }
 
 __global__ void __launch_bounds__(kWgThreads, 1)
@@ -948,31 +1022,45 @@ __global__ void __launch_bounds__(kWgThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sS = smem;  // stages: A tile then B tile
-  uint8_t* sO = sS + WG_STAGES * WG_STAGE_BYTES;  // output staging
+  uint8_t* sB = smem;                            // B ring
+  uint8_t* sA = sB + WG_BSLOTS * WG_B_BYTES;     // A ring
+  uint8_t* sO = sA + WG_ASTAGES * WG_A_BYTES;    // output staging
   uint64_t* bars = reinterpret_cast<uint64_t*>(sO + WG_OUT_BYTES);
-  uint64_t* full = bars;
-  uint64_t* empty = full + WG_STAGES;
-  uint64_t* tfull = empty + WG_STAGES;
+  uint64_t* afull = bars;
+  uint64_t* aempty = afull + WG_ASTAGES;
+  uint64_t* bfull = aempty + WG_ASTAGES;
+  uint64_t* bempty = bfull + WG_BSLOTS;
+  uint64_t* tfull = bempty + WG_BSLOTS;
   uint64_t* tempty = tfull + 2;
-  uint64_t* drain = tempty + 2;
+  uint64_t* qfull = tempty + 2;
+  uint64_t* qempty = qfull + WG_QN;
+  uint64_t* drain = qempty + WG_QN;
   volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(drain + 1);
+  volatile int* qv = reinterpret_cast<volatile int*>(misc + 4);
   const int NS = p.E + 1;
   const int NP = kMats * NS;
-  int* upre = reinterpret_cast<int*>(const_cast<uint32_t*>(misc) + 4);
-  int* srows = upre + NP + 1;
-  int* srow0 = srows + NS;
+  int* upre = const_cast<int*>(qv) + WG_QN;
+  int* spoff = upre + NP + 1;   // the padded offsets [E + 1]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < WG_STAGES; ++i) {
-      mbar_init(smem_u32(&full[i]), 1);
-      mbar_init(smem_u32(&empty[i]), 1);
+    for (int i = 0; i < WG_ASTAGES; ++i) {
+      mbar_init(smem_u32(&afull[i]), 1);
+      mbar_init(smem_u32(&aempty[i]), 1);
+    }
+    for (int i = 0; i < WG_BSLOTS; ++i) {
+      mbar_init(smem_u32(&bfull[i]), 1);
+      mbar_init(smem_u32(&bempty[i]), 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&tfull[i]), 1);
       mbar_init(smem_u32(&tempty[i]), 32 * kWgEpiWarps);
+    }
+    // a task id is read by the MMA thread and each epilogue warp
+    for (int i = 0; i < WG_QN; ++i) {
+      mbar_init(smem_u32(&qfull[i]), 1);
+      mbar_init(smem_u32(&qempty[i]), 1 + kWgEpiWarps);
     }
     mbar_init(smem_u32(drain), 1);
     misc[1] = 0;
@@ -980,24 +1068,16 @@ __global__ void __launch_bounds__(kWgThreads, 1)
     fence_mbar_init();
   }
   if (warp == 2) {
-    // segment rows, then units per (matrix, segment) pair and their prefix
+    // the segments' offsets (checked), then tasks per (matrix, segment)
+    // pair and their prefix
     bool bad = false;
-    for (int s = lane; s < NS; s += 32) {
-      int r0 = 0, rows = p.T;
-      if (s > 0) {
-        r0 = p.poff[s - 1];
-        const int r1 = p.poff[s];
-        if (r0 < 0 || r1 < r0 || r1 > p.TKP) {
-          bad = true;
-          r0 = 0;
-          rows = 0;
-        } else {
-          rows = r1 - r0;
-        }
-      }
-      srows[s] = rows;
-      srow0[s] = r0;
+    for (int e = lane; e < NS; e += 32) {
+      const int r1 = p.poff[e];
+      const int r0 = e > 0 ? p.poff[e - 1] : 0;
+      if (r0 < 0 || r1 < r0 || r1 > p.TKP) bad = true;
+      spoff[e] = r1;
     }
+    bad = __any_sync(0xffffffffu, bad);
     __syncwarp();
     const int per = (NP + 31) / 32;
     const int lo = min(NP, lane * per), hi = min(NP, lo + per);
@@ -1006,7 +1086,7 @@ __global__ void __launch_bounds__(kWgThreads, 1)
       const int mat = i / NS, s = i - mat * NS;
       int M, N;
       wg_dims(p, mat, s, M, N);
-      mine += ((M + BM - 1) / BM) * ((N + WG_N - 1) / WG_N);
+      mine += bad ? 0 : wg_tasks(M, N, wg_rows(p, spoff, s));
     }
     int incl = mine;
 #pragma unroll
@@ -1020,10 +1100,10 @@ __global__ void __launch_bounds__(kWgThreads, 1)
       const int mat = i / NS, s = i - mat * NS;
       int M, N;
       wg_dims(p, mat, s, M, N);
-      run += ((M + BM - 1) / BM) * ((N + WG_N - 1) / WG_N);
+      run += bad ? 0 : wg_tasks(M, N, wg_rows(p, spoff, s));
     }
     if (lane == 31) upre[NP] = incl;
-    if (__any_sync(0xffffffffu, bad) && lane == 0) misc[2] = 1;
+    if (bad && lane == 0) misc[2] = 1;
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(const_cast<uint32_t*>(&misc[0])), TMEM_COLS);
@@ -1043,100 +1123,163 @@ __global__ void __launch_bounds__(kWgThreads, 1)
 
   if (warp == 0) {
     if (lane == 0) {
-      // ---------------------------------------------- operand producer
-      uint32_t stage = 0, phase = 0, issued = 0;
+      // ------------------------------------- task queue + operand producer
+      uint32_t af = 0, bf = 0, qf = 0;
       const uint64_t pol = policy_evict_last();
-      for (int u = blockIdx.x; u < total; u += gridDim.x) {
-        const WUnit w = wg_decode(p, u, upre, srow0, srows, NP);
+      bool ok = true;
+      // one stage of the A ring (two 64-column boxes) or the B ring
+      auto load_a = [&](const CUtensorMap* m64, const CUtensorMap* m16,
+                        int m0, int row, int left) {
+        const uint32_t s = af % WG_ASTAGES;
+        if (!mbar_wait_bounded(smem_u32(&aempty[s]),
+                               ((af / WG_ASTAGES) & 1) ^ 1, abort_flag, limit,
+                               p.status, kSiteProducer))
+          return false;
+        const uint32_t fb = smem_u32(&afull[s]);
+        mbar_arrive_expect_tx(fb, wg_rows_bytes(2, left));
+        wg_load_rows(smem_u32(sA + s * WG_A_BYTES), m64, m16, m0, 2,
+                     WG_BOX_BYTES, row, left, fb, pol);
+        ++af;
+        return true;
+      };
+      auto load_b = [&](const CUtensorMap* m64, const CUtensorMap* m16,
+                        int n0, int nbox, int row, int left) {
+        const uint32_t s = bf % WG_BSLOTS;
+        if (!mbar_wait_bounded(smem_u32(&bempty[s]),
+                               ((bf / WG_BSLOTS) & 1) ^ 1, abort_flag, limit,
+                               p.status, kSiteProducer))
+          return false;
+        const uint32_t fb = smem_u32(&bfull[s]);
+        mbar_arrive_expect_tx(fb, wg_rows_bytes(nbox, left));
+        wg_load_rows(smem_u32(sB + s * WG_B_BYTES), m64, m16, n0, nbox,
+                     WG_BOX_BYTES, row, left, fb, pol);
+        ++bf;
+        return true;
+      };
+      while (ok) {
+        int t = atomicAdd(p.ticket, 1);
+        if (t >= total) t = -1;
+        const uint32_t qs = qf % WG_QN;
+        if (!mbar_wait_bounded(smem_u32(&qempty[qs]), ((qf / WG_QN) & 1) ^ 1,
+                               abort_flag, limit, p.status, kSiteQueue))
+          break;
+        qv[qs] = t;
+        mbar_arrive(smem_u32(&qfull[qs]));
+        ++qf;
+        if (t < 0) break;
+        const WTask w = wg_decode(p, t, upre, spoff, NP);
         if (w.rows == 0) continue;
         const bool sh = w.seg == 0;
         const CUtensorMap* ma = sh ? &p.a_s[w.mat] : &p.a_r[w.mat];
         const CUtensorMap* mb = sh ? &p.b_s[w.mat] : &p.b_r[w.mat];
+        const CUtensorMap* ma16 = sh ? &p.a_s16[w.mat] : &p.a_r16[w.mat];
+        const CUtensorMap* mb16 = sh ? &p.b_s16[w.mat] : &p.b_r16[w.mat];
         const int nkb = (w.rows + BK - 1) / BK;
         const int nbox = (w.nt + 63) / 64;
-        const uint32_t tx = WG_A_BYTES + nbox * (WG_B_BYTES / 4);
-        bool ok = true;
-        for (int kb = 0; kb < nkb; ++kb) {
-          if (!mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1,
-                                 abort_flag, limit, p.status,
-                                 kSiteProducer)) {
-            ok = false;
-            break;
+        if (w.res)
+          for (int kb = 0; kb < nkb && ok; ++kb)
+            ok = load_b(mb, mb16, w.n0, nbox, w.row0 + kb * BK,
+                        w.rows - kb * BK);
+        for (int mblk = w.mb0; mblk < w.mb1 && ok; ++mblk)
+          for (int kb = 0; kb < nkb && ok; ++kb) {
+            const int row = w.row0 + kb * BK, left = w.rows - kb * BK;
+            if (!w.res) ok = load_b(mb, mb16, w.n0, nbox, row, left);
+            if (ok) ok = load_a(ma, ma16, mblk * BM, row, left);
           }
-          const uint32_t fb = smem_u32(&full[stage]);
-          uint8_t* st = sS + stage * WG_STAGE_BYTES;
-          const int row = w.row0 + kb * BK;
-          mbar_arrive_expect_tx(fb, tx);
-          tma_load_2d_hint(smem_u32(st), ma, w.m0, row, fb, pol);
-          tma_load_2d_hint(smem_u32(st + WG_A_BYTES / 2), ma, w.m0 + 64, row,
-                           fb, pol);
-          for (int b = 0; b < nbox; ++b)
-            tma_load_2d_hint(smem_u32(st + WG_A_BYTES + b * (WG_B_BYTES / 4)),
-                             mb, w.n0 + 64 * b, row, fb, pol);
-          ++issued;
-          if (++stage == WG_STAGES) {
-            stage = 0;
-            phase ^= 1;
-          }
-        }
-        if (!ok) break;
       }
-      const uint32_t first = issued > WG_STAGES ? issued - WG_STAGES : 0;
-      for (uint32_t i = first; i < issued; ++i)
-        mbar_wait_bounded(smem_u32(&full[i % WG_STAGES]),
-                          (i / WG_STAGES) & 1, nullptr, kDrainNs, p.status,
+      // the copies still in flight land before the CTA exits
+      const uint32_t first = af > WG_ASTAGES ? af - WG_ASTAGES : 0;
+      for (uint32_t i = first; i < af; ++i)
+        mbar_wait_bounded(smem_u32(&afull[i % WG_ASTAGES]),
+                          (i / WG_ASTAGES) & 1, nullptr, kDrainNs, p.status,
+                          kSiteDrain);
+      const uint32_t firstb = bf > WG_BSLOTS ? bf - WG_BSLOTS : 0;
+      for (uint32_t i = firstb; i < bf; ++i)
+        mbar_wait_bounded(smem_u32(&bfull[i % WG_BSLOTS]),
+                          (i / WG_BSLOTS) & 1, nullptr, kDrainNs, p.status,
                           kSiteDrain);
     }
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0) {
       // ----------------------------------------------------------- MMA
-      uint32_t stage = 0, phase = 0, tph = 0;
+      uint32_t af = 0, bf = 0, qf = 0, tph = 0;
       int slot = 0;
-      bool any = false;
-      for (int u = blockIdx.x; u < total; u += gridDim.x) {
-        const WUnit w = wg_decode(p, u, upre, srow0, srows, NP);
-        if (w.rows == 0) continue;
-        if (!mbar_wait_bounded(smem_u32(&tempty[slot]),
-                               ((tph >> slot) & 1) ^ 1, abort_flag, limit,
-                               p.status, kSiteMmaAcc))
+      bool any = false, ok = true;
+      auto wait_b = [&](uint32_t i) {
+        return mbar_wait_bounded(smem_u32(&bfull[i % WG_BSLOTS]),
+                                 (i / WG_BSLOTS) & 1, abort_flag, limit,
+                                 p.status, kSiteMmaFull);
+      };
+      while (ok) {
+        const uint32_t qs = qf % WG_QN;
+        if (!mbar_wait_bounded(smem_u32(&qfull[qs]), (qf / WG_QN) & 1,
+                               abort_flag, limit, p.status, kSiteQueue))
           break;
-        tc_fence_after();
-        const uint32_t d = tmem_base + slot * SLOT;
+        const int t = qv[qs];
+        mbar_arrive(smem_u32(&qempty[qs]));
+        ++qf;
+        if (t < 0) break;
+        const WTask w = wg_decode(p, t, upre, spoff, NP);
+        if (w.rows == 0) continue;
+        const int nkb = (w.rows + BK - 1) / BK;
         const int ntile = ((w.nt + 63) / 64) * 64;
         const uint32_t idesc =
             idesc_bf16_f32(BM, ntile) | kAMajorMN | kBMajorMN;
-        const int nkb = (w.rows + BK - 1) / BK;
-        bool ok = true;
-        for (int kb = 0; kb < nkb; ++kb) {
-          if (!mbar_wait_bounded(smem_u32(&full[stage]), phase, abort_flag,
-                                 limit, p.status, kSiteMmaFull)) {
+        const uint32_t b0 = bf;  // first B stage of a resident slice
+        if (w.res) {
+          for (int kb = 0; kb < nkb && ok; ++kb) ok = wait_b(b0 + kb);
+          bf += nkb;
+        }
+        for (int mblk = w.mb0; mblk < w.mb1 && ok; ++mblk) {
+          if (!mbar_wait_bounded(smem_u32(&tempty[slot]),
+                                 ((tph >> slot) & 1) ^ 1, abort_flag, limit,
+                                 p.status, kSiteMmaAcc)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t sa = smem_u32(sS + stage * WG_STAGE_BYTES);
-          const uint32_t sb = sa + WG_A_BYTES;
-          // reduction rows of this stage that belong to the segment (the
-          // segment's length is a multiple of 16, or its map ends there)
-          const int left = w.rows - kb * BK;
-          const int steps = min(BK / UMMA_K, (left + UMMA_K - 1) / UMMA_K);
-          for (int kk = 0; kk < steps; ++kk) {
-            tc_mma_f16(d, sw128_mnmajor_desc(sa + kk * UMMA_K * 128),
-                       sw128_mnmajor_desc(sb + kk * UMMA_K * 128), idesc,
-                       (kb | kk) != 0);
+          const uint32_t d = tmem_base + slot * SLOT;
+          for (int kb = 0; kb < nkb; ++kb) {
+            const uint32_t bi = w.res ? b0 + kb : bf;
+            if (!w.res && !wait_b(bi)) {
+              ok = false;
+              break;
+            }
+            const uint32_t as = af % WG_ASTAGES;
+            if (!mbar_wait_bounded(smem_u32(&afull[as]),
+                                   (af / WG_ASTAGES) & 1, abort_flag, limit,
+                                   p.status, kSiteMmaFull)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t sa = smem_u32(sA + as * WG_A_BYTES);
+            const uint32_t sb = smem_u32(sB + (bi % WG_BSLOTS) * WG_B_BYTES);
+            // reduction rows of this stage that belong to the segment (the
+            // segment's length is a multiple of 16, or its map ends there)
+            const int left = w.rows - kb * BK;
+            const int steps = min(BK / UMMA_K, (left + UMMA_K - 1) / UMMA_K);
+            for (int kk = 0; kk < steps; ++kk)
+              tc_mma_f16(d, sw128_mnmajor_desc(sa + kk * UMMA_K * 128),
+                         sw128_mnmajor_desc(sb + kk * UMMA_K * 128), idesc,
+                         (kb | kk) != 0);
+            any = true;
+            tc_commit(smem_u32(&aempty[as]));
+            ++af;
+            if (!w.res) {
+              tc_commit(smem_u32(&bempty[bi % WG_BSLOTS]));
+              ++bf;
+            }
           }
-          any = true;
-          tc_commit(smem_u32(&empty[stage]));
-          if (++stage == WG_STAGES) {
-            stage = 0;
-            phase ^= 1;
-          }
+          if (!ok) break;
+          tc_commit(smem_u32(&tfull[slot]));
+          tph ^= 1u << slot;
+          slot ^= 1;
         }
-        if (!ok) break;
-        tc_commit(smem_u32(&tfull[slot]));
-        tph ^= 1u << slot;
-        slot ^= 1;
+        if (ok && w.res)
+          for (int kb = 0; kb < nkb; ++kb)
+            tc_commit(smem_u32(&bempty[(b0 + kb) % WG_BSLOTS]));
       }
       if (any) {
         tc_commit(smem_u32(drain));
@@ -1147,7 +1290,7 @@ __global__ void __launch_bounds__(kWgThreads, 1)
     __syncwarp();
   } else if (warp >= kEpiWarp0) {
     // ------------------------------------------------------- epilogue
-    // Each warp owns 32 rows (its TMEM lane quadrant) and half of a unit's
+    // Each warp owns 32 rows (its TMEM lane quadrant) and half of a block's
     // columns: per 32 columns it writes its rows into a swizzled 4 KB
     // staging tile and one lane issues the TMA store (or reduce-add) of the
     // tile; two tiles alternate, so a tile is rewritten only after its
@@ -1155,79 +1298,107 @@ __global__ void __launch_bounds__(kWgThreads, 1)
     const int q = warp & 3;
     const int hw = (warp - kEpiWarp0) >> 2;  // which half of the columns
     const int r = q * 32 + lane;
-    uint32_t tph = 0;
+    uint32_t tph = 0, qf = 0;
     int slot = 0;
     int ob = 0;
+    bool ok = true;
     uint8_t* stage_base =
         sO + (warp - kEpiWarp0) * WG_OUT_BUFS * WG_OUT_TILE;
     // the gradients stream out once: their lines go first when L2 needs
     // room, so the operand rows (kept with evict_last) stay resident
     const uint64_t pol_out = policy_evict_first();
-    for (int u = blockIdx.x; u < total; u += gridDim.x) {
-      const WUnit w = wg_decode(p, u, upre, srow0, srows, NP);
+    while (ok) {
+      int t = -1;
+      if (lane == 0) {
+        const uint32_t qs = qf % WG_QN;
+        if (mbar_wait_bounded(smem_u32(&qfull[qs]), (qf / WG_QN) & 1,
+                              abort_flag, limit, p.status, kSiteQueue)) {
+          t = qv[qs];
+          mbar_arrive(smem_u32(&qempty[qs]));
+        }
+      }
+      t = __shfl_sync(0xffffffffu, t, 0);
+      ++qf;
+      if (t < 0) break;
+      const WTask w = wg_decode(p, t, upre, spoff, NP);
       const bool sh = w.seg == 0;
       const int nch = (w.nt + 31) / 32;
       const int c_lo = hw ? (nch + 1) / 2 : 0;
       const int c_hi = hw ? nch : (nch + 1) / 2;
-      if (w.rows == 0) {
-        // an expert with no tokens has a zero gradient
-        const int row = w.m0 + r;
-        if (!p.accumulate && row < w.M) {
-          float* out = p.out_r[w.mat] + (size_t)(w.seg - 1) * w.M * w.N;
-          float* orow = out + (size_t)row * w.N + w.n0;
-          for (int c = 32 * c_lo; c < min(w.nt, 32 * c_hi); c += 4)
-            *reinterpret_cast<float4*>(orow + c) = make_float4(0, 0, 0, 0);
-        }
-        continue;
-      }
-      int ok = 0;
-      if (lane == 0)
-        ok = mbar_wait_bounded(smem_u32(&tfull[slot]), (tph >> slot) & 1,
-                               abort_flag, limit, p.status, kSiteEpilogue);
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
-      tc_fence_after();
-      const uint32_t ta =
-          tmem_base + (static_cast<uint32_t>(q * 32) << 16) + slot * SLOT;
       const CUtensorMap* om = sh ? &p.o_s[w.mat] : &p.o_r[w.mat];
-      const int mrow = w.m0 + q * 32;        // first row of this warp
       const int mat_idx = sh ? 0 : w.seg - 1;
-      for (int c = c_lo; c < c_hi; ++c) {
-        uint32_t v[32];
-        tmem_ld16(ta + 32 * c, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
-        tmem_ld16(ta + 32 * c + 16,
-                  *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
-        tmem_ld_wait();
-        uint8_t* tile = stage_base + ob * WG_OUT_TILE;
-        if (lane == 0) bulk_wait_read_le1();
-        __syncwarp();
-        // row `lane`: 16-byte chunk k at position k ^ (lane & 7) (the
-        // 128-byte swizzle of the tensor map)
+      for (int mblk = w.mb0; mblk < w.mb1; ++mblk) {
+        const int m0 = mblk * BM;
+        if (w.rows == 0) {
+          // an expert with no tokens has a zero gradient
+          const int row = m0 + r;
+          if (!p.accumulate && row < w.M) {
+            float* out = p.out_r[w.mat] + (size_t)(w.seg - 1) * w.M * w.N;
+            float* orow = out + (size_t)row * w.N + w.n0;
+            for (int c = 32 * c_lo; c < min(w.nt, 32 * c_hi); c += 4)
+              *reinterpret_cast<float4*>(orow + c) = make_float4(0, 0, 0, 0);
+          }
+          continue;
+        }
+        int okw = 0;
+        if (lane == 0)
+          okw = mbar_wait_bounded(smem_u32(&tfull[slot]), (tph >> slot) & 1,
+                                  abort_flag, limit, p.status, kSiteEpilogue);
+        okw = __shfl_sync(0xffffffffu, okw, 0);
+        if (!okw) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t ta =
+            tmem_base + (static_cast<uint32_t>(q * 32) << 16) + slot * SLOT;
+        const int mrow = m0 + q * 32;        // first row of this warp
+        // a warp whose rows lie past M (a partial last block) has nothing
+        // to store; it skips the staging too, whose buffers the previous
+        // block's last stores may still be reading (bulk_wait_read_le1
+        // counts only committed stores)
+        if (mrow < w.M) {
+          for (int c = c_lo; c < c_hi; ++c) {
+            uint32_t v[32];
+            tmem_ld16(ta + 32 * c,
+                      *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
+            tmem_ld16(ta + 32 * c + 16,
+                      *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
+            tmem_ld_wait();
+            uint8_t* tile = stage_base + ob * WG_OUT_TILE;
+            if (lane == 0) bulk_wait_read_le1();
+            __syncwarp();
+            // row `lane`: 16-byte chunk k at position k ^ (lane & 7) (the
+            // 128-byte swizzle of the tensor map)
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint32_t a = smem_u32(tile + lane * 128 + ((k ^ (lane & 7)) * 16));
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a),
-                       "r"(v[4 * k]), "r"(v[4 * k + 1]), "r"(v[4 * k + 2]),
-                       "r"(v[4 * k + 3])
-                       : "memory");
+            for (int k = 0; k < 8; ++k) {
+              const uint32_t a =
+                  smem_u32(tile + lane * 128 + ((k ^ (lane & 7)) * 16));
+              asm volatile(
+                  "st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a),
+                  "r"(v[4 * k]), "r"(v[4 * k + 1]), "r"(v[4 * k + 2]),
+                  "r"(v[4 * k + 3])
+                  : "memory");
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              if (p.accumulate)
+                tma_reduce_add_3d(om, smem_u32(tile), w.n0 + 32 * c, mrow,
+                                  mat_idx, pol_out);
+              else
+                tma_store_3d(om, smem_u32(tile), w.n0 + 32 * c, mrow,
+                             mat_idx, pol_out);
+              bulk_commit();
+            }
+            ob = (ob + 1) % WG_OUT_BUFS;
+          }
         }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0 && mrow < w.M) {
-          if (p.accumulate)
-            tma_reduce_add_3d(om, smem_u32(tile), w.n0 + 32 * c, mrow,
-                              mat_idx, pol_out);
-          else
-            tma_store_3d(om, smem_u32(tile), w.n0 + 32 * c, mrow, mat_idx,
-                         pol_out);
-          bulk_commit();
-        }
-        ob = (ob + 1) % WG_OUT_BUFS;
+        tc_fence_before();
+        mbar_arrive(smem_u32(&tempty[slot]));
+        tph ^= 1u << slot;
+        slot ^= 1;
       }
-      tc_fence_before();
-      mbar_arrive(smem_u32(&tempty[slot]));
-      tph ^= 1u << slot;
-      slot ^= 1;
     }
     if (lane == 0) bulk_wait_all();
     __syncwarp();
@@ -1240,9 +1411,9 @@ __global__ void __launch_bounds__(kWgThreads, 1)
 }
 
 size_t wgrad_smem_bytes(int E) {
-  return 1024 + WG_STAGES * WG_STAGE_BYTES + WG_OUT_BYTES +
-         (2 * WG_STAGES + 5) * sizeof(uint64_t) + 4 * sizeof(uint32_t) +
-         sizeof(int) * (kMats * (E + 1) + 1 + 2 * (E + 1));
+  return 1024 + WG_BSLOTS * WG_B_BYTES + WG_ASTAGES * WG_A_BYTES +
+         WG_OUT_BYTES + kWgBars * sizeof(uint64_t) + 4 * sizeof(uint32_t) +
+         sizeof(int) * (WG_QN + kMats * (E + 1) + 1 + (E + 1));
 }
 
 bool token_maps(CUtensorMap (&m)[kTokBoxes], const void* base, uint64_t k,
@@ -1273,7 +1444,7 @@ int launch_expert_backward(const BwdArgs& a, cudaStream_t s) {
   mark(0);
   bwd_pad_kernel<<<(TK + kPadThreads - 1) / kPadThreads, kPadThreads, 0, s>>>(
       a.topk_idx, a.dest, a.offsets, a.counts, a.gate, TK, E, cap, a.poff,
-      a.pdest, a.gp, a.status);
+      a.pdest, a.gp, a.ticket, a.status);
   bwd_gather_kernel<<<T, kRowThreads, 0, s>>>(a.x, a.dout, a.pdest, H, K,
                                               a.xpp, a.dpp);
   bwd_zero_pad_kernel<<<E, kRowThreads, 0, s>>>(a.counts, a.poff, H, a.xpp,
@@ -1392,8 +1563,20 @@ int launch_expert_backward(const BwdArgs& a, cudaStream_t s) {
        make_tmap_bf16(&wp.a_s[2], a.dout, H, T, BK) &&
        make_tmap_bf16(&wp.b_s[0], a.x, H, T, BK) &&
        make_tmap_bf16(&wp.b_s[1], a.x, H, T, BK) &&
-       make_tmap_bf16(&wp.b_s[2], a.hg_s, Is, T, BK);
-  ok = make_tmap_f32_3d_store(&wp.o_r[0], a.dw1, H, I, E) &&
+       make_tmap_bf16(&wp.b_s[2], a.hg_s, Is, T, BK) &&
+       make_tmap_bf16(&wp.a_r16[0], a.dp_r, I, cap, 16) &&
+       make_tmap_bf16(&wp.a_r16[1], a.dq_r, I, cap, 16) &&
+       make_tmap_bf16(&wp.a_r16[2], a.dpp, H, cap, 16) &&
+       make_tmap_bf16(&wp.b_r16[0], a.xpp, H, cap, 16) &&
+       make_tmap_bf16(&wp.b_r16[1], a.xpp, H, cap, 16) &&
+       make_tmap_bf16(&wp.b_r16[2], a.hg_r, I, cap, 16) &&
+       make_tmap_bf16(&wp.a_s16[0], a.dp_s, Is, T, 16) &&
+       make_tmap_bf16(&wp.a_s16[1], a.dq_s, Is, T, 16) &&
+       make_tmap_bf16(&wp.a_s16[2], a.dout, H, T, 16) &&
+       make_tmap_bf16(&wp.b_s16[0], a.x, H, T, 16) &&
+       make_tmap_bf16(&wp.b_s16[1], a.x, H, T, 16) &&
+       make_tmap_bf16(&wp.b_s16[2], a.hg_s, Is, T, 16);
+  ok = ok && make_tmap_f32_3d_store(&wp.o_r[0], a.dw1, H, I, E) &&
        make_tmap_f32_3d_store(&wp.o_r[1], a.dw3, H, I, E) &&
        make_tmap_f32_3d_store(&wp.o_r[2], a.dw2, I, H, E) &&
        make_tmap_f32_3d_store(&wp.o_s[0], a.dws1, H, Is, 1) &&
@@ -1401,6 +1584,7 @@ int launch_expert_backward(const BwdArgs& a, cudaStream_t s) {
        make_tmap_f32_3d_store(&wp.o_s[2], a.dws2, Is, H, 1);
   if (!ok) return MOE_ERR_CUDA;
   wp.poff = a.poff;
+  wp.ticket = a.ticket;
   wp.out_r[0] = a.dw1;
   wp.out_r[1] = a.dw3;
   wp.out_r[2] = a.dw2;

@@ -128,6 +128,7 @@ struct BwdArgs {
   const float* gate;                         // [T, K]
   const uint16_t *w1, *w3, *w2, *ws1, *ws3, *ws2;
   int32_t *poff, *pdest;                     // [E+1], [T*K]
+  int* ticket;                               // [1] weight-gradient tasks
   float* gp;                                 // [cap]
   uint16_t *xpp, *dpp;                       // [cap, H]
   float *p_r, *q_r;                          // [cap, I]

@@ -96,7 +96,7 @@ struct Layout {
   size_t f8_mq = 0, f8_ms = 0, f8_msq = 0, f8_mss = 0;  // FP8 intermediate
   size_t mx_mq = 0, mx_ms = 0, mx_msq = 0, mx_mss = 0;  // its UE8M0 form
   // expert backward (padded dispatch of cap rows)
-  size_t b_poff = 0, b_pdest = 0, b_gp = 0, b_xpp = 0, b_dpp = 0, b_p = 0,
+  size_t b_poff = 0, b_ticket = 0, b_pdest = 0, b_gp = 0, b_xpp = 0, b_dpp = 0, b_p = 0,
          b_q = 0, b_hg = 0, b_dp = 0, b_dq = 0, b_dgp = 0, b_dxpp = 0,
          b_ps = 0, b_qs = 0, b_hgs = 0, b_dps = 0, b_dqs = 0, b_dxs = 0;
   size_t total = 0;
@@ -138,6 +138,7 @@ Layout layout(const moe_dims_t* d, moe_ws_kind_t which) {
     L.dest = take(T * K * 4);
     L.src_row = take(T * K * 4);
     L.b_poff = take((E + 1) * 4);
+    L.b_ticket = take(4);
     L.b_pdest = take(T * K * 4);
     L.b_gp = take(cap * 4);
     L.b_xpp = take(cap * H * 2);
@@ -1024,6 +1025,7 @@ moe_status_t moe_expert_backward(const moe_dims_t* d, const moe_weights_t* w,
   a.ws3 = w->ws3;
   a.ws2 = w->ws2;
   a.poff = at<int32_t>(ws, L.b_poff);
+  a.ticket = at<int>(ws, L.b_ticket);
   a.pdest = at<int32_t>(ws, L.b_pdest);
   a.gp = at<float>(ws, L.b_gp);
   a.xpp = at<uint16_t>(ws, L.b_xpp);

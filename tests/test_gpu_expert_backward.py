@@ -224,6 +224,28 @@ def test_backward_unused_expert_single_row_expert_and_full_segments():
     _small_case(cfg, idx)
 
 
+def test_backward_resident_and_streamed_segments_and_row_block_groups():
+    """The weight-gradient GEMM keeps a segment's B operand in shared
+    memory when the segment has at most 192 rows and streams it otherwise:
+    expert 1 gets 210 rows (224 padded: streamed, four reduction blocks),
+    expert 3 150 (160: resident, a 32-row tail), expert 0 16, expert 2
+    none, the shared expert 260 (streamed, a 4-row tail past which the map
+    ends).  H = 2176 gives dW2 17 row blocks (a group of 16 and one more)
+    and dW1 / dW3 a partial 256-column block."""
+    cfg = inputs.custom_config("bwd_g", 803, T=260, H=2176, E=8, n_group=4,
+                               topk_group=2, topk=2, I=128, I_shared=64)
+    T = cfg.T
+    idx = np.zeros((T, 2), np.int32)
+    idx[:210, 0] = 1
+    idx[210:, 0] = 3
+    idx[:100, 1] = 3
+    idx[100:116, 1] = 0
+    idx[116:, 1] = np.array([4, 5, 6, 7] * 36)
+    counts = np.bincount(idx.ravel(), minlength=8)
+    assert counts.tolist() == [16, 210, 0, 150, 36, 36, 36, 36]
+    _small_case(cfg, idx)
+
+
 def test_backward_accumulates_into_the_weight_gradients():
     """accumulate != 0 adds to the arrays: a second call on the same inputs
     doubles every weight gradient exactly (x + x is exact in fp32)."""
