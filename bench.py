@@ -227,25 +227,24 @@ def config_json(cfg, n_gpus):
                   "per step; 4 rotating activation batches"}
 
 
-def e2e_loop(step, xs, T, H, steps, stream, barrier=lambda: None):
-    """End to end with host buffers: every step uploads its x [T, H] bf16
-    from pinned host memory and downloads its output [T, H] bf16 into
-    pinned host memory.  The copies run on their own streams with
-    double-buffered device x / out, so that step i+1's upload and step i's
-    download overlap step i's compute.  step(x_dev, out_dev) enqueues one
-    layer on `stream`.  Returns the elapsed ms of `steps` steps."""
+def e2e_loop_multi(step, host_in, out_like, steps, stream,
+                   barrier=lambda: None):
+    """End to end with host buffers: every step uploads its inputs from
+    pinned host memory and downloads its outputs into pinned host memory.
+    host_in[b] is the list of pinned host inputs of batch b (steps cycle
+    over the batches); out_like lists (shape, dtype) of the outputs.  The
+    copies run on their own streams with double-buffered device inputs and
+    outputs, so that step i+1's uploads and step i's downloads overlap
+    step i's compute.  step(ins_dev, outs_dev) enqueues one step on
+    `stream`.  Returns the elapsed ms of `steps` steps."""
     import torch
-    NB = len(xs)
-    xh = [torch.empty((T, H), dtype=torch.int16).pin_memory()
-          for _ in range(NB)]
-    for i in range(NB):
-        xh[i].copy_(xs[i].cpu())
-    oh = [torch.empty((T, H), dtype=torch.int16).pin_memory()
-          for _ in range(2)]
-    xd = [torch.empty((T, H), dtype=torch.int16, device="cuda")
-          for _ in range(2)]
-    od = [torch.empty((T, H), dtype=torch.int16, device="cuda")
-          for _ in range(2)]
+    NB = len(host_in)
+    ind = [[torch.empty_like(t, device="cuda") for t in host_in[0]]
+           for _ in range(2)]
+    outd = [[torch.empty(sh, dtype=dt, device="cuda") for sh, dt in out_like]
+            for _ in range(2)]
+    outh = [[torch.empty(sh, dtype=dt).pin_memory() for sh, dt in out_like]
+            for _ in range(2)]
     up_s, dn_s = torch.cuda.Stream(), torch.cuda.Stream()
     ev = lambda: torch.cuda.Event()  # noqa: E731
     h2d_done = [ev() for _ in range(2)]
@@ -261,17 +260,19 @@ def e2e_loop(step, xs, T, H, steps, stream, barrier=lambda: None):
     dn_s.wait_event(e0)
     for i in range(steps):
         b = i % 2
-        up_s.wait_event(comp_done[b])          # xd[b] no longer read
+        up_s.wait_event(comp_done[b])          # ind[b] no longer read
         with torch.cuda.stream(up_s):
-            xd[b].copy_(xh[i % NB], non_blocking=True)
+            for dst, src in zip(ind[b], host_in[i % NB]):
+                dst.copy_(src, non_blocking=True)
         h2d_done[b].record(up_s)
         stream.wait_event(h2d_done[b])
-        stream.wait_event(d2h_done[b])         # od[b] already downloaded
-        step(xd[b], od[b])
+        stream.wait_event(d2h_done[b])         # outd[b] already downloaded
+        step(ind[b], outd[b])
         comp_done[b].record(stream)
         dn_s.wait_event(comp_done[b])
         with torch.cuda.stream(dn_s):
-            oh[b].copy_(od[b], non_blocking=True)
+            for dst, src in zip(outh[b], outd[b]):
+                dst.copy_(src, non_blocking=True)
         d2h_done[b].record(dn_s)
     stream.wait_event(d2h_done[(steps - 1) % 2])
     stream.wait_event(d2h_done[steps % 2])
@@ -279,6 +280,15 @@ def e2e_loop(step, xs, T, H, steps, stream, barrier=lambda: None):
     barrier()
     torch.cuda.synchronize()
     return e0.elapsed_time(e1)
+
+
+def e2e_loop(step, xs, T, H, steps, stream, barrier=lambda: None):
+    """e2e_loop_multi for a layer with one input x [T, H] bf16 and one
+    output [T, H] bf16: step(x_dev, out_dev)."""
+    import torch
+    host_in = [[xs[i].cpu().pin_memory()] for i in range(len(xs))]
+    return e2e_loop_multi(lambda i_, o_: step(i_[0], o_[0]), host_in,
+                          [((T, H), torch.int16)], steps, stream, barrier)
 
 
 def run_gpu(args, rank, world, local_rank):
@@ -992,10 +1002,12 @@ def run_decode_fp8_reference(args):
 
 def run_backward_gpu(args, rank, world, local_rank):
     """The routing side of a training step's backward at the V3 shape: per
-    step, moe_route_backward (the gates' gradient to the logits) and
-    moe_seq_balance_loss_backward accumulated into the same dlogits, on
-    T=16384 fp32 logits (four 4096-token sequences).  8 rotating batches
-    (134 MB of logits > L2), replayed from a CUDA graph."""
+    step, moe_route_balance_backward (the gates' gradient and the
+    sequence-wise balance loss's gradient to the logits in one pass; equal
+    bit for bit to moe_route_backward followed by
+    moe_seq_balance_loss_backward), on T=16384 fp32 logits (four 4096-token
+    sequences).  8 rotating batches (134 MB of logits > L2), replayed from a
+    CUDA graph."""
     import torch
     from deepseekmoe_routing_expert_moe_b300 import inputs, ops
     torch.cuda.set_device(local_rank)
@@ -1031,10 +1043,9 @@ def run_backward_gpu(args, rank, world, local_rank):
     stream = torch.cuda.current_stream()
 
     def step(i):
-        ops.moe_route_backward(d, zs[i % NB], idxs[i % NB], dgate, dz, ws)
-        ops.moe_seq_balance_loss_backward(d, zs[i % NB], S, 1e-4,
-                                          cnts[i % NB], dz, dloss=dloss,
-                                          accumulate=True)
+        ops.moe_route_balance_backward(d, zs[i % NB], idxs[i % NB], dgate, S,
+                                       1e-4, cnts[i % NB], dz, ws,
+                                       dloss=dloss)
 
     for i in range(args.warmup):
         step(i)
@@ -1071,8 +1082,8 @@ def run_backward_gpu(args, rank, world, local_rank):
             "peak": hbm, "unit": "GB/s"}
     roof["frac"] = round(roof["achieved"] / hbm, 4)
     roof["traffic"] = None
-    roof["kernel"] = ("route_backward_kernel + balance_backward_kernel "
-                      "(the latter re-reads the logits and accumulates)")
+    roof["kernel"] = ("route_balance_backward_kernel (both gradients, the "
+                      "logits read once, dlogits written once)")
     roof["algorithmic_bytes"] = int(alg)
     roof["peak_source"] = f"{pk_src} (MEASURED_PEAKS.json)"
     return {
@@ -1090,7 +1101,7 @@ def run_backward_gpu(args, rank, world, local_rank):
                    "T": T, "E": E, "topk": K, "seq_len": S,
                    "l2": "8 rotating logits batches, 134 MB > L2"},
         "roofline": roof,
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": args.steps,
         "clocks": clk.summary(),
         "impl": "b300",
     }
@@ -1228,26 +1239,18 @@ def run_expert_backward_gpu(args, rank, world, local_rank):
     roof["peak_source"] = f"{pk_src} (MEASURED_PEAKS.json)"
     # end to end: x and dout uploaded from pinned memory, dx and the gate
     # gradients read back every step (the weight gradients stay on the
-    # device for the optimizer)
-    xh = [xs[i].cpu().pin_memory() for i in range(NB)]
-    dh = [dos[i].cpu().pin_memory() for i in range(NB)]
-    xd = torch.empty_like(xs[0])
-    dd_ = torch.empty_like(dos[0])
-    dxh = torch.empty((T, H), dtype=torch.int16).pin_memory()
-    dgh = torch.empty((T, K), dtype=torch.float32).pin_memory()
-    torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for i in range(args.steps):
-        xd.copy_(xh[i % NB], non_blocking=True)
-        dd_.copy_(dh[i % NB], non_blocking=True)
-        step(i, xd, dd_)
-        dxh.copy_(dx, non_blocking=True)
-        dgh.copy_(dg, non_blocking=True)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
+    # device for the optimizer); the copies of neighbouring steps overlap
+    # the compute (e2e_loop_multi)
+    host_in = [[xs[i].cpu().pin_memory(), dos[i].cpu().pin_memory()]
+               for i in range(NB)]
+    cnt = [0]
+
+    def e2e_step(ins, outs):
+        step(cnt[0], ins[0], ins[1], outs[0], outs[1])
+        cnt[0] += 1
+    e2e_ms = e2e_loop_multi(e2e_step, host_in,
+                            [((T, H), torch.int16), ((T, K), torch.float32)],
+                            args.steps, stream)
     assert ops.moe_get_device_error(ws) == 0
     res = {
         "metric": "tokens/s through the experts' backward (recompute, dgrad, "

@@ -71,6 +71,12 @@ cudaError_t launch_seq_balance_backward(const float* logits, int T, int E,
                                         const int32_t* counts_seq,
                                         const float* dloss, int accumulate,
                                         float* dz, cudaStream_t s);
+// both: the gates' term, then the balance term, in one pass
+cudaError_t launch_route_balance_backward(
+    const float* logits, const int32_t* idx, const float* dgate, int T,
+    int E, int K, int seq_len, float alpha, const int32_t* counts_seq,
+    const float* dloss, int accumulate, float* dz, DevStatus* st,
+    cudaStream_t s);
 constexpr int kBalSplitTarget = 148;  // split up to 2 x this many CTAs
 constexpr long long kBalPartialElems = 2LL * kBalSplitTarget * 32;
 int seq_balance_splits(int T, int E, int seq_len);

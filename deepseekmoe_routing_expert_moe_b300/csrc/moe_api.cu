@@ -1100,6 +1100,32 @@ moe_status_t moe_seq_balance_loss_backward(const moe_dims_t* d,
       accumulate, dlogits, cs(stream)));
 }
 
+moe_status_t moe_route_balance_backward(
+    const moe_dims_t* d, const float* logits, const int32_t* topk_idx,
+    const float* dgate, int32_t seq_len, float alpha,
+    const int32_t* counts_seq, const float* dloss, int accumulate,
+    float* dlogits, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRY(check_dims(d, false));
+  if (seq_len < 1 || !std::isfinite(alpha)) return MOE_ERR_INVALID_ARG;
+  MOE_NEED_T(logits);
+  MOE_NEED_T(topk_idx);
+  MOE_NEED_T(dgate);
+  MOE_NEED_T(counts_seq);
+  MOE_NEED_T(dlogits);
+  MOE_ALIGN(logits);
+  MOE_ALIGN(topk_idx);
+  MOE_ALIGN(dgate);
+  MOE_ALIGN(counts_seq);
+  MOE_ALIGN(dloss);
+  MOE_ALIGN(dlogits);
+  MOE_TRY(check_ws(d, MOE_WS_ROUTE, ws, ws_bytes));
+  if (d->T == 0) return MOE_OK;
+  return cuda_ok(moe::launch_route_balance_backward(
+      logits, topk_idx, dgate, d->T, d->E, d->topk, seq_len, alpha,
+      counts_seq, dloss, accumulate, dlogits, at<DevStatus>(ws, 0),
+      cs(stream)));
+}
+
 moe_status_t moe_bias_update(const moe_dims_t* d, const int32_t* counts,
                              float* bias, float* load_stats,
                              moe_stream_t stream) {

@@ -737,6 +737,116 @@ __global__ void __launch_bounds__(WARPS * 32)
   store_row<EPL>(dz + (size_t)t * E + lane * EPL, o);
 }
 
+// Both gradients of one token in one pass (the gates' and the balance
+// loss's): the logits row is read once, the sigmoid of every expert is
+// taken once, and dz is written once.  The arithmetic and its order are
+// those of route_backward_kernel followed by balance_backward_kernel with
+// accumulate set (the gates' term is added first, then the balance term),
+// so the result equals the two calls' bit for bit.
+// (latency-bound: with at most eight experts per lane, eight blocks per SM
+// keep the most tokens in flight; wider rows would spill at that register
+// budget)
+template <int EPL, int WARPS>
+__global__ void __launch_bounds__(WARPS * 32, EPL <= 8 ? 8 : 1)
+    route_balance_backward_kernel(
+        const float* __restrict__ logits, const int32_t* __restrict__ idx,
+        const float* __restrict__ dgate, int T, int E, int K, int S,
+        float alpha, const int32_t* __restrict__ counts,
+        const float* __restrict__ dloss, int accumulate,
+        float* __restrict__ dz, DevStatus* st) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * WARPS + warp;
+  if (t >= T) return;
+  const bool active = lane < E / EPL;
+  // ---- the gates' term (lanes k < K hold the k-th chosen expert)
+  int e = -1;
+  float sk = 0.f, dg = 0.f;
+  if (lane < K) {
+    e = idx[(size_t)t * K + lane];
+    if (e >= 0 && e < E) {
+      sk = sigmoid_f32(logits[(size_t)t * E + e]);
+      dg = dgate[(size_t)t * K + lane];
+    } else {
+      record_error(st, MOE_ERR_DEVICE_BOUNDS, 50);
+      e = -1;
+    }
+  }
+  float D = sk;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1)
+    D = __fadd_rn(D, __shfl_xor_sync(0xffffffffu, D, off));
+  const float rD = D > 0.f ? __frcp_rn(D) : 0.f;
+  float gdot = __fmul_rn(dg, __fmul_rn(sk, rD));
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1)
+    gdot = __fadd_rn(gdot, __shfl_xor_sync(0xffffffffu, gdot, off));
+  const float c = __fmul_rn(__fmul_rn(__fmul_rn(sk, __fsub_rn(1.f, sk)), rD),
+                            __fsub_rn(dg, gdot));
+  // ---- the balance term's per-token sums
+  const int q = t / S;
+  int a, b;
+  seq_range(q, S, T, a, b);
+  const int Ts = b - a;
+  float s[EPL], f[EPL];
+  if (active) {
+    load_row<EPL>(logits + (size_t)t * E + lane * EPL, s);
+#pragma unroll
+    for (int j = 0; j < EPL; ++j) {
+      s[j] = sigmoid_f32(s[j]);
+      f[j] = __fdiv_rn(
+          __fmul_rn((float)E,
+                    (float)counts[(size_t)q * E + lane * EPL + j]),
+          (float)(K * Ts));
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < EPL; ++j) s[j] = f[j] = 0.f;
+  }
+  float Ssum = 0.f, dot = 0.f;
+#pragma unroll
+  for (int j = 0; j < EPL; ++j) {
+    Ssum = __fadd_rn(Ssum, s[j]);
+    dot = __fadd_rn(dot, __fmul_rn(f[j], s[j]));
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    Ssum = __fadd_rn(Ssum, __shfl_xor_sync(0xffffffffu, Ssum, off));
+    dot = __fadd_rn(dot, __shfl_xor_sync(0xffffffffu, dot, off));
+  }
+  const float rS = __frcp_rn(Ssum);
+  dot = __fmul_rn(dot, rS);
+  const float pre = __fdiv_rn(
+      __fmul_rn(dloss != nullptr ? dloss[q] : 1.f, alpha), (float)Ts);
+  // ---- dz = (dz or 0) + the gates' term + the balance term
+  float o[EPL];
+  if (active && accumulate) {
+    load_row<EPL>(dz + (size_t)t * E + lane * EPL, o);
+  } else {
+#pragma unroll
+    for (int j = 0; j < EPL; ++j) o[j] = 0.f;
+  }
+  for (int k = 0; k < K; ++k) {
+    const int ek = __shfl_sync(0xffffffffu, e, k);
+    const float ck = __shfl_sync(0xffffffffu, c, k);
+    if (ek >= 0 && lane == ek / EPL) {
+      const int jj = ek - lane * EPL;
+#pragma unroll
+      for (int j = 0; j < EPL; ++j)
+        if (j == jj) o[j] = __fadd_rn(o[j], ck);
+    }
+  }
+  if (!active) return;
+#pragma unroll
+  for (int j = 0; j < EPL; ++j) {
+    const float gj = __fmul_rn(
+        __fmul_rn(__fmul_rn(pre, __fmul_rn(s[j], __fsub_rn(1.f, s[j]))),
+                  rS),
+        __fsub_rn(f[j], dot));
+    o[j] = __fadd_rn(o[j], gj);
+  }
+  store_row<EPL>(dz + (size_t)t * E + lane * EPL, o);
+}
+
 // histogram of an existing topk_idx over the same token blocks
 __global__ void __launch_bounds__(256)
     block_counts_kernel(const int32_t* __restrict__ topk_idx, int T, int E,
@@ -1215,6 +1325,35 @@ cudaError_t launch_seq_balance_backward(const float* logits, int T, int E,
       return cudaErrorInvalidValue;
   }
 #undef MOE_BB_CASE
+  return cudaGetLastError();
+}
+
+cudaError_t launch_route_balance_backward(
+    const float* logits, const int32_t* idx, const float* dgate, int T,
+    int E, int K, int seq_len, float alpha, const int32_t* counts_seq,
+    const float* dloss, int accumulate, float* dz, DevStatus* st,
+    cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  const int epl = E <= 32 ? 1 : E / 32;
+  const int nblk = (T + kBalWarps - 1) / kBalWarps;
+#define MOE_RBB_CASE(N)                                                     \
+  case N:                                                                   \
+    route_balance_backward_kernel<N, kBalWarps>                             \
+        <<<nblk, kBalWarps * 32, 0, s>>>(logits, idx, dgate, T, E, K,       \
+                                         seq_len, alpha, counts_seq, dloss, \
+                                         accumulate, dz, st);               \
+    break;
+  switch (epl) {
+    MOE_RBB_CASE(1)
+    MOE_RBB_CASE(2)
+    MOE_RBB_CASE(4)
+    MOE_RBB_CASE(8)
+    MOE_RBB_CASE(16)
+    MOE_RBB_CASE(32)
+    default:
+      return cudaErrorInvalidValue;
+  }
+#undef MOE_RBB_CASE
   return cudaGetLastError();
 }
 

@@ -101,6 +101,9 @@ _SIGS = {
     "moe_seq_balance_loss_backward": (_I, [_D, _P, ctypes.c_int32,
                                            ctypes.c_float, _P, _P, _I, _P,
                                            _P]),
+    "moe_route_balance_backward": (_I, [_D, _P, _P, _P, ctypes.c_int32,
+                                        ctypes.c_float, _P, _P, _I, _P, _P,
+                                        _S, _P]),
     "moe_forward": (_I, [_D, _W, _P, _P, _I, _P, _P, _P, _P, _P, _P, _P, _S,
                          _P]),
     "moe_status_string": (ctypes.c_char_p, [_I]),
@@ -475,6 +478,17 @@ def moe_seq_balance_loss_backward(d, logits, seq_len, alpha, counts_seq,
                ctypes.byref(d), _ptr(logits), int(seq_len), float(alpha),
                _ptr(counts_seq), _ptr(dloss), 1 if accumulate else 0,
                _ptr(dlogits), _stream(stream)))
+
+
+def moe_route_balance_backward(d, logits, topk_idx, dgate, seq_len, alpha,
+                               counts_seq, dlogits, ws, dloss=None,
+                               accumulate=False, stream=None):
+    _check("moe_route_balance_backward",
+           lib().moe_route_balance_backward(
+               ctypes.byref(d), _ptr(logits), _ptr(topk_idx), _ptr(dgate),
+               int(seq_len), float(alpha), _ptr(counts_seq), _ptr(dloss),
+               1 if accumulate else 0, _ptr(dlogits), _ptr(ws), ws.numel(),
+               _stream(stream)))
 
 
 def moe_forward(d, w: Weights, x, bias, out, ws, update_bias=False,

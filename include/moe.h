@@ -53,7 +53,7 @@
 extern "C" {
 #endif
 
-#define MOE_ABI_VERSION 3
+#define MOE_ABI_VERSION 4
 
 typedef enum {
   MOE_OK = 0,
@@ -359,6 +359,27 @@ moe_status_t moe_seq_balance_loss_backward(const moe_dims_t* d,
                                            const float* dloss, int accumulate,
                                            float* dlogits,
                                            moe_stream_t stream);
+
+/* moe_route_balance_backward: both of the above in one pass, for a
+ * training step that backpropagates the gates and the sequence-wise
+ * balance loss through the same logits: dlogits = (dlogits when
+ * accumulate != 0, else 0) + the gates' term of moe_route_backward + the
+ * balance term of moe_seq_balance_loss_backward, added in that order, so
+ * the result equals moe_route_backward followed by
+ * moe_seq_balance_loss_backward with accumulate set, bit for bit.  Each
+ * logits row is read once and each sigmoid taken once.  Arguments as in
+ * those two calls; an expert id outside [0, E) is skipped and records
+ * MOE_ERR_DEVICE_BOUNDS in the workspace error word.
+ * Workspace: MOE_WS_ROUTE (only its error word is used). */
+moe_status_t moe_route_balance_backward(const moe_dims_t* d,
+                                        const float* logits,
+                                        const int32_t* topk_idx,
+                                        const float* dgate, int32_t seq_len,
+                                        float alpha,
+                                        const int32_t* counts_seq,
+                                        const float* dloss, int accumulate,
+                                        float* dlogits, void* ws,
+                                        size_t ws_bytes, moe_stream_t stream);
 
 /* FP8 (E4M3) fine-grained quantization ("02 · DeepSeek-V3" §2, mixed
  * precision): every group of 128 x 128 weights or 1 x 128 activations

@@ -93,6 +93,9 @@ def _calls(L, d, fault, which, ws_bytes):
             by(d), by(weightsmx(P)), A, A, A, A, A, A, A, A, ws_bytes, None)),
         "moe_route_backward": (4, lambda P: L.moe_route_backward(
             by(d), P(0), P(1), P(2), 0, P(3), A, ws_bytes, None)),
+        "moe_route_balance_backward": (5, lambda P: L.moe_route_balance_backward(
+            by(d), P(0), P(1), P(2), 64, 1e-4, P(3), None, 0, P(4), A,
+            ws_bytes, None)),
     }
     return {n: (lambda f=f, c=c: f(picker(c))) for n, (c, f) in table.items()}
 

@@ -42,7 +42,7 @@ def test_library_exports_every_declared_symbol(L):
 
 
 def test_abi_version_and_status_strings(L):
-    assert ops.moe_abi_version() == 3
+    assert ops.moe_abi_version() == 4
     for code, name in ops.STATUS.items():
         assert ops.moe_status_string(code) == name
 
@@ -304,6 +304,22 @@ def test_routing_backward_validation(L):
     assert bb(by(d), FAKE, 64, 1e-4, FAKE, FAKE + 4, 0, FAKE, None) == 3
     assert bb(by(ops.dims(**dict(V3, T=0))), None, 64, 1e-4, None, None, 0,
               None, None) == 0
+    fb = L.moe_route_balance_backward
+
+    def fused(dd=d, logits=FAKE, idx=FAKE, dg=FAKE, S=64, alpha=1e-4,
+              counts=FAKE, dloss=None, out=FAKE, ws_bytes=1 << 30):
+        return fb(by(dd), logits, idx, dg, S, alpha, counts, dloss, 0, out,
+                  FAKE, ws_bytes, None)
+    assert fused(idx=None) == 1
+    assert fused(counts=None) == 1
+    assert fused(S=0) == 1
+    assert fused(alpha=float("inf")) == 1
+    assert fused(dloss=FAKE + 4) == 3
+    assert fused(dg=FAKE + 2) == 3
+    assert fused(ws_bytes=8) == 4
+    assert fused(dd=ops.dims(**dict(V3, E=255))) == 1
+    assert fused(dd=ops.dims(**dict(V3, T=0)), logits=None, idx=None,
+                 dg=None, counts=None, out=None, ws_bytes=1 << 20) == 0
 
 
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):

@@ -183,3 +183,81 @@ def test_seq_balance_loss_backward_default_upstream_is_one():
     ref = O.seq_balance_loss_backward(z, 256, 8)
     np.testing.assert_allclose(host(out), ref, rtol=1e-4,
                                atol=1e-6 * np.abs(ref).max())
+
+
+@pytest.mark.parametrize("E,K,T,S", [(256, 8, 4096, 1000), (16, 4, 300, 64),
+                                     (1024, 8, 200, 77), (32, 32, 100, 100),
+                                     (64, 6, 777, 1)])
+@pytest.mark.parametrize("accumulate", [False, True])
+@pytest.mark.parametrize("with_dloss", [False, True])
+def test_route_balance_backward_equals_the_two_calls(E, K, T, S, accumulate,
+                                                     with_dloss):
+    """moe_route_balance_backward gives moe_route_backward followed by
+    moe_seq_balance_loss_backward (accumulate set) bit for bit, and both
+    gradients' sum within the two bounds of the oracle's."""
+    cfg = _cfg(E, K)
+    d = ops.dims_of(cfg, T=T)
+    z = _logits(cfg, T, 31 + E + K)
+    idx = O.route(z, np.zeros(E, np.float32), cfg.n_group, cfg.topk_group,
+                  K)["idx"]
+    dg = np.random.default_rng(9).standard_normal((T, K)).astype(np.float32)
+    alpha = 1e-4
+    n_seq = -(-T // S)
+    dloss = (np.random.default_rng(10).standard_normal(n_seq).astype(
+        np.float32) if with_dloss else None)
+    dl64 = (dloss.astype(np.float64) if with_dloss else np.ones(n_seq))
+    fw, bbound = _balance_bound(z, S, K, alpha, dl64, E)
+    prev = np.random.default_rng(12).standard_normal((T, E)).astype(
+        np.float32) * 1e-6
+    ws = ops.workspace(d, ops.MOE_WS_ROUTE)
+    two = dev(prev) if accumulate else torch.full(
+        (T, E), 7.0, dtype=torch.float32, device="cuda")
+    ops.moe_route_backward(d, dev(z), dev(idx), dev(dg), two, ws,
+                           accumulate=accumulate)
+    ops.moe_seq_balance_loss_backward(
+        d, dev(z), S, alpha, dev(fw["counts"]), two,
+        dloss=dev(dloss) if with_dloss else None, accumulate=True)
+    one = dev(prev) if accumulate else torch.full(
+        (T, E), 7.0, dtype=torch.float32, device="cuda")
+    ops.moe_route_balance_backward(
+        d, dev(z), dev(idx), dev(dg), S, alpha, dev(fw["counts"]), one, ws,
+        dloss=dev(dloss) if with_dloss else None, accumulate=accumulate)
+    assert ops.moe_get_device_error(ws) == 0
+    a, b = host(two), host(one)
+    assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+    ref = (O.route_backward(z, idx, dg.astype(np.float64)) +
+           O.seq_balance_loss_backward(z, S, K, alpha, dl64))
+    bound = _route_bound(z, idx, dg.astype(np.float64)) + bbound + \
+        U * np.abs(ref)
+    if accumulate:
+        ref = ref + prev
+        bound = bound + U * np.abs(ref)
+    over = np.abs(b.astype(np.float64) - ref) > bound
+    assert not over.any(), (int(over.sum()), np.abs(b - ref)[over][:4],
+                            bound[over][:4])
+
+
+def test_route_balance_backward_bad_index_is_reported_and_skipped():
+    cfg = _cfg(16, 4)
+    T, S = 64, 32
+    d = ops.dims_of(cfg, T=T)
+    z = _logits(cfg, T, 5)
+    idx = O.route(z, np.zeros(16, np.float32), cfg.n_group, cfg.topk_group,
+                  4)["idx"]
+    dg = np.random.default_rng(4).standard_normal((T, 4)).astype(np.float32)
+    bad = idx.copy()
+    bad[9, 2] = 99
+    fw = O.seq_balance_loss(z, S, 4, 1e-4)
+    ws = ops.workspace(d, ops.MOE_WS_ROUTE)
+    two = torch.zeros((T, 16), dtype=torch.float32, device="cuda")
+    ops.moe_route_backward(d, dev(z), dev(bad), dev(dg), two, ws)
+    ops.moe_seq_balance_loss_backward(d, dev(z), S, 1e-4, dev(fw["counts"]),
+                                      two, accumulate=True)
+    ws2 = ops.workspace(d, ops.MOE_WS_ROUTE)
+    one = torch.zeros((T, 16), dtype=torch.float32, device="cuda")
+    ops.moe_route_balance_backward(d, dev(z), dev(bad), dev(dg), S, 1e-4,
+                                   dev(fw["counts"]), one, ws2)
+    for w in (ws, ws2):
+        assert ops.moe_get_device_error(w) == ops.STATUS_CODES[
+            "MOE_ERR_DEVICE_BOUNDS"]
+    assert np.array_equal(host(two).view(np.uint32), host(one).view(np.uint32))

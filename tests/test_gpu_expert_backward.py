@@ -246,6 +246,55 @@ def test_backward_resident_and_streamed_segments_and_row_block_groups():
     _small_case(cfg, idx)
 
 
+def test_backward_repeats_bit_exactly_on_one_workspace():
+    """Calls on one workspace give the same results bit for bit: the
+    weight-gradient GEMM's task counter lives in the workspace and every
+    call resets it, also when the call is replayed from a CUDA graph (no
+    host step between the replays)."""
+    import torch
+    cfg = inputs.custom_config("bwd_rep", 804, T=96, H=256, E=8, n_group=4,
+                               topk_group=2, topk=2, I=128, I_shared=64,
+                               router_sigma=0.05)
+    d = ops.dims_of(cfg)
+    T, K, E = cfg.T, cfg.topk, cfg.E
+    w = inputs.layer_inputs(cfg)
+    z = O.router_logits(f32(w["x"]), w["w_router"])
+    r = O.route(z, w["bias"], cfg.n_group, cfg.topk_group, K)
+    W = ops.Weights(torch.zeros(E, cfg.H, dtype=torch.float32, device="cuda"),
+                    dev(w["w1"]), dev(w["w3"]), dev(w["w2"]), dev(w["ws1"]),
+                    dev(w["ws3"]), dev(w["ws2"]))
+    args = (dev(w["x"]), dev(_dout(cfg, T)), dev(r["idx"]), dev(r["gate"]))
+    ws = ops.workspace(d, ops.MOE_WS_EXPERT_BWD)
+    outs = []
+    for _ in range(3):
+        dx = torch.empty((T, cfg.H), dtype=torch.int16, device="cuda")
+        dg = torch.empty((T, K), dtype=torch.float32, device="cuda")
+        grads = ops.WeightGrads.empty(d)
+        for t in grads.tensors():
+            t.fill_(float("nan"))
+        outs.append((dx, dg, grads))
+    for dx, dg, grads in outs[:2]:
+        ops.moe_expert_backward(d, W, *args, dx, dg, grads, ws)
+    dx, dg, grads = outs[2]
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g, stream=side):
+            ops.moe_expert_backward(d, W, *args, dx, dg, grads, ws)
+    torch.cuda.current_stream().wait_stream(side)
+    g.replay()
+    g.replay()
+    torch.cuda.synchronize()
+    assert ops.moe_get_device_error(ws) == 0
+    ref = [host(t) for t in (outs[0][0], outs[0][1], *outs[0][2].tensors())]
+    assert all(np.isfinite(a).all() for a in ref[1:])
+    for dx_, dg_, gr_ in outs[1:]:
+        got = [host(t) for t in (dx_, dg_, *gr_.tensors())]
+        for a, b in zip(ref, got):
+            assert np.array_equal(a.view(np.uint8), b.view(np.uint8))
+
+
 def test_backward_accumulates_into_the_weight_gradients():
     """accumulate != 0 adds to the arrays: a second call on the same inputs
     doubles every weight gradient exactly (x + x is exact in fp32)."""
