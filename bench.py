@@ -151,6 +151,14 @@ def ncu_traffic(kernel: str, workload: str):
         return None
 
 
+def route_blocks(T):
+    """Routing blocks of a T-token batch, as the library forms them: ranges
+    of at most 64 tokens; from 32 blocks on, their number rounded up to a
+    multiple of the 148 SMs."""
+    nb = -(-T // 64)
+    return -(-nb // 148) * 148 if nb >= 32 else nb
+
+
 def router_extra_launches(T, H, E, presplit=False):
     """Launches of the router logits beyond one: the weight split on the
     tensor-core path (none when the weights carry a prepared split), and
@@ -573,8 +581,8 @@ def run_route_gpu(args, rank, world, local_rank):
         kt.append(ev0.elapsed_time(ev1) / (reps * NB))
     kt = np.array(kt)
     # algorithmic bytes of the routing call (logits + bias read; idx,
-    # gates, counts and the per-64-token histogram rows written)
-    nblk = (T + 63) // 64
+    # gates, counts and the per-block histogram rows written)
+    nblk = route_blocks(T)
     route_bytes = T * E * 4 + E * 4 + T * K * 8 + E * 4 + 2 * nblk * E * 4
     perm_bytes = T * K * 4 + 2 * T * K * 4 + (E + 1) * 4 + 3 * nblk * E * 4
     pk, pk_src = peaks()

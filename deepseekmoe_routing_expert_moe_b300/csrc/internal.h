@@ -13,12 +13,25 @@
 
 namespace moe {
 
-// tokens per routing block: the per-block expert histogram and the stable
-// dispatch order are both computed over these token ranges
+// Routing blocks (the per-block expert histogram and the stable dispatch
+// order are both computed over them): consecutive token ranges of at most
+// 64 tokens, each with one row of per-expert counts.  From 32 blocks
+// on their number is rounded up to a multiple of the B300's 148 SMs, so
+// every SM routes the same number of tokens (the work per token is fixed;
+// 256 blocks of 64 tokens at T = 16384 left 108 SMs with two blocks and 40
+// with one).  Block b covers [route_block_start(b), route_block_start(b+1)).
 constexpr int kRouteTokensPerBlock = 64;
+constexpr int kRouteSmMultiple = 148;
 
 inline int route_blocks(int T) {
-  return (T + kRouteTokensPerBlock - 1) / kRouteTokensPerBlock;
+  const int nb = (T + kRouteTokensPerBlock - 1) / kRouteTokensPerBlock;
+  return nb >= 32 ? (nb + kRouteSmMultiple - 1) / kRouteSmMultiple *
+                        kRouteSmMultiple
+                  : nb;
+}
+
+__host__ __device__ inline int route_block_start(int b, int T, int nb) {
+  return static_cast<int>(static_cast<long long>(b) * T / nb);
 }
 
 struct DevStatus;

@@ -1236,7 +1236,11 @@ moe_status_t moe_forward(const moe_dims_t* d, const moe_weights_t* w,
 // ---------------------------------------------------------------------------
 namespace {
 
-constexpr size_t kRouteScratchInts = 262144;  // 1 MiB of int32
+// The documented limit is ceil(T/64) * E <= 262144; the routing blocks of
+// a batch are that count rounded up to a multiple of 148 (at most 147 more
+// rows of up to 1024 experts), which the array covers.
+constexpr size_t kRouteLimitInts = 262144;
+constexpr size_t kRouteScratchInts = kRouteLimitInts + 147 * 1024;
 static __device__ __align__(256) int32_t g_route_scratch[kRouteScratchInts];
 
 // The address is cached per CUDA context, keyed by the context's unique id
@@ -1324,8 +1328,12 @@ extern "C" moe_status_t moe_route_static_scratch(
   MOE_ALIGN(topk_idx);
   MOE_ALIGN(topk_gate);
   MOE_ALIGN(counts);
-  // the histogram needs one row of E counts per 64-token block
-  if ((size_t)moe::route_blocks(d->T) * (size_t)d->E > kRouteScratchInts)
+  // the histogram needs one row of E counts per routing block
+  const size_t blocks64 =
+      ((size_t)d->T + moe::kRouteTokensPerBlock - 1) /
+      moe::kRouteTokensPerBlock;
+  if (blocks64 * (size_t)d->E > kRouteLimitInts ||
+      (size_t)moe::route_blocks(d->T) * (size_t)d->E > kRouteScratchInts)
     return MOE_ERR_WORKSPACE;
   cudaStream_t s = cs(stream);
   if (d->T == 0)

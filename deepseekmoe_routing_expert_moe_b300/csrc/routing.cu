@@ -285,10 +285,12 @@ __global__ void __launch_bounds__(WARPS * 32)
 #pragma unroll
   for (int j = 0; j < EPL; ++j) b[j] = active ? bias[lane * EPL + j] : 0.f;
 
-  const int tok0 = blockIdx.x * kRouteTokensPerBlock;
+  // this block's tokens (the grid has route_blocks(T) blocks)
+  const int tok0 = route_block_start(blockIdx.x, T, gridDim.x);
+  const int tok1 = route_block_start(blockIdx.x + 1, T, gridDim.x);
   for (int tt = warp; tt < kRouteTokensPerBlock; tt += WARPS) {
     const int t = tok0 + tt;
-    if (t >= T) break;
+    if (t >= tok1) break;
     float s[EPL], u[EPL];
     if (active) {
       load_row<EPL>(logits + (size_t)t * E + lane * EPL, s);
@@ -855,8 +857,8 @@ __global__ void __launch_bounds__(256)
   __shared__ int cnt[1024];
   for (int i = threadIdx.x; i < E; i += blockDim.x) cnt[i] = 0;
   __syncthreads();
-  const int t0 = blockIdx.x * kRouteTokensPerBlock;
-  const int t1 = min(T, t0 + kRouteTokensPerBlock);
+  const int t0 = route_block_start(blockIdx.x, T, gridDim.x);
+  const int t1 = route_block_start(blockIdx.x + 1, T, gridDim.x);
   for (int p = t0 * K + threadIdx.x; p < t1 * K; p += blockDim.x) {
     const int e = topk_idx[p];
     if (e >= 0 && e < E)
@@ -963,8 +965,9 @@ __global__ void __launch_bounds__(1024)
 }
 
 // ===================================================================
-// Stable dispatch order.  Block = kRouteTokensPerBlock tokens, one warp per
-// 32-token chunk, lane = token.  Every block first derives the expert
+// Stable dispatch order.  Block = one routing block (at most
+// kRouteTokensPerBlock tokens), one warp per 32-token chunk, lane = token.
+// Every block first derives the expert
 // offsets (exclusive scan of counts over experts); the block's base row
 // for expert e is offsets[e] + block_prefix[blk][e].  mask[w][e] has bit l
 // set when lane l's token chose e; a token's rank among the block's tokens
@@ -1033,8 +1036,9 @@ __global__ void __launch_bounds__(kDestWarps * 32)
   __syncthreads();
   if (blockIdx.x == 0 && offsets != nullptr)
     for (int e = tid; e <= E; e += blockDim.x) offsets[e] = offs[e];
-  const int t = blockIdx.x * kRouteTokensPerBlock + warp * 32 + lane;
-  const bool valid = t < T;
+  const int t = route_block_start(blockIdx.x, T, gridDim.x) + warp * 32 +
+                lane;
+  const bool valid = t < route_block_start(blockIdx.x + 1, T, gridDim.x);
   if (valid)
     for (int k = 0; k < K; ++k) {
       const int e = topk_idx[(size_t)t * K + k];

@@ -186,7 +186,7 @@ moe_status_t moe_route(const moe_dims_t* d, const float* logits,
  * scratch, or a loop that must not call cudaMalloc after start-up because
  * it synchronises the device.  (The pages have no counterpart: this is an
  * interface variant, not part of the method.)  Results are identical to
- * moe_route's.  Its scratch is one static device array of 1 MiB (262144
+ * moe_route's.  Its scratch is one static device array of 1.6 MiB (412672
  * int32) that every GPU loading this library holds until the process
  * exits; it allocates nothing and calls no allocating routine.
  *   Limit: ceil(T/64) * E <= 262144 (T <= 65536 at E = 256), else
