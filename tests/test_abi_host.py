@@ -42,7 +42,20 @@ def test_library_exports_every_declared_symbol(L):
 
 
 def test_abi_version_and_status_strings(L):
-    assert ops.moe_abi_version() == 4
+    with open(os.path.join(ROOT, "include", "moe.h")) as f:
+        want = int(re.search(r"#define MOE_ABI_VERSION (\d+)", f.read())[1])
+    assert want == 4 and ops.moe_abi_version() == want
+
+
+def test_build_entry_point_checks_the_built_library(L):
+    """__graft_entry__.build() compiles and verifies the library's
+    interface version against the header (run here without a GPU)."""
+    import importlib.util
+    spec = importlib.util.spec_from_file_location(
+        "graft_entry", os.path.join(ROOT, "__graft_entry__.py"))
+    g = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(g)
+    g.build()
     for code, name in ops.STATUS.items():
         assert ops.moe_status_string(code) == name
 
