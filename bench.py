@@ -1094,6 +1094,21 @@ def run_backward_gpu(args, rank, world, local_rank):
                       "logits read once, dlogits written once)")
     roof["algorithmic_bytes"] = int(alg)
     roof["peak_source"] = f"{pk_src} (MEASURED_PEAKS.json)"
+    clocks = clk.summary()
+    # end to end: each step uploads its logits, top-K ids, gate gradients
+    # and sequence counts from pinned memory and reads dlogits back (the
+    # copies of neighbouring steps overlap the compute)
+    host_in = [[zs[i].cpu().pin_memory(), idxs[i].cpu().pin_memory(),
+                dgate.cpu().pin_memory(), cnts[i].cpu().pin_memory()]
+               for i in range(NB)]
+    e2e_steps = min(args.steps, 64)
+    e2e_ms = e2e_loop_multi(
+        lambda ins, outs: ops.moe_route_balance_backward(
+            d, ins[0], ins[1], ins[2], S, 1e-4, ins[3], outs[0], ws,
+            dloss=dloss),
+        host_in, [((T, E), torch.float32)], e2e_steps, stream)
+    assert ops.moe_get_device_error(ws) == 0
+    h2d = sum(t.numel() * t.element_size() for t in host_in[0])
     return {
         "metric": "tokens/s through the routing backward (gates + "
                   "sequence-wise balance loss to the router logits) at the "
@@ -1109,8 +1124,11 @@ def run_backward_gpu(args, rank, world, local_rank):
                    "T": T, "E": E, "topk": K, "seq_len": S,
                    "l2": "8 rotating logits batches, 134 MB > L2"},
         "roofline": roof,
+        "e2e": {"value": round(T * e2e_steps / (e2e_ms / 1e3), 1),
+                "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": T * E * 4},
         "gpu_launches": args.steps,
-        "clocks": clk.summary(),
+        "clocks": clocks,
         "impl": "b300",
     }
 
@@ -1362,6 +1380,69 @@ def run_expert_backward_reference(args):
     }
 
 
+def run_route_reference(args):
+    """Oracle arm of route_v3: per step the first 2048 tokens of a V3
+    logits batch through the oracle's routing (sigmoid, bias, group-limited
+    top-8, gates), dispatch order and bias step -- the GPU arm's three
+    calls on a bounded sample."""
+    from deepseekmoe_routing_expert_moe_b300 import inputs
+    from oracle import moe_oracle as O
+    cfg = inputs.CONFIGS["route_v3"]
+    n = 2048
+    z = inputs.random_logits(cfg, T=n)
+    bias = inputs.bias(cfg)
+
+    def one():
+        r = O.route(z, bias, cfg.n_group, cfg.topk_group, cfg.topk)
+        O.permutation(r["idx"], cfg.E)
+        O.bias_update(O.expert_counts(r["idx"], cfg.E), bias, n, cfg.topk,
+                      cfg.gamma)
+
+    for _ in range(args.warmup):
+        one()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        one()
+    tot = time.perf_counter() - t0
+    v = n * args.steps / tot
+    sample = (f"the first {n} tokens of a logits batch per step through the "
+              "numpy oracle (routing, dispatch order, bias step)")
+    return {
+        "metric": "tokens/s routed (routing + dispatch order + bias step) "
+                  "at the V3 shape; oracle on the host cores",
+        "value": round(v, 1), "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(tot / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic, seeded",
+        "config": {"workload": f"route_v3: routing-only, {n} of the "
+                               f"{cfg.T} tokens per step, E={cfg.E}, "
+                               f"top-{cfg.topk}"},
+        "impl": "reference",
+        "cpu_baseline": {"value": round(v, 1), "unit": "tokens/s",
+                         "cores": blas_threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(v, 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def cpu_baseline_from_reference(args):
+    """The cpu_baseline object of a GPU line whose runner times no oracle
+    itself: the workload's oracle arm (its bounded sample, the oracle as it
+    stands) for a few steps (about 10-30 s of host time)."""
+    import copy
+    a = copy.copy(args)
+    a.impl = "reference"
+    # ~10 s of routing samples; an FP8 layer token takes ~10-20 s alone
+    a.steps = {"route_v3": 400, "route_backward_v3": 100}.get(args.workload, 1)
+    a.warmup = 1 if a.steps > 1 else 0
+    r = run_reference(a)
+    cb = dict(r["cpu_baseline"])
+    cb["sample"] = f"{cb['sample']}; {a.steps} steps"
+    return cb
+
+
 def run_backward_reference(args):
     """Oracle arm of route_backward_v3: one 4096-token sequence of V3
     logits per step through the oracle's gate and balance-loss gradients."""
@@ -1449,6 +1530,8 @@ def run_reference(args):
         return run_decode_fp8_reference(args)
     if args.workload == "route_backward_v3":
         return run_backward_reference(args)
+    if args.workload == "route_v3":
+        return run_route_reference(args)
     if args.workload in ("expert_backward_v3", "expert_backward_v3_e16"):
         return run_expert_backward_reference(args)
     cfg = inputs.CONFIGS[args.workload]
@@ -1522,6 +1605,9 @@ def main():
         res = run_expert_backward_gpu(args, rank, world, local_rank)
     else:
         res = run_gpu(args, rank, world, local_rank)
+    if (rank == 0 and world == 1 and not args.no_cpu_baseline and
+            "cpu_baseline" not in res):
+        res["cpu_baseline"] = cpu_baseline_from_reference(args)
     if rank == 0:
         print(json.dumps(res), flush=True)
     if world > 1:
