@@ -30,8 +30,8 @@
 //   bwd_finalize_kernel  dx_t and dgate[t, k]
 //
 // The GEMMs are persistent tcgen05 kernels like the forward ones: one CTA
-// per SM, a TMA producer per operand, one MMA-issuing thread, four epilogue
-// warps, fp32 accumulators in tensor memory.  The dgrad GEMMs read the
+// per SM, a TMA producer per operand, one MMA-issuing thread, eight
+// epilogue warps, fp32 accumulators in tensor memory.  The dgrad GEMMs read the
 // weights transposed: their tiles are loaded as MN-major operands (64
 // features x 64 reduction rows per TMA box, 128-byte swizzle) and described
 // to the MMA as such, so no transposed copy of any weight is made.  The
@@ -56,7 +56,11 @@ constexpr int kPadRows = 16;  // routed segments are padded to this
 constexpr int NT = 192;       // largest token chunk (MMA N) of the dgrad GEMMs
 constexpr int WSTAGES = 4;    // weight ring depth
 constexpr int TSTAGES = 3;    // token ring depth
-constexpr int kEpiWarps = 4;
+// eight epilogue warps: two per tensor-memory lane quadrant, each taking
+// half of a unit's 16-column chunks (a unit wider than 128 tokens holds
+// both accumulator slots, so the MMAs of the next unit wait for its
+// epilogue: the shorter the epilogue, the less they wait)
+constexpr int kEpiWarps = 8;
 constexpr int kEpiWarp0 = 3;
 constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps);
 constexpr int SLOT = 256;
@@ -67,7 +71,7 @@ constexpr uint32_t TSTAGE_BYTES = NT * BK * 2;          // 24 KB
 constexpr uint32_t TMEM_COLS = 2 * SLOT;
 constexpr size_t kSmemLimit = 232448;
 constexpr uint64_t kDrainNs = 2000000000ull;
-constexpr int kEpiBar = 1;    // named barrier of the four epilogue warps
+constexpr int kEpiBar = 1;    // named barrier of the dgrad epilogue warps
 
 enum { kRecomp = 0, kDgradDown = 1, kDgradUp = 2 };
 enum {
@@ -449,7 +453,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* drain = tempty + 2;
   float* dg_s = reinterpret_cast<float*>(drain + 1);      // [4][NT]
   volatile uint32_t* misc =
-      reinterpret_cast<volatile uint32_t*>(dg_s + kEpiWarps * NT);
+      reinterpret_cast<volatile uint32_t*>(dg_s + 4 * NT);
   // misc[0] TMEM base, [1] abort, [2] bad offsets, [4 + (unit parity)]
   // the epilogue's go flags (two, so a flag is never rewritten while a
   // warp may still read it)
@@ -729,11 +733,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ------------------------------------------------------- epilogue
     // One thread takes each go / stop decision and the named barrier of
-    // the four epilogue warps shares it, so the warps never part ways at
+    // the eight epilogue warps shares it, so the warps never part ways at
     // a barrier.
     const int q = warp & 3;
+    const int hw = (warp - kEpiWarp0) >> 2;  // which half of the chunks
     const int r = q * 32 + lane;
-    const int et = threadIdx.x - 32 * kEpiWarp0;  // 0..127
+    const int et = threadIdx.x - 32 * kEpiWarp0;  // 0..255
     uint32_t tph = 0;
     int slot = 0;
     int it = 0;
@@ -758,13 +763,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           wide ? tmem_base + lane_off + s1_ * SLOT : ta + SLOT / 2;
       const bool sh = (w.seg == 0);
       const int nfeat = sh ? p.n_s : p.n_r;
+      const int nch = (w.n + 15) / 16;
+      const int c_lo = hw ? (nch + 1) / 2 : 0;
+      const int c_hi = hw ? nch : (nch + 1) / 2;
       if (MODE == kRecomp) {
         const int fa = w.f * FB + r;
         const bool vf = fa < nfeat;
         float* po = sh ? p.p_s : p.p_r;
         float* qo = sh ? p.q_s : p.q_r;
         uint16_t* ho = sh ? p.hg_s : p.hg_r;
-        for (int c = 0; 16 * c < w.n; ++c) {
+        for (int c = c_lo; c < c_hi; ++c) {
           uint32_t a[16], b[16];
           tmem_ld16(ta + 16 * c, a);
           tmem_ld16(tb + 16 * c, b);
@@ -794,16 +802,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                        sh ? p.dp_s : p.dp_r, sh ? p.dq_s : p.dq_r,
                        sh ? nullptr : p.gp, w.row0, w.rows, nfeat, fa, fbb,
                        va, vb};
-        // the p, q and gate values of chunk c + 1 are loaded while chunk c
-        // is computed (two register sets, alternating)
-        float s0[5][16], s1[5][16];
-        dd_fetch(t, 0, s0);
-        for (int c = 0; 16 * c < w.n; c += 2) {
-          if (16 * (c + 1) < w.n) dd_fetch(t, c + 1, s1);
+        // each warp's chunks: p, q and the gates loaded, then the chunk
+        float s0[5][16];
+        for (int c = c_lo; c < c_hi; ++c) {
+          dd_fetch(t, c, s0);
           dd_chunk(t, c, ta, tb, s0, dg_s + q * NT, lane);
-          if (16 * (c + 1) >= w.n) break;
-          if (16 * (c + 2) < w.n) dd_fetch(t, c + 2, s0);
-          dd_chunk(t, c + 1, ta, tb, s1, dg_s + q * NT, lane);
         }
         tc_fence_before();
         mbar_arrive(smem_u32(&tempty[slot]));
@@ -821,7 +824,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int fbb = fa + BM;
         uint16_t* out = sh ? p.out_s : p.out_r;
         const int ld = nfeat;
-        for (int c = 0; 16 * c < w.n; ++c) {
+        for (int c = c_lo; c < c_hi; ++c) {
           uint32_t a[16], b[16];
           tmem_ld16(ta + 16 * c, a);
           tmem_ld16(tb + 16 * c, b);
@@ -858,7 +861,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 size_t dgrad_smem_bytes(int E) {
   return 1024 + WSTAGES * WSTAGE_BYTES + TSTAGES * TSTAGE_BYTES +
          (2 * WSTAGES + 2 * TSTAGES + 5) * sizeof(uint64_t) +
-         kEpiWarps * NT * sizeof(float) + 8 * sizeof(uint32_t) +
+         4 * NT * sizeof(float) + 8 * sizeof(uint32_t) +
          sizeof(int) * (3 * (E + 1) + 1);
 }
 
