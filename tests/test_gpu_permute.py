@@ -49,7 +49,9 @@ def _random_idx(T, E, K, rng, hot=None):
                      for _ in range(T)]).astype(np.int32)
 
 
-@pytest.mark.parametrize("T", [1, 31, 64, 65, 200, 4096])
+# 1984: 31 routing blocks of 64 tokens; 1985: 32 blocks, their number
+# rounded up to 148 (13-14 tokens each); 9473: 149 rounded up to 296
+@pytest.mark.parametrize("T", [1, 31, 64, 65, 200, 1984, 1985, 4096, 9473])
 def test_permute_v3_shape(T):
     cfg = inputs.CONFIGS["prefill_v3"]
     rng = np.random.default_rng(T)

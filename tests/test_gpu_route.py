@@ -31,7 +31,10 @@ def test_v3_routing_full_size_16384_tokens():
     assert np.all(r["kept"].sum(1) == 4)
 
 
-@pytest.mark.parametrize("T", [1, 2, 63, 64, 65, 1000, 4097])
+# 1984 / 1985 / 9473: either side of the rounding of the routing blocks'
+# number up to a multiple of 148 (31 blocks of 64; 148 of 13-14; 296 of 32)
+@pytest.mark.parametrize("T", [1, 2, 63, 64, 65, 1000, 1984, 1985, 4097,
+                               9473])
 def test_ragged_token_counts(T):
     cfg = inputs.CONFIGS["route_v3"]
     z = inputs.random_logits(cfg, T=T, step=T)
