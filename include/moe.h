@@ -58,7 +58,7 @@ extern "C" {
 typedef enum {
   MOE_OK = 0,
   MOE_ERR_INVALID_ARG = 1,   /* NULL pointer, negative or inconsistent dims */
-  MOE_ERR_UNSUPPORTED = 2,   /* valid dims this build has no kernel for     */
+  MOE_ERR_UNSUPPORTED = 2,   /* valid dims the library has no kernel for    */
   MOE_ERR_ALIGNMENT = 3,     /* a pointer is not 16-byte aligned            */
   MOE_ERR_WORKSPACE = 4,     /* workspace NULL or smaller than required     */
   MOE_ERR_CUDA = 5,          /* a CUDA runtime/driver call failed           */
