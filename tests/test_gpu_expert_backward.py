@@ -246,6 +246,17 @@ def test_backward_resident_and_streamed_segments_and_row_block_groups():
     _small_case(cfg, idx)
 
 
+def test_backward_1024_experts_mostly_empty():
+    """E = 1024 (the largest expert count): ~2 rows per chosen expert and
+    most experts without a token, so the weight-gradient GEMM's task table
+    has 3 x 1025 (matrix, segment) pairs and most of its tasks zero-fill a
+    whole group of row blocks."""
+    cfg = inputs.custom_config("bwd_e1k", 805, T=300, H=256, E=1024,
+                               n_group=8, topk_group=4, topk=8, I=128,
+                               I_shared=64, router_sigma=0.05)
+    _small_case(cfg)
+
+
 def test_backward_repeats_bit_exactly_on_one_workspace():
     """Calls on one workspace give the same results bit for bit: the
     weight-gradient GEMM's task counter lives in the workspace and every
