@@ -106,6 +106,31 @@ def test_layer_ragged_small_batches(T):
     rms_tolerance_check(g["out"], ref["out"], rows=ok)
 
 
+@pytest.mark.parametrize("T", [600, 8192])
+def test_layer_1024_experts(T):
+    """E = 1024, the largest expert count: the grouped GEMMs' segment
+    tables at their largest; T = 600 (under 64 rows per expert: the up GEMM
+    gathers the routed rows from x) and T = 8192 (64 per expert: the
+    expert-sorted copy, many routing blocks)."""
+    cfg = inputs.custom_config("lay_e1k", 610, T=T, H=256, E=1024,
+                               n_group=8, topk_group=4, topk=8, I=128,
+                               I_shared=128, router_sigma=0.02)
+    w, W = host_weights(cfg)
+    g = forward_gpu(cfg, W, w["x"], w["bias"])
+    f = inputs.bf16_bits_to_f32
+    ref = O.layer_forward(f(w["x"]), w["w_router"], w["bias"], f(w["w1"]),
+                          f(w["w3"]), f(w["w2"]), f(w["ws1"]), f(w["ws3"]),
+                          f(w["ws2"]), n_group=cfg.n_group,
+                          topk_group=cfg.topk_group, topk=cfg.topk)
+    ok = margins_ok(ref["route"], cfg)
+    assert ok.sum() >= 0.8 * T
+    assert np.array_equal(by_expert(g["idx"][ok], g["gate"][ok])[0],
+                          by_expert(ref["route"]["idx"][ok],
+                                    ref["route"]["gate"][ok])[0])
+    assert np.array_equal(g["counts"], O.expert_counts(g["idx"], cfg.E))
+    rms_tolerance_check(g["out"], ref["out"], rows=ok)
+
+
 def test_v3_generator_bits_match_on_device(v3_weights):
     """The device-generated V3 weights are the host generator's bits (so the
     oracle can regenerate any expert on the host)."""
