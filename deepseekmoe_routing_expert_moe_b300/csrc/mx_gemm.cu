@@ -744,12 +744,17 @@ int mx_launch_shape(const MxParams& mp, cudaStream_t s) {
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
-// the pipeline shape for this launch's mean rows per routed expert
+// the pipeline shape for this launch's mean rows per routed expert; the
+// streaming shape's deeper rings do not fit beside the segment tables of
+// the largest expert counts (E = 1024), and the compute shape, correct at
+// any rows per expert, serves those
 template <int MODE>
 int mx_launch(const MxParams& mp, cudaStream_t s) {
   const long long mean_rows = mp.E > 0 ? (long long)mp.TK / mp.E : 0;
-  return mean_rows >= kMxComputeRows ? mx_launch_shape<MODE, MxCompute>(mp, s)
-                                     : mx_launch_shape<MODE, MxStream>(mp, s);
+  const bool stream = mean_rows < kMxComputeRows &&
+                      mx_smem_bytes<MxStream>(mp.E) <= XSMEM_LIMIT;
+  return stream ? mx_launch_shape<MODE, MxStream>(mp, s)
+                : mx_launch_shape<MODE, MxCompute>(mp, s);
 }
 
 // token-operand maps of one [rows, k] E4M3 tensor, boxes of 16..128 rows
@@ -764,8 +769,8 @@ bool mx_token_maps(CUtensorMap (&m)[XTOK_BOXES], const void* base,
 
 int mx_ffn_supported(int H, int I, int I_shared, int E) {
   if (H % 128 || I % 128 || I_shared % 128) return 0;
-  return mx_smem_bytes<MxStream>(E) <= XSMEM_LIMIT &&
-         mx_smem_bytes<MxCompute>(E) <= XSMEM_LIMIT;
+  // the compute shape is the fallback of every launch (mx_launch)
+  return mx_smem_bytes<MxCompute>(E) <= XSMEM_LIMIT;
 }
 
 int launch_expert_ffn_mx(const FfnMxArgs& a, cudaStream_t s) {

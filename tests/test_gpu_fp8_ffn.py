@@ -133,6 +133,7 @@ def test_empty_single_row_and_ragged_chunks():
     (32, 4, 3, 384, 128, 77),      # 32 experts, shared I != routed I
     (16, 4, 1, 128, 256, 33),      # top-1, one feature block per expert
     (64, 8, 6, 256, 384, 250),
+    (1024, 8, 8, 128, 128, 600),   # the largest expert count
 ])
 def test_expert_and_width_shapes(E, G, K, I, Is, T):
     cfg = inputs.custom_config("fp8s", 980 + E + K, T=T, H=384, E=E,

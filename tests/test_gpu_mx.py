@@ -238,6 +238,7 @@ def test_compute_shape_wide_chunks():
                                      # holds one 128-row tile only
     (16, 4, 1, 128, 256, 33, 640),   # top-1, one feature block per expert
     (64, 8, 6, 256, 384, 250, 256),
+    (1024, 8, 8, 128, 128, 600, 256),  # the largest expert count
 ])
 def test_expert_and_width_shapes(E, G, K, I, Is, T, H):
     cfg = inputs.custom_config("mxs", 994 + E + K, T=T, H=H, E=E,
