@@ -246,6 +246,16 @@ def test_backward_resident_and_streamed_segments_and_row_block_groups():
     _small_case(cfg, idx)
 
 
+def test_backward_largest_hidden_size():
+    """H = 16384 (the backward's limit): the token gather and the finalize
+    at their widest rows, dW1 / dW3 with 64 256-column blocks, dW2 with 128
+    row blocks (groups of 16)."""
+    cfg = inputs.custom_config("bwd_h16k", 806, T=40, H=16384, E=8,
+                               n_group=4, topk_group=2, topk=2, I=128,
+                               I_shared=64, router_sigma=0.01)
+    _small_case(cfg)
+
+
 def test_backward_1024_experts_mostly_empty():
     """E = 1024 (the largest expert count): ~2 rows per chosen expert and
     most experts without a token, so the weight-gradient GEMM's task table

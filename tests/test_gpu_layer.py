@@ -106,6 +106,42 @@ def test_layer_ragged_small_batches(T):
     rms_tolerance_check(g["out"], ref["out"], rows=ok)
 
 
+def test_layer_largest_hidden_size():
+    """H = 16384, the largest hidden size: 256 reduction blocks in the
+    router and up GEMMs, 2048 16-byte vectors per gathered row (the row
+    copy's limit) and 64 256-column blocks in the down GEMM.
+
+    Bound, per element: the layer bar (2e-2 x RMS) plus the bf16 rounding
+    of the output itself (at most 2^-8 |out|).  The bar is a maximum over
+    the compared elements; here they are 655k, against ~29k on the sampled
+    V3 tokens, so the output's tails reach |out| ~ 8, where half a bf16
+    step alone is 2^-6 (the oracle's output rounded to bf16 is 0.0156 off
+    at worst, half the bar)."""
+    cfg = inputs.custom_config("lay_h16k", 611, T=40, H=16384, E=16,
+                               n_group=4, topk_group=2, topk=4, I=128,
+                               I_shared=128, router_sigma=0.01)
+    w, W = host_weights(cfg)
+    g = forward_gpu(cfg, W, w["x"], w["bias"])
+    f = inputs.bf16_bits_to_f32
+    ref = O.layer_forward(f(w["x"]), w["w_router"], w["bias"], f(w["w1"]),
+                          f(w["w3"]), f(w["w2"]), f(w["ws1"]), f(w["ws3"]),
+                          f(w["ws2"]), n_group=cfg.n_group,
+                          topk_group=cfg.topk_group, topk=cfg.topk)
+    ok = margins_ok(ref["route"], cfg)
+    assert ok.sum() >= 0.75 * cfg.T
+    assert np.array_equal(by_expert(g["idx"][ok], g["gate"][ok])[0],
+                          by_expert(ref["route"]["idx"][ok],
+                                    ref["route"]["gate"][ok])[0])
+    gout = np.asarray(g["out"], np.float64)[ok]
+    fout = np.asarray(ref["out"], np.float64)[ok]
+    rms = np.sqrt(np.mean(fout * fout))
+    bound = 2e-2 * rms + 2.0 ** -8 * np.abs(fout)
+    err = np.abs(gout - fout)
+    assert np.all(err <= bound), float((err / bound).max())
+    # not vacuous: the worst element uses a visible part of its bound
+    assert float((err / bound).max()) > 0.1
+
+
 @pytest.mark.parametrize("T", [600, 8192])
 def test_layer_1024_experts(T):
     """E = 1024, the largest expert count: the grouped GEMMs' segment
