@@ -142,6 +142,28 @@ def test_layer_largest_hidden_size():
     assert float((err / bound).max()) > 0.1
 
 
+def test_layer_top16():
+    """top-K above 8: the combine's general per-slot loop (the K <= 8 form
+    keeps the slots in registers) and 16 gates per token."""
+    cfg = inputs.custom_config("lay_k16", 612, T=200, H=256, E=64,
+                               n_group=8, topk_group=4, topk=16, I=128,
+                               I_shared=128, router_sigma=0.02)
+    w, W = host_weights(cfg)
+    g = forward_gpu(cfg, W, w["x"], w["bias"])
+    f = inputs.bf16_bits_to_f32
+    ref = O.layer_forward(f(w["x"]), w["w_router"], w["bias"], f(w["w1"]),
+                          f(w["w3"]), f(w["w2"]), f(w["ws1"]), f(w["ws3"]),
+                          f(w["ws2"]), n_group=cfg.n_group,
+                          topk_group=cfg.topk_group, topk=cfg.topk)
+    ok = margins_ok(ref["route"], cfg)
+    assert ok.sum() >= 0.75 * cfg.T
+    gi, gg = by_expert(g["idx"][ok], g["gate"][ok])
+    ri, rg = by_expert(ref["route"]["idx"][ok], ref["route"]["gate"][ok])
+    assert np.array_equal(gi, ri)
+    np.testing.assert_allclose(gg, rg, rtol=1e-5)
+    rms_tolerance_check(g["out"], ref["out"], rows=ok)
+
+
 @pytest.mark.parametrize("T", [600, 8192])
 def test_layer_1024_experts(T):
     """E = 1024, the largest expert count: the grouped GEMMs' segment
