@@ -87,6 +87,25 @@ def test_router_extra_launches(T, extra):
     assert (ws > split_parts + 4096) == (extra == 2)
 
 
+@pytest.mark.parametrize("T", [1, 64, 1984, 1985, 4096, 9473, 16384])
+def test_route_blocks_match_the_library(T):
+    """bench.py counts the routing histogram rows in the routing call's
+    algorithmic bytes: its block count must be the library's, whose routing
+    workspace holds two [blocks, E] int32 tables (histogram, prefixes)."""
+    from deepseekmoe_routing_expert_moe_b300 import ops
+    E = 256
+
+    def ws(t):
+        return ops.workspace_bytes(ops.dims(t, 7168, E, 8, 4, 8, 2048, 2048,
+                                            0.001), ops.MOE_WS_ROUTE)
+
+    def up(b):
+        return -(-b // 256) * 256
+    nb = bench.route_blocks(T)
+    assert ws(T) - ws(1) == 2 * (up(nb * E * 4) - up(1 * E * 4))
+    assert nb * 64 >= T and (nb < 32 or nb % 148 == 0)
+
+
 def test_gpu_index_for_smi(monkeypatch):
     monkeypatch.delenv("CUDA_VISIBLE_DEVICES", raising=False)
     assert bench.gpu_index_for_smi(3) == 3
