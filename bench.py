@@ -1133,6 +1133,185 @@ def run_backward_gpu(args, rank, world, local_rank):
     }
 
 
+EP_SOURCES = 8   # devices of the expert-parallel deployment
+
+
+def ep_counts(P, El, T, oracle=False):
+    """[P, El] rows each of P sources sends to the first device's El
+    experts: the per-expert counts of each source's top-8 routing of T
+    tokens of seeded logits -- moe_route on the GPU arm, the oracle's
+    routing on the oracle arm (routing is bit-exact, so both see the same
+    layout)."""
+    from deepseekmoe_routing_expert_moe_b300 import inputs
+    cfg = inputs.CONFIGS["route_v3"]
+    out = np.zeros((P, El), np.int32)
+    for s in range(P):
+        z = inputs.random_logits(cfg, T=T, step=100 + s)
+        if oracle:
+            from oracle import moe_oracle as O
+            r = O.route(z, inputs.bias(cfg), cfg.n_group, cfg.topk_group,
+                        cfg.topk)
+            out[s] = O.expert_counts(r["idx"], cfg.E)[:El]
+        else:
+            import torch
+            from deepseekmoe_routing_expert_moe_b300 import ops
+            d = ops.dims_of(cfg, T=T)
+            idx = torch.empty((T, cfg.topk), dtype=torch.int32, device="cuda")
+            gate = torch.empty((T, cfg.topk), dtype=torch.float32,
+                               device="cuda")
+            cnt = torch.empty(cfg.E, dtype=torch.int32, device="cuda")
+            ws = ops.workspace(d, ops.MOE_WS_ROUTE)
+            ops.moe_route(d, torch.from_numpy(z).cuda(),
+                          torch.from_numpy(inputs.bias(cfg)).cuda(), idx,
+                          gate, cnt, ws)
+            out[s] = cnt.cpu().numpy()[:El]
+    return out
+
+
+def run_ep_gpu(args, rank, world, local_rank):
+    """Expert parallelism's receive side at the V3 shape: one device of an
+    8-way deployment (32 local experts of 256) at T = 4096 tokens per
+    source.  Per step: moe_ep_plan on the [8, 32] counts the sources send,
+    moe_ep_permute_rows of the received bf16 rows into expert-major order
+    (the grouped GEMM's segments) and of the expert outputs back into
+    source-major order for the return trip.  One GPU: the exchange itself
+    is not part of the step; the received rows are resident (470 MB, larger
+    than L2)."""
+    import torch
+    from deepseekmoe_routing_expert_moe_b300 import inputs, ops
+    torch.cuda.set_device(local_rank)
+    cfg = inputs.CONFIGS["prefill_v3"]
+    T, E, H = cfg.T, cfg.E, cfg.H
+    P = EP_SOURCES
+    El = E // P
+    counts = ep_counts(P, El, T)
+    rows = int(counts.sum())
+    cnt_d = torch.from_numpy(counts).cuda()
+    g = torch.Generator(device="cuda").manual_seed(17 + rank)
+    xr = (torch.randn((rows, H), device="cuda", generator=g)
+          .to(torch.bfloat16).view(torch.int16))
+    perm = torch.empty(rows, dtype=torch.int32, device="cuda")
+    off = torch.empty(El + 1, dtype=torch.int32, device="cuda")
+    xe = torch.empty_like(xr)
+    yb = torch.empty_like(xr)
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step(src, dst):
+        ops.moe_ep_plan(cnt_d, rows, perm, off, ws=ws)
+        ops.moe_ep_permute_rows(src, perm, xe, inverse=False, ws=ws)
+        ops.moe_ep_permute_rows(xe, perm, dst, inverse=True, ws=ws)
+
+    for _ in range(args.warmup):
+        step(xr, yb)
+    torch.cuda.synchronize()
+    assert ops.moe_get_device_error(ws) == 0
+    assert torch.equal(yb, xr)      # the return trip restores the order
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(gpu_index_for_smi(local_rank)) as clk:
+        torch.cuda.synchronize()
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step(xr, yb)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    ms = ev0.elapsed_time(ev1)
+    clocks = clk.summary()
+    row_b = H * 2
+    alg = (P * El * 4 + rows * 4 + (El + 1) * 4 +      # the plan
+           2 * (2 * rows * row_b + rows * 4))           # two row moves
+    pk, pk_src = peaks()
+    hbm = float(pk["hbm_gbs"])
+    roof = {"bound": "hbm",
+            "achieved": round(alg * args.steps / (ms / 1e3) / 1e9, 1),
+            "peak": hbm, "unit": "GB/s"}
+    roof["frac"] = round(roof["achieved"] / hbm, 4)
+    roof["traffic"] = ncu_traffic("ep_step", args.workload)
+    roof["kernel"] = ("ep_rows_kernel (two row moves) + ep_plan_kernel; "
+                      "the moves read and write every received row once")
+    roof["algorithmic_bytes"] = int(alg)
+    roof["peak_source"] = f"{pk_src} (MEASURED_PEAKS.json)"
+    # end to end: the received rows uploaded, the returned rows read back
+    host_in = [[xr.cpu().pin_memory()]]
+    e2e_steps = min(args.steps, 8)
+    e2e_ms = e2e_loop_multi(lambda ins, outs: step(ins[0], outs[0]),
+                            host_in, [((rows, H), torch.int16)], e2e_steps,
+                            stream)
+    assert ops.moe_get_device_error(ws) == 0
+    return {
+        "metric": "received rows/s through the expert-parallel receive "
+                  "side (plan, rows to expert order and back) at the V3 "
+                  "shape on 1 B300; % of HBM roofline",
+        "value": round(rows * args.steps / (ms / 1e3), 1),
+        "unit": "rows/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic, seeded (counts from routing 8 "
+                                 "sources' logits; rows ~N(0,1))",
+        "config": {"workload": f"ep_v3: one device of {P}-way expert "
+                               f"parallelism, {El} of {E} experts, "
+                               f"{rows} received rows of H={H}",
+                   "sources": P, "local_experts": El, "rows": rows, "H": H,
+                   "l2": "470 MB of received rows per move > L2"},
+        "roofline": roof,
+        "e2e": {"value": round(rows * e2e_steps / (e2e_ms / 1e3), 1),
+                "unit": "rows/s", "h2d_bytes_per_step": rows * row_b,
+                "d2h_bytes_per_step": rows * row_b},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clocks,
+        "impl": "b300",
+    }
+
+
+def run_ep_reference(args):
+    """Oracle arm of ep_v3: per step the oracle's map (ep_plan) and the two
+    row moves in numpy, on the same counts with rows cut to their first 1024
+    of 7168 columns (a bounded sample of the bytes)."""
+    from deepseekmoe_routing_expert_moe_b300 import inputs
+    from oracle import moe_oracle as O
+    cfg = inputs.CONFIGS["prefill_v3"]
+    P = EP_SOURCES
+    El = cfg.E // P
+    counts = ep_counts(P, El, cfg.T, oracle=True)
+    rows = int(counts.sum())
+    x = np.random.default_rng(17).standard_normal((rows, 1024)).astype(
+        np.float32).view(np.int32).astype(np.int16)
+
+    def one():
+        perm, _ = O.ep_plan(counts)
+        xe = np.empty_like(x)
+        xe[perm] = x
+        return xe[perm]
+
+    for _ in range(args.warmup):
+        one()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        one()
+    tot = time.perf_counter() - t0
+    v = rows * args.steps / tot
+    sample = (f"all {rows} received rows per step, cut to 1024 of 7168 "
+              "columns, through the oracle's map and numpy row moves")
+    return {
+        "metric": "received rows/s through the expert-parallel receive side "
+                  "at the V3 shape; oracle on the host cores",
+        "value": round(v, 1), "unit": "rows/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(tot / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "int16 rows", "data": "synthetic, seeded",
+        "config": {"workload": f"ep_v3: {P} sources, {El} local experts, "
+                               f"{rows} rows (1024 columns)"},
+        "impl": "reference",
+        "cpu_baseline": {"value": round(v, 1), "unit": "rows/s",
+                         "cores": blas_threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(v, 1), "unit": "rows/s",
+                "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
 def run_expert_backward_gpu(args, rank, world, local_rank):
     """The experts' backward at the V3 prefill size (T = 4096, 256 experts of
     7168 x 2048 + shared, top-8): per step one moe_expert_backward call --
@@ -1435,7 +1614,8 @@ def cpu_baseline_from_reference(args):
     a = copy.copy(args)
     a.impl = "reference"
     # ~10 s of routing samples; an FP8 layer token takes ~10-20 s alone
-    a.steps = {"route_v3": 400, "route_backward_v3": 100}.get(args.workload, 1)
+    a.steps = {"route_v3": 400, "route_backward_v3": 100,
+               "ep_v3": 200}.get(args.workload, 1)
     a.warmup = 1 if a.steps > 1 else 0
     r = run_reference(a)
     cb = dict(r["cpu_baseline"])
@@ -1532,6 +1712,8 @@ def run_reference(args):
         return run_backward_reference(args)
     if args.workload == "route_v3":
         return run_route_reference(args)
+    if args.workload == "ep_v3":
+        return run_ep_reference(args)
     if args.workload in ("expert_backward_v3", "expert_backward_v3_e16"):
         return run_expert_backward_reference(args)
     cfg = inputs.CONFIGS[args.workload]
@@ -1570,7 +1752,7 @@ def main():
                     choices=("prefill_v3", "decode_v3", "skewed_v3",
                              "route_v3", "prefill_v3_e32", "balance_v3",
                              *FP8_WORKLOADS,
-                             "route_backward_v3",
+                             "route_backward_v3", "ep_v3",
                              "expert_backward_v3", "expert_backward_v3_e16"))
     ap.add_argument("--cpu-sample-tokens", type=int, default=4)
     ap.add_argument("--ref-tokens", type=int, default=1)
@@ -1601,6 +1783,8 @@ def main():
         res = run_fp8_gpu(args, rank, world, local_rank)
     elif args.workload == "route_backward_v3":
         res = run_backward_gpu(args, rank, world, local_rank)
+    elif args.workload == "ep_v3":
+        res = run_ep_gpu(args, rank, world, local_rank)
     elif args.workload in ("expert_backward_v3", "expert_backward_v3_e16"):
         res = run_expert_backward_gpu(args, rank, world, local_rank)
     else:

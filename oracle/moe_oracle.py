@@ -29,7 +29,8 @@ What it computes, and where the pages say so (page titles as cited):
   groups with power-of-two scales (the microscaling form the page points
   to for Blackwell's tensor cores).
 * same page §5.1: redundant copies of high-load experts from the load
-  statistics.
+  statistics; §1.3 / §5.1 expert parallelism: the receive side's regrouping
+  of rows from source order into expert order.
 
 The page's formulas were lost in extraction; each step below restates the
 prose.  Readings where the pages are silent (tie-breaks, the "at the mean"
@@ -47,8 +48,8 @@ Parity status: every function here is pinned by a ``-m "not gpu"`` test
 finite differences, and textbook reductions) -- see tests/test_oracle_pins.py,
 test_oracle_margin_pins.py, test_oracle_balance_pins.py,
 test_oracle_fp8_pins.py, test_oracle_mx_pins.py,
-test_oracle_backward_pins.py, test_oracle_expert_backward_pins.py and
-test_planner.py.
+test_oracle_backward_pins.py, test_oracle_expert_backward_pins.py,
+test_oracle_ep_pins.py and test_planner.py.
 """
 from __future__ import annotations
 
@@ -538,6 +539,36 @@ def quantize_128x128_pow2(w: np.ndarray):
     e = group_exponent_pow2(np.abs(b).max(axis=(1, 3)))
     q = _codes_pow2(b, e[:, None, :, None])
     return q.reshape(R, C), ue8m0_decode(ue8m0_encode(e))
+
+
+# --------------------------------------------------------------------------
+# Expert parallelism's receive side ("02 · DeepSeek-V3" §1.3, node-limited
+# routing over experts partitioned across devices; §5.1, the EP deployment):
+# the rows a device receives arrive source by source, each source's rows
+# sorted by expert ("source-major"); the grouped GEMM wants each local
+# expert's rows together, sources in order ("expert-major").
+# --------------------------------------------------------------------------
+def ep_plan(recv_counts: np.ndarray):
+    """recv_counts [P, El]: rows source s sends for local expert l.
+    Source-major row order: (s, l, j) sorted by s, then l, then j;
+    expert-major: by l, then s, then j.  Returns (perm [rows], offsets
+    [El + 1]): perm[i] = expert-major position of source-major row i;
+    offsets[l] = first expert-major row of local expert l."""
+    rc = np.asarray(recv_counts, np.int64)
+    P, El = rc.shape
+    rows = int(rc.sum())
+    # first row of block (s, l) in each order: counts before it, row-major
+    # (source-major) resp. column-major (expert-major)
+    src_first = (np.cumsum(rc.ravel()) - rc.ravel()).reshape(P, El)
+    exp_first = (np.cumsum(rc.T.ravel()) - rc.T.ravel()).reshape(El, P).T
+    perm = np.empty(rows, np.int64)
+    for s in range(P):
+        for l in range(El):
+            n = int(rc[s, l])
+            a = int(src_first[s, l])
+            perm[a:a + n] = exp_first[s, l] + np.arange(n)
+    offsets = np.append(exp_first[0, :], rows)
+    return perm, offsets
 
 
 # --------------------------------------------------------------------------

@@ -274,6 +274,10 @@ def test_regroup_matches_numpy_and_inverts(P, El, H):
     assert ops.moe_get_device_error(ws) == 0
     want, want_off = _np_regroup(counts, rows)
     assert np.array_equal(host(off), want_off)
+    # the map itself, index for index, against the oracle's
+    operm, ooff = O.ep_plan(counts)
+    assert np.array_equal(host(perm), operm)
+    assert np.array_equal(host(off), ooff)
     assert np.array_equal(host(xr), want)
     assert np.array_equal(host(back), rows)
 
