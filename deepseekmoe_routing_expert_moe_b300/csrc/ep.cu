@@ -22,35 +22,63 @@ namespace moe {
 namespace {
 
 constexpr int kPlanThreads = 256;
-constexpr int kPlanRowsPerBlock = 4096;
+constexpr int kPlanRowsPerBlock = 1024;
 
 // counts [n_src][n_local]: rows source s sends for local expert l.
 // perm[i] for source-major row i = expert-major row; block 0 also writes
 // offsets_local [n_local + 1] (expert-major segment starts).
+// Exclusive prefix sums of v(0), ..., v(n - 1) into out[0..n) and the total
+// into out[n], by all kPlanThreads threads: each takes a contiguous chunk,
+// the chunk sums are scanned across the warps, then each chunk is written.
+template <class F>
+__device__ __forceinline__ void block_exclusive_scan(int n, F v, int* out,
+                                                     int* wsum) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int per = (n + kPlanThreads - 1) / kPlanThreads;
+  const int a = min(n, tid * per), b = min(n, a + per);
+  int loc = 0;
+  for (int i = a; i < b; ++i) loc += v(i);
+  int incl = loc;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += t;
+  }
+  if (lane == 31) wsum[warp] = incl;
+  __syncthreads();
+  int run = incl - loc, total = 0;
+  for (int w = 0; w < kPlanThreads / 32; ++w) {
+    run += w < warp ? wsum[w] : 0;
+    total += wsum[w];
+  }
+  for (int i = a; i < b; ++i) {
+    out[i] = run;
+    run += v(i);
+  }
+  if (tid == 0) out[n] = total;
+  __syncthreads();  // wsum is reused by the next scan
+}
+
 __global__ void __launch_bounds__(kPlanThreads)
     ep_plan_kernel(const int32_t* __restrict__ counts, int n_src, int n_local,
                    long long rows, int32_t* __restrict__ perm,
                    int32_t* __restrict__ offsets_local, DevStatus* st) {
   extern __shared__ int sm[];
+  __shared__ int wsum[kPlanThreads / 32];
   const int n = n_src * n_local;
   int* src_off = sm;          // [n + 1] exclusive prefix, source-major
-  int* exp_off = sm + n + 1;  // [n] exclusive prefix, expert-major (l, s)
-  if (threadIdx.x == 0) {
-    int run = 0;
-    for (int i = 0; i < n; ++i) {
-      src_off[i] = run;
-      run += counts[i];
-    }
-    src_off[n] = run;
-    run = 0;
-    for (int l = 0; l < n_local; ++l)
-      for (int s = 0; s < n_src; ++s) {
-        exp_off[l * n_src + s] = run;
-        run += counts[s * n_local + l];
-      }
-    if (src_off[n] != rows) record_error(st, MOE_ERR_DEVICE_BOUNDS, 60);
-  }
-  __syncthreads();
+  int* exp_off = sm + n + 1;  // [n + 1] exclusive prefix, expert-major (l, s)
+  block_exclusive_scan(
+      n, [&](int i) { return __ldg(counts + i); }, src_off, wsum);
+  block_exclusive_scan(
+      n,
+      [&](int j) {
+        const int l = j / n_src, s = j - l * n_src;
+        return __ldg(counts + s * n_local + l);
+      },
+      exp_off, wsum);
+  if (threadIdx.x == 0 && blockIdx.x == 0 && src_off[n] != rows)
+    record_error(st, MOE_ERR_DEVICE_BOUNDS, 60);
   if (blockIdx.x == 0) {
     for (int l = threadIdx.x; l <= n_local; l += kPlanThreads)
       offsets_local[l] = l < n_local ? exp_off[l * n_src] : src_off[n];
@@ -110,7 +138,7 @@ cudaError_t launch_ep_plan(const int32_t* counts, int n_src, int n_local,
                            cudaStream_t s) {
   const long long nb =
       rows > 0 ? (rows + kPlanRowsPerBlock - 1) / kPlanRowsPerBlock : 1;
-  const size_t smem = sizeof(int) * (2 * n_src * n_local + 1);
+  const size_t smem = sizeof(int) * (2 * n_src * n_local + 2);
   ep_plan_kernel<<<(unsigned)nb, kPlanThreads, smem, s>>>(
       counts, n_src, n_local, rows, perm, offsets_local, st);
   return cudaGetLastError();
