@@ -87,7 +87,8 @@ def test_router_extra_launches(T, extra):
     assert (ws > split_parts + 4096) == (extra == 2)
 
 
-@pytest.mark.parametrize("T", [1, 64, 1984, 1985, 4096, 9473, 16384])
+@pytest.mark.parametrize("T", [1, 64, 128, 147, 148, 1984, 1985, 4096, 9473,
+                               16384])
 def test_route_blocks_match_the_library(T):
     """bench.py counts the routing histogram rows in the routing call's
     algorithmic bytes: its block count must be the library's, whose routing
